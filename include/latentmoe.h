@@ -1,0 +1,160 @@
+/*
+ * latentmoe.h - C ABI of the LatentMoE layer forward pass on one GB300 GPU (sm_103a).
+ *
+ * The layer (page "Lesson 6 - LatentMoE", kimi-k3-course.pages.dev, section
+ * "show me the actual equation", eq. 11 and eq. 13, quoting the K3 report section 2.3):
+ *
+ *   s    = Sigmoid(W_r x)                       router scores, one per routed expert
+ *   T_k  = argtopk(s + b)                       b steers selection only (eq. 13)
+ *   p_i  = s_i / sum_{r in T_k} s_r             weights over the selected set (eq. 13)
+ *   z    = W_down x                             d -> latent width l, before dispatch
+ *   u    = sum_{i in T_k} p_i E_i(z)            routed GLU experts in latent space (eq. 11)
+ *   y    = sum_{j<N_s} S_j(x) + W_up RMSNorm(u) shared full-width GLU experts + up-projection
+ *
+ * with E(v) = D( SiLU(G v) * (U v) ) for every expert, and
+ * RMSNorm(u) = u * g / sqrt(mean(u^2) + eps) (section "What extreme sparsity breaks":
+ * the norm sits between aggregation and W_up).
+ *
+ * Conventions for every entry point
+ *  - Matrices are row-major [out][in] (K contiguous).  All tensor pointers are DEVICE
+ *    pointers unless the name ends in _host; device pointers must be 16-byte aligned.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t passed as void*; NULL = legacy
+ *    default stream).  A handle must not be used from two streams at once and is not
+ *    thread-safe.
+ *  - The caller owns x, y, the weights and any routing buffers; the handle owns its
+ *    workspace (sized at create time for cfg.max_tokens) and a device status word.
+ *  - Every call returns an lmoe_status and never throws across the ABI.  Argument errors
+ *    are detected on the host before any launch and leave outputs untouched.  Errors a
+ *    kernel detects (a bounded wait that ran out, an out-of-range routing index) are sticky
+ *    in the device status word and are reported by latentmoe_status().
+ */
+#ifndef LATENTMOE_H
+#define LATENTMOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  LMOE_OK = 0,
+  LMOE_ERR_INVALID_ARG = 1,   /* bad pointer, size, alignment or config field           */
+  LMOE_ERR_UNSUPPORTED = 2,   /* valid but not implemented (shape/dtype combination)     */
+  LMOE_ERR_CUDA = 3,          /* a CUDA runtime/driver call failed                       */
+  LMOE_ERR_OOM = 4,           /* workspace allocation failed                             */
+  LMOE_ERR_TIMEOUT = 5,       /* a kernel's bounded wait ran out (device status word)    */
+  LMOE_ERR_DEVICE_CHECK = 6   /* a kernel rejected its input (e.g. routing index >= E)   */
+} lmoe_status;
+
+typedef enum {
+  LMOE_F32 = 0,               /* IEEE fp32                                               */
+  LMOE_BF16 = 1,              /* bfloat16                                                */
+  LMOE_MXFP4 = 2              /* OCP MXFP4: E2M1 pairs per byte (element 2i in the low    */
+                              /* nibble) + one E8M0 scale byte per 32 elements along K   */
+} lmoe_dtype;
+
+/* Routed experts are the identity map: forward() returns u = sum_i p_i z (width l) and
+ * stops there (no RMSNorm, W_up or shared experts).  Used by the routing/dispatch
+ * stress workload. */
+#define LMOE_FLAG_IDENTITY_EXPERTS 0x1u
+
+typedef struct {
+  int32_t d;             /* model width                                                 */
+  int32_t latent;        /* l, routed-expert width                                      */
+  int32_t hidden;        /* h, routed-expert GLU hidden width (ignored with identity)   */
+  int32_t num_experts;   /* E, 1..1024                                                  */
+  int32_t top_k;         /* k, 1..min(E, 32)                                            */
+  int32_t num_shared;    /* N_s >= 0                                                    */
+  int32_t shared_hidden; /* shared-expert GLU hidden width                              */
+  int32_t max_tokens;    /* largest T any call will pass (sizes the workspace)          */
+  int32_t act;           /* lmoe_dtype of x, y, W_down, W_up, shared experts: F32|BF16 */
+  int32_t router_w;      /* lmoe_dtype of W_r: F32|BF16                                 */
+  int32_t routed_w;      /* lmoe_dtype of routed experts: F32|BF16|MXFP4                */
+  float rms_eps;         /* RMSNorm epsilon                                             */
+  uint32_t flags;        /* LMOE_FLAG_*                                                 */
+} lmoe_config;
+
+/* Weight pointers (device, row-major [out][in]); types per lmoe_config. */
+typedef struct {
+  const void *w_router;                 /* W_r [E][d]                                   */
+  const float *router_bias;             /* b [E] fp32, or NULL (= 0); selection only    */
+  const void *w_down_proj;              /* W_down [l][d]                                */
+  const float *rms_gain;                /* g [l] fp32                                   */
+  const void *routed_gate_up;           /* [E][2h][l]: gate rows 0..h-1, up rows h..2h-1;
+                                           MXFP4: bytes [E][2h][l/2]                    */
+  const uint8_t *routed_gate_up_scale;  /* MXFP4 only: E8M0 [E][2h][l/32]               */
+  const void *routed_down;              /* [E][l][h]; MXFP4: bytes [E][l][h/2]          */
+  const uint8_t *routed_down_scale;     /* MXFP4 only: E8M0 [E][l][h/32]                */
+  const void *w_up_proj;                /* W_up [d][l]                                  */
+  const void *shared_gate_up;           /* [N_s][2h_s][d]: gate rows then up rows       */
+  const void *shared_down;              /* [N_s][d][h_s]                                */
+} lmoe_weights;
+
+typedef struct lmoe_handle lmoe_handle;
+
+/* Validate `cfg`, allocate the workspace for cfg->max_tokens tokens on the current
+ * device, and return a handle in *out.  Synchronous.  Errors: INVALID_ARG (bad field),
+ * UNSUPPORTED (e.g. widths that do not tile), OOM, CUDA. */
+lmoe_status latentmoe_create(const lmoe_config *cfg, lmoe_handle **out);
+
+/* Free the workspace and the handle.  Synchronises the device first.  NULL is a no-op. */
+lmoe_status latentmoe_destroy(lmoe_handle *h);
+
+/* Router and dispatch only (eq. 13 and the conversion of selections into expert batches).
+ *   x              [T][d] act dtype
+ *   topk_idx       [T][k] int32, out: selected experts in rank order (largest s+b first,
+ *                  equal keys -> lower expert index first)
+ *   topk_p         [T][k] fp32, out: p = s / sum of s over the selected set
+ *   expert_offsets [E+1] int32, out: exclusive prefix sum of per-expert row counts
+ *   tok_of_row     [T*k] int32, out: token of each row, rows ordered by (expert, token)
+ *   row_of         [T][k] int32, out: the row holding (token t, rank j)
+ * Any output pointer may be NULL (not written).  0 <= T <= max_tokens. */
+lmoe_status latentmoe_route(lmoe_handle *h, const void *x, int32_t T, const lmoe_weights *w,
+                            int32_t *topk_idx, float *topk_p, int32_t *expert_offsets,
+                            int32_t *tok_of_row, int32_t *row_of, void *stream);
+
+/* The whole layer: y [T][d] act dtype (with LMOE_FLAG_IDENTITY_EXPERTS: u [T][l]).
+ * 0 <= T <= max_tokens; T == 0 returns LMOE_OK without launching anything. */
+lmoe_status latentmoe_forward(lmoe_handle *h, const void *x, int32_t T, const lmoe_weights *w,
+                              void *y, void *stream);
+
+/* As latentmoe_forward, but with the routing supplied by the caller instead of the
+ * router: topk_idx [T][k] int32 (distinct experts per token, each in [0,E)) and topk_p
+ * [T][k] fp32.  An index outside [0,E) sets LMOE_ERR_DEVICE_CHECK in the status word and
+ * its row is skipped. */
+lmoe_status latentmoe_forward_routed(lmoe_handle *h, const void *x, int32_t T, const lmoe_weights *w,
+                                     const int32_t *topk_idx, const float *topk_p, void *y,
+                                     void *stream);
+
+/* End to end from HOST memory: copies x_host [T][d] to the device, runs the layer, and
+ * copies the result back to y_host ([T][d], or [T][l] with identity experts), all on
+ * `stream`; returns after the stream has finished.  Weights stay device pointers.
+ * Page-locked host buffers give full copy bandwidth. */
+lmoe_status latentmoe_forward_host(lmoe_handle *h, const void *x_host, int32_t T, const lmoe_weights *w,
+                                   void *y_host, void *stream);
+
+/* Synchronise `stream`, read and clear the device status word, and return the first
+ * sticky error (TIMEOUT before DEVICE_CHECK), or LMOE_OK. */
+lmoe_status latentmoe_status(lmoe_handle *h, void *stream);
+
+/* Number of kernels the last route/forward call enqueued. */
+int32_t latentmoe_last_launch_count(const lmoe_handle *h);
+
+/* Device workspace bytes held by the handle. */
+size_t latentmoe_workspace_bytes(const lmoe_handle *h);
+
+/* Test hook: bound every in-kernel wait of later calls to `timeout_ns` nanoseconds
+ * (default 4e9), and with inject != 0 make the next forward's first routed GEMM tile
+ * skip one pipeline-stage signal so that its consumer's bounded wait runs out and reports
+ * LMOE_ERR_TIMEOUT.  No fault, trap or hang results; other tiles complete normally. */
+lmoe_status latentmoe_set_wait_limit(lmoe_handle *h, uint64_t timeout_ns, int32_t inject);
+
+/* Static description of a status code. */
+const char *latentmoe_status_string(lmoe_status s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* LATENTMOE_H */

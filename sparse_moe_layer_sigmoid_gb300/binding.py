@@ -1,0 +1,187 @@
+"""ctypes binding of the C-ABI library (argument marshalling only; every step runs in the
+library's CUDA kernels).  torch supplies device memory and streams.
+
+Raises if the shared library is missing: there is no CPU fallback.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import re
+
+import torch
+
+from .configs import LayerConfig
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_lib", "liblatentmoe.so")
+HEADER = os.path.join(os.path.dirname(_PKG), "include", "latentmoe.h")
+
+LMOE_OK, LMOE_ERR_INVALID_ARG, LMOE_ERR_UNSUPPORTED, LMOE_ERR_CUDA, LMOE_ERR_OOM, LMOE_ERR_TIMEOUT, \
+    LMOE_ERR_DEVICE_CHECK = range(7)
+DTYPES = {"f32": 0, "bf16": 1, "mxfp4": 2}
+LMOE_FLAG_IDENTITY_EXPERTS = 0x1
+
+
+class LmoeConfig(C.Structure):
+    _fields_ = [("d", C.c_int32), ("latent", C.c_int32), ("hidden", C.c_int32), ("num_experts", C.c_int32),
+                ("top_k", C.c_int32), ("num_shared", C.c_int32), ("shared_hidden", C.c_int32),
+                ("max_tokens", C.c_int32), ("act", C.c_int32), ("router_w", C.c_int32), ("routed_w", C.c_int32),
+                ("rms_eps", C.c_float), ("flags", C.c_uint32)]
+
+
+class LmoeWeights(C.Structure):
+    _fields_ = [(n, C.c_void_p) for n in (
+        "w_router", "router_bias", "w_down_proj", "rms_gain", "routed_gate_up", "routed_gate_up_scale",
+        "routed_down", "routed_down_scale", "w_up_proj", "shared_gate_up", "shared_down")]
+
+
+class LatentMoEError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {_lib().latentmoe_status_string(status).decode()} (status {status})")
+
+
+_LIB = None
+
+
+def _lib():
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"CUDA library not built: {LIB_PATH} (run sparse_moe_layer_sigmoid_gb300.build)")
+        lib = C.CDLL(LIB_PATH)
+        vp, i32, st = C.c_void_p, C.c_int32, C.c_int
+        lib.latentmoe_create.argtypes = [C.POINTER(LmoeConfig), C.POINTER(vp)]
+        lib.latentmoe_destroy.argtypes = [vp]
+        lib.latentmoe_route.argtypes = [vp, vp, i32, C.POINTER(LmoeWeights), vp, vp, vp, vp, vp, vp]
+        lib.latentmoe_forward.argtypes = [vp, vp, i32, C.POINTER(LmoeWeights), vp, vp]
+        lib.latentmoe_forward_routed.argtypes = [vp, vp, i32, C.POINTER(LmoeWeights), vp, vp, vp, vp]
+        lib.latentmoe_forward_host.argtypes = [vp, vp, i32, C.POINTER(LmoeWeights), vp, vp]
+        lib.latentmoe_status.argtypes = [vp, vp]
+        lib.latentmoe_last_launch_count.argtypes = [vp]
+        lib.latentmoe_last_launch_count.restype = i32
+        lib.latentmoe_workspace_bytes.argtypes = [vp]
+        lib.latentmoe_workspace_bytes.restype = C.c_size_t
+        lib.latentmoe_set_wait_limit.argtypes = [vp, C.c_uint64, i32]
+        lib.latentmoe_status_string.argtypes = [st]
+        lib.latentmoe_status_string.restype = C.c_char_p
+        for name in ("latentmoe_create", "latentmoe_destroy", "latentmoe_route", "latentmoe_forward",
+                     "latentmoe_forward_routed", "latentmoe_forward_host", "latentmoe_status",
+                     "latentmoe_set_wait_limit"):
+            getattr(lib, name).restype = st
+        _LIB = lib
+    return _LIB
+
+
+def header_functions():
+    """Names of the functions declared in include/latentmoe.h."""
+    with open(HEADER) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(latentmoe_\w+)\s*\(", text)))
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def _check(status, what):
+    if status != LMOE_OK:
+        raise LatentMoEError(status, what)
+
+
+def make_config(cfg: LayerConfig, max_tokens: int | None = None) -> LmoeConfig:
+    return LmoeConfig(cfg.d, cfg.latent, cfg.hidden, cfg.experts, cfg.top_k, cfg.n_shared, cfg.shared_hidden,
+                      max_tokens or cfg.tokens, DTYPES[cfg.act], DTYPES[cfg.router_w], DTYPES[cfg.routed_w],
+                      cfg.rms_eps, LMOE_FLAG_IDENTITY_EXPERTS if cfg.identity_experts else 0)
+
+
+def make_weights(inp: dict) -> LmoeWeights:
+    return LmoeWeights(*[_ptr(inp.get(n)) for n, _ in LmoeWeights._fields_])
+
+
+class LatentMoE:
+    """One layer instance: a handle with a workspace sized for ``max_tokens`` tokens."""
+
+    def __init__(self, cfg: LayerConfig, max_tokens: int | None = None):
+        self.cfg = cfg
+        self.max_tokens = max_tokens or cfg.tokens
+        self._c = make_config(cfg, self.max_tokens)
+        h = C.c_void_p()
+        _check(_lib().latentmoe_create(C.byref(self._c), C.byref(h)), "latentmoe_create")
+        self._h = h
+
+    def close(self):
+        if getattr(self, "_h", None):
+            _lib().latentmoe_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    @property
+    def out_width(self):
+        return self.cfg.latent if self.cfg.identity_experts else self.cfg.d
+
+    def _out(self, x, y):
+        if y is None:
+            y = torch.empty((x.shape[0], self.out_width), dtype=x.dtype, device=x.device)
+        return y
+
+    def forward(self, x, weights: dict, y=None, stream=None):
+        y = self._out(x, y)
+        w = make_weights(weights)
+        _check(_lib().latentmoe_forward(self._h, _ptr(x), x.shape[0], C.byref(w), _ptr(y), _stream(stream)),
+               "latentmoe_forward")
+        return y
+
+    def forward_routed(self, x, weights: dict, topk_idx, topk_p, y=None, stream=None):
+        y = self._out(x, y)
+        w = make_weights(weights)
+        _check(_lib().latentmoe_forward_routed(self._h, _ptr(x), x.shape[0], C.byref(w), _ptr(topk_idx),
+                                               _ptr(topk_p), _ptr(y), _stream(stream)), "latentmoe_forward_routed")
+        return y
+
+    def forward_host(self, x_host, weights: dict, y_host=None, stream=None):
+        if y_host is None:
+            y_host = torch.empty((x_host.shape[0], self.out_width), dtype=x_host.dtype, pin_memory=True)
+        w = make_weights(weights)
+        _check(_lib().latentmoe_forward_host(self._h, _ptr(x_host), x_host.shape[0], C.byref(w), _ptr(y_host),
+                                             _stream(stream)), "latentmoe_forward_host")
+        return y_host
+
+    def route(self, x, weights: dict, stream=None):
+        T, k, E = x.shape[0], self.cfg.top_k, self.cfg.experts
+        dev = x.device
+        out = {"idx": torch.empty((T, k), dtype=torch.int32, device=dev),
+               "p": torch.empty((T, k), dtype=torch.float32, device=dev),
+               "offsets": torch.empty(E + 1, dtype=torch.int32, device=dev),
+               "tok_of_row": torch.empty(T * k, dtype=torch.int32, device=dev),
+               "row_of": torch.empty((T, k), dtype=torch.int32, device=dev)}
+        w = make_weights(weights)
+        _check(_lib().latentmoe_route(self._h, _ptr(x), T, C.byref(w), _ptr(out["idx"]), _ptr(out["p"]),
+                                      _ptr(out["offsets"]), _ptr(out["tok_of_row"]), _ptr(out["row_of"]),
+                                      _stream(stream)), "latentmoe_route")
+        return out
+
+    def status(self, stream=None) -> int:
+        return _lib().latentmoe_status(self._h, _stream(stream))
+
+    def last_launch_count(self) -> int:
+        return _lib().latentmoe_last_launch_count(self._h)
+
+    def workspace_bytes(self) -> int:
+        return _lib().latentmoe_workspace_bytes(self._h)
+
+    def set_wait_limit(self, timeout_ns: int, inject: bool = False):
+        _check(_lib().latentmoe_set_wait_limit(self._h, int(timeout_ns), 1 if inject else 0), "set_wait_limit")

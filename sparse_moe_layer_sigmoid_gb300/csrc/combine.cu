@@ -1,0 +1,138 @@
+// Deterministic combine + RMSNorm (page "Lesson 6 - LatentMoE", kimi-k3-course.pages.dev:
+// eq. 11 "u = sum over the selected experts of p_i E_i(W_down x)", and section "What extreme
+// sparsity breaks": RMSNorm between aggregation and W_up).
+//
+// One CTA per token.  The k expert rows of the token are summed in rank order j = 0..k-1 in
+// fp32 registers (the same order on every run), then sum(u^2) is reduced in a fixed tree and
+// n = u * g / sqrt(mean(u^2) + eps) is written.  HBM-bound: it reads k rows per token once.
+#include "common.cuh"
+#include "internal.h"
+
+namespace lmoe {
+namespace {
+
+constexpr int kThreads = 128;
+
+template <typename T>
+struct Vec {  // 16-byte vector of T
+  static constexpr int N = 16 / sizeof(T);
+};
+
+__device__ __forceinline__ void unpack(const uint4& v, float (&f)[8], __nv_bfloat16) {
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 t = __bfloat1622float2(h[i]);
+    f[2 * i] = t.x;
+    f[2 * i + 1] = t.y;
+  }
+}
+__device__ __forceinline__ void unpack(const uint4& v, float (&f)[8], float) {
+  f[0] = __uint_as_float(v.x);
+  f[1] = __uint_as_float(v.y);
+  f[2] = __uint_as_float(v.z);
+  f[3] = __uint_as_float(v.w);
+}
+__device__ __forceinline__ uint4 pack(const float (&f)[8], __nv_bfloat16) {
+  uint4 v;
+  v.x = pack_bf16x2(f[0], f[1]);
+  v.y = pack_bf16x2(f[2], f[3]);
+  v.z = pack_bf16x2(f[4], f[5]);
+  v.w = pack_bf16x2(f[6], f[7]);
+  return v;
+}
+__device__ __forceinline__ uint4 pack(const float (&f)[8], float) {
+  return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]), __float_as_uint(f[3]));
+}
+
+template <typename T, int VPT>
+__global__ void __launch_bounds__(kThreads) combine_kernel(const T* __restrict__ o, const int32_t* __restrict__ row_of,
+                                                           const float* __restrict__ p,
+                                                           const float* __restrict__ gain, float eps, int k,
+                                                           int width, T* __restrict__ out, int64_t ld_out) {
+  constexpr int EPV = Vec<T>::N;
+  const int t = blockIdx.x;
+  const int nvec = width / EPV;
+  float acc[VPT][8];
+#pragma unroll
+  for (int i = 0; i < VPT; ++i)
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[i][e] = 0.f;
+
+  for (int j = 0; j < k; ++j) {
+    const int r = row_of[(size_t)t * k + j];
+    if (r < 0) continue;
+    const float w = p ? p[(size_t)t * k + j] : 1.0f;
+    const uint4* src = reinterpret_cast<const uint4*>(o + (size_t)r * width);
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+      const int v = threadIdx.x + i * kThreads;
+      if (v < nvec) {
+        float f[8];
+        unpack(__ldg(src + v), f, T());
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) acc[i][e] = p ? fmaf(w, f[e], acc[i][e]) : acc[i][e] + f[e];
+      }
+    }
+  }
+
+  float scale = 1.0f;
+  if (gain) {
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < VPT; ++i)
+#pragma unroll
+      for (int e = 0; e < EPV; ++e) ss = fmaf(acc[i][e], acc[i][e], ss);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+    __shared__ float warp_ss[kThreads / 32];
+    if ((threadIdx.x & 31) == 0) warp_ss[threadIdx.x >> 5] = ss;
+    __syncthreads();
+    float tot = 0.f;
+#pragma unroll
+    for (int w = 0; w < kThreads / 32; ++w) tot += warp_ss[w];
+    scale = 1.0f / sqrtf(tot / (float)width + eps);
+  }
+
+  uint4* dst = reinterpret_cast<uint4*>(out + (size_t)t * ld_out);
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) {
+    const int v = threadIdx.x + i * kThreads;
+    if (v < nvec) {
+      float f[8];
+#pragma unroll
+      for (int e = 0; e < EPV; ++e) f[e] = gain ? acc[i][e] * __ldg(gain + v * EPV + e) * scale : acc[i][e];
+      dst[v] = pack(f, T());
+    }
+  }
+}
+
+template <typename T>
+cudaError_t launch_typed(const void* o, const int32_t* row_of, const float* p, const float* gain, float eps, int T_,
+                         int k, int width, void* out, int64_t ld_out, cudaStream_t s) {
+  const int nvec = width / Vec<T>::N;
+  const T* op = static_cast<const T*>(o);
+  T* dp = static_cast<T*>(out);
+  if (nvec <= kThreads)
+    combine_kernel<T, 1><<<T_, kThreads, 0, s>>>(op, row_of, p, gain, eps, k, width, dp, ld_out);
+  else if (nvec <= 2 * kThreads)
+    combine_kernel<T, 2><<<T_, kThreads, 0, s>>>(op, row_of, p, gain, eps, k, width, dp, ld_out);
+  else if (nvec <= 4 * kThreads)
+    combine_kernel<T, 4><<<T_, kThreads, 0, s>>>(op, row_of, p, gain, eps, k, width, dp, ld_out);
+  else if (nvec <= 8 * kThreads)
+    combine_kernel<T, 8><<<T_, kThreads, 0, s>>>(op, row_of, p, gain, eps, k, width, dp, ld_out);
+  else
+    return cudaErrorInvalidValue;
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const void* o, int dtype, const int32_t* row_of, const float* p, const float* gain,
+                           float eps, int T, int k, int width, void* out, int64_t ld_out, cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  if (dtype == kF32) return launch_typed<float>(o, row_of, p, gain, eps, T, k, width, out, ld_out, s);
+  return launch_typed<__nv_bfloat16>(o, row_of, p, gain, eps, T, k, width, out, ld_out, s);
+}
+
+}  // namespace lmoe

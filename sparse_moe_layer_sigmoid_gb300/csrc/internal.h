@@ -1,0 +1,84 @@
+// Host-side launchers shared between the translation units of the library.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace lmoe {
+
+// ---------------------------------------------------------------- routing (route.cu)
+// logits[T][E] = x[T][d] . W_r[E][d]^T in fp32 (CUDA cores, fixed K order per output).
+cudaError_t launch_router_logits(const void* x, int x_dtype, const void* w_router, int w_dtype, float* logits,
+                                 int T, int E, int d, cudaStream_t s);
+// s = sigmoid(logits), key = s + b, top-k by (key desc, index asc), p = s / sum(s over T_k).
+cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, int k, int32_t* idx, float* p,
+                        cudaStream_t s);
+// Deterministic expert batches: per-chunk counts, scan, stable (expert, token) rows, the
+// grouped-GEMM M-tile list, and per-row weights.  idx entries outside [0,E) are reported.
+struct DispatchBuffers {
+  int32_t* chunk_counts;  // [nchunks][E]
+  int32_t* chunk_base;    // [nchunks][E]
+  int32_t* offsets;       // [E+1]
+  int4* tiles;            // [max_tiles]: {expert, first m-tile of expert, m-tiles of expert, 0}
+  int32_t* num_tiles;     // [1]
+  int32_t* tok_of_row;    // [T*k]
+  int32_t* row_of;        // [T][k]
+  float* p_row;           // [T*k]
+};
+cudaError_t launch_dispatch(const int32_t* idx, const float* p, int T, int E, int k, const DispatchBuffers& b,
+                            uint32_t* status, int* launches, cudaStream_t s);
+// dst[row_of[t][j]] = src[t] for every (t, j): rows of `width` elements of `elem_bytes`.
+cudaError_t launch_scatter_rows(const void* src, void* dst, const int32_t* row_of, int T, int k, int width,
+                                int elem_bytes, cudaStream_t s);
+
+// ---------------------------------------------------------------- combine (combine.cu)
+// u_t = sum_j o[row_of[t][j]] (rank order, fp32) [times p[t][j] when p != nullptr];
+// with gain != nullptr writes n_t = u_t * g / sqrt(mean(u_t^2) + eps), else u_t.
+cudaError_t launch_combine(const void* o, int dtype, const int32_t* row_of, const float* p, const float* gain,
+                           float eps, int T, int k, int width, void* out, int64_t ld_out, cudaStream_t s);
+
+// ---------------------------------------------------------------- fp32 CUDA-core GEMM (simt.cu)
+struct SimtSegment {
+  const void* ptr;        // B segment: element (group g, row n, col c) at ptr + g*group_stride + n*ld + c
+  int64_t ld;
+  int64_t group_stride;
+  int k_len;              // K extent of this segment
+  int k_per_group;        // K columns per group inside the segment (segment spans k_len/k_per_group groups)
+};
+struct SimtGemm {
+  const void* A; int64_t lda; int a_dtype;
+  int b_dtype;
+  int nseg; SimtSegment seg[6];
+  int M, N, K;            // N = output columns
+  int glu_h;              // > 0: gate rows j, up rows j + glu_h of the group; out = SiLU(gate)*up
+  const int4* tiles; const int32_t* num_tiles; const int32_t* offsets; int max_tiles;  // grouped mode
+  void* C; int64_t ldc; int c_dtype;
+  const float* row_scale; // per output row multiplier (or nullptr)
+};
+cudaError_t launch_simt_gemm(const SimtGemm& g, cudaStream_t s);
+
+// ---------------------------------------------------------------- tcgen05 GEMM (gemm_tc.cu)
+enum TcEpilogue : int { kEpiF32 = 0, kEpiBF16 = 1, kEpiGluBF16 = 2, kEpiScaleBF16 = 3 };
+struct TcOperand {        // a bf16 tensor viewed as [depth][rows][cols], cols = K contiguous
+  const void* ptr;
+  int64_t cols, rows, depth;
+  int64_t row_stride;     // elements
+  int64_t depth_stride;   // elements
+};
+struct TcGemm {
+  int epi;
+  int M, N, K;            // N = output columns (GLU: hidden outputs); K multiple of 64
+  TcOperand A;            // [1][rows][K]
+  TcOperand B0, B1;       // B1.ptr == nullptr when K has a single segment
+  int k0_len;             // K columns served by B0 (multiple of 64)
+  int k0_per_group;       // B0 K columns per depth slice (K-concatenated groups), else k0_len
+  int glu_h;              // GLU: rows of B between gate and up; output column j -> (j / glu_h, j % glu_h)
+  const int4* tiles; const int32_t* num_tiles; const int32_t* offsets; int max_tiles;  // grouped mode
+  void* C; int64_t ldc;
+  const float* row_scale;
+};
+cudaError_t launch_tc_gemm(const TcGemm& g, uint32_t* status, uint64_t timeout_ns, int inject_fault, int num_sms,
+                           cudaStream_t s);
+
+}  // namespace lmoe

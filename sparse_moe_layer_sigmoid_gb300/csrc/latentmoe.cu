@@ -1,0 +1,471 @@
+// Host orchestrator and C-ABI entry points of the LatentMoE layer (declared in latentmoe.h).
+//
+// One forward pass enqueues, on the caller's stream and without any host synchronisation:
+//   router logits -> sigmoid/top-k/p -> dispatch (count, scan, scatter) -> W_down ->
+//   row scatter into expert-contiguous batches -> grouped gate/up GLU -> grouped down x p ->
+//   fixed-order combine + RMSNorm -> shared-expert gate/up GLU -> final GEMM
+//   y = [shared activations | RMSNorm(u)] . [shared down | W_up]^T
+// (page "Lesson 6 - LatentMoE", kimi-k3-course.pages.dev, eq. 11 and eq. 13).
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <new>
+
+#include "common.cuh"
+#include "internal.h"
+#include "latentmoe.h"
+
+using namespace lmoe;
+
+struct lmoe_handle {
+  lmoe_config cfg;
+  int device;
+  int num_sms;
+  uint8_t* ws;
+  size_t ws_bytes;
+  uint32_t* status;
+  float* logits;
+  int32_t* idx;
+  float* p;
+  DispatchBuffers db;
+  int max_tiles;
+  void* z;
+  void* z_perm;  // gathered expert-contiguous rows; reused for the routed down output
+  void* a;       // routed GLU activations [T*k][h]
+  void* act_cat; // [T][N_s*h_s + l]: shared GLU activations | RMSNorm(u)
+  void* x_stage; // forward_host staging
+  void* y_stage;
+  int last_launches;
+  uint64_t timeout_ns;
+  int inject;
+};
+
+namespace {
+
+constexpr uint64_t kDefaultTimeoutNs = 4000000000ull;
+
+size_t dtype_bytes(int dt) { return dt == kF32 ? 4 : 2; }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+lmoe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? LMOE_OK : LMOE_ERR_CUDA; }
+
+#define LMOE_TRY(expr)                          \
+  do {                                          \
+    cudaError_t e__ = (expr);                   \
+    if (e__ != cudaSuccess) return LMOE_ERR_CUDA; \
+  } while (0)
+
+lmoe_status validate_config(const lmoe_config& c) {
+  const bool identity = (c.flags & LMOE_FLAG_IDENTITY_EXPERTS) != 0;
+  if (c.d <= 0 || c.latent <= 0 || c.num_experts < 1 || c.num_experts > 1024) return LMOE_ERR_INVALID_ARG;
+  if (c.top_k < 1 || c.top_k > c.num_experts || c.top_k > 32) return LMOE_ERR_INVALID_ARG;
+  if (c.num_shared < 0 || c.max_tokens < 1) return LMOE_ERR_INVALID_ARG;
+  if (!identity && (c.hidden <= 0 || (c.num_shared > 0 && c.shared_hidden <= 0))) return LMOE_ERR_INVALID_ARG;
+  if ((int64_t)c.max_tokens * c.top_k >= (int64_t)1 << 31) return LMOE_ERR_INVALID_ARG;
+  if (c.act != LMOE_F32 && c.act != LMOE_BF16) return LMOE_ERR_INVALID_ARG;
+  if (c.router_w != LMOE_F32 && c.router_w != LMOE_BF16) return LMOE_ERR_INVALID_ARG;
+  if (c.routed_w != LMOE_F32 && c.routed_w != LMOE_BF16 && c.routed_w != LMOE_MXFP4) return LMOE_ERR_INVALID_ARG;
+  if (!(c.rms_eps >= 0.0f)) return LMOE_ERR_INVALID_ARG;
+  if (c.flags & ~LMOE_FLAG_IDENTITY_EXPERTS) return LMOE_ERR_INVALID_ARG;
+  // router GEMM and the CUDA-core path step K by 16; combine moves 16-byte vectors
+  if (c.d % 16 || c.latent % 16) return LMOE_ERR_UNSUPPORTED;
+  if (c.act == LMOE_F32) {
+    if (!identity && c.routed_w != LMOE_F32) return LMOE_ERR_UNSUPPORTED;
+    if (!identity && (c.hidden % 16 || (c.num_shared > 0 && c.shared_hidden % 16))) return LMOE_ERR_UNSUPPORTED;
+    if (c.latent > 4096) return LMOE_ERR_UNSUPPORTED;
+  } else {
+    // tensor-core tiles: K steps of 64, output tiles of 256 columns (128 for GLU halves)
+    if (c.d % 256 || c.latent % 256 || c.latent > 8192) return LMOE_ERR_UNSUPPORTED;
+    if (!identity) {
+      if (c.routed_w != LMOE_BF16) return LMOE_ERR_UNSUPPORTED;
+      if (c.hidden % 128) return LMOE_ERR_UNSUPPORTED;
+      if (c.num_shared > 0 && c.shared_hidden % 128) return LMOE_ERR_UNSUPPORTED;
+    }
+  }
+  return LMOE_OK;
+}
+
+// Carve the workspace.  With base == nullptr only computes the size.
+size_t layout(lmoe_handle* h, uint8_t* base) {
+  const lmoe_config& c = h->cfg;
+  const bool identity = (c.flags & LMOE_FLAG_IDENTITY_EXPERTS) != 0;
+  const size_t T = (size_t)c.max_tokens, E = (size_t)c.num_experts, k = (size_t)c.top_k;
+  const size_t rows = T * k;
+  const size_t nchunks = (T + kDispatchChunk - 1) / kDispatchChunk;
+  const size_t ab = dtype_bytes(c.act);
+  const size_t kcat = (size_t)c.num_shared * c.shared_hidden + c.latent;
+  size_t off = 0;
+  auto take = [&](size_t bytes) -> uint8_t* {
+    uint8_t* p = base ? base + off : nullptr;
+    off += round_up(bytes, 256);
+    return p;
+  };
+  h->max_tiles = (int)(rows / kTileM + E + 1);
+  h->status = reinterpret_cast<uint32_t*>(take(sizeof(uint32_t)));
+  h->logits = reinterpret_cast<float*>(take(T * E * 4));
+  h->idx = reinterpret_cast<int32_t*>(take(rows * 4));
+  h->p = reinterpret_cast<float*>(take(rows * 4));
+  h->db.chunk_counts = reinterpret_cast<int32_t*>(take(nchunks * E * 4));
+  h->db.chunk_base = reinterpret_cast<int32_t*>(take(nchunks * E * 4));
+  h->db.offsets = reinterpret_cast<int32_t*>(take((E + 1) * 4));
+  h->db.tiles = reinterpret_cast<int4*>(take((size_t)h->max_tiles * 16));
+  h->db.num_tiles = reinterpret_cast<int32_t*>(take(4));
+  h->db.tok_of_row = reinterpret_cast<int32_t*>(take(rows * 4));
+  h->db.row_of = reinterpret_cast<int32_t*>(take(rows * 4));
+  h->db.p_row = reinterpret_cast<float*>(take(rows * 4));
+  h->z = take(T * c.latent * ab);
+  h->z_perm = take(rows * c.latent * ab);
+  h->a = identity ? nullptr : take(rows * (size_t)c.hidden * ab);
+  h->act_cat = identity ? nullptr : take(T * kcat * ab);
+  h->x_stage = take(T * (size_t)c.d * ab);
+  h->y_stage = take(T * (size_t)(identity ? c.latent : c.d) * ab);
+  return off;
+}
+
+bool weights_ok(const lmoe_handle* h, const lmoe_weights* w, bool need_router) {
+  const lmoe_config& c = h->cfg;
+  const bool identity = (c.flags & LMOE_FLAG_IDENTITY_EXPERTS) != 0;
+  if (!w) return false;
+  if (need_router && (!w->w_router || !aligned16(w->w_router))) return false;
+  if (w->router_bias && !aligned16(w->router_bias)) return false;
+  if (!w->w_down_proj || !aligned16(w->w_down_proj)) return false;
+  if (identity) return true;
+  if (!w->rms_gain || !w->routed_gate_up || !w->routed_down || !w->w_up_proj) return false;
+  if (!aligned16(w->rms_gain) || !aligned16(w->routed_gate_up) || !aligned16(w->routed_down) ||
+      !aligned16(w->w_up_proj))
+    return false;
+  if (c.num_shared > 0) {
+    if (!w->shared_gate_up || !w->shared_down || !aligned16(w->shared_gate_up) || !aligned16(w->shared_down))
+      return false;
+  }
+  return true;
+}
+
+TcOperand op2d(const void* ptr, int64_t rows, int64_t cols) {
+  return TcOperand{ptr, cols, rows, 1, cols, rows * cols};
+}
+TcOperand op3d(const void* ptr, int64_t depth, int64_t rows, int64_t cols) {
+  return TcOperand{ptr, cols, rows, depth, cols, rows * cols};
+}
+
+// Routing into the handle's buffers: router + top-k unless the caller supplies idx/p.
+lmoe_status run_routing(lmoe_handle* h, const void* x, int T, const lmoe_weights* w, const int32_t* ext_idx,
+                        const float* ext_p, const int32_t** idx_out, const float** p_out, cudaStream_t s) {
+  const lmoe_config& c = h->cfg;
+  const int32_t* idx = ext_idx;
+  const float* p = ext_p;
+  if (!ext_idx) {
+    LMOE_TRY(launch_router_logits(x, c.act, w->w_router, c.router_w, h->logits, T, c.num_experts, c.d, s));
+    LMOE_TRY(launch_topk(h->logits, w->router_bias, T, c.num_experts, c.top_k, h->idx, h->p, s));
+    h->last_launches += 2;
+    idx = h->idx;
+    p = h->p;
+  }
+  LMOE_TRY(launch_dispatch(idx, p, T, c.num_experts, c.top_k, h->db, h->status, &h->last_launches, s));
+  *idx_out = idx;
+  *p_out = p;
+  return LMOE_OK;
+}
+
+lmoe_status run_forward(lmoe_handle* h, const void* x, int T, const lmoe_weights* w, const int32_t* ext_idx,
+                        const float* ext_p, void* y, cudaStream_t s) {
+  const lmoe_config& c = h->cfg;
+  const bool identity = (c.flags & LMOE_FLAG_IDENTITY_EXPERTS) != 0;
+  const bool tc = c.act == LMOE_BF16;
+  const int k = c.top_k, l = c.latent, d = c.d, hdim = c.hidden;
+  const int rows = T * k;
+  const int ns = c.num_shared, hs = c.shared_hidden;
+  const int kcat = ns * hs + l;
+  const size_t ab = dtype_bytes(c.act);
+  h->last_launches = 0;
+
+  const int32_t* idx;
+  const float* p;
+  lmoe_status st = run_routing(h, x, T, w, ext_idx, ext_p, &idx, &p, s);
+  if (st != LMOE_OK) return st;
+
+  // z = W_down x
+  if (tc) {
+    TcGemm g = {};
+    g.epi = kEpiBF16;
+    g.M = T; g.N = l; g.K = d;
+    g.A = op2d(x, T, d);
+    g.B0 = op2d(w->w_down_proj, l, d);
+    g.k0_len = d; g.k0_per_group = d;
+    g.C = h->z; g.ldc = l;
+    LMOE_TRY(launch_tc_gemm(g, h->status, h->timeout_ns, 0, h->num_sms, s));
+  } else {
+    SimtGemm g = {};
+    g.A = x; g.lda = d; g.a_dtype = c.act; g.b_dtype = c.act;
+    g.nseg = 1; g.seg[0] = SimtSegment{w->w_down_proj, d, 0, d, d};
+    g.M = T; g.N = l; g.K = d;
+    g.C = h->z; g.ldc = l; g.c_dtype = c.act;
+    LMOE_TRY(launch_simt_gemm(g, s));
+  }
+  // rows of z into expert-contiguous order
+  LMOE_TRY(launch_scatter_rows(h->z, h->z_perm, h->db.row_of, T, k, l, (int)ab, s));
+  h->last_launches += 2;
+
+  if (identity) {
+    LMOE_TRY(launch_combine(h->z_perm, c.act, h->db.row_of, p, nullptr, 0.f, T, k, l, y, l, s));
+    h->last_launches += 1;
+    return LMOE_OK;
+  }
+
+  void* o = h->z_perm;  // the down projection overwrites the gathered rows it no longer needs
+  uint8_t* n_out = static_cast<uint8_t*>(h->act_cat) + (size_t)ns * hs * ab;
+  if (tc) {
+    TcGemm g = {};
+    g.epi = kEpiGluBF16;
+    g.M = rows; g.N = hdim; g.K = l;
+    g.A = op2d(h->z_perm, rows, l);
+    g.B0 = op3d(w->routed_gate_up, c.num_experts, 2 * hdim, l);
+    g.k0_len = l; g.k0_per_group = l; g.glu_h = hdim;
+    g.tiles = h->db.tiles; g.num_tiles = h->db.num_tiles; g.offsets = h->db.offsets; g.max_tiles = h->max_tiles;
+    g.C = h->a; g.ldc = hdim;
+    LMOE_TRY(launch_tc_gemm(g, h->status, h->timeout_ns, h->inject, h->num_sms, s));
+    h->inject = 0;
+
+    TcGemm dn = {};
+    dn.epi = kEpiScaleBF16;
+    dn.M = rows; dn.N = l; dn.K = hdim;
+    dn.A = op2d(h->a, rows, hdim);
+    dn.B0 = op3d(w->routed_down, c.num_experts, l, hdim);
+    dn.k0_len = hdim; dn.k0_per_group = hdim;
+    dn.tiles = h->db.tiles; dn.num_tiles = h->db.num_tiles; dn.offsets = h->db.offsets; dn.max_tiles = h->max_tiles;
+    dn.C = o; dn.ldc = l; dn.row_scale = h->db.p_row;
+    LMOE_TRY(launch_tc_gemm(dn, h->status, h->timeout_ns, 0, h->num_sms, s));
+  } else {
+    SimtGemm g = {};
+    g.A = h->z_perm; g.lda = l; g.a_dtype = c.act; g.b_dtype = c.routed_w;
+    g.nseg = 1; g.seg[0] = SimtSegment{w->routed_gate_up, l, (int64_t)2 * hdim * l, l, l};
+    g.M = rows; g.N = hdim; g.K = l; g.glu_h = hdim;
+    g.tiles = h->db.tiles; g.num_tiles = h->db.num_tiles; g.offsets = h->db.offsets; g.max_tiles = h->max_tiles;
+    g.C = h->a; g.ldc = hdim; g.c_dtype = c.act;
+    LMOE_TRY(launch_simt_gemm(g, s));
+
+    SimtGemm dn = {};
+    dn.A = h->a; dn.lda = hdim; dn.a_dtype = c.act; dn.b_dtype = c.routed_w;
+    dn.nseg = 1; dn.seg[0] = SimtSegment{w->routed_down, hdim, (int64_t)l * hdim, hdim, hdim};
+    dn.M = rows; dn.N = l; dn.K = hdim;
+    dn.tiles = h->db.tiles; dn.num_tiles = h->db.num_tiles; dn.offsets = h->db.offsets; dn.max_tiles = h->max_tiles;
+    dn.C = o; dn.ldc = l; dn.c_dtype = c.act; dn.row_scale = h->db.p_row;
+    LMOE_TRY(launch_simt_gemm(dn, s));
+  }
+  // u = sum_j o_j (rank order), n = RMSNorm(u) into the tail columns of act_cat
+  LMOE_TRY(launch_combine(o, c.act, h->db.row_of, nullptr, w->rms_gain, c.rms_eps, T, k, l, n_out, kcat, s));
+  h->last_launches += 3;
+
+  if (tc) {
+    if (ns > 0) {
+      TcGemm g = {};
+      g.epi = kEpiGluBF16;
+      g.M = T; g.N = ns * hs; g.K = d;
+      g.A = op2d(x, T, d);
+      g.B0 = op3d(w->shared_gate_up, ns, 2 * hs, d);
+      g.k0_len = d; g.k0_per_group = d; g.glu_h = hs;
+      g.C = h->act_cat; g.ldc = kcat;
+      LMOE_TRY(launch_tc_gemm(g, h->status, h->timeout_ns, 0, h->num_sms, s));
+      h->last_launches += 1;
+    }
+    TcGemm f = {};
+    f.epi = kEpiBF16;
+    f.M = T; f.N = d; f.K = kcat;
+    f.A = op2d(h->act_cat, T, kcat);
+    if (ns > 0) {
+      f.B0 = op3d(w->shared_down, ns, d, hs);
+      f.k0_len = ns * hs; f.k0_per_group = hs;
+      f.B1 = op2d(w->w_up_proj, d, l);
+    } else {
+      f.B0 = op2d(w->w_up_proj, d, l);
+      f.k0_len = l; f.k0_per_group = l;
+    }
+    f.C = y; f.ldc = d;
+    LMOE_TRY(launch_tc_gemm(f, h->status, h->timeout_ns, 0, h->num_sms, s));
+    h->last_launches += 1;
+  } else {
+    if (ns > 0) {
+      SimtGemm g = {};
+      g.A = x; g.lda = d; g.a_dtype = c.act; g.b_dtype = c.act;
+      g.nseg = 1; g.seg[0] = SimtSegment{w->shared_gate_up, d, (int64_t)2 * hs * d, d, d};
+      g.M = T; g.N = ns * hs; g.K = d; g.glu_h = hs;
+      g.C = h->act_cat; g.ldc = kcat; g.c_dtype = c.act;
+      LMOE_TRY(launch_simt_gemm(g, s));
+      h->last_launches += 1;
+    }
+    SimtGemm f = {};
+    f.A = h->act_cat; f.lda = kcat; f.a_dtype = c.act; f.b_dtype = c.act;
+    f.nseg = 0;
+    if (ns > 0) f.seg[f.nseg++] = SimtSegment{w->shared_down, hs, (int64_t)d * hs, ns * hs, hs};
+    f.seg[f.nseg++] = SimtSegment{w->w_up_proj, l, 0, l, l};
+    f.M = T; f.N = d; f.K = kcat;
+    f.C = y; f.ldc = d; f.c_dtype = c.act;
+    LMOE_TRY(launch_simt_gemm(f, s));
+    h->last_launches += 1;
+  }
+  return LMOE_OK;
+}
+
+lmoe_status check_call(lmoe_handle* h, const void* x, int32_t T) {
+  if (!h) return LMOE_ERR_INVALID_ARG;
+  if (T < 0 || T > h->cfg.max_tokens) return LMOE_ERR_INVALID_ARG;
+  if (T > 0 && (!x || !aligned16(x))) return LMOE_ERR_INVALID_ARG;
+  if (cudaSetDevice(h->device) != cudaSuccess) return LMOE_ERR_CUDA;
+  return LMOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+lmoe_status latentmoe_create(const lmoe_config* cfg, lmoe_handle** out) {
+  if (!cfg || !out) return LMOE_ERR_INVALID_ARG;
+  *out = nullptr;
+  lmoe_status st = validate_config(*cfg);
+  if (st != LMOE_OK) return st;
+  lmoe_handle* h = new (std::nothrow) lmoe_handle();
+  if (!h) return LMOE_ERR_OOM;
+  h->cfg = *cfg;
+  h->timeout_ns = kDefaultTimeoutNs;
+  if (cudaGetDevice(&h->device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device) != cudaSuccess) {
+    delete h;
+    return LMOE_ERR_CUDA;
+  }
+  h->ws_bytes = layout(h, nullptr);
+  if (cudaMalloc(&h->ws, h->ws_bytes) != cudaSuccess) {
+    cudaGetLastError();
+    delete h;
+    return LMOE_ERR_OOM;
+  }
+  layout(h, h->ws);
+  if (cudaMemset(h->status, 0, sizeof(uint32_t)) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
+    cudaFree(h->ws);
+    delete h;
+    return LMOE_ERR_CUDA;
+  }
+  *out = h;
+  return LMOE_OK;
+}
+
+lmoe_status latentmoe_destroy(lmoe_handle* h) {
+  if (!h) return LMOE_OK;
+  cudaSetDevice(h->device);
+  cudaError_t e = cudaDeviceSynchronize();
+  cudaFree(h->ws);
+  delete h;
+  return cuda_status(e);
+}
+
+lmoe_status latentmoe_route(lmoe_handle* h, const void* x, int32_t T, const lmoe_weights* w, int32_t* topk_idx,
+                            float* topk_p, int32_t* expert_offsets, int32_t* tok_of_row, int32_t* row_of,
+                            void* stream) {
+  lmoe_status st = check_call(h, x, T);
+  if (st != LMOE_OK) return st;
+  if (!w || !w->w_router || !aligned16(w->w_router)) return LMOE_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const lmoe_config& c = h->cfg;
+  h->last_launches = 0;
+  const size_t rows = (size_t)T * c.top_k;
+  if (T > 0) {
+    const int32_t* idx;
+    const float* p;
+    st = run_routing(h, x, T, w, nullptr, nullptr, &idx, &p, s);
+    if (st != LMOE_OK) return st;
+  }
+  if (topk_idx && rows) LMOE_TRY(cudaMemcpyAsync(topk_idx, h->idx, rows * 4, cudaMemcpyDeviceToDevice, s));
+  if (topk_p && rows) LMOE_TRY(cudaMemcpyAsync(topk_p, h->p, rows * 4, cudaMemcpyDeviceToDevice, s));
+  if (expert_offsets) {
+    if (T > 0)
+      LMOE_TRY(cudaMemcpyAsync(expert_offsets, h->db.offsets, (c.num_experts + 1) * 4, cudaMemcpyDeviceToDevice, s));
+    else
+      LMOE_TRY(cudaMemsetAsync(expert_offsets, 0, (c.num_experts + 1) * 4, s));
+  }
+  if (tok_of_row && rows) LMOE_TRY(cudaMemcpyAsync(tok_of_row, h->db.tok_of_row, rows * 4, cudaMemcpyDeviceToDevice, s));
+  if (row_of && rows) LMOE_TRY(cudaMemcpyAsync(row_of, h->db.row_of, rows * 4, cudaMemcpyDeviceToDevice, s));
+  return LMOE_OK;
+}
+
+lmoe_status latentmoe_forward(lmoe_handle* h, const void* x, int32_t T, const lmoe_weights* w, void* y,
+                              void* stream) {
+  lmoe_status st = check_call(h, x, T);
+  if (st != LMOE_OK) return st;
+  if (!weights_ok(h, w, true) || (T > 0 && (!y || !aligned16(y)))) return LMOE_ERR_INVALID_ARG;
+  h->last_launches = 0;
+  if (T == 0) return LMOE_OK;
+  return run_forward(h, x, T, w, nullptr, nullptr, y, static_cast<cudaStream_t>(stream));
+}
+
+lmoe_status latentmoe_forward_routed(lmoe_handle* h, const void* x, int32_t T, const lmoe_weights* w,
+                                     const int32_t* topk_idx, const float* topk_p, void* y, void* stream) {
+  lmoe_status st = check_call(h, x, T);
+  if (st != LMOE_OK) return st;
+  if (!weights_ok(h, w, false) || (T > 0 && (!y || !aligned16(y) || !topk_idx || !topk_p)))
+    return LMOE_ERR_INVALID_ARG;
+  h->last_launches = 0;
+  if (T == 0) return LMOE_OK;
+  return run_forward(h, x, T, w, topk_idx, topk_p, y, static_cast<cudaStream_t>(stream));
+}
+
+lmoe_status latentmoe_forward_host(lmoe_handle* h, const void* x_host, int32_t T, const lmoe_weights* w,
+                                   void* y_host, void* stream) {
+  if (!h) return LMOE_ERR_INVALID_ARG;
+  if (T < 0 || T > h->cfg.max_tokens || (T > 0 && (!x_host || !y_host))) return LMOE_ERR_INVALID_ARG;
+  if (!weights_ok(h, w, true)) return LMOE_ERR_INVALID_ARG;
+  if (cudaSetDevice(h->device) != cudaSuccess) return LMOE_ERR_CUDA;
+  h->last_launches = 0;
+  if (T == 0) return LMOE_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const lmoe_config& c = h->cfg;
+  const size_t ab = dtype_bytes(c.act);
+  const bool identity = (c.flags & LMOE_FLAG_IDENTITY_EXPERTS) != 0;
+  const size_t in_bytes = (size_t)T * c.d * ab;
+  const size_t out_bytes = (size_t)T * (identity ? c.latent : c.d) * ab;
+  LMOE_TRY(cudaMemcpyAsync(h->x_stage, x_host, in_bytes, cudaMemcpyHostToDevice, s));
+  lmoe_status st = run_forward(h, h->x_stage, T, w, nullptr, nullptr, h->y_stage, s);
+  if (st != LMOE_OK) return st;
+  LMOE_TRY(cudaMemcpyAsync(y_host, h->y_stage, out_bytes, cudaMemcpyDeviceToHost, s));
+  LMOE_TRY(cudaStreamSynchronize(s));
+  return LMOE_OK;
+}
+
+lmoe_status latentmoe_status(lmoe_handle* h, void* stream) {
+  if (!h) return LMOE_ERR_INVALID_ARG;
+  if (cudaSetDevice(h->device) != cudaSuccess) return LMOE_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint32_t word = 0;
+  LMOE_TRY(cudaStreamSynchronize(s));
+  LMOE_TRY(cudaMemcpy(&word, h->status, sizeof(word), cudaMemcpyDeviceToHost));
+  LMOE_TRY(cudaMemset(h->status, 0, sizeof(word)));
+  if (word & kStatusTimeout) return LMOE_ERR_TIMEOUT;
+  if (word & kStatusDeviceCheck) return LMOE_ERR_DEVICE_CHECK;
+  return LMOE_OK;
+}
+
+int32_t latentmoe_last_launch_count(const lmoe_handle* h) { return h ? h->last_launches : 0; }
+
+size_t latentmoe_workspace_bytes(const lmoe_handle* h) { return h ? h->ws_bytes : 0; }
+
+lmoe_status latentmoe_set_wait_limit(lmoe_handle* h, uint64_t timeout_ns, int32_t inject) {
+  if (!h || timeout_ns == 0) return LMOE_ERR_INVALID_ARG;
+  h->timeout_ns = timeout_ns;
+  h->inject = inject ? 1 : 0;
+  return LMOE_OK;
+}
+
+const char* latentmoe_status_string(lmoe_status s) {
+  switch (s) {
+    case LMOE_OK: return "ok";
+    case LMOE_ERR_INVALID_ARG: return "invalid argument";
+    case LMOE_ERR_UNSUPPORTED: return "unsupported configuration";
+    case LMOE_ERR_CUDA: return "CUDA error";
+    case LMOE_ERR_OOM: return "out of device memory";
+    case LMOE_ERR_TIMEOUT: return "a kernel's bounded wait ran out";
+    case LMOE_ERR_DEVICE_CHECK: return "a kernel rejected its input";
+  }
+  return "unknown status";
+}
+
+}  // extern "C"

@@ -1,0 +1,189 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle on the same seeded inputs."""
+from dataclasses import replace
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from parity import (REL_FRO, assert_close, check_dispatch, compare_routing, device_inputs, oracle_for_rows,
+                    to_np)
+from sparse_moe_layer_sigmoid_gb300 import configs, inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def binding():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    import __graft_entry__
+    __graft_entry__.build()
+    from sparse_moe_layer_sigmoid_gb300 import binding as b
+    return b
+
+
+def _free():
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+
+
+# Reduced-width bf16 layers with K3's structure: several tiles in every GEMM dimension and
+# ragged per-expert row counts.
+SMALL_BF16 = replace(configs.K3W_E128_BF16_PREFILL, name="small_bf16", tokens=300, d=512, latent=256, hidden=256,
+                     experts=16, top_k=4, n_shared=2, shared_hidden=256, seed=21)
+SMALL_CASES = [
+    configs.TINY_F32,
+    SMALL_BF16,
+    replace(SMALL_BF16, name="small_bf16_noshared", n_shared=0, seed=22),
+    replace(SMALL_BF16, name="small_bf16_skew", bias="normal1.5", tokens=777, seed=23),
+    replace(SMALL_BF16, name="small_bf16_k1", top_k=1, tokens=129, seed=24),
+    replace(SMALL_BF16, name="small_bf16_wide", tokens=520, d=1024, latent=512, hidden=384, experts=40, top_k=6,
+            shared_hidden=384, seed=25),
+    replace(configs.ROUTING_DISPATCH_STRESS, name="small_identity", tokens=1000, d=512, latent=256, experts=64,
+            top_k=8, seed=26),
+    replace(configs.TINY_F32, name="tiny_f32_skew_ragged", tokens=301, bias="normal1.5", seed=27),
+]
+
+
+def _run_and_check(b, cfg, on_device=False, sample=None):
+    dev = torch.device("cuda")
+    inp = device_inputs(cfg, dev, on_device)
+    layer = b.LatentMoE(cfg)
+    x = inp["x"]
+    r = layer.route(x, inp)
+    y = layer.forward(x, inp)
+    assert layer.status() == 0
+    n_launch = layer.last_launch_count()
+    assert n_launch >= 7
+    T = cfg.tokens
+    rows = inputs.sample_tokens(T, sample or T, cfg.seed)
+    ref, host = oracle_for_rows(inp, cfg, rows)
+    idx_gpu = r["idx"].cpu().numpy()
+    p_gpu = r["p"].cpu().numpy()
+    mism, near = compare_routing(idx_gpu[rows], ref)
+    counts = check_dispatch(r, idx_gpu, cfg.experts)
+    ok = ~mism
+    assert np.allclose(p_gpu[rows][ok], ref["p"][ok], rtol=2e-6, atol=1e-7)
+    key = "u" if cfg.identity_experts else "y"
+    want = ref[key].copy()
+    if mism.any():  # near-tie tokens: compare against the oracle under the GPU's own choice
+        sub = rows[mism]
+        s_sel = np.take_along_axis(ref["s"][mism], idx_gpu[sub].astype(np.int64), axis=1)
+        ref2 = oracle.layer_forward(host, cfg, tokens=sub, routing=(idx_gpu[sub], s_sel / s_sel.sum(1, keepdims=True)))
+        want[mism] = ref2[key]
+    got = to_np(y)[rows]
+    rel, mx = assert_close(got, want, REL_FRO[cfg.routed_w if not cfg.identity_experts else cfg.act], cfg.name)
+    layer.close()
+    return {"rel": rel, "max": mx, "near_ties": near, "counts": counts, "y": y, "inp": inp}
+
+
+@pytest.mark.parametrize("cfg", SMALL_CASES, ids=lambda c: c.name)
+def test_small_layers_match_oracle(binding, cfg):
+    res = _run_and_check(binding, cfg)
+    print(f"{cfg.name}: rel_fro={res['rel']:.3e} max/rms={res['max']:.3e} near_ties={res['near_ties']}")
+
+
+def test_k3w_e128_bf16_prefill_sampled_rows(binding):
+    cfg = configs.K3W_E128_BF16_PREFILL
+    res = _run_and_check(binding, cfg, on_device=True, sample=256)
+    c = res["counts"]
+    print(f"{cfg.name}: rel_fro={res['rel']:.3e} max/rms={res['max']:.3e} near_ties={res['near_ties']} "
+          f"load max/mean={c.max() / c.mean():.2f}")
+    del res
+    _free()
+
+
+def test_routing_dispatch_stress_sampled_rows(binding):
+    cfg = configs.ROUTING_DISPATCH_STRESS
+    res = _run_and_check(binding, cfg, on_device=True, sample=256)
+    c = res["counts"]
+    print(f"{cfg.name}: rel_fro={res['rel']:.3e} near_ties={res['near_ties']} load max/mean={c.max() / c.mean():.2f}")
+    assert c.sum() == cfg.tokens * cfg.top_k
+    del res
+    _free()
+
+
+def test_token_permutation_is_bitwise_invariant(binding):
+    cfg = replace(SMALL_BF16, name="perm", tokens=333, seed=31)
+    dev = torch.device("cuda")
+    inp = device_inputs(cfg, dev, False)
+    layer = binding.LatentMoE(cfg)
+    y = layer.forward(inp["x"], inp).clone()
+    perm = torch.randperm(cfg.tokens, generator=torch.Generator().manual_seed(5)).to(dev)
+    y2 = layer.forward(inp["x"][perm].contiguous(), inp)
+    assert layer.status() == 0
+    assert torch.equal(y2, y[perm])
+    y3 = layer.forward(inp["x"], inp)
+    assert torch.equal(y3, y)  # run-to-run determinism
+    layer.close()
+
+
+def test_forward_host_matches_device_path(binding):
+    cfg = replace(SMALL_BF16, name="host", seed=32)
+    dev = torch.device("cuda")
+    inp = device_inputs(cfg, dev, False)
+    layer = binding.LatentMoE(cfg)
+    y = layer.forward(inp["x"], inp)
+    x_host = inp["x"].cpu().pin_memory()
+    y_host = layer.forward_host(x_host, inp)
+    assert torch.equal(y_host, y.cpu())
+    assert layer.status() == 0
+    layer.close()
+
+
+def test_edge_sizes_and_errors(binding):
+    cfg = replace(SMALL_BF16, name="edges", tokens=64, seed=33)
+    dev = torch.device("cuda")
+    inp = device_inputs(cfg, dev, False)
+    layer = binding.LatentMoE(cfg)
+    # T = 0: nothing launched, OK
+    y0 = layer.forward(inp["x"][:0], inp)
+    assert y0.shape == (0, cfg.d) and layer.last_launch_count() == 0
+    # T = 1 and a ragged T give the same rows as the full batch (rows are independent)
+    y_full = layer.forward(inp["x"], inp).clone()
+    y1 = layer.forward(inp["x"][:1].contiguous(), inp)
+    assert torch.equal(y1, y_full[:1])
+    y37 = layer.forward(inp["x"][:37].contiguous(), inp)
+    assert torch.equal(y37, y_full[:37])
+    # T above max_tokens is rejected on the host
+    big = torch.zeros((cfg.tokens + 1, cfg.d), dtype=inp["x"].dtype, device=dev)
+    with pytest.raises(binding.LatentMoEError) as ei:
+        layer.forward(big, inp)
+    assert ei.value.status == binding.LMOE_ERR_INVALID_ARG
+    # missing weight pointer is rejected
+    bad = dict(inp)
+    bad["w_down_proj"] = None
+    with pytest.raises(binding.LatentMoEError):
+        layer.forward(inp["x"], bad)
+    # caller-supplied routing with an out-of-range expert is flagged by the device check
+    idx = torch.zeros((cfg.tokens, cfg.top_k), dtype=torch.int32, device=dev)
+    idx[:] = torch.arange(cfg.top_k, dtype=torch.int32, device=dev)
+    idx[3, 1] = cfg.experts + 5
+    p = torch.full((cfg.tokens, cfg.top_k), 1.0 / cfg.top_k, device=dev)
+    layer.forward_routed(inp["x"], inp, idx, p)
+    assert layer.status() == binding.LMOE_ERR_DEVICE_CHECK
+    assert layer.status() == 0  # the status word is cleared once read
+    layer.close()
+    # unsupported / invalid configurations are refused at create
+    with pytest.raises(binding.LatentMoEError) as ei:
+        binding.LatentMoE(replace(SMALL_BF16, d=500))
+    assert ei.value.status == binding.LMOE_ERR_UNSUPPORTED
+    with pytest.raises(binding.LatentMoEError) as ei:
+        binding.LatentMoE(replace(SMALL_BF16, top_k=0))
+    assert ei.value.status == binding.LMOE_ERR_INVALID_ARG
+
+
+def test_forward_routed_with_oracle_routing(binding):
+    cfg = replace(SMALL_BF16, name="routed", seed=34)
+    dev = torch.device("cuda")
+    inp = device_inputs(cfg, dev, False)
+    host = inputs.host_inputs(inp)
+    ref = oracle.layer_forward(host, cfg)
+    layer = binding.LatentMoE(cfg)
+    idx = torch.from_numpy(ref["idx"].astype(np.int32)).to(dev)
+    p = torch.from_numpy(ref["p"].astype(np.float32)).to(dev)
+    y = layer.forward_routed(inp["x"], inp, idx, p)
+    assert layer.status() == 0
+    assert_close(to_np(y), ref["y"], REL_FRO["bf16"], "forward_routed")
+    layer.close()
