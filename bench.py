@@ -1,0 +1,350 @@
+#!/usr/bin/env python
+"""Benchmark of the LatentMoE layer forward pass: tokens/s per layer and roofline fraction.
+
+Default workload: the K3-width bf16 prefill layer (T=4096, d=7168, l=3584, h=3072, E=128,
+k=16, N_s=2), synthetic seeded inputs and random-init weights resident in HBM.  One step is
+one full forward pass (router, top-k, dispatch, W_down, experts, combine + RMSNorm, shared
+experts, W_up).  L2 is flushed (512 MiB write, untimed) before every timed step.
+
+  python bench.py [--gpus N --steps K --warmup W] [--impl ours|reference] [--workload NAME]
+
+Under torchrun each rank runs an independent replica on its own GPU (the layer's tokens
+are independent: no collective), timed between barriers; the slowest rank sets the time.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "LatentMoE layer tokens/s; % of HBM (decode) / tensor (prefill) roofline"
+UNIT = "tokens/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+# DRAM bytes per launch of the dominant kernel from one ncu capture, valid only while the kernel
+# source is unchanged (sha256 of the file it lives in).  Filled from the committed profile.
+TRAFFIC = {
+    "routed_gate_up_glu": {"bytes_per_launch": None, "src": "sparse_moe_layer_sigmoid_gb300/csrc/gemm_tc.cu",
+                           "sha256": None},
+}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def stage_work(cfg):
+    """Algorithmic work of each stage: ('tensor', FLOPs) or ('hbm', bytes)."""
+    T, d, l, h, E, k = cfg.tokens, cfg.d, cfg.latent, cfg.hidden, cfg.experts, cfg.top_k
+    ns, hs = cfg.n_shared, cfg.shared_hidden
+    ab = 4 if cfg.act == "f32" else 2
+    rows = T * k
+    w = {
+        "router_logits": ("alu", 2.0 * T * E * d),
+        "topk": ("hbm", 4.0 * T * E + 8.0 * rows),
+        "dispatch": ("hbm", 3 * 4.0 * rows),
+        "w_down": ("tensor", 2.0 * T * d * l),
+        "scatter_rows": ("hbm", float(ab) * (T * l + rows * l)),
+        "combine_rmsnorm": ("hbm", float(ab) * (rows * l + T * l)),
+    }
+    if not cfg.identity_experts:
+        w["routed_gate_up_glu"] = ("tensor", 2.0 * rows * l * 2 * h)
+        w["routed_down"] = ("tensor", 2.0 * rows * h * l)
+        w["shared_gate_up_glu"] = ("tensor", 2.0 * T * d * 2 * ns * hs)
+        w["final_gemm"] = ("tensor", 2.0 * T * (ns * hs + l) * d)
+    return w
+
+
+def file_sha(rel):
+    with open(os.path.join(ROOT, rel), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle sampling in the background during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", "-i", str(gpu_id), f"--query-gpu={self.FIELDS}",
+                                       "--format=csv,noheader,nounits", "-lms", "200"],
+                                      stdout=self.out, stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.p = None
+
+    def stop(self):
+        if self.p is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.p.terminate()
+        try:
+            self.p.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.p.kill()
+        self.out.flush()
+        self.out.seek(0)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.out.read().splitlines():
+            parts = [s.strip() for s in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        os.unlink(self.out.name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        under_load = [s for s in sm if s > 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(under_load), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def blas_threads():
+    """Threads numpy's BLAS runs with (read from the loaded OpenBLAS), else the CPU count."""
+    try:
+        with open("/proc/self/maps") as f:
+            libs = {ln.split()[-1] for ln in f if "openblas" in ln.lower() and ln.rstrip().endswith(".so")}
+        for path in libs:
+            lib = ctypes.CDLL(path)
+            for name in ("scipy_openblas_get_num_threads64_", "openblas_get_num_threads64_",
+                         "openblas_get_num_threads", "scipy_openblas_get_num_threads"):
+                fn = getattr(lib, name, None)
+                if fn is not None:
+                    return int(fn())
+    except OSError:
+        pass
+    return os.cpu_count()
+
+
+def oracle_sample(cfg, host, n_tokens, seed):
+    """Seconds the oracle takes on ``n_tokens`` seeded token rows of the workload (host cores).
+
+    ``host`` is the host copy of the inputs (made once, outside the timing)."""
+    import oracle
+    from sparse_moe_layer_sigmoid_gb300 import inputs
+
+    rows = inputs.sample_tokens(cfg.tokens, n_tokens, seed)
+    t0 = time.perf_counter()
+    oracle.layer_forward(host, cfg, tokens=rows)
+    return time.perf_counter() - t0
+
+
+def run_reference(args, cfg, rank, world):
+    """Reference arm: the fp64 oracle, timed as it stands on this machine's host cores."""
+    if rank != 0:
+        return
+    import torch
+
+    from sparse_moe_layer_sigmoid_gb300 import inputs
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    host = inputs.host_inputs(inputs.make_inputs(cfg, dev))
+    per_step = 1
+    times = []
+    for i in range(args.warmup + args.steps):
+        dt = oracle_sample(cfg, host, per_step, cfg.seed + 17 * i)
+        if i >= args.warmup:
+            times.append(dt)
+    ms = 1e3 * statistics.mean(times)
+    value = per_step / (ms / 1e3)
+    cores = blas_threads()
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(cfg, args),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": f"{per_step} seeded token row(s) of the workload per step"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(cfg, args):
+    return {"workload": cfg.name, "tokens": cfg.tokens, "d": cfg.d, "latent": cfg.latent, "hidden": cfg.hidden,
+            "experts": cfg.experts, "top_k": cfg.top_k, "n_shared": cfg.n_shared,
+            "shared_hidden": cfg.shared_hidden, "routed_w": cfg.routed_w, "seed": cfg.seed,
+            "global_batch": cfg.tokens * args.gpus, "parallelism": f"replicas x{args.gpus}",
+            "l2": "flushed before every timed step (512 MiB write, untimed)"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default="k3w_e128_bf16_prefill")
+    ap.add_argument("--cpu-sample", type=int, default=8, help="token rows for the oracle CPU baseline")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    import torch
+
+    from sparse_moe_layer_sigmoid_gb300 import configs
+
+    cfg = configs.CONFIGS[args.workload]
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    if args.impl == "reference":
+        run_reference(args, cfg, rank, world)
+        if dist:
+            dist.destroy_process_group()
+        return
+
+    import __graft_entry__
+    from sparse_moe_layer_sigmoid_gb300 import inputs
+    from sparse_moe_layer_sigmoid_gb300.binding import LatentMoE
+
+    if rank == 0:
+        __graft_entry__.build()
+    if dist:
+        dist.barrier()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    inp = inputs.make_inputs(cfg, dev)
+    layer = LatentMoE(cfg)
+    layer.enable_stage_timing()
+    x = inp["x"]
+    y = torch.empty((cfg.tokens, layer.out_width), dtype=x.dtype, device=dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        layer.forward(x, inp, y)
+    torch.cuda.synchronize()
+    st = layer.status()
+    if st != 0:
+        raise RuntimeError(f"layer reported status {st} during warm-up")
+
+    props = torch.cuda.get_device_properties(dev)
+    gpu_id = f"GPU-{props.uuid}" if getattr(props, "uuid", None) else local
+    clocks = ClockSampler(gpu_id) if rank == 0 else None
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    step_ms, stages, launches = [], {}, 0
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    for _ in range(args.steps):
+        flush.zero_()
+        ev0.record(stream)
+        layer.forward(x, inp, y)
+        ev1.record(stream)
+        launches += layer.last_launch_count()
+        ev1.synchronize()
+        step_ms.append(ev0.elapsed_time(ev1))
+        for k_, v in layer.stage_times_ms().items():
+            stages.setdefault(k_, []).append(v)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clk = clocks.stop() if clocks else None
+    ms = sum(step_ms) / len(step_ms)
+    if dist:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    if layer.status() != 0:
+        raise RuntimeError("layer reported an error status during the timed steps")
+
+    # end to end through the public host-memory entry point
+    x_host = x.cpu().pin_memory()
+    y_host = torch.empty((cfg.tokens, layer.out_width), dtype=x.dtype, pin_memory=True)
+    layer.enable_stage_timing()
+    for _ in range(2):
+        layer.forward_host(x_host, inp, y_host)
+    e2e_ms = []
+    for _ in range(args.steps):
+        flush.zero_()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        layer.forward_host(x_host, inp, y_host)
+        e2e_ms.append(1e3 * (time.perf_counter() - t0))
+    e2e = sum(e2e_ms) / len(e2e_ms)
+    if dist:
+        t = torch.tensor([e2e], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e = float(t.item())
+    elem = x.element_size()
+
+    peaks, src = load_peaks()
+    work = stage_work(cfg)
+    st_ms = {k_: sum(v) / len(v) for k_, v in stages.items()}
+    tensor_stages = {k_: st_ms[k_] for k_, (kind, _) in work.items() if kind == "tensor" and k_ in st_ms}
+    dom = max(tensor_stages, key=tensor_stages.get) if tensor_stages else max(st_ms, key=st_ms.get)
+    kind, amount = work[dom]
+    if kind == "tensor":
+        achieved = amount / (st_ms[dom] * 1e-3) / 1e12
+        peak = peaks["bf16_tflops"]
+        unit = "TFLOP/s"
+    else:
+        achieved = amount / (st_ms[dom] * 1e-3) / 1e9
+        peak = peaks["hbm_gbs"]
+        unit = "GB/s"
+    tr = TRAFFIC.get(dom)
+    traffic = None
+    if tr and tr["bytes_per_launch"] and tr["sha256"] == file_sha(tr["src"]):
+        traffic = tr["bytes_per_launch"]
+    total_flops = sum(a for kd, a in work.values() if kd in ("tensor", "alu"))
+
+    line = {"metric": METRIC, "value": world * cfg.tokens / (ms * 1e-3), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": cfg.act, "data": "synthetic",
+            "config": workload_config(cfg, args),
+            "roofline": {"bound": "tensor" if kind == "tensor" else "hbm", "kernel": dom, "achieved": achieved,
+                         "peak": peak, "unit": unit, "frac": achieved / peak, "traffic": traffic,
+                         "peak_source": f"{src} {'bf16_tflops (burst)' if kind == 'tensor' else 'hbm_gbs'}"},
+            "layer": {"flops": total_flops, "achieved_tflops": total_flops / (ms * 1e-3) / 1e12,
+                      "frac_of_bf16_peak": total_flops / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"],
+                      "stages_ms": st_ms},
+            "e2e": {"value": world * cfg.tokens / (e2e * 1e-3), "unit": UNIT,
+                    "h2d_bytes_per_step": cfg.tokens * cfg.d * elem,
+                    "d2h_bytes_per_step": cfg.tokens * layer.out_width * elem},
+            "gpu_launches": launches,
+            "clocks": clk}
+    if rank == 0 and world == 1 and args.cpu_sample > 0:
+        layer.close()
+        y = flush = None
+        host = inputs.host_inputs(inp)
+        dt = oracle_sample(cfg, host, args.cpu_sample, cfg.seed + 99)
+        line["cpu_baseline"] = {"value": args.cpu_sample / dt, "unit": UNIT, "cores": blas_threads(),
+                                "kind": "oracle",
+                                "sample": f"{args.cpu_sample} seeded token rows of the workload, fp64 oracle"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    layer.close()
+    if dist:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

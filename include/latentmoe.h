@@ -151,6 +151,20 @@ size_t latentmoe_workspace_bytes(const lmoe_handle *h);
  * LMOE_ERR_TIMEOUT.  No fault, trap or hang results; other tiles complete normally. */
 lmoe_status latentmoe_set_wait_limit(lmoe_handle *h, uint64_t timeout_ns, int32_t inject);
 
+/* Stage timing.  With `events` non-NULL (n_events >= LMOE_NUM_STAGES + 1 cudaEvent_t
+ * handles created by the caller, passed as void*), later route/forward calls record
+ * events[0] on `stream` before their first launch and events[i+1] after stage i, so that
+ * cudaEventElapsedTime(events[i], events[i+1]) is the device time of stage i on the
+ * launching stream.  Stages a call does not run are recorded back to back (zero time).
+ * NULL switches recording off.  The handle does not own the events. */
+#define LMOE_NUM_STAGES 10
+lmoe_status latentmoe_set_stage_events(lmoe_handle *h, void *const *events, int32_t n_events);
+
+/* Name of stage i (0 <= i < LMOE_NUM_STAGES): router_logits, topk, dispatch, w_down,
+ * scatter_rows, routed_gate_up_glu, routed_down, combine_rmsnorm, shared_gate_up_glu,
+ * final_gemm; NULL otherwise. */
+const char *latentmoe_stage_name(int32_t i);
+
 /* Static description of a status code. */
 const char *latentmoe_status_string(lmoe_status s);
 

@@ -21,6 +21,7 @@ LMOE_OK, LMOE_ERR_INVALID_ARG, LMOE_ERR_UNSUPPORTED, LMOE_ERR_CUDA, LMOE_ERR_OOM
     LMOE_ERR_DEVICE_CHECK = range(7)
 DTYPES = {"f32": 0, "bf16": 1, "mxfp4": 2}
 LMOE_FLAG_IDENTITY_EXPERTS = 0x1
+LMOE_NUM_STAGES = 10
 
 
 class LmoeConfig(C.Structure):
@@ -64,6 +65,10 @@ def _lib():
         lib.latentmoe_workspace_bytes.argtypes = [vp]
         lib.latentmoe_workspace_bytes.restype = C.c_size_t
         lib.latentmoe_set_wait_limit.argtypes = [vp, C.c_uint64, i32]
+        lib.latentmoe_set_stage_events.argtypes = [vp, C.POINTER(vp), i32]
+        lib.latentmoe_set_stage_events.restype = st
+        lib.latentmoe_stage_name.argtypes = [i32]
+        lib.latentmoe_stage_name.restype = C.c_char_p
         lib.latentmoe_status_string.argtypes = [st]
         lib.latentmoe_status_string.restype = C.c_char_p
         for name in ("latentmoe_create", "latentmoe_destroy", "latentmoe_route", "latentmoe_forward",
@@ -182,6 +187,18 @@ class LatentMoE:
 
     def workspace_bytes(self) -> int:
         return _lib().latentmoe_workspace_bytes(self._h)
+
+    def enable_stage_timing(self):
+        """Record a CUDA event between the stages of later calls (see stage_times_ms)."""
+        self._events = [torch.cuda.Event(enable_timing=True) for _ in range(LMOE_NUM_STAGES + 1)]
+        arr = (C.c_void_p * len(self._events))(*[e.cuda_event for e in self._events])
+        _check(_lib().latentmoe_set_stage_events(self._h, arr, len(self._events)), "set_stage_events")
+
+    def stage_times_ms(self) -> dict:
+        """Device time of each stage of the last call (synchronises on its last event)."""
+        self._events[-1].synchronize()
+        return {_lib().latentmoe_stage_name(i).decode(): self._events[i].elapsed_time(self._events[i + 1])
+                for i in range(LMOE_NUM_STAGES)}
 
     def set_wait_limit(self, timeout_ns: int, inject: bool = False):
         _check(_lib().latentmoe_set_wait_limit(self._h, int(timeout_ns), 1 if inject else 0), "set_wait_limit")

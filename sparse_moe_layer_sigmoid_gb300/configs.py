@@ -50,9 +50,13 @@ K3_MXFP4_PREFILL_MILD = replace(K3_MXFP4_PREFILL_SKEW, name="k3_mxfp4_prefill_mi
 ROUTING_DISPATCH_STRESS = LayerConfig("routing_dispatch_t65536", 65536, 7168, 3584, 0, 896, 16, 0, 0,
                                       "bf16", "f32", "bf16", "zipf1.1", True, 4)
 
+# Same widths as the bf16 prefill workload with 32 experts and 1024 tokens: about 2.5 GB on the
+# device (weights still far larger than L2), small enough for multi-pass profiler captures.
+K3W_E32_BF16_PROFILE = replace(K3W_E128_BF16_PREFILL, name="k3w_e32_bf16_t1024", tokens=1024, experts=32)
+
 CONFIGS = {c.name: c for c in (TINY_F32, K3W_E128_BF16_PREFILL, K3_MXFP4_DECODE,
                                K3_MXFP4_PREFILL_SKEW, K3_MXFP4_PREFILL_MILD,
-                               ROUTING_DISPATCH_STRESS)}
+                               ROUTING_DISPATCH_STRESS, K3W_E32_BF16_PROFILE)}
 
 
 def scaled(cfg: LayerConfig, **kw) -> LayerConfig:

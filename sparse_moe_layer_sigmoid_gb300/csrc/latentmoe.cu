@@ -39,6 +39,9 @@ struct lmoe_handle {
   int last_launches;
   uint64_t timeout_ns;
   int inject;
+  cudaEvent_t stage_ev[LMOE_NUM_STAGES + 1];  // caller-owned; recording on when stage_on
+  bool stage_on;
+  int marked;                                 // index of the last stage event recorded
 };
 
 namespace {
@@ -50,6 +53,30 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 lmoe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? LMOE_OK : LMOE_ERR_CUDA; }
+
+enum Stage : int {
+  kStRouter = 0, kStTopk, kStDispatch, kStWDown, kStScatter, kStGlu, kStDown, kStCombine, kStSharedGlu, kStFinal
+};
+const char* const kStageNames[LMOE_NUM_STAGES] = {
+    "router_logits", "topk", "dispatch", "w_down", "scatter_rows", "routed_gate_up_glu", "routed_down",
+    "combine_rmsnorm", "shared_gate_up_glu", "final_gemm"};
+
+// Stage i spans stage_ev[i] .. stage_ev[i+1]; skipped stages get zero width.
+void stages_start(lmoe_handle* h, cudaStream_t s) {
+  if (!h->stage_on) return;
+  cudaEventRecord(h->stage_ev[0], s);
+  h->marked = 0;
+}
+void stage_begin(lmoe_handle* h, int i, cudaStream_t s) {
+  if (!h->stage_on) return;
+  while (h->marked < i) cudaEventRecord(h->stage_ev[++h->marked], s);
+}
+void stage_end(lmoe_handle* h, int i, cudaStream_t s) {
+  if (!h->stage_on) return;
+  stage_begin(h, i, s);
+  cudaEventRecord(h->stage_ev[++h->marked], s);
+}
+void stages_finish(lmoe_handle* h, cudaStream_t s) { stage_begin(h, LMOE_NUM_STAGES, s); }
 
 #define LMOE_TRY(expr)                          \
   do {                                          \
@@ -157,13 +184,18 @@ lmoe_status run_routing(lmoe_handle* h, const void* x, int T, const lmoe_weights
   const int32_t* idx = ext_idx;
   const float* p = ext_p;
   if (!ext_idx) {
+    stage_begin(h, kStRouter, s);
     LMOE_TRY(launch_router_logits(x, c.act, w->w_router, c.router_w, h->logits, T, c.num_experts, c.d, s));
+    stage_end(h, kStRouter, s);
     LMOE_TRY(launch_topk(h->logits, w->router_bias, T, c.num_experts, c.top_k, h->idx, h->p, s));
+    stage_end(h, kStTopk, s);
     h->last_launches += 2;
     idx = h->idx;
     p = h->p;
   }
+  stage_begin(h, kStDispatch, s);
   LMOE_TRY(launch_dispatch(idx, p, T, c.num_experts, c.top_k, h->db, h->status, &h->last_launches, s));
+  stage_end(h, kStDispatch, s);
   *idx_out = idx;
   *p_out = p;
   return LMOE_OK;
@@ -180,11 +212,13 @@ lmoe_status run_forward(lmoe_handle* h, const void* x, int T, const lmoe_weights
   const int kcat = ns * hs + l;
   const size_t ab = dtype_bytes(c.act);
   h->last_launches = 0;
+  stages_start(h, s);
 
   const int32_t* idx;
   const float* p;
   lmoe_status st = run_routing(h, x, T, w, ext_idx, ext_p, &idx, &p, s);
   if (st != LMOE_OK) return st;
+  stage_begin(h, kStWDown, s);
 
   // z = W_down x
   if (tc) {
@@ -204,12 +238,17 @@ lmoe_status run_forward(lmoe_handle* h, const void* x, int T, const lmoe_weights
     g.C = h->z; g.ldc = l; g.c_dtype = c.act;
     LMOE_TRY(launch_simt_gemm(g, s));
   }
+  stage_end(h, kStWDown, s);
   // rows of z into expert-contiguous order
   LMOE_TRY(launch_scatter_rows(h->z, h->z_perm, h->db.row_of, T, k, l, (int)ab, s));
+  stage_end(h, kStScatter, s);
   h->last_launches += 2;
 
   if (identity) {
+    stage_begin(h, kStCombine, s);
     LMOE_TRY(launch_combine(h->z_perm, c.act, h->db.row_of, p, nullptr, 0.f, T, k, l, y, l, s));
+    stage_end(h, kStCombine, s);
+    stages_finish(h, s);
     h->last_launches += 1;
     return LMOE_OK;
   }
@@ -227,6 +266,7 @@ lmoe_status run_forward(lmoe_handle* h, const void* x, int T, const lmoe_weights
     g.C = h->a; g.ldc = hdim;
     LMOE_TRY(launch_tc_gemm(g, h->status, h->timeout_ns, h->inject, h->num_sms, s));
     h->inject = 0;
+    stage_end(h, kStGlu, s);
 
     TcGemm dn = {};
     dn.epi = kEpiScaleBF16;
@@ -237,6 +277,7 @@ lmoe_status run_forward(lmoe_handle* h, const void* x, int T, const lmoe_weights
     dn.tiles = h->db.tiles; dn.num_tiles = h->db.num_tiles; dn.offsets = h->db.offsets; dn.max_tiles = h->max_tiles;
     dn.C = o; dn.ldc = l; dn.row_scale = h->db.p_row;
     LMOE_TRY(launch_tc_gemm(dn, h->status, h->timeout_ns, 0, h->num_sms, s));
+    stage_end(h, kStDown, s);
   } else {
     SimtGemm g = {};
     g.A = h->z_perm; g.lda = l; g.a_dtype = c.act; g.b_dtype = c.routed_w;
@@ -245,6 +286,7 @@ lmoe_status run_forward(lmoe_handle* h, const void* x, int T, const lmoe_weights
     g.tiles = h->db.tiles; g.num_tiles = h->db.num_tiles; g.offsets = h->db.offsets; g.max_tiles = h->max_tiles;
     g.C = h->a; g.ldc = hdim; g.c_dtype = c.act;
     LMOE_TRY(launch_simt_gemm(g, s));
+    stage_end(h, kStGlu, s);
 
     SimtGemm dn = {};
     dn.A = h->a; dn.lda = hdim; dn.a_dtype = c.act; dn.b_dtype = c.routed_w;
@@ -253,9 +295,11 @@ lmoe_status run_forward(lmoe_handle* h, const void* x, int T, const lmoe_weights
     dn.tiles = h->db.tiles; dn.num_tiles = h->db.num_tiles; dn.offsets = h->db.offsets; dn.max_tiles = h->max_tiles;
     dn.C = o; dn.ldc = l; dn.c_dtype = c.act; dn.row_scale = h->db.p_row;
     LMOE_TRY(launch_simt_gemm(dn, s));
+    stage_end(h, kStDown, s);
   }
   // u = sum_j o_j (rank order), n = RMSNorm(u) into the tail columns of act_cat
   LMOE_TRY(launch_combine(o, c.act, h->db.row_of, nullptr, w->rms_gain, c.rms_eps, T, k, l, n_out, kcat, s));
+  stage_end(h, kStCombine, s);
   h->last_launches += 3;
 
   if (tc) {
@@ -268,8 +312,10 @@ lmoe_status run_forward(lmoe_handle* h, const void* x, int T, const lmoe_weights
       g.k0_len = d; g.k0_per_group = d; g.glu_h = hs;
       g.C = h->act_cat; g.ldc = kcat;
       LMOE_TRY(launch_tc_gemm(g, h->status, h->timeout_ns, 0, h->num_sms, s));
+      stage_end(h, kStSharedGlu, s);
       h->last_launches += 1;
     }
+    stage_begin(h, kStFinal, s);
     TcGemm f = {};
     f.epi = kEpiBF16;
     f.M = T; f.N = d; f.K = kcat;
@@ -284,6 +330,7 @@ lmoe_status run_forward(lmoe_handle* h, const void* x, int T, const lmoe_weights
     }
     f.C = y; f.ldc = d;
     LMOE_TRY(launch_tc_gemm(f, h->status, h->timeout_ns, 0, h->num_sms, s));
+    stage_end(h, kStFinal, s);
     h->last_launches += 1;
   } else {
     if (ns > 0) {
@@ -293,8 +340,10 @@ lmoe_status run_forward(lmoe_handle* h, const void* x, int T, const lmoe_weights
       g.M = T; g.N = ns * hs; g.K = d; g.glu_h = hs;
       g.C = h->act_cat; g.ldc = kcat; g.c_dtype = c.act;
       LMOE_TRY(launch_simt_gemm(g, s));
+      stage_end(h, kStSharedGlu, s);
       h->last_launches += 1;
     }
+    stage_begin(h, kStFinal, s);
     SimtGemm f = {};
     f.A = h->act_cat; f.lda = kcat; f.a_dtype = c.act; f.b_dtype = c.act;
     f.nseg = 0;
@@ -303,8 +352,10 @@ lmoe_status run_forward(lmoe_handle* h, const void* x, int T, const lmoe_weights
     f.M = T; f.N = d; f.K = kcat;
     f.C = y; f.ldc = d; f.c_dtype = c.act;
     LMOE_TRY(launch_simt_gemm(f, s));
+    stage_end(h, kStFinal, s);
     h->last_launches += 1;
   }
+  stages_finish(h, s);
   return LMOE_OK;
 }
 
@@ -372,8 +423,10 @@ lmoe_status latentmoe_route(lmoe_handle* h, const void* x, int32_t T, const lmoe
   if (T > 0) {
     const int32_t* idx;
     const float* p;
+    stages_start(h, s);
     st = run_routing(h, x, T, w, nullptr, nullptr, &idx, &p, s);
     if (st != LMOE_OK) return st;
+    stages_finish(h, s);
   }
   if (topk_idx && rows) LMOE_TRY(cudaMemcpyAsync(topk_idx, h->idx, rows * 4, cudaMemcpyDeviceToDevice, s));
   if (topk_p && rows) LMOE_TRY(cudaMemcpyAsync(topk_p, h->p, rows * 4, cudaMemcpyDeviceToDevice, s));
@@ -453,6 +506,25 @@ lmoe_status latentmoe_set_wait_limit(lmoe_handle* h, uint64_t timeout_ns, int32_
   h->timeout_ns = timeout_ns;
   h->inject = inject ? 1 : 0;
   return LMOE_OK;
+}
+
+lmoe_status latentmoe_set_stage_events(lmoe_handle* h, void* const* events, int32_t n_events) {
+  if (!h) return LMOE_ERR_INVALID_ARG;
+  if (!events) {
+    h->stage_on = false;
+    return LMOE_OK;
+  }
+  if (n_events < LMOE_NUM_STAGES + 1) return LMOE_ERR_INVALID_ARG;
+  for (int i = 0; i <= LMOE_NUM_STAGES; ++i) {
+    if (!events[i]) return LMOE_ERR_INVALID_ARG;
+    h->stage_ev[i] = static_cast<cudaEvent_t>(events[i]);
+  }
+  h->stage_on = true;
+  return LMOE_OK;
+}
+
+const char* latentmoe_stage_name(int32_t i) {
+  return (i >= 0 && i < LMOE_NUM_STAGES) ? kStageNames[i] : nullptr;
 }
 
 const char* latentmoe_status_string(lmoe_status s) {
