@@ -165,6 +165,25 @@ lmoe_status latentmoe_set_stage_events(lmoe_handle *h, void *const *events, int3
  * final_gemm; NULL otherwise. */
 const char *latentmoe_stage_name(int32_t i);
 
+/* Router and dispatch without any device allocation, for callers that must not allocate
+ * (for example a plugin whose host framework owns all device memory and forbids allocation
+ * while it executes, or a serving loop that plans every byte ahead).  The paper has no
+ * counterpart to this entry point; it computes exactly what latentmoe_route computes.
+ *
+ * No handle: `cfg` supplies d, num_experts, top_k, act and router_w (other fields are
+ * ignored).  Outputs are as for latentmoe_route, but all five must be non-NULL when T > 0.
+ * Scratch lives in one fixed 16 MiB device array inside the library, held on every GPU that
+ * loads the library until the process exits; a call needs
+ *   256*ceil(T*E*4/256) + 2*256*ceil(ceil(T/256)*E*4/256) + 256*ceil((T*k/128+E+1)*16/256) + 256
+ * bytes of it (with k=16: T up to 32,383 for E=128 and up to 4,636 for E=896), and a
+ * larger T returns LMOE_ERR_INVALID_ARG before any launch.  The first call on a device looks
+ * up the array's device address (cudaGetSymbolAddress) and should come before any stream
+ * capture.  Calls that overlap on the GPU share the array and race: serialise them.  Errors:
+ * INVALID_ARG (bad field, pointer or size), CUDA. */
+lmoe_status latentmoe_route_noalloc(const lmoe_config *cfg, const void *x, int32_t T, const lmoe_weights *w,
+                                    int32_t *topk_idx, float *topk_p, int32_t *expert_offsets,
+                                    int32_t *tok_of_row, int32_t *row_of, void *stream);
+
 /* Static description of a status code. */
 const char *latentmoe_status_string(lmoe_status s);
 

@@ -69,6 +69,9 @@ def _lib():
         lib.latentmoe_set_stage_events.restype = st
         lib.latentmoe_stage_name.argtypes = [i32]
         lib.latentmoe_stage_name.restype = C.c_char_p
+        lib.latentmoe_route_noalloc.argtypes = [C.POINTER(LmoeConfig), vp, i32, C.POINTER(LmoeWeights), vp, vp,
+                                                vp, vp, vp, vp]
+        lib.latentmoe_route_noalloc.restype = st
         lib.latentmoe_status_string.argtypes = [st]
         lib.latentmoe_status_string.restype = C.c_char_p
         for name in ("latentmoe_create", "latentmoe_destroy", "latentmoe_route", "latentmoe_forward",
@@ -110,6 +113,17 @@ def make_config(cfg: LayerConfig, max_tokens: int | None = None) -> LmoeConfig:
 
 def make_weights(inp: dict) -> LmoeWeights:
     return LmoeWeights(*[_ptr(inp.get(n)) for n, _ in LmoeWeights._fields_])
+
+
+def route_noalloc(cfg: LayerConfig, x, weights: dict, out: dict, stream=None):
+    """Router and dispatch through latentmoe_route_noalloc (no handle, no device allocation).
+
+    ``out`` holds the caller's output tensors idx, p, offsets, tok_of_row, row_of."""
+    c = make_config(cfg, max(1, x.shape[0]))
+    w = make_weights(weights)
+    return _lib().latentmoe_route_noalloc(C.byref(c), _ptr(x), x.shape[0], C.byref(w), _ptr(out["idx"]),
+                                          _ptr(out["p"]), _ptr(out["offsets"]), _ptr(out["tok_of_row"]),
+                                          _ptr(out["row_of"]), _stream(stream))
 
 
 class LatentMoE:
@@ -191,6 +205,9 @@ class LatentMoE:
     def enable_stage_timing(self):
         """Record a CUDA event between the stages of later calls (see stage_times_ms)."""
         self._events = [torch.cuda.Event(enable_timing=True) for _ in range(LMOE_NUM_STAGES + 1)]
+        for e in self._events:  # torch creates the CUDA event on its first record
+            e.record()
+        torch.cuda.synchronize()
         arr = (C.c_void_p * len(self._events))(*[e.cuda_event for e in self._events])
         _check(_lib().latentmoe_set_stage_events(self._h, arr, len(self._events)), "set_stage_events")
 
