@@ -165,6 +165,15 @@ lmoe_status latentmoe_set_stage_events(lmoe_handle *h, void *const *events, int3
  * final_gemm; NULL otherwise. */
 const char *latentmoe_stage_name(int32_t i);
 
+/* Test hook: device address and byte size of an intermediate of the last call inside the
+ * handle's workspace, by name: "logits" [T][E] fp32, "z" [T][l], "gathered" [T*k][l] (the
+ * expert-contiguous rows; after a full forward it holds the p-scaled expert outputs), "act"
+ * [T*k][h] (routed GLU activations), "act_cat" [T][N_s*h_s + l] (shared activations and
+ * RMSNorm(u)), "p_row" [T*k] fp32.  Activations use the act dtype; T is the last call's T.
+ * The pointers stay valid until latentmoe_destroy.  Unknown name or absent buffer:
+ * LMOE_ERR_INVALID_ARG. */
+lmoe_status latentmoe_debug_buffer(const lmoe_handle *h, const char *name, void **ptr, size_t *bytes);
+
 /* Router and dispatch without any device allocation, for callers that must not allocate
  * (for example a plugin whose host framework owns all device memory and forbids allocation
  * while it executes, or a serving loop that plans every byte ahead).  The paper has no
@@ -175,8 +184,9 @@ const char *latentmoe_stage_name(int32_t i);
  * Scratch lives in one fixed 16 MiB device array inside the library, held on every GPU that
  * loads the library until the process exits; a call needs
  *   256*ceil(T*E*4/256) + 2*256*ceil(ceil(T/256)*E*4/256) + 256*ceil((T*k/128+E+1)*16/256) + 256
- * bytes of it (with k=16: T up to 32,383 for E=128 and up to 4,636 for E=896), and a
- * larger T returns LMOE_ERR_INVALID_ARG before any launch.  The first call on a device looks
+ * bytes of it, plus 256*ceil(3*E*d*2/256) when act is BF16 and router_w is F32 (the three bf16
+ * terms of W_r); with k=16 and a bf16 W_r, T up to 32,383 for E=128 and up to 4,636 for E=896; a
+ * larger need returns LMOE_ERR_INVALID_ARG before any launch.  The first call on a device looks
  * up the array's device address (cudaGetSymbolAddress) and should come before any stream
  * capture.  Calls that overlap on the GPU share the array and race: serialise them.  Errors:
  * INVALID_ARG (bad field, pointer or size), CUDA. */

@@ -102,9 +102,14 @@ def sigmoid(v):
         return 1.0 / (1.0 + np.exp(-v))
 
 
+def router_logits(x, w_router) -> np.ndarray:
+    """W_r x for each token row of x: [n, E]."""
+    return x @ w_router.T
+
+
 def router_scores(x, w_router) -> np.ndarray:
     """s = Sigmoid(W_r x) for each token row of x: [n, E]."""
-    return sigmoid(x @ w_router.T)
+    return sigmoid(router_logits(x, w_router))
 
 
 def select_topk(s, bias, k):

@@ -72,6 +72,8 @@ def _lib():
         lib.latentmoe_route_noalloc.argtypes = [C.POINTER(LmoeConfig), vp, i32, C.POINTER(LmoeWeights), vp, vp,
                                                 vp, vp, vp, vp]
         lib.latentmoe_route_noalloc.restype = st
+        lib.latentmoe_debug_buffer.argtypes = [vp, C.c_char_p, C.POINTER(vp), C.POINTER(C.c_size_t)]
+        lib.latentmoe_debug_buffer.restype = st
         lib.latentmoe_status_string.argtypes = [st]
         lib.latentmoe_status_string.restype = C.c_char_p
         for name in ("latentmoe_create", "latentmoe_destroy", "latentmoe_route", "latentmoe_forward",
@@ -103,6 +105,20 @@ def _stream(stream):
 def _check(status, what):
     if status != LMOE_OK:
         raise LatentMoEError(status, what)
+
+
+class _DeviceArray:
+    """Minimal __cuda_array_interface__ holder for a raw device pointer (no ownership)."""
+
+    def __init__(self, ptr: int, nbytes: int):
+        self.__cuda_array_interface__ = {"shape": (nbytes,), "typestr": "|u1", "data": (ptr, False), "version": 3}
+
+
+def _wrap_device_pointer(ptr: int, nbytes: int, dtype, shape):
+    """Copy `nbytes` at a raw device pointer into a new torch tensor viewed as dtype/shape."""
+    torch.cuda.synchronize()
+    raw = torch.as_tensor(_DeviceArray(ptr, nbytes), device="cuda")
+    return raw.clone().view(dtype).reshape(shape)
 
 
 def make_config(cfg: LayerConfig, max_tokens: int | None = None) -> LmoeConfig:
@@ -192,6 +208,18 @@ class LatentMoE:
                                       _ptr(out["offsets"]), _ptr(out["tok_of_row"]), _ptr(out["row_of"]),
                                       _stream(stream)), "latentmoe_route")
         return out
+
+    def debug_buffer(self, name: str, dtype, shape):
+        """View of a workspace intermediate of the last call (test hook; see latentmoe.h)."""
+        ptr, nbytes = C.c_void_p(), C.c_size_t()
+        _check(_lib().latentmoe_debug_buffer(self._h, name.encode(), C.byref(ptr), C.byref(nbytes)),
+               f"debug_buffer({name})")
+        n = 1
+        for s_ in shape:
+            n *= s_
+        esize = torch.empty((), dtype=dtype).element_size()
+        assert n * esize <= nbytes.value, (name, n * esize, nbytes.value)
+        return _wrap_device_pointer(ptr.value, n * esize, dtype, shape)
 
     def status(self, stream=None) -> int:
         return _lib().latentmoe_status(self._h, _stream(stream))

@@ -41,6 +41,7 @@ struct Cfg {
 struct TcParams {
   int M, N;
   int num_kb, kb0, kb0_per_group;
+  int a_kb_period;  // A's K coordinate repeats every a_kb_period k-blocks (K-concatenated B terms)
   int glu_h;
   int num_m_tiles, num_n_tiles;
   const int4* tiles;
@@ -139,7 +140,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint8_t* sA = smem + stage * C::kStageBytes;
           uint8_t* sB = sA + C::kABytes;
           ptx::mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
-          ptx::tma_load_3d(sA, &tmA, &full[stage], kb * BK, ti.row0, 0);
+          ptx::tma_load_3d(sA, &tmA, &full[stage], (kb % p.a_kb_period) * BK, ti.row0, 0);
           if (GLU) {
             const int grp = ti.group + ti.n0 / p.glu_h, j0 = ti.n0 % p.glu_h;
             ptx::tma_load_3d(sB, &tmB0, &full[stage], kb * BK, j0, grp);
@@ -235,6 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float sc = (EPI == kEpiScaleBF16 && live) ? p.row_scale[row] : 1.0f;
 #pragma unroll 1
         for (int c = 0; c < BN; c += 32) {
+          if (ti.n0 + c >= p.N) break;  // ragged last column tile (fp32: N % 4 == 0, else N % 32 == 0)
           uint32_t r[32];
           ptx::tmem_ld_32x32b_x32(t_row + c, r);
           ptx::tmem_ld_wait();
@@ -242,7 +244,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (EPI == kEpiF32) {
               uint4* dst = reinterpret_cast<uint4*>(static_cast<float*>(p.C) + (int64_t)row * p.ldc + ti.n0 + c);
 #pragma unroll
-              for (int i = 0; i < 8; ++i) dst[i] = make_uint4(r[4 * i], r[4 * i + 1], r[4 * i + 2], r[4 * i + 3]);
+              for (int i = 0; i < 8; ++i)
+                if (ti.n0 + c + 4 * i < p.N) dst[i] = make_uint4(r[4 * i], r[4 * i + 1], r[4 * i + 2], r[4 * i + 3]);
             } else {
               uint32_t packed[16];
 #pragma unroll
@@ -325,7 +328,10 @@ cudaError_t launch_tc_gemm(const TcGemm& g, uint32_t* status, uint64_t timeout_n
   const bool grouped = g.tiles != nullptr;
   const int bn = 256;
   const int bn_out = glu ? bn / 2 : bn;
-  if (g.K % BK || g.k0_len % BK || g.k0_per_group % BK || g.N % bn_out) return cudaErrorInvalidValue;
+  if (g.K % BK || g.k0_len % BK || g.k0_per_group % BK) return cudaErrorInvalidValue;
+  if (glu ? g.N % bn_out : g.N % (g.epi == kEpiF32 ? 4 : 32)) return cudaErrorInvalidValue;
+  const int a_period = g.a_k_period ? g.a_k_period : g.K;
+  if (a_period % BK || g.K % a_period) return cudaErrorInvalidValue;
   if (glu && g.glu_h % kBoxRows) return cudaErrorInvalidValue;
   CUtensorMap ma, mb0, mb1;
   if (!make_map(&ma, g.A) || !make_map(&mb0, g.B0)) return cudaErrorInvalidValue;
@@ -340,9 +346,10 @@ cudaError_t launch_tc_gemm(const TcGemm& g, uint32_t* status, uint64_t timeout_n
   p.num_kb = g.K / BK;
   p.kb0 = g.k0_len / BK;
   p.kb0_per_group = g.k0_per_group / BK;
+  p.a_kb_period = a_period / BK;
   p.glu_h = glu ? g.glu_h : 1;
   p.num_m_tiles = (g.M + BM - 1) / BM;
-  p.num_n_tiles = g.N / bn_out;
+  p.num_n_tiles = (g.N + bn_out - 1) / bn_out;
   p.tiles = g.tiles;
   p.num_tiles = g.num_tiles;
   p.offsets = g.offsets;

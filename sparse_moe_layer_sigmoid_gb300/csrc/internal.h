@@ -11,9 +11,30 @@ namespace lmoe {
 // logits[T][E] = x[T][d] . W_r[E][d]^T in fp32 (CUDA cores, fixed K order per output).
 cudaError_t launch_router_logits(const void* x, int x_dtype, const void* w_router, int w_dtype, float* logits,
                                  int T, int E, int d, cudaStream_t s);
-// s = sigmoid(logits), key = s + b, top-k by (key desc, index asc), p = s / sum(s over T_k).
-cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, int k, int32_t* idx, float* p,
-                        cudaStream_t s);
+// Router logits for either activation type: bf16 activations use the tensor cores (an fp32 W_r
+// is first split into three bf16 terms in `wr_split`, [3][E][d] bf16, then contracted over
+// K = 3d), fp32 activations the CUDA-core GEMM.  Adds its kernel count to *launches.
+cudaError_t launch_router(const void* x, int act, const void* w_router, int router_w, float* logits,
+                          void* wr_split, int T, int E, int d, uint32_t* status, uint64_t timeout_ns, int num_sms,
+                          int* launches, cudaStream_t s);
+// Exact split of fp32 W_r into three bf16 terms, out[t][e][c], t = hi, mid, lo:
+// w = hi + mid + lo with each term the bf16 rounding of what the previous terms left.
+cudaError_t launch_split_bf16x3(const float* w, int64_t n, void* out, cudaStream_t s);
+// Operands of the router GEMM, for exact recomputation of logits near the top-k boundary.
+struct RouterSrc {
+  const void* x; int x_dtype;  // [T][d]
+  const void* w; int w_dtype;  // [E][d]
+  int d;
+  float margin;                // bound on |logits[t][e] - exact logit|
+};
+// Logit error bound used for the router GEMMs (tensor cores with fp32 accumulation, or the
+// fp32 CUDA-core GEMM): measured errors are below 1e-4 at d = 7168 (tested).
+constexpr float kRouterLogitMargin = 1e-3f;
+// s = sigmoid(logits), key = s + b, top-k by (key desc, index asc), p = s / sum(s over T_k);
+// membership at the k-th/(k+1)-th boundary is decided on exact fp64 keys when the
+// approximate keys are within the margin.
+cudaError_t launch_topk(const float* logits, const float* bias, const RouterSrc& src, int T, int E, int k,
+                        int32_t* idx, float* p, cudaStream_t s);
 // Deterministic expert batches: per-chunk counts, scan, stable (expert, token) rows, the
 // grouped-GEMM M-tile list, and per-row weights.  idx entries outside [0,E) are reported.
 struct DispatchBuffers {
@@ -73,6 +94,7 @@ struct TcGemm {
   TcOperand B0, B1;       // B1.ptr == nullptr when K has a single segment
   int k0_len;             // K columns served by B0 (multiple of 64)
   int k0_per_group;       // B0 K columns per depth slice (K-concatenated groups), else k0_len
+  int a_k_period;         // A's K coordinate wraps every a_k_period columns (0 = K: no wrap)
   int glu_h;              // GLU: rows of B between gate and up; output column j -> (j / glu_h, j % glu_h)
   const int4* tiles; const int32_t* num_tiles; const int32_t* offsets; int max_tiles;  // grouped mode
   void* C; int64_t ldc;

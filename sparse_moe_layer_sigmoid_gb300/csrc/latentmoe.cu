@@ -36,9 +36,11 @@ struct lmoe_handle {
   void* act_cat; // [T][N_s*h_s + l]: shared GLU activations | RMSNorm(u)
   void* x_stage; // forward_host staging
   void* y_stage;
+  void* wr_split; // bf16 hi/mid/lo terms of an fp32 W_r [3][E][d] (bf16 activations only)
   int last_launches;
   uint64_t timeout_ns;
   int inject;
+  int last_T;                                 // T of the last call (for latentmoe_debug_buffer)
   cudaEvent_t stage_ev[LMOE_NUM_STAGES + 1];  // caller-owned; recording on when stage_on
   bool stage_on;
   int marked;                                 // index of the last stage event recorded
@@ -104,7 +106,7 @@ lmoe_status validate_config(const lmoe_config& c) {
     if (c.latent > 4096) return LMOE_ERR_UNSUPPORTED;
   } else {
     // tensor-core tiles: K steps of 64, output tiles of 256 columns (128 for GLU halves)
-    if (c.d % 256 || c.latent % 256 || c.latent > 8192) return LMOE_ERR_UNSUPPORTED;
+    if (c.d % 256 || c.latent % 256 || c.latent > 8192 || c.num_experts % 4) return LMOE_ERR_UNSUPPORTED;
     if (!identity) {
       if (c.routed_w != LMOE_BF16) return LMOE_ERR_UNSUPPORTED;
       if (c.hidden % 128) return LMOE_ERR_UNSUPPORTED;
@@ -148,6 +150,7 @@ size_t layout(lmoe_handle* h, uint8_t* base) {
   h->act_cat = identity ? nullptr : take(T * kcat * ab);
   h->x_stage = take(T * (size_t)c.d * ab);
   h->y_stage = take(T * (size_t)(identity ? c.latent : c.d) * ab);
+  h->wr_split = (c.act == LMOE_BF16 && c.router_w == LMOE_F32) ? take(3 * E * (size_t)c.d * 2) : nullptr;
   return off;
 }
 
@@ -185,11 +188,13 @@ lmoe_status run_routing(lmoe_handle* h, const void* x, int T, const lmoe_weights
   const float* p = ext_p;
   if (!ext_idx) {
     stage_begin(h, kStRouter, s);
-    LMOE_TRY(launch_router_logits(x, c.act, w->w_router, c.router_w, h->logits, T, c.num_experts, c.d, s));
+    LMOE_TRY(launch_router(x, c.act, w->w_router, c.router_w, h->logits, h->wr_split, T, c.num_experts, c.d,
+                           h->status, h->timeout_ns, h->num_sms, &h->last_launches, s));
     stage_end(h, kStRouter, s);
-    LMOE_TRY(launch_topk(h->logits, w->router_bias, T, c.num_experts, c.top_k, h->idx, h->p, s));
+    const RouterSrc rs{x, c.act, w->w_router, c.router_w, c.d, kRouterLogitMargin};
+    LMOE_TRY(launch_topk(h->logits, w->router_bias, rs, T, c.num_experts, c.top_k, h->idx, h->p, s));
     stage_end(h, kStTopk, s);
-    h->last_launches += 2;
+    h->last_launches += 1;
     idx = h->idx;
     p = h->p;
   }
@@ -212,6 +217,7 @@ lmoe_status run_forward(lmoe_handle* h, const void* x, int T, const lmoe_weights
   const int kcat = ns * hs + l;
   const size_t ab = dtype_bytes(c.act);
   h->last_launches = 0;
+  h->last_T = T;
   stages_start(h, s);
 
   const int32_t* idx;
@@ -520,6 +526,25 @@ lmoe_status latentmoe_set_stage_events(lmoe_handle* h, void* const* events, int3
     h->stage_ev[i] = static_cast<cudaEvent_t>(events[i]);
   }
   h->stage_on = true;
+  return LMOE_OK;
+}
+
+lmoe_status latentmoe_debug_buffer(const lmoe_handle* h, const char* name, void** ptr, size_t* bytes) {
+  if (!h || !name || !ptr || !bytes) return LMOE_ERR_INVALID_ARG;
+  const lmoe_config& c = h->cfg;
+  const size_t T = (size_t)h->last_T, k = (size_t)c.top_k, ab = dtype_bytes(c.act);
+  const size_t kcat = (size_t)c.num_shared * c.shared_hidden + c.latent;
+  void* p = nullptr;
+  size_t n = 0;
+  if (!strcmp(name, "logits")) { p = h->logits; n = T * c.num_experts * 4; }
+  else if (!strcmp(name, "z")) { p = h->z; n = T * c.latent * ab; }
+  else if (!strcmp(name, "gathered")) { p = h->z_perm; n = T * k * c.latent * ab; }
+  else if (!strcmp(name, "act")) { p = h->a; n = T * k * (size_t)c.hidden * ab; }
+  else if (!strcmp(name, "act_cat")) { p = h->act_cat; n = T * kcat * ab; }
+  else if (!strcmp(name, "p_row")) { p = h->db.p_row; n = T * k * 4; }
+  if (!p) return LMOE_ERR_INVALID_ARG;
+  *ptr = p;
+  *bytes = n;
   return LMOE_OK;
 }
 

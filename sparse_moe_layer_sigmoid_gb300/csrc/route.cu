@@ -17,43 +17,147 @@ __device__ __forceinline__ uint32_t orderable(float f) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// One warp per token.  Keys are packed as (orderable(s + b) << 32) | (~expert) so that the
+__device__ __forceinline__ float from_orderable(uint32_t u) {
+  return __uint_as_float((u & 0x80000000u) ? (u & 0x7FFFFFFFu) : ~u);
+}
+
+// Double-float accumulator (hi + lo, |lo| <= ulp(hi)/2): products of bf16/fp32 operands are
+// split exactly with an FMA (TwoProd) and added with Knuth's TwoSum, so the sum of d products
+// keeps about 44 significant bits: far below the spacing of the decisions it settles.
+struct DF {
+  float hi, lo;
+};
+__device__ __forceinline__ void df_add_prod(DF& a, float x, float w) {
+  const float p = x * w;
+  const float pe = fmaf(x, w, -p);  // exact: p + pe == x * w
+  const float s = a.hi + p;
+  const float bb = s - a.hi;
+  const float se = (a.hi - (s - bb)) + (p - bb);  // exact: s + se == a.hi + p
+  a.hi = s;
+  a.lo += se + pe;
+}
+__device__ __forceinline__ DF df_add(DF a, DF b) {
+  const float s = a.hi + b.hi;
+  const float bb = s - a.hi;
+  const float se = (a.hi - (s - bb)) + (b.hi - bb);
+  DF r;
+  r.lo = se + a.lo + b.lo;
+  r.hi = s + r.lo;  // renormalise
+  r.lo = r.lo - (r.hi - s);
+  return r;
+}
+
+__device__ __forceinline__ void load8(const __nv_bfloat16* p, float (&f)[8]) {
+  const uint4 v = *reinterpret_cast<const uint4*>(p);
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 t = __bfloat1622float2(h[i]);
+    f[2 * i] = t.x;
+    f[2 * i + 1] = t.y;
+  }
+}
+__device__ __forceinline__ void load8(const float* p, float (&f)[8]) {
+  const float4 a = *reinterpret_cast<const float4*>(p);
+  const float4 b = *reinterpret_cast<const float4*>(p + 4);
+  f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+  f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+}
+
+template <typename TX, typename TW>
+__device__ DF dot_df(const TX* x, const TW* w, int d, int lane) {
+  DF acc0 = {0.f, 0.f}, acc1 = {0.f, 0.f};
+  for (int c = lane * 8; c < d; c += 32 * 8) {  // d % 16 == 0 and 16-byte aligned rows
+    float xf[8], wf[8];
+    load8(x + c, xf);
+    load8(w + c, wf);
+#pragma unroll
+    for (int i = 0; i < 8; i += 2) {
+      df_add_prod(acc0, xf[i], wf[i]);
+      df_add_prod(acc1, xf[i + 1], wf[i + 1]);
+    }
+  }
+  DF acc = df_add(acc0, acc1);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    DF o;
+    o.hi = __shfl_xor_sync(0xffffffffu, acc.hi, off);
+    o.lo = __shfl_xor_sync(0xffffffffu, acc.lo, off);
+    acc = df_add(acc, o);
+  }
+  return acc;
+}
+
+// Logit of expert e for token t to ~44 bits (one warp; every lane returns the same value).
+__device__ double exact_logit(const RouterSrc& r, int t, int e, int lane) {
+  const int64_t xo = (int64_t)t * r.d, wo = (int64_t)e * r.d;
+  DF v;
+  if (r.x_dtype == kBF16 && r.w_dtype == kBF16)
+    v = dot_df(static_cast<const __nv_bfloat16*>(r.x) + xo, static_cast<const __nv_bfloat16*>(r.w) + wo, r.d, lane);
+  else if (r.x_dtype == kBF16)
+    v = dot_df(static_cast<const __nv_bfloat16*>(r.x) + xo, static_cast<const float*>(r.w) + wo, r.d, lane);
+  else if (r.w_dtype == kBF16)
+    v = dot_df(static_cast<const float*>(r.x) + xo, static_cast<const __nv_bfloat16*>(r.w) + wo, r.d, lane);
+  else
+    v = dot_df(static_cast<const float*>(r.x) + xo, static_cast<const float*>(r.w) + wo, r.d, lane);
+  return (double)v.hi + (double)v.lo;
+}
+
+// One warp per token.  Keys s + b are packed as (orderable(key) << 32) | (~expert) so that the
 // 64-bit maximum is the largest key and, among equal keys, the lowest expert index.
+//
+// The logits come from a GEMM whose error is bounded by `src.margin`, so a key is known to
+// within eta = margin/4 (+ fp32 rounding).  When the k-th and (k+1)-th keys are closer than
+// 2*eta the selected set is not certain: every expert whose key lies in the band around the
+// boundary has its logit recomputed to ~44 bits and its key evaluated in fp64, and the open
+// slots are filled from those keys (ties to the lower index).  Experts above the
+// band are in for certain, experts below it out.  The output lists the certain experts in
+// descending key order, then the refined winners in descending exact-key order.
 template <int NPL>
 __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ logits,
-                                                   const float* __restrict__ bias, int T, int E, int k,
-                                                   int32_t* __restrict__ idx, float* __restrict__ p) {
-  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+                                                   const float* __restrict__ bias, RouterSrc src, int T, int E,
+                                                   int k, int32_t* __restrict__ idx, float* __restrict__ p) {
+  const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
-  if (warp >= T) return;
-  const float* row = logits + (size_t)warp * E;
-  uint64_t key[NPL];
-  float sv[NPL];
+  if (t >= T) return;
+  const float* row = logits + (size_t)t * E;
+  float kf[NPL], sv[NPL];
+  uint32_t taken = 0;
 #pragma unroll
   for (int i = 0; i < NPL; ++i) {
     const int e = lane + 32 * i;
-    key[i] = 0;
+    kf[i] = -INFINITY;
     sv[i] = 0.f;
     if (e < E) {
       const float s = 1.0f / (1.0f + expf(-row[e]));
-      const float kf = bias ? s + bias[e] : s;
-      key[i] = ((uint64_t)orderable(kf) << 32) | (uint64_t)(0xFFFFFFFFu - (uint32_t)e);
+      kf[i] = bias ? s + bias[e] : s;
       sv[i] = s;
     }
   }
-  float sum = 0.f;
   int my_e = 0;
-  float my_s = 0.f;
-  for (int j = 0; j < k; ++j) {
+  float my_s = 0.f, my_kf = 0.f, a_k = 0.f, a_k1 = -INFINITY;
+  const int rounds = k < E ? k + 1 : k;
+  for (int j = 0; j < rounds; ++j) {
     uint64_t best = 0;
 #pragma unroll
-    for (int i = 0; i < NPL; ++i) best = key[i] > best ? key[i] : best;
+    for (int i = 0; i < NPL; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E && !((taken >> i) & 1u)) {
+        const uint64_t pk = ((uint64_t)orderable(kf[i]) << 32) | (uint64_t)(0xFFFFFFFFu - (uint32_t)e);
+        best = pk > best ? pk : best;
+      }
+    }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
       const uint64_t o = __shfl_xor_sync(0xffffffffu, best, off);
       best = o > best ? o : best;
     }
     const int e_win = (int)(0xFFFFFFFFu - (uint32_t)(best & 0xFFFFFFFFu));
+    const float kf_win = from_orderable((uint32_t)(best >> 32));
+    if (j == k) {
+      a_k1 = kf_win;
+      break;
+    }
     const int owner = e_win & 31, slot = e_win >> 5;
     float s_here = 0.f;
     if (lane == owner) {
@@ -61,19 +165,95 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ log
       for (int i = 0; i < NPL; ++i)
         if (i == slot) {
           s_here = sv[i];
-          key[i] = 0;
+          taken |= 1u << i;
         }
     }
     const float s_win = __shfl_sync(0xffffffffu, s_here, owner);
-    sum += s_win;  // rank order
     if (lane == j) {
       my_e = e_win;
       my_s = s_win;
+      my_kf = kf_win;
+    }
+    if (j == k - 1) a_k = kf_win;
+  }
+
+  const float eta = 0.25f * src.margin + 1e-6f;
+  if (k < E && a_k - a_k1 < 2.0f * eta) {
+    const float hi = a_k + 2.0f * eta, lo = a_k1 - 2.0f * eta;
+    const int n_cert = __popc(__ballot_sync(0xffffffffu, lane < k && my_kf > hi));  // ranks 0..n_cert-1
+    double ex[NPL];
+#pragma unroll
+    for (int i = 0; i < NPL; ++i) {
+      ex[i] = -INFINITY;
+      const int e = lane + 32 * i;
+      uint32_t m = __ballot_sync(0xffffffffu, e < E && kf[i] >= lo && kf[i] <= hi);
+      while (m) {
+        const int src_lane = __ffs(m) - 1;
+        m &= m - 1;
+        const int ce = src_lane + 32 * i;
+        const double l = exact_logit(src, t, ce, lane);
+        if (lane == src_lane) {
+          const double s64 = 1.0 / (1.0 + exp(-l));
+          ex[i] = s64 + (bias ? (double)bias[ce] : 0.0);
+          sv[i] = (float)s64;
+        }
+      }
+    }
+    for (int q = n_cert; q < k; ++q) {
+      double bv = -INFINITY;
+      int be = 0x7FFFFFFF;
+#pragma unroll
+      for (int i = 0; i < NPL; ++i) {
+        const int e = lane + 32 * i;
+        if (ex[i] > bv || (ex[i] == bv && ex[i] != -INFINITY && e < be)) {
+          bv = ex[i];
+          be = e;
+        }
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        const double ov = __shfl_xor_sync(0xffffffffu, bv, off);
+        const int oe = __shfl_xor_sync(0xffffffffu, be, off);
+        if (ov > bv || (ov == bv && oe < be)) {
+          bv = ov;
+          be = oe;
+        }
+      }
+      const int owner = be & 31, slot = be >> 5;
+      float s_here = 0.f;
+      if (lane == owner) {
+#pragma unroll
+        for (int i = 0; i < NPL; ++i)
+          if (i == slot) {
+            s_here = sv[i];
+            ex[i] = -INFINITY;
+          }
+      }
+      const float s_win = __shfl_sync(0xffffffffu, s_here, owner);
+      if (lane == q) {
+        my_e = be;
+        my_s = s_win;
+      }
     }
   }
+  float sum = 0.f;
+  for (int j = 0; j < k; ++j) sum += __shfl_sync(0xffffffffu, my_s, j);  // rank order
   if (lane < k) {
-    idx[(size_t)warp * k + lane] = my_e;
-    p[(size_t)warp * k + lane] = my_s / sum;
+    idx[(size_t)t * k + lane] = my_e;
+    p[(size_t)t * k + lane] = my_s / sum;
+  }
+}
+
+__global__ void split_bf16x3_kernel(const float* __restrict__ w, int64_t n, __nv_bfloat16* __restrict__ out) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    const float v = w[i];
+    const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+    const float r1 = v - __bfloat162float(hi);  // exact in fp32
+    const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+    const float r2 = r1 - __bfloat162float(mid);
+    out[i] = hi;
+    out[n + i] = mid;
+    out[2 * n + i] = __float2bfloat16_rn(r2);
   }
 }
 
@@ -220,18 +400,59 @@ cudaError_t launch_router_logits(const void* x, int x_dtype, const void* w_route
   return launch_simt_gemm(g, s);
 }
 
-cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, int k, int32_t* idx, float* p,
-                        cudaStream_t s) {
+cudaError_t launch_router(const void* x, int act, const void* w_router, int router_w, float* logits,
+                          void* wr_split, int T, int E, int d, uint32_t* status, uint64_t timeout_ns, int num_sms,
+                          int* launches, cudaStream_t s) {
+  if (act != kBF16) {
+    if (launches) *launches += 1;
+    return launch_router_logits(x, act, w_router, router_w, logits, T, E, d, s);
+  }
+  const void* wr = w_router;
+  int terms = 1;
+  if (router_w == kF32) {
+    if (!wr_split) return cudaErrorInvalidValue;
+    cudaError_t e = launch_split_bf16x3(static_cast<const float*>(w_router), (int64_t)E * d, wr_split, s);
+    if (e != cudaSuccess) return e;
+    if (launches) *launches += 1;
+    wr = wr_split;
+    terms = 3;
+  }
+  TcGemm g = {};
+  g.epi = kEpiF32;
+  g.M = T;
+  g.N = E;
+  g.K = terms * d;
+  g.A = TcOperand{x, d, T, 1, d, (int64_t)T * d};
+  g.B0 = TcOperand{wr, d, E, terms, d, (int64_t)E * d};
+  g.k0_len = terms * d;
+  g.k0_per_group = d;
+  g.a_k_period = d;
+  g.C = logits;
+  g.ldc = E;
+  if (launches) *launches += 1;
+  return launch_tc_gemm(g, status, timeout_ns, 0, num_sms, s);
+}
+
+cudaError_t launch_split_bf16x3(const float* w, int64_t n, void* out, cudaStream_t s) {
+  const int threads = 256;
+  const int64_t blocks = (n + threads - 1) / threads;
+  split_bf16x3_kernel<<<(int)(blocks < 4096 ? blocks : 4096), threads, 0, s>>>(w, n,
+                                                                              static_cast<__nv_bfloat16*>(out));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_topk(const float* logits, const float* bias, const RouterSrc& src, int T, int E, int k,
+                        int32_t* idx, float* p, cudaStream_t s) {
   const int warps_per_block = 8;
   dim3 grid((T + warps_per_block - 1) / warps_per_block), block(32 * warps_per_block);
   const int npl = (E + 31) / 32;
-  if (npl <= 1) topk_kernel<1><<<grid, block, 0, s>>>(logits, bias, T, E, k, idx, p);
-  else if (npl <= 2) topk_kernel<2><<<grid, block, 0, s>>>(logits, bias, T, E, k, idx, p);
-  else if (npl <= 4) topk_kernel<4><<<grid, block, 0, s>>>(logits, bias, T, E, k, idx, p);
-  else if (npl <= 8) topk_kernel<8><<<grid, block, 0, s>>>(logits, bias, T, E, k, idx, p);
-  else if (npl <= 16) topk_kernel<16><<<grid, block, 0, s>>>(logits, bias, T, E, k, idx, p);
-  else if (npl <= 28) topk_kernel<28><<<grid, block, 0, s>>>(logits, bias, T, E, k, idx, p);
-  else topk_kernel<32><<<grid, block, 0, s>>>(logits, bias, T, E, k, idx, p);
+  if (npl <= 1) topk_kernel<1><<<grid, block, 0, s>>>(logits, bias, src, T, E, k, idx, p);
+  else if (npl <= 2) topk_kernel<2><<<grid, block, 0, s>>>(logits, bias, src, T, E, k, idx, p);
+  else if (npl <= 4) topk_kernel<4><<<grid, block, 0, s>>>(logits, bias, src, T, E, k, idx, p);
+  else if (npl <= 8) topk_kernel<8><<<grid, block, 0, s>>>(logits, bias, src, T, E, k, idx, p);
+  else if (npl <= 16) topk_kernel<16><<<grid, block, 0, s>>>(logits, bias, src, T, E, k, idx, p);
+  else if (npl <= 28) topk_kernel<28><<<grid, block, 0, s>>>(logits, bias, src, T, E, k, idx, p);
+  else topk_kernel<32><<<grid, block, 0, s>>>(logits, bias, src, T, E, k, idx, p);
   return cudaGetLastError();
 }
 

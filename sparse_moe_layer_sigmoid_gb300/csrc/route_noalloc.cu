@@ -35,10 +35,10 @@ void* g_scratch_addr[kMaxDevices] = {};
 size_t round256(size_t v) { return (v + 255) / 256 * 256; }
 
 struct ScratchLayout {
-  size_t logits, chunk_counts, chunk_base, tiles, num_tiles, total;
+  size_t logits, chunk_counts, chunk_base, tiles, num_tiles, wr_split, total;
 };
 
-ScratchLayout scratch_layout(int T, int E, int k) {
+ScratchLayout scratch_layout(int T, int E, int k, size_t wr_split_bytes) {
   const size_t nchunks = ((size_t)T + lmoe::kDispatchChunk - 1) / lmoe::kDispatchChunk;
   const size_t max_tiles = (size_t)T * k / lmoe::kTileM + E + 1;
   ScratchLayout s;
@@ -47,7 +47,8 @@ ScratchLayout scratch_layout(int T, int E, int k) {
   s.chunk_base = s.chunk_counts + round256(nchunks * E * sizeof(int32_t));
   s.tiles = s.chunk_base + round256(nchunks * E * sizeof(int32_t));
   s.num_tiles = s.tiles + round256(max_tiles * sizeof(int4));
-  s.total = s.num_tiles + 256;
+  s.wr_split = s.num_tiles + 256;
+  s.total = s.wr_split + round256(wr_split_bytes);
   return s;
 }
 
@@ -78,6 +79,7 @@ extern "C" lmoe_status latentmoe_route_noalloc(const lmoe_config* cfg, const voi
   if (!cfg || !w) return LMOE_ERR_INVALID_ARG;
   const int E = cfg->num_experts, k = cfg->top_k, d = cfg->d;
   if (E < 1 || E > 1024 || k < 1 || k > E || k > 32 || d <= 0 || d % 16) return LMOE_ERR_INVALID_ARG;
+  if (cfg->act == LMOE_BF16 && (d % 64 || E % 4)) return LMOE_ERR_INVALID_ARG;  // tensor-core router tiles
   if ((cfg->act != LMOE_F32 && cfg->act != LMOE_BF16) || (cfg->router_w != LMOE_F32 && cfg->router_w != LMOE_BF16))
     return LMOE_ERR_INVALID_ARG;
   if (T < 0) return LMOE_ERR_INVALID_ARG;
@@ -85,7 +87,9 @@ extern "C" lmoe_status latentmoe_route_noalloc(const lmoe_config* cfg, const voi
                 !expert_offsets || !tok_of_row || !row_of))
     return LMOE_ERR_INVALID_ARG;
   if (w->router_bias && !aligned16(w->router_bias)) return LMOE_ERR_INVALID_ARG;
-  const ScratchLayout L = scratch_layout(T, E, k);
+  // bf16 activations with an fp32 W_r contract three bf16 terms of W_r (3*E*d*2 bytes)
+  const size_t wr_split_bytes = (cfg->act == LMOE_BF16 && cfg->router_w == LMOE_F32) ? (size_t)3 * E * d * 2 : 0;
+  const ScratchLayout L = scratch_layout(T, E, k, wr_split_bytes);
   if (L.total > kScratchBytes) return LMOE_ERR_INVALID_ARG;  // beyond the fixed scratch
   if (T == 0) return LMOE_OK;
 
@@ -103,9 +107,17 @@ extern "C" lmoe_status latentmoe_route_noalloc(const lmoe_config* cfg, const voi
   db.tok_of_row = tok_of_row;
   db.row_of = row_of;
   db.p_row = nullptr;
-  if (lmoe::launch_router_logits(x, cfg->act, w->w_router, cfg->router_w, logits, T, E, d, s) != cudaSuccess)
+  int dev = 0, num_sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return LMOE_ERR_CUDA;
-  if (lmoe::launch_topk(logits, w->router_bias, T, E, k, topk_idx, topk_p, s) != cudaSuccess) return LMOE_ERR_CUDA;
+  if (lmoe::launch_router(x, cfg->act, w->w_router, cfg->router_w, logits,
+                          wr_split_bytes ? base + L.wr_split : nullptr, T, E, d, nullptr, 4000000000ull, num_sms,
+                          nullptr, s) != cudaSuccess)
+    return LMOE_ERR_CUDA;
+  const lmoe::RouterSrc rs{x, cfg->act, w->w_router, cfg->router_w, d, lmoe::kRouterLogitMargin};
+  if (lmoe::launch_topk(logits, w->router_bias, rs, T, E, k, topk_idx, topk_p, s) != cudaSuccess)
+    return LMOE_ERR_CUDA;
   if (lmoe::launch_dispatch(topk_idx, topk_p, T, E, k, db, nullptr, nullptr, s) != cudaSuccess)
     return LMOE_ERR_CUDA;
   return LMOE_OK;

@@ -36,13 +36,22 @@ def assert_close(got, want, tol_rel, what=""):
 
 
 def compare_routing(idx_gpu: np.ndarray, ref: dict):
-    """Return (mismatched token mask, near-tie count); asserts mismatches are near ties only."""
-    mism = np.any(idx_gpu != ref["idx"], axis=1)
+    """Compare the selected sets T_k per token (eq. 13 defines a set; the GPU lists it in
+    descending key order, which may differ from the oracle's order only where keys are within
+    the router's refinement margin).  Returns (mismatched token mask, near-tie count); asserts
+    that every mismatch is a near tie."""
+    mism = np.any(np.sort(idx_gpu, axis=1) != np.sort(ref["idx"], axis=1), axis=1)
     near = ref["gap"] < NEAR_TIE
     bad = mism & ~near
     assert not bad.any(), f"routing differs on {int(bad.sum())} tokens with gap >= {NEAR_TIE}: " \
                           f"{np.nonzero(bad)[0][:10]}"
     return mism, int(near.sum())
+
+
+def p_by_expert(idx, p):
+    """p rearranged in ascending expert order per token (for order-free comparison)."""
+    order = np.argsort(idx, axis=1)
+    return np.take_along_axis(p, order, axis=1)
 
 
 def check_dispatch(out: dict, idx_gpu: np.ndarray, E: int):

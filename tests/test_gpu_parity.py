@@ -7,7 +7,7 @@ import torch
 
 import oracle
 from parity import (REL_FRO, assert_close, check_dispatch, compare_routing, device_inputs, oracle_for_rows,
-                    to_np)
+                    p_by_expert, to_np)
 from sparse_moe_layer_sigmoid_gb300 import configs, inputs
 
 pytestmark = pytest.mark.gpu
@@ -64,7 +64,21 @@ def _run_and_check(b, cfg, on_device=False, sample=None):
     mism, near = compare_routing(idx_gpu[rows], ref)
     counts = check_dispatch(r, idx_gpu, cfg.experts)
     ok = ~mism
-    assert np.allclose(p_gpu[rows][ok], ref["p"][ok], rtol=2e-6, atol=1e-7)
+    # p: fp32 from logits accurate to the router margin -> relative error well below 1e-4
+    assert np.allclose(p_by_expert(idx_gpu[rows][ok], p_gpu[rows][ok]), p_by_expert(ref["idx"][ok], ref["p"][ok]),
+                       rtol=1e-4, atol=1e-7)
+    # per-stage intermediates of the last forward, against the oracle on the same rows
+    logits = to_np(layer.debug_buffer("logits", torch.float32, (T, cfg.experts)))[rows]
+    want_l = oracle.router_logits(oracle.widen(host["x"][rows]), oracle.widen(host["w_router"]))
+    l_err = float(np.abs(logits - want_l).max())
+    assert l_err < 0.25e-3, f"router logit error {l_err:.3e} above a quarter of the refinement margin"
+    z = to_np(layer.debug_buffer("z", x.dtype, (T, cfg.latent)))[rows]
+    assert_close(z, ref["z"], REL_FRO[cfg.act], cfg.name + " z")
+    if not cfg.identity_experts:
+        kcat = cfg.n_shared * cfg.shared_hidden + cfg.latent
+        n_gpu = to_np(layer.debug_buffer("act_cat", x.dtype, (T, kcat)))[rows][:, kcat - cfg.latent:]
+        n_ok = ~mism
+        assert_close(n_gpu[n_ok], ref["n"][n_ok], REL_FRO[cfg.routed_w], cfg.name + " RMSNorm(u)")
     key = "u" if cfg.identity_experts else "y"
     want = ref[key].copy()
     if mism.any():  # near-tie tokens: compare against the oracle under the GPU's own choice
@@ -75,13 +89,14 @@ def _run_and_check(b, cfg, on_device=False, sample=None):
     got = to_np(y)[rows]
     rel, mx = assert_close(got, want, REL_FRO[cfg.routed_w if not cfg.identity_experts else cfg.act], cfg.name)
     layer.close()
-    return {"rel": rel, "max": mx, "near_ties": near, "counts": counts, "y": y, "inp": inp}
+    return {"rel": rel, "max": mx, "near_ties": near, "counts": counts, "y": y, "inp": inp, "logit_err": l_err}
 
 
 @pytest.mark.parametrize("cfg", SMALL_CASES, ids=lambda c: c.name)
 def test_small_layers_match_oracle(binding, cfg):
     res = _run_and_check(binding, cfg)
-    print(f"{cfg.name}: rel_fro={res['rel']:.3e} max/rms={res['max']:.3e} near_ties={res['near_ties']}")
+    print(f"{cfg.name}: rel_fro={res['rel']:.3e} max/rms={res['max']:.3e} near_ties={res['near_ties']} "
+          f"logit_err={res['logit_err']:.2e}")
 
 
 def test_k3w_e128_bf16_prefill_sampled_rows(binding):
@@ -89,7 +104,7 @@ def test_k3w_e128_bf16_prefill_sampled_rows(binding):
     res = _run_and_check(binding, cfg, on_device=True, sample=256)
     c = res["counts"]
     print(f"{cfg.name}: rel_fro={res['rel']:.3e} max/rms={res['max']:.3e} near_ties={res['near_ties']} "
-          f"load max/mean={c.max() / c.mean():.2f}")
+          f"load max/mean={c.max() / c.mean():.2f} logit_err={res['logit_err']:.2e}")
     del res
     _free()
 
@@ -98,7 +113,8 @@ def test_routing_dispatch_stress_sampled_rows(binding):
     cfg = configs.ROUTING_DISPATCH_STRESS
     res = _run_and_check(binding, cfg, on_device=True, sample=256)
     c = res["counts"]
-    print(f"{cfg.name}: rel_fro={res['rel']:.3e} near_ties={res['near_ties']} load max/mean={c.max() / c.mean():.2f}")
+    print(f"{cfg.name}: rel_fro={res['rel']:.3e} near_ties={res['near_ties']} load max/mean={c.max() / c.mean():.2f} "
+          f"logit_err={res['logit_err']:.2e}")
     assert c.sum() == cfg.tokens * cfg.top_k
     del res
     _free()
@@ -186,4 +202,23 @@ def test_forward_routed_with_oracle_routing(binding):
     y = layer.forward_routed(inp["x"], inp, idx, p)
     assert layer.status() == 0
     assert_close(to_np(y), ref["y"], REL_FRO["bf16"], "forward_routed")
+    layer.close()
+
+
+def test_bounded_wait_runs_out_and_reports_timeout(binding):
+    """A dropped pipeline-stage signal makes one consumer's bounded wait run out: the kernel
+    unwinds, the status word reports LMOE_ERR_TIMEOUT, and the next call is correct again."""
+    cfg = replace(SMALL_BF16, name="timeout", seed=35)
+    dev = torch.device("cuda")
+    inp = device_inputs(cfg, dev, False)
+    layer = binding.LatentMoE(cfg)
+    y_ref = layer.forward(inp["x"], inp).clone()
+    assert layer.status() == 0
+    layer.set_wait_limit(50_000_000, inject=True)  # 50 ms, drop one stage signal in the next forward
+    layer.forward(inp["x"], inp)
+    assert layer.status() == binding.LMOE_ERR_TIMEOUT
+    layer.set_wait_limit(4_000_000_000, inject=False)
+    y = layer.forward(inp["x"], inp)
+    assert layer.status() == 0
+    assert torch.equal(y, y_ref)
     layer.close()
