@@ -76,20 +76,36 @@ def file_sha(rel):
 
 
 class ClockSampler:
-    """nvidia-smi clock/throttle sampling in the background during the timed region."""
+    """nvidia-smi clock/throttle sampling in the background; only samples time-stamped inside
+    the timed region (mark_start/mark_stop) are kept."""
 
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
-              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
-              "clocks_event_reasons.sw_power_cap")
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, gpu_id):
         self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.t0 = self.t1 = None
         try:
             self.p = subprocess.Popen(["nvidia-smi", "-i", str(gpu_id), f"--query-gpu={self.FIELDS}",
-                                       "--format=csv,noheader,nounits", "-lms", "200"],
+                                       "--format=csv,noheader,nounits", "-lms", "50"],
                                       stdout=self.out, stderr=subprocess.DEVNULL)
         except (OSError, ValueError):
             self.p = None
+
+    def wait_first_sample(self, timeout=10.0):
+        t = time.time()
+        while self.p is not None and time.time() - t < timeout:
+            if os.path.getsize(self.out.name) > 0:
+                return
+            time.sleep(0.05)
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_stop(self):
+        self.t1 = time.time()
+        time.sleep(0.2)  # let the sampler flush the samples of the last interval
 
     def stop(self):
         if self.p is None:
@@ -101,25 +117,28 @@ class ClockSampler:
             self.p.kill()
         self.out.flush()
         self.out.seek(0)
+        import datetime
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in self.out.read().splitlines():
             parts = [s.strip() for s in line.split(",")]
-            if len(parts) < 8:
+            if len(parts) < 9:
                 continue
             try:
-                sm.append(float(parts[0]))
-                mx.append(float(parts[1]))
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                if self.t0 is not None and not (self.t0 - 0.05 <= ts <= self.t1 + 0.05):
+                    continue
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
             except ValueError:
                 continue
-            for n, v in zip(names, parts[4:8]):
+            for n, v in zip(names, parts[5:9]):
                 if v.lower().startswith("active"):
                     reasons.add(n)
         os.unlink(self.out.name)
         if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        under_load = [s for s in sm if s > 0.5 * max(sm)] or sm
-        return {"sm_mhz": statistics.median(under_load), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples in the timed region"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
                 "samples": len(sm)}
 
 
@@ -192,7 +211,7 @@ def workload_config(cfg, args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default="k3w_e128_bf16_prefill")
@@ -237,6 +256,9 @@ def main():
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
+    props = torch.cuda.get_device_properties(dev)
+    gpu_id = f"GPU-{props.uuid}" if getattr(props, "uuid", None) else local
+    clocks = ClockSampler(gpu_id) if rank == 0 else None
     for _ in range(args.warmup):
         flush.zero_()
         layer.forward(x, inp, y)
@@ -244,16 +266,27 @@ def main():
     st = layer.status()
     if st != 0:
         raise RuntimeError(f"layer reported status {st} during warm-up")
+    if clocks:
+        clocks.wait_first_sample()
 
-    props = torch.cuda.get_device_properties(dev)
-    gpu_id = f"GPU-{props.uuid}" if getattr(props, "uuid", None) else local
-    clocks = ClockSampler(gpu_id) if rank == 0 else None
+    # grouped-GEMM M-tile utilisation of this routing (rows / (128-row tiles * 128))
+    r = layer.route(x, inp)
+    counts = (r["offsets"][1:] - r["offsets"][:-1]).cpu()
+    m_tiles = int(((counts + 127) // 128).sum())
+    route_stats = {"rows": int(counts.sum()), "m_tiles_128": m_tiles,
+                   "m_tile_utilization": float(counts.sum()) / max(1, 128 * m_tiles),
+                   "experts_touched": int((counts > 0).sum()),
+                   "load_max_over_mean": float(counts.max()) / max(1e-9, float(counts.float().mean()))}
+    del r
+
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
     step_ms, stages, launches = [], {}, 0
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
+    if clocks:
+        clocks.mark_start()
     for _ in range(args.steps):
         flush.zero_()
         ev0.record(stream)
@@ -265,6 +298,8 @@ def main():
         for k_, v in layer.stage_times_ms().items():
             stages.setdefault(k_, []).append(v)
     torch.cuda.synchronize()
+    if clocks:
+        clocks.mark_stop()
     if dist:
         dist.barrier()
     clk = clocks.stop() if clocks else None
@@ -330,6 +365,7 @@ def main():
                     "h2d_bytes_per_step": cfg.tokens * cfg.d * elem,
                     "d2h_bytes_per_step": cfg.tokens * layer.out_width * elem},
             "gpu_launches": launches,
+            "routing": route_stats,
             "clocks": clk}
     if rank == 0 and world == 1 and args.cpu_sample > 0:
         layer.close()

@@ -71,7 +71,9 @@ typedef struct {
   int32_t max_tokens;    /* largest T any call will pass (sizes the workspace)          */
   int32_t act;           /* lmoe_dtype of x, y, W_down, W_up, shared experts: F32|BF16 */
   int32_t router_w;      /* lmoe_dtype of W_r: F32|BF16                                 */
-  int32_t routed_w;      /* lmoe_dtype of routed experts: F32|BF16|MXFP4                */
+  int32_t routed_w;      /* lmoe_dtype of routed experts: F32|BF16|MXFP4 (MXFP4 needs bf16
+                            act, l and h multiples of 512, E8M0 scale exponents in
+                            [-24, 13]; others set LMOE_ERR_DEVICE_CHECK)                 */
   float rms_eps;         /* RMSNorm epsilon                                             */
   uint32_t flags;        /* LMOE_FLAG_*                                                 */
 } lmoe_config;
@@ -169,7 +171,8 @@ const char *latentmoe_stage_name(int32_t i);
  * handle's workspace, by name: "logits" [T][E] fp32, "z" [T][l], "gathered" [T*k][l] (the
  * expert-contiguous rows; after a full forward it holds the p-scaled expert outputs), "act"
  * [T*k][h] (routed GLU activations), "act_cat" [T][N_s*h_s + l] (shared activations and
- * RMSNorm(u)), "p_row" [T*k] fp32.  Activations use the act dtype; T is the last call's T.
+ * RMSNorm(u)), "p_row" [T*k] fp32.  Activations use the act dtype, except that "z",
+ * "gathered" and "act" are fp16 when routed_w is MXFP4; T is the last call's T.
  * The pointers stay valid until latentmoe_destroy.  Unknown name or absent buffer:
  * LMOE_ERR_INVALID_ARG. */
 lmoe_status latentmoe_debug_buffer(const lmoe_handle *h, const char *name, void **ptr, size_t *bytes);

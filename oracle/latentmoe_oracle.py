@@ -83,7 +83,10 @@ def mxfp4_decode(packed, scales) -> np.ndarray:
     nib[..., 0::2] = packed & 0x0F
     nib[..., 1::2] = packed >> 4
     assert scales.shape[-1] * 32 == K
-    return e2m1_value(nib) * np.repeat(e8m0_value(scales), 32, axis=-1)
+    # the 16 code values from the bit-field definition, then looked up per element
+    values = e2m1_value(np.arange(16))[nib]
+    values *= np.repeat(e8m0_value(scales), 32, axis=-1)
+    return values
 
 
 def weight_values(w, scale=None) -> np.ndarray:

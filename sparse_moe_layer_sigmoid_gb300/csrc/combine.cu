@@ -5,6 +5,8 @@
 // One CTA per token.  The k expert rows of the token are summed in rank order j = 0..k-1 in
 // fp32 registers (the same order on every run), then sum(u^2) is reduced in a fixed tree and
 // n = u * g / sqrt(mean(u^2) + eps) is written.  HBM-bound: it reads k rows per token once.
+#include <cuda_fp16.h>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -27,6 +29,15 @@ __device__ __forceinline__ void unpack(const uint4& v, float (&f)[8], __nv_bfloa
     f[2 * i + 1] = t.y;
   }
 }
+__device__ __forceinline__ void unpack(const uint4& v, float (&f)[8], __half) {
+  const __half2* h = reinterpret_cast<const __half2*>(&v);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 t = __half22float2(h[i]);
+    f[2 * i] = t.x;
+    f[2 * i + 1] = t.y;
+  }
+}
 __device__ __forceinline__ void unpack(const uint4& v, float (&f)[8], float) {
   f[0] = __uint_as_float(v.x);
   f[1] = __uint_as_float(v.y);
@@ -45,11 +56,12 @@ __device__ __forceinline__ uint4 pack(const float (&f)[8], float) {
   return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]), __float_as_uint(f[3]));
 }
 
-template <typename T, int VPT>
+template <typename T, typename TO, int VPT>
 __global__ void __launch_bounds__(kThreads) combine_kernel(const T* __restrict__ o, const int32_t* __restrict__ row_of,
                                                            const float* __restrict__ p,
                                                            const float* __restrict__ gain, float eps, int k,
-                                                           int width, T* __restrict__ out, int64_t ld_out) {
+                                                           int width, TO* __restrict__ out, int64_t ld_out) {
+  static_assert(Vec<T>::N == Vec<TO>::N, "input and output vectors must hold the same element count");
   constexpr int EPV = Vec<T>::N;
   const int t = blockIdx.x;
   const int nvec = width / EPV;
@@ -102,25 +114,25 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const T* __restrict__
       float f[8];
 #pragma unroll
       for (int e = 0; e < EPV; ++e) f[e] = gain ? acc[i][e] * __ldg(gain + v * EPV + e) * scale : acc[i][e];
-      dst[v] = pack(f, T());
+      dst[v] = pack(f, TO());
     }
   }
 }
 
-template <typename T>
+template <typename T, typename TO>
 cudaError_t launch_typed(const void* o, const int32_t* row_of, const float* p, const float* gain, float eps, int T_,
                          int k, int width, void* out, int64_t ld_out, cudaStream_t s) {
   const int nvec = width / Vec<T>::N;
   const T* op = static_cast<const T*>(o);
-  T* dp = static_cast<T*>(out);
+  TO* dp = static_cast<TO*>(out);
   if (nvec <= kThreads)
-    combine_kernel<T, 1><<<T_, kThreads, 0, s>>>(op, row_of, p, gain, eps, k, width, dp, ld_out);
+    combine_kernel<T, TO, 1><<<T_, kThreads, 0, s>>>(op, row_of, p, gain, eps, k, width, dp, ld_out);
   else if (nvec <= 2 * kThreads)
-    combine_kernel<T, 2><<<T_, kThreads, 0, s>>>(op, row_of, p, gain, eps, k, width, dp, ld_out);
+    combine_kernel<T, TO, 2><<<T_, kThreads, 0, s>>>(op, row_of, p, gain, eps, k, width, dp, ld_out);
   else if (nvec <= 4 * kThreads)
-    combine_kernel<T, 4><<<T_, kThreads, 0, s>>>(op, row_of, p, gain, eps, k, width, dp, ld_out);
+    combine_kernel<T, TO, 4><<<T_, kThreads, 0, s>>>(op, row_of, p, gain, eps, k, width, dp, ld_out);
   else if (nvec <= 8 * kThreads)
-    combine_kernel<T, 8><<<T_, kThreads, 0, s>>>(op, row_of, p, gain, eps, k, width, dp, ld_out);
+    combine_kernel<T, TO, 8><<<T_, kThreads, 0, s>>>(op, row_of, p, gain, eps, k, width, dp, ld_out);
   else
     return cudaErrorInvalidValue;
   return cudaGetLastError();
@@ -128,11 +140,17 @@ cudaError_t launch_typed(const void* o, const int32_t* row_of, const float* p, c
 
 }  // namespace
 
-cudaError_t launch_combine(const void* o, int dtype, const int32_t* row_of, const float* p, const float* gain,
-                           float eps, int T, int k, int width, void* out, int64_t ld_out, cudaStream_t s) {
+cudaError_t launch_combine(const void* o, int in_dtype, int out_dtype, const int32_t* row_of, const float* p,
+                           const float* gain, float eps, int T, int k, int width, void* out, int64_t ld_out,
+                           cudaStream_t s) {
   if (T == 0) return cudaSuccess;
-  if (dtype == kF32) return launch_typed<float>(o, row_of, p, gain, eps, T, k, width, out, ld_out, s);
-  return launch_typed<__nv_bfloat16>(o, row_of, p, gain, eps, T, k, width, out, ld_out, s);
+  if (in_dtype == kF32 && out_dtype == kF32)
+    return launch_typed<float, float>(o, row_of, p, gain, eps, T, k, width, out, ld_out, s);
+  if (in_dtype == kBF16 && out_dtype == kBF16)
+    return launch_typed<__nv_bfloat16, __nv_bfloat16>(o, row_of, p, gain, eps, T, k, width, out, ld_out, s);
+  if (in_dtype == kF16 && out_dtype == kBF16)
+    return launch_typed<__half, __nv_bfloat16>(o, row_of, p, gain, eps, T, k, width, out, ld_out, s);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace lmoe

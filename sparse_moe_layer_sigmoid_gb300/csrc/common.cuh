@@ -11,7 +11,7 @@ namespace lmoe {
 // LMOE_ERR_TIMEOUT / LMOE_ERR_DEVICE_CHECK.
 enum : uint32_t { kStatusTimeout = 1u, kStatusDeviceCheck = 2u };
 
-enum DType : int { kF32 = 0, kBF16 = 1, kMXFP4 = 2 };
+enum DType : int { kF32 = 0, kBF16 = 1, kMXFP4 = 2, kF16 = 3 /* internal: fp16 activations */ };
 
 // Rows of one grouped-GEMM M tile; the dispatch step builds its tile list in these units.
 constexpr int kTileM = 128;

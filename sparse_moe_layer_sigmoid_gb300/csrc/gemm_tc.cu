@@ -1,18 +1,27 @@
-// Persistent bf16 GEMM on the 5th-generation tensor cores (tcgen05 + TMEM, operands staged by
-// TMA) for every dense contraction of the layer: W_down, the routed experts' gate/up and down
-// projections (grouped by expert), the shared experts' gate/up, and the final GEMM that
-// concatenates the shared experts' down projections with W_up along K (page "Lesson 6 -
-// LatentMoE", kimi-k3-course.pages.dev, eq. 11; section "Deriving the headline number" for
+// Persistent GEMM on the 5th-generation tensor cores (tcgen05 + TMEM, operands staged by TMA)
+// for every dense contraction of the layer: the router logits, W_down, the routed experts'
+// gate/up and down projections (grouped by expert), the shared experts' gate/up, and the final
+// GEMM that concatenates the shared experts' down projections with W_up along K (page "Lesson 6
+// - LatentMoE", kimi-k3-course.pages.dev, eq. 11; section "Deriving the headline number" for
 // the gate/up/down structure of an expert).
 //
-//   C[r][n] = epilogue( sum_c A[r][c] * B[n][c] ),  A, B bf16 K-major, fp32 accumulation.
+//   C[r][n] = epilogue( sum_c A[r][c] * B[n][c] ),  A, B K-major 16-bit, fp32 accumulation.
 //
-// CTA = 6 warps: warp 0 issues TMA loads (one thread), warp 1 owns TMEM and issues the MMAs
-// (one thread), warps 2..5 drain the accumulator (tcgen05.ld) and run the epilogue.  Tiles are
-// 128 x BN x 64 (BN = 256 or 128) with a 4..6-stage shared-memory ring and two TMEM
-// accumulators, so the epilogue of one tile overlaps the main loop of the next.  Every wait is
-// bounded: on timeout the CTA flags the device status word and unwinds (no trap, no hang).
+// CTA roles: warp 0 issues TMA loads (one thread), warp 1 owns TMEM and issues the MMAs (one
+// thread), warps 2..5 drain the accumulator (tcgen05.ld) and run the epilogue.  Tiles are
+// 128 x 256 x 64 with a multi-stage shared-memory ring and two TMEM accumulators, so the
+// epilogue of one tile overlaps the main loop of the next.
+//
+// MXFP4 weights (B as E2M1 pairs + one E8M0 scale per 32 elements along K): TMA stages the
+// packed bytes, and 8 converter warps turn each 256 x 64 block into fp16 with the hardware
+// pair conversion (cvt.rn.f16x2.e2m1x2) times the block scale, writing the 128-byte-swizzled
+// K-major layout the MMA reads; the MMA then runs kind::f16 with fp16 activations.  Values are
+// exact: an E2M1 value times a power of two fits fp16 for scale exponents in [-24, 13].
+//
+// Every wait is bounded: on timeout the CTA flags the device status word and unwinds through
+// the normal teardown (no trap, no hang).
 #include <cuda.h>
+#include <cuda_fp16.h>
 
 #include <mutex>
 
@@ -24,18 +33,24 @@ namespace lmoe {
 namespace {
 
 constexpr int BM = 128, BK = 64;
-constexpr int kThreads = 192;
 constexpr int kBoxRows = 128;
-constexpr uint32_t kBoxBytes = kBoxRows * BK * 2;  // 16 KB: one 128-row x 64-col bf16 box
+constexpr uint32_t kBoxBytes = kBoxRows * BK * 2;  // 16 KB: one 128-row x 64-col 16-bit box
+constexpr int kBaseThreads = 192;                   // producer, MMA, 4 epilogue warps
 
-template <int BN>
+template <int BN, bool FP4B>
 struct Cfg {
-  static constexpr int kStages = BN == 256 ? 4 : 6;
-  static constexpr uint32_t kABytes = BM * BK * 2;
-  static constexpr uint32_t kBBytes = BN * BK * 2;
-  static constexpr uint32_t kStageBytes = kABytes + kBBytes;
-  static constexpr uint32_t kTmemCols = 2 * BN;  // two fp32 accumulators of BN columns
-  static constexpr size_t kSmem = (size_t)kStages * kStageBytes + 1024 + 256;
+  static constexpr int kS1 = FP4B ? 6 : 4;                       // TMA ring stages
+  static constexpr int kS2 = FP4B ? 2 : 0;                       // converted-B ring stages
+  static constexpr uint32_t kABytes = BM * BK * 2;               // 16 KB
+  static constexpr uint32_t kBBytes = BN * BK * 2;               // 32 KB (16-bit B tile)
+  static constexpr uint32_t kBRawBytes = BN * BK / 2;            // 8 KB (packed E2M1)
+  static constexpr uint32_t kStage1Bytes = kABytes + (FP4B ? kBRawBytes : kBBytes);
+  static constexpr uint32_t kRing1 = kS1 * kStage1Bytes;
+  static constexpr uint32_t kRing2 = kS2 * kBBytes;
+  static constexpr uint32_t kTmemCols = 2 * BN;                  // two fp32 accumulators
+  static constexpr int kConvWarps = FP4B ? BN / 32 : 0;          // one converter thread per B row
+  static constexpr int kThreads = kBaseThreads + 32 * kConvWarps;
+  static constexpr size_t kSmem = (size_t)kRing1 + kRing2 + 1024 + 512;
 };
 
 struct TcParams {
@@ -50,6 +65,8 @@ struct TcParams {
   void* C;
   int64_t ldc;
   const float* row_scale;
+  const uint8_t* b_scale;  // MXFP4 B: E8M0 [group][rows][K/32]
+  int b_rows;              // MXFP4 B: rows per group
   uint32_t* status;
   uint64_t timeout_ns;
   int inject;
@@ -81,21 +98,77 @@ __device__ __forceinline__ Tile decode_tile(const TcParams& p, int t) {
   return ti;
 }
 
-template <int BN, int EPI, bool GROUPED>
-__global__ void __launch_bounds__(kThreads, 1)
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// fp16 bits (duplicated into both halves) of 2^(s-127) for an E8M0 byte s; sets *bad when the
+// decoded block could leave the exact fp16 range (6 * scale above 65504) or s is NaN.
+__device__ __forceinline__ uint32_t e8m0_to_f16x2(uint32_t s, bool* bad) {
+  const int e = (int)s - 127;
+  uint32_t h;
+  if (s == 255u || e > 13) {
+    *bad = true;
+    h = 0;
+  } else if (e >= -14) {
+    h = (uint32_t)(e + 15) << 10;
+  } else if (e >= -24) {
+    h = 1u << (e + 24);  // subnormal
+  } else {
+    h = 0;
+  }
+  return h | (h << 16);
+}
+
+// 32 E2M1 values (16 bytes, element 2i in the low nibble of byte i) times a scale -> 16 f16x2.
+__device__ __forceinline__ void e2m1x32_to_f16(const uint4& q, uint32_t scale2, uint32_t (&o)[16]) {
+  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+  const __half2 sc = *reinterpret_cast<const __half2*>(&scale2);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint32_t r0, r1, r2, r3;
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+        "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+        : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+        : "r"(w[i]));
+    const uint32_t rr[4] = {r0, r1, r2, r3};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      __half2 v = __hmul2(*reinterpret_cast<const __half2*>(&rr[j]), sc);
+      o[4 * i + j] = *reinterpret_cast<uint32_t*>(&v);
+    }
+  }
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+template <int BN, int EPI, bool GROUPED, bool AB_F16, bool FP4B>
+__global__ void __launch_bounds__(Cfg<BN, FP4B>::kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                    const __grid_constant__ CUtensorMap tmB1, const TcParams p) {
-  using C = Cfg<BN>;
-  constexpr bool GLU = EPI == kEpiGluBF16;
+  using C = Cfg<BN, FP4B>;
+  constexpr bool GLU = EPI == kEpiGluBF16 || EPI == kEpiGluF16;
+  constexpr bool SCALE = EPI == kEpiScaleBF16 || EPI == kEpiScaleF16;
+  constexpr bool OUT_F16 = EPI == kEpiF16 || EPI == kEpiGluF16 || EPI == kEpiScaleF16;
   constexpr int BN_OUT = GLU ? BN / 2 : BN;
-  constexpr int S = C::kStages;
+  constexpr int S1 = C::kS1, S2 = C::kS2 > 0 ? C::kS2 : 1;
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = ptx::smem_addr(smem_raw);
   uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * C::kStageBytes);
-  uint64_t* empty = full + S;
-  uint64_t* tmem_full = empty + S;
+  uint8_t* ring2 = smem + C::kRing1;
+  uint64_t* full1 = reinterpret_cast<uint64_t*>(ring2 + C::kRing2);
+  uint64_t* empty1 = full1 + S1;
+  uint64_t* full2 = empty1 + S1;
+  uint64_t* empty2 = full2 + S2;
+  uint64_t* tmem_full = empty2 + S2;
   uint64_t* tmem_empty = tmem_full + 2;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(tmem_empty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
@@ -103,9 +176,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < S; ++s) {
-      ptx::mbar_init(&full[s], 1);
-      ptx::mbar_init(&empty[s], 1);
+    for (int s = 0; s < S1; ++s) {
+      ptx::mbar_init(&full1[s], 1);
+      ptx::mbar_init(&empty1[s], 1);
+    }
+    for (int s = 0; s < S2; ++s) {
+      ptx::mbar_init(&full2[s], C::kConvWarps > 0 ? C::kConvWarps : 1);
+      ptx::mbar_init(&empty2[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(&tmem_full[a], 1);
@@ -133,32 +210,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
       const Tile ti = decode_tile<BN_OUT, GROUPED>(p, t);
       for (int kb = 0; kb < p.num_kb; ++kb) {
-        if (!ptx::mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, p.status, p.timeout_ns)) goto done;
+        if (!ptx::mbar_wait_bounded(&empty1[stage], phase ^ 1u, abort_flag, p.status, p.timeout_ns)) goto done;
         const bool skip = p.inject && first && blockIdx.x == 0;  // test hook: drop one stage signal
         first = false;
         if (!skip) {
-          uint8_t* sA = smem + stage * C::kStageBytes;
+          uint8_t* sA = smem + stage * C::kStage1Bytes;
           uint8_t* sB = sA + C::kABytes;
-          ptx::mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
-          ptx::tma_load_3d(sA, &tmA, &full[stage], (kb % p.a_kb_period) * BK, ti.row0, 0);
+          constexpr uint32_t kBoxB = FP4B ? kBoxRows * BK / 2 : kBoxBytes;  // bytes of one B box
+          const int kx = FP4B ? kb * (BK / 2) : kb * BK;                     // B inner coordinate
+          ptx::mbar_arrive_expect_tx(&full1[stage], C::kStage1Bytes);
+          ptx::tma_load_3d(sA, &tmA, &full1[stage], (kb % p.a_kb_period) * BK, ti.row0, 0);
           if (GLU) {
             const int grp = ti.group + ti.n0 / p.glu_h, j0 = ti.n0 % p.glu_h;
-            ptx::tma_load_3d(sB, &tmB0, &full[stage], kb * BK, j0, grp);
-            ptx::tma_load_3d(sB + kBoxBytes, &tmB0, &full[stage], kb * BK, p.glu_h + j0, grp);
+            ptx::tma_load_3d(sB, &tmB0, &full1[stage], kx, j0, grp);
+            ptx::tma_load_3d(sB + kBoxB, &tmB0, &full1[stage], kx, p.glu_h + j0, grp);
           } else if (kb < p.kb0) {
-            const int goff = kb / p.kb0_per_group, kin = (kb - goff * p.kb0_per_group) * BK;
+            const int goff = kb / p.kb0_per_group;
+            const int kin = (kb - goff * p.kb0_per_group) * (FP4B ? BK / 2 : BK);
 #pragma unroll
             for (int h = 0; h < BN / kBoxRows; ++h)
-              ptx::tma_load_3d(sB + h * kBoxBytes, &tmB0, &full[stage], kin, ti.n0 + h * kBoxRows,
-                               ti.group + goff);
+              ptx::tma_load_3d(sB + h * kBoxB, &tmB0, &full1[stage], kin, ti.n0 + h * kBoxRows, ti.group + goff);
           } else {
             const int kin = (kb - p.kb0) * BK;
 #pragma unroll
             for (int h = 0; h < BN / kBoxRows; ++h)
-              ptx::tma_load_3d(sB + h * kBoxBytes, &tmB1, &full[stage], kin, ti.n0 + h * kBoxRows, 0);
+              ptx::tma_load_3d(sB + h * kBoxB, &tmB1, &full1[stage], kin, ti.n0 + h * kBoxRows, 0);
           }
         }
-        if (++stage == S) {
+        if (++stage == S1) {
           stage = 0;
           phase ^= 1u;
         }
@@ -166,9 +245,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1 && lane == 0) {
     // ------------------------------------------------------------------ MMA issuer
-    constexpr uint32_t idesc = ptx::idesc_bf16_f32(BM, BN);
-    int stage = 0;
-    uint32_t phase = 0;
+    constexpr uint32_t idesc = AB_F16 ? ptx::idesc_f16_f32(BM, BN) : ptx::idesc_bf16_f32(BM, BN);
+    int s1 = 0, s2 = 0;
+    uint32_t ph1 = 0, ph2 = 0;
     int it = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
       const int acc = it & 1;
@@ -178,23 +257,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::tc_fence_after();
       const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
       for (int kb = 0; kb < p.num_kb; ++kb) {
-        if (!ptx::mbar_wait_bounded(&full[stage], phase, abort_flag, p.status, p.timeout_ns)) goto done;
+        if (FP4B && !ptx::mbar_wait_bounded(&full2[s2], ph2, abort_flag, p.status, p.timeout_ns)) goto done;
+        if (!ptx::mbar_wait_bounded(&full1[s1], ph1, abort_flag, p.status, p.timeout_ns)) goto done;
         ptx::tc_fence_after();
-        const uint32_t a_addr = ptx::smem_addr(smem + stage * C::kStageBytes);
-        const uint32_t b_addr = a_addr + C::kABytes;
+        const uint32_t a_addr = ptx::smem_addr(smem + s1 * C::kStage1Bytes);
+        const uint32_t b_addr = FP4B ? ptx::smem_addr(ring2 + s2 * C::kBBytes) : a_addr + C::kABytes;
 #pragma unroll
         for (int kk = 0; kk < BK / 16; ++kk)
           ptx::mma_f16(d_tmem, ptx::sw128_kmajor_desc(a_addr + kk * 32), ptx::sw128_kmajor_desc(b_addr + kk * 32),
                        idesc, (kb | kk) != 0 ? 1u : 0u);
-        ptx::mma_commit(&empty[stage]);
-        if (++stage == S) {
-          stage = 0;
-          phase ^= 1u;
+        ptx::mma_commit(&empty1[s1]);
+        if (++s1 == S1) {
+          s1 = 0;
+          ph1 ^= 1u;
+        }
+        if (FP4B) {
+          ptx::mma_commit(&empty2[s2]);
+          if (++s2 == S2) {
+            s2 = 0;
+            ph2 ^= 1u;
+          }
         }
       }
       ptx::mma_commit(&tmem_full[acc]);
     }
-  } else if (warp >= 2) {
+  } else if (warp >= 2 && warp < 6) {
     // ------------------------------------------------------------------ epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     int it = 0;
@@ -211,7 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool live = row < ti.row_end;
       const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
       if (GLU) {
-        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.C) + (int64_t)row * p.ldc + ti.n0;
+        uint16_t* out = static_cast<uint16_t*>(p.C) + (int64_t)row * p.ldc + ti.n0;
 #pragma unroll 1
         for (int c = 0; c < BN_OUT; c += 32) {
           uint32_t g[32], u[32];
@@ -224,7 +311,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < 16; ++i) {
               const float a0 = silu(__uint_as_float(g[2 * i])) * __uint_as_float(u[2 * i]);
               const float a1 = silu(__uint_as_float(g[2 * i + 1])) * __uint_as_float(u[2 * i + 1]);
-              packed[i] = pack_bf16x2(a0, a1);
+              packed[i] = OUT_F16 ? pack_f16x2(a0, a1) : pack_bf16x2(a0, a1);
             }
             uint4* dst = reinterpret_cast<uint4*>(out + c);
 #pragma unroll
@@ -233,7 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       } else {
-        const float sc = (EPI == kEpiScaleBF16 && live) ? p.row_scale[row] : 1.0f;
+        const float sc = (SCALE && live) ? p.row_scale[row] : 1.0f;
 #pragma unroll 1
         for (int c = 0; c < BN; c += 32) {
           if (ti.n0 + c >= p.N) break;  // ragged last column tile (fp32: N % 4 == 0, else N % 32 == 0)
@@ -249,10 +336,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else {
               uint32_t packed[16];
 #pragma unroll
-              for (int i = 0; i < 16; ++i)
-                packed[i] = pack_bf16x2(__uint_as_float(r[2 * i]) * sc, __uint_as_float(r[2 * i + 1]) * sc);
-              uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.C) + (int64_t)row * p.ldc +
-                                                    ti.n0 + c);
+              for (int i = 0; i < 16; ++i) {
+                const float v0 = __uint_as_float(r[2 * i]) * sc, v1 = __uint_as_float(r[2 * i + 1]) * sc;
+                packed[i] = OUT_F16 ? pack_f16x2(v0, v1) : pack_bf16x2(v0, v1);
+              }
+              uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.C) + (int64_t)row * p.ldc + ti.n0 + c);
 #pragma unroll
               for (int i = 0; i < 4; ++i)
                 dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
@@ -264,6 +352,70 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&tmem_empty[acc]);
     }
+  } else if (FP4B && warp >= 6) {
+    // ------------------------------------------------------------------ E2M1 -> fp16 converters
+    const int r = threadIdx.x - kBaseThreads;  // B tile row handled by this thread
+    const int kscale = p.num_kb * 2;           // E8M0 bytes per B row (K / 32)
+    int s1 = 0, s2 = 0;
+    uint32_t ph1 = 0, ph2 = 0;
+    bool bad = false;
+    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+      const Tile ti = decode_tile<BN_OUT, GROUPED>(p, t);
+      int brow, bgrp;
+      if (GLU) {
+        bgrp = ti.group + ti.n0 / p.glu_h;
+        const int j0 = ti.n0 % p.glu_h;
+        brow = r < kBoxRows ? j0 + r : p.glu_h + j0 + (r - kBoxRows);
+      } else {
+        bgrp = ti.group;
+        brow = ti.n0 + r;
+      }
+      const uint4* srow = reinterpret_cast<const uint4*>(p.b_scale + ((int64_t)bgrp * p.b_rows + brow) * kscale);
+      uint4 sc16 = make_uint4(0, 0, 0, 0);
+      for (int kb = 0; kb < p.num_kb; ++kb) {
+        if ((kb & 7) == 0) sc16 = __ldg(srow + (kb >> 3));  // scales of 8 k-blocks (512 elements)
+        int ok = 1;
+        if (lane == 0) {
+          ok = ptx::mbar_wait_bounded(&full1[s1], ph1, abort_flag, p.status, p.timeout_ns) &&
+               ptx::mbar_wait_bounded(&empty2[s2], ph2 ^ 1u, abort_flag, p.status, p.timeout_ns);
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) goto conv_done;
+        {
+          const uint8_t* braw = smem + s1 * C::kStage1Bytes + C::kABytes + r * (BK / 2);
+          const uint4 q0 = *reinterpret_cast<const uint4*>(braw);
+          const uint4 q1 = *reinterpret_cast<const uint4*>(braw + 16);
+          const int wsel = (kb & 7) >> 1;
+          const uint32_t sw = wsel == 0 ? sc16.x : wsel == 1 ? sc16.y : wsel == 2 ? sc16.z : sc16.w;
+          const uint32_t sb0 = (sw >> ((kb & 1) * 16)) & 0xFFu, sb1 = (sw >> ((kb & 1) * 16 + 8)) & 0xFFu;
+          uint32_t o0[16], o1[16];
+          e2m1x32_to_f16(q0, e8m0_to_f16x2(sb0, &bad), o0);
+          e2m1x32_to_f16(q1, e8m0_to_f16x2(sb1, &bad), o1);
+          uint8_t* dst = ring2 + s2 * C::kBBytes + (r >> 3) * 1024 + (r & 7) * 128;
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            *reinterpret_cast<uint4*>(dst + ((c ^ (r & 7)) << 4)) =
+                make_uint4(o0[4 * c], o0[4 * c + 1], o0[4 * c + 2], o0[4 * c + 3]);
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            *reinterpret_cast<uint4*>(dst + (((c + 4) ^ (r & 7)) << 4)) =
+                make_uint4(o1[4 * c], o1[4 * c + 1], o1[4 * c + 2], o1[4 * c + 3]);
+        }
+        fence_proxy_async_smem();  // generic-proxy writes -> visible to the tensor cores
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&full2[s2]);
+        if (++s1 == S1) {
+          s1 = 0;
+          ph1 ^= 1u;
+        }
+        if (++s2 == S2) {
+          s2 = 0;
+          ph2 ^= 1u;
+        }
+      }
+    }
+  conv_done:
+    if (bad) report(p.status, kStatusDeviceCheck);
   }
 done:
   ptx::tc_fence_before();
@@ -293,6 +445,7 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
+// 16-bit operand [depth][rows][cols]: boxes of 64 cols x 128 rows, 128-byte swizzle.
 bool make_map(CUtensorMap* m, const TcOperand& op) {
   EncodeTiledFn enc = encode_fn();
   if (!enc || !op.ptr) return false;
@@ -306,17 +459,34 @@ bool make_map(CUtensorMap* m, const TcOperand& op) {
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BN, int EPI, bool GROUPED>
+// Packed E2M1 operand [depth][rows][cols/2 bytes] (element strides in `op`): boxes of 32
+// bytes (64 elements) x 128 rows, no swizzle.
+bool make_map_fp4(CUtensorMap* m, const TcOperand& op) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc || !op.ptr) return false;
+  const int64_t rb = op.row_stride / 2;  // bytes per row
+  const int64_t depth_stride = op.depth > 1 ? op.depth_stride / 2 : op.rows * rb;
+  cuuint64_t dims[3] = {(cuuint64_t)(op.cols / 2), (cuuint64_t)op.rows, (cuuint64_t)op.depth};
+  cuuint64_t strides[2] = {(cuuint64_t)rb, (cuuint64_t)depth_stride};
+  cuuint32_t box[3] = {BK / 2, kBoxRows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(op.ptr), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int BN, int EPI, bool GROUPED, bool AB_F16, bool FP4B>
 cudaError_t launch_inst(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1, const TcParams& p,
                         int grid, cudaStream_t s) {
-  auto kern = tc_gemm_kernel<BN, EPI, GROUPED>;
+  using C = Cfg<BN, FP4B>;
+  auto kern = tc_gemm_kernel<BN, EPI, GROUPED, AB_F16, FP4B>;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg<BN>::kSmem);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  kern<<<grid, kThreads, Cfg<BN>::kSmem, s>>>(a, b0, b1, p);
+  kern<<<grid, C::kThreads, C::kSmem, s>>>(a, b0, b1, p);
   return cudaGetLastError();
 }
 
@@ -324,17 +494,21 @@ cudaError_t launch_inst(const CUtensorMap& a, const CUtensorMap& b0, const CUten
 
 cudaError_t launch_tc_gemm(const TcGemm& g, uint32_t* status, uint64_t timeout_ns, int inject_fault, int num_sms,
                            cudaStream_t s) {
-  const bool glu = g.epi == kEpiGluBF16;
+  const bool glu = g.epi == kEpiGluBF16 || g.epi == kEpiGluF16;
   const bool grouped = g.tiles != nullptr;
+  const bool fp4 = g.b_scale != nullptr;
   const int bn = 256;
   const int bn_out = glu ? bn / 2 : bn;
   if (g.K % BK || g.k0_len % BK || g.k0_per_group % BK) return cudaErrorInvalidValue;
   if (glu ? g.N % bn_out : g.N % (g.epi == kEpiF32 ? 4 : 32)) return cudaErrorInvalidValue;
   const int a_period = g.a_k_period ? g.a_k_period : g.K;
   if (a_period % BK || g.K % a_period) return cudaErrorInvalidValue;
+  if (fp4 && (!g.ab_f16 || g.B1.ptr || g.K % 512 || g.k0_len != g.K || g.k0_per_group != g.K))
+    return cudaErrorInvalidValue;
   if (glu && g.glu_h % kBoxRows) return cudaErrorInvalidValue;
   CUtensorMap ma, mb0, mb1;
-  if (!make_map(&ma, g.A) || !make_map(&mb0, g.B0)) return cudaErrorInvalidValue;
+  if (!make_map(&ma, g.A)) return cudaErrorInvalidValue;
+  if (!(fp4 ? make_map_fp4(&mb0, g.B0) : make_map(&mb0, g.B0))) return cudaErrorInvalidValue;
   if (g.B1.ptr) {
     if (!make_map(&mb1, g.B1)) return cudaErrorInvalidValue;
   } else {
@@ -356,24 +530,37 @@ cudaError_t launch_tc_gemm(const TcGemm& g, uint32_t* status, uint64_t timeout_n
   p.C = g.C;
   p.ldc = g.ldc;
   p.row_scale = g.row_scale;
+  p.b_scale = g.b_scale;
+  p.b_rows = (int)g.B0.rows;
   p.status = status;
   p.timeout_ns = timeout_ns;
   p.inject = inject_fault;
   const long long tiles = grouped ? (long long)g.max_tiles * p.num_n_tiles : (long long)p.num_m_tiles * p.num_n_tiles;
   if (tiles == 0) return cudaSuccess;
   const int grid = (int)(tiles < num_sms ? tiles : num_sms);
+  if (fp4) {
+    if (!grouped) return cudaErrorInvalidValue;
+    switch (g.epi) {
+      case kEpiGluF16: return launch_inst<256, kEpiGluF16, true, true, true>(ma, mb0, mb1, p, grid, s);
+      case kEpiScaleF16: return launch_inst<256, kEpiScaleF16, true, true, true>(ma, mb0, mb1, p, grid, s);
+    }
+    return cudaErrorInvalidValue;
+  }
+  if (g.ab_f16) return cudaErrorInvalidValue;  // fp16 operands only come with converted MXFP4 weights
   switch (g.epi) {
     case kEpiBF16:
-      return grouped ? launch_inst<256, kEpiBF16, true>(ma, mb0, mb1, p, grid, s)
-                     : launch_inst<256, kEpiBF16, false>(ma, mb0, mb1, p, grid, s);
+      return grouped ? launch_inst<256, kEpiBF16, true, false, false>(ma, mb0, mb1, p, grid, s)
+                     : launch_inst<256, kEpiBF16, false, false, false>(ma, mb0, mb1, p, grid, s);
+    case kEpiF16:
+      return grouped ? cudaErrorInvalidValue : launch_inst<256, kEpiF16, false, false, false>(ma, mb0, mb1, p, grid, s);
     case kEpiGluBF16:
-      return grouped ? launch_inst<256, kEpiGluBF16, true>(ma, mb0, mb1, p, grid, s)
-                     : launch_inst<256, kEpiGluBF16, false>(ma, mb0, mb1, p, grid, s);
+      return grouped ? launch_inst<256, kEpiGluBF16, true, false, false>(ma, mb0, mb1, p, grid, s)
+                     : launch_inst<256, kEpiGluBF16, false, false, false>(ma, mb0, mb1, p, grid, s);
     case kEpiScaleBF16:
-      return grouped ? launch_inst<256, kEpiScaleBF16, true>(ma, mb0, mb1, p, grid, s)
-                     : launch_inst<256, kEpiScaleBF16, false>(ma, mb0, mb1, p, grid, s);
+      return grouped ? launch_inst<256, kEpiScaleBF16, true, false, false>(ma, mb0, mb1, p, grid, s)
+                     : cudaErrorInvalidValue;
     case kEpiF32:
-      return launch_inst<256, kEpiF32, false>(ma, mb0, mb1, p, grid, s);
+      return launch_inst<256, kEpiF32, false, false, false>(ma, mb0, mb1, p, grid, s);
   }
   return cudaErrorInvalidValue;
 }

@@ -56,8 +56,10 @@ cudaError_t launch_scatter_rows(const void* src, void* dst, const int32_t* row_o
 // ---------------------------------------------------------------- combine (combine.cu)
 // u_t = sum_j o[row_of[t][j]] (rank order, fp32) [times p[t][j] when p != nullptr];
 // with gain != nullptr writes n_t = u_t * g / sqrt(mean(u_t^2) + eps), else u_t.
-cudaError_t launch_combine(const void* o, int dtype, const int32_t* row_of, const float* p, const float* gain,
-                           float eps, int T, int k, int width, void* out, int64_t ld_out, cudaStream_t s);
+// in_dtype: kF32, kBF16 or kF16 (expert rows); out_dtype: kF32 or kBF16.
+cudaError_t launch_combine(const void* o, int in_dtype, int out_dtype, const int32_t* row_of, const float* p,
+                           const float* gain, float eps, int T, int k, int width, void* out, int64_t ld_out,
+                           cudaStream_t s);
 
 // ---------------------------------------------------------------- fp32 CUDA-core GEMM (simt.cu)
 struct SimtSegment {
@@ -80,8 +82,16 @@ struct SimtGemm {
 cudaError_t launch_simt_gemm(const SimtGemm& g, cudaStream_t s);
 
 // ---------------------------------------------------------------- tcgen05 GEMM (gemm_tc.cu)
-enum TcEpilogue : int { kEpiF32 = 0, kEpiBF16 = 1, kEpiGluBF16 = 2, kEpiScaleBF16 = 3 };
-struct TcOperand {        // a bf16 tensor viewed as [depth][rows][cols], cols = K contiguous
+enum TcEpilogue : int {
+  kEpiF32 = 0,        // fp32 store (router logits)
+  kEpiBF16 = 1,       // bf16 store
+  kEpiGluBF16 = 2,    // SiLU(gate) * up, bf16
+  kEpiScaleBF16 = 3,  // row_scale[r] * acc, bf16
+  kEpiF16 = 4,        // fp16 variants of the above
+  kEpiGluF16 = 5,
+  kEpiScaleF16 = 6
+};
+struct TcOperand {        // a 16-bit (or packed E2M1) tensor viewed as [depth][rows][cols], cols = K contiguous
   const void* ptr;
   int64_t cols, rows, depth;
   int64_t row_stride;     // elements
@@ -99,6 +109,8 @@ struct TcGemm {
   const int4* tiles; const int32_t* num_tiles; const int32_t* offsets; int max_tiles;  // grouped mode
   void* C; int64_t ldc;
   const float* row_scale;
+  int ab_f16;                // operands are fp16 (with MXFP4 B) instead of bf16
+  const uint8_t* b_scale;    // non-null: B0 holds packed E2M1 bytes, b_scale E8M0 [depth][rows][K/32]
 };
 cudaError_t launch_tc_gemm(const TcGemm& g, uint32_t* status, uint64_t timeout_ns, int inject_fault, int num_sms,
                            cudaStream_t s);

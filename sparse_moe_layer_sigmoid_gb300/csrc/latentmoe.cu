@@ -108,9 +108,11 @@ lmoe_status validate_config(const lmoe_config& c) {
     // tensor-core tiles: K steps of 64, output tiles of 256 columns (128 for GLU halves)
     if (c.d % 256 || c.latent % 256 || c.latent > 8192 || c.num_experts % 4) return LMOE_ERR_UNSUPPORTED;
     if (!identity) {
-      if (c.routed_w != LMOE_BF16) return LMOE_ERR_UNSUPPORTED;
+      if (c.routed_w == LMOE_F32) return LMOE_ERR_UNSUPPORTED;
       if (c.hidden % 128) return LMOE_ERR_UNSUPPORTED;
       if (c.num_shared > 0 && c.shared_hidden % 128) return LMOE_ERR_UNSUPPORTED;
+      // MXFP4 experts: the converters read E8M0 scales 16 bytes (512 elements) at a time
+      if (c.routed_w == LMOE_MXFP4 && (c.latent % 512 || c.hidden % 512)) return LMOE_ERR_UNSUPPORTED;
     }
   }
   return LMOE_OK;
@@ -170,8 +172,17 @@ bool weights_ok(const lmoe_handle* h, const lmoe_weights* w, bool need_router) {
     if (!w->shared_gate_up || !w->shared_down || !aligned16(w->shared_gate_up) || !aligned16(w->shared_down))
       return false;
   }
+  if (c.routed_w == LMOE_MXFP4) {
+    if (!w->routed_gate_up_scale || !w->routed_down_scale || !aligned16(w->routed_gate_up_scale) ||
+        !aligned16(w->routed_down_scale))
+      return false;
+  }
   return true;
 }
+
+// Storage type of the routed-expert activations (z, gathered rows, GLU outputs, expert outputs):
+// fp16 next to MXFP4 weights (the converted weights are fp16), else the activation type.
+int routed_act_dtype(const lmoe_config& c) { return c.routed_w == LMOE_MXFP4 ? kF16 : c.act; }
 
 TcOperand op2d(const void* ptr, int64_t rows, int64_t cols) {
   return TcOperand{ptr, cols, rows, 1, cols, rows * cols};
@@ -227,9 +238,10 @@ lmoe_status run_forward(lmoe_handle* h, const void* x, int T, const lmoe_weights
   stage_begin(h, kStWDown, s);
 
   // z = W_down x
+  const int rt = routed_act_dtype(c);
   if (tc) {
     TcGemm g = {};
-    g.epi = kEpiBF16;
+    g.epi = rt == kF16 ? kEpiF16 : kEpiBF16;
     g.M = T; g.N = l; g.K = d;
     g.A = op2d(x, T, d);
     g.B0 = op2d(w->w_down_proj, l, d);
@@ -252,7 +264,7 @@ lmoe_status run_forward(lmoe_handle* h, const void* x, int T, const lmoe_weights
 
   if (identity) {
     stage_begin(h, kStCombine, s);
-    LMOE_TRY(launch_combine(h->z_perm, c.act, h->db.row_of, p, nullptr, 0.f, T, k, l, y, l, s));
+    LMOE_TRY(launch_combine(h->z_perm, c.act, c.act, h->db.row_of, p, nullptr, 0.f, T, k, l, y, l, s));
     stage_end(h, kStCombine, s);
     stages_finish(h, s);
     h->last_launches += 1;
@@ -262,11 +274,14 @@ lmoe_status run_forward(lmoe_handle* h, const void* x, int T, const lmoe_weights
   void* o = h->z_perm;  // the down projection overwrites the gathered rows it no longer needs
   uint8_t* n_out = static_cast<uint8_t*>(h->act_cat) + (size_t)ns * hs * ab;
   if (tc) {
+    const bool fp4 = c.routed_w == LMOE_MXFP4;
     TcGemm g = {};
-    g.epi = kEpiGluBF16;
+    g.epi = fp4 ? kEpiGluF16 : kEpiGluBF16;
     g.M = rows; g.N = hdim; g.K = l;
     g.A = op2d(h->z_perm, rows, l);
     g.B0 = op3d(w->routed_gate_up, c.num_experts, 2 * hdim, l);
+    g.ab_f16 = fp4;
+    g.b_scale = fp4 ? w->routed_gate_up_scale : nullptr;
     g.k0_len = l; g.k0_per_group = l; g.glu_h = hdim;
     g.tiles = h->db.tiles; g.num_tiles = h->db.num_tiles; g.offsets = h->db.offsets; g.max_tiles = h->max_tiles;
     g.C = h->a; g.ldc = hdim;
@@ -275,10 +290,12 @@ lmoe_status run_forward(lmoe_handle* h, const void* x, int T, const lmoe_weights
     stage_end(h, kStGlu, s);
 
     TcGemm dn = {};
-    dn.epi = kEpiScaleBF16;
+    dn.epi = fp4 ? kEpiScaleF16 : kEpiScaleBF16;
     dn.M = rows; dn.N = l; dn.K = hdim;
     dn.A = op2d(h->a, rows, hdim);
     dn.B0 = op3d(w->routed_down, c.num_experts, l, hdim);
+    dn.ab_f16 = fp4;
+    dn.b_scale = fp4 ? w->routed_down_scale : nullptr;
     dn.k0_len = hdim; dn.k0_per_group = hdim;
     dn.tiles = h->db.tiles; dn.num_tiles = h->db.num_tiles; dn.offsets = h->db.offsets; dn.max_tiles = h->max_tiles;
     dn.C = o; dn.ldc = l; dn.row_scale = h->db.p_row;
@@ -304,7 +321,7 @@ lmoe_status run_forward(lmoe_handle* h, const void* x, int T, const lmoe_weights
     stage_end(h, kStDown, s);
   }
   // u = sum_j o_j (rank order), n = RMSNorm(u) into the tail columns of act_cat
-  LMOE_TRY(launch_combine(o, c.act, h->db.row_of, nullptr, w->rms_gain, c.rms_eps, T, k, l, n_out, kcat, s));
+  LMOE_TRY(launch_combine(o, rt, c.act, h->db.row_of, nullptr, w->rms_gain, c.rms_eps, T, k, l, n_out, kcat, s));
   stage_end(h, kStCombine, s);
   h->last_launches += 3;
 

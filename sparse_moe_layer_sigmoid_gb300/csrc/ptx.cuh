@@ -157,5 +157,12 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
          | ((uint32_t)(M >> 4) << 24);   // M / 16
 }
 
+// Instruction descriptor for kind::f16 with fp16 A/B, fp32 accumulator, both K-major.
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
+  return (1u << 4)                       // D format: f32
+         | ((uint32_t)(N >> 3) << 17)    // N / 8  (A, B format fields 0: f16)
+         | ((uint32_t)(M >> 4) << 24);   // M / 16
+}
+
 }  // namespace ptx
 }  // namespace lmoe

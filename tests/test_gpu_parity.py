@@ -43,6 +43,9 @@ SMALL_CASES = [
     replace(configs.ROUTING_DISPATCH_STRESS, name="small_identity", tokens=1000, d=512, latent=256, experts=64,
             top_k=8, seed=26),
     replace(configs.TINY_F32, name="tiny_f32_skew_ragged", tokens=301, bias="normal1.5", seed=27),
+    replace(SMALL_BF16, name="small_mxfp4", routed_w="mxfp4", latent=512, hidden=512, seed=28),
+    replace(SMALL_BF16, name="small_mxfp4_skew", routed_w="mxfp4", latent=512, hidden=1024, experts=24,
+            bias="normal1.5", tokens=900, seed=29),
 ]
 
 
@@ -72,7 +75,8 @@ def _run_and_check(b, cfg, on_device=False, sample=None):
     want_l = oracle.router_logits(oracle.widen(host["x"][rows]), oracle.widen(host["w_router"]))
     l_err = float(np.abs(logits - want_l).max())
     assert l_err < 0.25e-3, f"router logit error {l_err:.3e} above a quarter of the refinement margin"
-    z = to_np(layer.debug_buffer("z", x.dtype, (T, cfg.latent)))[rows]
+    z_dtype = torch.float16 if cfg.routed_w == "mxfp4" and not cfg.identity_experts else x.dtype
+    z = to_np(layer.debug_buffer("z", z_dtype, (T, cfg.latent)))[rows]
     assert_close(z, ref["z"], REL_FRO[cfg.act], cfg.name + " z")
     if not cfg.identity_experts:
         kcat = cfg.n_shared * cfg.shared_hidden + cfg.latent
@@ -105,6 +109,26 @@ def test_k3w_e128_bf16_prefill_sampled_rows(binding):
     c = res["counts"]
     print(f"{cfg.name}: rel_fro={res['rel']:.3e} max/rms={res['max']:.3e} near_ties={res['near_ties']} "
           f"load max/mean={c.max() / c.mean():.2f} logit_err={res['logit_err']:.2e}")
+    del res
+    _free()
+
+
+def test_k3_mxfp4_decode_sampled_rows(binding):
+    cfg = configs.K3_MXFP4_DECODE
+    res = _run_and_check(binding, cfg, on_device=True, sample=8)
+    print(f"{cfg.name}: rel_fro={res['rel']:.3e} max/rms={res['max']:.3e} near_ties={res['near_ties']} "
+          f"experts touched={int((res['counts'] > 0).sum())} logit_err={res['logit_err']:.2e}")
+    del res
+    _free()
+
+
+def test_k3_mxfp4_prefill_skew_sampled_rows(binding):
+    cfg = configs.K3_MXFP4_PREFILL_SKEW
+    res = _run_and_check(binding, cfg, on_device=True, sample=256)
+    c = res["counts"]
+    print(f"{cfg.name}: rel_fro={res['rel']:.3e} max/rms={res['max']:.3e} near_ties={res['near_ties']} "
+          f"experts touched={int((c > 0).sum())} load max/mean={c.max() / c.mean():.2f} "
+          f"logit_err={res['logit_err']:.2e}")
     del res
     _free()
 
