@@ -1,0 +1,372 @@
+// Grouped expert GEMM for experts that receive few rows (decode-sized batches): the roles of
+// the operands are swapped, so that the expert's weights fill the 128-row M side of the
+// tcgen05 MMA and the expert's token rows are the N side (N = 16..128 in steps of 16), instead
+// of a 128-row token tile that is almost empty (page "What K3 actually is", srikanthmalla.com,
+// first section: decode is bound by reading the active expert weights).
+//
+//   D[f][j] = sum_c W_e[f][c] * X[row_j][c]     (f: 128 weight rows, j: the tile's token rows)
+//
+// Gate/up tiles hold 64 features: in every 32-row quarter of the M side, rows 0..15 are gate
+// rows and rows 16..31 the matching up rows, so one warp holds both halves of each GLU pair
+// and combines them with a lane shuffle.  Down tiles hold 128 output features and scale each
+// token column by its routing weight p.  MXFP4 weights are staged as packed bytes and
+// converted to fp16 in shared memory by 8 converter warps (hardware E2M1 pair conversion times
+// the E8M0 block scale), as in the main GEMM.  Every wait is bounded.
+#include "common.cuh"
+#include "internal.h"
+#include "ptx.cuh"
+#include "tc_common.cuh"
+
+namespace lmoe {
+namespace {
+
+using namespace tc;
+
+constexpr int kWRows = 128;   // weight rows per tile (MMA M)
+constexpr int kBox = 16;      // rows per TMA box (weights and tokens)
+constexpr int kMaxN = 128;    // token rows per tile: one 128-row dispatch tile
+constexpr int kBase = 192;    // producer, MMA, 4 epilogue warps
+
+template <bool FP4W>
+struct SwapCfg {
+  static constexpr int kS1 = FP4W ? 8 : 6;
+  static constexpr int kS2 = FP4W ? 3 : 1;
+  static constexpr uint32_t kAConvBytes = kWRows * BK * 2;                     // 16 KB 16-bit A tile
+  static constexpr uint32_t kARawBytes = FP4W ? kWRows * BK / 2 : kAConvBytes;  // 4 KB packed or 16 KB
+  static constexpr uint32_t kBBytes = kMaxN * BK * 2;                          // 16 KB token tile
+  static constexpr uint32_t kStage1Bytes = kARawBytes + kBBytes;
+  static constexpr uint32_t kRing1 = kS1 * kStage1Bytes;
+  static constexpr uint32_t kRing2 = FP4W ? kS2 * kAConvBytes : 0;
+  static constexpr uint32_t kTmemCols = 2 * kMaxN;
+  static constexpr int kConvWarps = FP4W ? 8 : 0;
+  static constexpr int kThreads = kBase + 32 * kConvWarps;
+  static constexpr size_t kSmem = (size_t)kRing1 + kRing2 + 1024 + 512;
+};
+
+struct SwapParams {
+  int num_kb;
+  int num_wt;  // weight tiles per expert
+  int glu_h;   // > 0: gate/up weights [2h][K] (64 features per tile); 0: plain rows (128 per tile)
+  int w_rows;  // weight rows per expert
+  const int4* tiles;
+  const int32_t* num_tiles;
+  const int32_t* offsets;
+  void* C;
+  int64_t ldc;
+  const float* row_scale;
+  const uint8_t* w_scale;
+  uint32_t* status;
+  uint64_t timeout_ns;
+};
+
+struct SwapTile {
+  int expert, row0, nrows, nb, wt;
+};
+
+__device__ __forceinline__ SwapTile decode_swap(const SwapParams& p, int u) {
+  SwapTile t;
+  const int q = u / p.num_wt;
+  t.wt = u - q * p.num_wt;
+  const int4 tl = p.tiles[q];
+  t.expert = tl.x;
+  t.row0 = p.offsets[tl.x] + (q - tl.y) * kMaxN;
+  t.nrows = min(kMaxN, p.offsets[tl.x + 1] - t.row0);
+  t.nb = (t.nrows + kBox - 1) / kBox;
+  return t;
+}
+
+// Weight row (within the expert) held by M-side row r of tile wt.
+__device__ __forceinline__ int weight_row(const SwapParams& p, int wt, int r) {
+  if (p.glu_h > 0) {
+    const int qq = r >> 5, w = r & 31;
+    const int j = wt * 64 + 16 * qq + (w & 15);
+    return w < 16 ? j : p.glu_h + j;
+  }
+  return wt * kWRows + r;
+}
+
+__device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+
+template <bool GLU, bool OUT_F16, bool AB_F16, bool FP4W>
+__global__ void __launch_bounds__(SwapCfg<FP4W>::kThreads, 1)
+    tc_swap_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                   const SwapParams p) {
+  using C = SwapCfg<FP4W>;
+  constexpr int S1 = C::kS1, S2 = C::kS2;
+
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = ptx::smem_addr(smem_raw);
+  uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+  uint8_t* ring2 = smem + C::kRing1;
+  uint64_t* full1 = reinterpret_cast<uint64_t*>(ring2 + C::kRing2);
+  uint64_t* empty1 = full1 + S1;
+  uint64_t* full2 = empty1 + S1;
+  uint64_t* empty2 = full2 + S2;
+  uint64_t* tmem_full = empty2 + S2;
+  uint64_t* tmem_empty = tmem_full + 2;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(tmem_empty + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S1; ++s) {
+      ptx::mbar_init(&full1[s], 1);
+      ptx::mbar_init(&empty1[s], 1);
+    }
+    for (int s = 0; s < S2; ++s) {
+      ptx::mbar_init(&full2[s], C::kConvWarps > 0 ? C::kConvWarps : 1);
+      ptx::mbar_init(&empty2[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      ptx::mbar_init(&tmem_full[a], 1);
+      ptx::mbar_init(&tmem_empty[a], 4);
+    }
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+    ptx::prefetch_tmap(&tmW);
+    ptx::prefetch_tmap(&tmX);
+  }
+  if (warp == 1) ptx::tmem_alloc(tmem_holder, C::kTmemCols);
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+  const int total = *p.num_tiles * p.num_wt;
+
+  if (warp == 0 && lane == 0) {
+    // ------------------------------------------------------------------ TMA producer
+    int stage = 0;
+    uint32_t phase = 0;
+    for (int u = blockIdx.x; u < total; u += gridDim.x) {
+      const SwapTile ti = decode_swap(p, u);
+      constexpr uint32_t kWBox = FP4W ? kBox * BK / 2 : kBox * BK * 2;  // bytes per weight box
+      const uint32_t tx = C::kARawBytes + (uint32_t)ti.nb * (kBox * BK * 2);
+      for (int kb = 0; kb < p.num_kb; ++kb) {
+        if (!ptx::mbar_wait_bounded(&empty1[stage], phase ^ 1u, abort_flag, p.status, p.timeout_ns)) goto done;
+        uint8_t* sW = smem + stage * C::kStage1Bytes;
+        uint8_t* sX = sW + C::kARawBytes;
+        ptx::mbar_arrive_expect_tx(&full1[stage], tx);
+        const int kx = FP4W ? kb * (BK / 2) : kb * BK;
+#pragma unroll
+        for (int b = 0; b < kWRows / kBox; ++b)
+          ptx::tma_load_3d(sW + b * kWBox, &tmW, &full1[stage], kx, weight_row(p, ti.wt, b * kBox), ti.expert);
+        for (int b = 0; b < ti.nb; ++b)
+          ptx::tma_load_3d(sX + b * (kBox * BK * 2), &tmX, &full1[stage], kb * BK, ti.row0 + b * kBox, 0);
+        if (++stage == S1) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ------------------------------------------------------------------ MMA issuer
+    constexpr uint32_t idesc0 = AB_F16 ? ptx::idesc_f16_f32(kWRows, 0) : ptx::idesc_bf16_f32(kWRows, 0);
+    int s1 = 0, s2 = 0;
+    uint32_t ph1 = 0, ph2 = 0;
+    int it = 0;
+    for (int u = blockIdx.x; u < total; u += gridDim.x, ++it) {
+      const SwapTile ti = decode_swap(p, u);
+      const uint32_t idesc = idesc0 | ((uint32_t)((ti.nb * kBox) >> 3) << 17);  // N = 16 * nb
+      const int acc = it & 1;
+      const uint32_t use = (uint32_t)(it >> 1);
+      if (!ptx::mbar_wait_bounded(&tmem_empty[acc], (use & 1u) ^ 1u, abort_flag, p.status, p.timeout_ns))
+        goto done;
+      ptx::tc_fence_after();
+      const uint32_t d_tmem = tmem_base + (uint32_t)(acc * kMaxN);
+      for (int kb = 0; kb < p.num_kb; ++kb) {
+        if (FP4W && !ptx::mbar_wait_bounded(&full2[s2], ph2, abort_flag, p.status, p.timeout_ns)) goto done;
+        if (!ptx::mbar_wait_bounded(&full1[s1], ph1, abort_flag, p.status, p.timeout_ns)) goto done;
+        ptx::tc_fence_after();
+        const uint32_t st_addr = ptx::smem_addr(smem + s1 * C::kStage1Bytes);
+        const uint32_t a_addr = FP4W ? ptx::smem_addr(ring2 + s2 * C::kAConvBytes) : st_addr;
+        const uint32_t b_addr = st_addr + C::kARawBytes;
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk)
+          ptx::mma_f16(d_tmem, ptx::sw128_kmajor_desc(a_addr + kk * 32), ptx::sw128_kmajor_desc(b_addr + kk * 32),
+                       idesc, (kb | kk) != 0 ? 1u : 0u);
+        ptx::mma_commit(&empty1[s1]);
+        if (++s1 == S1) {
+          s1 = 0;
+          ph1 ^= 1u;
+        }
+        if (FP4W) {
+          ptx::mma_commit(&empty2[s2]);
+          if (++s2 == S2) {
+            s2 = 0;
+            ph2 ^= 1u;
+          }
+        }
+      }
+      ptx::mma_commit(&tmem_full[acc]);
+    }
+  } else if (warp >= 2 && warp < 6) {
+    // ------------------------------------------------------------------ epilogue (transposed)
+    const int q = warp & 3;
+    int it = 0;
+    for (int u = blockIdx.x; u < total; u += gridDim.x, ++it) {
+      const SwapTile ti = decode_swap(p, u);
+      const int acc = it & 1;
+      const uint32_t use = (uint32_t)(it >> 1);
+      int ok = 1;
+      if (lane == 0) ok = ptx::mbar_wait_bounded(&tmem_full[acc], use & 1u, abort_flag, p.status, p.timeout_ns);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      ptx::tc_fence_after();
+      const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * kMaxN);
+      uint16_t* out = static_cast<uint16_t*>(p.C);
+      const int col = GLU ? ti.wt * 64 + 16 * q + (lane & 15) : ti.wt * kWRows + 32 * q + lane;
+      for (int ch = 0; ch < ti.nb; ++ch) {
+        uint32_t r[16];
+        tmem_ld_32x32b_x16(t_row + ch * kBox, r);
+        ptx::tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < kBox; ++i) {
+          const int j = ch * kBox + i;
+          if (j < ti.nrows) {  // uniform across the warp
+            const int row = ti.row0 + j;
+            const float v = __uint_as_float(r[i]);
+            float o;
+            bool write;
+            if (GLU) {
+              const float up = __shfl_down_sync(0xffffffffu, v, 16);
+              o = silu(v) * up;
+              write = lane < 16;
+            } else {
+              o = v * p.row_scale[row];
+              write = true;
+            }
+            if (write) {
+              const uint32_t bits = OUT_F16 ? (uint32_t)__half_as_ushort(__float2half_rn(o))
+                                            : (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(o));
+              out[(int64_t)row * p.ldc + col] = (uint16_t)bits;
+            }
+          }
+        }
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&tmem_empty[acc]);
+    }
+  } else if (FP4W && warp >= 6) {
+    // ------------------------------------------------------------------ E2M1 -> fp16 converters
+    const int cid = threadIdx.x - kBase;  // 0..255
+    const int r = cid >> 1, half = cid & 1;
+    const int kscale = p.num_kb * 2;
+    int s1 = 0, s2 = 0;
+    uint32_t ph1 = 0, ph2 = 0;
+    bool bad = false;
+    for (int u = blockIdx.x; u < total; u += gridDim.x) {
+      const SwapTile ti = decode_swap(p, u);
+      const int wrow = weight_row(p, ti.wt, r);
+      const uint4* srow =
+          reinterpret_cast<const uint4*>(p.w_scale + ((int64_t)ti.expert * p.w_rows + wrow) * kscale);
+      uint4 sc16 = make_uint4(0, 0, 0, 0);
+      for (int kb = 0; kb < p.num_kb; ++kb) {
+        if ((kb & 7) == 0) sc16 = __ldg(srow + (kb >> 3));
+        int ok = 1;
+        if (lane == 0) {
+          ok = ptx::mbar_wait_bounded(&full1[s1], ph1, abort_flag, p.status, p.timeout_ns) &&
+               ptx::mbar_wait_bounded(&empty2[s2], ph2 ^ 1u, abort_flag, p.status, p.timeout_ns);
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) goto conv_done;
+        {
+          const uint4 qv = *reinterpret_cast<const uint4*>(smem + s1 * C::kStage1Bytes + r * (BK / 2) + half * 16);
+          const int wsel = (kb & 7) >> 1;
+          const uint32_t sw = wsel == 0 ? sc16.x : wsel == 1 ? sc16.y : wsel == 2 ? sc16.z : sc16.w;
+          const uint32_t sb = (sw >> ((kb & 1) * 16 + half * 8)) & 0xFFu;
+          uint32_t o[16];
+          e2m1x32_to_f16(qv, e8m0_to_f16x2(sb, &bad), o);
+          uint8_t* dst = ring2 + s2 * C::kAConvBytes + (r >> 3) * 1024 + (r & 7) * 128;
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            *reinterpret_cast<uint4*>(dst + (((4 * half + c) ^ (r & 7)) << 4)) =
+                make_uint4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&full2[s2]);
+        if (++s1 == S1) {
+          s1 = 0;
+          ph1 ^= 1u;
+        }
+        if (++s2 == S2) {
+          s2 = 0;
+          ph2 ^= 1u;
+        }
+      }
+    }
+  conv_done:
+    if (bad) report(p.status, kStatusDeviceCheck);
+  }
+done:
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem_base, C::kTmemCols);
+  }
+}
+
+template <bool GLU, bool OUT_F16, bool AB_F16, bool FP4W>
+cudaError_t launch_swap_inst(const CUtensorMap& w, const CUtensorMap& x, const SwapParams& p, int grid,
+                             cudaStream_t s) {
+  using C = SwapCfg<FP4W>;
+  auto kern = tc_swap_kernel<GLU, OUT_F16, AB_F16, FP4W>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  kern<<<grid, C::kThreads, C::kSmem, s>>>(w, x, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_tc_swap(const TcSwap& g, uint32_t* status, uint64_t timeout_ns, int num_sms, cudaStream_t s) {
+  const bool glu = g.epi == kEpiGluBF16 || g.epi == kEpiGluF16;
+  const bool out_f16 = g.epi == kEpiGluF16 || g.epi == kEpiScaleF16;
+  const bool fp4 = g.w_scale != nullptr;
+  if (g.K % BK || (fp4 && g.K % 512)) return cudaErrorInvalidValue;
+  if (glu ? (g.glu_h % 64 || g.out_features != g.glu_h) : g.out_features % kWRows) return cudaErrorInvalidValue;
+  if (fp4 && !g.ab_f16) return cudaErrorInvalidValue;
+  CUtensorMap mw, mx;
+  if (!(fp4 ? make_map_fp4(&mw, g.w, kBox) : make_map(&mw, g.w, kBox))) return cudaErrorInvalidValue;
+  if (!make_map(&mx, g.act, kBox)) return cudaErrorInvalidValue;
+  SwapParams p = {};
+  p.num_kb = g.K / BK;
+  p.num_wt = glu ? g.glu_h / 64 : g.out_features / kWRows;
+  p.glu_h = glu ? g.glu_h : 0;
+  p.w_rows = (int)g.w.rows;
+  p.tiles = g.tiles;
+  p.num_tiles = g.num_tiles;
+  p.offsets = g.offsets;
+  p.C = g.C;
+  p.ldc = g.ldc;
+  p.row_scale = g.row_scale;
+  p.w_scale = g.w_scale;
+  p.status = status;
+  p.timeout_ns = timeout_ns;
+  const long long units = (long long)g.max_tiles * p.num_wt;
+  if (units == 0) return cudaSuccess;
+  const int grid = (int)(units < num_sms ? units : num_sms);
+  if (fp4) {
+    return glu ? launch_swap_inst<true, true, true, true>(mw, mx, p, grid, s)
+               : launch_swap_inst<false, true, true, true>(mw, mx, p, grid, s);
+  }
+  if (g.ab_f16) return cudaErrorInvalidValue;
+  if (out_f16) return cudaErrorInvalidValue;
+  return glu ? launch_swap_inst<true, false, false, false>(mw, mx, p, grid, s)
+             : launch_swap_inst<false, false, false, false>(mw, mx, p, grid, s);
+}
+
+}  // namespace lmoe

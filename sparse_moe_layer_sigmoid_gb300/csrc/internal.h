@@ -115,4 +115,21 @@ struct TcGemm {
 cudaError_t launch_tc_gemm(const TcGemm& g, uint32_t* status, uint64_t timeout_ns, int inject_fault, int num_sms,
                            cudaStream_t s);
 
+// Swapped-operand grouped GEMM for experts with few rows (gemm_swap.cu): weights are the
+// 128-row M operand, the tile's token rows (up to 128) the N operand.
+struct TcSwap {
+  int epi;                  // kEpiGlu{BF16,F16} (output h features) or kEpiScale{BF16,F16}
+  int K;                    // reduction width
+  int out_features;         // h for gate/up, l for down
+  TcOperand act;            // [rows][K] 16-bit token rows (expert-contiguous)
+  TcOperand w;              // [E][w_rows][K] weights (16-bit, or packed E2M1 when w_scale)
+  const uint8_t* w_scale;   // E8M0 [E][w_rows][K/32] or nullptr
+  int ab_f16;
+  int glu_h;
+  const int4* tiles; const int32_t* num_tiles; const int32_t* offsets; int max_tiles;
+  void* C; int64_t ldc;
+  const float* row_scale;   // down: routing weight per row
+};
+cudaError_t launch_tc_swap(const TcSwap& g, uint32_t* status, uint64_t timeout_ns, int num_sms, cudaStream_t s);
+
 }  // namespace lmoe

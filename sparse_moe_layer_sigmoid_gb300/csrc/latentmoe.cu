@@ -273,7 +273,34 @@ lmoe_status run_forward(lmoe_handle* h, const void* x, int T, const lmoe_weights
 
   void* o = h->z_perm;  // the down projection overwrites the gathered rows it no longer needs
   uint8_t* n_out = static_cast<uint8_t*>(h->act_cat) + (size_t)ns * hs * ab;
-  if (tc) {
+  // few rows per expert (decode): weights on the M side of the MMA, tokens on the N side
+  const bool swap = tc && (int64_t)T * k <= 32LL * c.num_experts;
+  if (swap) {
+    const bool fp4 = c.routed_w == LMOE_MXFP4;
+    TcSwap g = {};
+    g.epi = fp4 ? kEpiGluF16 : kEpiGluBF16;
+    g.K = l; g.out_features = hdim; g.glu_h = hdim;
+    g.act = op2d(h->z_perm, rows, l);
+    g.w = op3d(w->routed_gate_up, c.num_experts, 2 * hdim, l);
+    g.w_scale = fp4 ? w->routed_gate_up_scale : nullptr;
+    g.ab_f16 = fp4;
+    g.tiles = h->db.tiles; g.num_tiles = h->db.num_tiles; g.offsets = h->db.offsets; g.max_tiles = h->max_tiles;
+    g.C = h->a; g.ldc = hdim;
+    LMOE_TRY(launch_tc_swap(g, h->status, h->timeout_ns, h->num_sms, s));
+    stage_end(h, kStGlu, s);
+
+    TcSwap dn = {};
+    dn.epi = fp4 ? kEpiScaleF16 : kEpiScaleBF16;
+    dn.K = hdim; dn.out_features = l;
+    dn.act = op2d(h->a, rows, hdim);
+    dn.w = op3d(w->routed_down, c.num_experts, l, hdim);
+    dn.w_scale = fp4 ? w->routed_down_scale : nullptr;
+    dn.ab_f16 = fp4;
+    dn.tiles = h->db.tiles; dn.num_tiles = h->db.num_tiles; dn.offsets = h->db.offsets; dn.max_tiles = h->max_tiles;
+    dn.C = o; dn.ldc = l; dn.row_scale = h->db.p_row;
+    LMOE_TRY(launch_tc_swap(dn, h->status, h->timeout_ns, h->num_sms, s));
+    stage_end(h, kStDown, s);
+  } else if (tc) {
     const bool fp4 = c.routed_w == LMOE_MXFP4;
     TcGemm g = {};
     g.epi = fp4 ? kEpiGluF16 : kEpiGluBF16;

@@ -64,43 +64,56 @@ __device__ __forceinline__ void load8(const float* p, float (&f)[8]) {
   f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
 }
 
+constexpr int kCandBatch = 8;  // boundary candidates evaluated per pass over d
+
+// Up to kCandBatch dot products x . W_r[e_m] in double-float, one warp: each step loads 8
+// elements of x once and 8 elements of every candidate row (independent loads in flight).
 template <typename TX, typename TW>
-__device__ DF dot_df(const TX* x, const TW* w, int d, int lane) {
-  DF acc0 = {0.f, 0.f}, acc1 = {0.f, 0.f};
-  for (int c = lane * 8; c < d; c += 32 * 8) {  // d % 16 == 0 and 16-byte aligned rows
-    float xf[8], wf[8];
-    load8(x + c, xf);
-    load8(w + c, wf);
+__device__ void dots_df(const TX* x, const TW* w, int64_t d, const int (&ce)[kCandBatch], int nc, int lane,
+                        double (&out)[kCandBatch]) {
+  DF acc[kCandBatch];
 #pragma unroll
-    for (int i = 0; i < 8; i += 2) {
-      df_add_prod(acc0, xf[i], wf[i]);
-      df_add_prod(acc1, xf[i + 1], wf[i + 1]);
+  for (int m = 0; m < kCandBatch; ++m) acc[m] = DF{0.f, 0.f};
+  for (int c = lane * 8; c < d; c += 32 * 8) {  // d % 16 == 0 and 16-byte aligned rows
+    float xf[8];
+    load8(x + c, xf);
+#pragma unroll
+    for (int m = 0; m < kCandBatch; ++m) {
+      if (m < nc) {
+        float wf[8];
+        load8(w + ce[m] * d + c, wf);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) df_add_prod(acc[m], xf[i], wf[i]);
+      }
     }
   }
-  DF acc = df_add(acc0, acc1);
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    DF o;
-    o.hi = __shfl_xor_sync(0xffffffffu, acc.hi, off);
-    o.lo = __shfl_xor_sync(0xffffffffu, acc.lo, off);
-    acc = df_add(acc, o);
+  for (int m = 0; m < kCandBatch; ++m) {
+    DF a = acc[m];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      DF o;
+      o.hi = __shfl_xor_sync(0xffffffffu, a.hi, off);
+      o.lo = __shfl_xor_sync(0xffffffffu, a.lo, off);
+      a = df_add(a, o);
+    }
+    out[m] = (double)a.hi + (double)a.lo;
   }
-  return acc;
 }
 
-// Logit of expert e for token t to ~44 bits (one warp; every lane returns the same value).
-__device__ double exact_logit(const RouterSrc& r, int t, int e, int lane) {
-  const int64_t xo = (int64_t)t * r.d, wo = (int64_t)e * r.d;
-  DF v;
+// Logits of the candidate experts ce[0..nc) for token t to ~44 bits (one warp; all lanes get
+// every value).
+__device__ void exact_logits(const RouterSrc& r, int t, const int (&ce)[kCandBatch], int nc, int lane,
+                             double (&out)[kCandBatch]) {
+  const int64_t xo = (int64_t)t * r.d;
   if (r.x_dtype == kBF16 && r.w_dtype == kBF16)
-    v = dot_df(static_cast<const __nv_bfloat16*>(r.x) + xo, static_cast<const __nv_bfloat16*>(r.w) + wo, r.d, lane);
+    dots_df(static_cast<const __nv_bfloat16*>(r.x) + xo, static_cast<const __nv_bfloat16*>(r.w), r.d, ce, nc, lane, out);
   else if (r.x_dtype == kBF16)
-    v = dot_df(static_cast<const __nv_bfloat16*>(r.x) + xo, static_cast<const float*>(r.w) + wo, r.d, lane);
+    dots_df(static_cast<const __nv_bfloat16*>(r.x) + xo, static_cast<const float*>(r.w), r.d, ce, nc, lane, out);
   else if (r.w_dtype == kBF16)
-    v = dot_df(static_cast<const float*>(r.x) + xo, static_cast<const __nv_bfloat16*>(r.w) + wo, r.d, lane);
+    dots_df(static_cast<const float*>(r.x) + xo, static_cast<const __nv_bfloat16*>(r.w), r.d, ce, nc, lane, out);
   else
-    v = dot_df(static_cast<const float*>(r.x) + xo, static_cast<const float*>(r.w) + wo, r.d, lane);
-  return (double)v.hi + (double)v.lo;
+    dots_df(static_cast<const float*>(r.x) + xo, static_cast<const float*>(r.w), r.d, ce, nc, lane, out);
 }
 
 // One warp per token.  Keys s + b are packed as (orderable(key) << 32) | (~expert) so that the
@@ -183,22 +196,42 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ log
     const int n_cert = __popc(__ballot_sync(0xffffffffu, lane < k && my_kf > hi));  // ranks 0..n_cert-1
     double ex[NPL];
 #pragma unroll
+    for (int i = 0; i < NPL; ++i) ex[i] = -INFINITY;
+    // candidates in warp-uniform batches: exact logits, then the owner lane stores the key
+    int ce[kCandBatch];
+    int nc = 0;
+    auto flush = [&]() {
+      double lg[kCandBatch];
+      exact_logits(src, t, ce, nc, lane, lg);
+#pragma unroll
+      for (int m = 0; m < kCandBatch; ++m) {
+        if (m < nc && lane == (ce[m] & 31)) {
+          const double s64 = 1.0 / (1.0 + exp(-lg[m]));
+          const double key = s64 + (bias ? (double)bias[ce[m]] : 0.0);
+#pragma unroll
+          for (int i = 0; i < NPL; ++i)
+            if (i == (ce[m] >> 5)) {
+              ex[i] = key;
+              sv[i] = (float)s64;
+            }
+        }
+      }
+      nc = 0;
+    };
+#pragma unroll
     for (int i = 0; i < NPL; ++i) {
-      ex[i] = -INFINITY;
       const int e = lane + 32 * i;
       uint32_t m = __ballot_sync(0xffffffffu, e < E && kf[i] >= lo && kf[i] <= hi);
       while (m) {
         const int src_lane = __ffs(m) - 1;
         m &= m - 1;
-        const int ce = src_lane + 32 * i;
-        const double l = exact_logit(src, t, ce, lane);
-        if (lane == src_lane) {
-          const double s64 = 1.0 / (1.0 + exp(-l));
-          ex[i] = s64 + (bias ? (double)bias[ce] : 0.0);
-          sv[i] = (float)s64;
-        }
+#pragma unroll
+        for (int q = 0; q < kCandBatch; ++q)
+          if (q == nc) ce[q] = src_lane + 32 * i;
+        if (++nc == kCandBatch) flush();
       }
     }
+    if (nc > 0) flush();
     for (int q = n_cert; q < k; ++q) {
       double bv = -INFINITY;
       int be = 0x7FFFFFFF;

@@ -46,6 +46,11 @@ SMALL_CASES = [
     replace(SMALL_BF16, name="small_mxfp4", routed_w="mxfp4", latent=512, hidden=512, seed=28),
     replace(SMALL_BF16, name="small_mxfp4_skew", routed_w="mxfp4", latent=512, hidden=1024, experts=24,
             bias="normal1.5", tokens=900, seed=29),
+    # decode-shaped (T*k <= 32*E): the swapped-operand expert GEMMs
+    replace(SMALL_BF16, name="small_bf16_decode", tokens=24, seed=36),
+    replace(SMALL_BF16, name="small_bf16_decode_skew", tokens=150, top_k=2, bias="normal1.5", seed=37),
+    replace(SMALL_BF16, name="small_mxfp4_decode", routed_w="mxfp4", latent=512, hidden=512, experts=24, tokens=40,
+            seed=38),
 ]
 
 
