@@ -186,9 +186,10 @@ lmoe_status latentmoe_debug_buffer(const lmoe_handle *h, const char *name, void 
  * ignored).  Outputs are as for latentmoe_route, but all five must be non-NULL when T > 0.
  * Scratch lives in one fixed 16 MiB device array inside the library, held on every GPU that
  * loads the library until the process exits; a call needs
- *   256*ceil(T*E*4/256) + 2*256*ceil(ceil(T/256)*E*4/256) + 256*ceil((T*k/128+E+1)*16/256) + 256
+ *   256*ceil(T*E*4/256) + 2*256*ceil(ceil(T/256)*E*4/256) + 256*ceil((T*k/128+E+1)*16/256)
+ *   + 256*ceil(T*4/256) + 512
  * bytes of it, plus 256*ceil(3*E*d*2/256) when act is BF16 and router_w is F32 (the three bf16
- * terms of W_r); with k=16 and a bf16 W_r, T up to 32,383 for E=128 and up to 4,636 for E=896; a
+ * terms of W_r); with k=16 and a bf16 W_r, T up to 32,133 for E=128 and up to 4,631 for E=896; a
  * larger need returns LMOE_ERR_INVALID_ARG before any launch.  The first call on a device looks
  * up the array's device address (cudaGetSymbolAddress) and should come before any stream
  * capture.  Calls that overlap on the GPU share the array and race: serialise them.  Errors:

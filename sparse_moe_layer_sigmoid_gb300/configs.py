@@ -54,9 +54,16 @@ ROUTING_DISPATCH_STRESS = LayerConfig("routing_dispatch_t65536", 65536, 7168, 35
 # device (weights still far larger than L2), small enough for multi-pass profiler captures.
 K3W_E32_BF16_PROFILE = replace(K3W_E128_BF16_PREFILL, name="k3w_e32_bf16_t1024", tokens=1024, experts=32)
 
+# MXFP4 cases of the same kind for profiler captures: decode-shaped (8 tokens over 128 experts,
+# about one row per touched expert) and prefill-shaped (1024 tokens over 32 experts).
+K3_MXFP4_DECODE_PROFILE = replace(K3_MXFP4_DECODE, name="k3_mxfp4_decode_e128_t8", tokens=8, experts=128)
+K3_MXFP4_PREFILL_PROFILE = replace(K3_MXFP4_PREFILL_SKEW, name="k3_mxfp4_prefill_e32_t1024", tokens=1024,
+                                   experts=32, bias="none")
+
 CONFIGS = {c.name: c for c in (TINY_F32, K3W_E128_BF16_PREFILL, K3_MXFP4_DECODE,
                                K3_MXFP4_PREFILL_SKEW, K3_MXFP4_PREFILL_MILD,
-                               ROUTING_DISPATCH_STRESS, K3W_E32_BF16_PROFILE)}
+                               ROUTING_DISPATCH_STRESS, K3W_E32_BF16_PROFILE,
+                               K3_MXFP4_DECODE_PROFILE, K3_MXFP4_PREFILL_PROFILE)}
 
 
 def scaled(cfg: LayerConfig, **kw) -> LayerConfig:

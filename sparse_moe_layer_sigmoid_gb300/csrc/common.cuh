@@ -15,6 +15,8 @@ enum DType : int { kF32 = 0, kBF16 = 1, kMXFP4 = 2, kF16 = 3 /* internal: fp16 a
 
 // Rows of one grouped-GEMM M tile; the dispatch step builds its tile list in these units.
 constexpr int kTileM = 128;
+// Rows of one unit of the swapped-operand (decode) expert GEMM: a second, finer tile list.
+constexpr int kTileS = 16;
 // Tokens per dispatch chunk (one CTA, one bit per token in the per-expert masks).
 constexpr int kDispatchChunk = 256;
 

@@ -1,17 +1,22 @@
 // Grouped expert GEMM for experts that receive few rows (decode-sized batches): the roles of
 // the operands are swapped, so that the expert's weights fill the 128-row M side of the
-// tcgen05 MMA and the expert's token rows are the N side (N = 16..128 in steps of 16), instead
-// of a 128-row token tile that is almost empty (page "What K3 actually is", srikanthmalla.com,
+// tcgen05 MMA and the expert's token rows are the N side (a multiple of 16), instead of a
+// 128-row token tile that is almost empty (page "What K3 actually is", srikanthmalla.com,
 // first section: decode is bound by reading the active expert weights).
 //
-//   D[f][j] = sum_c W_e[f][c] * X[row_j][c]     (f: 128 weight rows, j: the tile's token rows)
+//   D[f][j] = sum_c W_e[f][c] * X[row_j][c]     (f: 128 weight rows, j: the unit's token rows)
 //
 // Gate/up tiles hold 64 features: in every 32-row quarter of the M side, rows 0..15 are gate
 // rows and rows 16..31 the matching up rows, so one warp holds both halves of each GLU pair
 // and combines them with a lane shuffle.  Down tiles hold 128 output features and scale each
-// token column by its routing weight p.  MXFP4 weights are staged as packed bytes and
-// converted to fp16 in shared memory by 8 converter warps (hardware E2M1 pair conversion times
-// the E8M0 block scale), as in the main GEMM.  Every wait is bounded.
+// token column by its routing weight p.
+//
+// MXFP4 weights stream as 256-element super-blocks (128 contiguous bytes per weight row, 16 KB
+// per stage, stored with the 128-byte swizzle) and are converted to fp16 in 64-element
+// sub-blocks by 8 converter warps (hardware E2M1 pair conversion times the E8M0 block scale),
+// each handed to the MMA as soon as it is ready.  bf16 weights go to the MMA straight from TMA,
+// 64 elements per stage.  A unit is one entry of the dispatch's 16-row tile list (an expert's
+// rows in groups of at most 16), so decode batches run N = 16 MMAs.  Every wait is bounded.
 #include "common.cuh"
 #include "internal.h"
 #include "ptx.cuh"
@@ -22,35 +27,35 @@ namespace {
 
 using namespace tc;
 
-constexpr int kWRows = 128;   // weight rows per tile (MMA M)
-constexpr int kBox = 16;      // rows per TMA box (weights and tokens)
-constexpr int kMaxN = 128;    // token rows per tile: one 128-row dispatch tile
-constexpr int kBase = 192;    // producer, MMA, 4 epilogue warps
+constexpr int kWRows = 128;  // weight rows per tile (MMA M)
+constexpr int kBox = 16;     // rows per TMA box (weights and tokens)
+constexpr int kBase = 192;   // producer, MMA, 4 epilogue warps
 
 template <bool FP4W>
 struct SwapCfg {
-  static constexpr int kS1 = FP4W ? 8 : 6;
-  static constexpr int kS2 = FP4W ? 3 : 1;
-  static constexpr uint32_t kAConvBytes = kWRows * BK * 2;                     // 16 KB 16-bit A tile
-  static constexpr uint32_t kARawBytes = FP4W ? kWRows * BK / 2 : kAConvBytes;  // 4 KB packed or 16 KB
-  static constexpr uint32_t kBBytes = kMaxN * BK * 2;                          // 16 KB token tile
-  static constexpr uint32_t kStage1Bytes = kARawBytes + kBBytes;
+  static constexpr int kSub = FP4W ? 4 : 1;                 // 64-element sub-blocks per TMA stage
+  static constexpr int kMaxN = kTileS;                      // token rows per unit (16-row tile list)
+  static constexpr int kS1 = FP4W ? 4 : 10;
+  static constexpr int kS2 = FP4W ? 8 : 1;
+  static constexpr uint32_t kAConvBytes = kWRows * BK * 2;  // 16 KB 16-bit A sub-tile
+  static constexpr uint32_t kWStageBytes = FP4W ? kWRows * BK * kSub / 2 : kAConvBytes;  // 16 KB
+  static constexpr uint32_t kXSubBytes = kMaxN * BK * 2;    // token sub-tile (2 KB)
+  static constexpr uint32_t kStage1Bytes = kWStageBytes + kSub * kXSubBytes;  // 24 KB or 18 KB
   static constexpr uint32_t kRing1 = kS1 * kStage1Bytes;
   static constexpr uint32_t kRing2 = FP4W ? kS2 * kAConvBytes : 0;
-  static constexpr uint32_t kTmemCols = 2 * kMaxN;
+  static constexpr uint32_t kTmemCols = 32;                 // two accumulators of kMaxN columns
   static constexpr int kConvWarps = FP4W ? 8 : 0;
   static constexpr int kThreads = kBase + 32 * kConvWarps;
   static constexpr size_t kSmem = (size_t)kRing1 + kRing2 + 1024 + 512;
 };
 
 struct SwapParams {
-  int num_kb;
+  int num_kb;  // 64-element k-blocks
   int num_wt;  // weight tiles per expert
   int glu_h;   // > 0: gate/up weights [2h][K] (64 features per tile); 0: plain rows (128 per tile)
   int w_rows;  // weight rows per expert
-  const int4* tiles;
-  const int32_t* num_tiles;
-  const int32_t* offsets;
+  const int4* tiles_s;  // {expert, first row, rows}
+  const int32_t* num_tiles_s;
   void* C;
   int64_t ldc;
   const float* row_scale;
@@ -67,11 +72,11 @@ __device__ __forceinline__ SwapTile decode_swap(const SwapParams& p, int u) {
   SwapTile t;
   const int q = u / p.num_wt;
   t.wt = u - q * p.num_wt;
-  const int4 tl = p.tiles[q];
+  const int4 tl = p.tiles_s[q];
   t.expert = tl.x;
-  t.row0 = p.offsets[tl.x] + (q - tl.y) * kMaxN;
-  t.nrows = min(kMaxN, p.offsets[tl.x + 1] - t.row0);
-  t.nb = (t.nrows + kBox - 1) / kBox;
+  t.row0 = tl.y;
+  t.nrows = tl.z;
+  t.nb = 1;
   return t;
 }
 
@@ -99,7 +104,7 @@ __global__ void __launch_bounds__(SwapCfg<FP4W>::kThreads, 1)
     tc_swap_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                    const SwapParams p) {
   using C = SwapCfg<FP4W>;
-  constexpr int S1 = C::kS1, S2 = C::kS2;
+  constexpr int S1 = C::kS1, S2 = C::kS2, SUB = C::kSub, MAXN = C::kMaxN;
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = ptx::smem_addr(smem_raw);
@@ -138,7 +143,8 @@ __global__ void __launch_bounds__(SwapCfg<FP4W>::kThreads, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
-  const int total = *p.num_tiles * p.num_wt;
+  const int total = *p.num_tiles_s * p.num_wt;
+  const int num_st = p.num_kb / SUB;  // TMA stages per unit
 
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------------ TMA producer
@@ -146,19 +152,22 @@ __global__ void __launch_bounds__(SwapCfg<FP4W>::kThreads, 1)
     uint32_t phase = 0;
     for (int u = blockIdx.x; u < total; u += gridDim.x) {
       const SwapTile ti = decode_swap(p, u);
-      constexpr uint32_t kWBox = FP4W ? kBox * BK / 2 : kBox * BK * 2;  // bytes per weight box
-      const uint32_t tx = C::kARawBytes + (uint32_t)ti.nb * (kBox * BK * 2);
-      for (int kb = 0; kb < p.num_kb; ++kb) {
+      constexpr uint32_t kWBox = C::kWStageBytes / (kWRows / kBox);  // bytes per weight box
+      const uint32_t tx = C::kWStageBytes + (uint32_t)(SUB * ti.nb) * (kBox * BK * 2);
+      for (int st = 0; st < num_st; ++st) {
         if (!ptx::mbar_wait_bounded(&empty1[stage], phase ^ 1u, abort_flag, p.status, p.timeout_ns)) goto done;
         uint8_t* sW = smem + stage * C::kStage1Bytes;
-        uint8_t* sX = sW + C::kARawBytes;
+        uint8_t* sX = sW + C::kWStageBytes;
         ptx::mbar_arrive_expect_tx(&full1[stage], tx);
-        const int kx = FP4W ? kb * (BK / 2) : kb * BK;
+        const int kx = FP4W ? st * (BK * SUB / 2) : st * BK;  // bytes (packed) or elements
 #pragma unroll
         for (int b = 0; b < kWRows / kBox; ++b)
           ptx::tma_load_3d(sW + b * kWBox, &tmW, &full1[stage], kx, weight_row(p, ti.wt, b * kBox), ti.expert);
-        for (int b = 0; b < ti.nb; ++b)
-          ptx::tma_load_3d(sX + b * (kBox * BK * 2), &tmX, &full1[stage], kb * BK, ti.row0 + b * kBox, 0);
+#pragma unroll
+        for (int sb = 0; sb < SUB; ++sb)
+          for (int b = 0; b < ti.nb; ++b)
+            ptx::tma_load_3d(sX + sb * C::kXSubBytes + b * (kBox * BK * 2), &tmX, &full1[stage],
+                             (st * SUB + sb) * BK, ti.row0 + b * kBox, 0);
         if (++stage == S1) {
           stage = 0;
           phase ^= 1u;
@@ -171,37 +180,41 @@ __global__ void __launch_bounds__(SwapCfg<FP4W>::kThreads, 1)
     int s1 = 0, s2 = 0;
     uint32_t ph1 = 0, ph2 = 0;
     int it = 0;
-    for (int u = blockIdx.x; u < total; u += gridDim.x, ++it) {
+    for (int u = blockIdx.x; u < total; u += gridDim.x) {
       const SwapTile ti = decode_swap(p, u);
       const uint32_t idesc = idesc0 | ((uint32_t)((ti.nb * kBox) >> 3) << 17);  // N = 16 * nb
       const int acc = it & 1;
       const uint32_t use = (uint32_t)(it >> 1);
+      ++it;
       if (!ptx::mbar_wait_bounded(&tmem_empty[acc], (use & 1u) ^ 1u, abort_flag, p.status, p.timeout_ns))
         goto done;
       ptx::tc_fence_after();
-      const uint32_t d_tmem = tmem_base + (uint32_t)(acc * kMaxN);
-      for (int kb = 0; kb < p.num_kb; ++kb) {
-        if (FP4W && !ptx::mbar_wait_bounded(&full2[s2], ph2, abort_flag, p.status, p.timeout_ns)) goto done;
+      const uint32_t d_tmem = tmem_base + (uint32_t)(acc * MAXN);
+      for (int st = 0; st < num_st; ++st) {
         if (!ptx::mbar_wait_bounded(&full1[s1], ph1, abort_flag, p.status, p.timeout_ns)) goto done;
-        ptx::tc_fence_after();
         const uint32_t st_addr = ptx::smem_addr(smem + s1 * C::kStage1Bytes);
-        const uint32_t a_addr = FP4W ? ptx::smem_addr(ring2 + s2 * C::kAConvBytes) : st_addr;
-        const uint32_t b_addr = st_addr + C::kARawBytes;
 #pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk)
-          ptx::mma_f16(d_tmem, ptx::sw128_kmajor_desc(a_addr + kk * 32), ptx::sw128_kmajor_desc(b_addr + kk * 32),
-                       idesc, (kb | kk) != 0 ? 1u : 0u);
+        for (int sb = 0; sb < SUB; ++sb) {
+          if (FP4W && !ptx::mbar_wait_bounded(&full2[s2], ph2, abort_flag, p.status, p.timeout_ns)) goto done;
+          ptx::tc_fence_after();
+          const uint32_t a_addr = FP4W ? ptx::smem_addr(ring2 + s2 * C::kAConvBytes) : st_addr;
+          const uint32_t b_addr = st_addr + C::kWStageBytes + sb * C::kXSubBytes;
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk)
+            ptx::mma_f16(d_tmem, ptx::sw128_kmajor_desc(a_addr + kk * 32),
+                         ptx::sw128_kmajor_desc(b_addr + kk * 32), idesc, (st | sb | kk) != 0 ? 1u : 0u);
+          if (FP4W) {
+            ptx::mma_commit(&empty2[s2]);
+            if (++s2 == S2) {
+              s2 = 0;
+              ph2 ^= 1u;
+            }
+          }
+        }
         ptx::mma_commit(&empty1[s1]);
         if (++s1 == S1) {
           s1 = 0;
           ph1 ^= 1u;
-        }
-        if (FP4W) {
-          ptx::mma_commit(&empty2[s2]);
-          if (++s2 == S2) {
-            s2 = 0;
-            ph2 ^= 1u;
-          }
         }
       }
       ptx::mma_commit(&tmem_full[acc]);
@@ -210,16 +223,17 @@ __global__ void __launch_bounds__(SwapCfg<FP4W>::kThreads, 1)
     // ------------------------------------------------------------------ epilogue (transposed)
     const int q = warp & 3;
     int it = 0;
-    for (int u = blockIdx.x; u < total; u += gridDim.x, ++it) {
+    for (int u = blockIdx.x; u < total; u += gridDim.x) {
       const SwapTile ti = decode_swap(p, u);
       const int acc = it & 1;
       const uint32_t use = (uint32_t)(it >> 1);
+      ++it;
       int ok = 1;
       if (lane == 0) ok = ptx::mbar_wait_bounded(&tmem_full[acc], use & 1u, abort_flag, p.status, p.timeout_ns);
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       ptx::tc_fence_after();
-      const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * kMaxN);
+      const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * MAXN);
       uint16_t* out = static_cast<uint16_t*>(p.C);
       const int col = GLU ? ti.wt * 64 + 16 * q + (lane & 15) : ti.wt * kWRows + 32 * q + lane;
       for (int ch = 0; ch < ti.nb; ++ch) {
@@ -258,7 +272,7 @@ __global__ void __launch_bounds__(SwapCfg<FP4W>::kThreads, 1)
     // ------------------------------------------------------------------ E2M1 -> fp16 converters
     const int cid = threadIdx.x - kBase;  // 0..255
     const int r = cid >> 1, half = cid & 1;
-    const int kscale = p.num_kb * 2;
+    const int kscale = p.num_kb * 2;     // E8M0 bytes per weight row
     int s1 = 0, s2 = 0;
     uint32_t ph1 = 0, ph2 = 0;
     bool bad = false;
@@ -268,38 +282,46 @@ __global__ void __launch_bounds__(SwapCfg<FP4W>::kThreads, 1)
       const uint4* srow =
           reinterpret_cast<const uint4*>(p.w_scale + ((int64_t)ti.expert * p.w_rows + wrow) * kscale);
       uint4 sc16 = make_uint4(0, 0, 0, 0);
-      for (int kb = 0; kb < p.num_kb; ++kb) {
-        if ((kb & 7) == 0) sc16 = __ldg(srow + (kb >> 3));
+      for (int st = 0; st < num_st; ++st) {
+        if ((st & 1) == 0) sc16 = __ldg(srow + (st >> 1));  // scales of 2 stages (512 elements)
+        // each 64-element sub-block is handed to the MMA as soon as it is converted
         int ok = 1;
-        if (lane == 0) {
-          ok = ptx::mbar_wait_bounded(&full1[s1], ph1, abort_flag, p.status, p.timeout_ns) &&
-               ptx::mbar_wait_bounded(&empty2[s2], ph2 ^ 1u, abort_flag, p.status, p.timeout_ns);
-        }
+        if (lane == 0) ok = ptx::mbar_wait_bounded(&full1[s1], ph1, abort_flag, p.status, p.timeout_ns);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) goto conv_done;
-        {
-          const uint4 qv = *reinterpret_cast<const uint4*>(smem + s1 * C::kStage1Bytes + r * (BK / 2) + half * 16);
-          const int wsel = (kb & 7) >> 1;
-          const uint32_t sw = wsel == 0 ? sc16.x : wsel == 1 ? sc16.y : wsel == 2 ? sc16.z : sc16.w;
-          const uint32_t sb = (sw >> ((kb & 1) * 16 + half * 8)) & 0xFFu;
-          uint32_t o[16];
-          e2m1x32_to_f16(qv, e8m0_to_f16x2(sb, &bad), o);
-          uint8_t* dst = ring2 + s2 * C::kAConvBytes + (r >> 3) * 1024 + (r & 7) * 128;
 #pragma unroll
-          for (int c = 0; c < 4; ++c)
-            *reinterpret_cast<uint4*>(dst + (((4 * half + c) ^ (r & 7)) << 4)) =
-                make_uint4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
+        for (int sb = 0; sb < SUB; ++sb) {
+          ok = 1;
+          if (lane == 0) ok = ptx::mbar_wait_bounded(&empty2[s2], ph2 ^ 1u, abort_flag, p.status, p.timeout_ns);
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) goto conv_done;
+          {
+            // raw rows are 128 bytes with the 128-byte swizzle: chunk j of row r sits at j ^ (r % 8)
+            const int chunk = 2 * sb + half;
+            const uint4 qv =
+                *reinterpret_cast<const uint4*>(smem + s1 * C::kStage1Bytes + r * 128 + ((chunk ^ (r & 7)) << 4));
+            const int byte = 8 * (st & 1) + chunk;  // scale index within the 16-byte vector
+            const int wsel = byte >> 2;
+            const uint32_t sw = wsel == 0 ? sc16.x : wsel == 1 ? sc16.y : wsel == 2 ? sc16.z : sc16.w;
+            uint32_t o[16];
+            e2m1x32_to_f16(qv, e8m0_to_f16x2((sw >> ((byte & 3) * 8)) & 0xFFu, &bad), o);
+            uint8_t* dst = ring2 + s2 * C::kAConvBytes + (r >> 3) * 1024 + (r & 7) * 128;
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+              *reinterpret_cast<uint4*>(dst + (((4 * half + c) ^ (r & 7)) << 4)) =
+                  make_uint4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(&full2[s2]);
+          if (++s2 == S2) {
+            s2 = 0;
+            ph2 ^= 1u;
+          }
         }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&full2[s2]);
         if (++s1 == S1) {
           s1 = 0;
           ph1 ^= 1u;
-        }
-        if (++s2 == S2) {
-          s2 = 0;
-          ph2 ^= 1u;
         }
       }
     }
@@ -340,31 +362,31 @@ cudaError_t launch_tc_swap(const TcSwap& g, uint32_t* status, uint64_t timeout_n
   if (glu ? (g.glu_h % 64 || g.out_features != g.glu_h) : g.out_features % kWRows) return cudaErrorInvalidValue;
   if (fp4 && !g.ab_f16) return cudaErrorInvalidValue;
   CUtensorMap mw, mx;
-  if (!(fp4 ? make_map_fp4(&mw, g.w, kBox) : make_map(&mw, g.w, kBox))) return cudaErrorInvalidValue;
+  if (!(fp4 ? make_map_fp4(&mw, g.w, kBox, BK * SwapCfg<true>::kSub / 2, /*swizzle128=*/true)
+            : make_map(&mw, g.w, kBox)))
+    return cudaErrorInvalidValue;
   if (!make_map(&mx, g.act, kBox)) return cudaErrorInvalidValue;
   SwapParams p = {};
   p.num_kb = g.K / BK;
   p.num_wt = glu ? g.glu_h / 64 : g.out_features / kWRows;
   p.glu_h = glu ? g.glu_h : 0;
   p.w_rows = (int)g.w.rows;
-  p.tiles = g.tiles;
-  p.num_tiles = g.num_tiles;
-  p.offsets = g.offsets;
+  p.tiles_s = g.tiles_s;
+  p.num_tiles_s = g.num_tiles_s;
   p.C = g.C;
   p.ldc = g.ldc;
   p.row_scale = g.row_scale;
   p.w_scale = g.w_scale;
   p.status = status;
   p.timeout_ns = timeout_ns;
-  const long long units = (long long)g.max_tiles * p.num_wt;
+  const long long units = (long long)g.max_tiles_s * p.num_wt;
   if (units == 0) return cudaSuccess;
   const int grid = (int)(units < num_sms ? units : num_sms);
   if (fp4) {
     return glu ? launch_swap_inst<true, true, true, true>(mw, mx, p, grid, s)
                : launch_swap_inst<false, true, true, true>(mw, mx, p, grid, s);
   }
-  if (g.ab_f16) return cudaErrorInvalidValue;
-  if (out_f16) return cudaErrorInvalidValue;
+  if (g.ab_f16 || out_f16) return cudaErrorInvalidValue;
   return glu ? launch_swap_inst<true, false, false, false>(mw, mx, p, grid, s)
              : launch_swap_inst<false, false, false, false>(mw, mx, p, grid, s);
 }

@@ -41,8 +41,8 @@ constexpr int kBaseThreads = 192;                   // producer, MMA, 4 epilogue
 
 template <int BN, bool FP4B>
 struct Cfg {
-  static constexpr int kS1 = FP4B ? 6 : 4;                       // TMA ring stages
-  static constexpr int kS2 = FP4B ? 2 : 0;                       // converted-B ring stages
+  static constexpr int kS1 = FP4B ? 5 : 4;                       // TMA ring stages
+  static constexpr int kS2 = FP4B ? 3 : 0;                       // converted-B ring stages
   static constexpr uint32_t kABytes = BM * BK * 2;               // 16 KB
   static constexpr uint32_t kBBytes = BN * BK * 2;               // 32 KB (16-bit B tile)
   static constexpr uint32_t kBRawBytes = BN * BK / 2;            // 8 KB (packed E2M1)
@@ -305,63 +305,91 @@ __global__ void __launch_bounds__(Cfg<BN, FP4B>::kThreads, 1)
     }
   } else if (FP4B && warp >= 6) {
     // ------------------------------------------------------------------ E2M1 -> fp16 converters
-    const int r = threadIdx.x - kBaseThreads;  // B tile row handled by this thread
-    const int kscale = p.num_kb * 2;           // E8M0 bytes per B row (K / 32)
+    // Thread i converts one 32-element scale block (half i%2 of the k-block) of B rows i/2 and
+    // i/2 + 128; consecutive threads read consecutive 16-byte chunks.  Each k-block is handed to
+    // the MMA as soon as it is converted.
+    constexpr int G = 1;
+    const int cid = threadIdx.x - kBaseThreads;  // 0..255
+    const int half = cid & 1;
+    const int rows[2] = {cid >> 1, (cid >> 1) + kBoxRows};
+    const int kscale = p.num_kb * 2;  // E8M0 bytes per B row (K / 32)
     int s1 = 0, s2 = 0;
     uint32_t ph1 = 0, ph2 = 0;
     bool bad = false;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
       const Tile ti = decode_tile<BN_OUT, GROUPED>(p, t);
-      int brow, bgrp;
-      if (GLU) {
-        bgrp = ti.group + ti.n0 / p.glu_h;
-        const int j0 = ti.n0 % p.glu_h;
-        brow = r < kBoxRows ? j0 + r : p.glu_h + j0 + (r - kBoxRows);
-      } else {
-        bgrp = ti.group;
-        brow = ti.n0 + r;
+      const uint4* srow[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int r = rows[h];
+        int brow, bgrp;
+        if (GLU) {
+          bgrp = ti.group + ti.n0 / p.glu_h;
+          const int j0 = ti.n0 % p.glu_h;
+          brow = r < kBoxRows ? j0 + r : p.glu_h + j0 + (r - kBoxRows);
+        } else {
+          bgrp = ti.group;
+          brow = ti.n0 + r;
+        }
+        srow[h] = reinterpret_cast<const uint4*>(p.b_scale + ((int64_t)bgrp * p.b_rows + brow) * kscale);
       }
-      const uint4* srow = reinterpret_cast<const uint4*>(p.b_scale + ((int64_t)bgrp * p.b_rows + brow) * kscale);
-      uint4 sc16 = make_uint4(0, 0, 0, 0);
-      for (int kb = 0; kb < p.num_kb; ++kb) {
-        if ((kb & 7) == 0) sc16 = __ldg(srow + (kb >> 3));  // scales of 8 k-blocks (512 elements)
+      uint4 sc16[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+      for (int kb0 = 0; kb0 < p.num_kb; kb0 += G) {  // num_kb % 8 == 0
+        if ((kb0 & 7) == 0) {
+          sc16[0] = __ldg(srow[0] + (kb0 >> 3));  // scales of 8 k-blocks (512 elements)
+          sc16[1] = __ldg(srow[1] + (kb0 >> 3));
+        }
+        int gs1[G], gs2[G];
+        uint32_t gp1[G], gp2[G];
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          gs1[g] = s1;
+          gp1[g] = ph1;
+          gs2[g] = s2;
+          gp2[g] = ph2;
+          if (++s1 == S1) {
+            s1 = 0;
+            ph1 ^= 1u;
+          }
+          if (++s2 == S2) {
+            s2 = 0;
+            ph2 ^= 1u;
+          }
+        }
         int ok = 1;
         if (lane == 0) {
-          ok = ptx::mbar_wait_bounded(&full1[s1], ph1, abort_flag, p.status, p.timeout_ns) &&
-               ptx::mbar_wait_bounded(&empty2[s2], ph2 ^ 1u, abort_flag, p.status, p.timeout_ns);
+#pragma unroll
+          for (int g = 0; g < G; ++g)
+            ok = ok && ptx::mbar_wait_bounded(&full1[gs1[g]], gp1[g], abort_flag, p.status, p.timeout_ns) &&
+                 ptx::mbar_wait_bounded(&empty2[gs2[g]], gp2[g] ^ 1u, abort_flag, p.status, p.timeout_ns);
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) goto conv_done;
-        {
-          const uint8_t* braw = smem + s1 * C::kStage1Bytes + C::kABytes + r * (BK / 2);
-          const uint4 q0 = *reinterpret_cast<const uint4*>(braw);
-          const uint4 q1 = *reinterpret_cast<const uint4*>(braw + 16);
-          const int wsel = (kb & 7) >> 1;
-          const uint32_t sw = wsel == 0 ? sc16.x : wsel == 1 ? sc16.y : wsel == 2 ? sc16.z : sc16.w;
-          const uint32_t sb0 = (sw >> ((kb & 1) * 16)) & 0xFFu, sb1 = (sw >> ((kb & 1) * 16 + 8)) & 0xFFu;
-          uint32_t o0[16], o1[16];
-          e2m1x32_to_f16(q0, e8m0_to_f16x2(sb0, &bad), o0);
-          e2m1x32_to_f16(q1, e8m0_to_f16x2(sb1, &bad), o1);
-          uint8_t* dst = ring2 + s2 * C::kBBytes + (r >> 3) * 1024 + (r & 7) * 128;
 #pragma unroll
-          for (int c = 0; c < 4; ++c)
-            *reinterpret_cast<uint4*>(dst + ((c ^ (r & 7)) << 4)) =
-                make_uint4(o0[4 * c], o0[4 * c + 1], o0[4 * c + 2], o0[4 * c + 3]);
+        for (int g = 0; g < G; ++g) {
+          const int kb = kb0 + g;
+          const int byte = (kb & 7) * 2 + half;  // scale index within the 16-byte vector
+          const int wsel = byte >> 2;
 #pragma unroll
-          for (int c = 0; c < 4; ++c)
-            *reinterpret_cast<uint4*>(dst + (((c + 4) ^ (r & 7)) << 4)) =
-                make_uint4(o1[4 * c], o1[4 * c + 1], o1[4 * c + 2], o1[4 * c + 3]);
+          for (int h = 0; h < 2; ++h) {
+            const int r = rows[h];
+            const uint4 qv =
+                *reinterpret_cast<const uint4*>(smem + gs1[g] * C::kStage1Bytes + C::kABytes + r * (BK / 2) + half * 16);
+            const uint32_t sw = wsel == 0 ? sc16[h].x : wsel == 1 ? sc16[h].y : wsel == 2 ? sc16[h].z : sc16[h].w;
+            uint32_t o[16];
+            e2m1x32_to_f16(qv, e8m0_to_f16x2((sw >> ((byte & 3) * 8)) & 0xFFu, &bad), o);
+            uint8_t* dst = ring2 + gs2[g] * C::kBBytes + (r >> 3) * 1024 + (r & 7) * 128;
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+              *reinterpret_cast<uint4*>(dst + (((4 * half + c) ^ (r & 7)) << 4)) =
+                  make_uint4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
+          }
         }
         fence_proxy_async_smem();  // generic-proxy writes -> visible to the tensor cores
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&full2[s2]);
-        if (++s1 == S1) {
-          s1 = 0;
-          ph1 ^= 1u;
-        }
-        if (++s2 == S2) {
-          s2 = 0;
-          ph2 ^= 1u;
+        if (lane == 0) {
+#pragma unroll
+          for (int g = 0; g < G; ++g) ptx::mbar_arrive(&full2[gs2[g]]);
         }
       }
     }

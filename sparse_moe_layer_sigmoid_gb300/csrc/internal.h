@@ -33,8 +33,11 @@ constexpr float kRouterLogitMargin = 1e-3f;
 // s = sigmoid(logits), key = s + b, top-k by (key desc, index asc), p = s / sum(s over T_k);
 // membership at the k-th/(k+1)-th boundary is decided on exact fp64 keys when the
 // approximate keys are within the margin.
+// Two kernels: a selection pass that appends tokens with an uncertain boundary to
+// refine_list[T] (count in *refine_count, reset here), and a refinement pass over that list.
 cudaError_t launch_topk(const float* logits, const float* bias, const RouterSrc& src, int T, int E, int k,
-                        int32_t* idx, float* p, cudaStream_t s);
+                        int32_t* idx, float* p, int32_t* refine_list, int32_t* refine_count, int num_sms,
+                        cudaStream_t s);
 // Deterministic expert batches: per-chunk counts, scan, stable (expert, token) rows, the
 // grouped-GEMM M-tile list, and per-row weights.  idx entries outside [0,E) are reported.
 struct DispatchBuffers {
@@ -43,6 +46,8 @@ struct DispatchBuffers {
   int32_t* offsets;       // [E+1]
   int4* tiles;            // [max_tiles]: {expert, first m-tile of expert, m-tiles of expert, 0}
   int32_t* num_tiles;     // [1]
+  int4* tiles_s;          // [T*k/16 + E + 1]: {expert, first row, rows (<= 16), 0}
+  int32_t* num_tiles_s;   // [1]
   int32_t* tok_of_row;    // [T*k]
   int32_t* row_of;        // [T][k]
   float* p_row;           // [T*k]
@@ -126,7 +131,7 @@ struct TcSwap {
   const uint8_t* w_scale;   // E8M0 [E][w_rows][K/32] or nullptr
   int ab_f16;
   int glu_h;
-  const int4* tiles; const int32_t* num_tiles; const int32_t* offsets; int max_tiles;
+  const int4* tiles_s; const int32_t* num_tiles_s; int max_tiles_s;  // 16-row units
   void* C; int64_t ldc;
   const float* row_scale;   // down: routing weight per row
 };

@@ -26,10 +26,13 @@ struct lmoe_handle {
   size_t ws_bytes;
   uint32_t* status;
   float* logits;
+  int32_t* refine_list;   // [T] tokens whose top-k boundary is settled exactly
+  int32_t* refine_count;
   int32_t* idx;
   float* p;
   DispatchBuffers db;
   int max_tiles;
+  int max_tiles_s;
   void* z;
   void* z_perm;  // gathered expert-contiguous rows; reused for the routed down output
   void* a;       // routed GLU activations [T*k][h]
@@ -136,6 +139,8 @@ size_t layout(lmoe_handle* h, uint8_t* base) {
   h->max_tiles = (int)(rows / kTileM + E + 1);
   h->status = reinterpret_cast<uint32_t*>(take(sizeof(uint32_t)));
   h->logits = reinterpret_cast<float*>(take(T * E * 4));
+  h->refine_list = reinterpret_cast<int32_t*>(take(T * 4));
+  h->refine_count = reinterpret_cast<int32_t*>(take(4));
   h->idx = reinterpret_cast<int32_t*>(take(rows * 4));
   h->p = reinterpret_cast<float*>(take(rows * 4));
   h->db.chunk_counts = reinterpret_cast<int32_t*>(take(nchunks * E * 4));
@@ -143,6 +148,9 @@ size_t layout(lmoe_handle* h, uint8_t* base) {
   h->db.offsets = reinterpret_cast<int32_t*>(take((E + 1) * 4));
   h->db.tiles = reinterpret_cast<int4*>(take((size_t)h->max_tiles * 16));
   h->db.num_tiles = reinterpret_cast<int32_t*>(take(4));
+  h->max_tiles_s = (int)(rows / kTileS + E + 1);
+  h->db.tiles_s = reinterpret_cast<int4*>(take((size_t)h->max_tiles_s * 16));
+  h->db.num_tiles_s = reinterpret_cast<int32_t*>(take(4));
   h->db.tok_of_row = reinterpret_cast<int32_t*>(take(rows * 4));
   h->db.row_of = reinterpret_cast<int32_t*>(take(rows * 4));
   h->db.p_row = reinterpret_cast<float*>(take(rows * 4));
@@ -203,9 +211,10 @@ lmoe_status run_routing(lmoe_handle* h, const void* x, int T, const lmoe_weights
                            h->status, h->timeout_ns, h->num_sms, &h->last_launches, s));
     stage_end(h, kStRouter, s);
     const RouterSrc rs{x, c.act, w->w_router, c.router_w, c.d, kRouterLogitMargin};
-    LMOE_TRY(launch_topk(h->logits, w->router_bias, rs, T, c.num_experts, c.top_k, h->idx, h->p, s));
+    LMOE_TRY(launch_topk(h->logits, w->router_bias, rs, T, c.num_experts, c.top_k, h->idx, h->p, h->refine_list,
+                         h->refine_count, h->num_sms, s));
     stage_end(h, kStTopk, s);
-    h->last_launches += 1;
+    h->last_launches += 2;
     idx = h->idx;
     p = h->p;
   }
@@ -284,7 +293,7 @@ lmoe_status run_forward(lmoe_handle* h, const void* x, int T, const lmoe_weights
     g.w = op3d(w->routed_gate_up, c.num_experts, 2 * hdim, l);
     g.w_scale = fp4 ? w->routed_gate_up_scale : nullptr;
     g.ab_f16 = fp4;
-    g.tiles = h->db.tiles; g.num_tiles = h->db.num_tiles; g.offsets = h->db.offsets; g.max_tiles = h->max_tiles;
+    g.tiles_s = h->db.tiles_s; g.num_tiles_s = h->db.num_tiles_s; g.max_tiles_s = h->max_tiles_s;
     g.C = h->a; g.ldc = hdim;
     LMOE_TRY(launch_tc_swap(g, h->status, h->timeout_ns, h->num_sms, s));
     stage_end(h, kStGlu, s);
@@ -296,7 +305,7 @@ lmoe_status run_forward(lmoe_handle* h, const void* x, int T, const lmoe_weights
     dn.w = op3d(w->routed_down, c.num_experts, l, hdim);
     dn.w_scale = fp4 ? w->routed_down_scale : nullptr;
     dn.ab_f16 = fp4;
-    dn.tiles = h->db.tiles; dn.num_tiles = h->db.num_tiles; dn.offsets = h->db.offsets; dn.max_tiles = h->max_tiles;
+    dn.tiles_s = h->db.tiles_s; dn.num_tiles_s = h->db.num_tiles_s; dn.max_tiles_s = h->max_tiles_s;
     dn.C = o; dn.ldc = l; dn.row_scale = h->db.p_row;
     LMOE_TRY(launch_tc_swap(dn, h->status, h->timeout_ns, h->num_sms, s));
     stage_end(h, kStDown, s);

@@ -74,6 +74,7 @@ __device__ void dots_df(const TX* x, const TW* w, int64_t d, const int (&ce)[kCa
   DF acc[kCandBatch];
 #pragma unroll
   for (int m = 0; m < kCandBatch; ++m) acc[m] = DF{0.f, 0.f};
+#pragma unroll 2
   for (int c = lane * 8; c < d; c += 32 * 8) {  // d % 16 == 0 and 16-byte aligned rows
     float xf[8];
     load8(x + c, xf);
@@ -116,6 +117,41 @@ __device__ void exact_logits(const RouterSrc& r, int t, const int (&ce)[kCandBat
     dots_df(static_cast<const float*>(r.x) + xo, static_cast<const float*>(r.w), r.d, ce, nc, lane, out);
 }
 
+struct Refined {
+  double key;  // exact s + b
+  float s;     // s rounded to fp32
+};
+
+// Exact keys of the candidate experts lane + 32*slot for the lanes set in `m` (one warp, all
+// lanes call it); each candidate lane receives its own key.
+__device__ __noinline__ Refined refine_slot(const RouterSrc src, const float* __restrict__ bias, int t, int slot,
+                                            uint32_t m, int lane) {
+  Refined out{-INFINITY, 0.f};
+  int ce[kCandBatch];
+  int nc = 0;
+  while (m) {
+    const int src_lane = __ffs(m) - 1;
+    m &= m - 1;
+#pragma unroll
+    for (int q = 0; q < kCandBatch; ++q)
+      if (q == nc) ce[q] = src_lane + 32 * slot;
+    if (++nc == kCandBatch || m == 0) {
+      double lg[kCandBatch];
+      exact_logits(src, t, ce, nc, lane, lg);
+#pragma unroll
+      for (int q = 0; q < kCandBatch; ++q) {
+        if (q < nc && lane == (ce[q] & 31)) {
+          const double s64 = 1.0 / (1.0 + exp(-lg[q]));
+          out.key = s64 + (bias ? (double)bias[ce[q]] : 0.0);
+          out.s = (float)s64;
+        }
+      }
+      nc = 0;
+    }
+  }
+  return out;
+}
+
 // One warp per token.  Keys s + b are packed as (orderable(key) << 32) | (~expert) so that the
 // 64-bit maximum is the largest key and, among equal keys, the lowest expert index.
 //
@@ -126,13 +162,12 @@ __device__ void exact_logits(const RouterSrc& r, int t, const int (&ce)[kCandBat
 // slots are filled from those keys (ties to the lower index).  Experts above the
 // band are in for certain, experts below it out.  The output lists the certain experts in
 // descending key order, then the refined winners in descending exact-key order.
-template <int NPL>
-__global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ logits,
-                                                   const float* __restrict__ bias, RouterSrc src, int T, int E,
-                                                   int k, int32_t* __restrict__ idx, float* __restrict__ p) {
-  const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (t >= T) return;
+// Selection for token t by one warp.  Without REFINE, a token whose boundary is not certain is
+// left unwritten and the function returns true; with REFINE its boundary is settled exactly.
+template <int NPL, bool REFINE>
+__device__ __forceinline__ bool topk_token(const float* __restrict__ logits, const float* __restrict__ bias,
+                                           const RouterSrc& src, int t, int E, int k, int32_t* __restrict__ idx,
+                                           float* __restrict__ p, int lane) {
   const float* row = logits + (size_t)t * E;
   float kf[NPL], sv[NPL];
   uint32_t taken = 0;
@@ -192,46 +227,25 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ log
 
   const float eta = 0.25f * src.margin + 1e-6f;
   if (k < E && a_k - a_k1 < 2.0f * eta) {
+    if (!REFINE) return true;
     const float hi = a_k + 2.0f * eta, lo = a_k1 - 2.0f * eta;
     const int n_cert = __popc(__ballot_sync(0xffffffffu, lane < k && my_kf > hi));  // ranks 0..n_cert-1
     double ex[NPL];
 #pragma unroll
     for (int i = 0; i < NPL; ++i) ex[i] = -INFINITY;
-    // candidates in warp-uniform batches: exact logits, then the owner lane stores the key
-    int ce[kCandBatch];
-    int nc = 0;
-    auto flush = [&]() {
-      double lg[kCandBatch];
-      exact_logits(src, t, ce, nc, lane, lg);
-#pragma unroll
-      for (int m = 0; m < kCandBatch; ++m) {
-        if (m < nc && lane == (ce[m] & 31)) {
-          const double s64 = 1.0 / (1.0 + exp(-lg[m]));
-          const double key = s64 + (bias ? (double)bias[ce[m]] : 0.0);
-#pragma unroll
-          for (int i = 0; i < NPL; ++i)
-            if (i == (ce[m] >> 5)) {
-              ex[i] = key;
-              sv[i] = (float)s64;
-            }
-        }
-      }
-      nc = 0;
-    };
+    // exact keys for every expert in the band, slot by slot
 #pragma unroll
     for (int i = 0; i < NPL; ++i) {
       const int e = lane + 32 * i;
-      uint32_t m = __ballot_sync(0xffffffffu, e < E && kf[i] >= lo && kf[i] <= hi);
-      while (m) {
-        const int src_lane = __ffs(m) - 1;
-        m &= m - 1;
-#pragma unroll
-        for (int q = 0; q < kCandBatch; ++q)
-          if (q == nc) ce[q] = src_lane + 32 * i;
-        if (++nc == kCandBatch) flush();
+      const uint32_t m = __ballot_sync(0xffffffffu, e < E && kf[i] >= lo && kf[i] <= hi);
+      if (m) {
+        const Refined rf = refine_slot(src, bias, t, i, m, lane);
+        if ((m >> lane) & 1u) {
+          ex[i] = rf.key;
+          sv[i] = rf.s;
+        }
       }
     }
-    if (nc > 0) flush();
     for (int q = n_cert; q < k; ++q) {
       double bv = -INFINITY;
       int be = 0x7FFFFFFF;
@@ -275,6 +289,33 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ log
     idx[(size_t)t * k + lane] = my_e;
     p[(size_t)t * k + lane] = my_s / sum;
   }
+  return false;
+}
+
+// Pass 1: one warp per token; tokens whose boundary is uncertain go to the refinement list.
+template <int NPL>
+__global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ logits, const float* __restrict__ bias,
+                                                   RouterSrc src, int T, int E, int k, int32_t* __restrict__ idx,
+                                                   float* __restrict__ p, int32_t* __restrict__ refine_list,
+                                                   int32_t* __restrict__ refine_count) {
+  const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (t >= T) return;
+  if (topk_token<NPL, false>(logits, bias, src, t, E, k, idx, p, lane) && lane == 0)
+    refine_list[atomicAdd(refine_count, 1)] = t;  // list order is irrelevant: each token is independent
+}
+
+// Pass 2: the listed tokens, their boundary experts' logits recomputed exactly.
+template <int NPL>
+__global__ void __launch_bounds__(128) topk_refine_kernel(const float* __restrict__ logits,
+                                                          const float* __restrict__ bias, RouterSrc src, int E,
+                                                          int k, int32_t* __restrict__ idx, float* __restrict__ p,
+                                                          const int32_t* __restrict__ refine_list,
+                                                          const int32_t* __restrict__ refine_count) {
+  const int lane = threadIdx.x & 31;
+  const int n = *refine_count;
+  for (int w = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; w < n; w += (gridDim.x * blockDim.x) >> 5)
+    topk_token<NPL, true>(logits, bias, src, refine_list[w], E, k, idx, p, lane);
 }
 
 __global__ void split_bf16x3_kernel(const float* __restrict__ w, int64_t n, __nv_bfloat16* __restrict__ out) {
@@ -331,28 +372,36 @@ __global__ void __launch_bounds__(kDispatchChunk) dispatch_count_kernel(const in
 __global__ void __launch_bounds__(1024) dispatch_scan_kernel(const int32_t* __restrict__ chunk_counts,
                                                              int nchunks, int E, int32_t* __restrict__ chunk_base,
                                                              int32_t* __restrict__ offsets, int4* __restrict__ tiles,
-                                                             int32_t* __restrict__ num_tiles) {
+                                                             int32_t* __restrict__ num_tiles,
+                                                             int4* __restrict__ tiles_s,
+                                                             int32_t* __restrict__ num_tiles_s) {
   __shared__ int s_cnt[1024];
   __shared__ int s_tiles[1024];
+  __shared__ int s_tiles_s[1024];
   const int e = threadIdx.x;
   int total = 0;
   if (e < E)
     for (int c = 0; c < nchunks; ++c) total += chunk_counts[(size_t)c * E + e];
   const int nt = (total + kTileM - 1) / kTileM;
+  const int nts = (total + kTileS - 1) / kTileS;
   s_cnt[e] = total;
   s_tiles[e] = nt;
+  s_tiles_s[e] = nts;
   __syncthreads();
   // Hillis-Steele inclusive scans over 1024 entries (fixed order, integer: exact).
   for (int off = 1; off < 1024; off <<= 1) {
     const int a = e >= off ? s_cnt[e - off] : 0;
     const int b = e >= off ? s_tiles[e - off] : 0;
+    const int c = e >= off ? s_tiles_s[e - off] : 0;
     __syncthreads();
     s_cnt[e] += a;
     s_tiles[e] += b;
+    s_tiles_s[e] += c;
     __syncthreads();
   }
   const int row0 = s_cnt[e] - total;
   const int tile0 = s_tiles[e] - nt;
+  const int tile0s = s_tiles_s[e] - nts;
   if (e < E) {
     offsets[e] = row0;
     int run = row0;
@@ -361,10 +410,13 @@ __global__ void __launch_bounds__(1024) dispatch_scan_kernel(const int32_t* __re
       run += chunk_counts[(size_t)c * E + e];
     }
     for (int j = 0; j < nt; ++j) tiles[tile0 + j] = make_int4(e, tile0, nt, 0);
+    if (tiles_s)
+      for (int j = 0; j < nts; ++j) tiles_s[tile0s + j] = make_int4(e, row0 + kTileS * j, min(kTileS, total - kTileS * j), 0);
   }
   if (e == E - 1) {
     offsets[E] = s_cnt[e];
     *num_tiles = s_tiles[e];
+    if (num_tiles_s) *num_tiles_s = s_tiles_s[e];
   }
 }
 
@@ -475,17 +527,27 @@ cudaError_t launch_split_bf16x3(const float* w, int64_t n, void* out, cudaStream
 }
 
 cudaError_t launch_topk(const float* logits, const float* bias, const RouterSrc& src, int T, int E, int k,
-                        int32_t* idx, float* p, cudaStream_t s) {
+                        int32_t* idx, float* p, int32_t* refine_list, int32_t* refine_count, int num_sms,
+                        cudaStream_t s) {
+  cudaError_t e = cudaMemsetAsync(refine_count, 0, sizeof(int32_t), s);
+  if (e != cudaSuccess) return e;
   const int warps_per_block = 8;
   dim3 grid((T + warps_per_block - 1) / warps_per_block), block(32 * warps_per_block);
+  const int rgrid = 4 * num_sms;
   const int npl = (E + 31) / 32;
-  if (npl <= 1) topk_kernel<1><<<grid, block, 0, s>>>(logits, bias, src, T, E, k, idx, p);
-  else if (npl <= 2) topk_kernel<2><<<grid, block, 0, s>>>(logits, bias, src, T, E, k, idx, p);
-  else if (npl <= 4) topk_kernel<4><<<grid, block, 0, s>>>(logits, bias, src, T, E, k, idx, p);
-  else if (npl <= 8) topk_kernel<8><<<grid, block, 0, s>>>(logits, bias, src, T, E, k, idx, p);
-  else if (npl <= 16) topk_kernel<16><<<grid, block, 0, s>>>(logits, bias, src, T, E, k, idx, p);
-  else if (npl <= 28) topk_kernel<28><<<grid, block, 0, s>>>(logits, bias, src, T, E, k, idx, p);
-  else topk_kernel<32><<<grid, block, 0, s>>>(logits, bias, src, T, E, k, idx, p);
+#define LMOE_TOPK(N)                                                                                     \
+  do {                                                                                                   \
+    topk_kernel<N><<<grid, block, 0, s>>>(logits, bias, src, T, E, k, idx, p, refine_list, refine_count); \
+    topk_refine_kernel<N><<<rgrid, 128, 0, s>>>(logits, bias, src, E, k, idx, p, refine_list, refine_count); \
+  } while (0)
+  if (npl <= 1) LMOE_TOPK(1);
+  else if (npl <= 2) LMOE_TOPK(2);
+  else if (npl <= 4) LMOE_TOPK(4);
+  else if (npl <= 8) LMOE_TOPK(8);
+  else if (npl <= 16) LMOE_TOPK(16);
+  else if (npl <= 28) LMOE_TOPK(28);
+  else LMOE_TOPK(32);
+#undef LMOE_TOPK
   return cudaGetLastError();
 }
 
@@ -495,7 +557,7 @@ cudaError_t launch_dispatch(const int32_t* idx, const float* p, int T, int E, in
   const size_t smem = (size_t)E * kMaskWords * sizeof(uint32_t);
   dispatch_count_kernel<<<nchunks, kDispatchChunk, smem, s>>>(idx, T, E, k, b.chunk_counts, status);
   dispatch_scan_kernel<<<1, 1024, 0, s>>>(b.chunk_counts, nchunks, E, b.chunk_base, b.offsets, b.tiles,
-                                          b.num_tiles);
+                                          b.num_tiles, b.tiles_s, b.num_tiles_s);
   dispatch_scatter_kernel<<<nchunks, kDispatchChunk, smem, s>>>(idx, p, T, E, k, b.chunk_base, b.tok_of_row,
                                                                 b.row_of, b.p_row);
   if (launches) *launches += 3;

@@ -11,8 +11,8 @@
 // Scratch: kScratchBytes in `g_route_scratch`, present on every GPU that loads the library
 // until the process exits.  All calls share it, so calls that overlap on the GPU (different
 // streams, or different host threads without ordering) race and must be serialised by the
-// caller.  Every scratch word a kernel reads is written earlier in the same call, so nothing
-// needs clearing between calls.
+// caller.  The refinement-list counter is reset (cudaMemsetAsync, no allocation) at the start
+// of every call; every other scratch word a kernel reads is written earlier in the same call.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -35,7 +35,7 @@ void* g_scratch_addr[kMaxDevices] = {};
 size_t round256(size_t v) { return (v + 255) / 256 * 256; }
 
 struct ScratchLayout {
-  size_t logits, chunk_counts, chunk_base, tiles, num_tiles, wr_split, total;
+  size_t logits, chunk_counts, chunk_base, tiles, num_tiles, refine_list, refine_count, wr_split, total;
 };
 
 ScratchLayout scratch_layout(int T, int E, int k, size_t wr_split_bytes) {
@@ -47,7 +47,9 @@ ScratchLayout scratch_layout(int T, int E, int k, size_t wr_split_bytes) {
   s.chunk_base = s.chunk_counts + round256(nchunks * E * sizeof(int32_t));
   s.tiles = s.chunk_base + round256(nchunks * E * sizeof(int32_t));
   s.num_tiles = s.tiles + round256(max_tiles * sizeof(int4));
-  s.wr_split = s.num_tiles + 256;
+  s.refine_list = s.num_tiles + 256;
+  s.refine_count = s.refine_list + round256((size_t)T * sizeof(int32_t));
+  s.wr_split = s.refine_count + 256;
   s.total = s.wr_split + round256(wr_split_bytes);
   return s;
 }
@@ -104,6 +106,8 @@ extern "C" lmoe_status latentmoe_route_noalloc(const lmoe_config* cfg, const voi
   db.offsets = expert_offsets;
   db.tiles = reinterpret_cast<int4*>(base + L.tiles);
   db.num_tiles = reinterpret_cast<int32_t*>(base + L.num_tiles);
+  db.tiles_s = nullptr;  // the 16-row list serves only the expert GEMMs
+  db.num_tiles_s = nullptr;
   db.tok_of_row = tok_of_row;
   db.row_of = row_of;
   db.p_row = nullptr;
@@ -116,7 +120,9 @@ extern "C" lmoe_status latentmoe_route_noalloc(const lmoe_config* cfg, const voi
                           nullptr, s) != cudaSuccess)
     return LMOE_ERR_CUDA;
   const lmoe::RouterSrc rs{x, cfg->act, w->w_router, cfg->router_w, d, lmoe::kRouterLogitMargin};
-  if (lmoe::launch_topk(logits, w->router_bias, rs, T, E, k, topk_idx, topk_p, s) != cudaSuccess)
+  if (lmoe::launch_topk(logits, w->router_bias, rs, T, E, k, topk_idx, topk_p,
+                        reinterpret_cast<int32_t*>(base + L.refine_list),
+                        reinterpret_cast<int32_t*>(base + L.refine_count), num_sms, s) != cudaSuccess)
     return LMOE_ERR_CUDA;
   if (lmoe::launch_dispatch(topk_idx, topk_p, T, E, k, db, nullptr, nullptr, s) != cudaSuccess)
     return LMOE_ERR_CUDA;

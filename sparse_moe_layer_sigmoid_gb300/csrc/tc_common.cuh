@@ -100,20 +100,22 @@ inline bool make_map(CUtensorMap* m, const TcOperand& op, int box_rows = 128) {
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Packed E2M1 operand [depth][rows][cols/2 bytes] (element strides in `op`): boxes of 32
-// bytes (64 elements) x box_rows rows, no swizzle.
-inline bool make_map_fp4(CUtensorMap* m, const TcOperand& op, int box_rows = 128) {
+// Packed E2M1 operand [depth][rows][cols/2 bytes] (element strides in `op`): boxes of
+// box_bytes bytes (2 elements per byte) x box_rows rows, no swizzle, or the 128-byte swizzle
+// (box_bytes == 128) when the reader takes column slices of the rows.
+inline bool make_map_fp4(CUtensorMap* m, const TcOperand& op, int box_rows = 128, int box_bytes = BK / 2,
+                         bool swizzle128 = false) {
   EncodeTiledFn enc = encode_fn();
   if (!enc || !op.ptr) return false;
   const int64_t rb = op.row_stride / 2;  // bytes per row
   const int64_t depth_stride = op.depth > 1 ? op.depth_stride / 2 : op.rows * rb;
   cuuint64_t dims[3] = {(cuuint64_t)(op.cols / 2), (cuuint64_t)op.rows, (cuuint64_t)op.depth};
   cuuint64_t strides[2] = {(cuuint64_t)rb, (cuuint64_t)depth_stride};
-  cuuint32_t box[3] = {BK / 2, (cuuint32_t)box_rows, 1};
+  cuuint32_t box[3] = {(cuuint32_t)box_bytes, (cuuint32_t)box_rows, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(op.ptr), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+             CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 
