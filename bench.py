@@ -216,6 +216,8 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default="k3w_e128_bf16_prefill")
     ap.add_argument("--cpu-sample", type=int, default=8, help="token rows for the oracle CPU baseline")
+    ap.add_argument("--single-cta", action="store_true",
+                    help="run every tensor-core GEMM on single CTAs (no CTA-pair GEMMs)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -240,6 +242,7 @@ def main():
 
     import __graft_entry__
     from sparse_moe_layer_sigmoid_gb300 import inputs
+    from sparse_moe_layer_sigmoid_gb300 import binding
     from sparse_moe_layer_sigmoid_gb300.binding import LatentMoE
 
     if rank == 0:
@@ -249,7 +252,7 @@ def main():
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     inp = inputs.make_inputs(cfg, dev)
-    layer = LatentMoE(cfg)
+    layer = LatentMoE(cfg, flags=binding.LMOE_FLAG_SINGLE_CTA_GEMM if args.single_cta else 0)
     layer.enable_stage_timing()
     x = inp["x"]
     y = torch.empty((cfg.tokens, layer.out_width), dtype=x.dtype, device=dev)

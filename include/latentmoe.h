@@ -59,6 +59,10 @@ typedef enum {
  * stops there (no RMSNorm, W_up or shared experts).  Used by the routing/dispatch
  * stress workload. */
 #define LMOE_FLAG_IDENTITY_EXPERTS 0x1u
+/* Run every tensor-core GEMM on single CTAs (128-row tiles) instead of CTA pairs (256-row
+ * tiles, tcgen05 cta_group::2) where the latter would apply.  Same results up to fp32
+ * accumulation order; for comparison and testing. */
+#define LMOE_FLAG_SINGLE_CTA_GEMM 0x2u
 
 typedef struct {
   int32_t d;             /* model width                                                 */

@@ -21,6 +21,7 @@ LMOE_OK, LMOE_ERR_INVALID_ARG, LMOE_ERR_UNSUPPORTED, LMOE_ERR_CUDA, LMOE_ERR_OOM
     LMOE_ERR_DEVICE_CHECK = range(7)
 DTYPES = {"f32": 0, "bf16": 1, "mxfp4": 2}
 LMOE_FLAG_IDENTITY_EXPERTS = 0x1
+LMOE_FLAG_SINGLE_CTA_GEMM = 0x2
 LMOE_NUM_STAGES = 10
 
 
@@ -121,10 +122,10 @@ def _wrap_device_pointer(ptr: int, nbytes: int, dtype, shape):
     return raw.clone().view(dtype).reshape(shape)
 
 
-def make_config(cfg: LayerConfig, max_tokens: int | None = None) -> LmoeConfig:
+def make_config(cfg: LayerConfig, max_tokens: int | None = None, flags: int = 0) -> LmoeConfig:
     return LmoeConfig(cfg.d, cfg.latent, cfg.hidden, cfg.experts, cfg.top_k, cfg.n_shared, cfg.shared_hidden,
                       max_tokens or cfg.tokens, DTYPES[cfg.act], DTYPES[cfg.router_w], DTYPES[cfg.routed_w],
-                      cfg.rms_eps, LMOE_FLAG_IDENTITY_EXPERTS if cfg.identity_experts else 0)
+                      cfg.rms_eps, flags | (LMOE_FLAG_IDENTITY_EXPERTS if cfg.identity_experts else 0))
 
 
 def make_weights(inp: dict) -> LmoeWeights:
@@ -145,10 +146,10 @@ def route_noalloc(cfg: LayerConfig, x, weights: dict, out: dict, stream=None):
 class LatentMoE:
     """One layer instance: a handle with a workspace sized for ``max_tokens`` tokens."""
 
-    def __init__(self, cfg: LayerConfig, max_tokens: int | None = None):
+    def __init__(self, cfg: LayerConfig, max_tokens: int | None = None, flags: int = 0):
         self.cfg = cfg
         self.max_tokens = max_tokens or cfg.tokens
-        self._c = make_config(cfg, self.max_tokens)
+        self._c = make_config(cfg, self.max_tokens, flags)
         h = C.c_void_p()
         _check(_lib().latentmoe_create(C.byref(self._c), C.byref(h)), "latentmoe_create")
         self._h = h

@@ -10,6 +10,15 @@ namespace lmoe {
 // Bits of the device status word.  Kernels OR these in; the host maps them to
 // LMOE_ERR_TIMEOUT / LMOE_ERR_DEVICE_CHECK.
 enum : uint32_t { kStatusTimeout = 1u, kStatusDeviceCheck = 2u };
+// Diagnostic bits naming the wait that ran out (bits 8..15 of the status word).
+enum : uint32_t {
+  kWaitProducer = 1u << 8,    // producer: stage free
+  kWaitAccFree = 1u << 9,     // MMA: accumulator drained
+  kWaitFull = 1u << 10,       // MMA: operands landed
+  kWaitConverted = 1u << 11,  // MMA: converted operands ready
+  kWaitAccFull = 1u << 12,    // epilogue: accumulator complete
+  kWaitMmaDone = 1u << 13     // producer: own MMA finished with a stage (paired CTAs)
+};
 
 enum DType : int { kF32 = 0, kBF16 = 1, kMXFP4 = 2, kF16 = 3 /* internal: fp16 activations */ };
 
@@ -17,6 +26,8 @@ enum DType : int { kF32 = 0, kBF16 = 1, kMXFP4 = 2, kF16 = 3 /* internal: fp16 a
 constexpr int kTileM = 128;
 // Rows of one unit of the swapped-operand (decode) expert GEMM: a second, finer tile list.
 constexpr int kTileS = 16;
+// Rows of the M tile a pair of clustered CTAs shares (each CTA computes 128 of them).
+constexpr int kTileP = 256;
 // Tokens per dispatch chunk (one CTA, one bit per token in the per-expert masks).
 constexpr int kDispatchChunk = 256;
 

@@ -155,7 +155,7 @@ __global__ void __launch_bounds__(SwapCfg<FP4W>::kThreads, 1)
       constexpr uint32_t kWBox = C::kWStageBytes / (kWRows / kBox);  // bytes per weight box
       const uint32_t tx = C::kWStageBytes + (uint32_t)(SUB * ti.nb) * (kBox * BK * 2);
       for (int st = 0; st < num_st; ++st) {
-        if (!ptx::mbar_wait_bounded(&empty1[stage], phase ^ 1u, abort_flag, p.status, p.timeout_ns)) goto done;
+        if (!ptx::mbar_wait_bounded(&empty1[stage], phase ^ 1u, abort_flag, p.status, p.timeout_ns, kWaitProducer)) goto done;
         uint8_t* sW = smem + stage * C::kStage1Bytes;
         uint8_t* sX = sW + C::kWStageBytes;
         ptx::mbar_arrive_expect_tx(&full1[stage], tx);
@@ -186,16 +186,16 @@ __global__ void __launch_bounds__(SwapCfg<FP4W>::kThreads, 1)
       const int acc = it & 1;
       const uint32_t use = (uint32_t)(it >> 1);
       ++it;
-      if (!ptx::mbar_wait_bounded(&tmem_empty[acc], (use & 1u) ^ 1u, abort_flag, p.status, p.timeout_ns))
+      if (!ptx::mbar_wait_bounded(&tmem_empty[acc], (use & 1u) ^ 1u, abort_flag, p.status, p.timeout_ns, kWaitAccFree))
         goto done;
       ptx::tc_fence_after();
       const uint32_t d_tmem = tmem_base + (uint32_t)(acc * MAXN);
       for (int st = 0; st < num_st; ++st) {
-        if (!ptx::mbar_wait_bounded(&full1[s1], ph1, abort_flag, p.status, p.timeout_ns)) goto done;
+        if (!ptx::mbar_wait_bounded(&full1[s1], ph1, abort_flag, p.status, p.timeout_ns, kWaitFull)) goto done;
         const uint32_t st_addr = ptx::smem_addr(smem + s1 * C::kStage1Bytes);
 #pragma unroll
         for (int sb = 0; sb < SUB; ++sb) {
-          if (FP4W && !ptx::mbar_wait_bounded(&full2[s2], ph2, abort_flag, p.status, p.timeout_ns)) goto done;
+          if (FP4W && !ptx::mbar_wait_bounded(&full2[s2], ph2, abort_flag, p.status, p.timeout_ns, kWaitConverted)) goto done;
           ptx::tc_fence_after();
           const uint32_t a_addr = FP4W ? ptx::smem_addr(ring2 + s2 * C::kAConvBytes) : st_addr;
           const uint32_t b_addr = st_addr + C::kWStageBytes + sb * C::kXSubBytes;
@@ -229,7 +229,7 @@ __global__ void __launch_bounds__(SwapCfg<FP4W>::kThreads, 1)
       const uint32_t use = (uint32_t)(it >> 1);
       ++it;
       int ok = 1;
-      if (lane == 0) ok = ptx::mbar_wait_bounded(&tmem_full[acc], use & 1u, abort_flag, p.status, p.timeout_ns);
+      if (lane == 0) ok = ptx::mbar_wait_bounded(&tmem_full[acc], use & 1u, abort_flag, p.status, p.timeout_ns, kWaitAccFull);
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       ptx::tc_fence_after();

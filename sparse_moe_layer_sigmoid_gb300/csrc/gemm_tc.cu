@@ -106,8 +106,6 @@ __global__ void __launch_bounds__(Cfg<BN, FP4B>::kThreads, 1)
                    const __grid_constant__ CUtensorMap tmB1, const TcParams p) {
   using C = Cfg<BN, FP4B>;
   constexpr bool GLU = EPI == kEpiGluBF16 || EPI == kEpiGluF16;
-  constexpr bool SCALE = EPI == kEpiScaleBF16 || EPI == kEpiScaleF16;
-  constexpr bool OUT_F16 = EPI == kEpiF16 || EPI == kEpiGluF16 || EPI == kEpiScaleF16;
   constexpr int BN_OUT = GLU ? BN / 2 : BN;
   constexpr int S1 = C::kS1, S2 = C::kS2 > 0 ? C::kS2 : 1;
 
@@ -161,7 +159,7 @@ __global__ void __launch_bounds__(Cfg<BN, FP4B>::kThreads, 1)
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
       const Tile ti = decode_tile<BN_OUT, GROUPED>(p, t);
       for (int kb = 0; kb < p.num_kb; ++kb) {
-        if (!ptx::mbar_wait_bounded(&empty1[stage], phase ^ 1u, abort_flag, p.status, p.timeout_ns)) goto done;
+        if (!ptx::mbar_wait_bounded(&empty1[stage], phase ^ 1u, abort_flag, p.status, p.timeout_ns, kWaitProducer)) goto done;
         const bool skip = p.inject && first && blockIdx.x == 0;  // test hook: drop one stage signal
         first = false;
         if (!skip) {
@@ -203,13 +201,13 @@ __global__ void __launch_bounds__(Cfg<BN, FP4B>::kThreads, 1)
     for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
       const int acc = it & 1;
       const uint32_t use = (uint32_t)(it >> 1);
-      if (!ptx::mbar_wait_bounded(&tmem_empty[acc], (use & 1u) ^ 1u, abort_flag, p.status, p.timeout_ns))
+      if (!ptx::mbar_wait_bounded(&tmem_empty[acc], (use & 1u) ^ 1u, abort_flag, p.status, p.timeout_ns, kWaitAccFree))
         goto done;
       ptx::tc_fence_after();
       const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
       for (int kb = 0; kb < p.num_kb; ++kb) {
-        if (FP4B && !ptx::mbar_wait_bounded(&full2[s2], ph2, abort_flag, p.status, p.timeout_ns)) goto done;
-        if (!ptx::mbar_wait_bounded(&full1[s1], ph1, abort_flag, p.status, p.timeout_ns)) goto done;
+        if (FP4B && !ptx::mbar_wait_bounded(&full2[s2], ph2, abort_flag, p.status, p.timeout_ns, kWaitConverted)) goto done;
+        if (!ptx::mbar_wait_bounded(&full1[s1], ph1, abort_flag, p.status, p.timeout_ns, kWaitFull)) goto done;
         ptx::tc_fence_after();
         const uint32_t a_addr = ptx::smem_addr(smem + s1 * C::kStage1Bytes);
         const uint32_t b_addr = FP4B ? ptx::smem_addr(ring2 + s2 * C::kBBytes) : a_addr + C::kABytes;
@@ -241,64 +239,14 @@ __global__ void __launch_bounds__(Cfg<BN, FP4B>::kThreads, 1)
       const int acc = it & 1;
       const uint32_t use = (uint32_t)(it >> 1);
       int ok = 1;
-      if (lane == 0) ok = ptx::mbar_wait_bounded(&tmem_full[acc], use & 1u, abort_flag, p.status, p.timeout_ns);
+      if (lane == 0) ok = ptx::mbar_wait_bounded(&tmem_full[acc], use & 1u, abort_flag, p.status, p.timeout_ns, kWaitAccFull);
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       ptx::tc_fence_after();
       const int row = ti.row0 + q * 32 + lane;
       const bool live = row < ti.row_end;
       const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
-      if (GLU) {
-        uint16_t* out = static_cast<uint16_t*>(p.C) + (int64_t)row * p.ldc + ti.n0;
-#pragma unroll 1
-        for (int c = 0; c < BN_OUT; c += 32) {
-          uint32_t g[32], u[32];
-          ptx::tmem_ld_32x32b_x32(t_row + c, g);
-          ptx::tmem_ld_32x32b_x32(t_row + BN_OUT + c, u);
-          ptx::tmem_ld_wait();
-          if (live) {
-            uint32_t packed[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const float a0 = silu(__uint_as_float(g[2 * i])) * __uint_as_float(u[2 * i]);
-              const float a1 = silu(__uint_as_float(g[2 * i + 1])) * __uint_as_float(u[2 * i + 1]);
-              packed[i] = OUT_F16 ? pack_f16x2(a0, a1) : pack_bf16x2(a0, a1);
-            }
-            uint4* dst = reinterpret_cast<uint4*>(out + c);
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-              dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
-          }
-        }
-      } else {
-        const float sc = (SCALE && live) ? p.row_scale[row] : 1.0f;
-#pragma unroll 1
-        for (int c = 0; c < BN; c += 32) {
-          if (ti.n0 + c >= p.N) break;  // ragged last column tile (fp32: N % 4 == 0, else N % 32 == 0)
-          uint32_t r[32];
-          ptx::tmem_ld_32x32b_x32(t_row + c, r);
-          ptx::tmem_ld_wait();
-          if (live) {
-            if (EPI == kEpiF32) {
-              uint4* dst = reinterpret_cast<uint4*>(static_cast<float*>(p.C) + (int64_t)row * p.ldc + ti.n0 + c);
-#pragma unroll
-              for (int i = 0; i < 8; ++i)
-                if (ti.n0 + c + 4 * i < p.N) dst[i] = make_uint4(r[4 * i], r[4 * i + 1], r[4 * i + 2], r[4 * i + 3]);
-            } else {
-              uint32_t packed[16];
-#pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                const float v0 = __uint_as_float(r[2 * i]) * sc, v1 = __uint_as_float(r[2 * i + 1]) * sc;
-                packed[i] = OUT_F16 ? pack_f16x2(v0, v1) : pack_bf16x2(v0, v1);
-              }
-              uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.C) + (int64_t)row * p.ldc + ti.n0 + c);
-#pragma unroll
-              for (int i = 0; i < 4; ++i)
-                dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
-            }
-          }
-        }
-      }
+      store_accumulator<BN, EPI>(t_row, row, live, ti.n0, p.N, p.C, p.ldc, p.row_scale);
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&tmem_empty[acc]);

@@ -48,6 +48,8 @@ struct DispatchBuffers {
   int32_t* num_tiles;     // [1]
   int4* tiles_s;          // [T*k/16 + E + 1]: {expert, first row, rows (<= 16), 0}
   int32_t* num_tiles_s;   // [1]
+  int4* tiles_p;          // [T*k/256 + E + 1]: 256-row tiles, same layout as `tiles` (or nullptr)
+  int32_t* num_tiles_p;   // [1]
   int32_t* tok_of_row;    // [T*k]
   int32_t* row_of;        // [T][k]
   float* p_row;           // [T*k]
@@ -112,6 +114,7 @@ struct TcGemm {
   int a_k_period;         // A's K coordinate wraps every a_k_period columns (0 = K: no wrap)
   int glu_h;              // GLU: rows of B between gate and up; output column j -> (j / glu_h, j % glu_h)
   const int4* tiles; const int32_t* num_tiles; const int32_t* offsets; int max_tiles;  // grouped mode
+  const int4* tiles_p; const int32_t* num_tiles_p; int max_tiles_p;  // grouped, paired CTAs: 256-row tiles
   void* C; int64_t ldc;
   const float* row_scale;
   int ab_f16;                // operands are fp16 (with MXFP4 B) instead of bf16
@@ -119,6 +122,12 @@ struct TcGemm {
 };
 cudaError_t launch_tc_gemm(const TcGemm& g, uint32_t* status, uint64_t timeout_ns, int inject_fault, int num_sms,
                            cudaStream_t s);
+
+// The same GEMM on CTA pairs (gemm_pair.cu): 256 x 256 tiles, tcgen05.mma.cta_group::2.  For
+// bf16 operands with the bf16, GLU and (grouped) scale epilogues; tc_pair_supported says whether
+// `g` qualifies.
+bool tc_pair_supported(const TcGemm& g);
+cudaError_t launch_tc_pair(const TcGemm& g, uint32_t* status, uint64_t timeout_ns, cudaStream_t s);
 
 // Swapped-operand grouped GEMM for experts with few rows (gemm_swap.cu): weights are the
 // 128-row M operand, the tile's token rows (up to 128) the N operand.

@@ -33,6 +33,7 @@ struct lmoe_handle {
   DispatchBuffers db;
   int max_tiles;
   int max_tiles_s;
+  int max_tiles_p;
   void* z;
   void* z_perm;  // gathered expert-contiguous rows; reused for the routed down output
   void* a;       // routed GLU activations [T*k][h]
@@ -100,7 +101,7 @@ lmoe_status validate_config(const lmoe_config& c) {
   if (c.router_w != LMOE_F32 && c.router_w != LMOE_BF16) return LMOE_ERR_INVALID_ARG;
   if (c.routed_w != LMOE_F32 && c.routed_w != LMOE_BF16 && c.routed_w != LMOE_MXFP4) return LMOE_ERR_INVALID_ARG;
   if (!(c.rms_eps >= 0.0f)) return LMOE_ERR_INVALID_ARG;
-  if (c.flags & ~LMOE_FLAG_IDENTITY_EXPERTS) return LMOE_ERR_INVALID_ARG;
+  if (c.flags & ~(LMOE_FLAG_IDENTITY_EXPERTS | LMOE_FLAG_SINGLE_CTA_GEMM)) return LMOE_ERR_INVALID_ARG;
   // router GEMM and the CUDA-core path step K by 16; combine moves 16-byte vectors
   if (c.d % 16 || c.latent % 16) return LMOE_ERR_UNSUPPORTED;
   if (c.act == LMOE_F32) {
@@ -151,6 +152,9 @@ size_t layout(lmoe_handle* h, uint8_t* base) {
   h->max_tiles_s = (int)(rows / kTileS + E + 1);
   h->db.tiles_s = reinterpret_cast<int4*>(take((size_t)h->max_tiles_s * 16));
   h->db.num_tiles_s = reinterpret_cast<int32_t*>(take(4));
+  h->max_tiles_p = (int)(rows / kTileP + E + 1);
+  h->db.tiles_p = reinterpret_cast<int4*>(take((size_t)h->max_tiles_p * 16));
+  h->db.num_tiles_p = reinterpret_cast<int32_t*>(take(4));
   h->db.tok_of_row = reinterpret_cast<int32_t*>(take(rows * 4));
   h->db.row_of = reinterpret_cast<int32_t*>(take(rows * 4));
   h->db.p_row = reinterpret_cast<float*>(take(rows * 4));
@@ -226,6 +230,21 @@ lmoe_status run_routing(lmoe_handle* h, const void* x, int T, const lmoe_weights
   return LMOE_OK;
 }
 
+// A tensor-core GEMM of the layer: on CTA pairs (256-row tiles) when it qualifies and its row
+// groups are tall enough for 256-row tiles to pay, else on single CTAs (128-row tiles).
+cudaError_t run_tc_gemm(lmoe_handle* h, TcGemm g, int inject, cudaStream_t s) {
+  const bool grouped = g.tiles != nullptr;
+  if (grouped) {
+    g.tiles_p = h->db.tiles_p; g.num_tiles_p = h->db.num_tiles_p; g.max_tiles_p = h->max_tiles_p;
+  }
+  // grouped: 256-row tiles pad each expert by up to 255 rows (128-row tiles: 127), so pairs pay
+  // once experts average 1.5 pair tiles
+  const bool tall = grouped ? (int64_t)g.M * 2 >= (int64_t)3 * kTileP * h->cfg.num_experts : g.M >= kTileP;
+  const bool pair = !(h->cfg.flags & LMOE_FLAG_SINGLE_CTA_GEMM) && !inject && tall && tc_pair_supported(g);
+  if (pair) return launch_tc_pair(g, h->status, h->timeout_ns, s);
+  return launch_tc_gemm(g, h->status, h->timeout_ns, inject, h->num_sms, s);
+}
+
 lmoe_status run_forward(lmoe_handle* h, const void* x, int T, const lmoe_weights* w, const int32_t* ext_idx,
                         const float* ext_p, void* y, cudaStream_t s) {
   const lmoe_config& c = h->cfg;
@@ -256,7 +275,7 @@ lmoe_status run_forward(lmoe_handle* h, const void* x, int T, const lmoe_weights
     g.B0 = op2d(w->w_down_proj, l, d);
     g.k0_len = d; g.k0_per_group = d;
     g.C = h->z; g.ldc = l;
-    LMOE_TRY(launch_tc_gemm(g, h->status, h->timeout_ns, 0, h->num_sms, s));
+    LMOE_TRY(run_tc_gemm(h, g, 0, s));
   } else {
     SimtGemm g = {};
     g.A = x; g.lda = d; g.a_dtype = c.act; g.b_dtype = c.act;
@@ -321,7 +340,7 @@ lmoe_status run_forward(lmoe_handle* h, const void* x, int T, const lmoe_weights
     g.k0_len = l; g.k0_per_group = l; g.glu_h = hdim;
     g.tiles = h->db.tiles; g.num_tiles = h->db.num_tiles; g.offsets = h->db.offsets; g.max_tiles = h->max_tiles;
     g.C = h->a; g.ldc = hdim;
-    LMOE_TRY(launch_tc_gemm(g, h->status, h->timeout_ns, h->inject, h->num_sms, s));
+    LMOE_TRY(run_tc_gemm(h, g, h->inject, s));
     h->inject = 0;
     stage_end(h, kStGlu, s);
 
@@ -335,7 +354,7 @@ lmoe_status run_forward(lmoe_handle* h, const void* x, int T, const lmoe_weights
     dn.k0_len = hdim; dn.k0_per_group = hdim;
     dn.tiles = h->db.tiles; dn.num_tiles = h->db.num_tiles; dn.offsets = h->db.offsets; dn.max_tiles = h->max_tiles;
     dn.C = o; dn.ldc = l; dn.row_scale = h->db.p_row;
-    LMOE_TRY(launch_tc_gemm(dn, h->status, h->timeout_ns, 0, h->num_sms, s));
+    LMOE_TRY(run_tc_gemm(h, dn, 0, s));
     stage_end(h, kStDown, s);
   } else {
     SimtGemm g = {};
@@ -370,7 +389,7 @@ lmoe_status run_forward(lmoe_handle* h, const void* x, int T, const lmoe_weights
       g.B0 = op3d(w->shared_gate_up, ns, 2 * hs, d);
       g.k0_len = d; g.k0_per_group = d; g.glu_h = hs;
       g.C = h->act_cat; g.ldc = kcat;
-      LMOE_TRY(launch_tc_gemm(g, h->status, h->timeout_ns, 0, h->num_sms, s));
+      LMOE_TRY(run_tc_gemm(h, g, 0, s));
       stage_end(h, kStSharedGlu, s);
       h->last_launches += 1;
     }
@@ -388,7 +407,7 @@ lmoe_status run_forward(lmoe_handle* h, const void* x, int T, const lmoe_weights
       f.k0_len = l; f.k0_per_group = l;
     }
     f.C = y; f.ldc = d;
-    LMOE_TRY(launch_tc_gemm(f, h->status, h->timeout_ns, 0, h->num_sms, s));
+    LMOE_TRY(run_tc_gemm(h, f, 0, s));
     stage_end(h, kStFinal, s);
     h->last_launches += 1;
   } else {

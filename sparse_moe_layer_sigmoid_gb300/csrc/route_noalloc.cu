@@ -108,6 +108,8 @@ extern "C" lmoe_status latentmoe_route_noalloc(const lmoe_config* cfg, const voi
   db.num_tiles = reinterpret_cast<int32_t*>(base + L.num_tiles);
   db.tiles_s = nullptr;  // the 16-row list serves only the expert GEMMs
   db.num_tiles_s = nullptr;
+  db.tiles_p = nullptr;
+  db.num_tiles_p = nullptr;
   db.tok_of_row = tok_of_row;
   db.row_of = row_of;
   db.p_row = nullptr;

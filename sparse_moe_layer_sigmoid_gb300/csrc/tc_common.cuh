@@ -1,5 +1,5 @@
-// Helpers shared by the tcgen05 GEMM kernels: tensor-map encoding (TMA descriptors) and the
-// in-shared-memory E2M1 -> fp16 conversion of MXFP4 weights.
+// Helpers shared by the tcgen05 GEMM kernels: tensor-map encoding (TMA descriptors), the
+// in-shared-memory E2M1 -> fp16 conversion of MXFP4 weights, and the accumulator epilogue.
 #pragma once
 
 #include <cuda.h>
@@ -67,6 +67,69 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// Epilogue of one warp over a 128 x BN fp32 accumulator: `t_row` addresses the warp's 32 TMEM
+// lanes (one output row each, row `row` of C, stored only when `live`).  GLU epilogues read gate
+// columns [0, BN/2) and up columns [BN/2, BN) and store BN/2 outputs SiLU(gate) * up; the
+// others store columns n0 .. n0+BN-1 (clipped at N) of acc, times row_scale[row] for kEpiScale*.
+template <int BN, int EPI>
+__device__ __forceinline__ void store_accumulator(uint32_t t_row, int row, bool live, int n0, int N, void* C,
+                                                  int64_t ldc, const float* row_scale) {
+  constexpr bool GLU = EPI == kEpiGluBF16 || EPI == kEpiGluF16;
+  constexpr bool SCALE = EPI == kEpiScaleBF16 || EPI == kEpiScaleF16;
+  constexpr bool OUT_F16 = EPI == kEpiF16 || EPI == kEpiGluF16 || EPI == kEpiScaleF16;
+  constexpr int BN_OUT = GLU ? BN / 2 : BN;
+  if (GLU) {
+    uint16_t* out = static_cast<uint16_t*>(C) + (int64_t)row * ldc + n0;
+#pragma unroll 1
+    for (int c = 0; c < BN_OUT; c += 32) {
+      uint32_t g[32], u[32];
+      ptx::tmem_ld_32x32b_x32(t_row + c, g);
+      ptx::tmem_ld_32x32b_x32(t_row + BN_OUT + c, u);
+      ptx::tmem_ld_wait();
+      if (live) {
+        uint32_t packed[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float a0 = silu(__uint_as_float(g[2 * i])) * __uint_as_float(u[2 * i]);
+          const float a1 = silu(__uint_as_float(g[2 * i + 1])) * __uint_as_float(u[2 * i + 1]);
+          packed[i] = OUT_F16 ? pack_f16x2(a0, a1) : pack_bf16x2(a0, a1);
+        }
+        uint4* dst = reinterpret_cast<uint4*>(out + c);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+      }
+    }
+  } else {
+    const float sc = (SCALE && live) ? row_scale[row] : 1.0f;
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 32) {
+      if (n0 + c >= N) break;  // ragged last column tile (fp32: N % 4 == 0, else N % 32 == 0)
+      uint32_t r[32];
+      ptx::tmem_ld_32x32b_x32(t_row + c, r);
+      ptx::tmem_ld_wait();
+      if (live) {
+        if (EPI == kEpiF32) {
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<float*>(C) + (int64_t)row * ldc + n0 + c);
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            if (n0 + c + 4 * i < N) dst[i] = make_uint4(r[4 * i], r[4 * i + 1], r[4 * i + 2], r[4 * i + 3]);
+        } else {
+          uint32_t packed[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float v0 = __uint_as_float(r[2 * i]) * sc, v1 = __uint_as_float(r[2 * i + 1]) * sc;
+            packed[i] = OUT_F16 ? pack_f16x2(v0, v1) : pack_bf16x2(v0, v1);
+          }
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(C) + (int64_t)row * ldc + n0 + c);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+        }
+      }
+    }
+  }
+}
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,

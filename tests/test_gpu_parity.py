@@ -51,6 +51,10 @@ SMALL_CASES = [
     replace(SMALL_BF16, name="small_bf16_decode_skew", tokens=150, top_k=2, bias="normal1.5", seed=37),
     replace(SMALL_BF16, name="small_mxfp4_decode", routed_w="mxfp4", latent=512, hidden=512, experts=24, tokens=40,
             seed=38),
+    # >= 256 rows per expert on average: routed GEMMs on CTA pairs (256-row tiles), ragged counts
+    replace(SMALL_BF16, name="small_bf16_pair_skew", tokens=700, experts=8, bias="normal1.5", seed=39),
+    replace(SMALL_BF16, name="small_bf16_pair_wide", tokens=600, d=1024, latent=512, hidden=384, experts=4,
+            top_k=2, n_shared=1, shared_hidden=384, seed=40),
 ]
 
 
@@ -162,6 +166,26 @@ def test_token_permutation_is_bitwise_invariant(binding):
     y3 = layer.forward(inp["x"], inp)
     assert torch.equal(y3, y)  # run-to-run determinism
     layer.close()
+
+
+@pytest.mark.parametrize("cfg", [SMALL_BF16, replace(SMALL_BF16, name="pair_grouped", tokens=700, experts=8,
+                                                      bias="normal1.5", seed=41)], ids=lambda c: c.name)
+def test_cta_pair_gemms_match_single_cta(binding, cfg):
+    """CTA-pair GEMMs (256-row tiles) and single-CTA GEMMs (128-row tiles) accumulate every output
+    over the same K order in fp32: the layer outputs agree to fp32 rounding of the stored value."""
+    dev = torch.device("cuda")
+    inp = device_inputs(cfg, dev, False)
+    pair = binding.LatentMoE(cfg)
+    single = binding.LatentMoE(cfg, flags=binding.LMOE_FLAG_SINGLE_CTA_GEMM)
+    y_pair = pair.forward(inp["x"], inp)
+    y_single = single.forward(inp["x"], inp)
+    assert pair.status() == 0 and single.status() == 0
+    diff = (y_pair.float() - y_single.float()).abs().max().item()
+    same = torch.equal(y_pair, y_single)
+    print(f"{cfg.name}: bitwise equal={same} max abs diff={diff:.3e}")
+    assert_close(to_np(y_pair), to_np(y_single).astype(np.float64), 1e-5, "pair vs single")
+    pair.close()
+    single.close()
 
 
 def test_forward_host_matches_device_path(binding):
