@@ -45,7 +45,7 @@ struct PairParams {
   int num_kb, kb0, kb0_per_group;
   int glu_h;
   int num_m_tiles, num_n_tiles;  // dense mode: 256-row tiles
-  const int4* tiles;             // grouped mode: 256-row tile list {expert, first tile, tiles, 0}
+  const int4* tiles;             // grouped mode: 256-row tile list {expert, first tile, tiles, first row}
   const int32_t* num_tiles;
   const int32_t* offsets;
   void* C;
@@ -59,6 +59,37 @@ struct PairTile {
   int row0, row_end, n0, group;  // row0: first of the tile's 256 rows
 };
 
+// TMA coordinates of this CTA's boxes for k-block kb of a tile: A rows, and its half of B (the
+// even CTA takes B rows n0..n0+127 or, for GLU, the gate rows; the odd CTA the next 128 rows or
+// the matching up rows).  `second` selects the tensor map of the K range after kb0.
+struct Boxes {
+  int ax, ay;
+  int bx, by, bz;
+  bool second;
+};
+__device__ __forceinline__ Boxes boxes_for(const PairParams& p, const PairTile& ti, int kb, int rank, bool glu) {
+  Boxes b;
+  b.ax = kb * BK;
+  b.ay = ti.row0 + rank * kRows;
+  b.second = false;
+  if (glu) {
+    b.bx = kb * BK;
+    b.by = rank * p.glu_h + ti.n0 % p.glu_h;
+    b.bz = ti.group + ti.n0 / p.glu_h;
+  } else if (kb < p.kb0) {
+    const int goff = kb / p.kb0_per_group;
+    b.bx = (kb - goff * p.kb0_per_group) * BK;
+    b.by = ti.n0 + rank * kRows;
+    b.bz = ti.group + goff;
+  } else {
+    b.bx = (kb - p.kb0) * BK;
+    b.by = ti.n0 + rank * kRows;
+    b.bz = 0;
+    b.second = true;
+  }
+  return b;
+}
+
 template <int BN_OUT, bool GROUPED>
 __device__ __forceinline__ PairTile decode_pair_tile(const PairParams& p, int t) {
   PairTile ti;
@@ -67,7 +98,7 @@ __device__ __forceinline__ PairTile decode_pair_tile(const PairParams& p, int t)
     const int4 tl = p.tiles[q];
     const int local = t - tl.y * p.num_n_tiles;
     const int n = local / tl.z, m = local - n * tl.z;
-    ti.row0 = p.offsets[tl.x] + m * kTileP;
+    ti.row0 = tl.w + m * kTileP;
     ti.row_end = min(ti.row0 + kTileP, p.offsets[tl.x + 1]);
     ti.n0 = n * BN_OUT;
     ti.group = tl.x;
@@ -132,28 +163,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     uint32_t phase = 0;
     for (int t = pair; t < total; t += npairs) {
       const PairTile ti = decode_pair_tile<BN_OUT, GROUPED>(p, t);
-      const int my_row0 = ti.row0 + (int)rank * kRows;
       for (int kb = 0; kb < p.num_kb; ++kb, ++iter) {
-        if (!ptx::mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, p.status, p.timeout_ns,
-                                          kWaitProducer))
+        if (!ptx::mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, p.status, p.timeout_ns, kWaitProducer))
           goto done;
         // the MMA read both CTAs' copy of this stage: pass the release on to the partner
         if (rank == 0 && iter >= kStages) ptx::mbar_arrive_remote(&empty[stage], 1);
         uint8_t* sA = smem + stage * kStageBytes;
-        uint8_t* sB = sA + kHalfBytes;
         const uint32_t bar = ptx::mapa_shared(&full[stage], 0);  // the even CTA's full[stage]
         if (rank == 0) ptx::mbar_arrive_expect_tx(&full[stage], 2 * kStageBytes);
-        ptx::tma_load_3d_pair(sA, &tmA, bar, kb * BK, my_row0, 0);
-        if (GLU) {  // even CTA: gate rows, odd CTA: the matching up rows
-          const int grp = ti.group + ti.n0 / p.glu_h, j0 = ti.n0 % p.glu_h;
-          ptx::tma_load_3d_pair(sB, &tmB0, bar, kb * BK, (int)rank * p.glu_h + j0, grp);
-        } else if (kb < p.kb0) {
-          const int goff = kb / p.kb0_per_group;
-          const int kin = (kb - goff * p.kb0_per_group) * BK;
-          ptx::tma_load_3d_pair(sB, &tmB0, bar, kin, ti.n0 + (int)rank * kRows, ti.group + goff);
-        } else {
-          ptx::tma_load_3d_pair(sB, &tmB1, bar, (kb - p.kb0) * BK, ti.n0 + (int)rank * kRows, 0);
-        }
+        const Boxes bx = boxes_for(p, ti, kb, (int)rank, GLU);
+        ptx::tma_load_3d_pair(sA, &tmA, bar, bx.ax, bx.ay, 0);
+        ptx::tma_load_3d_pair(sA + kHalfBytes, bx.second ? &tmB1 : &tmB0, bar, bx.bx, bx.by, bx.bz);
         if (++stage == kStages) {
           stage = 0;
           phase ^= 1u;
@@ -263,7 +283,7 @@ bool tc_pair_supported(const TcGemm& g) {
   if (g.a_k_period && g.a_k_period != g.K) return false;
   if (g.K % BK || g.k0_len % BK || g.k0_per_group % BK) return false;
   if (glu ? (g.N % (BN / 2) || g.glu_h % kRows) : g.N % 32) return false;
-  if (g.tiles && !g.tiles_p) return false;
+  if (g.tiles && (!g.tiles_p || !g.tiles_t)) return false;
   return g.epi != kEpiScaleBF16 || g.tiles;
 }
 

@@ -86,7 +86,7 @@ __device__ __forceinline__ Tile decode_tile(const TcParams& p, int t) {
     const int4 tl = p.tiles[q];
     const int local = t - tl.y * p.num_n_tiles;
     const int n = local / tl.z, m = local - n * tl.z;
-    ti.row0 = p.offsets[tl.x] + m * BM;
+    ti.row0 = tl.w + m * BM;
     ti.row_end = min(ti.row0 + BM, p.offsets[tl.x + 1]);
     ti.n0 = n * BN_OUT;
     ti.group = tl.x;

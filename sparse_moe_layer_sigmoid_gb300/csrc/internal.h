@@ -44,12 +44,15 @@ struct DispatchBuffers {
   int32_t* chunk_counts;  // [nchunks][E]
   int32_t* chunk_base;    // [nchunks][E]
   int32_t* offsets;       // [E+1]
-  int4* tiles;            // [max_tiles]: {expert, first m-tile of expert, m-tiles of expert, 0}
+  int4* tiles;            // [max_tiles]: {expert, first m-tile of expert, m-tiles of expert, first row}
   int32_t* num_tiles;     // [1]
   int4* tiles_s;          // [T*k/16 + E + 1]: {expert, first row, rows (<= 16), 0}
   int32_t* num_tiles_s;   // [1]
-  int4* tiles_p;          // [T*k/256 + E + 1]: 256-row tiles, same layout as `tiles` (or nullptr)
+  int4* tiles_p;          // [T*k/256 + E + 1]: 256-row tiles, same layout as `tiles` (or nullptr);
+                          // an expert's last <= 128 rows are left to tiles_t
   int32_t* num_tiles_p;   // [1]
+  int4* tiles_t;          // [E]: the 128-row tail tiles tiles_p leaves, same layout (or nullptr)
+  int32_t* num_tiles_t;   // [1]
   int32_t* tok_of_row;    // [T*k]
   int32_t* row_of;        // [T][k]
   float* p_row;           // [T*k]
@@ -115,6 +118,7 @@ struct TcGemm {
   int glu_h;              // GLU: rows of B between gate and up; output column j -> (j / glu_h, j % glu_h)
   const int4* tiles; const int32_t* num_tiles; const int32_t* offsets; int max_tiles;  // grouped mode
   const int4* tiles_p; const int32_t* num_tiles_p; int max_tiles_p;  // grouped, paired CTAs: 256-row tiles
+  const int4* tiles_t; const int32_t* num_tiles_t;                    // grouped: the 128-row tails of tiles_p
   void* C; int64_t ldc;
   const float* row_scale;
   int ab_f16;                // operands are fp16 (with MXFP4 B) instead of bf16

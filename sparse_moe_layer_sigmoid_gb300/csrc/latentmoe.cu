@@ -155,6 +155,8 @@ size_t layout(lmoe_handle* h, uint8_t* base) {
   h->max_tiles_p = (int)(rows / kTileP + E + 1);
   h->db.tiles_p = reinterpret_cast<int4*>(take((size_t)h->max_tiles_p * 16));
   h->db.num_tiles_p = reinterpret_cast<int32_t*>(take(4));
+  h->db.tiles_t = reinterpret_cast<int4*>(take(E * 16));
+  h->db.num_tiles_t = reinterpret_cast<int32_t*>(take(4));
   h->db.tok_of_row = reinterpret_cast<int32_t*>(take(rows * 4));
   h->db.row_of = reinterpret_cast<int32_t*>(take(rows * 4));
   h->db.p_row = reinterpret_cast<float*>(take(rows * 4));
@@ -230,19 +232,27 @@ lmoe_status run_routing(lmoe_handle* h, const void* x, int T, const lmoe_weights
   return LMOE_OK;
 }
 
-// A tensor-core GEMM of the layer: on CTA pairs (256-row tiles) when it qualifies and its row
-// groups are tall enough for 256-row tiles to pay, else on single CTAs (128-row tiles).
-cudaError_t run_tc_gemm(lmoe_handle* h, TcGemm g, int inject, cudaStream_t s) {
+// A tensor-core GEMM of the layer: on CTA pairs (256-row tiles) when it qualifies, else on single
+// CTAs (128-row tiles).  Grouped GEMMs on pairs take two launches: the pairs cover each expert's
+// rows in 256-row tiles except a remainder of at most 128 rows, which a single-CTA launch over
+// the tail list covers, so no expert is padded by more than 127 rows either way.  Returns the
+// number of kernels launched through *launches.
+cudaError_t run_tc_gemm(lmoe_handle* h, TcGemm g, int inject, int* launches, cudaStream_t s) {
   const bool grouped = g.tiles != nullptr;
   if (grouped) {
     g.tiles_p = h->db.tiles_p; g.num_tiles_p = h->db.num_tiles_p; g.max_tiles_p = h->max_tiles_p;
+    g.tiles_t = h->db.tiles_t; g.num_tiles_t = h->db.num_tiles_t;
   }
-  // grouped: 256-row tiles pad each expert by up to 255 rows (128-row tiles: 127), so pairs pay
-  // once experts average 1.5 pair tiles
-  const bool tall = grouped ? (int64_t)g.M * 2 >= (int64_t)3 * kTileP * h->cfg.num_experts : g.M >= kTileP;
+  const bool tall = grouped ? (int64_t)g.M >= (int64_t)kTileM * h->cfg.num_experts : g.M >= kTileP;
   const bool pair = !(h->cfg.flags & LMOE_FLAG_SINGLE_CTA_GEMM) && !inject && tall && tc_pair_supported(g);
-  if (pair) return launch_tc_pair(g, h->status, h->timeout_ns, s);
-  return launch_tc_gemm(g, h->status, h->timeout_ns, inject, h->num_sms, s);
+  *launches += 1;
+  if (!pair) return launch_tc_gemm(g, h->status, h->timeout_ns, inject, h->num_sms, s);
+  cudaError_t e = launch_tc_pair(g, h->status, h->timeout_ns, s);
+  if (e != cudaSuccess || !grouped) return e;
+  TcGemm t = g;
+  t.tiles = g.tiles_t; t.num_tiles = g.num_tiles_t; t.max_tiles = h->cfg.num_experts;
+  *launches += 1;
+  return launch_tc_gemm(t, h->status, h->timeout_ns, 0, h->num_sms, s);
 }
 
 lmoe_status run_forward(lmoe_handle* h, const void* x, int T, const lmoe_weights* w, const int32_t* ext_idx,
@@ -275,7 +285,7 @@ lmoe_status run_forward(lmoe_handle* h, const void* x, int T, const lmoe_weights
     g.B0 = op2d(w->w_down_proj, l, d);
     g.k0_len = d; g.k0_per_group = d;
     g.C = h->z; g.ldc = l;
-    LMOE_TRY(run_tc_gemm(h, g, 0, s));
+    LMOE_TRY(run_tc_gemm(h, g, 0, &h->last_launches, s));
   } else {
     SimtGemm g = {};
     g.A = x; g.lda = d; g.a_dtype = c.act; g.b_dtype = c.act;
@@ -283,12 +293,13 @@ lmoe_status run_forward(lmoe_handle* h, const void* x, int T, const lmoe_weights
     g.M = T; g.N = l; g.K = d;
     g.C = h->z; g.ldc = l; g.c_dtype = c.act;
     LMOE_TRY(launch_simt_gemm(g, s));
+    h->last_launches += 1;
   }
   stage_end(h, kStWDown, s);
   // rows of z into expert-contiguous order
   LMOE_TRY(launch_scatter_rows(h->z, h->z_perm, h->db.row_of, T, k, l, (int)ab, s));
   stage_end(h, kStScatter, s);
-  h->last_launches += 2;
+  h->last_launches += 1;
 
   if (identity) {
     stage_begin(h, kStCombine, s);
@@ -328,6 +339,7 @@ lmoe_status run_forward(lmoe_handle* h, const void* x, int T, const lmoe_weights
     dn.C = o; dn.ldc = l; dn.row_scale = h->db.p_row;
     LMOE_TRY(launch_tc_swap(dn, h->status, h->timeout_ns, h->num_sms, s));
     stage_end(h, kStDown, s);
+    h->last_launches += 2;
   } else if (tc) {
     const bool fp4 = c.routed_w == LMOE_MXFP4;
     TcGemm g = {};
@@ -340,7 +352,7 @@ lmoe_status run_forward(lmoe_handle* h, const void* x, int T, const lmoe_weights
     g.k0_len = l; g.k0_per_group = l; g.glu_h = hdim;
     g.tiles = h->db.tiles; g.num_tiles = h->db.num_tiles; g.offsets = h->db.offsets; g.max_tiles = h->max_tiles;
     g.C = h->a; g.ldc = hdim;
-    LMOE_TRY(run_tc_gemm(h, g, h->inject, s));
+    LMOE_TRY(run_tc_gemm(h, g, h->inject, &h->last_launches, s));
     h->inject = 0;
     stage_end(h, kStGlu, s);
 
@@ -354,7 +366,7 @@ lmoe_status run_forward(lmoe_handle* h, const void* x, int T, const lmoe_weights
     dn.k0_len = hdim; dn.k0_per_group = hdim;
     dn.tiles = h->db.tiles; dn.num_tiles = h->db.num_tiles; dn.offsets = h->db.offsets; dn.max_tiles = h->max_tiles;
     dn.C = o; dn.ldc = l; dn.row_scale = h->db.p_row;
-    LMOE_TRY(run_tc_gemm(h, dn, 0, s));
+    LMOE_TRY(run_tc_gemm(h, dn, 0, &h->last_launches, s));
     stage_end(h, kStDown, s);
   } else {
     SimtGemm g = {};
@@ -374,11 +386,12 @@ lmoe_status run_forward(lmoe_handle* h, const void* x, int T, const lmoe_weights
     dn.C = o; dn.ldc = l; dn.c_dtype = c.act; dn.row_scale = h->db.p_row;
     LMOE_TRY(launch_simt_gemm(dn, s));
     stage_end(h, kStDown, s);
+    h->last_launches += 2;
   }
   // u = sum_j o_j (rank order), n = RMSNorm(u) into the tail columns of act_cat
   LMOE_TRY(launch_combine(o, rt, c.act, h->db.row_of, nullptr, w->rms_gain, c.rms_eps, T, k, l, n_out, kcat, s));
   stage_end(h, kStCombine, s);
-  h->last_launches += 3;
+  h->last_launches += 1;
 
   if (tc) {
     if (ns > 0) {
@@ -389,9 +402,8 @@ lmoe_status run_forward(lmoe_handle* h, const void* x, int T, const lmoe_weights
       g.B0 = op3d(w->shared_gate_up, ns, 2 * hs, d);
       g.k0_len = d; g.k0_per_group = d; g.glu_h = hs;
       g.C = h->act_cat; g.ldc = kcat;
-      LMOE_TRY(run_tc_gemm(h, g, 0, s));
+      LMOE_TRY(run_tc_gemm(h, g, 0, &h->last_launches, s));
       stage_end(h, kStSharedGlu, s);
-      h->last_launches += 1;
     }
     stage_begin(h, kStFinal, s);
     TcGemm f = {};
@@ -407,9 +419,8 @@ lmoe_status run_forward(lmoe_handle* h, const void* x, int T, const lmoe_weights
       f.k0_len = l; f.k0_per_group = l;
     }
     f.C = y; f.ldc = d;
-    LMOE_TRY(run_tc_gemm(h, f, 0, s));
+    LMOE_TRY(run_tc_gemm(h, f, 0, &h->last_launches, s));
     stage_end(h, kStFinal, s);
-    h->last_launches += 1;
   } else {
     if (ns > 0) {
       SimtGemm g = {};

@@ -188,6 +188,34 @@ def test_cta_pair_gemms_match_single_cta(binding, cfg):
     single.close()
 
 
+def test_forward_routed_tile_boundary_counts(binding):
+    """Caller routing that gives experts row counts at every tile boundary of the 16-, 128- and
+    256-row tile lists (0, 1, 127..129, 255..257, 383..385, 512): pair tiles, their 128-row tail
+    tiles and single-CTA tiles all match the oracle on every row."""
+    counts = [0, 1, 127, 128, 129, 255, 256, 257, 383, 384, 385, 512, 0, 16, 17, 14]
+    E, k = len(counts), 2
+    T = sum(counts) // k
+    cfg = replace(SMALL_BF16, name="tile_counts", tokens=T, experts=E, top_k=k, n_shared=1, seed=42)
+    slots = np.repeat(np.arange(E), counts)
+    assert slots.size == T * k and max(counts) <= T
+    idx_np = np.stack([slots[:T], slots[T:]], axis=1).astype(np.int32)  # distinct experts per token
+    assert np.all(idx_np[:, 0] != idx_np[:, 1])
+    rng = np.random.default_rng(7)
+    p_np = rng.uniform(0.2, 0.8, size=(T, k))
+    p_np /= p_np.sum(axis=1, keepdims=True)
+    dev = torch.device("cuda")
+    inp = device_inputs(cfg, dev, False)
+    host = inputs.host_inputs(inp)
+    ref = oracle.layer_forward(host, cfg, routing=(idx_np, p_np))
+    for flags in (0, binding.LMOE_FLAG_SINGLE_CTA_GEMM):
+        layer = binding.LatentMoE(cfg, flags=flags)
+        y = layer.forward_routed(inp["x"], inp, torch.from_numpy(idx_np).to(dev),
+                                 torch.from_numpy(p_np.astype(np.float32)).to(dev))
+        assert layer.status() == 0
+        assert_close(to_np(y), ref["y"], REL_FRO["bf16"], f"tile counts, flags={flags}")
+        layer.close()
+
+
 def test_forward_host_matches_device_path(binding):
     cfg = replace(SMALL_BF16, name="host", seed=32)
     dev = torch.device("cuda")
