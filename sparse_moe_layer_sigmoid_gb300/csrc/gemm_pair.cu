@@ -1,7 +1,6 @@
-// Paired-CTA persistent GEMM on the 5th-generation tensor cores for the 16-bit contractions with
-// many rows: the routed experts' gate/up and down projections (grouped by expert, page "Lesson 6
-// - LatentMoE", kimi-k3-course.pages.dev, eq. 11 and section "Deriving the headline number"),
-// and the dense W_down, shared gate/up and final GEMMs of the same layer.
+// Paired-CTA persistent GEMM on the 5th-generation tensor cores for the dense 16-bit
+// contractions with many rows: W_down, the shared experts' gate/up and the final GEMM of the
+// layer (page "Lesson 6 - LatentMoE", kimi-k3-course.pages.dev, eq. 11).
 //
 //   C[r][n] = epilogue( sum_c A[r][c] * B[n][c] ),  A, B bf16 K-major, fp32 accumulation.
 //
@@ -44,10 +43,7 @@ struct PairParams {
   int M, N;
   int num_kb, kb0, kb0_per_group;
   int glu_h;
-  int num_m_tiles, num_n_tiles;  // dense mode: 256-row tiles
-  const int4* tiles;             // grouped mode: 256-row tile list {expert, first tile, tiles, first row}
-  const int32_t* num_tiles;
-  const int32_t* offsets;
+  int num_m_tiles, num_n_tiles;  // 256-row tiles, 256-column (GLU: 128-output) tiles
   void* C;
   int64_t ldc;
   const float* row_scale;
@@ -90,29 +86,18 @@ __device__ __forceinline__ Boxes boxes_for(const PairParams& p, const PairTile& 
   return b;
 }
 
-template <int BN_OUT, bool GROUPED>
+template <int BN_OUT>
 __device__ __forceinline__ PairTile decode_pair_tile(const PairParams& p, int t) {
   PairTile ti;
-  if (GROUPED) {
-    const int q = t / p.num_n_tiles;
-    const int4 tl = p.tiles[q];
-    const int local = t - tl.y * p.num_n_tiles;
-    const int n = local / tl.z, m = local - n * tl.z;
-    ti.row0 = tl.w + m * kTileP;
-    ti.row_end = min(ti.row0 + kTileP, p.offsets[tl.x + 1]);
-    ti.n0 = n * BN_OUT;
-    ti.group = tl.x;
-  } else {
-    const int m = t % p.num_m_tiles, n = t / p.num_m_tiles;
-    ti.row0 = m * kTileP;
-    ti.row_end = min(ti.row0 + kTileP, p.M);
-    ti.n0 = n * BN_OUT;
-    ti.group = 0;
-  }
+  const int m = t % p.num_m_tiles, n = t / p.num_m_tiles;
+  ti.row0 = m * kTileP;
+  ti.row_end = min(ti.row0 + kTileP, p.M);
+  ti.n0 = n * BN_OUT;
+  ti.group = 0;
   return ti;
 }
 
-template <int EPI, bool GROUPED>
+template <int EPI>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                    const __grid_constant__ CUtensorMap tmB1, const PairParams p) {
@@ -155,14 +140,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
 
-  const int total = (GROUPED ? *p.num_tiles : p.num_m_tiles) * p.num_n_tiles;
+  const int total = p.num_m_tiles * p.num_n_tiles;
 
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------------ TMA producer (both CTAs)
     int stage = 0, iter = 0;
     uint32_t phase = 0;
     for (int t = pair; t < total; t += npairs) {
-      const PairTile ti = decode_pair_tile<BN_OUT, GROUPED>(p, t);
+      const PairTile ti = decode_pair_tile<BN_OUT>(p, t);
       for (int kb = 0; kb < p.num_kb; ++kb, ++iter) {
         if (!ptx::mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, p.status, p.timeout_ns, kWaitProducer))
           goto done;
@@ -216,7 +201,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     int it = 0;
     for (int t = pair; t < total; t += npairs, ++it) {
-      const PairTile ti = decode_pair_tile<BN_OUT, GROUPED>(p, t);
+      const PairTile ti = decode_pair_tile<BN_OUT>(p, t);
       const int acc = it & 1;
       const uint32_t use = (uint32_t)(it >> 1);
       int ok = 1;
@@ -251,10 +236,10 @@ done:
   }
 }
 
-template <int EPI, bool GROUPED>
+template <int EPI>
 cudaError_t launch_inst(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1, const PairParams& p,
                         long long pair_tiles, cudaStream_t s) {
-  auto kern = tc_pair_kernel<EPI, GROUPED>;
+  auto kern = tc_pair_kernel<EPI>;
   static int max_pairs = 0;
   if (max_pairs == 0) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
@@ -278,19 +263,16 @@ cudaError_t launch_inst(const CUtensorMap& a, const CUtensorMap& b0, const CUten
 
 bool tc_pair_supported(const TcGemm& g) {
   const bool glu = g.epi == kEpiGluBF16;
-  if (g.b_scale || g.ab_f16) return false;
-  if (g.epi != kEpiBF16 && g.epi != kEpiGluBF16 && g.epi != kEpiScaleBF16) return false;
+  if (g.tiles || g.b_scale || g.ab_f16) return false;
+  if (g.epi != kEpiBF16 && g.epi != kEpiGluBF16) return false;
   if (g.a_k_period && g.a_k_period != g.K) return false;
   if (g.K % BK || g.k0_len % BK || g.k0_per_group % BK) return false;
-  if (glu ? (g.N % (BN / 2) || g.glu_h % kRows) : g.N % 32) return false;
-  if (g.tiles && (!g.tiles_p || !g.tiles_t)) return false;
-  return g.epi != kEpiScaleBF16 || g.tiles;
+  return glu ? g.N % (BN / 2) == 0 && g.glu_h % kRows == 0 : g.N % 32 == 0;
 }
 
 cudaError_t launch_tc_pair(const TcGemm& g, uint32_t* status, uint64_t timeout_ns, cudaStream_t s) {
   if (!tc_pair_supported(g)) return cudaErrorInvalidValue;
   const bool glu = g.epi == kEpiGluBF16;
-  const bool grouped = g.tiles != nullptr;
   const int bn_out = glu ? BN / 2 : BN;
   CUtensorMap ma, mb0, mb1;
   if (!make_map(&ma, g.A) || !make_map(&mb0, g.B0)) return cudaErrorInvalidValue;
@@ -308,28 +290,14 @@ cudaError_t launch_tc_pair(const TcGemm& g, uint32_t* status, uint64_t timeout_n
   p.glu_h = glu ? g.glu_h : 1;
   p.num_m_tiles = (g.M + kTileP - 1) / kTileP;
   p.num_n_tiles = (g.N + bn_out - 1) / bn_out;
-  p.tiles = g.tiles_p;
-  p.num_tiles = g.num_tiles_p;
-  p.offsets = g.offsets;
   p.C = g.C;
   p.ldc = g.ldc;
   p.row_scale = g.row_scale;
   p.status = status;
   p.timeout_ns = timeout_ns;
-  const long long tiles =
-      grouped ? (long long)g.max_tiles_p * p.num_n_tiles : (long long)p.num_m_tiles * p.num_n_tiles;
+  const long long tiles = (long long)p.num_m_tiles * p.num_n_tiles;
   if (tiles == 0) return cudaSuccess;
-  switch (g.epi) {
-    case kEpiBF16:
-      return grouped ? launch_inst<kEpiBF16, true>(ma, mb0, mb1, p, tiles, s)
-                     : launch_inst<kEpiBF16, false>(ma, mb0, mb1, p, tiles, s);
-    case kEpiGluBF16:
-      return grouped ? launch_inst<kEpiGluBF16, true>(ma, mb0, mb1, p, tiles, s)
-                     : launch_inst<kEpiGluBF16, false>(ma, mb0, mb1, p, tiles, s);
-    case kEpiScaleBF16:
-      return launch_inst<kEpiScaleBF16, true>(ma, mb0, mb1, p, tiles, s);
-  }
-  return cudaErrorInvalidValue;
+  return glu ? launch_inst<kEpiGluBF16>(ma, mb0, mb1, p, tiles, s) : launch_inst<kEpiBF16>(ma, mb0, mb1, p, tiles, s);
 }
 
 }  // namespace lmoe

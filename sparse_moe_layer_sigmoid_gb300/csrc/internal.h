@@ -48,11 +48,8 @@ struct DispatchBuffers {
   int32_t* num_tiles;     // [1]
   int4* tiles_s;          // [T*k/16 + E + 1]: {expert, first row, rows (<= 16), 0}
   int32_t* num_tiles_s;   // [1]
-  int4* tiles_p;          // [T*k/256 + E + 1]: 256-row tiles, same layout as `tiles` (or nullptr);
-                          // an expert's last <= 128 rows are left to tiles_t
+  int4* tiles_p;          // [T*k/256 + E + 1]: 256-row tiles, same layout as `tiles` (or nullptr)
   int32_t* num_tiles_p;   // [1]
-  int4* tiles_t;          // [E]: the 128-row tail tiles tiles_p leaves, same layout (or nullptr)
-  int32_t* num_tiles_t;   // [1]
   int32_t* tok_of_row;    // [T*k]
   int32_t* row_of;        // [T][k]
   float* p_row;           // [T*k]
@@ -117,8 +114,6 @@ struct TcGemm {
   int a_k_period;         // A's K coordinate wraps every a_k_period columns (0 = K: no wrap)
   int glu_h;              // GLU: rows of B between gate and up; output column j -> (j / glu_h, j % glu_h)
   const int4* tiles; const int32_t* num_tiles; const int32_t* offsets; int max_tiles;  // grouped mode
-  const int4* tiles_p; const int32_t* num_tiles_p; int max_tiles_p;  // grouped, paired CTAs: 256-row tiles
-  const int4* tiles_t; const int32_t* num_tiles_t;                    // grouped: the 128-row tails of tiles_p
   void* C; int64_t ldc;
   const float* row_scale;
   int ab_f16;                // operands are fp16 (with MXFP4 B) instead of bf16
@@ -127,9 +122,9 @@ struct TcGemm {
 cudaError_t launch_tc_gemm(const TcGemm& g, uint32_t* status, uint64_t timeout_ns, int inject_fault, int num_sms,
                            cudaStream_t s);
 
-// The same GEMM on CTA pairs (gemm_pair.cu): 256 x 256 tiles, tcgen05.mma.cta_group::2.  For
-// bf16 operands with the bf16, GLU and (grouped) scale epilogues; tc_pair_supported says whether
-// `g` qualifies.
+// The same GEMM on CTA pairs (gemm_pair.cu): 256 x 256 tiles, tcgen05.mma.cta_group::2.  Dense
+// (not grouped), bf16 operands, bf16 or GLU epilogue; tc_pair_supported says whether `g`
+// qualifies.
 bool tc_pair_supported(const TcGemm& g);
 cudaError_t launch_tc_pair(const TcGemm& g, uint32_t* status, uint64_t timeout_ns, cudaStream_t s);
 
@@ -149,5 +144,11 @@ struct TcSwap {
   const float* row_scale;   // down: routing weight per row
 };
 cudaError_t launch_tc_swap(const TcSwap& g, uint32_t* status, uint64_t timeout_ns, int num_sms, cudaStream_t s);
+// The same swapped-operand grouped GEMM on CTA pairs for experts with many rows
+// (gemm_pair_swap.cu): 256 weight rows x up to 256 token rows per tile, each expert's rows cut
+// into ceil(rows/256) equal token tiles (tiles_p: the dispatch's 256-row tile list).  bf16 only
+// (kEpiGluBF16 with glu_h % 128 == 0, or kEpiScaleBF16 with out_features % 256 == 0).
+cudaError_t launch_tc_pair_swap(const TcSwap& g, const int4* tiles_p, const int32_t* num_tiles_p, int max_tiles_p,
+                                const int32_t* offsets, uint32_t* status, uint64_t timeout_ns, cudaStream_t s);
 
 }  // namespace lmoe

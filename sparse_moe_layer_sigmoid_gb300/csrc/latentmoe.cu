@@ -155,8 +155,6 @@ size_t layout(lmoe_handle* h, uint8_t* base) {
   h->max_tiles_p = (int)(rows / kTileP + E + 1);
   h->db.tiles_p = reinterpret_cast<int4*>(take((size_t)h->max_tiles_p * 16));
   h->db.num_tiles_p = reinterpret_cast<int32_t*>(take(4));
-  h->db.tiles_t = reinterpret_cast<int4*>(take(E * 16));
-  h->db.num_tiles_t = reinterpret_cast<int32_t*>(take(4));
   h->db.tok_of_row = reinterpret_cast<int32_t*>(take(rows * 4));
   h->db.row_of = reinterpret_cast<int32_t*>(take(rows * 4));
   h->db.p_row = reinterpret_cast<float*>(take(rows * 4));
@@ -232,27 +230,13 @@ lmoe_status run_routing(lmoe_handle* h, const void* x, int T, const lmoe_weights
   return LMOE_OK;
 }
 
-// A tensor-core GEMM of the layer: on CTA pairs (256-row tiles) when it qualifies, else on single
-// CTAs (128-row tiles).  Grouped GEMMs on pairs take two launches: the pairs cover each expert's
-// rows in 256-row tiles except a remainder of at most 128 rows, which a single-CTA launch over
-// the tail list covers, so no expert is padded by more than 127 rows either way.  Returns the
-// number of kernels launched through *launches.
-cudaError_t run_tc_gemm(lmoe_handle* h, TcGemm g, int inject, int* launches, cudaStream_t s) {
-  const bool grouped = g.tiles != nullptr;
-  if (grouped) {
-    g.tiles_p = h->db.tiles_p; g.num_tiles_p = h->db.num_tiles_p; g.max_tiles_p = h->max_tiles_p;
-    g.tiles_t = h->db.tiles_t; g.num_tiles_t = h->db.num_tiles_t;
-  }
-  const bool tall = grouped ? (int64_t)g.M >= (int64_t)kTileM * h->cfg.num_experts : g.M >= kTileP;
-  const bool pair = !(h->cfg.flags & LMOE_FLAG_SINGLE_CTA_GEMM) && !inject && tall && tc_pair_supported(g);
+// A tensor-core GEMM of the layer: dense GEMMs with at least 256 rows run on CTA pairs (256 x 256
+// tiles), everything else on single CTAs (128-row tiles).  Adds its launch to *launches.
+cudaError_t run_tc_gemm(lmoe_handle* h, const TcGemm& g, int inject, int* launches, cudaStream_t s) {
   *launches += 1;
-  if (!pair) return launch_tc_gemm(g, h->status, h->timeout_ns, inject, h->num_sms, s);
-  cudaError_t e = launch_tc_pair(g, h->status, h->timeout_ns, s);
-  if (e != cudaSuccess || !grouped) return e;
-  TcGemm t = g;
-  t.tiles = g.tiles_t; t.num_tiles = g.num_tiles_t; t.max_tiles = h->cfg.num_experts;
-  *launches += 1;
-  return launch_tc_gemm(t, h->status, h->timeout_ns, 0, h->num_sms, s);
+  const bool pair = !(h->cfg.flags & LMOE_FLAG_SINGLE_CTA_GEMM) && !inject && g.M >= kTileP && tc_pair_supported(g);
+  if (pair) return launch_tc_pair(g, h->status, h->timeout_ns, s);
+  return launch_tc_gemm(g, h->status, h->timeout_ns, inject, h->num_sms, s);
 }
 
 lmoe_status run_forward(lmoe_handle* h, const void* x, int T, const lmoe_weights* w, const int32_t* ext_idx,
@@ -314,7 +298,31 @@ lmoe_status run_forward(lmoe_handle* h, const void* x, int T, const lmoe_weights
   uint8_t* n_out = static_cast<uint8_t*>(h->act_cat) + (size_t)ns * hs * ab;
   // few rows per expert (decode): weights on the M side of the MMA, tokens on the N side
   const bool swap = tc && (int64_t)T * k <= 32LL * c.num_experts;
-  if (swap) {
+  // many rows per expert, bf16 experts: swapped operands on CTA pairs (token tiles cut to fit)
+  const bool pair_swap = tc && !swap && c.routed_w == LMOE_BF16 && !(c.flags & LMOE_FLAG_SINGLE_CTA_GEMM) &&
+                         !h->inject && hdim % 128 == 0 && l % 256 == 0;
+  if (pair_swap) {
+    TcSwap g = {};
+    g.epi = kEpiGluBF16;
+    g.K = l; g.out_features = hdim; g.glu_h = hdim;
+    g.act = op2d(h->z_perm, rows, l);
+    g.w = op3d(w->routed_gate_up, c.num_experts, 2 * hdim, l);
+    g.C = h->a; g.ldc = hdim;
+    LMOE_TRY(launch_tc_pair_swap(g, h->db.tiles_p, h->db.num_tiles_p, h->max_tiles_p, h->db.offsets, h->status,
+                                 h->timeout_ns, s));
+    stage_end(h, kStGlu, s);
+
+    TcSwap dn = {};
+    dn.epi = kEpiScaleBF16;
+    dn.K = hdim; dn.out_features = l;
+    dn.act = op2d(h->a, rows, hdim);
+    dn.w = op3d(w->routed_down, c.num_experts, l, hdim);
+    dn.C = o; dn.ldc = l; dn.row_scale = h->db.p_row;
+    LMOE_TRY(launch_tc_pair_swap(dn, h->db.tiles_p, h->db.num_tiles_p, h->max_tiles_p, h->db.offsets, h->status,
+                                 h->timeout_ns, s));
+    stage_end(h, kStDown, s);
+    h->last_launches += 2;
+  } else if (swap) {
     const bool fp4 = c.routed_w == LMOE_MXFP4;
     TcSwap g = {};
     g.epi = fp4 ? kEpiGluF16 : kEpiGluBF16;

@@ -376,30 +376,22 @@ __global__ void __launch_bounds__(1024) dispatch_scan_kernel(const int32_t* __re
                                                              int4* __restrict__ tiles_s,
                                                              int32_t* __restrict__ num_tiles_s,
                                                              int4* __restrict__ tiles_p,
-                                                             int32_t* __restrict__ num_tiles_p,
-                                                             int4* __restrict__ tiles_t,
-                                                             int32_t* __restrict__ num_tiles_t) {
+                                                             int32_t* __restrict__ num_tiles_p) {
   __shared__ int s_cnt[1024];
   __shared__ int s_tiles[1024];
   __shared__ int s_tiles_s[1024];
   __shared__ int s_tiles_p[1024];
-  __shared__ int s_tiles_t[1024];
   const int e = threadIdx.x;
   int total = 0;
   if (e < E)
     for (int c = 0; c < nchunks; ++c) total += chunk_counts[(size_t)c * E + e];
   const int nt = (total + kTileM - 1) / kTileM;
   const int nts = (total + kTileS - 1) / kTileS;
-  // 256-row tiles; a remainder of at most 128 rows goes to a 128-row tail tile instead
-  const int rem = total % kTileP;
-  const bool short_tail = rem > 0 && rem <= kTileM;
-  const int ntp = short_tail ? total / kTileP : (total + kTileP - 1) / kTileP;
-  const int ntt = short_tail ? 1 : 0;
+  const int ntp = (total + kTileP - 1) / kTileP;
   s_cnt[e] = total;
   s_tiles[e] = nt;
   s_tiles_s[e] = nts;
   s_tiles_p[e] = ntp;
-  s_tiles_t[e] = ntt;
   __syncthreads();
   // Hillis-Steele inclusive scans over 1024 entries (fixed order, integer: exact).
   for (int off = 1; off < 1024; off <<= 1) {
@@ -407,20 +399,17 @@ __global__ void __launch_bounds__(1024) dispatch_scan_kernel(const int32_t* __re
     const int b = e >= off ? s_tiles[e - off] : 0;
     const int c = e >= off ? s_tiles_s[e - off] : 0;
     const int f = e >= off ? s_tiles_p[e - off] : 0;
-    const int g = e >= off ? s_tiles_t[e - off] : 0;
     __syncthreads();
     s_cnt[e] += a;
     s_tiles[e] += b;
     s_tiles_s[e] += c;
     s_tiles_p[e] += f;
-    s_tiles_t[e] += g;
     __syncthreads();
   }
   const int row0 = s_cnt[e] - total;
   const int tile0 = s_tiles[e] - nt;
   const int tile0s = s_tiles_s[e] - nts;
   const int tile0p = s_tiles_p[e] - ntp;
-  const int tile0t = s_tiles_t[e] - ntt;
   if (e < E) {
     offsets[e] = row0;
     int run = row0;
@@ -433,14 +422,12 @@ __global__ void __launch_bounds__(1024) dispatch_scan_kernel(const int32_t* __re
       for (int j = 0; j < nts; ++j) tiles_s[tile0s + j] = make_int4(e, row0 + kTileS * j, min(kTileS, total - kTileS * j), 0);
     if (tiles_p)
       for (int j = 0; j < ntp; ++j) tiles_p[tile0p + j] = make_int4(e, tile0p, ntp, row0);
-    if (tiles_t && short_tail) tiles_t[tile0t] = make_int4(e, tile0t, 1, row0 + total - rem);
   }
   if (e == E - 1) {
     offsets[E] = s_cnt[e];
     *num_tiles = s_tiles[e];
     if (num_tiles_s) *num_tiles_s = s_tiles_s[e];
     if (num_tiles_p) *num_tiles_p = s_tiles_p[e];
-    if (num_tiles_t) *num_tiles_t = s_tiles_t[e];
   }
 }
 
@@ -581,8 +568,7 @@ cudaError_t launch_dispatch(const int32_t* idx, const float* p, int T, int E, in
   const size_t smem = (size_t)E * kMaskWords * sizeof(uint32_t);
   dispatch_count_kernel<<<nchunks, kDispatchChunk, smem, s>>>(idx, T, E, k, b.chunk_counts, status);
   dispatch_scan_kernel<<<1, 1024, 0, s>>>(b.chunk_counts, nchunks, E, b.chunk_base, b.offsets, b.tiles,
-                                          b.num_tiles, b.tiles_s, b.num_tiles_s, b.tiles_p, b.num_tiles_p,
-                                          b.tiles_t, b.num_tiles_t);
+                                          b.num_tiles, b.tiles_s, b.num_tiles_s, b.tiles_p, b.num_tiles_p);
   dispatch_scatter_kernel<<<nchunks, kDispatchChunk, smem, s>>>(idx, p, T, E, k, b.chunk_base, b.tok_of_row,
                                                                 b.row_of, b.p_row);
   if (launches) *launches += 3;

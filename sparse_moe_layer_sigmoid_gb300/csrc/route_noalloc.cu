@@ -110,8 +110,6 @@ extern "C" lmoe_status latentmoe_route_noalloc(const lmoe_config* cfg, const voi
   db.num_tiles_s = nullptr;
   db.tiles_p = nullptr;
   db.num_tiles_p = nullptr;
-  db.tiles_t = nullptr;
-  db.num_tiles_t = nullptr;
   db.tok_of_row = tok_of_row;
   db.row_of = row_of;
   db.p_row = nullptr;

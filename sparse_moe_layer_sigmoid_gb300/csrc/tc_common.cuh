@@ -163,6 +163,23 @@ inline bool make_map(CUtensorMap* m, const TcOperand& op, int box_rows = 128) {
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Gate/up weights [depth][2h][cols] (gate rows 0..h-1, up rows h..2h-1) viewed as 5-D
+// {cols, 16, 2, h/16, depth} with a box of {64, 16, 2, groups, 1}: one load brings `groups` x
+// (16 gate rows, then the matching 16 up rows), 128-byte swizzled rows in that order.
+inline bool make_map_glu_interleaved(CUtensorMap* m, const TcOperand& op, int glu_h, int groups) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc || !op.ptr || glu_h % 16 || op.rows != 2 * (int64_t)glu_h) return false;
+  const int64_t rs = op.row_stride * 2;  // bytes per row
+  const int64_t depth_stride = op.depth > 1 ? op.depth_stride * 2 : op.rows * rs;
+  cuuint64_t dims[5] = {(cuuint64_t)op.cols, 16, 2, (cuuint64_t)(glu_h / 16), (cuuint64_t)op.depth};
+  cuuint64_t strides[4] = {(cuuint64_t)rs, (cuuint64_t)(glu_h * rs), (cuuint64_t)(16 * rs), (cuuint64_t)depth_stride};
+  cuuint32_t box[5] = {BK, 16, 2, (cuuint32_t)groups, 1};
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(op.ptr), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Packed E2M1 operand [depth][rows][cols/2 bytes] (element strides in `op`): boxes of
 // box_bytes bytes (2 elements per byte) x box_rows rows, no swizzle, or the 128-byte swizzle
 // (box_bytes == 128) when the reader takes column slices of the rows.
