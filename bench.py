@@ -48,23 +48,39 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def stage_work(cfg):
-    """Algorithmic work of each stage: ('tensor', FLOPs) or ('hbm', bytes)."""
+def expert_weight_bytes(cfg, rows, cols):
+    """Stored bytes of one routed weight matrix [rows][cols] (MXFP4: E2M1 + one E8M0 per 32)."""
+    if cfg.routed_w == "mxfp4":
+        return rows * cols // 2 + rows * cols // 32
+    return rows * cols * (4 if cfg.routed_w == "f32" else 2)
+
+
+def stage_work(cfg, experts_touched):
+    """Algorithmic work of each stage: ('tensor', FLOPs) or ('hbm', bytes).
+
+    Decode-shaped batches (T*k <= 32*E, the swapped-operand kernels) are bound by streaming the
+    touched experts' weights: their routed stages count those bytes (plus activations)."""
     T, d, l, h, E, k = cfg.tokens, cfg.d, cfg.latent, cfg.hidden, cfg.experts, cfg.top_k
     ns, hs = cfg.n_shared, cfg.shared_hidden
     ab = 4 if cfg.act == "f32" else 2
     rows = T * k
     w = {
-        "router_logits": ("alu", 2.0 * T * E * d),
+        # bf16 activations: tensor cores (over 3 bf16 terms of W_r); fp32: CUDA-core FMA
+        "router_logits": ("tensor" if cfg.act == "bf16" else "alu", 2.0 * T * E * d),
         "topk": ("hbm", 4.0 * T * E + 8.0 * rows),
         "dispatch": ("hbm", 3 * 4.0 * rows),
         "w_down": ("tensor", 2.0 * T * d * l),
         "scatter_rows": ("hbm", float(ab) * (T * l + rows * l)),
         "combine_rmsnorm": ("hbm", float(ab) * (rows * l + T * l)),
     }
-    if not cfg.identity_experts:
+    if not cfg.identity_experts and rows <= 32 * E:
+        w["routed_gate_up_glu"] = ("hbm", float(experts_touched * expert_weight_bytes(cfg, 2 * h, l)
+                                                + ab * rows * (l + h)))
+        w["routed_down"] = ("hbm", float(experts_touched * expert_weight_bytes(cfg, l, h) + ab * rows * (h + l)))
+    elif not cfg.identity_experts:
         w["routed_gate_up_glu"] = ("tensor", 2.0 * rows * l * 2 * h)
         w["routed_down"] = ("tensor", 2.0 * rows * h * l)
+    if not cfg.identity_experts:
         w["shared_gate_up_glu"] = ("tensor", 2.0 * T * d * 2 * ns * hs)
         w["final_gemm"] = ("tensor", 2.0 * T * (ns * hs + l) * d)
     return w
@@ -335,14 +351,18 @@ def main():
     elem = x.element_size()
 
     peaks, src = load_peaks()
-    work = stage_work(cfg)
+    work = stage_work(cfg, route_stats["experts_touched"])
     st_ms = {k_: sum(v) / len(v) for k_, v in stages.items()}
-    tensor_stages = {k_: st_ms[k_] for k_, (kind, _) in work.items() if kind == "tensor" and k_ in st_ms}
-    dom = max(tensor_stages, key=tensor_stages.get) if tensor_stages else max(st_ms, key=st_ms.get)
+    dom = max((k_ for k_ in work if k_ in st_ms), key=st_ms.get)
     kind, amount = work[dom]
     if kind == "tensor":
         achieved = amount / (st_ms[dom] * 1e-3) / 1e12
         peak = peaks["bf16_tflops"]
+        unit = "TFLOP/s"
+    elif kind == "alu":
+        # fp32 FMA on CUDA cores: 152 SMs x 128 lanes x 2 FLOP x max SM clock
+        achieved = amount / (st_ms[dom] * 1e-3) / 1e12
+        peak = 152 * 128 * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
         unit = "TFLOP/s"
     else:
         achieved = amount / (st_ms[dom] * 1e-3) / 1e9
@@ -358,9 +378,10 @@ def main():
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": cfg.act, "data": "synthetic",
             "config": workload_config(cfg, args),
-            "roofline": {"bound": "tensor" if kind == "tensor" else "hbm", "kernel": dom, "achieved": achieved,
+            "roofline": {"bound": kind, "kernel": dom, "achieved": achieved,
                          "peak": peak, "unit": unit, "frac": achieved / peak, "traffic": traffic,
-                         "peak_source": f"{src} {'bf16_tflops (burst)' if kind == 'tensor' else 'hbm_gbs'}"},
+                         "peak_source": {"tensor": f"{src} bf16_tflops (burst)", "hbm": f"{src} hbm_gbs",
+                                         "alu": "derived: 152 SMs x 128 fp32 lanes x 2 x sm_max_mhz"}[kind]},
             "layer": {"flops": total_flops, "achieved_tflops": total_flops / (ms * 1e-3) / 1e12,
                       "frac_of_bf16_peak": total_flops / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"],
                       "stages_ms": st_ms},

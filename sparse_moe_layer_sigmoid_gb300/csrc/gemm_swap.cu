@@ -152,22 +152,20 @@ __global__ void __launch_bounds__(SwapCfg<FP4W>::kThreads, 1)
     uint32_t phase = 0;
     for (int u = blockIdx.x; u < total; u += gridDim.x) {
       const SwapTile ti = decode_swap(p, u);
-      constexpr uint32_t kWBox = C::kWStageBytes / (kWRows / kBox);  // bytes per weight box
-      const uint32_t tx = C::kWStageBytes + (uint32_t)(SUB * ti.nb) * (kBox * BK * 2);
+      const uint32_t tx = C::kWStageBytes + (uint32_t)SUB * C::kXSubBytes;
       for (int st = 0; st < num_st; ++st) {
         if (!ptx::mbar_wait_bounded(&empty1[stage], phase ^ 1u, abort_flag, p.status, p.timeout_ns, kWaitProducer)) goto done;
         uint8_t* sW = smem + stage * C::kStage1Bytes;
         uint8_t* sX = sW + C::kWStageBytes;
         ptx::mbar_arrive_expect_tx(&full1[stage], tx);
         const int kx = FP4W ? st * (BK * SUB / 2) : st * BK;  // bytes (packed) or elements
-#pragma unroll
-        for (int b = 0; b < kWRows / kBox; ++b)
-          ptx::tma_load_3d(sW + b * kWBox, &tmW, &full1[stage], kx, weight_row(p, ti.wt, b * kBox), ti.expert);
-#pragma unroll
-        for (int sb = 0; sb < SUB; ++sb)
-          for (int b = 0; b < ti.nb; ++b)
-            ptx::tma_load_3d(sX + sb * C::kXSubBytes + b * (kBox * BK * 2), &tmX, &full1[stage],
-                             (st * SUB + sb) * BK, ti.row0 + b * kBox, 0);
+        // weights: one box of 128 rows (gate/up: 4 x (16 gate rows, 16 up rows) of features wt*64..)
+        if (GLU)
+          ptx::tma_load_5d(sW, &tmW, &full1[stage], kx, 0, 0, ti.wt * 4, ti.expert);
+        else
+          ptx::tma_load_3d(sW, &tmW, &full1[stage], kx, ti.wt * kWRows, ti.expert);
+        // tokens: the unit's 16 rows for the stage's SUB 64-column blocks, one box
+        ptx::tma_load_3d(sX, &tmX, &full1[stage], 0, ti.row0, st * SUB);
         if (++stage == S1) {
           stage = 0;
           phase ^= 1u;
@@ -362,10 +360,11 @@ cudaError_t launch_tc_swap(const TcSwap& g, uint32_t* status, uint64_t timeout_n
   if (glu ? (g.glu_h % 64 || g.out_features != g.glu_h) : g.out_features % kWRows) return cudaErrorInvalidValue;
   if (fp4 && !g.ab_f16) return cudaErrorInvalidValue;
   CUtensorMap mw, mx;
-  if (!(fp4 ? make_map_fp4(&mw, g.w, kBox, BK * SwapCfg<true>::kSub / 2, /*swizzle128=*/true)
-            : make_map(&mw, g.w, kBox)))
-    return cudaErrorInvalidValue;
-  if (!make_map(&mx, g.act, kBox)) return cudaErrorInvalidValue;
+  const bool wmap = glu ? make_map_glu_interleaved(&mw, g.w, g.glu_h, kWRows / 32, fp4)
+                        : (fp4 ? make_map_fp4(&mw, g.w, kWRows, BK * SwapCfg<true>::kSub / 2, /*swizzle128=*/true)
+                               : make_map(&mw, g.w, kWRows));
+  if (!wmap) return cudaErrorInvalidValue;
+  if (!make_map_kslabs(&mx, g.act, kBox, fp4 ? SwapCfg<true>::kSub : SwapCfg<false>::kSub)) return cudaErrorInvalidValue;
   SwapParams p = {};
   p.num_kb = g.K / BK;
   p.num_wt = glu ? g.glu_h / 64 : g.out_features / kWRows;

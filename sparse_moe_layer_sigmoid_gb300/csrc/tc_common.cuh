@@ -164,18 +164,35 @@ inline bool make_map(CUtensorMap* m, const TcOperand& op, int box_rows = 128) {
 }
 
 // Gate/up weights [depth][2h][cols] (gate rows 0..h-1, up rows h..2h-1) viewed as 5-D
-// {cols, 16, 2, h/16, depth} with a box of {64, 16, 2, groups, 1}: one load brings `groups` x
-// (16 gate rows, then the matching 16 up rows), 128-byte swizzled rows in that order.
-inline bool make_map_glu_interleaved(CUtensorMap* m, const TcOperand& op, int glu_h, int groups) {
+// {cols, 16, 2, h/16, depth} with a box of {64 elements, 16, 2, groups, 1}: one load brings
+// `groups` x (16 gate rows, then the matching 16 up rows), 128-byte swizzled rows in that order.
+// `fp4`: the operand holds packed E2M1 bytes (cols/2 bytes per row, 128-byte box rows = 256
+// elements); otherwise bf16.
+inline bool make_map_glu_interleaved(CUtensorMap* m, const TcOperand& op, int glu_h, int groups, bool fp4 = false) {
   EncodeTiledFn enc = encode_fn();
   if (!enc || !op.ptr || glu_h % 16 || op.rows != 2 * (int64_t)glu_h) return false;
-  const int64_t rs = op.row_stride * 2;  // bytes per row
-  const int64_t depth_stride = op.depth > 1 ? op.depth_stride * 2 : op.rows * rs;
-  cuuint64_t dims[5] = {(cuuint64_t)op.cols, 16, 2, (cuuint64_t)(glu_h / 16), (cuuint64_t)op.depth};
+  const int64_t rs = fp4 ? op.row_stride / 2 : op.row_stride * 2;  // bytes per row
+  const int64_t depth_stride = op.depth > 1 ? (fp4 ? op.depth_stride / 2 : op.depth_stride * 2) : op.rows * rs;
+  cuuint64_t dims[5] = {(cuuint64_t)(fp4 ? op.cols / 2 : op.cols), 16, 2, (cuuint64_t)(glu_h / 16),
+                        (cuuint64_t)op.depth};
   cuuint64_t strides[4] = {(cuuint64_t)rs, (cuuint64_t)(glu_h * rs), (cuuint64_t)(16 * rs), (cuuint64_t)depth_stride};
-  cuuint32_t box[5] = {BK, 16, 2, (cuuint32_t)groups, 1};
+  cuuint32_t box[5] = {fp4 ? 128u : (cuuint32_t)BK, 16, 2, (cuuint32_t)groups, 1};
   cuuint32_t estr[5] = {1, 1, 1, 1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(op.ptr), dims, strides, box, estr,
+  return enc(m, fp4 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(op.ptr),
+             dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 16-bit operand [rows][cols] viewed as 3-D {64, rows, cols/64}: a box of {64, box_rows, slabs}
+// lands as `slabs` consecutive 64-column blocks of box_rows 128-byte swizzled rows each.
+inline bool make_map_kslabs(CUtensorMap* m, const TcOperand& op, int box_rows, int slabs) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc || !op.ptr || op.cols % BK || op.depth != 1) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)BK, (cuuint64_t)op.rows, (cuuint64_t)(op.cols / BK)};
+  cuuint64_t strides[2] = {(cuuint64_t)op.row_stride * 2, (cuuint64_t)BK * 2};
+  cuuint32_t box[3] = {BK, (cuuint32_t)box_rows, (cuuint32_t)slabs};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(op.ptr), dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
