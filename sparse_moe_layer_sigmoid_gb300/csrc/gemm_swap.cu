@@ -56,6 +56,7 @@ struct SwapParams {
   int w_rows;  // weight rows per expert
   const int4* tiles_s;  // {expert, first row, rows}
   const int32_t* num_tiles_s;
+  int skip_rows_upto;   // units with at most this many rows belong to another kernel
   void* C;
   int64_t ldc;
   const float* row_scale;
@@ -152,6 +153,7 @@ __global__ void __launch_bounds__(SwapCfg<FP4W>::kThreads, 1)
     uint32_t phase = 0;
     for (int u = blockIdx.x; u < total; u += gridDim.x) {
       const SwapTile ti = decode_swap(p, u);
+      if (ti.nrows <= p.skip_rows_upto) continue;
       const uint32_t tx = C::kWStageBytes + (uint32_t)SUB * C::kXSubBytes;
       for (int st = 0; st < num_st; ++st) {
         if (!ptx::mbar_wait_bounded(&empty1[stage], phase ^ 1u, abort_flag, p.status, p.timeout_ns, kWaitProducer)) goto done;
@@ -180,6 +182,7 @@ __global__ void __launch_bounds__(SwapCfg<FP4W>::kThreads, 1)
     int it = 0;
     for (int u = blockIdx.x; u < total; u += gridDim.x) {
       const SwapTile ti = decode_swap(p, u);
+      if (ti.nrows <= p.skip_rows_upto) continue;
       const uint32_t idesc = idesc0 | ((uint32_t)((ti.nb * kBox) >> 3) << 17);  // N = 16 * nb
       const int acc = it & 1;
       const uint32_t use = (uint32_t)(it >> 1);
@@ -223,6 +226,7 @@ __global__ void __launch_bounds__(SwapCfg<FP4W>::kThreads, 1)
     int it = 0;
     for (int u = blockIdx.x; u < total; u += gridDim.x) {
       const SwapTile ti = decode_swap(p, u);
+      if (ti.nrows <= p.skip_rows_upto) continue;
       const int acc = it & 1;
       const uint32_t use = (uint32_t)(it >> 1);
       ++it;
@@ -276,6 +280,7 @@ __global__ void __launch_bounds__(SwapCfg<FP4W>::kThreads, 1)
     bool bad = false;
     for (int u = blockIdx.x; u < total; u += gridDim.x) {
       const SwapTile ti = decode_swap(p, u);
+      if (ti.nrows <= p.skip_rows_upto) continue;
       const int wrow = weight_row(p, ti.wt, r);
       const uint4* srow =
           reinterpret_cast<const uint4*>(p.w_scale + ((int64_t)ti.expert * p.w_rows + wrow) * kscale);
@@ -372,6 +377,7 @@ cudaError_t launch_tc_swap(const TcSwap& g, uint32_t* status, uint64_t timeout_n
   p.w_rows = (int)g.w.rows;
   p.tiles_s = g.tiles_s;
   p.num_tiles_s = g.num_tiles_s;
+  p.skip_rows_upto = g.skip_rows_upto;
   p.C = g.C;
   p.ldc = g.ldc;
   p.row_scale = g.row_scale;
