@@ -146,10 +146,10 @@ struct TcSwap {
 };
 cudaError_t launch_tc_swap(const TcSwap& g, uint32_t* status, uint64_t timeout_ns, int num_sms, cudaStream_t s);
 // MXFP4 routed experts for units of at most 4 rows on the CUDA cores (gemv_fp4.cu): the same
-// descriptor as launch_tc_swap (kEpiGluF16 or kEpiScaleF16, fp16 activations, K <= 4096); units
-// with more rows are skipped (run launch_tc_swap with skip_rows_upto = 4 for them).
+// descriptor as launch_tc_swap (kEpiGluF16 or kEpiScaleF16, fp16 activations, K % 512 == 0,
+// K <= 4096); units with more rows are skipped (run launch_tc_swap with skip_rows_upto = 4).
 constexpr int kGemvMaxRows = 4;
-cudaError_t launch_gemv_fp4(const TcSwap& g, uint32_t* status, int num_sms, cudaStream_t s);
+cudaError_t launch_gemv_fp4(const TcSwap& g, uint32_t* status, uint64_t timeout_ns, int num_sms, cudaStream_t s);
 
 // The same swapped-operand grouped GEMM on CTA pairs for experts with many rows
 // (gemm_pair_swap.cu): 256 weight rows x up to 256 token rows per tile, each expert's rows cut

@@ -336,7 +336,7 @@ lmoe_status run_forward(lmoe_handle* h, const void* x, int T, const lmoe_weights
     // MXFP4: units of at most kGemvMaxRows rows stream their weights through the CUDA cores,
     // larger ones go to the tensor cores
     g.skip_rows_upto = fp4 ? kGemvMaxRows : 0;
-    if (fp4) LMOE_TRY(launch_gemv_fp4(g, h->status, h->num_sms, s));
+    if (fp4) LMOE_TRY(launch_gemv_fp4(g, h->status, h->timeout_ns, h->num_sms, s));
     LMOE_TRY(launch_tc_swap(g, h->status, h->timeout_ns, h->num_sms, s));
     stage_end(h, kStGlu, s);
 
@@ -350,7 +350,7 @@ lmoe_status run_forward(lmoe_handle* h, const void* x, int T, const lmoe_weights
     dn.tiles_s = h->db.tiles_s; dn.num_tiles_s = h->db.num_tiles_s; dn.max_tiles_s = h->max_tiles_s;
     dn.C = o; dn.ldc = l; dn.row_scale = h->db.p_row;
     dn.skip_rows_upto = fp4 ? kGemvMaxRows : 0;
-    if (fp4) LMOE_TRY(launch_gemv_fp4(dn, h->status, h->num_sms, s));
+    if (fp4) LMOE_TRY(launch_gemv_fp4(dn, h->status, h->timeout_ns, h->num_sms, s));
     LMOE_TRY(launch_tc_swap(dn, h->status, h->timeout_ns, h->num_sms, s));
     stage_end(h, kStDown, s);
     h->last_launches += fp4 ? 4 : 2;
