@@ -3,9 +3,10 @@
 // "Kimi K3 architectural innovations", manishklach.github.io, section "A router decision is
 // also a scheduling decision": selections become expert batches).
 //
-// Everything here is integer or per-token fp32 work on CUDA cores; the router GEMM itself is
-// the fp32 CUDA-core GEMM of simt.cu.  All results are deterministic: no reduction depends on
-// thread scheduling (counts use atomicOr on bit masks, which commute exactly).
+// Everything here is integer or per-token fp32 work on CUDA cores; the router GEMM itself runs on
+// the tensor cores (bf16 activations) or the fp32 CUDA-core GEMM of simt.cu.  All results are
+// deterministic: no reduction depends on thread scheduling (counts use atomicOr on bit masks,
+// which commute exactly).
 #include "common.cuh"
 #include "internal.h"
 
@@ -66,16 +67,18 @@ __device__ __forceinline__ void load8(const float* p, float (&f)[8]) {
 
 constexpr int kCandBatch = 8;  // boundary candidates evaluated per pass over d
 
-// Up to kCandBatch dot products x . W_r[e_m] in double-float, one warp: each step loads 8
-// elements of x once and 8 elements of every candidate row (independent loads in flight).
+// Partial dot products x . W_r[e_m] in double-float for up to kCandBatch candidates, one warp
+// over the 256-element blocks part, part + nparts, ... of d: each step loads 8 elements of x once
+// and 8 elements of every candidate row (independent loads in flight).  Every lane receives the
+// warp's partial sums.
 template <typename TX, typename TW>
-__device__ void dots_df(const TX* x, const TW* w, int64_t d, const int (&ce)[kCandBatch], int nc, int lane,
-                        double (&out)[kCandBatch]) {
+__device__ void dots_df_part(const TX* x, const TW* w, int64_t d, const int (&ce)[kCandBatch], int nc, int part,
+                             int nparts, int lane, DF (&out)[kCandBatch]) {
   DF acc[kCandBatch];
 #pragma unroll
   for (int m = 0; m < kCandBatch; ++m) acc[m] = DF{0.f, 0.f};
 #pragma unroll 2
-  for (int c = lane * 8; c < d; c += 32 * 8) {  // d % 16 == 0 and 16-byte aligned rows
+  for (int64_t c = (int64_t)part * 256 + lane * 8; c < d; c += (int64_t)nparts * 256) {  // d % 16 == 0
     float xf[8];
     load8(x + c, xf);
 #pragma unroll
@@ -98,92 +101,70 @@ __device__ void dots_df(const TX* x, const TW* w, int64_t d, const int (&ce)[kCa
       o.lo = __shfl_xor_sync(0xffffffffu, a.lo, off);
       a = df_add(a, o);
     }
-    out[m] = (double)a.hi + (double)a.lo;
+    out[m] = a;
   }
 }
 
-// Logits of the candidate experts ce[0..nc) for token t to ~44 bits (one warp; all lanes get
-// every value).
-__device__ void exact_logits(const RouterSrc& r, int t, const int (&ce)[kCandBatch], int nc, int lane,
-                             double (&out)[kCandBatch]) {
+// Partial logits of the candidate experts ce[0..nc) for token t (see dots_df_part).
+__device__ void exact_logit_parts(const RouterSrc& r, int t, const int (&ce)[kCandBatch], int nc, int part,
+                                  int nparts, int lane, DF (&out)[kCandBatch]) {
   const int64_t xo = (int64_t)t * r.d;
   if (r.x_dtype == kBF16 && r.w_dtype == kBF16)
-    dots_df(static_cast<const __nv_bfloat16*>(r.x) + xo, static_cast<const __nv_bfloat16*>(r.w), r.d, ce, nc, lane, out);
+    dots_df_part(static_cast<const __nv_bfloat16*>(r.x) + xo, static_cast<const __nv_bfloat16*>(r.w), r.d, ce, nc,
+                 part, nparts, lane, out);
   else if (r.x_dtype == kBF16)
-    dots_df(static_cast<const __nv_bfloat16*>(r.x) + xo, static_cast<const float*>(r.w), r.d, ce, nc, lane, out);
+    dots_df_part(static_cast<const __nv_bfloat16*>(r.x) + xo, static_cast<const float*>(r.w), r.d, ce, nc, part,
+                 nparts, lane, out);
   else if (r.w_dtype == kBF16)
-    dots_df(static_cast<const float*>(r.x) + xo, static_cast<const __nv_bfloat16*>(r.w), r.d, ce, nc, lane, out);
+    dots_df_part(static_cast<const float*>(r.x) + xo, static_cast<const __nv_bfloat16*>(r.w), r.d, ce, nc, part,
+                 nparts, lane, out);
   else
-    dots_df(static_cast<const float*>(r.x) + xo, static_cast<const float*>(r.w), r.d, ce, nc, lane, out);
-}
-
-struct Refined {
-  double key;  // exact s + b
-  float s;     // s rounded to fp32
-};
-
-// Exact keys of the candidate experts lane + 32*slot for the lanes set in `m` (one warp, all
-// lanes call it); each candidate lane receives its own key.
-__device__ __noinline__ Refined refine_slot(const RouterSrc src, const float* __restrict__ bias, int t, int slot,
-                                            uint32_t m, int lane) {
-  Refined out{-INFINITY, 0.f};
-  int ce[kCandBatch];
-  int nc = 0;
-  while (m) {
-    const int src_lane = __ffs(m) - 1;
-    m &= m - 1;
-#pragma unroll
-    for (int q = 0; q < kCandBatch; ++q)
-      if (q == nc) ce[q] = src_lane + 32 * slot;
-    if (++nc == kCandBatch || m == 0) {
-      double lg[kCandBatch];
-      exact_logits(src, t, ce, nc, lane, lg);
-#pragma unroll
-      for (int q = 0; q < kCandBatch; ++q) {
-        if (q < nc && lane == (ce[q] & 31)) {
-          const double s64 = 1.0 / (1.0 + exp(-lg[q]));
-          out.key = s64 + (bias ? (double)bias[ce[q]] : 0.0);
-          out.s = (float)s64;
-        }
-      }
-      nc = 0;
-    }
-  }
-  return out;
+    dots_df_part(static_cast<const float*>(r.x) + xo, static_cast<const float*>(r.w), r.d, ce, nc, part, nparts,
+                 lane, out);
 }
 
 // One warp per token.  Keys s + b are packed as (orderable(key) << 32) | (~expert) so that the
-// 64-bit maximum is the largest key and, among equal keys, the lowest expert index.
+// 64-bit maximum is the largest key and, among equal keys, the lowest expert index.  Lane l holds
+// experts l, l + 32, ... (NPL slots); after the pass, lane j < k holds the rank-j winner.
 //
 // The logits come from a GEMM whose error is bounded by `src.margin`, so a key is known to
 // within eta = margin/4 (+ fp32 rounding).  When the k-th and (k+1)-th keys are closer than
 // 2*eta the selected set is not certain: every expert whose key lies in the band around the
 // boundary has its logit recomputed to ~44 bits and its key evaluated in fp64, and the open
-// slots are filled from those keys (ties to the lower index).  Experts above the
-// band are in for certain, experts below it out.  The output lists the certain experts in
-// descending key order, then the refined winners in descending exact-key order.
-// Selection for token t by one warp.  Without REFINE, a token whose boundary is not certain is
-// left unwritten and the function returns true; with REFINE its boundary is settled exactly.
-template <int NPL, bool REFINE>
-__device__ __forceinline__ bool topk_token(const float* __restrict__ logits, const float* __restrict__ bias,
-                                           const RouterSrc& src, int t, int E, int k, int32_t* __restrict__ idx,
-                                           float* __restrict__ p, int lane) {
+// slots are filled from those keys (ties to the lower index).  Experts above the band are in
+// for certain, experts below it out.  The output lists the certain experts in descending key
+// order, then the refined winners in descending exact-key order.
+template <int NPL>
+struct TopkState {
+  float kf[NPL], sv[NPL];  // keys and scores of this lane's experts
+  int my_e;                // lane j < k: expert of rank j
+  float my_s, my_kf;       // its score and key
+  float a_k, a_k1;         // k-th and (k+1)-th keys
+};
+
+__device__ __forceinline__ float key_eta(const RouterSrc& src) { return 0.25f * src.margin + 1e-6f; }
+
+template <int NPL>
+__device__ __forceinline__ void topk_pass(const float* __restrict__ logits, const float* __restrict__ bias, int t,
+                                          int E, int k, int lane, TopkState<NPL>& st) {
   const float* row = logits + (size_t)t * E;
-  float kf[NPL], sv[NPL];
   uint32_t taken = 0;
 #pragma unroll
   for (int i = 0; i < NPL; ++i) {
     const int e = lane + 32 * i;
-    kf[i] = -INFINITY;
-    sv[i] = 0.f;
+    st.kf[i] = -INFINITY;
+    st.sv[i] = 0.f;
     if (e < E) {
       const float s = 1.0f / (1.0f + expf(-row[e]));
-      kf[i] = bias ? s + bias[e] : s;
-      sv[i] = s;
+      st.kf[i] = bias ? s + bias[e] : s;
+      st.sv[i] = s;
     }
   }
-  int my_e = 0;
-  float my_s = 0.f, my_kf = 0.f, a_k = 0.f, a_k1 = -INFINITY;
+  st.my_e = 0;
+  st.my_s = 0.f;
+  st.my_kf = 0.f;
+  st.a_k = 0.f;
+  st.a_k1 = -INFINITY;
   const int rounds = k < E ? k + 1 : k;
   for (int j = 0; j < rounds; ++j) {
     uint64_t best = 0;
@@ -191,7 +172,7 @@ __device__ __forceinline__ bool topk_token(const float* __restrict__ logits, con
     for (int i = 0; i < NPL; ++i) {
       const int e = lane + 32 * i;
       if (e < E && !((taken >> i) & 1u)) {
-        const uint64_t pk = ((uint64_t)orderable(kf[i]) << 32) | (uint64_t)(0xFFFFFFFFu - (uint32_t)e);
+        const uint64_t pk = ((uint64_t)orderable(st.kf[i]) << 32) | (uint64_t)(0xFFFFFFFFu - (uint32_t)e);
         best = pk > best ? pk : best;
       }
     }
@@ -203,7 +184,7 @@ __device__ __forceinline__ bool topk_token(const float* __restrict__ logits, con
     const int e_win = (int)(0xFFFFFFFFu - (uint32_t)(best & 0xFFFFFFFFu));
     const float kf_win = from_orderable((uint32_t)(best >> 32));
     if (j == k) {
-      a_k1 = kf_win;
+      st.a_k1 = kf_win;
       break;
     }
     const int owner = e_win & 31, slot = e_win >> 5;
@@ -212,40 +193,151 @@ __device__ __forceinline__ bool topk_token(const float* __restrict__ logits, con
 #pragma unroll
       for (int i = 0; i < NPL; ++i)
         if (i == slot) {
-          s_here = sv[i];
+          s_here = st.sv[i];
           taken |= 1u << i;
         }
     }
     const float s_win = __shfl_sync(0xffffffffu, s_here, owner);
     if (lane == j) {
-      my_e = e_win;
-      my_s = s_win;
-      my_kf = kf_win;
+      st.my_e = e_win;
+      st.my_s = s_win;
+      st.my_kf = kf_win;
     }
-    if (j == k - 1) a_k = kf_win;
+    if (j == k - 1) st.a_k = kf_win;
   }
+}
 
-  const float eta = 0.25f * src.margin + 1e-6f;
-  if (k < E && a_k - a_k1 < 2.0f * eta) {
-    if (!REFINE) return true;
-    const float hi = a_k + 2.0f * eta, lo = a_k1 - 2.0f * eta;
-    const int n_cert = __popc(__ballot_sync(0xffffffffu, lane < k && my_kf > hi));  // ranks 0..n_cert-1
-    double ex[NPL];
-#pragma unroll
-    for (int i = 0; i < NPL; ++i) ex[i] = -INFINITY;
-    // exact keys for every expert in the band, slot by slot
+// p = s / sum(s over the selected set), summed in rank order; lanes j < k store rank j.
+__device__ __forceinline__ void topk_write(int t, int k, int my_e, float my_s, int32_t* __restrict__ idx,
+                                           float* __restrict__ p, int lane) {
+  float sum = 0.f;
+  for (int j = 0; j < k; ++j) sum += __shfl_sync(0xffffffffu, my_s, j);  // rank order
+  if (lane < k) {
+    idx[(size_t)t * k + lane] = my_e;
+    p[(size_t)t * k + lane] = my_s / sum;
+  }
+}
+
+// Pass 1: one warp per token; tokens whose boundary is uncertain go to the refinement list.
+template <int NPL>
+__global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ logits, const float* __restrict__ bias,
+                                                   RouterSrc src, int T, int E, int k, int32_t* __restrict__ idx,
+                                                   float* __restrict__ p, int32_t* __restrict__ refine_list,
+                                                   int32_t* __restrict__ refine_count) {
+  const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (t >= T) return;
+  TopkState<NPL> st;
+  topk_pass<NPL>(logits, bias, t, E, k, lane, st);
+  if (k < E && st.a_k - st.a_k1 < 2.0f * key_eta(src)) {
+    if (lane == 0) refine_list[atomicAdd(refine_count, 1)] = t;  // list order is irrelevant: tokens are independent
+    return;
+  }
+  topk_write(t, k, st.my_e, st.my_s, idx, p, lane);
+}
+
+constexpr int kRefineWarps = 4;  // warps of a refinement CTA
+constexpr int kMaxCand = 64;     // boundary candidates per round
+
+// Shared memory of one refinement group (a warp, or the whole CTA).
+struct RefineSmem {
+  int* cand;       // [kMaxCand] candidate experts of this round
+  float2* part;    // [G][kMaxCand] partial logits (double-float) of the G warps
+  double* key;     // [kMaxCand] exact keys
+  float* s;        // [kMaxCand] exact scores rounded to fp32
+  int* n;          // candidates in this round
+};
+
+template <int G>
+__device__ __forceinline__ void group_sync() {
+  if (G == 1)
+    __syncwarp();
+  else
+    __syncthreads();
+}
+
+// Settle the selection of token t exactly: G warps (gw = 0..G-1) cooperate.  Warp 0 of the group
+// repeats the selection and lists the experts in the band around the boundary (rounds of at most
+// kMaxCand); the G warps recompute their logits to ~44 bits, warp gw over the 256-element blocks
+// gw, gw + G, ... of d, and warp 0 sums the G partials in a fixed order, takes fp64 keys and fills
+// the open ranks.
+template <int NPL, int G>
+__device__ __forceinline__ void refine_token(const float* __restrict__ logits, const float* __restrict__ bias,
+                                             const RouterSrc& src, int t, int E, int k, int32_t* __restrict__ idx,
+                                             float* __restrict__ p, int gw, int lane, const RefineSmem& sm) {
+  const uint32_t lt_mask = (1u << lane) - 1u;
+  TopkState<NPL> st;
+  double ex[NPL];
+  uint32_t pend = 0;  // bit i: this lane's expert lane + 32 i is in the band and not yet refined
+  int n_cert = 0;
+  if (gw == 0) {
+    topk_pass<NPL>(logits, bias, t, E, k, lane, st);
+    const float eta = key_eta(src);
+    const float hi = st.a_k + 2.0f * eta, lo = st.a_k1 - 2.0f * eta;
+    n_cert = __popc(__ballot_sync(0xffffffffu, lane < k && st.my_kf > hi));  // ranks 0..n_cert-1
 #pragma unroll
     for (int i = 0; i < NPL; ++i) {
+      ex[i] = -INFINITY;
       const int e = lane + 32 * i;
-      const uint32_t m = __ballot_sync(0xffffffffu, e < E && kf[i] >= lo && kf[i] <= hi);
-      if (m) {
-        const Refined rf = refine_slot(src, bias, t, i, m, lane);
-        if ((m >> lane) & 1u) {
-          ex[i] = rf.key;
-          sv[i] = rf.s;
+      if (e < E && st.kf[i] >= lo && st.kf[i] <= hi) pend |= 1u << i;
+    }
+  }
+  while (true) {
+    int pos[NPL];
+    if (gw == 0) {
+      int cnt = 0;
+#pragma unroll
+      for (int i = 0; i < NPL; ++i) {
+        pos[i] = -1;
+        const bool mine = (pend >> i) & 1u;
+        const uint32_t m = __ballot_sync(0xffffffffu, mine);
+        const int at = cnt + __popc(m & lt_mask);
+        if (mine && at < kMaxCand) {
+          sm.cand[at] = lane + 32 * i;
+          pos[i] = at;
+          pend &= ~(1u << i);
         }
+        cnt += __popc(m);
+      }
+      if (lane == 0) *sm.n = cnt < kMaxCand ? cnt : kMaxCand;
+    }
+    group_sync<G>();
+    const int nc_total = *sm.n;
+    if (nc_total == 0) break;  // uniform over the group
+    for (int b0 = 0; b0 < nc_total; b0 += kCandBatch) {
+      int ce[kCandBatch];
+      const int nc = nc_total - b0 < kCandBatch ? nc_total - b0 : kCandBatch;
+#pragma unroll
+      for (int m = 0; m < kCandBatch; ++m) ce[m] = m < nc ? sm.cand[b0 + m] : 0;
+      DF part[kCandBatch];
+      exact_logit_parts(src, t, ce, nc, gw, G, lane, part);
+      if (lane == 0) {
+#pragma unroll
+        for (int m = 0; m < kCandBatch; ++m)
+          if (m < nc) sm.part[gw * kMaxCand + b0 + m] = make_float2(part[m].hi, part[m].lo);
       }
     }
+    group_sync<G>();
+    if (gw == 0) {
+      for (int c = lane; c < nc_total; c += 32) {
+        DF a{sm.part[c].x, sm.part[c].y};
+#pragma unroll
+        for (int q = 1; q < G; ++q) a = df_add(a, DF{sm.part[q * kMaxCand + c].x, sm.part[q * kMaxCand + c].y});
+        const double s64 = 1.0 / (1.0 + exp(-((double)a.hi + (double)a.lo)));
+        sm.key[c] = s64 + (bias ? (double)bias[sm.cand[c]] : 0.0);
+        sm.s[c] = (float)s64;
+      }
+      __syncwarp();
+#pragma unroll
+      for (int i = 0; i < NPL; ++i)
+        if (pos[i] >= 0) {
+          ex[i] = sm.key[pos[i]];
+          st.sv[i] = sm.s[pos[i]];
+        }
+    }
+    group_sync<G>();  // cand, part and key are rewritten by the next round
+  }
+  if (gw == 0) {
     for (int q = n_cert; q < k; ++q) {
       double bv = -INFINITY;
       int be = 0x7FFFFFFF;
@@ -272,50 +364,45 @@ __device__ __forceinline__ bool topk_token(const float* __restrict__ logits, con
 #pragma unroll
         for (int i = 0; i < NPL; ++i)
           if (i == slot) {
-            s_here = sv[i];
+            s_here = st.sv[i];
             ex[i] = -INFINITY;
           }
       }
       const float s_win = __shfl_sync(0xffffffffu, s_here, owner);
       if (lane == q) {
-        my_e = be;
-        my_s = s_win;
+        st.my_e = be;
+        st.my_s = s_win;
       }
     }
+    topk_write(t, k, st.my_e, st.my_s, idx, p, lane);
   }
-  float sum = 0.f;
-  for (int j = 0; j < k; ++j) sum += __shfl_sync(0xffffffffu, my_s, j);  // rank order
-  if (lane < k) {
-    idx[(size_t)t * k + lane] = my_e;
-    p[(size_t)t * k + lane] = my_s / sum;
-  }
-  return false;
+  group_sync<G>();  // *n of this token is read by every warp before the next token's round
 }
 
-// Pass 1: one warp per token; tokens whose boundary is uncertain go to the refinement list.
+// Pass 2: the listed tokens.  With enough of them to keep every warp busy for several tokens,
+// each warp settles its own tokens; otherwise the 4 warps of a CTA split d for one token at a
+// time (short lists: decode and most prefill batches).
 template <int NPL>
-__global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ logits, const float* __restrict__ bias,
-                                                   RouterSrc src, int T, int E, int k, int32_t* __restrict__ idx,
-                                                   float* __restrict__ p, int32_t* __restrict__ refine_list,
-                                                   int32_t* __restrict__ refine_count) {
-  const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (t >= T) return;
-  if (topk_token<NPL, false>(logits, bias, src, t, E, k, idx, p, lane) && lane == 0)
-    refine_list[atomicAdd(refine_count, 1)] = t;  // list order is irrelevant: each token is independent
-}
-
-// Pass 2: the listed tokens, their boundary experts' logits recomputed exactly.
-template <int NPL>
-__global__ void __launch_bounds__(128) topk_refine_kernel(const float* __restrict__ logits,
-                                                          const float* __restrict__ bias, RouterSrc src, int E,
-                                                          int k, int32_t* __restrict__ idx, float* __restrict__ p,
-                                                          const int32_t* __restrict__ refine_list,
-                                                          const int32_t* __restrict__ refine_count) {
-  const int lane = threadIdx.x & 31;
+__global__ void __launch_bounds__(32 * kRefineWarps) topk_refine_kernel(
+    const float* __restrict__ logits, const float* __restrict__ bias, RouterSrc src, int E, int k,
+    int32_t* __restrict__ idx, float* __restrict__ p, const int32_t* __restrict__ refine_list,
+    const int32_t* __restrict__ refine_count) {
+  __shared__ int s_cand[kRefineWarps][kMaxCand];
+  __shared__ float2 s_part[kRefineWarps][kMaxCand];
+  __shared__ double s_key[kRefineWarps][kMaxCand];
+  __shared__ float s_s[kRefineWarps][kMaxCand];
+  __shared__ int s_n[kRefineWarps];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n = *refine_count;
-  for (int w = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; w < n; w += (gridDim.x * blockDim.x) >> 5)
-    topk_token<NPL, true>(logits, bias, src, refine_list[w], E, k, idx, p, lane);
+  if (n >= 4 * (int)gridDim.x * kRefineWarps) {  // at least 4 tokens per warp
+    const RefineSmem sm{s_cand[warp], s_part[warp], s_key[warp], s_s[warp], &s_n[warp]};
+    for (int w = blockIdx.x * kRefineWarps + warp; w < n; w += gridDim.x * kRefineWarps)
+      refine_token<NPL, 1>(logits, bias, src, refine_list[w], E, k, idx, p, 0, lane, sm);
+  } else {
+    const RefineSmem sm{s_cand[0], &s_part[0][0], s_key[0], s_s[0], &s_n[0]};
+    for (int w = blockIdx.x; w < n; w += gridDim.x)
+      refine_token<NPL, kRefineWarps>(logits, bias, src, refine_list[w], E, k, idx, p, warp, lane, sm);
+  }
 }
 
 __global__ void split_bf16x3_kernel(const float* __restrict__ w, int64_t n, __nv_bfloat16* __restrict__ out) {
