@@ -72,10 +72,16 @@ struct TcParams {
   uint32_t* status;
   uint64_t timeout_ns;
   int inject;
+  // split-K (dense, one M tile): k_splits ranges of kb_per_split k-blocks, raw fp32 accumulator
+  // tiles to partial[split][row][n_tile * BN + c] (ldp columns, split_stride floats per split)
+  int k_splits, kb_per_split;
+  float* partial;
+  int64_t ldp, split_stride;
 };
 
 struct Tile {
   int row0, row_end, n0, group;
+  int kb_lo, kb_hi, split;
 };
 
 template <int BN_OUT, bool GROUPED>
@@ -90,17 +96,25 @@ __device__ __forceinline__ Tile decode_tile(const TcParams& p, int t) {
     ti.row_end = min(ti.row0 + BM, p.offsets[tl.x + 1]);
     ti.n0 = n * BN_OUT;
     ti.group = tl.x;
+    ti.kb_lo = 0;
+    ti.kb_hi = p.num_kb;
+    ti.split = 0;
   } else {
-    const int m = t % p.num_m_tiles, n = t / p.num_m_tiles;
+    const int mn = p.num_m_tiles * p.num_n_tiles;
+    const int sp = t / mn, r = t - sp * mn;
+    const int m = r % p.num_m_tiles, n = r / p.num_m_tiles;
     ti.row0 = m * BM;
     ti.row_end = min(ti.row0 + BM, p.M);
     ti.n0 = n * BN_OUT;
     ti.group = 0;
+    ti.split = sp;
+    ti.kb_lo = sp * p.kb_per_split;
+    ti.kb_hi = min(p.num_kb, ti.kb_lo + p.kb_per_split);
   }
   return ti;
 }
 
-template <int BN, int EPI, bool GROUPED, bool AB_F16, bool FP4B>
+template <int BN, int EPI, bool GROUPED, bool AB_F16, bool FP4B, bool SPLIT = false>
 __global__ void __launch_bounds__(Cfg<BN, FP4B>::kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                    const __grid_constant__ CUtensorMap tmB1, const TcParams p) {
@@ -149,7 +163,7 @@ __global__ void __launch_bounds__(Cfg<BN, FP4B>::kThreads, 1)
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
 
-  const int total = (GROUPED ? *p.num_tiles : p.num_m_tiles) * p.num_n_tiles;
+  const int total = (GROUPED ? *p.num_tiles : p.num_m_tiles * p.k_splits) * p.num_n_tiles;
 
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------------ TMA producer
@@ -158,7 +172,7 @@ __global__ void __launch_bounds__(Cfg<BN, FP4B>::kThreads, 1)
     bool first = true;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
       const Tile ti = decode_tile<BN_OUT, GROUPED>(p, t);
-      for (int kb = 0; kb < p.num_kb; ++kb) {
+      for (int kb = ti.kb_lo; kb < ti.kb_hi; ++kb) {
         if (!ptx::mbar_wait_bounded(&empty1[stage], phase ^ 1u, abort_flag, p.status, p.timeout_ns, kWaitProducer)) goto done;
         const bool skip = p.inject && first && blockIdx.x == 0;  // test hook: drop one stage signal
         first = false;
@@ -201,11 +215,17 @@ __global__ void __launch_bounds__(Cfg<BN, FP4B>::kThreads, 1)
     for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
       const int acc = it & 1;
       const uint32_t use = (uint32_t)(it >> 1);
+      int kb_lo = 0, kb_hi = p.num_kb;
+      if (!GROUPED) {
+        const Tile ti = decode_tile<BN_OUT, GROUPED>(p, t);
+        kb_lo = ti.kb_lo;
+        kb_hi = ti.kb_hi;
+      }
       if (!ptx::mbar_wait_bounded(&tmem_empty[acc], (use & 1u) ^ 1u, abort_flag, p.status, p.timeout_ns, kWaitAccFree))
         goto done;
       ptx::tc_fence_after();
       const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
-      for (int kb = 0; kb < p.num_kb; ++kb) {
+      for (int kb = kb_lo; kb < kb_hi; ++kb) {
         if (FP4B && !ptx::mbar_wait_bounded(&full2[s2], ph2, abort_flag, p.status, p.timeout_ns, kWaitConverted)) goto done;
         if (!ptx::mbar_wait_bounded(&full1[s1], ph1, abort_flag, p.status, p.timeout_ns, kWaitFull)) goto done;
         ptx::tc_fence_after();
@@ -214,7 +234,7 @@ __global__ void __launch_bounds__(Cfg<BN, FP4B>::kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < BK / 16; ++kk)
           ptx::mma_f16(d_tmem, ptx::sw128_kmajor_desc(a_addr + kk * 32), ptx::sw128_kmajor_desc(b_addr + kk * 32),
-                       idesc, (kb | kk) != 0 ? 1u : 0u);
+                       idesc, (kb != kb_lo || kk != 0) ? 1u : 0u);
         ptx::mma_commit(&empty1[s1]);
         if (++s1 == S1) {
           s1 = 0;
@@ -246,7 +266,11 @@ __global__ void __launch_bounds__(Cfg<BN, FP4B>::kThreads, 1)
       const int row = ti.row0 + q * 32 + lane;
       const bool live = row < ti.row_end;
       const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
-      store_accumulator<BN, EPI>(t_row, row, live, ti.n0, p.N, p.C, p.ldc, p.row_scale);
+      if (SPLIT)  // raw accumulator columns of n tile n0 / BN_OUT, reduced later in split order
+        store_accumulator<BN, kEpiF32>(t_row, row, live, (ti.n0 / BN_OUT) * BN, (int)p.ldp,
+                                       p.partial + (int64_t)ti.split * p.split_stride, p.ldp, nullptr);
+      else
+        store_accumulator<BN, EPI>(t_row, row, live, ti.n0, p.N, p.C, p.ldc, p.row_scale);
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&tmem_empty[acc]);
@@ -353,11 +377,11 @@ done:
   }
 }
 
-template <int BN, int EPI, bool GROUPED, bool AB_F16, bool FP4B>
+template <int BN, int EPI, bool GROUPED, bool AB_F16, bool FP4B, bool SPLIT = false>
 cudaError_t launch_inst(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1, const TcParams& p,
                         int grid, cudaStream_t s) {
   using C = Cfg<BN, FP4B>;
-  auto kern = tc_gemm_kernel<BN, EPI, GROUPED, AB_F16, FP4B>;
+  auto kern = tc_gemm_kernel<BN, EPI, GROUPED, AB_F16, FP4B, SPLIT>;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
@@ -368,7 +392,55 @@ cudaError_t launch_inst(const CUtensorMap& a, const CUtensorMap& b0, const CUten
   return cudaGetLastError();
 }
 
+// Split-K reduction: out[row][f] = epilogue( sum over splits, in split order, of the partial
+// accumulators ).  GLU outputs f read gate column (f / 128) * 256 + f % 128 and the up column 128
+// to the right; the other epilogues read column f.  Four outputs per thread.
+template <int EPI>
+__global__ void __launch_bounds__(256) splitk_reduce_kernel(const float* __restrict__ part, int splits,
+                                                            int64_t split_stride, int64_t ldp, int M, int N,
+                                                            void* __restrict__ C, int64_t ldc) {
+  constexpr bool GLU = EPI == kEpiGluBF16 || EPI == kEpiGluF16;
+  const int n4 = N / 4;
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= (int64_t)M * n4) return;
+  const int row = (int)(i / n4), f0 = (int)(i - (int64_t)row * n4) * 4;
+  float v[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const int f = f0 + e;
+    const int64_t col = GLU ? (int64_t)(f / 128) * 256 + f % 128 : f;
+    const float* src = part + (int64_t)row * ldp + col;
+    float g = 0.f, u = 0.f;
+    for (int sp = 0; sp < splits; ++sp) {
+      g += src[sp * split_stride];
+      if (GLU) u += src[sp * split_stride + 128];
+    }
+    v[e] = GLU ? silu(g) * u : g;
+  }
+  if (EPI == kEpiF32) {
+    *reinterpret_cast<float4*>(static_cast<float*>(C) + (int64_t)row * ldc + f0) = make_float4(v[0], v[1], v[2], v[3]);
+  } else {
+    constexpr bool F16 = EPI == kEpiF16 || EPI == kEpiGluF16;
+    const uint32_t a = F16 ? pack_f16x2(v[0], v[1]) : pack_bf16x2(v[0], v[1]);
+    const uint32_t b = F16 ? pack_f16x2(v[2], v[3]) : pack_bf16x2(v[2], v[3]);
+    *reinterpret_cast<uint2*>(static_cast<uint16_t*>(C) + (int64_t)row * ldc + f0) = make_uint2(a, b);
+  }
+}
+
+template <int EPI>
+cudaError_t launch_split(const CUtensorMap& ma, const CUtensorMap& mb0, const CUtensorMap& mb1, const TcParams& p,
+                         int grid, cudaStream_t s) {
+  cudaError_t e = launch_inst<256, EPI, false, false, false, true>(ma, mb0, mb1, p, grid, s);
+  if (e != cudaSuccess) return e;
+  const int64_t n = (int64_t)p.M * (p.N / 4);
+  splitk_reduce_kernel<EPI><<<(unsigned)((n + 255) / 256), 256, 0, s>>>(p.partial, p.k_splits, p.split_stride, p.ldp,
+                                                                       p.M, p.N, p.C, p.ldc);
+  return cudaGetLastError();
+}
+
 }  // namespace
+
+size_t tc_splitk_partial_bytes(int num_sms) { return (size_t)num_sms * 256 * BM * sizeof(float); }
 
 cudaError_t launch_tc_gemm(const TcGemm& g, uint32_t* status, uint64_t timeout_ns, int inject_fault, int num_sms,
                            cudaStream_t s) {
@@ -413,9 +485,21 @@ cudaError_t launch_tc_gemm(const TcGemm& g, uint32_t* status, uint64_t timeout_n
   p.status = status;
   p.timeout_ns = timeout_ns;
   p.inject = inject_fault;
+  p.k_splits = 1;
+  p.kb_per_split = p.num_kb;
   const long long tiles = grouped ? (long long)g.max_tiles * p.num_n_tiles : (long long)p.num_m_tiles * p.num_n_tiles;
   if (tiles == 0) return cudaSuccess;
   const int grid = (int)(tiles < num_sms ? tiles : num_sms);
+  // One M tile and fewer tiles than SMs: split K so that tiles x splits fills the GPU.  The split
+  // count depends on N and K only, so every batch of up to 128 rows sums in the same order.
+  int splits = 1;
+  if (!grouped && !fp4 && !g.ab_f16 && g.partial && p.num_m_tiles == 1 && p.num_n_tiles * 2 <= num_sms &&
+      g.N % 4 == 0 && (g.epi == kEpiBF16 || g.epi == kEpiF16 || g.epi == kEpiGluBF16 || g.epi == kEpiF32)) {
+    splits = num_sms / p.num_n_tiles;
+    if (splits > p.num_kb / 4) splits = p.num_kb / 4;  // at least 4 k-blocks per split
+    if (splits < 1) splits = 1;
+  }
+  if (g.launch_count) *g.launch_count += splits > 1 ? 2 : 1;
   if (fp4) {
     if (!grouped) return cudaErrorInvalidValue;
     switch (g.epi) {
@@ -425,6 +509,22 @@ cudaError_t launch_tc_gemm(const TcGemm& g, uint32_t* status, uint64_t timeout_n
     return cudaErrorInvalidValue;
   }
   if (g.ab_f16) return cudaErrorInvalidValue;  // fp16 operands only come with converted MXFP4 weights
+  if (splits > 1) {
+    p.kb_per_split = (p.num_kb + splits - 1) / splits;
+    p.k_splits = (p.num_kb + p.kb_per_split - 1) / p.kb_per_split;
+    p.partial = g.partial;
+    p.ldp = (int64_t)p.num_n_tiles * 256;
+    p.split_stride = (int64_t)BM * p.ldp;
+    if ((size_t)p.k_splits * p.split_stride * sizeof(float) > g.partial_bytes) return cudaErrorInvalidValue;
+    const int grid_s = p.num_n_tiles * p.k_splits < num_sms ? p.num_n_tiles * p.k_splits : num_sms;
+    switch (g.epi) {
+      case kEpiBF16: return launch_split<kEpiBF16>(ma, mb0, mb1, p, grid_s, s);
+      case kEpiF16: return launch_split<kEpiF16>(ma, mb0, mb1, p, grid_s, s);
+      case kEpiGluBF16: return launch_split<kEpiGluBF16>(ma, mb0, mb1, p, grid_s, s);
+      case kEpiF32: return launch_split<kEpiF32>(ma, mb0, mb1, p, grid_s, s);
+    }
+    return cudaErrorInvalidValue;
+  }
   switch (g.epi) {
     case kEpiBF16:
       return grouped ? launch_inst<256, kEpiBF16, true, false, false>(ma, mb0, mb1, p, grid, s)

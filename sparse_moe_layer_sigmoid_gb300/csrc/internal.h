@@ -16,7 +16,7 @@ cudaError_t launch_router_logits(const void* x, int x_dtype, const void* w_route
 // K = 3d), fp32 activations the CUDA-core GEMM.  Adds its kernel count to *launches.
 cudaError_t launch_router(const void* x, int act, const void* w_router, int router_w, float* logits,
                           void* wr_split, int T, int E, int d, uint32_t* status, uint64_t timeout_ns, int num_sms,
-                          int* launches, cudaStream_t s);
+                          int* launches, cudaStream_t s, float* splitk = nullptr, size_t splitk_bytes = 0);
 // Exact split of fp32 W_r into three bf16 terms, out[t][e][c], t = hi, mid, lo:
 // w = hi + mid + lo with each term the bf16 rounding of what the previous terms left.
 cudaError_t launch_split_bf16x3(const float* w, int64_t n, void* out, cudaStream_t s);
@@ -118,7 +118,12 @@ struct TcGemm {
   const float* row_scale;
   int ab_f16;                // operands are fp16 (with MXFP4 B) instead of bf16
   const uint8_t* b_scale;    // non-null: B0 holds packed E2M1 bytes, b_scale E8M0 [depth][rows][K/32]
+  float* partial;            // split-K workspace (dense GEMMs of one M tile) or nullptr: no split
+  size_t partial_bytes;      // its size (tc_splitk_partial_bytes)
+  int* launch_count;         // incremented by the number of kernels launched (or nullptr)
 };
+// Workspace the split-K path needs at most (splits x N tiles <= SMs, 128 rows, 256 columns each).
+size_t tc_splitk_partial_bytes(int num_sms);
 cudaError_t launch_tc_gemm(const TcGemm& g, uint32_t* status, uint64_t timeout_ns, int inject_fault, int num_sms,
                            cudaStream_t s);
 

@@ -41,6 +41,8 @@ struct lmoe_handle {
   void* x_stage; // forward_host staging
   void* y_stage;
   void* wr_split; // bf16 hi/mid/lo terms of an fp32 W_r [3][E][d] (bf16 activations only)
+  float* splitk;  // split-K partial accumulators of dense tensor-core GEMMs with <= 128 rows
+  size_t splitk_bytes;
   int last_launches;
   uint64_t timeout_ns;
   int inject;
@@ -165,6 +167,8 @@ size_t layout(lmoe_handle* h, uint8_t* base) {
   h->x_stage = take(T * (size_t)c.d * ab);
   h->y_stage = take(T * (size_t)(identity ? c.latent : c.d) * ab);
   h->wr_split = (c.act == LMOE_BF16 && c.router_w == LMOE_F32) ? take(3 * E * (size_t)c.d * 2) : nullptr;
+  h->splitk_bytes = c.act == LMOE_BF16 ? tc_splitk_partial_bytes(h->num_sms) : 0;
+  h->splitk = h->splitk_bytes ? reinterpret_cast<float*>(take(h->splitk_bytes)) : nullptr;
   return off;
 }
 
@@ -212,7 +216,7 @@ lmoe_status run_routing(lmoe_handle* h, const void* x, int T, const lmoe_weights
   if (!ext_idx) {
     stage_begin(h, kStRouter, s);
     LMOE_TRY(launch_router(x, c.act, w->w_router, c.router_w, h->logits, h->wr_split, T, c.num_experts, c.d,
-                           h->status, h->timeout_ns, h->num_sms, &h->last_launches, s));
+                           h->status, h->timeout_ns, h->num_sms, &h->last_launches, s, h->splitk, h->splitk_bytes));
     stage_end(h, kStRouter, s);
     const RouterSrc rs{x, c.act, w->w_router, c.router_w, c.d, kRouterLogitMargin};
     LMOE_TRY(launch_topk(h->logits, w->router_bias, rs, T, c.num_experts, c.top_k, h->idx, h->p, h->refine_list,
@@ -231,11 +235,20 @@ lmoe_status run_routing(lmoe_handle* h, const void* x, int T, const lmoe_weights
 }
 
 // A tensor-core GEMM of the layer: dense GEMMs with at least 256 rows run on CTA pairs (256 x 256
-// tiles), everything else on single CTAs (128-row tiles).  Adds its launch to *launches.
-cudaError_t run_tc_gemm(lmoe_handle* h, const TcGemm& g, int inject, int* launches, cudaStream_t s) {
-  *launches += 1;
+// tiles), everything else on single CTAs (128-row tiles; dense ones of one M tile split K when
+// their N tiles alone would leave SMs idle).  Adds its launches to *launches.
+cudaError_t run_tc_gemm(lmoe_handle* h, TcGemm g, int inject, int* launches, cudaStream_t s) {
   const bool pair = !(h->cfg.flags & LMOE_FLAG_SINGLE_CTA_GEMM) && !inject && g.M >= kTileP && tc_pair_supported(g);
-  if (pair) return launch_tc_pair(g, h->status, h->timeout_ns, s);
+  if (pair) {
+    *launches += 1;
+    return launch_tc_pair(g, h->status, h->timeout_ns, s);
+  }
+  // dense GEMMs of at most 128 rows may split K over the SMs (decode batches)
+  if (!g.tiles) {
+    g.partial = h->splitk;
+    g.partial_bytes = h->splitk_bytes;
+  }
+  g.launch_count = launches;
   return launch_tc_gemm(g, h->status, h->timeout_ns, inject, h->num_sms, s);
 }
 

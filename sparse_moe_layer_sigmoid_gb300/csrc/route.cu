@@ -585,7 +585,7 @@ cudaError_t launch_router_logits(const void* x, int x_dtype, const void* w_route
 
 cudaError_t launch_router(const void* x, int act, const void* w_router, int router_w, float* logits,
                           void* wr_split, int T, int E, int d, uint32_t* status, uint64_t timeout_ns, int num_sms,
-                          int* launches, cudaStream_t s) {
+                          int* launches, cudaStream_t s, float* splitk, size_t splitk_bytes) {
   if (act != kBF16) {
     if (launches) *launches += 1;
     return launch_router_logits(x, act, w_router, router_w, logits, T, E, d, s);
@@ -612,7 +612,9 @@ cudaError_t launch_router(const void* x, int act, const void* w_router, int rout
   g.a_k_period = d;
   g.C = logits;
   g.ldc = E;
-  if (launches) *launches += 1;
+  g.partial = splitk;
+  g.partial_bytes = splitk_bytes;
+  g.launch_count = launches;
   return launch_tc_gemm(g, status, timeout_ns, 0, num_sms, s);
 }
 
