@@ -13,7 +13,7 @@
 // epilogue of one tile overlaps the main loop of the next.
 //
 // MXFP4 weights (B as E2M1 pairs + one E8M0 scale per 32 elements along K): TMA stages the
-// packed bytes, and 8 converter warps turn each 256 x 64 block into fp16 with the hardware
+// packed bytes, and 16 converter warps turn each 256 x 64 block into fp16 with the hardware
 // pair conversion (cvt.rn.f16x2.e2m1x2) times the block scale, writing the 128-byte-swizzled
 // K-major layout the MMA reads; the MMA then runs kind::f16 with fp16 activations.  Values are
 // exact: an E2M1 value times a power of two fits fp16 for scale exponents in [-24, 13].
@@ -50,7 +50,8 @@ struct Cfg {
   static constexpr uint32_t kRing1 = kS1 * kStage1Bytes;
   static constexpr uint32_t kRing2 = kS2 * kBBytes;
   static constexpr uint32_t kTmemCols = 2 * BN;                  // two fp32 accumulators
-  static constexpr int kConvWarps = FP4B ? BN / 32 : 0;          // one converter thread per B row
+  static constexpr int kConvWarps = FP4B ? BN / 16 : 0;          // 2 * BN threads: one per (B row, K half)
+  static constexpr int kRowsPerThread = FP4B ? 2 * BN / (32 * kConvWarps) : 0;
   static constexpr int kThreads = kBaseThreads + 32 * kConvWarps;
   static constexpr size_t kSmem = (size_t)kRing1 + kRing2 + 1024 + 512;
 };
@@ -277,22 +278,25 @@ __global__ void __launch_bounds__(Cfg<BN, FP4B>::kThreads, 1)
     }
   } else if (FP4B && warp >= 6) {
     // ------------------------------------------------------------------ E2M1 -> fp16 converters
-    // Thread i converts one 32-element scale block (half i%2 of the k-block) of B rows i/2 and
-    // i/2 + 128; consecutive threads read consecutive 16-byte chunks.  Each k-block is handed to
-    // the MMA as soon as it is converted.
+    // Thread i converts one 32-element scale block (half i%2 of the k-block) of B rows i/2,
+    // i/2 + 32 * kConvWarps / 2, ... (kRowsPerThread rows); consecutive threads read consecutive
+    // 16-byte chunks.  Each k-block is handed to the MMA as soon as it is converted.
     constexpr int G = 1;
-    const int cid = threadIdx.x - kBaseThreads;  // 0..255
+    constexpr int RPT = C::kRowsPerThread > 0 ? C::kRowsPerThread : 1;  // (instantiated only with FP4B)
+    const int cid = threadIdx.x - kBaseThreads;  // 0 .. 32 * kConvWarps - 1
     const int half = cid & 1;
-    const int rows[2] = {cid >> 1, (cid >> 1) + kBoxRows};
+    int rows[RPT];
+#pragma unroll
+    for (int h = 0; h < RPT; ++h) rows[h] = (cid >> 1) + h * (16 * C::kConvWarps);
     const int kscale = p.num_kb * 2;  // E8M0 bytes per B row (K / 32)
     int s1 = 0, s2 = 0;
     uint32_t ph1 = 0, ph2 = 0;
     bool bad = false;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
       const Tile ti = decode_tile<BN_OUT, GROUPED>(p, t);
-      const uint4* srow[2];
+      const uint4* srow[RPT];
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
+      for (int h = 0; h < RPT; ++h) {
         const int r = rows[h];
         int brow, bgrp;
         if (GLU) {
@@ -305,11 +309,11 @@ __global__ void __launch_bounds__(Cfg<BN, FP4B>::kThreads, 1)
         }
         srow[h] = reinterpret_cast<const uint4*>(p.b_scale + ((int64_t)bgrp * p.b_rows + brow) * kscale);
       }
-      uint4 sc16[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+      uint4 sc16[RPT];
       for (int kb0 = 0; kb0 < p.num_kb; kb0 += G) {  // num_kb % 8 == 0
         if ((kb0 & 7) == 0) {
-          sc16[0] = __ldg(srow[0] + (kb0 >> 3));  // scales of 8 k-blocks (512 elements)
-          sc16[1] = __ldg(srow[1] + (kb0 >> 3));
+#pragma unroll
+          for (int h = 0; h < RPT; ++h) sc16[h] = __ldg(srow[h] + (kb0 >> 3));  // scales of 8 k-blocks
         }
         int gs1[G], gs2[G];
         uint32_t gp1[G], gp2[G];
@@ -343,7 +347,7 @@ __global__ void __launch_bounds__(Cfg<BN, FP4B>::kThreads, 1)
           const int byte = (kb & 7) * 2 + half;  // scale index within the 16-byte vector
           const int wsel = byte >> 2;
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
+          for (int h = 0; h < RPT; ++h) {
             const int r = rows[h];
             const uint4 qv =
                 *reinterpret_cast<const uint4*>(smem + gs1[g] * C::kStage1Bytes + C::kABytes + r * (BK / 2) + half * 16);
