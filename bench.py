@@ -54,6 +54,27 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+def max_over_ranks(x, dist, device):
+    """Largest ``x`` over all ranks: the slowest replica sets the job's step time."""
+    if dist is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(world, tokens_per_rank, ms):
+    """Whole-job throughput: every replica processes ``tokens_per_rank`` tokens per step."""
+    return world * tokens_per_rank / (ms * 1e-3)
+
+
+def rank_env():
+    """(world, rank, local rank) from the launcher's environment (1, 0, 0 without one)."""
+    return (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
 def expert_weight_bytes(cfg, rows, cols):
     """Stored bytes of one routed weight matrix [rows][cols] (MXFP4: E2M1 + one E8M0 per 32)."""
     if cfg.routed_w == "mxfp4":
@@ -248,9 +269,7 @@ def main():
     from sparse_moe_layer_sigmoid_gb300 import configs
 
     cfg = configs.CONFIGS[args.workload]
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
+    world, rank, local = rank_env()
     dist = None
     if world > 1:
         import torch.distributed as dist
@@ -328,11 +347,7 @@ def main():
     if dist:
         dist.barrier()
     clk = clocks.stop() if clocks else None
-    ms = sum(step_ms) / len(step_ms)
-    if dist:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(sum(step_ms) / len(step_ms), dist, dev)
     if layer.status() != 0:
         raise RuntimeError("layer reported an error status during the timed steps")
 
@@ -349,11 +364,7 @@ def main():
         t0 = time.perf_counter()
         layer.forward_host(x_host, inp, y_host)
         e2e_ms.append(1e3 * (time.perf_counter() - t0))
-    e2e = sum(e2e_ms) / len(e2e_ms)
-    if dist:
-        t = torch.tensor([e2e], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e = float(t.item())
+    e2e = max_over_ranks(sum(e2e_ms) / len(e2e_ms), dist, dev)
     elem = x.element_size()
 
     peaks, src = load_peaks()
@@ -380,7 +391,7 @@ def main():
         traffic = tr["bytes_per_launch"]
     total_flops = sum(a for kd, a in work.values() if kd in ("tensor", "alu"))
 
-    line = {"metric": METRIC, "value": world * cfg.tokens / (ms * 1e-3), "unit": UNIT, "n_gpus": world,
+    line = {"metric": METRIC, "value": job_tokens_per_s(world, cfg.tokens, ms), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": cfg.act, "data": "synthetic",
             "config": workload_config(cfg, args),
@@ -391,7 +402,7 @@ def main():
             "layer": {"flops": total_flops, "achieved_tflops": total_flops / (ms * 1e-3) / 1e12,
                       "frac_of_bf16_peak": total_flops / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"],
                       "stages_ms": st_ms},
-            "e2e": {"value": world * cfg.tokens / (e2e * 1e-3), "unit": UNIT,
+            "e2e": {"value": job_tokens_per_s(world, cfg.tokens, e2e), "unit": UNIT,
                     "h2d_bytes_per_step": cfg.tokens * cfg.d * elem,
                     "d2h_bytes_per_step": cfg.tokens * layer.out_width * elem},
             "gpu_launches": launches,

@@ -71,19 +71,41 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const T* __restrict__
 #pragma unroll
     for (int e = 0; e < 8; ++e) acc[i][e] = 0.f;
 
-  for (int j = 0; j < k; ++j) {
-    const int r = row_of[(size_t)t * k + j];
-    if (r < 0) continue;
-    const float w = p ? p[(size_t)t * k + j] : 1.0f;
-    const uint4* src = reinterpret_cast<const uint4*>(o + (size_t)r * width);
+  // U expert rows at a time: their loads are all issued before any is summed, and the sums still
+  // run in rank order j = 0..k-1.
+  constexpr int U = VPT <= 4 ? 4 : 2;
+  for (int j0 = 0; j0 < k; j0 += U) {
+    int r[U];
+    float w[U];
+    uint4 raw[U][VPT];
 #pragma unroll
-    for (int i = 0; i < VPT; ++i) {
-      const int v = threadIdx.x + i * kThreads;
-      if (v < nvec) {
-        float f[8];
-        unpack(__ldg(src + v), f, T());
+    for (int u = 0; u < U; ++u) {
+      const int j = j0 + u;
+      r[u] = j < k ? row_of[(size_t)t * k + j] : -1;
+      w[u] = p && j < k ? p[(size_t)t * k + j] : 1.0f;
+    }
 #pragma unroll
-        for (int e = 0; e < EPV; ++e) acc[i][e] = p ? fmaf(w, f[e], acc[i][e]) : acc[i][e] + f[e];
+    for (int u = 0; u < U; ++u) {
+      if (r[u] < 0) continue;
+      const uint4* src = reinterpret_cast<const uint4*>(o + (size_t)r[u] * width);
+#pragma unroll
+      for (int i = 0; i < VPT; ++i) {
+        const int v = threadIdx.x + i * kThreads;
+        if (v < nvec) raw[u][i] = __ldg(src + v);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      if (r[u] < 0) continue;
+#pragma unroll
+      for (int i = 0; i < VPT; ++i) {
+        const int v = threadIdx.x + i * kThreads;
+        if (v < nvec) {
+          float f[8];
+          unpack(raw[u][i], f, T());
+#pragma unroll
+          for (int e = 0; e < EPV; ++e) acc[i][e] = p ? fmaf(w[u], f[e], acc[i][e]) : acc[i][e] + f[e];
+        }
       }
     }
   }

@@ -73,7 +73,7 @@ struct TcParams {
   uint32_t* status;
   uint64_t timeout_ns;
   int inject;
-  // split-K (dense, one M tile): k_splits ranges of kb_per_split k-blocks, raw fp32 accumulator
+  // split-K (dense, few output tiles): k_splits ranges of kb_per_split k-blocks, raw fp32 accumulator
   // tiles to partial[split][row][n_tile * BN + c] (ldp columns, split_stride floats per split)
   int k_splits, kb_per_split;
   float* partial;
@@ -494,12 +494,13 @@ cudaError_t launch_tc_gemm(const TcGemm& g, uint32_t* status, uint64_t timeout_n
   const long long tiles = grouped ? (long long)g.max_tiles * p.num_n_tiles : (long long)p.num_m_tiles * p.num_n_tiles;
   if (tiles == 0) return cudaSuccess;
   const int grid = (int)(tiles < num_sms ? tiles : num_sms);
-  // One M tile and fewer tiles than SMs: split K so that tiles x splits fills the GPU.  The split
-  // count depends on N and K only, so every batch of up to 128 rows sums in the same order.
+  // At most half as many output tiles as SMs: split K so that tiles x splits fills the GPU.  The
+  // split count depends on the tile count and K, so for one M tile (up to 128 rows) on N and K
+  // only: every batch of up to 128 rows sums in the same order.
   int splits = 1;
-  if (!grouped && !fp4 && !g.ab_f16 && g.partial && p.num_m_tiles == 1 && p.num_n_tiles * 2 <= num_sms &&
-      g.N % 4 == 0 && (g.epi == kEpiBF16 || g.epi == kEpiF16 || g.epi == kEpiGluBF16 || g.epi == kEpiF32)) {
-    splits = num_sms / p.num_n_tiles;
+  if (!grouped && !fp4 && !g.ab_f16 && g.partial && tiles * 2 <= num_sms && g.N % 4 == 0 &&
+      (g.epi == kEpiBF16 || g.epi == kEpiF16 || g.epi == kEpiGluBF16 || g.epi == kEpiF32)) {
+    splits = num_sms / (int)tiles;
     if (splits > p.num_kb / 4) splits = p.num_kb / 4;  // at least 4 k-blocks per split
     if (splits < 1) splits = 1;
   }
@@ -518,9 +519,10 @@ cudaError_t launch_tc_gemm(const TcGemm& g, uint32_t* status, uint64_t timeout_n
     p.k_splits = (p.num_kb + p.kb_per_split - 1) / p.kb_per_split;
     p.partial = g.partial;
     p.ldp = (int64_t)p.num_n_tiles * 256;
-    p.split_stride = (int64_t)BM * p.ldp;
+    p.split_stride = (int64_t)p.num_m_tiles * BM * p.ldp;
     if ((size_t)p.k_splits * p.split_stride * sizeof(float) > g.partial_bytes) return cudaErrorInvalidValue;
-    const int grid_s = p.num_n_tiles * p.k_splits < num_sms ? p.num_n_tiles * p.k_splits : num_sms;
+    const long long work = tiles * p.k_splits;
+    const int grid_s = (int)(work < num_sms ? work : num_sms);
     switch (g.epi) {
       case kEpiBF16: return launch_split<kEpiBF16>(ma, mb0, mb1, p, grid_s, s);
       case kEpiF16: return launch_split<kEpiF16>(ma, mb0, mb1, p, grid_s, s);

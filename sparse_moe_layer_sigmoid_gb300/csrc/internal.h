@@ -56,9 +56,10 @@ struct DispatchBuffers {
 };
 cudaError_t launch_dispatch(const int32_t* idx, const float* p, int T, int E, int k, const DispatchBuffers& b,
                             uint32_t* status, int* launches, cudaStream_t s);
-// dst[row_of[t][j]] = src[t] for every (t, j): rows of `width` elements of `elem_bytes`.
+// dst[row_of[t][j]] = src[t] for every (t, j) with row_of[t][j] >= 0: rows of `width` elements of
+// `elem_bytes` (a multiple of 16 bytes, at most 16 KB; 16-byte aligned buffers; k <= 32).
 cudaError_t launch_scatter_rows(const void* src, void* dst, const int32_t* row_of, int T, int k, int width,
-                                int elem_bytes, cudaStream_t s);
+                                int elem_bytes, uint32_t* status, uint64_t timeout_ns, int num_sms, cudaStream_t s);
 
 // ---------------------------------------------------------------- combine (combine.cu)
 // u_t = sum_j o[row_of[t][j]] (rank order, fp32) [times p[t][j] when p != nullptr];
@@ -118,7 +119,7 @@ struct TcGemm {
   const float* row_scale;
   int ab_f16;                // operands are fp16 (with MXFP4 B) instead of bf16
   const uint8_t* b_scale;    // non-null: B0 holds packed E2M1 bytes, b_scale E8M0 [depth][rows][K/32]
-  float* partial;            // split-K workspace (dense GEMMs of one M tile) or nullptr: no split
+  float* partial;            // split-K workspace (dense GEMMs of few tiles) or nullptr: no split
   size_t partial_bytes;      // its size (tc_splitk_partial_bytes)
   int* launch_count;         // incremented by the number of kernels launched (or nullptr)
 };

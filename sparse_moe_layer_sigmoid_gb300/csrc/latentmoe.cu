@@ -235,8 +235,8 @@ lmoe_status run_routing(lmoe_handle* h, const void* x, int T, const lmoe_weights
 }
 
 // A tensor-core GEMM of the layer: dense GEMMs with at least 256 rows run on CTA pairs (256 x 256
-// tiles), everything else on single CTAs (128-row tiles; dense ones of one M tile split K when
-// their N tiles alone would leave SMs idle).  Adds its launches to *launches.
+// tiles), everything else on single CTAs (128-row tiles; dense ones with at most half as many
+// output tiles as SMs split K).  Adds its launches to *launches.
 cudaError_t run_tc_gemm(lmoe_handle* h, TcGemm g, int inject, int* launches, cudaStream_t s) {
   const bool pair = !(h->cfg.flags & LMOE_FLAG_SINGLE_CTA_GEMM) && !inject && g.M >= kTileP && tc_pair_supported(g);
   if (pair) {
@@ -294,7 +294,8 @@ lmoe_status run_forward(lmoe_handle* h, const void* x, int T, const lmoe_weights
   }
   stage_end(h, kStWDown, s);
   // rows of z into expert-contiguous order
-  LMOE_TRY(launch_scatter_rows(h->z, h->z_perm, h->db.row_of, T, k, l, (int)ab, s));
+  LMOE_TRY(launch_scatter_rows(h->z, h->z_perm, h->db.row_of, T, k, l, (int)ab, h->status, h->timeout_ns,
+                               h->num_sms, s));
   stage_end(h, kStScatter, s);
   h->last_launches += 1;
 

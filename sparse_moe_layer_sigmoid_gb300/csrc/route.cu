@@ -9,6 +9,7 @@
 // which commute exactly).
 #include "common.cuh"
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace lmoe {
 namespace {
@@ -544,23 +545,62 @@ __global__ void __launch_bounds__(kDispatchChunk) dispatch_scatter_kernel(
   }
 }
 
-// One warp per token: read the token's row once, write it to each of its k rows.
-__global__ void __launch_bounds__(256) scatter_rows_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
-                                                           const int32_t* __restrict__ row_of, int T, int k,
-                                                           int nvec) {
-  const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (t >= T) return;
-  int rows[32];
-#pragma unroll
-  for (int j = 0; j < 32; ++j) rows[j] = (j < k) ? row_of[(size_t)t * k + j] : -1;
-  const uint4* s = src + (size_t)t * nvec;
-  for (int v = lane; v < nvec; v += 32) {
-    const uint4 val = s[v];
-#pragma unroll
-    for (int j = 0; j < 32; ++j)
-      if (j < k && rows[j] >= 0) dst[(size_t)rows[j] * nvec + v] = val;
+// Rows of z into expert-contiguous order with bulk copies: one warp per CTA keeps kScatterSlots
+// token rows in shared memory.  Lane 0 loads rows kScatterAhead tokens ahead of their use; lane j
+// writes the slot to the token's j-th destination row (k <= 32), one bulk group per token and lane.
+// A slot is reloaded once every lane's stores from it have finished reading.
+constexpr int kScatterSlots = 4, kScatterAhead = 2;
+
+__global__ void __launch_bounds__(32) scatter_rows_kernel(const char* __restrict__ src, char* __restrict__ dst,
+                                                          const int32_t* __restrict__ row_of, int T, int k,
+                                                          uint32_t row_bytes, uint32_t* status, uint64_t timeout_ns) {
+  extern __shared__ __align__(128) unsigned char slot_mem[];
+  __shared__ __align__(8) uint64_t full[kScatterSlots];
+  __shared__ int abort_flag;
+  const int lane = threadIdx.x;
+  const int first = blockIdx.x, stride = gridDim.x;
+  const int n = first < T ? (T - first + stride - 1) / stride : 0;  // tokens first, first + stride, ...
+  if (lane == 0) {
+    for (int i = 0; i < kScatterSlots; ++i) ptx::mbar_init(&full[i], 1);
+    abort_flag = 0;
+    ptx::fence_mbar_init();
   }
+  __syncwarp();
+  auto load = [&](int i) {
+    uint64_t* bar = &full[i % kScatterSlots];
+    ptx::mbar_arrive_expect_tx(bar, row_bytes);
+    ptx::bulk_load(slot_mem + (size_t)(i % kScatterSlots) * row_bytes, src + (size_t)(first + i * stride) * row_bytes,
+                   row_bytes, bar);
+  };
+  int issued = n < kScatterAhead ? n : kScatterAhead;
+  if (lane == 0)
+    for (int i = 0; i < issued; ++i) load(i);
+  int i = 0;
+  for (; i < n; ++i) {
+    if (i + kScatterAhead < n) {
+      // the slot of token i + ahead last held token i + ahead - slots: its stores are the
+      // (slots - ahead)-th most recent bulk group of every lane
+      ptx::bulk_wait_read<kScatterSlots - kScatterAhead - 1>();
+      __syncwarp();
+      if (lane == 0) load(i + kScatterAhead);
+      ++issued;
+    }
+    const int t = first + i * stride;
+    const int r = lane < k ? row_of[(size_t)t * k + lane] : -1;
+    const bool ok = ptx::mbar_wait_bounded(&full[i % kScatterSlots], (uint32_t)(i / kScatterSlots) & 1u, &abort_flag,
+                                           status, timeout_ns);
+    if (!__all_sync(0xffffffffu, ok)) break;
+    if (r >= 0) ptx::bulk_store(dst + (size_t)r * row_bytes, slot_mem + (size_t)(i % kScatterSlots) * row_bytes, row_bytes);
+    ptx::bulk_commit();
+  }
+  if (lane == 0)  // after a wait gave up: let the loads still in flight land before the CTA exits
+    for (int j = i; j < issued; ++j) {
+      const uint32_t bar = ptx::smem_addr(&full[j % kScatterSlots]);
+      const uint64_t t0 = globaltimer_ns();
+      while (!ptx::mbar_try_wait(bar, (uint32_t)(j / kScatterSlots) & 1u) && globaltimer_ns() - t0 < timeout_ns) {
+      }
+    }
+  ptx::bulk_wait_all();
 }
 
 }  // namespace
@@ -665,11 +705,24 @@ cudaError_t launch_dispatch(const int32_t* idx, const float* p, int T, int E, in
 }
 
 cudaError_t launch_scatter_rows(const void* src, void* dst, const int32_t* row_of, int T, int k, int width,
-                                int elem_bytes, cudaStream_t s) {
-  const int nvec = width * elem_bytes / 16;
-  const int warps = 8;
-  scatter_rows_kernel<<<(T + warps - 1) / warps, 32 * warps, 0, s>>>(
-      static_cast<const uint4*>(src), static_cast<uint4*>(dst), row_of, T, k, nvec);
+                                int elem_bytes, uint32_t* status, uint64_t timeout_ns, int num_sms, cudaStream_t s) {
+  const int64_t row_bytes = (int64_t)width * elem_bytes;
+  if (T <= 0) return cudaSuccess;
+  if (k < 1 || k > 32 || row_bytes % 16 || row_bytes > 16384 || (reinterpret_cast<uintptr_t>(src) & 15u) ||
+      (reinterpret_cast<uintptr_t>(dst) & 15u))
+    return cudaErrorInvalidValue;
+  const int smem = kScatterSlots * (int)row_bytes;  // <= 64 KB
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(scatter_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kScatterSlots * 16384);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const int per_sm = smem <= 32768 ? 6 : 3;
+  const int grid = T < per_sm * num_sms ? T : per_sm * num_sms;
+  scatter_rows_kernel<<<grid, 32, smem, s>>>(static_cast<const char*>(src), static_cast<char*>(dst), row_of, T, k,
+                                             (uint32_t)row_bytes, status, timeout_ns);
   return cudaGetLastError();
 }
 

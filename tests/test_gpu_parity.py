@@ -272,6 +272,54 @@ def test_edge_sizes_and_errors(binding):
     assert ei.value.status == binding.LMOE_ERR_INVALID_ARG
 
 
+@pytest.mark.parametrize("cfg", [
+    replace(SMALL_BF16, name="ties_bf16", top_k=5, seed=41),
+    replace(configs.ROUTING_DISPATCH_STRESS, name="ties_f32_router_zipf", tokens=600, d=512, latent=256,
+            experts=64, top_k=7, seed=42),
+    replace(configs.TINY_F32, name="ties_f32_skew", tokens=200, top_k=3, bias="normal1.5", seed=43),
+], ids=lambda c: c.name)
+def test_exact_ties_go_to_the_lower_index(binding, cfg):
+    """Experts 2j and 2j+1 get identical router rows and biases, so their keys tie exactly; with
+    k odd the k-th selected expert always has its twin as the (k+1)-th, and eq. 13's tie rule
+    keeps the lower index.  The expected sets come from the oracle's scores of the distinct
+    experts; tokens whose distinct boundary pairs are within 1e-6 of each other are skipped."""
+    dev = torch.device("cuda")
+    host_inp = inputs.make_inputs(cfg, "cpu")
+    w = host_inp["w_router"]
+    w[1::2] = w[0::2].clone()
+    if host_inp["router_bias"] is not None:
+        b = host_inp["router_bias"]
+        b[1::2] = b[0::2].clone()
+    inp = {k_: (None if v is None else v.to(dev)) for k_, v in host_inp.items()}
+    layer = binding.LatentMoE(cfg)
+    r = layer.route(inp["x"], inp)
+    assert layer.status() == 0
+    idx_gpu = r["idx"].cpu().numpy().astype(np.int64)
+    p_gpu = r["p"].cpu().numpy()
+    layer.close()
+
+    host = inputs.host_inputs(host_inp)
+    s_half = oracle.router_scores(oracle.widen(host["x"]), oracle.widen(host["w_router"])[0::2])
+    b_half = None if host["router_bias"] is None else oracle.widen(host["router_bias"])[0::2]
+    s_full = np.repeat(s_half, 2, axis=1)
+    b_full = None if b_half is None else np.repeat(b_half, 2)
+    k = cfg.top_k
+    want, _ = oracle.select_topk(s_full, b_full, k)
+    m = (k - 1) // 2  # rank of the boundary pair among the distinct experts
+    _, gap_after = oracle.select_topk(s_half, b_half, m + 1)
+    gap_before = oracle.select_topk(s_half, b_half, m)[1] if m > 0 else np.full(cfg.tokens, np.inf)
+    clear = (gap_after >= 1e-6) & (gap_before >= 1e-6)
+    assert clear.mean() > 0.99
+    # the boundary expert is always the even member of its pair
+    assert np.all(want[:, k - 1] % 2 == 0)
+    got_sets, want_sets = np.sort(idx_gpu, axis=1), np.sort(want, axis=1)
+    bad = np.any(got_sets != want_sets, axis=1) & clear
+    assert not bad.any(), f"{int(bad.sum())} tokens differ, e.g. {np.nonzero(bad)[0][:5]}"
+    p_want = oracle.route_weights(s_full, want)
+    assert np.allclose(p_by_expert(idx_gpu[clear], p_gpu[clear]), p_by_expert(want[clear], p_want[clear]),
+                       rtol=1e-4, atol=1e-7)
+
+
 def test_forward_routed_with_oracle_routing(binding):
     cfg = replace(SMALL_BF16, name="routed", seed=34)
     dev = torch.device("cuda")
