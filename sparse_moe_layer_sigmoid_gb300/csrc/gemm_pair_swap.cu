@@ -51,7 +51,6 @@ struct PSwapParams {
   int glu_h;         // > 0: gate/up weights [2h][K], 128 features per tile; 0: 256 rows per tile
   const int4* tiles; // token tiles of 256 rows: {expert, first tile of expert, tiles of expert, first row}
   const int32_t* num_tiles;
-  const int32_t* offsets;
   void* C;
   int64_t ldc;
   const float* row_scale;
@@ -66,19 +65,22 @@ struct PSwapTile {
 };
 
 // Work item t: expert-major, then weight tile, then token tile (consecutive items share the
-// weight tile, so an expert's weights are read from HBM once and re-read from L2).
-__device__ __forceinline__ PSwapTile decode_pswap(const PSwapParams& p, int t) {
-  const int q = t / p.num_wt;
-  const int4 tl = p.tiles[q];
+// weight tile, so an expert's weights are read from HBM once and re-read from L2).  The table
+// entry of item t is loaded one item ahead (pswap_entry) and decoded when the item starts, so
+// no role waits on a global load between items.
+__device__ __forceinline__ int4 pswap_entry(const PSwapParams& p, int t) { return p.tiles[t / p.num_wt]; }
+
+__device__ __forceinline__ PSwapTile decode_pswap(const PSwapParams& p, int t, int4 tl) {
+  const int rows = tl.z;
+  const int ntiles = (rows + kMaxN - 1) / kMaxN;
   const int local = t - tl.y * p.num_wt;
   PSwapTile ti;
   ti.expert = tl.x;
-  ti.wt = local / tl.z;
-  const int j = local - ti.wt * tl.z;
-  const int rows = p.offsets[tl.x + 1] - tl.w;
-  // tl.z = ceil(rows / 256) tiles of equal width (multiple of 16, at most 256): every tile has
-  // at least one row because width * (tl.z - 1) <= 256 * (tl.z - 1) < rows
-  const int width = ((rows + tl.z - 1) / tl.z + 15) & ~15;
+  ti.wt = local / ntiles;
+  const int j = local - ti.wt * ntiles;
+  // ntiles = ceil(rows / 256) tiles of equal width (multiple of 16, at most 256): every tile has
+  // at least one row because width * (ntiles - 1) <= 256 * (ntiles - 1) < rows
+  const int width = ((rows + ntiles - 1) / ntiles + 15) & ~15;
   ti.row0 = tl.w + j * width;
   ti.nrows = min(width, rows - j * width);
   ti.n = (ti.nrows + 15) & ~15;
@@ -131,8 +133,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------------ TMA producer (both CTAs)
     int stage = 0, iter = 0;
     uint32_t phase = 0;
+    int4 entry = pair < total ? pswap_entry(p, pair) : make_int4(0, 0, 0, 0);
     for (int t = pair; t < total; t += npairs) {
-      const PSwapTile ti = decode_pswap(p, t);
+      const PSwapTile ti = decode_pswap(p, t, entry);
+      if (t + npairs < total) entry = pswap_entry(p, t + npairs);
       // this CTA's token rows: N/2 from row0 + rank * N/2 (one 128-row box; rows past N/2 unused)
       const int xrow0 = ti.row0 + (int)rank * (ti.n >> 1);
       for (int kb = 0; kb < p.num_kb; ++kb, ++iter) {
@@ -162,8 +166,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     int s = 0;
     uint32_t ph = 0;
     int it = 0;
+    int4 entry = pair < total ? pswap_entry(p, pair) : make_int4(0, 0, 0, 0);
     for (int t = pair; t < total; t += npairs, ++it) {
-      const PSwapTile ti = decode_pswap(p, t);
+      const PSwapTile ti = decode_pswap(p, t, entry);
+      if (t + npairs < total) entry = pswap_entry(p, t + npairs);
       const uint32_t idesc = idesc0 | ((uint32_t)(ti.n >> 3) << 17);
       const int acc = it & 1;
       const uint32_t use = (uint32_t)(it >> 1);
@@ -194,8 +200,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     uint16_t* out = static_cast<uint16_t*>(p.C);
     int it = 0;
+    int4 entry = pair < total ? pswap_entry(p, pair) : make_int4(0, 0, 0, 0);
     for (int t = pair; t < total; t += npairs, ++it) {
-      const PSwapTile ti = decode_pswap(p, t);
+      const PSwapTile ti = decode_pswap(p, t, entry);
+      if (t + npairs < total) entry = pswap_entry(p, t + npairs);
       const int acc = it & 1;
       const uint32_t use = (uint32_t)(it >> 1);
       int ok = 1;
@@ -293,13 +301,13 @@ cudaError_t launch_pswap_inst(const CUtensorMap& w, const CUtensorMap& x, const 
 }  // namespace
 
 cudaError_t launch_tc_pair_swap(const TcSwap& g, const int4* tiles_p, const int32_t* num_tiles_p, int max_tiles_p,
-                                const int32_t* offsets, uint32_t* status, uint64_t timeout_ns, cudaStream_t s) {
+                                uint32_t* status, uint64_t timeout_ns, cudaStream_t s) {
   const bool glu = g.epi == kEpiGluBF16;
   if (g.epi != kEpiGluBF16 && g.epi != kEpiScaleBF16) return cudaErrorInvalidValue;
   if (g.w_scale || g.ab_f16 || g.K % BK || g.ldc % 8) return cudaErrorInvalidValue;
   if (glu ? (g.glu_h % 128 || g.out_features != g.glu_h) : g.out_features % (2 * kWRows))
     return cudaErrorInvalidValue;
-  if (!tiles_p || !num_tiles_p || !offsets) return cudaErrorInvalidValue;
+  if (!tiles_p || !num_tiles_p) return cudaErrorInvalidValue;
   CUtensorMap mw, mx;
   if (!(glu ? make_map_glu_interleaved(&mw, g.w, g.glu_h, kWRows / 32) : make_map(&mw, g.w, kWRows)) ||
       !make_map(&mx, g.act, kMaxN / 2))
@@ -310,7 +318,6 @@ cudaError_t launch_tc_pair_swap(const TcSwap& g, const int4* tiles_p, const int3
   p.glu_h = glu ? g.glu_h : 0;
   p.tiles = tiles_p;
   p.num_tiles = num_tiles_p;
-  p.offsets = offsets;
   p.C = g.C;
   p.ldc = g.ldc;
   p.row_scale = g.row_scale;

@@ -64,7 +64,6 @@ struct TcParams {
   int num_m_tiles, num_n_tiles;
   const int4* tiles;
   const int32_t* num_tiles;
-  const int32_t* offsets;
   void* C;
   int64_t ldc;
   const float* row_scale;
@@ -85,16 +84,22 @@ struct Tile {
   int kb_lo, kb_hi, split;
 };
 
+// Grouped mode: the tile-table entry of work item t, loaded one item ahead of its use so that no
+// role waits on a global load between items ({expert, first m-tile, rows, first row}).
+template <bool GROUPED>
+__device__ __forceinline__ int4 tile_entry(const TcParams& p, int t) {
+  return GROUPED ? p.tiles[t / p.num_n_tiles] : make_int4(0, 0, 0, 0);
+}
+
 template <int BN_OUT, bool GROUPED>
-__device__ __forceinline__ Tile decode_tile(const TcParams& p, int t) {
+__device__ __forceinline__ Tile decode_tile(const TcParams& p, int t, int4 tl) {
   Tile ti;
   if (GROUPED) {
-    const int q = t / p.num_n_tiles;
-    const int4 tl = p.tiles[q];
+    const int mt = (tl.z + BM - 1) / BM;  // m-tiles of the expert
     const int local = t - tl.y * p.num_n_tiles;
-    const int n = local / tl.z, m = local - n * tl.z;
+    const int n = local / mt, m = local - n * mt;
     ti.row0 = tl.w + m * BM;
-    ti.row_end = min(ti.row0 + BM, p.offsets[tl.x + 1]);
+    ti.row_end = min(ti.row0 + BM, tl.w + tl.z);
     ti.n0 = n * BN_OUT;
     ti.group = tl.x;
     ti.kb_lo = 0;
@@ -171,8 +176,10 @@ __global__ void __launch_bounds__(Cfg<BN, FP4B>::kThreads, 1)
     int stage = 0;
     uint32_t phase = 0;
     bool first = true;
+    int4 entry = (int)blockIdx.x < total ? tile_entry<GROUPED>(p, blockIdx.x) : make_int4(0, 0, 0, 0);
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
-      const Tile ti = decode_tile<BN_OUT, GROUPED>(p, t);
+      const Tile ti = decode_tile<BN_OUT, GROUPED>(p, t, entry);
+      if (t + (int)gridDim.x < total) entry = tile_entry<GROUPED>(p, t + gridDim.x);
       for (int kb = ti.kb_lo; kb < ti.kb_hi; ++kb) {
         if (!ptx::mbar_wait_bounded(&empty1[stage], phase ^ 1u, abort_flag, p.status, p.timeout_ns, kWaitProducer)) goto done;
         const bool skip = p.inject && first && blockIdx.x == 0;  // test hook: drop one stage signal
@@ -218,7 +225,7 @@ __global__ void __launch_bounds__(Cfg<BN, FP4B>::kThreads, 1)
       const uint32_t use = (uint32_t)(it >> 1);
       int kb_lo = 0, kb_hi = p.num_kb;
       if (!GROUPED) {
-        const Tile ti = decode_tile<BN_OUT, GROUPED>(p, t);
+        const Tile ti = decode_tile<BN_OUT, GROUPED>(p, t, make_int4(0, 0, 0, 0));
         kb_lo = ti.kb_lo;
         kb_hi = ti.kb_hi;
       }
@@ -255,8 +262,10 @@ __global__ void __launch_bounds__(Cfg<BN, FP4B>::kThreads, 1)
     // ------------------------------------------------------------------ epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     int it = 0;
+    int4 entry = (int)blockIdx.x < total ? tile_entry<GROUPED>(p, blockIdx.x) : make_int4(0, 0, 0, 0);
     for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
-      const Tile ti = decode_tile<BN_OUT, GROUPED>(p, t);
+      const Tile ti = decode_tile<BN_OUT, GROUPED>(p, t, entry);
+      if (t + (int)gridDim.x < total) entry = tile_entry<GROUPED>(p, t + gridDim.x);
       const int acc = it & 1;
       const uint32_t use = (uint32_t)(it >> 1);
       int ok = 1;
@@ -292,8 +301,10 @@ __global__ void __launch_bounds__(Cfg<BN, FP4B>::kThreads, 1)
     int s1 = 0, s2 = 0;
     uint32_t ph1 = 0, ph2 = 0;
     bool bad = false;
+    int4 entry = (int)blockIdx.x < total ? tile_entry<GROUPED>(p, blockIdx.x) : make_int4(0, 0, 0, 0);
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
-      const Tile ti = decode_tile<BN_OUT, GROUPED>(p, t);
+      const Tile ti = decode_tile<BN_OUT, GROUPED>(p, t, entry);
+      if (t + (int)gridDim.x < total) entry = tile_entry<GROUPED>(p, t + gridDim.x);
       const uint4* srow[RPT];
 #pragma unroll
       for (int h = 0; h < RPT; ++h) {
@@ -480,7 +491,6 @@ cudaError_t launch_tc_gemm(const TcGemm& g, uint32_t* status, uint64_t timeout_n
   p.num_n_tiles = (g.N + bn_out - 1) / bn_out;
   p.tiles = g.tiles;
   p.num_tiles = g.num_tiles;
-  p.offsets = g.offsets;
   p.C = g.C;
   p.ldc = g.ldc;
   p.row_scale = g.row_scale;

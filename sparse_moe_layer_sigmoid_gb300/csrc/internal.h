@@ -44,11 +44,12 @@ struct DispatchBuffers {
   int32_t* chunk_counts;  // [nchunks][E]
   int32_t* chunk_base;    // [nchunks][E]
   int32_t* offsets;       // [E+1]
-  int4* tiles;            // [max_tiles]: {expert, first m-tile of expert, m-tiles of expert, first row}
+  int4* tiles;            // [max_tiles]: {expert, first m-tile of expert, rows of expert, first row}
   int32_t* num_tiles;     // [1]
   int4* tiles_s;          // [T*k/16 + E + 1]: {expert, first row, rows (<= 16), 0}
   int32_t* num_tiles_s;   // [1]
   int4* tiles_p;          // [T*k/256 + E + 1]: 256-row tiles, same layout as `tiles` (or nullptr)
+                          // (one load gives a work item everything: the tile count is ceil(rows / tile))
   int32_t* num_tiles_p;   // [1]
   int32_t* tok_of_row;    // [T*k]
   int32_t* row_of;        // [T][k]
@@ -162,6 +163,6 @@ cudaError_t launch_gemv_fp4(const TcSwap& g, uint32_t* status, uint64_t timeout_
 // into ceil(rows/256) equal token tiles (tiles_p: the dispatch's 256-row tile list).  bf16 only
 // (kEpiGluBF16 with glu_h % 128 == 0, or kEpiScaleBF16 with out_features % 256 == 0).
 cudaError_t launch_tc_pair_swap(const TcSwap& g, const int4* tiles_p, const int32_t* num_tiles_p, int max_tiles_p,
-                                const int32_t* offsets, uint32_t* status, uint64_t timeout_ns, cudaStream_t s);
+                                uint32_t* status, uint64_t timeout_ns, cudaStream_t s);
 
 }  // namespace lmoe

@@ -322,7 +322,7 @@ lmoe_status run_forward(lmoe_handle* h, const void* x, int T, const lmoe_weights
     g.act = op2d(h->z_perm, rows, l);
     g.w = op3d(w->routed_gate_up, c.num_experts, 2 * hdim, l);
     g.C = h->a; g.ldc = hdim;
-    LMOE_TRY(launch_tc_pair_swap(g, h->db.tiles_p, h->db.num_tiles_p, h->max_tiles_p, h->db.offsets, h->status,
+    LMOE_TRY(launch_tc_pair_swap(g, h->db.tiles_p, h->db.num_tiles_p, h->max_tiles_p, h->status,
                                  h->timeout_ns, s));
     stage_end(h, kStGlu, s);
 
@@ -332,7 +332,7 @@ lmoe_status run_forward(lmoe_handle* h, const void* x, int T, const lmoe_weights
     dn.act = op2d(h->a, rows, hdim);
     dn.w = op3d(w->routed_down, c.num_experts, l, hdim);
     dn.C = o; dn.ldc = l; dn.row_scale = h->db.p_row;
-    LMOE_TRY(launch_tc_pair_swap(dn, h->db.tiles_p, h->db.num_tiles_p, h->max_tiles_p, h->db.offsets, h->status,
+    LMOE_TRY(launch_tc_pair_swap(dn, h->db.tiles_p, h->db.num_tiles_p, h->max_tiles_p, h->status,
                                  h->timeout_ns, s));
     stage_end(h, kStDown, s);
     h->last_launches += 2;

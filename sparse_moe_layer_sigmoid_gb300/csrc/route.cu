@@ -505,11 +505,11 @@ __global__ void __launch_bounds__(1024) dispatch_scan_kernel(const int32_t* __re
       chunk_base[(size_t)c * E + e] = run;
       run += chunk_counts[(size_t)c * E + e];
     }
-    for (int j = 0; j < nt; ++j) tiles[tile0 + j] = make_int4(e, tile0, nt, row0);
+    for (int j = 0; j < nt; ++j) tiles[tile0 + j] = make_int4(e, tile0, total, row0);
     if (tiles_s)
       for (int j = 0; j < nts; ++j) tiles_s[tile0s + j] = make_int4(e, row0 + kTileS * j, min(kTileS, total - kTileS * j), 0);
     if (tiles_p)
-      for (int j = 0; j < ntp; ++j) tiles_p[tile0p + j] = make_int4(e, tile0p, ntp, row0);
+      for (int j = 0; j < ntp; ++j) tiles_p[tile0p + j] = make_int4(e, tile0p, total, row0);
   }
   if (e == E - 1) {
     offsets[E] = s_cnt[e];
