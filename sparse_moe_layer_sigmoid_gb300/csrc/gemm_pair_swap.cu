@@ -206,6 +206,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (t + npairs < total) entry = pswap_entry(p, t + npairs);
       const int acc = it & 1;
       const uint32_t use = (uint32_t)(it >> 1);
+      // down x p: the item's row scales, lane l holding token 32 c + l, loaded while the
+      // accumulator is still being computed
+      float sc_reg[kMaxN / 32];
+#pragma unroll
+      for (int c = 0; c < kMaxN / 32; ++c) {
+        const int jl = c * 32 + lane;
+        sc_reg[c] = !GLU && jl < ti.nrows ? p.row_scale[ti.row0 + jl] : 0.0f;
+      }
       int ok = 1;
       if (lane == 0) {
         ok = ptx::mbar_wait_bounded(&tmem_full[acc], use & 1u, abort_flag, p.status, p.timeout_ns, kWaitAccFull);
@@ -221,7 +229,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       constexpr int FW = GLU ? 16 : 32;
       const int f0 = GLU ? ti.wt * 128 + (int)rank * 64 + 16 * q : ti.wt * 2 * kWRows + (int)rank * kWRows + 32 * q;
       uint16_t* st = reinterpret_cast<uint16_t*>(out_stage + q * kStageOut);
-      for (int c0 = 0; c0 < ti.n; c0 += 32) {
+#pragma unroll
+      for (int c = 0; c < kMaxN / 32; ++c) {
+        const int c0 = c * 32;
+        if (c0 >= ti.n) break;
         uint32_t r[32];
         ptx::tmem_ld_32x32b_x32(t_row + c0, r);
         ptx::tmem_ld_wait();
@@ -236,11 +247,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             st[(2 * i + (lane >> 4)) * FW + (lane & 15)] = __bfloat16_as_ushort(__float2bfloat16_rn(silu(g) * u));
           }
         } else {
-          const int jl = c0 + lane;
-          const float sc_l = jl < ti.nrows ? p.row_scale[ti.row0 + jl] : 0.0f;
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
-            const float sc = __shfl_sync(0xffffffffu, sc_l, i);
+            const float sc = __shfl_sync(0xffffffffu, sc_reg[c], i);
             st[i * FW + lane] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(r[i]) * sc));
           }
         }
