@@ -124,9 +124,12 @@ __device__ void exact_logit_parts(const RouterSrc& r, int t, const int (&ce)[kCa
                  lane, out);
 }
 
-// One warp per token.  Keys s + b are packed as (orderable(key) << 32) | (~expert) so that the
-// 64-bit maximum is the largest key and, among equal keys, the lowest expert index.  Lane l holds
-// experts l, l + 32, ... (NPL slots); after the pass, lane j < k holds the rank-j winner.
+// One warp per token.  Lane l holds experts l, l + 32, ... (NPL slots).  The selection finds the
+// k-th largest key by bisection over the order-preserving 32-bit image of the fp32 keys (a warp
+// count per probe), keeps every key above it and, among keys equal to it, the lowest indices
+// (eq. 13's tie rule), then sorts the k winners by (key descending, index ascending) with a
+// 32-lane bitonic network; after the pass, lane j < k holds the rank-j winner.  `sk` / `ss` are
+// 32-entry scratch arrays private to the warp.
 //
 // The logits come from a GEMM whose error is bounded by `src.margin`, so a key is known to
 // within eta = margin/4 (+ fp32 rounding).  When the k-th and (k+1)-th keys are closer than
@@ -146,66 +149,105 @@ struct TopkState {
 __device__ __forceinline__ float key_eta(const RouterSrc& src) { return 0.25f * src.margin + 1e-6f; }
 
 template <int NPL>
+__device__ __forceinline__ int count_at_least(const uint32_t (&ko)[NPL], uint32_t v) {
+  int c = 0;
+#pragma unroll
+  for (int i = 0; i < NPL; ++i) c += ko[i] >= v ? 1 : 0;
+  return (int)__reduce_add_sync(0xffffffffu, (unsigned)c);
+}
+
+template <int NPL>
 __device__ __forceinline__ void topk_pass(const float* __restrict__ logits, const float* __restrict__ bias, int t,
-                                          int E, int k, int lane, TopkState<NPL>& st) {
+                                          int E, int k, int lane, TopkState<NPL>& st, uint64_t* sk, float* ss) {
   const float* row = logits + (size_t)t * E;
-  uint32_t taken = 0;
+  uint32_t ko[NPL];  // orderable keys; 0 (below every key) for slots past E
+  uint32_t kmax = 0;
 #pragma unroll
   for (int i = 0; i < NPL; ++i) {
     const int e = lane + 32 * i;
     st.kf[i] = -INFINITY;
     st.sv[i] = 0.f;
+    ko[i] = 0;
     if (e < E) {
       const float s = 1.0f / (1.0f + expf(-row[e]));
       st.kf[i] = bias ? s + bias[e] : s;
       st.sv[i] = s;
+      ko[i] = orderable(st.kf[i]);
     }
+    kmax = ko[i] > kmax ? ko[i] : kmax;
   }
+  kmax = __reduce_max_sync(0xffffffffu, kmax);
+  // K = the k-th largest key: the largest v with at least k keys >= v (every key is >= 1)
+  uint32_t lo = 1, hi = kmax;
+  while (lo < hi) {
+    const uint32_t mid = lo + ((hi - lo + 1u) >> 1);
+    if (count_at_least<NPL>(ko, mid) >= k)
+      lo = mid;
+    else
+      hi = mid - 1u;
+  }
+  const uint32_t K = lo;
+  const int n_gt = K == 0xFFFFFFFFu ? 0 : count_at_least<NPL>(ko, K + 1u);
+  // keys equal to K: the lowest indices (slot-major, then lane) fill the k - n_gt open ranks
+  int need = k - n_gt;
+  bool sel[NPL];
+#pragma unroll
+  for (int i = 0; i < NPL; ++i) {
+    const bool eq = ko[i] == K;
+    const uint32_t m = __ballot_sync(0xffffffffu, eq);
+    const int before = __popc(m & ((1u << lane) - 1u));
+    sel[i] = ko[i] > K || (eq && before < need);
+    const int n_eq = __popc(m);
+    need -= need < n_eq ? need : n_eq;
+  }
+  st.a_k = from_orderable(K);
+  st.a_k1 = -INFINITY;
+  if (k < E) {
+    uint32_t below = 0;  // largest key not selected
+#pragma unroll
+    for (int i = 0; i < NPL; ++i)
+      if (!sel[i] && ko[i] > below) below = ko[i];
+    st.a_k1 = from_orderable(__reduce_max_sync(0xffffffffu, below));
+  }
+  // compact the k winners into the scratch: key, then (1023 - expert) << 5, then the slot of its score
+  int c = 0;
+#pragma unroll
+  for (int i = 0; i < NPL; ++i) c += sel[i] ? 1 : 0;
+  int base = c;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int o = __shfl_up_sync(0xffffffffu, base, off);
+    if (lane >= off) base += o;
+  }
+  base -= c;
+#pragma unroll
+  for (int i = 0; i < NPL; ++i)
+    if (sel[i]) {
+      const uint32_t e = (uint32_t)(lane + 32 * i);
+      sk[base] = ((uint64_t)ko[i] << 32) | ((1023u - e) << 5) | (uint32_t)base;
+      ss[base] = st.sv[i];
+      ++base;
+    }
+  __syncwarp();
+  uint64_t v = lane < k ? sk[lane] : 0ull;
+  // bitonic sort, descending over the 32 lanes
+#pragma unroll
+  for (int size = 2; size <= 32; size <<= 1)
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      const uint64_t o = __shfl_xor_sync(0xffffffffu, v, stride);
+      const bool keep_max = ((lane & stride) == 0) == ((lane & size) == 0);
+      v = keep_max ? (o > v ? o : v) : (o < v ? o : v);
+    }
   st.my_e = 0;
   st.my_s = 0.f;
   st.my_kf = 0.f;
-  st.a_k = 0.f;
-  st.a_k1 = -INFINITY;
-  const int rounds = k < E ? k + 1 : k;
-  for (int j = 0; j < rounds; ++j) {
-    uint64_t best = 0;
-#pragma unroll
-    for (int i = 0; i < NPL; ++i) {
-      const int e = lane + 32 * i;
-      if (e < E && !((taken >> i) & 1u)) {
-        const uint64_t pk = ((uint64_t)orderable(st.kf[i]) << 32) | (uint64_t)(0xFFFFFFFFu - (uint32_t)e);
-        best = pk > best ? pk : best;
-      }
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const uint64_t o = __shfl_xor_sync(0xffffffffu, best, off);
-      best = o > best ? o : best;
-    }
-    const int e_win = (int)(0xFFFFFFFFu - (uint32_t)(best & 0xFFFFFFFFu));
-    const float kf_win = from_orderable((uint32_t)(best >> 32));
-    if (j == k) {
-      st.a_k1 = kf_win;
-      break;
-    }
-    const int owner = e_win & 31, slot = e_win >> 5;
-    float s_here = 0.f;
-    if (lane == owner) {
-#pragma unroll
-      for (int i = 0; i < NPL; ++i)
-        if (i == slot) {
-          s_here = st.sv[i];
-          taken |= 1u << i;
-        }
-    }
-    const float s_win = __shfl_sync(0xffffffffu, s_here, owner);
-    if (lane == j) {
-      st.my_e = e_win;
-      st.my_s = s_win;
-      st.my_kf = kf_win;
-    }
-    if (j == k - 1) st.a_k = kf_win;
+  if (lane < k) {
+    st.my_e = 1023 - (int)((v >> 5) & 1023u);
+    st.my_kf = from_orderable((uint32_t)(v >> 32));
+    st.my_s = ss[v & 31u];
   }
+  __syncwarp();  // the scratch is rewritten by the warp's next token
 }
 
 // p = s / sum(s over the selected set), summed in rank order; lanes j < k store rank j.
@@ -225,11 +267,13 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ log
                                                    RouterSrc src, int T, int E, int k, int32_t* __restrict__ idx,
                                                    float* __restrict__ p, int32_t* __restrict__ refine_list,
                                                    int32_t* __restrict__ refine_count) {
+  __shared__ uint64_t s_sk[8][32];
+  __shared__ float s_ss[8][32];
   const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (t >= T) return;
   TopkState<NPL> st;
-  topk_pass<NPL>(logits, bias, t, E, k, lane, st);
+  topk_pass<NPL>(logits, bias, t, E, k, lane, st, s_sk[warp], s_ss[warp]);
   if (k < E && st.a_k - st.a_k1 < 2.0f * key_eta(src)) {
     if (lane == 0) refine_list[atomicAdd(refine_count, 1)] = t;  // list order is irrelevant: tokens are independent
     return;
@@ -272,7 +316,8 @@ __device__ __forceinline__ void refine_token(const float* __restrict__ logits, c
   uint32_t pend = 0;  // bit i: this lane's expert lane + 32 i is in the band and not yet refined
   int n_cert = 0;
   if (gw == 0) {
-    topk_pass<NPL>(logits, bias, t, E, k, lane, st);
+    // the key and score arrays of the group double as the selection's scratch (32 entries)
+    topk_pass<NPL>(logits, bias, t, E, k, lane, st, reinterpret_cast<uint64_t*>(sm.key), sm.s);
     const float eta = key_eta(src);
     const float hi = st.a_k + 2.0f * eta, lo = st.a_k1 - 2.0f * eta;
     n_cert = __popc(__ballot_sync(0xffffffffu, lane < k && st.my_kf > hi));  // ranks 0..n_cert-1
