@@ -156,24 +156,36 @@ __device__ __forceinline__ int count_at_least(const uint32_t (&ko)[NPL], uint32_
   return (int)__reduce_add_sync(0xffffffffu, (unsigned)c);
 }
 
+// Score s = sigmoid(logit) and key s + b of expert e of token t (fp32, the same arithmetic
+// wherever a key is needed).
+__device__ __forceinline__ void expert_key(const float* __restrict__ logits, const float* __restrict__ bias, int t,
+                                           int E, int e, float& s, float& key) {
+  s = 1.0f / (1.0f + expf(-logits[(size_t)t * E + e]));
+  key = bias ? s + bias[e] : s;
+}
+
+// Keys and scores of this lane's experts (-inf / 0 past E).
 template <int NPL>
-__device__ __forceinline__ void topk_pass(const float* __restrict__ logits, const float* __restrict__ bias, int t,
-                                          int E, int k, int lane, TopkState<NPL>& st, uint64_t* sk, float* ss) {
-  const float* row = logits + (size_t)t * E;
-  uint32_t ko[NPL];  // orderable keys; 0 (below every key) for slots past E
-  uint32_t kmax = 0;
+__device__ __forceinline__ void topk_keys(const float* __restrict__ logits, const float* __restrict__ bias, int t,
+                                          int E, int lane, TopkState<NPL>& st) {
 #pragma unroll
   for (int i = 0; i < NPL; ++i) {
     const int e = lane + 32 * i;
     st.kf[i] = -INFINITY;
     st.sv[i] = 0.f;
-    ko[i] = 0;
-    if (e < E) {
-      const float s = 1.0f / (1.0f + expf(-row[e]));
-      st.kf[i] = bias ? s + bias[e] : s;
-      st.sv[i] = s;
-      ko[i] = orderable(st.kf[i]);
-    }
+    if (e < E) expert_key(logits, bias, t, E, e, st.sv[i], st.kf[i]);
+  }
+}
+
+template <int NPL>
+__device__ __forceinline__ void topk_pass(const float* __restrict__ logits, const float* __restrict__ bias, int t,
+                                          int E, int k, int lane, TopkState<NPL>& st, uint64_t* sk, float* ss) {
+  topk_keys<NPL>(logits, bias, t, E, lane, st);
+  uint32_t ko[NPL];  // orderable keys; 0 (below every key) for slots past E
+  uint32_t kmax = 0;
+#pragma unroll
+  for (int i = 0; i < NPL; ++i) {
+    ko[i] = lane + 32 * i < E ? orderable(st.kf[i]) : 0u;
     kmax = ko[i] > kmax ? ko[i] : kmax;
   }
   kmax = __reduce_max_sync(0xffffffffu, kmax);
@@ -275,6 +287,8 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ log
   TopkState<NPL> st;
   topk_pass<NPL>(logits, bias, t, E, k, lane, st, s_sk[warp], s_ss[warp]);
   if (k < E && st.a_k - st.a_k1 < 2.0f * key_eta(src)) {
+    // the ranked list stays in idx for the refinement, which rewrites idx and p
+    if (lane < k) idx[(size_t)t * k + lane] = st.my_e;
     if (lane == 0) refine_list[atomicAdd(refine_count, 1)] = t;  // list order is irrelevant: tokens are independent
     return;
   }
@@ -301,29 +315,52 @@ __device__ __forceinline__ void group_sync() {
     __syncthreads();
 }
 
+// Exact fp64 key -> unsigned integer of the same order (0 stays below every key).
+__device__ __forceinline__ uint64_t orderable64(double d) {
+  const uint64_t u = (uint64_t)__double_as_longlong(d);
+  return (u >> 63) ? ~u : (u | 0x8000000000000000ull);
+}
+
 // Settle the selection of token t exactly: G warps (gw = 0..G-1) cooperate.  Warp 0 of the group
-// repeats the selection and lists the experts in the band around the boundary (rounds of at most
-// kMaxCand); the G warps recompute their logits to ~44 bits, warp gw over the 256-element blocks
-// gw, gw + G, ... of d, and warp 0 sums the G partials in a fixed order, takes fp64 keys and fills
-// the open ranks.
+// takes pass 1's ranked list from idx (recomputing its keys and the (k+1)-th key) and lists the
+// experts in the band around the boundary (rounds of at most kMaxCand); the G warps recompute
+// their logits to ~44 bits, warp gw over the 256-element blocks gw, gw + G, ... of d, and warp 0
+// sums the G partials in a fixed order, takes fp64 keys and fills the open ranks.
 template <int NPL, int G>
 __device__ __forceinline__ void refine_token(const float* __restrict__ logits, const float* __restrict__ bias,
                                              const RouterSrc& src, int t, int E, int k, int32_t* __restrict__ idx,
                                              float* __restrict__ p, int gw, int lane, const RefineSmem& sm) {
   const uint32_t lt_mask = (1u << lane) - 1u;
   TopkState<NPL> st;
-  double ex[NPL];
+  uint64_t ex[NPL];   // orderable exact keys of this lane's refined experts (0: not refined or taken)
   uint32_t pend = 0;  // bit i: this lane's expert lane + 32 i is in the band and not yet refined
   int n_cert = 0;
   if (gw == 0) {
-    // the key and score arrays of the group double as the selection's scratch (32 entries)
-    topk_pass<NPL>(logits, bias, t, E, k, lane, st, reinterpret_cast<uint64_t*>(sm.key), sm.s);
+    topk_keys<NPL>(logits, bias, t, E, lane, st);
+    st.my_e = lane < k ? idx[(size_t)t * k + lane] : 0;
+    st.my_s = 0.f;
+    st.my_kf = 0.f;
+    if (lane < k) expert_key(logits, bias, t, E, st.my_e, st.my_s, st.my_kf);
+    // k-th key: the last rank's; (k+1)-th: equal to it if more than k keys reach it, else the
+    // largest key below it
+    st.a_k = __shfl_sync(0xffffffffu, st.my_kf, k - 1);
+    int n_ge = 0;
+    float below = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < NPL; ++i) {
+      n_ge += st.kf[i] >= st.a_k ? 1 : 0;
+      if (st.kf[i] < st.a_k && st.kf[i] > below) below = st.kf[i];
+    }
+    n_ge = (int)__reduce_add_sync(0xffffffffu, (unsigned)n_ge);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) below = fmaxf(below, __shfl_xor_sync(0xffffffffu, below, off));
+    st.a_k1 = n_ge > k ? st.a_k : below;
     const float eta = key_eta(src);
     const float hi = st.a_k + 2.0f * eta, lo = st.a_k1 - 2.0f * eta;
     n_cert = __popc(__ballot_sync(0xffffffffu, lane < k && st.my_kf > hi));  // ranks 0..n_cert-1
 #pragma unroll
     for (int i = 0; i < NPL; ++i) {
-      ex[i] = -INFINITY;
+      ex[i] = 0;
       const int e = lane + 32 * i;
       if (e < E && st.kf[i] >= lo && st.kf[i] <= hi) pend |= 1u << i;
     }
@@ -377,7 +414,7 @@ __device__ __forceinline__ void refine_token(const float* __restrict__ logits, c
 #pragma unroll
       for (int i = 0; i < NPL; ++i)
         if (pos[i] >= 0) {
-          ex[i] = sm.key[pos[i]];
+          ex[i] = orderable64(sm.key[pos[i]]);
           st.sv[i] = sm.s[pos[i]];
         }
     }
@@ -385,19 +422,19 @@ __device__ __forceinline__ void refine_token(const float* __restrict__ logits, c
   }
   if (gw == 0) {
     for (int q = n_cert; q < k; ++q) {
-      double bv = -INFINITY;
+      uint64_t bv = 0;
       int be = 0x7FFFFFFF;
 #pragma unroll
       for (int i = 0; i < NPL; ++i) {
         const int e = lane + 32 * i;
-        if (ex[i] > bv || (ex[i] == bv && ex[i] != -INFINITY && e < be)) {
+        if (ex[i] > bv || (ex[i] == bv && ex[i] != 0 && e < be)) {
           bv = ex[i];
           be = e;
         }
       }
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) {
-        const double ov = __shfl_xor_sync(0xffffffffu, bv, off);
+        const uint64_t ov = __shfl_xor_sync(0xffffffffu, bv, off);
         const int oe = __shfl_xor_sync(0xffffffffu, be, off);
         if (ov > bv || (ov == bv && oe < be)) {
           bv = ov;
@@ -411,7 +448,7 @@ __device__ __forceinline__ void refine_token(const float* __restrict__ logits, c
         for (int i = 0; i < NPL; ++i)
           if (i == slot) {
             s_here = st.sv[i];
-            ex[i] = -INFINITY;
+            ex[i] = 0;
           }
       }
       const float s_win = __shfl_sync(0xffffffffu, s_here, owner);
