@@ -35,13 +35,13 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes per launch of the dominant kernel from one ncu capture, valid only while the kernel
 # source is unchanged (sha256 of the file it lives in).  Filled from the committed profile.
 # k3w_e128_bf16_prefill: an ncu capture of the same kernel on the 32-expert, 1024-token workload
-# (k3w_e32_bf16_t1024) read 1.549152 GB and wrote 0.095486 GB; experts, rows and weight bytes all
+# (k3w_e32_bf16_t1024) read 1.543810 GB and wrote 0.095298 GB; experts, rows and weight bytes all
 # scale by 4 to the 128-expert, 4096-token workload.
 TRAFFIC = {
     "k3w_e128_bf16_prefill": {
-        "routed_gate_up_glu": {"bytes_per_launch": 4 * (1.549152e9 + 0.095486e9),
+        "routed_gate_up_glu": {"bytes_per_launch": 4 * (1.543810e9 + 0.095298e9),
                                "src": "sparse_moe_layer_sigmoid_gb300/csrc/gemm_pair_swap.cu",
-                               "sha256": "84475ec1ec3084bc028b9053e5ae8f9a549c9c14cc92ddc5110c4728f8a5e03f"},
+                               "sha256": "4c8662986621e27769abe47268aceb5b04935c128320d4c2667a934238757383"},
     },
 }
 
