@@ -41,7 +41,7 @@ TRAFFIC = {
     "k3w_e128_bf16_prefill": {
         "routed_gate_up_glu": {"bytes_per_launch": 4 * (1.543810e9 + 0.095298e9),
                                "src": "sparse_moe_layer_sigmoid_gb300/csrc/gemm_pair_swap.cu",
-                               "sha256": "4c8662986621e27769abe47268aceb5b04935c128320d4c2667a934238757383"},
+                               "sha256": "01bb6ec6eee881fa93642a6f02e244917e72cc9c4e61ae2398eb9c2ab6b281c9"},
     },
 }
 

@@ -240,7 +240,10 @@ template <int EPI>
 cudaError_t launch_inst(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1, const PairParams& p,
                         long long pair_tiles, cudaStream_t s) {
   auto kern = tc_pair_kernel<EPI>;
-  static int max_pairs = 0;
+  static PerDeviceValue max_pairs_of;
+  std::atomic<int>* slot = max_pairs_of.current();
+  if (!slot) return cudaErrorInvalidDevice;
+  int max_pairs = slot->load(std::memory_order_acquire);
   if (max_pairs == 0) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
     if (e != cudaSuccess) return e;
@@ -253,6 +256,7 @@ cudaError_t launch_inst(const CUtensorMap& a, const CUtensorMap& b0, const CUten
     if (e != cudaSuccess) return e;
     if (n < 1) return cudaErrorInvalidConfiguration;
     max_pairs = n;
+    slot->store(n, std::memory_order_release);
   }
   const int pairs = (int)(pair_tiles < max_pairs ? pair_tiles : max_pairs);
   kern<<<2 * pairs, kThreads, kSmem, s>>>(a, b0, b1, p);

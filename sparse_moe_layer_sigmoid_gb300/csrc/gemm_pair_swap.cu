@@ -288,7 +288,10 @@ template <bool GLU>
 cudaError_t launch_pswap_inst(const CUtensorMap& w, const CUtensorMap& x, const PSwapParams& p, long long items,
                               cudaStream_t s) {
   auto kern = tc_pair_swap_kernel<GLU>;
-  static int max_pairs = 0;
+  static PerDeviceValue max_pairs_of;
+  std::atomic<int>* slot = max_pairs_of.current();
+  if (!slot) return cudaErrorInvalidDevice;
+  int max_pairs = slot->load(std::memory_order_acquire);
   if (max_pairs == 0) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
     if (e != cudaSuccess) return e;
@@ -301,6 +304,7 @@ cudaError_t launch_pswap_inst(const CUtensorMap& w, const CUtensorMap& x, const 
     if (e != cudaSuccess) return e;
     if (n < 1) return cudaErrorInvalidConfiguration;
     max_pairs = n;
+    slot->store(n, std::memory_order_release);
   }
   const int pairs = (int)(items < max_pairs ? items : max_pairs);
   kern<<<2 * pairs, kThreads, kSmem, s>>>(w, x, p);

@@ -345,11 +345,13 @@ cudaError_t launch_swap_inst(const CUtensorMap& w, const CUtensorMap& x, const S
                              cudaStream_t s) {
   using C = SwapCfg<FP4W>;
   auto kern = tc_swap_kernel<GLU, OUT_F16, AB_F16, FP4W>;
-  static bool attr_set = false;
-  if (!attr_set) {
+  static PerDeviceValue attr_set;
+  std::atomic<int>* set = attr_set.current();
+  if (!set) return cudaErrorInvalidDevice;
+  if (set->load(std::memory_order_acquire) == 0) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    set->store(1, std::memory_order_release);
   }
   kern<<<grid, C::kThreads, C::kSmem, s>>>(w, x, p);
   return cudaGetLastError();

@@ -397,11 +397,13 @@ cudaError_t launch_inst(const CUtensorMap& a, const CUtensorMap& b0, const CUten
                         int grid, cudaStream_t s) {
   using C = Cfg<BN, FP4B>;
   auto kern = tc_gemm_kernel<BN, EPI, GROUPED, AB_F16, FP4B, SPLIT>;
-  static bool attr_set = false;
-  if (!attr_set) {
+  static PerDeviceValue attr_set;
+  std::atomic<int>* set = attr_set.current();
+  if (!set) return cudaErrorInvalidDevice;
+  if (set->load(std::memory_order_acquire) == 0) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    set->store(1, std::memory_order_release);
   }
   kern<<<grid, C::kThreads, C::kSmem, s>>>(a, b0, b1, p);
   return cudaGetLastError();

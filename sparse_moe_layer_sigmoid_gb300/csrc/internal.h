@@ -5,7 +5,27 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace lmoe {
+
+// ---------------------------------------------------------------- per-device launch setup
+// A kernel's launch attributes (the dynamic shared-memory opt-in) and occupancy queries belong
+// to a device: a launcher keeps one value per device, 0 until that device is set up.  Two
+// threads setting up the same device at once only repeat idempotent runtime calls.
+constexpr int kMaxSetupDevices = 64;
+struct PerDeviceValue {
+  std::atomic<int> v[kMaxSetupDevices];
+  PerDeviceValue() {
+    for (auto& x : v) x.store(0, std::memory_order_relaxed);
+  }
+  // The slot of the current device, or nullptr when there is none.
+  std::atomic<int>* current() {
+    int d = -1;
+    if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= kMaxSetupDevices) return nullptr;
+    return &v[d];
+  }
+};
 
 // ---------------------------------------------------------------- routing (route.cu)
 // logits[T][E] = x[T][d] . W_r[E][d]^T in fp32 (CUDA cores, fixed K order per output).

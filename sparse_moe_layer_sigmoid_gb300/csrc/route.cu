@@ -794,12 +794,9 @@ cudaError_t launch_scatter_rows(const void* src, void* dst, const int32_t* row_o
       (reinterpret_cast<uintptr_t>(dst) & 15u))
     return cudaErrorInvalidValue;
   const int smem = kScatterSlots * (int)row_bytes;  // <= 64 KB
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(scatter_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kScatterSlots * 16384);
+  if (smem > 48 * 1024) {  // the opt-in limit is a per-device function attribute: set it where it is needed
+    cudaError_t e = cudaFuncSetAttribute(scatter_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    attr_set = true;
   }
   const int per_sm = smem <= 32768 ? 6 : 3;
   const int grid = T < per_sm * num_sms ? T : per_sm * num_sms;
