@@ -42,6 +42,7 @@ constexpr size_t kSmem = (size_t)kStages * kStageBytes + 1024 + 512;
 struct PairParams {
   int M, N;
   int num_kb, kb0, kb0_per_group;
+  int a_kb_period;  // A's K coordinate repeats every a_kb_period k-blocks (K-concatenated B terms)
   int glu_h;
   int num_m_tiles, num_n_tiles;  // 256-row tiles, 256-column (GLU: 128-output) tiles
   void* C;
@@ -65,7 +66,7 @@ struct Boxes {
 };
 __device__ __forceinline__ Boxes boxes_for(const PairParams& p, const PairTile& ti, int kb, int rank, bool glu) {
   Boxes b;
-  b.ax = kb * BK;
+  b.ax = (kb % p.a_kb_period) * BK;
   b.ay = ti.row0 + rank * kRows;
   b.second = false;
   if (glu) {
@@ -268,10 +269,11 @@ cudaError_t launch_inst(const CUtensorMap& a, const CUtensorMap& b0, const CUten
 bool tc_pair_supported(const TcGemm& g) {
   const bool glu = g.epi == kEpiGluBF16;
   if (g.tiles || g.b_scale || g.ab_f16) return false;
-  if (g.epi != kEpiBF16 && g.epi != kEpiGluBF16) return false;
-  if (g.a_k_period && g.a_k_period != g.K) return false;
-  if (g.K % BK || g.k0_len % BK || g.k0_per_group % BK) return false;
-  return glu ? g.N % (BN / 2) == 0 && g.glu_h % kRows == 0 : g.N % 32 == 0;
+  if (g.epi != kEpiBF16 && g.epi != kEpiGluBF16 && g.epi != kEpiF32) return false;
+  const int a_period = g.a_k_period ? g.a_k_period : g.K;
+  if (g.K % BK || g.k0_len % BK || g.k0_per_group % BK || a_period % BK || g.K % a_period) return false;
+  if (glu) return g.N % (BN / 2) == 0 && g.glu_h % kRows == 0;
+  return g.N % (g.epi == kEpiF32 ? 4 : 32) == 0;
 }
 
 cudaError_t launch_tc_pair(const TcGemm& g, uint32_t* status, uint64_t timeout_ns, cudaStream_t s) {
@@ -291,6 +293,7 @@ cudaError_t launch_tc_pair(const TcGemm& g, uint32_t* status, uint64_t timeout_n
   p.num_kb = g.K / BK;
   p.kb0 = g.k0_len / BK;
   p.kb0_per_group = g.k0_per_group / BK;
+  p.a_kb_period = (g.a_k_period ? g.a_k_period : g.K) / BK;
   p.glu_h = glu ? g.glu_h : 1;
   p.num_m_tiles = (g.M + kTileP - 1) / kTileP;
   p.num_n_tiles = (g.N + bn_out - 1) / bn_out;
@@ -301,7 +304,11 @@ cudaError_t launch_tc_pair(const TcGemm& g, uint32_t* status, uint64_t timeout_n
   p.timeout_ns = timeout_ns;
   const long long tiles = (long long)p.num_m_tiles * p.num_n_tiles;
   if (tiles == 0) return cudaSuccess;
-  return glu ? launch_inst<kEpiGluBF16>(ma, mb0, mb1, p, tiles, s) : launch_inst<kEpiBF16>(ma, mb0, mb1, p, tiles, s);
+  switch (g.epi) {
+    case kEpiGluBF16: return launch_inst<kEpiGluBF16>(ma, mb0, mb1, p, tiles, s);
+    case kEpiF32: return launch_inst<kEpiF32>(ma, mb0, mb1, p, tiles, s);
+    default: return launch_inst<kEpiBF16>(ma, mb0, mb1, p, tiles, s);
+  }
 }
 
 }  // namespace lmoe

@@ -34,9 +34,12 @@ cudaError_t launch_router_logits(const void* x, int x_dtype, const void* w_route
 // Router logits for either activation type: bf16 activations use the tensor cores (an fp32 W_r
 // is first split into three bf16 terms in `wr_split`, [3][E][d] bf16, then contracted over
 // K = 3d), fp32 activations the CUDA-core GEMM.  Adds its kernel count to *launches.
+// With `pair_ok`, a router GEMM of at least 256 rows whose 128-row tiles would more than half
+// fill the SMs runs on CTA pairs; fewer tiles split K on single CTAs (`splitk` workspace).
 cudaError_t launch_router(const void* x, int act, const void* w_router, int router_w, float* logits,
                           void* wr_split, int T, int E, int d, uint32_t* status, uint64_t timeout_ns, int num_sms,
-                          int* launches, cudaStream_t s, float* splitk = nullptr, size_t splitk_bytes = 0);
+                          int* launches, cudaStream_t s, float* splitk = nullptr, size_t splitk_bytes = 0,
+                          bool pair_ok = false);
 // Exact split of fp32 W_r into three bf16 terms, out[t][e][c], t = hi, mid, lo:
 // w = hi + mid + lo with each term the bf16 rounding of what the previous terms left.
 cudaError_t launch_split_bf16x3(const float* w, int64_t n, void* out, cudaStream_t s);
@@ -150,7 +153,7 @@ cudaError_t launch_tc_gemm(const TcGemm& g, uint32_t* status, uint64_t timeout_n
                            cudaStream_t s);
 
 // The same GEMM on CTA pairs (gemm_pair.cu): 256 x 256 tiles, tcgen05.mma.cta_group::2.  Dense
-// (not grouped), bf16 operands, bf16 or GLU epilogue; tc_pair_supported says whether `g`
+// (not grouped), bf16 operands, bf16, GLU or fp32 epilogue; tc_pair_supported says whether `g`
 // qualifies.
 bool tc_pair_supported(const TcGemm& g);
 cudaError_t launch_tc_pair(const TcGemm& g, uint32_t* status, uint64_t timeout_ns, cudaStream_t s);

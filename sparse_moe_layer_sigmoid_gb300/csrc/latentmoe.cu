@@ -216,7 +216,8 @@ lmoe_status run_routing(lmoe_handle* h, const void* x, int T, const lmoe_weights
   if (!ext_idx) {
     stage_begin(h, kStRouter, s);
     LMOE_TRY(launch_router(x, c.act, w->w_router, c.router_w, h->logits, h->wr_split, T, c.num_experts, c.d,
-                           h->status, h->timeout_ns, h->num_sms, &h->last_launches, s, h->splitk, h->splitk_bytes));
+                           h->status, h->timeout_ns, h->num_sms, &h->last_launches, s, h->splitk, h->splitk_bytes,
+                           !(c.flags & LMOE_FLAG_SINGLE_CTA_GEMM)));
     stage_end(h, kStRouter, s);
     const RouterSrc rs{x, c.act, w->w_router, c.router_w, c.d, kRouterLogitMargin};
     LMOE_TRY(launch_topk(h->logits, w->router_bias, rs, T, c.num_experts, c.top_k, h->idx, h->p, h->refine_list,

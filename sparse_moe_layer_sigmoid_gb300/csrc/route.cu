@@ -707,7 +707,7 @@ cudaError_t launch_router_logits(const void* x, int x_dtype, const void* w_route
 
 cudaError_t launch_router(const void* x, int act, const void* w_router, int router_w, float* logits,
                           void* wr_split, int T, int E, int d, uint32_t* status, uint64_t timeout_ns, int num_sms,
-                          int* launches, cudaStream_t s, float* splitk, size_t splitk_bytes) {
+                          int* launches, cudaStream_t s, float* splitk, size_t splitk_bytes, bool pair_ok) {
   if (act != kBF16) {
     if (launches) *launches += 1;
     return launch_router_logits(x, act, w_router, router_w, logits, T, E, d, s);
@@ -737,6 +737,11 @@ cudaError_t launch_router(const void* x, int act, const void* w_router, int rout
   g.partial = splitk;
   g.partial_bytes = splitk_bytes;
   g.launch_count = launches;
+  const long long single_tiles = (long long)((T + 127) / 128) * ((E + 255) / 256);
+  if (pair_ok && T >= 256 && single_tiles * 2 > num_sms && tc_pair_supported(g)) {
+    if (launches) *launches += 1;
+    return launch_tc_pair(g, status, timeout_ns, s);
+  }
   return launch_tc_gemm(g, status, timeout_ns, 0, num_sms, s);
 }
 
