@@ -66,7 +66,7 @@ struct Boxes {
 };
 __device__ __forceinline__ Boxes boxes_for(const PairParams& p, const PairTile& ti, int kb, int rank, bool glu) {
   Boxes b;
-  b.ax = (kb % p.a_kb_period) * BK;
+  b.ax = (kb < p.a_kb_period ? kb : kb % p.a_kb_period) * BK;
   b.ay = ti.row0 + rank * kRows;
   b.second = false;
   if (glu) {
