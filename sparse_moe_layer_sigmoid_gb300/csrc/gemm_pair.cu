@@ -64,9 +64,12 @@ struct Boxes {
   int bx, by, bz;
   bool second;
 };
+// PERIODIC (the router's K-concatenated W_r terms): A's K coordinate wraps every a_kb_period
+// k-blocks.  Only that instantiation pays for the wrap: any extra work here delays the TMA issue.
+template <bool PERIODIC>
 __device__ __forceinline__ Boxes boxes_for(const PairParams& p, const PairTile& ti, int kb, int rank, bool glu) {
   Boxes b;
-  b.ax = (kb < p.a_kb_period ? kb : kb % p.a_kb_period) * BK;
+  b.ax = (PERIODIC ? kb % p.a_kb_period : kb) * BK;
   b.ay = ti.row0 + rank * kRows;
   b.second = false;
   if (glu) {
@@ -157,7 +160,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         uint8_t* sA = smem + stage * kStageBytes;
         const uint32_t bar = ptx::mapa_shared(&full[stage], 0);  // the even CTA's full[stage]
         if (rank == 0) ptx::mbar_arrive_expect_tx(&full[stage], 2 * kStageBytes);
-        const Boxes bx = boxes_for(p, ti, kb, (int)rank, GLU);
+        const Boxes bx = boxes_for<EPI == kEpiF32>(p, ti, kb, (int)rank, GLU);
         ptx::tma_load_3d_pair(sA, &tmA, bar, bx.ax, bx.ay, 0);
         ptx::tma_load_3d_pair(sA + kHalfBytes, bx.second ? &tmB1 : &tmB0, bar, bx.bx, bx.by, bx.bz);
         if (++stage == kStages) {
@@ -272,6 +275,7 @@ bool tc_pair_supported(const TcGemm& g) {
   if (g.epi != kEpiBF16 && g.epi != kEpiGluBF16 && g.epi != kEpiF32) return false;
   const int a_period = g.a_k_period ? g.a_k_period : g.K;
   if (g.K % BK || g.k0_len % BK || g.k0_per_group % BK || a_period % BK || g.K % a_period) return false;
+  if (a_period != g.K && g.epi != kEpiF32) return false;  // a periodic A only with the fp32 epilogue
   if (glu) return g.N % (BN / 2) == 0 && g.glu_h % kRows == 0;
   return g.N % (g.epi == kEpiF32 ? 4 : 32) == 0;
 }
