@@ -56,40 +56,6 @@ struct PairTile {
   int row0, row_end, n0, group;  // row0: first of the tile's 256 rows
 };
 
-// TMA coordinates of this CTA's boxes for k-block kb of a tile: A rows, and its half of B (the
-// even CTA takes B rows n0..n0+127 or, for GLU, the gate rows; the odd CTA the next 128 rows or
-// the matching up rows).  `second` selects the tensor map of the K range after kb0.
-struct Boxes {
-  int ax, ay;
-  int bx, by, bz;
-  bool second;
-};
-// PERIODIC (the router's K-concatenated W_r terms): A's K coordinate wraps every a_kb_period
-// k-blocks.  Only that instantiation pays for the wrap: any extra work here delays the TMA issue.
-template <bool PERIODIC>
-__device__ __forceinline__ Boxes boxes_for(const PairParams& p, const PairTile& ti, int kb, int rank, bool glu) {
-  Boxes b;
-  b.ax = (PERIODIC ? kb % p.a_kb_period : kb) * BK;
-  b.ay = ti.row0 + rank * kRows;
-  b.second = false;
-  if (glu) {
-    b.bx = kb * BK;
-    b.by = rank * p.glu_h + ti.n0 % p.glu_h;
-    b.bz = ti.group + ti.n0 / p.glu_h;
-  } else if (kb < p.kb0) {
-    const int goff = kb / p.kb0_per_group;
-    b.bx = (kb - goff * p.kb0_per_group) * BK;
-    b.by = ti.n0 + rank * kRows;
-    b.bz = ti.group + goff;
-  } else {
-    b.bx = (kb - p.kb0) * BK;
-    b.by = ti.n0 + rank * kRows;
-    b.bz = 0;
-    b.second = true;
-  }
-  return b;
-}
-
 template <int BN_OUT>
 __device__ __forceinline__ PairTile decode_pair_tile(const PairParams& p, int t) {
   PairTile ti;
@@ -150,8 +116,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------------ TMA producer (both CTAs)
     int stage = 0, iter = 0;
     uint32_t phase = 0;
+    // Boxes of k-block kb: A rows row0 + rank*128 at K block ka; this CTA's half of B (the even
+    // CTA takes B rows n0..n0+127 or, for GLU, the gate rows; the odd CTA the next 128 rows or
+    // the matching up rows).  Non-GLU B is K-concatenated: groups of kb0_per_group k-blocks of
+    // B0 (group offset goff, block kin within it), then B1 from kb0 on.  The K positions advance
+    // by counting, with no division per k-block: the producer's issue latency is on the
+    // pipeline's critical path.
+    constexpr bool PERIODIC = EPI == kEpiF32;  // the router's terms: A's K wraps every a_kb_period
     for (int t = pair; t < total; t += npairs) {
       const PairTile ti = decode_pair_tile<BN_OUT>(p, t);
+      const int ay = ti.row0 + (int)rank * kRows;
+      const int by = GLU ? (int)rank * p.glu_h + ti.n0 % p.glu_h : ti.n0 + (int)rank * kRows;
+      const int bz_glu = ti.group + ti.n0 / p.glu_h;
+      int ka = 0, goff = 0, kin = 0;
+      bool second = p.kb0 == 0;
       for (int kb = 0; kb < p.num_kb; ++kb, ++iter) {
         if (!ptx::mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, p.status, p.timeout_ns, kWaitProducer))
           goto done;
@@ -160,9 +138,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         uint8_t* sA = smem + stage * kStageBytes;
         const uint32_t bar = ptx::mapa_shared(&full[stage], 0);  // the even CTA's full[stage]
         if (rank == 0) ptx::mbar_arrive_expect_tx(&full[stage], 2 * kStageBytes);
-        const Boxes bx = boxes_for<EPI == kEpiF32>(p, ti, kb, (int)rank, GLU);
-        ptx::tma_load_3d_pair(sA, &tmA, bar, bx.ax, bx.ay, 0);
-        ptx::tma_load_3d_pair(sA + kHalfBytes, bx.second ? &tmB1 : &tmB0, bar, bx.bx, bx.by, bx.bz);
+        ptx::tma_load_3d_pair(sA, &tmA, bar, ka * BK, ay, 0);
+        if (GLU)
+          ptx::tma_load_3d_pair(sA + kHalfBytes, &tmB0, bar, kb * BK, by, bz_glu);
+        else
+          ptx::tma_load_3d_pair(sA + kHalfBytes, second ? &tmB1 : &tmB0, bar, kin * BK, by,
+                                second ? 0 : ti.group + goff);
+        if (PERIODIC) {
+          if (++ka == p.a_kb_period) ka = 0;
+        } else {
+          ++ka;
+        }
+        if (!GLU) {
+          if (!second && kb + 1 == p.kb0) {
+            second = true;
+            kin = 0;
+          } else if (!second && ++kin == p.kb0_per_group) {
+            kin = 0;
+            ++goff;
+          } else if (second) {
+            ++kin;
+          }
+        }
         if (++stage == kStages) {
           stage = 0;
           phase ^= 1u;

@@ -180,6 +180,15 @@ __global__ void __launch_bounds__(Cfg<BN, FP4B>::kThreads, 1)
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
       const Tile ti = decode_tile<BN_OUT, GROUPED>(p, t, entry);
       if (t + (int)gridDim.x < total) entry = tile_entry<GROUPED>(p, t + gridDim.x);
+      // K positions of k-block kb, advanced by counting (no division per k-block: the producer's
+      // issue latency is on the pipeline's critical path): A's block ka wraps every a_kb_period;
+      // non-GLU B is K-concatenated, groups of kb0_per_group blocks of B0 (offset goff, block kin
+      // within it), then B1 from kb0 on.
+      int ka = ti.kb_lo % p.a_kb_period;
+      bool second = ti.kb_lo >= p.kb0;
+      int goff = second ? 0 : ti.kb_lo / p.kb0_per_group;
+      int kin = second ? ti.kb_lo - p.kb0 : ti.kb_lo - goff * p.kb0_per_group;
+      const int grp = GLU ? ti.group + ti.n0 / p.glu_h : 0, j0 = GLU ? ti.n0 % p.glu_h : 0;
       for (int kb = ti.kb_lo; kb < ti.kb_hi; ++kb) {
         if (!ptx::mbar_wait_bounded(&empty1[stage], phase ^ 1u, abort_flag, p.status, p.timeout_ns, kWaitProducer)) goto done;
         const bool skip = p.inject && first && blockIdx.x == 0;  // test hook: drop one stage signal
@@ -190,22 +199,31 @@ __global__ void __launch_bounds__(Cfg<BN, FP4B>::kThreads, 1)
           constexpr uint32_t kBoxB = FP4B ? kBoxRows * BK / 2 : kBoxBytes;  // bytes of one B box
           const int kx = FP4B ? kb * (BK / 2) : kb * BK;                     // B inner coordinate
           ptx::mbar_arrive_expect_tx(&full1[stage], C::kStage1Bytes);
-          ptx::tma_load_3d(sA, &tmA, &full1[stage], (kb % p.a_kb_period) * BK, ti.row0, 0);
+          ptx::tma_load_3d(sA, &tmA, &full1[stage], ka * BK, ti.row0, 0);
           if (GLU) {
-            const int grp = ti.group + ti.n0 / p.glu_h, j0 = ti.n0 % p.glu_h;
             ptx::tma_load_3d(sB, &tmB0, &full1[stage], kx, j0, grp);
             ptx::tma_load_3d(sB + kBoxB, &tmB0, &full1[stage], kx, p.glu_h + j0, grp);
-          } else if (kb < p.kb0) {
-            const int goff = kb / p.kb0_per_group;
-            const int kin = (kb - goff * p.kb0_per_group) * (FP4B ? BK / 2 : BK);
+          } else if (!second) {
+            const int kin_el = kin * (FP4B ? BK / 2 : BK);
 #pragma unroll
             for (int h = 0; h < BN / kBoxRows; ++h)
-              ptx::tma_load_3d(sB + h * kBoxB, &tmB0, &full1[stage], kin, ti.n0 + h * kBoxRows, ti.group + goff);
+              ptx::tma_load_3d(sB + h * kBoxB, &tmB0, &full1[stage], kin_el, ti.n0 + h * kBoxRows, ti.group + goff);
           } else {
-            const int kin = (kb - p.kb0) * BK;
 #pragma unroll
             for (int h = 0; h < BN / kBoxRows; ++h)
-              ptx::tma_load_3d(sB + h * kBoxB, &tmB1, &full1[stage], kin, ti.n0 + h * kBoxRows, 0);
+              ptx::tma_load_3d(sB + h * kBoxB, &tmB1, &full1[stage], kin * BK, ti.n0 + h * kBoxRows, 0);
+          }
+        }
+        if (++ka == p.a_kb_period) ka = 0;
+        if (!GLU) {
+          if (!second && kb + 1 == p.kb0) {
+            second = true;
+            kin = 0;
+          } else if (!second && ++kin == p.kb0_per_group) {
+            kin = 0;
+            ++goff;
+          } else if (second) {
+            ++kin;
           }
         }
         if (++stage == S1) {
