@@ -147,7 +147,7 @@ struct TcGemm {
   size_t partial_bytes;      // its size (tc_splitk_partial_bytes)
   int* launch_count;         // incremented by the number of kernels launched (or nullptr)
 };
-// Workspace the split-K path needs at most (splits x N tiles <= SMs, 128 rows, 256 columns each).
+// Workspace the split-K path needs at most (splits x tiles <= SMs, 128 rows x 256 fp32 columns each).
 size_t tc_splitk_partial_bytes(int num_sms);
 cudaError_t launch_tc_gemm(const TcGemm& g, uint32_t* status, uint64_t timeout_ns, int inject_fault, int num_sms,
                            cudaStream_t s);

@@ -171,9 +171,9 @@ def test_token_permutation_is_bitwise_invariant(binding):
 @pytest.mark.parametrize("cfg", [SMALL_BF16, replace(SMALL_BF16, name="pair_grouped", tokens=700, experts=8,
                                                       bias="normal1.5", seed=41)], ids=lambda c: c.name)
 def test_cta_pair_gemms_match_single_cta(binding, cfg):
-    """CTA-pair GEMMs and single-CTA GEMMs accumulate every output over the same K order in fp32;
-    the layer outputs agree up to bf16 rounding of intermediate values that the two tensor-core
-    shapes may round differently."""
+    """CTA-pair GEMMs and single-CTA GEMMs accumulate in fp32 (single CTAs split K for dense GEMMs
+    of few tiles, which sums in another order); the layer outputs agree up to that and to the
+    bf16 rounding of intermediate values."""
     dev = torch.device("cuda")
     inp = device_inputs(cfg, dev, False)
     pair = binding.LatentMoE(cfg)
