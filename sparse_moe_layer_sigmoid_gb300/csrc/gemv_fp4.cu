@@ -92,51 +92,87 @@ __device__ __forceinline__ GemvItem gemv_item(const GemvParams& p, int it) {
   return g;
 }
 
+// Partial dot product of one 32-element K block: E2M1 weights wq (with E8M0 scale byte sc) against
+// the NT staged token blocks xa, added to acc[t] (fp16 pair sums within the block, fp32 across).
+template <int NT>
+__device__ __forceinline__ void block_dot(const uint4& wq, uint32_t sc, const uint32_t (&xa)[NT][16], float (&acc)[NT],
+                                          bool& bad) {
+  uint32_t q[16];
+  e2m1x32_unscaled(wq, q);
+  bad |= sc == 255u || sc > 127u + 13u;
+  const float scale = __uint_as_float(sc == 0u ? 0x00400000u : (sc << 23));  // 2^(e - 127)
+#pragma unroll
+  for (int t = 0; t < NT; ++t) {
+    __half2 s2 = __float2half2_rn(0.f);
+#pragma unroll
+    for (int k = 0; k < 16; ++k)
+      s2 = __hfma2(*reinterpret_cast<const __half2*>(&q[k]), *reinterpret_cast<const __half2*>(&xa[t][k]), s2);
+    const float2 f = __half22float2(s2);
+    acc[t] = fmaf(f.x + f.y, scale, acc[t]);
+  }
+}
+
+template <int NT>
+__device__ __forceinline__ void load_act(const uint4* __restrict__ act_s, int t0, int j, int l, uint32_t (&xa)[NT][16]) {
+#pragma unroll
+  for (int t = 0; t < NT; ++t)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint4 v = act_s[act_index(t0 + t, j, i, l)];
+      xa[t][4 * i] = v.x;
+      xa[t][4 * i + 1] = v.y;
+      xa[t][4 * i + 2] = v.z;
+      xa[t][4 * i + 3] = v.w;
+    }
+}
+
 // Dot products of the warp's staged weight rows (indices srow into the stage) with staged token
-// rows t0 .. t0 + NT - 1.
+// rows t0 .. t0 + NT - 1.  Lane l takes the K blocks l, l + 32, ...; when K holds a half round of
+// 16 blocks at the end (K = 3584: 112 blocks), the two half-warps split the rows there instead
+// of leaving half the lanes idle: lanes 0-15 take rows 0 and 1, lanes 16-31 rows 2 and 3.
 template <int NT>
 __device__ __forceinline__ void warp_rows(const GemvParams& p, const uint8_t* __restrict__ wst,
                                           const uint8_t* __restrict__ sst, const uint4* __restrict__ act_s, int t0,
                                           const int (&srow)[kRowsPerWarp], int lane, float (&acc)[kRowsPerWarp][NT],
                                           bool& bad) {
-  const int nchunks = p.K / 32;
+  static_assert(kRowsPerWarp == 4, "the half-round split pairs rows 0-1 with 2-3");
+  const int nchunks = p.K / 32;  // a multiple of 16 (K % 512 == 0)
+  const int nfull = nchunks >> 5;
 #pragma unroll
   for (int r = 0; r < kRowsPerWarp; ++r)
 #pragma unroll
     for (int t = 0; t < NT; ++t) acc[r][t] = 0.f;
 #pragma unroll 1
-  for (int j = 0; 32 * j < nchunks; ++j) {
+  for (int j = 0; j < nfull; ++j) {
     const int c = 32 * j + lane;
-    const bool live = c < nchunks;
     uint32_t xa[NT][16];
-#pragma unroll
-    for (int t = 0; t < NT; ++t)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        // blocks past the end of K were never staged: zero, not stale bits (0 * inf = NaN)
-        const uint4 v = live ? act_s[act_index(t0 + t, j, i, lane)] : make_uint4(0, 0, 0, 0);
-        xa[t][4 * i] = v.x;
-        xa[t][4 * i + 1] = v.y;
-        xa[t][4 * i + 2] = v.z;
-        xa[t][4 * i + 3] = v.w;
-      }
+    load_act<NT>(act_s, t0, j, lane, xa);
 #pragma unroll
     for (int r = 0; r < kRowsPerWarp; ++r) {
-      const uint4 wq = live ? *reinterpret_cast<const uint4*>(wst + srow[r] * p.row_bytes + 16 * c)
-                            : make_uint4(0, 0, 0, 0);
-      const uint32_t sc = live ? (uint32_t)sst[srow[r] * p.srow_bytes + c] : 127u;
-      uint32_t q[16];
-      e2m1x32_unscaled(wq, q);
-      bad |= sc == 255u || sc > 127u + 13u;
-      const float scale = __uint_as_float(sc == 0u ? 0x00400000u : (sc << 23));  // 2^(e - 127)
+      const uint4 wq = *reinterpret_cast<const uint4*>(wst + srow[r] * p.row_bytes + 16 * c);
+      const uint32_t sc = (uint32_t)sst[srow[r] * p.srow_bytes + c];
+      block_dot<NT>(wq, sc, xa, acc[r], bad);
+    }
+  }
+  if (nchunks & 31) {
+    const int hl = lane & 15;
+    const bool upper = lane >= 16;
+    const int c = 32 * nfull + hl;
+    uint32_t xa[NT][16];
+    load_act<NT>(act_s, t0, nfull, hl, xa);
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) {
+      const int row = upper ? srow[rr + 2] : srow[rr];
+      const uint4 wq = *reinterpret_cast<const uint4*>(wst + row * p.row_bytes + 16 * c);
+      const uint32_t sc = (uint32_t)sst[row * p.srow_bytes + c];
+      float part[NT];
+#pragma unroll
+      for (int t = 0; t < NT; ++t) part[t] = upper ? acc[rr + 2][t] : acc[rr][t];
+      block_dot<NT>(wq, sc, xa, part, bad);
 #pragma unroll
       for (int t = 0; t < NT; ++t) {
-        __half2 s2 = __float2half2_rn(0.f);
-#pragma unroll
-        for (int k = 0; k < 16; ++k)
-          s2 = __hfma2(*reinterpret_cast<const __half2*>(&q[k]), *reinterpret_cast<const __half2*>(&xa[t][k]), s2);
-        const float2 f = __half22float2(s2);
-        acc[r][t] = fmaf(f.x + f.y, scale, acc[r][t]);
+        acc[rr][t] = upper ? acc[rr][t] : part[t];
+        acc[rr + 2][t] = upper ? part[t] : acc[rr + 2][t];
       }
     }
   }
