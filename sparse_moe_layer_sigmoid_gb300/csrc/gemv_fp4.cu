@@ -94,12 +94,13 @@ __device__ __forceinline__ GemvItem gemv_item(const GemvParams& p, int it) {
 
 // Partial dot product of one 32-element K block: E2M1 weights wq (with E8M0 scale byte sc) against
 // the NT staged token blocks xa, added to acc[t] (fp16 pair sums within the block, fp32 across).
+// scmax tracks the largest scale byte seen (checked once per row group by the caller).
 template <int NT>
 __device__ __forceinline__ void block_dot(const uint4& wq, uint32_t sc, const uint32_t (&xa)[NT][16], float (&acc)[NT],
-                                          bool& bad) {
+                                          uint32_t& scmax) {
   uint32_t q[16];
   e2m1x32_unscaled(wq, q);
-  bad |= sc == 255u || sc > 127u + 13u;
+  scmax = max(scmax, sc);
   const float scale = __uint_as_float(sc == 0u ? 0x00400000u : (sc << 23));  // 2^(e - 127)
 #pragma unroll
   for (int t = 0; t < NT; ++t) {
@@ -138,6 +139,7 @@ __device__ __forceinline__ void warp_rows(const GemvParams& p, const uint8_t* __
   static_assert(kRowsPerWarp == 4, "the half-round split pairs rows 0-1 with 2-3");
   const int nchunks = p.K / 32;  // a multiple of 16 (K % 512 == 0)
   const int nfull = nchunks >> 5;
+  uint32_t scmax = 0;
 #pragma unroll
   for (int r = 0; r < kRowsPerWarp; ++r)
 #pragma unroll
@@ -151,7 +153,7 @@ __device__ __forceinline__ void warp_rows(const GemvParams& p, const uint8_t* __
     for (int r = 0; r < kRowsPerWarp; ++r) {
       const uint4 wq = *reinterpret_cast<const uint4*>(wst + srow[r] * p.row_bytes + 16 * c);
       const uint32_t sc = (uint32_t)sst[srow[r] * p.srow_bytes + c];
-      block_dot<NT>(wq, sc, xa, acc[r], bad);
+      block_dot<NT>(wq, sc, xa, acc[r], scmax);
     }
   }
   if (nchunks & 31) {
@@ -168,7 +170,7 @@ __device__ __forceinline__ void warp_rows(const GemvParams& p, const uint8_t* __
       float part[NT];
 #pragma unroll
       for (int t = 0; t < NT; ++t) part[t] = upper ? acc[rr + 2][t] : acc[rr][t];
-      block_dot<NT>(wq, sc, xa, part, bad);
+      block_dot<NT>(wq, sc, xa, part, scmax);
 #pragma unroll
       for (int t = 0; t < NT; ++t) {
         acc[rr][t] = upper ? acc[rr][t] : part[t];
@@ -176,6 +178,8 @@ __device__ __forceinline__ void warp_rows(const GemvParams& p, const uint8_t* __
       }
     }
   }
+  // scale bytes past 2^13 (and the NaN code 255) would leave fp16's range: a device check
+  bad |= scmax > 127u + 13u;
 #pragma unroll
   for (int r = 0; r < kRowsPerWarp; ++r)
 #pragma unroll
