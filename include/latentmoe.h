@@ -20,7 +20,9 @@
  *    pointers unless the name ends in _host; device pointers must be 16-byte aligned.
  *  - Calls are asynchronous on `stream` (a cudaStream_t passed as void*; NULL = legacy
  *    default stream).  A handle must not be used from two streams at once and is not
- *    thread-safe.
+ *    thread-safe.  A handle's calls run on the device that was current at create time
+ *    (stream and buffers must belong to it); the caller's current device is restored
+ *    before each call returns.
  *  - The caller owns x, y, the weights and any routing buffers; the handle owns its
  *    workspace (sized at create time for cfg.max_tokens) and a device status word.
  *  - Every call returns an lmoe_status and never throws across the ABI.  Argument errors

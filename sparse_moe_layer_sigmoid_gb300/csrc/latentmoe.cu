@@ -481,9 +481,26 @@ lmoe_status check_call(lmoe_handle* h, const void* x, int32_t T) {
   if (!h) return LMOE_ERR_INVALID_ARG;
   if (T < 0 || T > h->cfg.max_tokens) return LMOE_ERR_INVALID_ARG;
   if (T > 0 && (!x || !aligned16(x))) return LMOE_ERR_INVALID_ARG;
-  if (cudaSetDevice(h->device) != cudaSuccess) return LMOE_ERR_CUDA;
   return LMOE_OK;
 }
+
+// Makes the handle's device current for one call and gives the caller's current device back
+// when the call returns.
+struct DeviceGuard {
+  int prev = -1;
+  bool ok = false;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) != cudaSuccess) {
+      prev = -1;
+      return;
+    }
+    ok = prev == dev || cudaSetDevice(dev) == cudaSuccess;
+  }
+  ~DeviceGuard() {
+    int cur = -1;
+    if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+  }
+};
 
 }  // namespace
 
@@ -521,8 +538,8 @@ lmoe_status latentmoe_create(const lmoe_config* cfg, lmoe_handle** out) {
 
 lmoe_status latentmoe_destroy(lmoe_handle* h) {
   if (!h) return LMOE_OK;
-  cudaSetDevice(h->device);
-  cudaError_t e = cudaDeviceSynchronize();
+  DeviceGuard dg(h->device);
+  cudaError_t e = dg.ok ? cudaDeviceSynchronize() : cudaErrorInvalidDevice;
   cudaFree(h->ws);
   delete h;
   return cuda_status(e);
@@ -533,6 +550,8 @@ lmoe_status latentmoe_route(lmoe_handle* h, const void* x, int32_t T, const lmoe
                             void* stream) {
   lmoe_status st = check_call(h, x, T);
   if (st != LMOE_OK) return st;
+  DeviceGuard dg(h->device);
+  if (!dg.ok) return LMOE_ERR_CUDA;
   if (!w || !w->w_router || !aligned16(w->w_router)) return LMOE_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const lmoe_config& c = h->cfg;
@@ -563,6 +582,8 @@ lmoe_status latentmoe_forward(lmoe_handle* h, const void* x, int32_t T, const lm
                               void* stream) {
   lmoe_status st = check_call(h, x, T);
   if (st != LMOE_OK) return st;
+  DeviceGuard dg(h->device);
+  if (!dg.ok) return LMOE_ERR_CUDA;
   if (!weights_ok(h, w, true) || (T > 0 && (!y || !aligned16(y)))) return LMOE_ERR_INVALID_ARG;
   h->last_launches = 0;
   if (T == 0) return LMOE_OK;
@@ -573,6 +594,8 @@ lmoe_status latentmoe_forward_routed(lmoe_handle* h, const void* x, int32_t T, c
                                      const int32_t* topk_idx, const float* topk_p, void* y, void* stream) {
   lmoe_status st = check_call(h, x, T);
   if (st != LMOE_OK) return st;
+  DeviceGuard dg(h->device);
+  if (!dg.ok) return LMOE_ERR_CUDA;
   if (!weights_ok(h, w, false) || (T > 0 && (!y || !aligned16(y) || !topk_idx || !topk_p)))
     return LMOE_ERR_INVALID_ARG;
   h->last_launches = 0;
@@ -585,7 +608,8 @@ lmoe_status latentmoe_forward_host(lmoe_handle* h, const void* x_host, int32_t T
   if (!h) return LMOE_ERR_INVALID_ARG;
   if (T < 0 || T > h->cfg.max_tokens || (T > 0 && (!x_host || !y_host))) return LMOE_ERR_INVALID_ARG;
   if (!weights_ok(h, w, true)) return LMOE_ERR_INVALID_ARG;
-  if (cudaSetDevice(h->device) != cudaSuccess) return LMOE_ERR_CUDA;
+  DeviceGuard dg(h->device);
+  if (!dg.ok) return LMOE_ERR_CUDA;
   h->last_launches = 0;
   if (T == 0) return LMOE_OK;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -604,7 +628,8 @@ lmoe_status latentmoe_forward_host(lmoe_handle* h, const void* x_host, int32_t T
 
 lmoe_status latentmoe_status(lmoe_handle* h, void* stream) {
   if (!h) return LMOE_ERR_INVALID_ARG;
-  if (cudaSetDevice(h->device) != cudaSuccess) return LMOE_ERR_CUDA;
+  DeviceGuard dg(h->device);
+  if (!dg.ok) return LMOE_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint32_t word = 0;
   LMOE_TRY(cudaStreamSynchronize(s));
