@@ -1,15 +1,19 @@
 #!/usr/bin/env python
 """Benchmark of the LatentMoE layer forward pass: tokens/s per layer and roofline fraction.
 
-Default workload: the K3-width bf16 prefill layer (T=4096, d=7168, l=3584, h=3072, E=128,
-k=16, N_s=2), synthetic seeded inputs and random-init weights resident in HBM.  One step is
-one full forward pass (router, top-k, dispatch, W_down, experts, combine + RMSNorm, shared
-experts, W_up).  L2 is flushed (512 MiB write, untimed) before every timed step.
+Headline workload: the full Kimi K3 layer at prefill, the largest layer that fits one GPU (T=8192,
+d=7168, l=3584, h=3072, E=896, k=16, N_s=2, MXFP4 routed experts, skewed router bias).  With one
+GPU the same JSON line also carries a record for each other full-size workload: the K3-width bf16
+prefill layer (E=128), K3 decode (T=32, MXFP4), the milder-skew MXFP4 prefill and the
+routing/dispatch stress test (T=65536).  Synthetic seeded inputs and random-init weights are
+resident in HBM; one step is one full forward pass; L2 is flushed (512 MiB write, untimed) before
+every timed step.
 
-  python bench.py [--gpus N --steps K --warmup W] [--impl ours|reference] [--workload NAME]
+  python bench.py [--gpus N --steps K --warmup W] [--impl ours|reference] [--workload NAME] [--no-sub]
 
-Under torchrun each rank runs an independent replica on its own GPU (the layer's tokens
-are independent: no collective), timed between barriers; the slowest rank sets the time.
+Under torchrun each rank runs an independent replica of the headline workload on its own GPU (the
+layer's tokens are independent: no collective), timed between barriers; the slowest rank sets
+the time.
 """
 from __future__ import annotations
 
@@ -31,6 +35,16 @@ sys.path.insert(0, ROOT)
 METRIC = "LatentMoE layer tokens/s; % of HBM (decode) / tensor (prefill) roofline"
 UNIT = "tokens/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# Dense FP4 : BF16 tensor rate by the datasheet (13.5 vs 2.25 PFLOP/s), used only when the MMA
+# microbenchmark cannot run.
+NOMINAL_FP4_RATIO = 6.0
+HEADLINE = "k3_mxfp4_prefill_skew"
+SUB_WORKLOADS = ("k3w_e128_bf16_prefill", "k3_mxfp4_decode", "k3_mxfp4_prefill_mild", "routing_dispatch_t65536")
+# token rows of the oracle's CPU baseline per workload (about 5-20 s of host work each: an MXFP4
+# row decodes up to 16 experts of 6144 x 3584 + 3584 x 3072 values)
+CPU_SAMPLE = {"k3_mxfp4_prefill_skew": 8, "k3w_e128_bf16_prefill": 8, "k3_mxfp4_decode": 4,
+              "k3_mxfp4_prefill_mild": 4, "routing_dispatch_t65536": 64, "tiny_f32": 64}
+ROUTED = ("routed_gate_up_glu", "routed_down")
 
 # DRAM bytes per launch of the dominant kernel from one ncu capture, valid only while the kernel
 # source is unchanged (sha256 of the file it lives in).  Filled from the committed profile.
@@ -82,28 +96,39 @@ def expert_weight_bytes(cfg, rows, cols):
     return rows * cols * (4 if cfg.routed_w == "f32" else 2)
 
 
-def stage_work(cfg, experts_touched):
-    """Algorithmic work of each stage: ('tensor', FLOPs) or ('hbm', bytes).
+def expert_record_bytes(width):
+    """Bytes of one three-term MXFP4 activation record of ``width`` values (block-scaled path)."""
+    return 3 * width // 2 + 3 * width // 32
 
-    Decode-shaped batches (T*k <= 32*E, the swapped-operand kernels) are bound by streaming the
-    touched experts' weights: their routed stages count those bytes (plus activations)."""
+
+def stage_work(cfg, experts_touched, mx=None):
+    """Algorithmic work of each stage: ('tensor', FLOPs) or ('hbm', bytes) or ('alu', FLOPs).
+
+    Decode-shaped batches (T*k <= 32*E) are bound by streaming the touched experts' weights: their
+    routed stages count those bytes plus the activations read and written.  ``mx``: MXFP4 experts
+    on the block-scaled path (activations travel as three-term records); default: MXFP4 weights."""
     T, d, l, h, E, k = cfg.tokens, cfg.d, cfg.latent, cfg.hidden, cfg.experts, cfg.top_k
     ns, hs = cfg.n_shared, cfg.shared_hidden
     ab = 4 if cfg.act == "f32" else 2
     rows = T * k
+    if mx is None:
+        mx = cfg.routed_w == "mxfp4"
+    mx = mx and not cfg.identity_experts
+    zrow = expert_record_bytes(l) if mx else ab * l          # a gathered row of z
+    arow = expert_record_bytes(h) if mx else ab * h          # a routed GLU activation row
     w = {
         # bf16 activations: tensor cores (over 3 bf16 terms of W_r); fp32: CUDA-core FMA
         "router_logits": ("tensor" if cfg.act == "bf16" else "alu", 2.0 * T * E * d),
         "topk": ("hbm", 4.0 * T * E + 8.0 * rows),
         "dispatch": ("hbm", 3 * 4.0 * rows),
         "w_down": ("tensor", 2.0 * T * d * l),
-        "scatter_rows": ("hbm", float(ab) * (T * l + rows * l)),
+        "scatter_rows": ("hbm", float(ab * T * l + rows * zrow)),
         "combine_rmsnorm": ("hbm", float(ab) * (rows * l + T * l)),
     }
     if not cfg.identity_experts and rows <= 32 * E:
         w["routed_gate_up_glu"] = ("hbm", float(experts_touched * expert_weight_bytes(cfg, 2 * h, l)
-                                                + ab * rows * (l + h)))
-        w["routed_down"] = ("hbm", float(experts_touched * expert_weight_bytes(cfg, l, h) + ab * rows * (h + l)))
+                                                + rows * (zrow + arow)))
+        w["routed_down"] = ("hbm", float(experts_touched * expert_weight_bytes(cfg, l, h) + rows * (arow + ab * l)))
     elif not cfg.identity_experts:
         w["routed_gate_up_glu"] = ("tensor", 2.0 * rows * l * 2 * h)
         w["routed_down"] = ("tensor", 2.0 * rows * h * l)
@@ -111,6 +136,28 @@ def stage_work(cfg, experts_touched):
         w["shared_gate_up_glu"] = ("tensor", 2.0 * T * d * 2 * ns * hs)
         w["final_gemm"] = ("tensor", 2.0 * T * (ns * hs + l) * d)
     return w
+
+
+def tensor_peak(stage, mx, peaks):
+    """(peak TFLOP/s, name) a tensor stage is measured against: the routed stages of the
+    block-scaled path run E2M1 x E2M1 MMAs (the FP4 peak), everything else bf16 MMAs."""
+    if mx and stage in ROUTED:
+        return peaks["fp4_tflops"], "fp4"
+    return peaks["bf16_tflops"], "bf16"
+
+
+def layer_roofline_ms(work, mx, peaks):
+    """The layer's roofline time: every stage at its own bound (FLOPs at the tensor peak of the
+    MMA kind that runs it, bytes at the HBM bandwidth), summed."""
+    t = 0.0
+    for stage, (kind, amount) in work.items():
+        if kind == "tensor":
+            t += amount / (tensor_peak(stage, mx, peaks)[0] * 1e12)
+        elif kind == "hbm":
+            t += amount / (peaks["hbm_gbs"] * 1e9)
+        else:
+            t += amount / (peaks["alu_tflops"] * 1e12)
+    return 1e3 * t
 
 
 def file_sha(rel):
@@ -223,7 +270,7 @@ def run_reference(args, cfg, rank, world):
 
     from sparse_moe_layer_sigmoid_gb300 import inputs
     dev = "cuda" if torch.cuda.is_available() else "cpu"
-    host = inputs.host_inputs(inputs.make_inputs(cfg, dev))
+    host = inputs.host_inputs(inputs.make_inputs(cfg, dev), lazy_experts=True)
     per_step = 1
     times = []
     for i in range(args.warmup + args.steps):
@@ -246,81 +293,71 @@ def run_reference(args, cfg, rank, world):
 def workload_config(cfg, args):
     return {"workload": cfg.name, "tokens": cfg.tokens, "d": cfg.d, "latent": cfg.latent, "hidden": cfg.hidden,
             "experts": cfg.experts, "top_k": cfg.top_k, "n_shared": cfg.n_shared,
-            "shared_hidden": cfg.shared_hidden, "routed_w": cfg.routed_w, "seed": cfg.seed,
+            "shared_hidden": cfg.shared_hidden, "routed_w": cfg.routed_w, "bias": cfg.bias, "seed": cfg.seed,
             "global_batch": cfg.tokens * args.gpus, "parallelism": f"replicas x{args.gpus}",
             "l2": "flushed before every timed step (512 MiB write, untimed)"}
 
 
-def main():
-    ap = argparse.ArgumentParser()
-    ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=30)
-    ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--workload", default="k3w_e128_bf16_prefill")
-    ap.add_argument("--cpu-sample", type=int, default=8, help="token rows for the oracle CPU baseline")
-    ap.add_argument("--single-cta", action="store_true",
-                    help="run every tensor-core GEMM on single CTAs (no CTA-pair GEMMs)")
-    args = ap.parse_args()
-    args.warmup = max(args.warmup, 3)
+def measured_peaks(binding, device, src):
+    """Roofline denominators: HBM and bf16 from MEASURED_PEAKS.json (else the fallback); the FP4
+    tensor peak as the bf16 one times the kind::mxf4 / kind::f16 rate ratio that this GPU shows in
+    the library's MMA microbenchmark (the datasheet ratio only if that cannot run)."""
+    peaks, how = src
+    out = {"hbm_gbs": peaks["hbm_gbs"], "bf16_tflops": peaks["bf16_tflops"],
+           "bf16_tflops_sustained": peaks.get("bf16_tflops_sustained"),
+           "source": f"{how} (MEASURED_PEAKS.json)" if how == "measured" else "fallback"}
+    props = __import__("torch").cuda.get_device_properties(device)
+    clock = peaks.get("sm_max_mhz", 2070.0)
+    out["alu_tflops"] = props.multi_processor_count * 128 * 2 * clock * 1e6 / 1e12
+    try:
+        f16 = binding.mma_peak_tflops("f16")
+        fp4 = binding.mma_peak_tflops("mxf4")
+        out["mma_f16_tflops"], out["mma_mxf4_tflops"] = f16, fp4
+        out["fp4_over_bf16"] = fp4 / f16
+        out["fp4_source"] = ("bf16_tflops x measured kind::mxf4 / kind::f16 rate of back-to-back CTA-pair "
+                             "MMAs (latentmoe_mma_peak)")
+    except Exception as exc:  # noqa: BLE001 - reported in the line
+        out["fp4_over_bf16"] = NOMINAL_FP4_RATIO
+        out["fp4_source"] = f"bf16_tflops x datasheet ratio {NOMINAL_FP4_RATIO} (microbenchmark failed: {exc})"
+    out["fp4_tflops"] = out["bf16_tflops"] * out["fp4_over_bf16"]
+    return out
 
+
+def measure_workload(cfg, args, peaks, world, rank, dist, dev, flags, with_cpu):
+    """One workload: warm-up, timed steps (device events), stage times, end-to-end through the
+    host-memory entry point, roofline figures and (rank 0) the oracle's CPU baseline."""
     import torch
 
-    from sparse_moe_layer_sigmoid_gb300 import configs
-
-    cfg = configs.CONFIGS[args.workload]
-    world, rank, local = rank_env()
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
-    if args.impl == "reference":
-        run_reference(args, cfg, rank, world)
-        if dist:
-            dist.destroy_process_group()
-        return
-
-    import __graft_entry__
-    from sparse_moe_layer_sigmoid_gb300 import inputs
-    from sparse_moe_layer_sigmoid_gb300 import binding
+    from sparse_moe_layer_sigmoid_gb300 import binding, inputs
     from sparse_moe_layer_sigmoid_gb300.binding import LatentMoE
 
-    if rank == 0:
-        __graft_entry__.build()
-    if dist:
-        dist.barrier()
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
     inp = inputs.make_inputs(cfg, dev)
-    layer = LatentMoE(cfg, flags=binding.LMOE_FLAG_SINGLE_CTA_GEMM if args.single_cta else 0)
+    layer = LatentMoE(cfg, flags=flags)
+    mx = cfg.routed_w == "mxfp4" and not (flags & (binding.LMOE_FLAG_MXFP4_DEQUANT | binding.LMOE_FLAG_SINGLE_CTA_GEMM))
     layer.enable_stage_timing()
     x = inp["x"]
     y = torch.empty((cfg.tokens, layer.out_width), dtype=x.dtype, device=dev)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
-
     props = torch.cuda.get_device_properties(dev)
-    gpu_id = f"GPU-{props.uuid}" if getattr(props, "uuid", None) else local
+    gpu_id = f"GPU-{props.uuid}" if getattr(props, "uuid", None) else dev.index
     clocks = ClockSampler(gpu_id) if rank == 0 else None
     for _ in range(args.warmup):
         flush.zero_()
         layer.forward(x, inp, y)
     torch.cuda.synchronize()
-    st = layer.status()
-    if st != 0:
-        raise RuntimeError(f"layer reported status {st} during warm-up")
+    if layer.status() != 0:
+        raise RuntimeError(f"{cfg.name}: layer reported an error status during warm-up")
     if clocks:
         clocks.wait_first_sample()
 
-    # grouped-GEMM M-tile utilisation of this routing (rows / (128-row tiles * 128))
     r = layer.route(x, inp)
+    stats = layer.routing_stats()
     counts = (r["offsets"][1:] - r["offsets"][:-1]).cpu()
-    m_tiles = int(((counts + 127) // 128).sum())
-    route_stats = {"rows": int(counts.sum()), "m_tiles_128": m_tiles,
-                   "m_tile_utilization": float(counts.sum()) / max(1, 128 * m_tiles),
-                   "experts_touched": int((counts > 0).sum()),
-                   "load_max_over_mean": float(counts.max()) / max(1e-9, float(counts.float().mean()))}
+    route_stats = {"rows": int(counts.sum()), "experts_touched": int((counts > 0).sum()),
+                   "load_max_over_mean": float(counts.max()) / max(1e-9, float(counts.float().mean())),
+                   "refined_tokens": stats["refined_tokens"], "near_ties": stats["near_ties"],
+                   "near_tie_rule": "exact k-th / (k+1)-th key gap below 1e-6, counted on the GPU"}
     del r
 
     ev0 = torch.cuda.Event(enable_timing=True)
@@ -349,12 +386,11 @@ def main():
     clk = clocks.stop() if clocks else None
     ms = max_over_ranks(sum(step_ms) / len(step_ms), dist, dev)
     if layer.status() != 0:
-        raise RuntimeError("layer reported an error status during the timed steps")
+        raise RuntimeError(f"{cfg.name}: layer reported an error status during the timed steps")
 
-    # end to end through the public host-memory entry point
+    # end to end through the public host-memory entry point (copies inside the timed region)
     x_host = x.cpu().pin_memory()
     y_host = torch.empty((cfg.tokens, layer.out_width), dtype=x.dtype, pin_memory=True)
-    layer.enable_stage_timing()
     for _ in range(2):
         layer.forward_host(x_host, inp, y_host)
     e2e_ms = []
@@ -367,58 +403,143 @@ def main():
     e2e = max_over_ranks(sum(e2e_ms) / len(e2e_ms), dist, dev)
     elem = x.element_size()
 
-    peaks, src = load_peaks()
-    work = stage_work(cfg, route_stats["experts_touched"])
+    work = stage_work(cfg, route_stats["experts_touched"], mx)
     st_ms = {k_: sum(v) / len(v) for k_, v in stages.items()}
     dom = max((k_ for k_ in work if k_ in st_ms), key=st_ms.get)
     kind, amount = work[dom]
+    roof = {"bound": kind, "kernel": dom}
     if kind == "tensor":
+        peak, pname = tensor_peak(dom, mx, peaks)
         achieved = amount / (st_ms[dom] * 1e-3) / 1e12
-        peak = peaks["bf16_tflops"]
-        unit = "TFLOP/s"
+        roof.update({"achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                     "peak_source": f"{pname}: " + (peaks["fp4_source"] if pname == "fp4"
+                                                    else peaks["source"] + " bf16_tflops (burst)")})
+        if pname == "fp4":  # three E2M1 activation terms: three MMAs per algorithmic product
+            roof["mma_work_per_flop"] = 3
+            roof["mma_pipe_frac"] = 3 * achieved / peak
     elif kind == "alu":
-        # fp32 FMA on CUDA cores: 152 SMs x 128 lanes x 2 FLOP x max SM clock
         achieved = amount / (st_ms[dom] * 1e-3) / 1e12
-        peak = 152 * 128 * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
-        unit = "TFLOP/s"
+        roof.update({"achieved": achieved, "peak": peaks["alu_tflops"], "unit": "TFLOP/s",
+                     "frac": achieved / peaks["alu_tflops"],
+                     "peak_source": "derived: SMs x 128 fp32 lanes x 2 x sm_max_mhz"})
     else:
         achieved = amount / (st_ms[dom] * 1e-3) / 1e9
-        peak = peaks["hbm_gbs"]
-        unit = "GB/s"
+        roof.update({"achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                     "peak_source": peaks["source"] + " hbm_gbs"})
     tr = TRAFFIC.get(cfg.name, {}).get(dom)
-    traffic = None
+    roof["traffic"] = None
     if tr and tr["bytes_per_launch"] and tr["sha256"] == file_sha(tr["src"]):
-        traffic = tr["bytes_per_launch"]
+        roof["traffic"] = tr["bytes_per_launch"]
     total_flops = sum(a for kd, a in work.values() if kd in ("tensor", "alu"))
+    total_bytes = sum(a for kd, a in work.values() if kd == "hbm")
+    roof_ms = layer_roofline_ms(work, mx, peaks)
+    layer_rec = {"flops": total_flops, "hbm_bytes_counted": total_bytes,
+                 "achieved_tflops": total_flops / (ms * 1e-3) / 1e12, "roofline_ms": roof_ms,
+                 "roofline_frac": roof_ms / ms,
+                 "roofline_rule": "each stage at its own bound: FLOPs at the peak of its MMA kind, bytes at HBM",
+                 "stages_ms": st_ms}
+    if mx and work["routed_gate_up_glu"][0] == "tensor":
+        routed = work["routed_gate_up_glu"][1] + work["routed_down"][1]
+        dense = total_flops - routed
+        fp4_roof = 1e3 * (routed / (peaks["fp4_tflops"] * 1e12) + dense / (peaks["bf16_tflops"] * 1e12))
+        three = 1e3 * (3 * routed / (peaks["fp4_tflops"] * 1e12) + dense / (peaks["bf16_tflops"] * 1e12))
+        layer_rec.update({"fp4_aware_roofline_ms": fp4_roof, "fp4_aware_frac": fp4_roof / ms,
+                          "three_term_ceiling_frac": fp4_roof / three,
+                          "fp4_aware_rule": "routed FLOPs at the FP4 peak + the rest at the bf16 peak"})
+    elif work.get("routed_gate_up_glu", ("", 0))[0] == "hbm":
+        layer_rec.update({"achieved_gbs": total_bytes / (ms * 1e-3) / 1e9,
+                          "hbm_frac": total_bytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"]})
+    else:
+        layer_rec["frac_of_bf16_peak"] = total_flops / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"]
+    if cfg.identity_experts:
+        layer_rec["achieved_gbs"] = total_bytes / (ms * 1e-3) / 1e9
+    dtype = ("e2m1 x e2m1 experts (three-term MXFP4 activations), bf16 dense" if mx else
+             "fp16 (MXFP4 experts decoded), bf16 dense" if cfg.routed_w == "mxfp4" else cfg.act)
+    rec = {"value": job_tokens_per_s(world, cfg.tokens, ms), "unit": UNIT, "ms_per_step": ms, "dtype": dtype,
+           "config": workload_config(cfg, args), "roofline": roof, "layer": layer_rec,
+           "e2e": {"value": job_tokens_per_s(world, cfg.tokens, e2e), "unit": UNIT,
+                   "h2d_bytes_per_step": cfg.tokens * cfg.d * elem,
+                   "d2h_bytes_per_step": cfg.tokens * layer.out_width * elem},
+           "gpu_launches": launches, "routing": route_stats, "clocks": clk}
+    layer.close()
+    y = flush = None
+    if with_cpu and rank == 0 and world == 1:
+        n = CPU_SAMPLE.get(cfg.name, 8) if args.cpu_sample is None else args.cpu_sample
+        if n > 0:
+            host = inputs.host_inputs(inp, lazy_experts=True)
+            dt = oracle_sample(cfg, host, n, cfg.seed + 99)
+            rec["cpu_baseline"] = {"value": n / dt, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+                                   "sample": f"{n} seeded token rows of the workload, fp64 oracle"}
+            del host
+    del inp
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return rec
 
-    line = {"metric": METRIC, "value": job_tokens_per_s(world, cfg.tokens, ms), "unit": UNIT, "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": cfg.act, "data": "synthetic",
-            "config": workload_config(cfg, args),
-            "roofline": {"bound": kind, "kernel": dom, "achieved": achieved,
-                         "peak": peak, "unit": unit, "frac": achieved / peak, "traffic": traffic,
-                         "peak_source": {"tensor": f"{src} bf16_tflops (burst)", "hbm": f"{src} hbm_gbs",
-                                         "alu": "derived: 152 SMs x 128 fp32 lanes x 2 x sm_max_mhz"}[kind]},
-            "layer": {"flops": total_flops, "achieved_tflops": total_flops / (ms * 1e-3) / 1e12,
-                      "frac_of_bf16_peak": total_flops / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"],
-                      "stages_ms": st_ms},
-            "e2e": {"value": job_tokens_per_s(world, cfg.tokens, e2e), "unit": UNIT,
-                    "h2d_bytes_per_step": cfg.tokens * cfg.d * elem,
-                    "d2h_bytes_per_step": cfg.tokens * layer.out_width * elem},
-            "gpu_launches": launches,
-            "routing": route_stats,
-            "clocks": clk}
-    if rank == 0 and world == 1 and args.cpu_sample > 0:
-        layer.close()
-        y = flush = None
-        host = inputs.host_inputs(inp)
-        dt = oracle_sample(cfg, host, args.cpu_sample, cfg.seed + 99)
-        line["cpu_baseline"] = {"value": args.cpu_sample / dt, "unit": UNIT, "cores": blas_threads(),
-                                "kind": "oracle",
-                                "sample": f"{args.cpu_sample} seeded token rows of the workload, fp64 oracle"}
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default=HEADLINE)
+    ap.add_argument("--no-sub", action="store_true", help="time the headline workload only")
+    ap.add_argument("--cpu-sample", type=int, default=None, help="token rows for the oracle CPU baseline")
+    ap.add_argument("--single-cta", action="store_true",
+                    help="run every tensor-core GEMM on single CTAs (no CTA-pair GEMMs)")
+    ap.add_argument("--mxfp4-dequant", action="store_true",
+                    help="MXFP4 experts through the dequantizing kernels instead of the block-scaled MMA")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    import torch
+
+    from sparse_moe_layer_sigmoid_gb300 import configs
+
+    cfg = configs.CONFIGS[args.workload]
+    world, rank, local = rank_env()
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    if args.impl == "reference":
+        run_reference(args, cfg, rank, world)
+        if dist:
+            dist.destroy_process_group()
+        return
+
+    import __graft_entry__
+    from sparse_moe_layer_sigmoid_gb300 import binding
+
+    if rank == 0:
+        __graft_entry__.build()
+    if dist:
+        dist.barrier()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    flags = ((binding.LMOE_FLAG_SINGLE_CTA_GEMM if args.single_cta else 0) |
+             (binding.LMOE_FLAG_MXFP4_DEQUANT if args.mxfp4_dequant else 0))
+    peaks = measured_peaks(binding, dev, load_peaks())
+    head = measure_workload(cfg, args, peaks, world, rank, dist, dev, flags, with_cpu=True)
+    subs = {}
+    if world == 1 and not args.no_sub and args.workload == HEADLINE:
+        for name in SUB_WORKLOADS:
+            subs[name] = measure_workload(configs.CONFIGS[name], args, peaks, world, rank, dist, dev, flags,
+                                          with_cpu=True)
+    line = {"metric": METRIC, "value": head["value"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": head["dtype"], "data": "synthetic",
+            "config": head["config"], "roofline": head["roofline"], "layer": head["layer"],
+            "e2e": head["e2e"], "gpu_launches": head["gpu_launches"], "routing": head["routing"],
+            "clocks": head["clocks"], "peaks": peaks}
+    if "cpu_baseline" in head:
+        line["cpu_baseline"] = head["cpu_baseline"]
+    if subs:
+        line["workloads"] = subs
     if rank == 0:
         print(json.dumps(line), flush=True)
-    layer.close()
     if dist:
         dist.destroy_process_group()
 

@@ -47,14 +47,17 @@ typedef enum {
   LMOE_ERR_CUDA = 3,          /* a CUDA runtime/driver call failed                       */
   LMOE_ERR_OOM = 4,           /* workspace allocation failed                             */
   LMOE_ERR_TIMEOUT = 5,       /* a kernel's bounded wait ran out (device status word)    */
-  LMOE_ERR_DEVICE_CHECK = 6   /* a kernel rejected its input (e.g. routing index >= E)   */
+  LMOE_ERR_DEVICE_CHECK = 6   /* a kernel rejected its input (e.g. routing index >= E),  */
+                              /* or a router logit recomputed exactly was further from   */
+                              /* the GEMM's than half the error margin selection assumes */
 } lmoe_status;
 
 typedef enum {
   LMOE_F32 = 0,               /* IEEE fp32                                               */
   LMOE_BF16 = 1,              /* bfloat16                                                */
-  LMOE_MXFP4 = 2              /* OCP MXFP4: E2M1 pairs per byte (element 2i in the low    */
+  LMOE_MXFP4 = 2,             /* OCP MXFP4: E2M1 pairs per byte (element 2i in the low    */
                               /* nibble) + one E8M0 scale byte per 32 elements along K   */
+  LMOE_F16 = 3                /* IEEE fp16 (latentmoe_mx3_quantize input only)           */
 } lmoe_dtype;
 
 /* Routed experts are the identity map: forward() returns u = sum_i p_i z (width l) and
@@ -65,6 +68,10 @@ typedef enum {
  * tiles, tcgen05 cta_group::2) where the latter would apply.  Same results up to fp32
  * accumulation order; for comparison and testing. */
 #define LMOE_FLAG_SINGLE_CTA_GEMM 0x2u
+/* MXFP4 routed experts: decode the E2M1 weights to fp16 in shared memory and run fp16 MMAs
+ * (kind::f16), or a CUDA-core GEMV for decode units of at most 4 rows, instead of the default
+ * block-scaled kind::mxf4 MMAs on three-term MXFP4 activations.  For comparison and testing. */
+#define LMOE_FLAG_MXFP4_DEQUANT 0x4u
 
 typedef struct {
   int32_t d;             /* model width                                                 */
@@ -113,7 +120,11 @@ lmoe_status latentmoe_destroy(lmoe_handle *h);
 /* Router and dispatch only (eq. 13 and the conversion of selections into expert batches).
  *   x              [T][d] act dtype
  *   topk_idx       [T][k] int32, out: selected experts in rank order (largest s+b first,
- *                  equal keys -> lower expert index first)
+ *                  equal keys -> lower expert index first).  Keys closer together than the
+ *                  router GEMM's error bound are compared exactly (fp64 from a ~44-bit logit),
+ *                  so set and order equal those of an exact evaluation except where the k-th
+ *                  and (k+1)-th keys differ by less than 1e-6 (near ties; counted, see
+ *                  latentmoe_debug_buffer "refine_count").
  *   topk_p         [T][k] fp32, out: p = s / sum of s over the selected set
  *   expert_offsets [E+1] int32, out: exclusive prefix sum of per-expert row counts
  *   tok_of_row     [T*k] int32, out: token of each row, rows ordered by (expert, token)
@@ -154,9 +165,11 @@ int32_t latentmoe_last_launch_count(const lmoe_handle *h);
 size_t latentmoe_workspace_bytes(const lmoe_handle *h);
 
 /* Test hook: bound every in-kernel wait of later calls to `timeout_ns` nanoseconds
- * (default 4e9), and with inject != 0 make the next forward's first routed GEMM tile
- * skip one pipeline-stage signal so that its consumer's bounded wait runs out and reports
- * LMOE_ERR_TIMEOUT.  No fault, trap or hang results; other tiles complete normally. */
+ * (default 4e9).  With inject = 1 the next forward's first routed GEMM kernel(s), with
+ * inject = 2 its W_down GEMM, skip the loads and the signal of one pipeline stage in their first
+ * CTA (or CTA pair), so that the consumer's bounded wait runs out and reports LMOE_ERR_TIMEOUT;
+ * the kernel waits (bounded) for its own loads and MMAs in flight before it exits.  No fault,
+ * trap or hang results; other tiles complete normally.  inject outside 0..2: INVALID_ARG. */
 lmoe_status latentmoe_set_wait_limit(lmoe_handle *h, uint64_t timeout_ns, int32_t inject);
 
 /* Stage timing.  With `events` non-NULL (n_events >= LMOE_NUM_STAGES + 1 cudaEvent_t
@@ -177,8 +190,13 @@ const char *latentmoe_stage_name(int32_t i);
  * handle's workspace, by name: "logits" [T][E] fp32, "z" [T][l], "gathered" [T*k][l] (the
  * expert-contiguous rows; after a full forward it holds the p-scaled expert outputs), "act"
  * [T*k][h] (routed GLU activations), "act_cat" [T][N_s*h_s + l] (shared activations and
- * RMSNorm(u)), "p_row" [T*k] fp32.  Activations use the act dtype, except that "z",
- * "gathered" and "act" are fp16 when routed_w is MXFP4; T is the last call's T.
+ * RMSNorm(u)), "p_row" [T*k] fp32, "refine_count" [2] int32 (tokens of the last routing whose
+ * list was settled on exact keys, and among them the near ties: exact k-th/(k+1)-th key gap
+ * below 1e-6).  Activations use the act dtype, except that "z", "gathered" and "act" are fp16
+ * when routed_w is MXFP4 and the dequantizing kernels run; on the block-scaled path "gathered"
+ * holds three-term MXFP4 records of z's rows (3*l/2 packed E2M1 bytes, then 3*l/32 E8M0 scales)
+ * until the down projection overwrites it with fp16 rows, and "act" the records of the GLU
+ * activations (3*h/2 + 3*h/32 bytes per row); T is the last call's T.
  * The pointers stay valid until latentmoe_destroy.  Unknown name or absent buffer:
  * LMOE_ERR_INVALID_ARG. */
 lmoe_status latentmoe_debug_buffer(const lmoe_handle *h, const char *name, void **ptr, size_t *bytes);
@@ -195,14 +213,42 @@ lmoe_status latentmoe_debug_buffer(const lmoe_handle *h, const char *name, void 
  *   256*ceil(T*E*4/256) + 2*256*ceil(ceil(T/256)*E*4/256) + 256*ceil((T*k/128+E+1)*16/256)
  *   + 256*ceil(T*4/256) + 512
  * bytes of it, plus 256*ceil(3*E*d*2/256) when act is BF16 and router_w is F32 (the three bf16
- * terms of W_r); with k=16 and a bf16 W_r, T up to 32,133 for E=128 and up to 4,631 for E=896; a
- * larger need returns LMOE_ERR_INVALID_ARG before any launch.  The first call on a device looks
- * up the array's device address (cudaGetSymbolAddress) and should come before any stream
- * capture.  Calls that overlap on the GPU share the array and race: serialise them.  Errors:
- * INVALID_ARG (bad field, pointer or size), CUDA. */
+ * terms of W_r), plus 256 for a status word; with k=16 and a bf16 W_r, T up to 32,133 for E=128
+ * and up to 4,631 for E=896; a larger need returns LMOE_ERR_INVALID_ARG before any launch.  The
+ * first call on a device (T == 0 included) looks up the array's device address
+ * (cudaGetSymbolAddress), which also loads the library's kernels and the array on that device:
+ * make one such call, e.g. with T = 0, at start-up, before any stream capture.  A device reset
+ * invalidates the looked-up address: use a new process after one.  Calls that overlap on the GPU
+ * share the array and race: serialise them.  Returned errors: INVALID_ARG (bad field, pointer or
+ * size), CUDA.  Errors the kernels detect (a bounded wait that ran out, an index out of range, a
+ * router logit outside the error margin) are ORed into a status word inside the array and are
+ * reported by latentmoe_route_noalloc_status(). */
 lmoe_status latentmoe_route_noalloc(const lmoe_config *cfg, const void *x, int32_t T, const lmoe_weights *w,
                                     int32_t *topk_idx, float *topk_p, int32_t *expert_offsets,
                                     int32_t *tok_of_row, int32_t *row_of, void *stream);
+
+/* Test hook: the three-term MXFP4 records the block-scaled expert GEMMs read, for `rows` rows of
+ * K values (src [rows][K], src_dtype LMOE_BF16 or LMOE_F16; K % 512 == 0).  Row r of dst (rows x
+ * (3*K/2 + 3*K/32) bytes) holds terms q_0, q_1, q_2 (K/2 bytes each, element 2i in the low nibble
+ * of byte i), then their E8M0 scales (K/32 bytes each): per 32-element block, q_t rounds what the
+ * earlier terms left to nearest on the E2M1 grid (ties to the even code) with the smallest
+ * power-of-two scale that leaves no element above 6.  Asynchronous on `stream`; allocates nothing.
+ * Errors: INVALID_ARG, CUDA. */
+lmoe_status latentmoe_mx3_quantize(const void *src, int32_t src_dtype, int64_t rows, int32_t K, void *dst,
+                                   void *stream);
+
+/* Measurement hook: the dense tensor-core rate of this GPU, in TFLOP/s, for the instruction shape
+ * the expert GEMMs issue (tcgen05.mma.cta_group::2, M = N = 256 per CTA pair, back to back on
+ * every SM pair from shared-memory operands, fp32 accumulation in TMEM): kind 0 = kind::f16 (bf16
+ * operands, K = 16 per instruction), kind 1 = kind::mxf4 (E2M1 operands with E8M0 scales per 32,
+ * K = 64).  Synchronises `stream`; takes a few milliseconds.  Errors: INVALID_ARG, CUDA, TIMEOUT. */
+lmoe_status latentmoe_mma_peak(int32_t kind, double *tflops, void *stream);
+
+/* For callers of latentmoe_route_noalloc: synchronise `stream`, then read and clear the status
+ * word its kernels report into on the current device (shared by every no-allocation call on
+ * that device since the last read), and return the first sticky error (TIMEOUT before
+ * DEVICE_CHECK) or LMOE_OK.  Allocates nothing. */
+lmoe_status latentmoe_route_noalloc_status(void *stream);
 
 /* Static description of a status code. */
 const char *latentmoe_status_string(lmoe_status s);

@@ -22,6 +22,7 @@ LMOE_OK, LMOE_ERR_INVALID_ARG, LMOE_ERR_UNSUPPORTED, LMOE_ERR_CUDA, LMOE_ERR_OOM
 DTYPES = {"f32": 0, "bf16": 1, "mxfp4": 2}
 LMOE_FLAG_IDENTITY_EXPERTS = 0x1
 LMOE_FLAG_SINGLE_CTA_GEMM = 0x2
+LMOE_FLAG_MXFP4_DEQUANT = 0x4
 LMOE_NUM_STAGES = 10
 
 
@@ -73,6 +74,12 @@ def _lib():
         lib.latentmoe_route_noalloc.argtypes = [C.POINTER(LmoeConfig), vp, i32, C.POINTER(LmoeWeights), vp, vp,
                                                 vp, vp, vp, vp]
         lib.latentmoe_route_noalloc.restype = st
+        lib.latentmoe_mx3_quantize.argtypes = [vp, i32, C.c_int64, i32, vp, vp]
+        lib.latentmoe_mx3_quantize.restype = st
+        lib.latentmoe_mma_peak.argtypes = [i32, C.POINTER(C.c_double), vp]
+        lib.latentmoe_mma_peak.restype = st
+        lib.latentmoe_route_noalloc_status.argtypes = [vp]
+        lib.latentmoe_route_noalloc_status.restype = st
         lib.latentmoe_debug_buffer.argtypes = [vp, C.c_char_p, C.POINTER(vp), C.POINTER(C.c_size_t)]
         lib.latentmoe_debug_buffer.restype = st
         lib.latentmoe_status_string.argtypes = [st]
@@ -141,6 +148,27 @@ def route_noalloc(cfg: LayerConfig, x, weights: dict, out: dict, stream=None):
     return _lib().latentmoe_route_noalloc(C.byref(c), _ptr(x), x.shape[0], C.byref(w), _ptr(out["idx"]),
                                           _ptr(out["p"]), _ptr(out["offsets"]), _ptr(out["tok_of_row"]),
                                           _ptr(out["row_of"]), _stream(stream))
+
+
+def mx3_quantize(x: torch.Tensor, stream=None) -> torch.Tensor:
+    """Three-term MXFP4 records of the rows of x (bf16 or fp16 [rows][K]) as uint8 [rows][3K/2 + 3K/32]."""
+    rows, K = x.shape
+    out = torch.empty((rows, 3 * K // 2 + 3 * K // 32), dtype=torch.uint8, device=x.device)
+    dt = {torch.bfloat16: 1, torch.float16: 3}[x.dtype]
+    _check(_lib().latentmoe_mx3_quantize(_ptr(x), dt, rows, K, _ptr(out), _stream(stream)), "mx3_quantize")
+    return out
+
+
+def mma_peak_tflops(kind: str, stream=None) -> float:
+    """Measured tensor-core rate (TFLOP/s) of back-to-back CTA-pair MMAs: kind "f16" or "mxf4"."""
+    out = C.c_double()
+    _check(_lib().latentmoe_mma_peak({"f16": 0, "mxf4": 1}[kind], C.byref(out), _stream(stream)), "mma_peak")
+    return out.value
+
+
+def route_noalloc_status(stream=None) -> int:
+    """Sticky status of the no-allocation route's kernels on the current device (read and cleared)."""
+    return _lib().latentmoe_route_noalloc_status(_stream(stream))
 
 
 class LatentMoE:
@@ -222,6 +250,11 @@ class LatentMoE:
         assert n * esize <= nbytes.value, (name, n * esize, nbytes.value)
         return _wrap_device_pointer(ptr.value, n * esize, dtype, shape)
 
+    def routing_stats(self) -> dict:
+        """Tokens of the last routing settled on exact keys, and the near ties among them."""
+        v = self.debug_buffer("refine_count", torch.int32, (2,)).cpu()
+        return {"refined_tokens": int(v[0]), "near_ties": int(v[1])}
+
     def status(self, stream=None) -> int:
         return _lib().latentmoe_status(self._h, _stream(stream))
 
@@ -246,5 +279,6 @@ class LatentMoE:
         return {_lib().latentmoe_stage_name(i).decode(): self._events[i].elapsed_time(self._events[i + 1])
                 for i in range(LMOE_NUM_STAGES)}
 
-    def set_wait_limit(self, timeout_ns: int, inject: bool = False):
-        _check(_lib().latentmoe_set_wait_limit(self._h, int(timeout_ns), 1 if inject else 0), "set_wait_limit")
+    def set_wait_limit(self, timeout_ns: int, inject: int = 0):
+        """Bound in-kernel waits; inject 1 (first routed GEMM) or 2 (W_down) drops one pipeline signal."""
+        _check(_lib().latentmoe_set_wait_limit(self._h, int(timeout_ns), int(inject)), "set_wait_limit")

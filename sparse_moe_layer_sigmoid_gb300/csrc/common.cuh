@@ -19,6 +19,9 @@ enum : uint32_t {
   kWaitAccFull = 1u << 12,    // epilogue: accumulator complete
   kWaitMmaDone = 1u << 13     // producer: own MMA finished with a stage (paired CTAs)
 };
+// Diagnostic bit beside kStatusDeviceCheck: a router logit recomputed exactly differed from the
+// GEMM's by more than half the margin the top-k selection relies on.
+constexpr uint32_t kStatusRouterMargin = 1u << 16;
 
 enum DType : int { kF32 = 0, kBF16 = 1, kMXFP4 = 2, kF16 = 3 /* internal: fp16 activations */ };
 
@@ -28,6 +31,8 @@ constexpr int kTileM = 128;
 constexpr int kTileS = 16;
 // Rows of the M tile a pair of clustered CTAs shares (each CTA computes 128 of them).
 constexpr int kTileP = 256;
+// Token rows of one tile of the block-scaled (MXFP4) expert GEMM.
+constexpr int kTileMx = 192;
 // Tokens per dispatch chunk (one CTA, one bit per token in the per-expert masks).
 constexpr int kDispatchChunk = 256;
 

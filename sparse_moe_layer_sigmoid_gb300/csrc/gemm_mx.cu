@@ -1,0 +1,602 @@
+// Routed-expert GEMMs with MXFP4 weights on the block-scaled tensor-core MMA
+// (tcgen05.mma.cta_group::2.kind::mxf4): the experts' E2M1 bytes go from HBM to shared memory by
+// TMA exactly as stored and are multiplied as stored, their E8M0 scales applied by the MMA
+// itself, so no instruction of the kernel touches a weight value (page "What K3 actually is",
+// srikanthmalla.com: MXFP4 expert weights, and the dequantizing path's lost 4-bit arithmetic
+// rate that this kernel keeps; page "Lesson 6 - LatentMoE", kimi-k3-course.pages.dev, eq. 11 for
+// the routed experts' gate/up and down projections).
+//
+// The token rows arrive as three-term MXFP4 records (mx.cuh), so every product is E2M1 x E2M1:
+//
+//   D[f][j] = sum_t sum_c W_e[f][c] * 2^sw[f][c/32] * Q_t[row0 + j][c] * 2^sx_t[row0 + j][c/32]
+//
+// Swapped operands as in the bf16 grouped kernel: the expert's weights are the M = 256 side (128
+// rows in each CTA of the pair), its token rows the N side (at most 192 per tile, each expert's
+// rows cut into ceil(rows / 192) tiles of equal width rounded up to 16).  Per 256-element k-block
+// each CTA stages 16 KB of weights and 3 x 12 KB of token terms; the even CTA issues 3 terms x 4
+// MMAs of K = 64.
+//
+// Scale factors live in TMEM (two slots of 64 columns beside the two 192-column accumulators).
+// The producer brings each pair of k-blocks' scale bytes into a ring of their own by TMA (the
+// weight rows' scales, and all 192 token rows' scales of the three terms, since both CTAs' MMA
+// halves read every token row); a group of four scale warps (one per TMEM lane quadrant) copies
+// them from shared memory into TMEM with tcgen05.st in the layout the MMA reads: weight row m at
+// lane m, column + m/32 (four columns per 128 scale blocks); token row n at lane n % 32 of every
+// quadrant, column + n/32.  A slot is rewritten once the MMAs that read it have completed (a
+// commit multicast to both CTAs).
+//
+// Epilogues: gate/up tiles (128 features: rows 0..15 of each 32-row quarter are gate rows, 16..31
+// the matching up rows) compute SiLU(gate) * up, stage 64 tokens x 64 features in shared memory
+// and quantise them into three-term MXFP4 records (one 32-feature block per thread), the down
+// projection's input; down tiles (256 output features) scale each token column by its routing
+// weight and write fp16 rows.  Every wait is bounded; after an abort the even CTA waits for its
+// loads and MMAs in flight before the pair lets go of shared memory and TMEM.
+#include <cuda.h>
+#include <cuda_fp16.h>
+
+#include "common.cuh"
+#include "internal.h"
+#include "mx.cuh"
+#include "ptx.cuh"
+#include "tc_common.cuh"
+
+namespace lmoe {
+namespace {
+
+using namespace tc;
+constexpr int kWRows = 128;                              // weight rows per CTA (M = 256 per pair)
+constexpr int kMaxN = 192;                               // token columns per tile (MMA N)
+constexpr int kXRows = kMaxN / 2;                        // token rows per CTA
+constexpr int KB = 256;                                  // K elements per stage (128 packed bytes)
+constexpr uint32_t kWBytes = kWRows * 128;               // 16 KB
+constexpr uint32_t kXTermBytes = kXRows * 128;           // 12 KB
+constexpr uint32_t kXBytes = kMxTerms * kXTermBytes;     // 36 KB
+constexpr uint32_t kStageBytes = kWBytes + kXBytes;      // 52 KB
+constexpr int kStages = 3;
+// scale ring: per stage the scale bytes of two k-blocks (16 bytes of each row)
+constexpr uint32_t kWsBytes = kWRows * 16;               // 2 KB: this CTA's weight rows
+constexpr uint32_t kXsTermBytes = kMaxN * 16;            // 3 KB: all 192 token rows of one term
+constexpr uint32_t kSfStageBytes = kWsBytes + kMxTerms * kXsTermBytes;  // 11 KB
+// Token boxes sized to the tile: a CTA loads 8, 32 or 96 rows of each term (tiles of N <= 16,
+// <= 64, <= 192 tokens) and 16, 64 or 192 rows of their scales; decode tiles hold 1-4 rows.
+constexpr int kNumBoxes = 3;
+__host__ __device__ constexpr int x_box_rows(int b) { return b == 0 ? 8 : b == 1 ? 32 : kXRows; }
+__host__ __device__ constexpr int box_for(int n) { return n <= 16 ? 0 : n <= 64 ? 1 : 2; }
+constexpr int kSfStages = 3;
+constexpr int kSfSlots = 2;
+constexpr uint32_t kSfCols = 64;                         // weight scales 8 + token scales 3 x 2 x 8
+constexpr uint32_t kSfBase = 2 * kMaxN;                  // TMEM column of slot 0
+constexpr uint32_t kTmemCols = 512;
+constexpr int kThreads = 320;                            // producer, MMA, 4 epilogue, 4 scale warps
+constexpr int kEpiTokens = 64;                           // tokens per GLU epilogue chunk
+constexpr int kEpiStride = 72;                           // floats per staged token: blocks at 0 and 36
+constexpr uint32_t kEpiBytes = kEpiTokens * kEpiStride * 4;  // 18 KB (the down epilogue uses 8 KB)
+constexpr size_t kSmem =
+    (size_t)kStages * kStageBytes + (size_t)kSfStages * kSfStageBytes + kEpiBytes + 1024 + 512;
+static_assert(kSfBase + kSfSlots * kSfCols <= kTmemCols, "TMEM budget");
+static_assert(kMaxN == kTileMx, "the dispatch cuts expert rows into tiles of this kernel's width");
+static_assert(kSmem <= 227 * 1024, "shared memory budget");
+
+struct MxParams {
+  int num_kb;             // 256-element k-blocks (even: K % 512 == 0)
+  int K;                  // reduction width
+  int num_wt;             // weight tiles per expert
+  int glu_h;              // > 0: gate/up weights [2h][K], 128 features per tile; 0: 256 rows per tile
+  const int4* tiles;      // token tiles of 192 rows: {expert, first tile of expert, rows of expert, first row}
+  const int32_t* num_tiles;
+  void* C;                // GLU: records of the activations [rows][ldc bytes]; down: fp16 [rows][ldc]
+  int64_t ldc;
+  int out_k;              // GLU: h (the width the records hold)
+  const float* row_scale; // down: routing weight per row
+  uint32_t* status;
+  uint64_t timeout_ns;
+  int inject;             // test hook: pair 0 skips its first stage (loads and signal)
+};
+
+struct MxTile {
+  int expert, wt;
+  int row0, nrows, n;
+};
+
+__device__ __forceinline__ int4 mx_entry(const MxParams& p, int t) { return p.tiles[t / p.num_wt]; }
+
+__device__ __forceinline__ MxTile decode_mx(const MxParams& p, int t, int4 tl) {
+  const int rows = tl.z;
+  const int ntiles = (rows + kMaxN - 1) / kMaxN;
+  const int local = t - tl.y * p.num_wt;
+  MxTile ti;
+  ti.expert = tl.x;
+  ti.wt = local / ntiles;
+  const int j = local - ti.wt * ntiles;
+  // equal widths (multiples of 16, at most 192): width * (ntiles - 1) < rows, so no tile is empty
+  const int width = ((rows + ntiles - 1) / ntiles + 15) & ~15;
+  ti.row0 = tl.w + j * width;
+  ti.nrows = min(width, rows - j * width);
+  ti.n = (ti.nrows + 15) & ~15;
+  return ti;
+}
+
+// Epilogue-warp barrier (the 4 epilogue warps only).
+__device__ __forceinline__ void epi_barrier() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+template <bool GLU>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    tc_mx_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmWs,
+                 const __grid_constant__ CUtensorMap tmX0, const __grid_constant__ CUtensorMap tmX1,
+                 const __grid_constant__ CUtensorMap tmX2, const __grid_constant__ CUtensorMap tmXs0,
+                 const __grid_constant__ CUtensorMap tmXs1, const __grid_constant__ CUtensorMap tmXs2,
+                 const MxParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = ptx::smem_addr(smem_raw);
+  uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);  // same offset in both CTAs
+  uint8_t* sf_ring = smem + kStages * kStageBytes;
+  float* epi = reinterpret_cast<float*>(sf_ring + kSfStages * kSfStageBytes);
+  uint64_t* full = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(epi) + kEpiBytes);
+  uint64_t* empty = full + kStages;
+  uint64_t* sfr_full = empty + kStages;        // scale ring: bytes landed (this CTA)
+  uint64_t* sfr_empty = sfr_full + kSfStages;  // scale ring: copied to TMEM by the 4 scale warps
+  uint64_t* sf_full = sfr_empty + kSfStages;   // TMEM scale slot written (even CTA, 8 warps)
+  uint64_t* sf_empty = sf_full + kSfSlots;     // TMEM scale slot read by its MMAs (both CTAs)
+  uint64_t* tmem_full = sf_empty + kSfSlots;
+  uint64_t* tmem_empty = tmem_full + 2;
+  uint64_t* drain_bar = tmem_empty + 2;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain_bar + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  volatile int* epi_ok = abort_flag + 1;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = ptx::cluster_ctarank();  // 0: issues the MMAs; 1: partner
+  const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+  ptx::ArmedStages armed, armed_sf;  // producer: operand stages (even CTA) and scale stages armed
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      ptx::mbar_init(&full[s], 1);
+      ptx::mbar_init(&empty[s], 1);
+    }
+    for (int s = 0; s < kSfStages; ++s) {
+      ptx::mbar_init(&sfr_full[s], 1);
+      ptx::mbar_init(&sfr_empty[s], 4);
+    }
+    for (int s = 0; s < kSfSlots; ++s) {
+      ptx::mbar_init(&sf_full[s], 8);  // 4 scale warps in each CTA of the pair
+      ptx::mbar_init(&sf_empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      ptx::mbar_init(&tmem_full[a], 1);
+      ptx::mbar_init(&tmem_empty[a], 8);  // 4 epilogue warps in each CTA of the pair
+    }
+    ptx::mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+    ptx::prefetch_tmap(&tmW);
+    ptx::prefetch_tmap(&tmWs);
+    ptx::prefetch_tmap(&tmX0);
+    ptx::prefetch_tmap(&tmX1);
+    ptx::prefetch_tmap(&tmX2);
+    ptx::prefetch_tmap(&tmXs0);
+    ptx::prefetch_tmap(&tmXs1);
+    ptx::prefetch_tmap(&tmXs2);
+  }
+  if (warp == 1) ptx::tmem_alloc_pair(tmem_holder, kTmemCols);
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::cluster_sync();  // both CTAs' barriers exist before any signal crosses the pair
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+
+  const int total = *p.num_tiles * p.num_wt;
+
+  if (warp == 0 && lane == 0) {
+    // ------------------------------------------------------------------ TMA producer (both CTAs)
+    int stage = 0, iter = 0, sstage = 0;
+    uint32_t phase = 0, sphase = 0;
+    bool first = true;
+    int4 entry = pair < total ? mx_entry(p, pair) : make_int4(0, 0, 0, 0);
+    for (int t = pair; t < total; t += npairs) {
+      const MxTile ti = decode_mx(p, t, entry);
+      if (t + npairs < total) entry = mx_entry(p, t + npairs);
+      const int xrow0 = ti.row0 + (int)rank * (ti.n >> 1);  // this CTA's N/2 token rows
+      const int wrow_glu = (ti.wt * 128 + (int)rank * 64) / 16;                // GLU: first 16-row group
+      const int wrow = ti.wt * 2 * kWRows + (int)rank * kWRows;                // down: first weight row
+      const int bsel = box_for(ti.n);
+      const CUtensorMap* tmX = bsel == 0 ? &tmX0 : bsel == 1 ? &tmX1 : &tmX2;
+      const CUtensorMap* tmXs = bsel == 0 ? &tmXs0 : bsel == 1 ? &tmXs1 : &tmXs2;
+      const uint32_t stage_tx = kWBytes + kMxTerms * (uint32_t)x_box_rows(bsel) * 128u;
+      const uint32_t sf_tx = kWsBytes + kMxTerms * (uint32_t)(2 * x_box_rows(bsel)) * 16u;
+      for (int kb = 0; kb < p.num_kb; ++kb, ++iter) {
+        if ((kb & 1) == 0) {
+          // scale bytes of k-blocks kb, kb+1 (16 bytes of every row) into this CTA's scale ring
+          if (!ptx::mbar_wait_bounded(&sfr_empty[sstage], sphase ^ 1u, abort_flag, p.status, p.timeout_ns,
+                                      kWaitProducer))
+            goto done;
+          uint8_t* ss = sf_ring + sstage * kSfStageBytes;
+          ptx::mbar_arrive_expect_tx(&sfr_full[sstage], sf_tx);
+          armed_sf.arm(sstage, sphase);
+          const int xb = 8 * kb;  // byte of k-block kb in a scale row (16-byte aligned: kb even)
+          if (GLU)
+            ptx::tma_load_5d(ss, &tmWs, &sfr_full[sstage], xb, 0, 0, wrow_glu, ti.expert);
+          else
+            ptx::tma_load_3d(ss, &tmWs, &sfr_full[sstage], xb, wrow, ti.expert);
+#pragma unroll
+          for (int q = 0; q < kMxTerms; ++q)
+            ptx::tma_load_2d(ss + kWsBytes + q * kXsTermBytes, tmXs, &sfr_full[sstage], q * (p.K / 32) + xb,
+                             ti.row0);
+          if (++sstage == kSfStages) {
+            sstage = 0;
+            sphase ^= 1u;
+          }
+        }
+        if (!ptx::mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, p.status, p.timeout_ns, kWaitProducer))
+          goto done;
+        // the MMA read both CTAs' copy of this stage: pass the release on to the partner
+        if (rank == 0 && iter >= kStages) ptx::mbar_arrive_remote(&empty[stage], 1);
+        uint8_t* sW = smem + stage * kStageBytes;
+        uint8_t* sX = sW + kWBytes;
+        const uint32_t bar = ptx::mapa_shared(&full[stage], 0);  // the even CTA's full[stage]
+        const bool skip = p.inject && first && pair == 0;  // test hook, the same in both CTAs
+        first = false;
+        if (!skip) {
+          if (rank == 0) {
+            ptx::mbar_arrive_expect_tx(&full[stage], 2 * stage_tx);
+            armed.arm(stage, phase);
+          }
+          if (GLU)  // 4 x (16 gate rows, 16 up rows) of features wt*128 + rank*64 ..
+            ptx::tma_load_5d_pair(sW, &tmW, bar, kb * 128, 0, 0, wrow_glu, ti.expert);
+          else
+            ptx::tma_load_3d_pair(sW, &tmW, bar, kb * 128, wrow, ti.expert);
+#pragma unroll
+          for (int q = 0; q < kMxTerms; ++q)  // term q: 96 rows x 128 bytes at byte q * K/2 + kb * 128 of each record
+            ptx::tma_load_2d_pair(sX + q * kXTermBytes, tmX, bar, q * (p.K / 2) + kb * 128, xrow0);
+        }
+        if (++stage == kStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+  } else if (warp == 1 && lane == 0 && rank == 0) {
+    // ------------------------------------------------------------------ MMA issuer (even CTA)
+    int s = 0, g = 0;
+    uint32_t ph = 0;
+    int it = 0;
+    int4 entry = pair < total ? mx_entry(p, pair) : make_int4(0, 0, 0, 0);
+    for (int t = pair; t < total; t += npairs, ++it) {
+      const MxTile ti = decode_mx(p, t, entry);
+      if (t + npairs < total) entry = mx_entry(p, t + npairs);
+      const int acc = it & 1;
+      const uint32_t use = (uint32_t)(it >> 1);
+      if (!ptx::mbar_wait_bounded(&tmem_empty[acc], (use & 1u) ^ 1u, abort_flag, p.status, p.timeout_ns,
+                                  kWaitAccFree))
+        goto done;
+      ptx::tc_fence_after();
+      const uint32_t d_tmem = tmem_base + (uint32_t)(acc * kMaxN);
+      for (int kb = 0; kb < p.num_kb; ++kb, ++g) {
+        const int slot = g & 1;
+        if (!ptx::mbar_wait_bounded(&full[s], ph, abort_flag, p.status, p.timeout_ns, kWaitFull)) goto done;
+        if (!ptx::mbar_wait_bounded(&sf_full[slot], (uint32_t)(g >> 1) & 1u, abort_flag, p.status, p.timeout_ns,
+                                    kWaitConverted))
+          goto done;
+        ptx::tc_fence_after();
+        const uint32_t w_addr = ptx::smem_addr(smem + s * kStageBytes);
+        const uint32_t x_addr = w_addr + kWBytes;
+        const uint32_t sf = tmem_base + kSfBase + (uint32_t)slot * kSfCols;
+#pragma unroll
+        for (int kk = 0; kk < KB / 64; ++kk) {
+          const uint32_t sf_id = 2u * (uint32_t)(kk & 1);
+          const uint32_t idesc = ptx::idesc_mxf4(2 * kWRows, ti.n, sf_id, sf_id);
+          const uint64_t a_desc = ptx::sw128_kmajor_desc(w_addr + kk * 32);
+#pragma unroll
+          for (int q = 0; q < kMxTerms; ++q)
+            ptx::mma_mxf4_pair(d_tmem, a_desc, ptx::sw128_kmajor_desc(x_addr + q * kXTermBytes + kk * 32), idesc,
+                               sf + 4u * (uint32_t)(kk >> 1), sf + 8u + 16u * (uint32_t)q + 8u * (uint32_t)(kk >> 1),
+                               (kb | kk | q) != 0 ? 1u : 0u);
+        }
+        ptx::mma_commit_pair(&empty[s]);
+        ptx::mma_commit_pair_both(&sf_empty[slot]);
+        if (++s == kStages) {
+          s = 0;
+          ph ^= 1u;
+        }
+      }
+      ptx::mma_commit_pair(&tmem_full[acc]);
+    }
+  } else if (warp >= 6) {
+    // ------------------------------------------------------------------ scale warps (both CTAs)
+    const int q = warp & 3;  // TMEM lane quadrant this warp writes
+    const uint32_t lane_base = tmem_base + ((uint32_t)(32 * q) << 16) + kSfBase;
+    int g = 0, ss = 0;
+    uint32_t sph = 0;
+    for (int t = pair; t < total; t += npairs) {
+      for (int kb = 0; kb < p.num_kb; ++kb, ++g) {
+        const int slot = g & 1;
+        int ok = 1;
+        if (lane == 0) {
+          if ((kb & 1) == 0)
+            ok = ptx::mbar_wait_bounded(&sfr_full[ss], sph, abort_flag, p.status, p.timeout_ns, kWaitFull);
+          ok = ok && ptx::mbar_wait_bounded(&sf_empty[slot], ((uint32_t)(g >> 1) & 1u) ^ 1u, abort_flag, p.status,
+                                            p.timeout_ns, kWaitAccFree);
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) goto sf_done;
+        {
+          const uint8_t* st = sf_ring + ss * kSfStageBytes + 8 * (kb & 1);  // this k-block's 8 bytes of a row
+          const uint2 wv = *reinterpret_cast<const uint2*>(st + (32 * q + lane) * 16);
+          uint32_t lo[kMxTerms][8], hi[kMxTerms][8];
+#pragma unroll
+          for (int tt = 0; tt < kMxTerms; ++tt)
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              uint2 v = make_uint2(0u, 0u);
+              if (c < kMaxN / 32) v = *reinterpret_cast<const uint2*>(st + kWsBytes + tt * kXsTermBytes + (32 * c + lane) * 16);
+              lo[tt][c] = v.x;
+              hi[tt][c] = v.y;
+            }
+          ptx::tc_fence_after();
+          const uint32_t col = lane_base + (uint32_t)slot * kSfCols;
+          ptx::tmem_st_32x32b_x1(col + (uint32_t)q, wv.x);       // weight scale blocks 0..3 of the k-block
+          ptx::tmem_st_32x32b_x1(col + 4u + (uint32_t)q, wv.y);  // blocks 4..7
+#pragma unroll
+          for (int tt = 0; tt < kMxTerms; ++tt) {
+            ptx::tmem_st_32x32b_x8(col + 8u + 16u * (uint32_t)tt, lo[tt]);
+            ptx::tmem_st_32x32b_x8(col + 16u + 16u * (uint32_t)tt, hi[tt]);
+          }
+          ptx::tmem_st_wait();
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            if (rank == 0)
+              ptx::mbar_arrive(&sf_full[slot]);
+            else
+              ptx::mbar_arrive_remote(&sf_full[slot], 0);
+            if (kb & 1) ptx::mbar_arrive(&sfr_empty[ss]);  // both k-blocks of the stage copied
+          }
+        }
+        if (kb & 1) {
+          if (++ss == kSfStages) {
+            ss = 0;
+            sph ^= 1u;
+          }
+        }
+      }
+    }
+  sf_done:;
+  } else if (warp >= 2) {
+    // ------------------------------------------------------------------ epilogue (both CTAs)
+    const int q = warp & 3;  // TMEM lane quadrant this warp may access
+    const int etid = threadIdx.x - 64;  // 0..127
+    int it = 0;
+    int4 entry = pair < total ? mx_entry(p, pair) : make_int4(0, 0, 0, 0);
+    for (int t = pair; t < total; t += npairs, ++it) {
+      const MxTile ti = decode_mx(p, t, entry);
+      if (t + npairs < total) entry = mx_entry(p, t + npairs);
+      const int acc = it & 1;
+      const uint32_t use = (uint32_t)(it >> 1);
+      // down x p: the item's row scales, lane l holding token 32 c + l
+      float sc_reg[kMaxN / 32];
+#pragma unroll
+      for (int c = 0; c < kMaxN / 32; ++c) {
+        const int jl = c * 32 + lane;
+        sc_reg[c] = !GLU && jl < ti.nrows ? p.row_scale[ti.row0 + jl] : 0.0f;
+      }
+      // one warp waits; the decision is shared so that the four warps leave (or stay) together
+      if (warp == 2 && lane == 0) {
+        const int ok =
+            ptx::mbar_wait_bounded(&tmem_full[acc], use & 1u, abort_flag, p.status, p.timeout_ns, kWaitAccFull);
+        if (ok && rank == 0) ptx::mbar_arrive_remote(&tmem_full[acc], 1);
+        *epi_ok = ok;
+      }
+      epi_barrier();
+      const int ok = *epi_ok;
+      epi_barrier();  // every warp has read the flag before the next item rewrites it
+      if (!ok) break;
+      ptx::tc_fence_after();
+      const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * kMaxN);
+      if (GLU) {
+        // this CTA's 64 features fb .. fb+63: warp q holds 16 of them.  64 tokens at a time are
+        // staged as fp32 [token][2 blocks of 32 features] (block b at float 36 b of a 72-float
+        // row), then thread (token j, block b) quantises its 32 values into the record of row j
+        const int fb = ti.wt * 128 + (int)rank * 64;
+        uint8_t* out = static_cast<uint8_t*>(p.C);
+        const int64_t half_k = p.out_k / 2, sc0 = mx3_scale_offset(p.out_k), kscale = p.out_k / 32;
+        const int foff = 36 * (q >> 1) + 16 * (q & 1);  // this warp's 16 features in a staged row
+        for (int c0 = 0; c0 < ti.n; c0 += kEpiTokens) {
+#pragma unroll
+          for (int h2 = 0; h2 < kEpiTokens / 32; ++h2) {
+            if (c0 + 32 * h2 >= ti.n) break;  // uniform
+            uint32_t r[32];
+            ptx::tmem_ld_32x32b_x32(t_row + c0 + 32 * h2, r);
+            ptx::tmem_ld_wait();
+            // token pair (2i, 2i+1): lanes < 16 finish token 2i, lanes >= 16 token 2i+1
+#pragma unroll
+            for (int i2 = 0; i2 < 16; ++i2) {
+              const float send = __uint_as_float(lane < 16 ? r[2 * i2 + 1] : r[2 * i2]);
+              const float recv = __shfl_xor_sync(0xffffffffu, send, 16);
+              const float gt = lane < 16 ? __uint_as_float(r[2 * i2]) : recv;
+              const float up = lane < 16 ? recv : __uint_as_float(r[2 * i2 + 1]);
+              epi[(32 * h2 + 2 * i2 + (lane >> 4)) * kEpiStride + foff + (lane & 15)] = silu(gt) * up;
+            }
+          }
+          epi_barrier();
+          {
+            const int j = etid >> 1, b = etid & 1;
+            if (c0 + j < ti.nrows) {
+              float v[32];
+              const float4* src = reinterpret_cast<const float4*>(epi + j * kEpiStride + 36 * b);
+#pragma unroll
+              for (int e4 = 0; e4 < 8; ++e4) {
+                const float4 f = src[e4];
+                v[4 * e4] = f.x;
+                v[4 * e4 + 1] = f.y;
+                v[4 * e4 + 2] = f.z;
+                v[4 * e4 + 3] = f.w;
+              }
+              uint32_t packed[kMxTerms][4], scb[kMxTerms];
+              mx::quantize_block(v, packed, scb);
+              uint8_t* rec = out + (int64_t)(ti.row0 + c0 + j) * p.ldc;
+              const int f = fb + 32 * b;
+#pragma unroll
+              for (int tt = 0; tt < kMxTerms; ++tt) {
+                *reinterpret_cast<uint4*>(rec + tt * half_k + f / 2) =
+                    make_uint4(packed[tt][0], packed[tt][1], packed[tt][2], packed[tt][3]);
+                rec[sc0 + tt * kscale + f / 32] = (uint8_t)scb[tt];
+              }
+            }
+          }
+          epi_barrier();  // the staging tile is rewritten by the next chunk
+        }
+      } else {
+        // 32 output features per warp; each 32-token chunk goes through shared memory as
+        // [token][feature] fp16 and leaves in 16-byte stores
+        const int f0 = ti.wt * 2 * kWRows + (int)rank * kWRows + 32 * q;
+        __half* out = static_cast<__half*>(p.C);
+        uint16_t* st = reinterpret_cast<uint16_t*>(epi) + q * (32 * 32);
+        for (int c0 = 0; c0 < ti.n; c0 += 32) {
+          uint32_t r[32];
+          ptx::tmem_ld_32x32b_x32(t_row + c0, r);
+          ptx::tmem_ld_wait();
+          const int c = c0 >> 5;
+          float scv = 0.f;
+#pragma unroll
+          for (int cc = 0; cc < kMaxN / 32; ++cc)
+            if (cc == c) scv = sc_reg[cc];
+#pragma unroll
+          for (int i2 = 0; i2 < 32; ++i2) {
+            const float sc = __shfl_sync(0xffffffffu, scv, i2);
+            st[i2 * 32 + lane] = __half_as_ushort(__float2half_rn(__uint_as_float(r[i2]) * sc));
+          }
+          __syncwarp();
+#pragma unroll
+          for (int v = lane; v < 32 * 4; v += 32) {
+            const int j = v >> 2, part = v & 3;
+            if (c0 + j < ti.nrows)
+              *reinterpret_cast<uint4*>(out + (int64_t)(ti.row0 + c0 + j) * p.ldc + f0 + 8 * part) =
+                  *reinterpret_cast<const uint4*>(st + j * 32 + 8 * part);
+          }
+          __syncwarp();
+        }
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if (rank == 0)
+          ptx::mbar_arrive(&tmem_empty[acc]);
+        else
+          ptx::mbar_arrive_remote(&tmem_empty[acc], 0);
+      }
+    }
+  }
+done:
+  ptx::tc_fence_before();
+  __syncthreads();  // every role has left its loop; the abort flag no longer changes
+  if (*abort_flag) {  // let the loads and MMAs in flight finish before the pair lets go of them
+    if (warp == 0 && lane == 0) {
+      ptx::drain_armed(sfr_full, armed_sf, p.timeout_ns);  // this CTA's scale loads
+      if (rank == 0) ptx::drain_armed(full, armed, p.timeout_ns);  // both halves' operand loads
+    }
+    if (rank == 0 && warp == 1 && lane == 0) ptx::drain_mma_pair(drain_bar, p.timeout_ns);
+    __syncthreads();
+  }
+  ptx::cluster_sync();  // the partner no longer reads this CTA's shared memory or signals it
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc_pair(tmem_base, kTmemCols);
+  }
+}
+
+template <bool GLU>
+cudaError_t launch_mx_inst(const CUtensorMap (&maps)[8], const MxParams& p, long long items, cudaStream_t s) {
+  auto kern = tc_mx_kernel<GLU>;
+  static PerDeviceValue max_pairs_of;
+  std::atomic<int>* slot = max_pairs_of.current();
+  if (!slot) return cudaErrorInvalidDevice;
+  int max_pairs = slot->load(std::memory_order_acquire);
+  if (max_pairs == 0) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = kSmem;
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+    if (e != cudaSuccess) return e;
+    if (n < 1) return cudaErrorInvalidConfiguration;
+    max_pairs = n;
+    slot->store(n, std::memory_order_release);
+  }
+  const int pairs = (int)(items < max_pairs ? items : max_pairs);
+  kern<<<2 * pairs, kThreads, kSmem, s>>>(maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6], maps[7], p);
+  return cudaGetLastError();
+}
+
+bool encode_u8(CUtensorMap* m, const void* ptr, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
+               const cuuint32_t* box, bool swizzle128) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc || !ptr) return false;
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, (cuuint32_t)rank, const_cast<void*>(ptr), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+cudaError_t launch_tc_mx(const TcMx& g, const int4* tiles_m, const int32_t* num_tiles_m, int max_tiles_m,
+                         uint32_t* status, uint64_t timeout_ns, cudaStream_t s, int inject) {
+  const bool glu = g.glu_h > 0;
+  if (!g.w.ptr || !g.w_scale || !g.x || !g.C || !tiles_m || !num_tiles_m) return cudaErrorInvalidValue;
+  if (g.K % 512 || g.rows < 1) return cudaErrorInvalidValue;
+  if (glu ? (g.glu_h % 128 || g.out_features != g.glu_h || g.out_features % 512 || g.w.rows != 2 * g.glu_h)
+          : (g.out_features % (2 * kWRows) || g.w.rows != g.out_features || !g.row_scale || g.ldc % 8))
+    return cudaErrorInvalidValue;
+  const int64_t x_rec = mx3_row_bytes(g.K), kscale = g.K / 32, E = g.w.depth;
+  CUtensorMap maps[8];  // weights, weight scales, token terms (3 box heights), token scales (3)
+  bool ok = glu ? make_map_glu_interleaved(&maps[0], g.w, g.glu_h, kWRows / 32, true)
+                : make_map_fp4(&maps[0], g.w, kWRows, 128, true);
+  for (int b = 0; b < kNumBoxes; ++b) {
+    // the packed terms of the records as a 2-D byte array {3 K/2, rows}: boxes of 128 bytes
+    const cuuint64_t dims[2] = {(cuuint64_t)(kMxTerms * g.K / 2), (cuuint64_t)g.rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)x_rec};
+    const cuuint32_t box[2] = {128, (cuuint32_t)x_box_rows(b)};
+    ok = ok && encode_u8(&maps[2 + b], g.x, 2, dims, strides, box, true);
+    // the records' scale bytes {3 K/32, rows}: boxes of 16 bytes x (2 x the term box) rows
+    const cuuint64_t sdims[2] = {(cuuint64_t)(kMxTerms * kscale), (cuuint64_t)g.rows};
+    const cuuint32_t sbox[2] = {16, (cuuint32_t)(2 * x_box_rows(b))};
+    ok = ok && encode_u8(&maps[5 + b], static_cast<const uint8_t*>(g.x) + mx3_scale_offset(g.K), 2, sdims, strides,
+                         sbox, false);
+  }
+  if (glu) {  // weight scales [E][2h][K/32] as {K/32, 16, 2, h/16, E}: the rows in the weights' order
+    const int64_t h = g.glu_h;
+    const cuuint64_t dims[5] = {(cuuint64_t)kscale, 16, 2, (cuuint64_t)(h / 16), (cuuint64_t)E};
+    const cuuint64_t strides[4] = {(cuuint64_t)kscale, (cuuint64_t)(h * kscale), (cuuint64_t)(16 * kscale),
+                                   (cuuint64_t)(2 * h * kscale)};
+    const cuuint32_t box[5] = {16, 16, 2, (cuuint32_t)(kWRows / 32), 1};
+    ok = ok && encode_u8(&maps[1], g.w_scale, 5, dims, strides, box, false);
+  } else {    // weight scales [E][rows][K/32]
+    const cuuint64_t dims[3] = {(cuuint64_t)kscale, (cuuint64_t)g.w.rows, (cuuint64_t)E};
+    const cuuint64_t strides[2] = {(cuuint64_t)kscale, (cuuint64_t)(g.w.rows * kscale)};
+    const cuuint32_t box[3] = {16, (cuuint32_t)kWRows, 1};
+    ok = ok && encode_u8(&maps[1], g.w_scale, 3, dims, strides, box, false);
+  }
+  if (!ok) return cudaErrorInvalidValue;
+  MxParams p = {};
+  p.num_kb = g.K / KB;
+  p.K = g.K;
+  p.num_wt = glu ? g.glu_h / 128 : g.out_features / (2 * kWRows);
+  p.glu_h = glu ? g.glu_h : 0;
+  p.tiles = tiles_m;
+  p.num_tiles = num_tiles_m;
+  p.C = g.C;
+  p.ldc = glu ? mx3_row_bytes(g.out_features) : g.ldc;
+  p.out_k = g.out_features;
+  p.row_scale = g.row_scale;
+  p.status = status;
+  p.timeout_ns = timeout_ns;
+  p.inject = inject;
+  const long long items = (long long)max_tiles_m * p.num_wt;
+  if (items == 0) return cudaSuccess;
+  return glu ? launch_mx_inst<true>(maps, p, items, s) : launch_mx_inst<false>(maps, p, items, s);
+}
+
+}  // namespace lmoe

@@ -50,6 +50,7 @@ struct PairParams {
   const float* row_scale;
   uint32_t* status;
   uint64_t timeout_ns;
+  int inject;  // test hook: pair 0 skips its first stage (loads and signal) so a bounded wait runs out
 };
 
 struct PairTile {
@@ -81,12 +82,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   uint64_t* empty = full + kStages;
   uint64_t* tmem_full = empty + kStages;
   uint64_t* tmem_empty = tmem_full + 2;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(tmem_empty + 2);
+  uint64_t* drain_bar = tmem_empty + 2;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = ptx::cluster_ctarank();  // 0: issues the MMAs; 1: partner
   const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+  ptx::ArmedStages armed;  // even producer: stages armed (both halves' loads land on its full[s])
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -97,6 +100,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       ptx::mbar_init(&tmem_full[a], 1);
       ptx::mbar_init(&tmem_empty[a], 8);  // 4 epilogue warps in each CTA of the pair
     }
+    ptx::mbar_init(drain_bar, 1);
     *abort_flag = 0;
     ptx::fence_mbar_init();
     ptx::prefetch_tmap(&tmA);
@@ -123,6 +127,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // by counting, with no division per k-block: the producer's issue latency is on the
     // pipeline's critical path.
     constexpr bool PERIODIC = EPI == kEpiF32;  // the router's terms: A's K wraps every a_kb_period
+    bool first = true;
     for (int t = pair; t < total; t += npairs) {
       const PairTile ti = decode_pair_tile<BN_OUT>(p, t);
       const int ay = ti.row0 + (int)rank * kRows;
@@ -137,13 +142,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (rank == 0 && iter >= kStages) ptx::mbar_arrive_remote(&empty[stage], 1);
         uint8_t* sA = smem + stage * kStageBytes;
         const uint32_t bar = ptx::mapa_shared(&full[stage], 0);  // the even CTA's full[stage]
-        if (rank == 0) ptx::mbar_arrive_expect_tx(&full[stage], 2 * kStageBytes);
-        ptx::tma_load_3d_pair(sA, &tmA, bar, ka * BK, ay, 0);
-        if (GLU)
-          ptx::tma_load_3d_pair(sA + kHalfBytes, &tmB0, bar, kb * BK, by, bz_glu);
-        else
-          ptx::tma_load_3d_pair(sA + kHalfBytes, second ? &tmB1 : &tmB0, bar, kin * BK, by,
-                                second ? 0 : ti.group + goff);
+        const bool skip = p.inject && first && pair == 0;  // test hook, the same in both CTAs
+        first = false;
+        if (!skip) {
+          if (rank == 0) {
+            ptx::mbar_arrive_expect_tx(&full[stage], 2 * kStageBytes);
+            armed.arm(stage, phase);
+          }
+          ptx::tma_load_3d_pair(sA, &tmA, bar, ka * BK, ay, 0);
+          if (GLU)
+            ptx::tma_load_3d_pair(sA + kHalfBytes, &tmB0, bar, kb * BK, by, bz_glu);
+          else
+            ptx::tma_load_3d_pair(sA + kHalfBytes, second ? &tmB1 : &tmB0, bar, kin * BK, by,
+                                  second ? 0 : ti.group + goff);
+        }
         if (PERIODIC) {
           if (++ka == p.a_kb_period) ka = 0;
         } else {
@@ -229,7 +241,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   }
 done:
   ptx::tc_fence_before();
-  __syncthreads();
+  __syncthreads();  // every role has left its loop; the abort flag no longer changes
+  if (*abort_flag) {  // the even CTA lets both halves' loads and its MMAs finish
+    if (rank == 0 && warp == 0 && lane == 0) ptx::drain_armed(full, armed, p.timeout_ns);
+    if (rank == 0 && warp == 1 && lane == 0) ptx::drain_mma_pair(drain_bar, p.timeout_ns);
+    __syncthreads();
+  }
   ptx::cluster_sync();  // the partner no longer reads this CTA's shared memory or signals it
   if (warp == 1) {
     ptx::tc_fence_after();
@@ -277,7 +294,7 @@ bool tc_pair_supported(const TcGemm& g) {
   return g.N % (g.epi == kEpiF32 ? 4 : 32) == 0;
 }
 
-cudaError_t launch_tc_pair(const TcGemm& g, uint32_t* status, uint64_t timeout_ns, cudaStream_t s) {
+cudaError_t launch_tc_pair(const TcGemm& g, uint32_t* status, uint64_t timeout_ns, cudaStream_t s, int inject) {
   if (!tc_pair_supported(g)) return cudaErrorInvalidValue;
   const bool glu = g.epi == kEpiGluBF16;
   const int bn_out = glu ? BN / 2 : BN;
@@ -303,6 +320,7 @@ cudaError_t launch_tc_pair(const TcGemm& g, uint32_t* status, uint64_t timeout_n
   p.row_scale = g.row_scale;
   p.status = status;
   p.timeout_ns = timeout_ns;
+  p.inject = inject;
   const long long tiles = (long long)p.num_m_tiles * p.num_n_tiles;
   if (tiles == 0) return cudaSuccess;
   switch (g.epi) {

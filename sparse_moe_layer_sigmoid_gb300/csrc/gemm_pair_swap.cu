@@ -56,6 +56,7 @@ struct PSwapParams {
   const float* row_scale;
   uint32_t* status;
   uint64_t timeout_ns;
+  int inject;  // test hook: pair 0 skips its first stage (loads and signal) so a bounded wait runs out
 };
 
 struct PSwapTile {
@@ -99,12 +100,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   uint64_t* empty = full + kStages;
   uint64_t* tmem_full = empty + kStages;
   uint64_t* tmem_empty = tmem_full + 2;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(tmem_empty + 2);
+  uint64_t* drain_bar = tmem_empty + 2;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = ptx::cluster_ctarank();  // 0: issues the MMAs; 1: partner
   const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+  ptx::ArmedStages armed;  // even producer: stages armed (both halves' loads land on its full[s])
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -115,6 +118,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       ptx::mbar_init(&tmem_full[a], 1);
       ptx::mbar_init(&tmem_empty[a], 8);  // 4 epilogue warps in each CTA of the pair
     }
+    ptx::mbar_init(drain_bar, 1);
     *abort_flag = 0;
     ptx::fence_mbar_init();
     ptx::prefetch_tmap(&tmW);
@@ -133,6 +137,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------------ TMA producer (both CTAs)
     int stage = 0, iter = 0;
     uint32_t phase = 0;
+    bool first = true;
     int4 entry = pair < total ? pswap_entry(p, pair) : make_int4(0, 0, 0, 0);
     for (int t = pair; t < total; t += npairs) {
       const PSwapTile ti = decode_pswap(p, t, entry);
@@ -147,13 +152,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         uint8_t* sW = smem + stage * kStageBytes;
         uint8_t* sX = sW + kWBytes;
         const uint32_t bar = ptx::mapa_shared(&full[stage], 0);  // the even CTA's full[stage]
-        if (rank == 0) ptx::mbar_arrive_expect_tx(&full[stage], 2 * kStageBytes);
-        if (GLU) {  // 4 x (16 gate rows, 16 up rows) of features wt*128 + rank*64 ..
-          ptx::tma_load_5d_pair(sW, &tmW, bar, kb * BK, 0, 0, (ti.wt * 128 + (int)rank * 64) / 16, ti.expert);
-        } else {
-          ptx::tma_load_3d_pair(sW, &tmW, bar, kb * BK, ti.wt * 2 * kWRows + (int)rank * kWRows, ti.expert);
+        const bool skip = p.inject && first && pair == 0;  // test hook, the same in both CTAs
+        first = false;
+        if (!skip) {
+          if (rank == 0) {
+            ptx::mbar_arrive_expect_tx(&full[stage], 2 * kStageBytes);
+            armed.arm(stage, phase);
+          }
+          if (GLU) {  // 4 x (16 gate rows, 16 up rows) of features wt*128 + rank*64 ..
+            ptx::tma_load_5d_pair(sW, &tmW, bar, kb * BK, 0, 0, (ti.wt * 128 + (int)rank * 64) / 16, ti.expert);
+          } else {
+            ptx::tma_load_3d_pair(sW, &tmW, bar, kb * BK, ti.wt * 2 * kWRows + (int)rank * kWRows, ti.expert);
+          }
+          ptx::tma_load_3d_pair(sX, &tmX, bar, kb * BK, xrow0, 0);
         }
-        ptx::tma_load_3d_pair(sX, &tmX, bar, kb * BK, xrow0, 0);
         if (++stage == kStages) {
           stage = 0;
           phase ^= 1u;
@@ -276,7 +288,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   }
 done:
   ptx::tc_fence_before();
-  __syncthreads();
+  __syncthreads();  // every role has left its loop; the abort flag no longer changes
+  if (*abort_flag) {  // the even CTA lets both halves' loads and its MMAs finish
+    if (rank == 0 && warp == 0 && lane == 0) ptx::drain_armed(full, armed, p.timeout_ns);
+    if (rank == 0 && warp == 1 && lane == 0) ptx::drain_mma_pair(drain_bar, p.timeout_ns);
+    __syncthreads();
+  }
   ptx::cluster_sync();  // the partner no longer reads this CTA's shared memory or signals it
   if (warp == 1) {
     ptx::tc_fence_after();
@@ -314,7 +331,7 @@ cudaError_t launch_pswap_inst(const CUtensorMap& w, const CUtensorMap& x, const 
 }  // namespace
 
 cudaError_t launch_tc_pair_swap(const TcSwap& g, const int4* tiles_p, const int32_t* num_tiles_p, int max_tiles_p,
-                                uint32_t* status, uint64_t timeout_ns, cudaStream_t s) {
+                                uint32_t* status, uint64_t timeout_ns, cudaStream_t s, int inject) {
   const bool glu = g.epi == kEpiGluBF16;
   if (g.epi != kEpiGluBF16 && g.epi != kEpiScaleBF16) return cudaErrorInvalidValue;
   if (g.w_scale || g.ab_f16 || g.K % BK || g.ldc % 8) return cudaErrorInvalidValue;
@@ -336,6 +353,7 @@ cudaError_t launch_tc_pair_swap(const TcSwap& g, const int4* tiles_p, const int3
   p.row_scale = g.row_scale;
   p.status = status;
   p.timeout_ns = timeout_ns;
+  p.inject = inject;
   const long long items = (long long)max_tiles_p * p.num_wt;
   if (items == 0) return cudaSuccess;
   return glu ? launch_pswap_inst<true>(mw, mx, p, items, s) : launch_pswap_inst<false>(mw, mx, p, items, s);

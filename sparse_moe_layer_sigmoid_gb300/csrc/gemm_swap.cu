@@ -63,6 +63,7 @@ struct SwapParams {
   const uint8_t* w_scale;
   uint32_t* status;
   uint64_t timeout_ns;
+  int inject;  // test hook: CTA 0 skips its first stage (loads and signal) so a bounded wait runs out
 };
 
 struct SwapTile {
@@ -117,10 +118,12 @@ __global__ void __launch_bounds__(SwapCfg<FP4W>::kThreads, 1)
   uint64_t* empty2 = full2 + S2;
   uint64_t* tmem_full = empty2 + S2;
   uint64_t* tmem_empty = tmem_full + 2;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(tmem_empty + 2);
+  uint64_t* drain_bar = tmem_empty + 2;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  ptx::ArmedStages armed;  // producer: ring stages with loads issued (teardown after an abort)
   if (threadIdx.x == 0) {
     for (int s = 0; s < S1; ++s) {
       ptx::mbar_init(&full1[s], 1);
@@ -134,6 +137,7 @@ __global__ void __launch_bounds__(SwapCfg<FP4W>::kThreads, 1)
       ptx::mbar_init(&tmem_full[a], 1);
       ptx::mbar_init(&tmem_empty[a], 4);
     }
+    ptx::mbar_init(drain_bar, 1);
     *abort_flag = 0;
     ptx::fence_mbar_init();
     ptx::prefetch_tmap(&tmW);
@@ -151,23 +155,29 @@ __global__ void __launch_bounds__(SwapCfg<FP4W>::kThreads, 1)
     // ------------------------------------------------------------------ TMA producer
     int stage = 0;
     uint32_t phase = 0;
+    bool first = true;
     for (int u = blockIdx.x; u < total; u += gridDim.x) {
       const SwapTile ti = decode_swap(p, u);
       if (ti.nrows <= p.skip_rows_upto) continue;
       const uint32_t tx = C::kWStageBytes + (uint32_t)SUB * C::kXSubBytes;
       for (int st = 0; st < num_st; ++st) {
         if (!ptx::mbar_wait_bounded(&empty1[stage], phase ^ 1u, abort_flag, p.status, p.timeout_ns, kWaitProducer)) goto done;
-        uint8_t* sW = smem + stage * C::kStage1Bytes;
-        uint8_t* sX = sW + C::kWStageBytes;
-        ptx::mbar_arrive_expect_tx(&full1[stage], tx);
-        const int kx = FP4W ? st * (BK * SUB / 2) : st * BK;  // bytes (packed) or elements
-        // weights: one box of 128 rows (gate/up: 4 x (16 gate rows, 16 up rows) of features wt*64..)
-        if (GLU)
-          ptx::tma_load_5d(sW, &tmW, &full1[stage], kx, 0, 0, ti.wt * 4, ti.expert);
-        else
-          ptx::tma_load_3d(sW, &tmW, &full1[stage], kx, ti.wt * kWRows, ti.expert);
-        // tokens: the unit's 16 rows for the stage's SUB 64-column blocks, one box
-        ptx::tma_load_3d(sX, &tmX, &full1[stage], 0, ti.row0, st * SUB);
+        const bool skip = p.inject && first && blockIdx.x == 0;  // test hook: drop one stage
+        first = false;
+        if (!skip) {
+          uint8_t* sW = smem + stage * C::kStage1Bytes;
+          uint8_t* sX = sW + C::kWStageBytes;
+          ptx::mbar_arrive_expect_tx(&full1[stage], tx);
+          armed.arm(stage, phase);
+          const int kx = FP4W ? st * (BK * SUB / 2) : st * BK;  // bytes (packed) or elements
+          // weights: one box of 128 rows (gate/up: 4 x (16 gate rows, 16 up rows) of features wt*64..)
+          if (GLU)
+            ptx::tma_load_5d(sW, &tmW, &full1[stage], kx, 0, 0, ti.wt * 4, ti.expert);
+          else
+            ptx::tma_load_3d(sW, &tmW, &full1[stage], kx, ti.wt * kWRows, ti.expert);
+          // tokens: the unit's 16 rows for the stage's SUB 64-column blocks, one box
+          ptx::tma_load_3d(sX, &tmX, &full1[stage], 0, ti.row0, st * SUB);
+        }
         if (++stage == S1) {
           stage = 0;
           phase ^= 1u;
@@ -333,7 +343,12 @@ __global__ void __launch_bounds__(SwapCfg<FP4W>::kThreads, 1)
   }
 done:
   ptx::tc_fence_before();
-  __syncthreads();
+  __syncthreads();  // every role has left its loop; the abort flag no longer changes
+  if (*abort_flag) {  // let the loads and MMAs in flight finish before the CTA lets go of them
+    if (warp == 0 && lane == 0) ptx::drain_armed(full1, armed, p.timeout_ns);
+    if (warp == 1 && lane == 0) ptx::drain_mma(drain_bar, p.timeout_ns);
+    __syncthreads();
+  }
   if (warp == 1) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem_base, C::kTmemCols);
@@ -359,7 +374,8 @@ cudaError_t launch_swap_inst(const CUtensorMap& w, const CUtensorMap& x, const S
 
 }  // namespace
 
-cudaError_t launch_tc_swap(const TcSwap& g, uint32_t* status, uint64_t timeout_ns, int num_sms, cudaStream_t s) {
+cudaError_t launch_tc_swap(const TcSwap& g, uint32_t* status, uint64_t timeout_ns, int num_sms, cudaStream_t s,
+                           int inject) {
   const bool glu = g.epi == kEpiGluBF16 || g.epi == kEpiGluF16;
   const bool out_f16 = g.epi == kEpiGluF16 || g.epi == kEpiScaleF16;
   const bool fp4 = g.w_scale != nullptr;
@@ -386,6 +402,7 @@ cudaError_t launch_tc_swap(const TcSwap& g, uint32_t* status, uint64_t timeout_n
   p.w_scale = g.w_scale;
   p.status = status;
   p.timeout_ns = timeout_ns;
+  p.inject = inject;
   const long long units = (long long)g.max_tiles_s * p.num_wt;
   if (units == 0) return cudaSuccess;
   const int grid = (int)(units < num_sms ? units : num_sms);

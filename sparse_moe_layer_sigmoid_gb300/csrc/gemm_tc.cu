@@ -139,10 +139,12 @@ __global__ void __launch_bounds__(Cfg<BN, FP4B>::kThreads, 1)
   uint64_t* empty2 = full2 + S2;
   uint64_t* tmem_full = empty2 + S2;
   uint64_t* tmem_empty = tmem_full + 2;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(tmem_empty + 2);
+  uint64_t* drain_bar = tmem_empty + 2;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  ptx::ArmedStages armed;  // producer: ring stages with loads issued (teardown after an abort)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S1; ++s) {
@@ -157,6 +159,7 @@ __global__ void __launch_bounds__(Cfg<BN, FP4B>::kThreads, 1)
       ptx::mbar_init(&tmem_full[a], 1);
       ptx::mbar_init(&tmem_empty[a], 4);
     }
+    ptx::mbar_init(drain_bar, 1);
     *abort_flag = 0;
     ptx::fence_mbar_init();
     ptx::prefetch_tmap(&tmA);
@@ -199,6 +202,7 @@ __global__ void __launch_bounds__(Cfg<BN, FP4B>::kThreads, 1)
           constexpr uint32_t kBoxB = FP4B ? kBoxRows * BK / 2 : kBoxBytes;  // bytes of one B box
           const int kx = FP4B ? kb * (BK / 2) : kb * BK;                     // B inner coordinate
           ptx::mbar_arrive_expect_tx(&full1[stage], C::kStage1Bytes);
+          armed.arm(stage, phase);
           ptx::tma_load_3d(sA, &tmA, &full1[stage], ka * BK, ti.row0, 0);
           if (GLU) {
             ptx::tma_load_3d(sB, &tmB0, &full1[stage], kx, j0, grp);
@@ -403,7 +407,12 @@ __global__ void __launch_bounds__(Cfg<BN, FP4B>::kThreads, 1)
   }
 done:
   ptx::tc_fence_before();
-  __syncthreads();
+  __syncthreads();  // every role has left its loop; the abort flag no longer changes
+  if (*abort_flag) {  // let the loads and MMAs in flight finish before the CTA lets go of them
+    if (warp == 0 && lane == 0) ptx::drain_armed(full1, armed, p.timeout_ns);
+    if (warp == 1 && lane == 0) ptx::drain_mma(drain_bar, p.timeout_ns);
+    __syncthreads();
+  }
   if (warp == 1) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem_base, C::kTmemCols);

@@ -60,6 +60,7 @@ struct GemvParams {
   const float* row_scale; // plain: routing weight per row
   uint32_t* status;
   uint64_t timeout_ns;
+  int inject;             // test hook: CTA 0 skips its first stage (loads and signal)
 };
 
 // Activations in shared memory: token t, 16-byte quarter i of K block c = 32 j + l at
@@ -288,31 +289,41 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
+      bool first = true;
+      ptx::ArmedStages armed;
       for (int it = it_begin; it < it_end; ++it) {
         const GemvItem g = gemv_item(p, it);
         const int4 tl = p.tiles_s[g.q];
         if (tl.z > kGemvMaxRows) continue;  // the tensor-core kernel takes this unit
         if (!ptx::mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, p.status, p.timeout_ns, kWaitProducer))
           break;
-        uint8_t* wst = ring + (size_t)stage * p.stage_bytes;
-        uint8_t* sst = wst + kItemRows * p.row_bytes;
-        ptx::mbar_arrive_expect_tx(&full[stage], p.stage_bytes);
-        const int base = tl.x * p.w_rows;  // first weight row of the expert
-        const int f0 = g.fb * p.feats_per_item;
-        if (GLU) {  // 16 gate rows, then the 16 matching up rows
-          ptx::tma_load_3d(wst, &tmW, &full[stage], 0, 0, base + f0);
-          ptx::tma_load_3d(wst + 16 * p.row_bytes, &tmW, &full[stage], 0, 0, base + p.glu_h + f0);
-          ptx::tma_load_2d(sst, &tmS, &full[stage], 0, base + f0);
-          ptx::tma_load_2d(sst + 16 * p.srow_bytes, &tmS, &full[stage], 0, base + p.glu_h + f0);
-        } else {
-          ptx::tma_load_3d(wst, &tmW, &full[stage], 0, 0, base + f0);
-          ptx::tma_load_2d(sst, &tmS, &full[stage], 0, base + f0);
+        const bool skip = p.inject && first && blockIdx.x == 0;  // test hook: drop one stage
+        first = false;
+        if (!skip) {
+          uint8_t* wst = ring + (size_t)stage * p.stage_bytes;
+          uint8_t* sst = wst + kItemRows * p.row_bytes;
+          ptx::mbar_arrive_expect_tx(&full[stage], p.stage_bytes);
+          armed.arm(stage, phase);
+          const int base = tl.x * p.w_rows;  // first weight row of the expert
+          const int f0 = g.fb * p.feats_per_item;
+          if (GLU) {  // 16 gate rows, then the 16 matching up rows
+            ptx::tma_load_3d(wst, &tmW, &full[stage], 0, 0, base + f0);
+            ptx::tma_load_3d(wst + 16 * p.row_bytes, &tmW, &full[stage], 0, 0, base + p.glu_h + f0);
+            ptx::tma_load_2d(sst, &tmS, &full[stage], 0, base + f0);
+            ptx::tma_load_2d(sst + 16 * p.srow_bytes, &tmS, &full[stage], 0, base + p.glu_h + f0);
+          } else {
+            ptx::tma_load_3d(wst, &tmW, &full[stage], 0, 0, base + f0);
+            ptx::tma_load_2d(sst, &tmS, &full[stage], 0, base + f0);
+          }
         }
         if (++stage == p.stages) {
           stage = 0;
           phase ^= 1u;
         }
       }
+      // the CTA stays resident until its loads have landed (after an abort some were not
+      // consumed; in a normal run every armed stage has already completed)
+      ptx::drain_armed(full, armed, p.timeout_ns);
     }
   } else {
     // ------------------------------------------------------------------ compute warps
@@ -426,7 +437,8 @@ bool make_map_scale_rows(CUtensorMap* m, const void* ptr, int64_t rows_total, in
 
 }  // namespace
 
-cudaError_t launch_gemv_fp4(const TcSwap& g, uint32_t* status, uint64_t timeout_ns, int num_sms, cudaStream_t s) {
+cudaError_t launch_gemv_fp4(const TcSwap& g, uint32_t* status, uint64_t timeout_ns, int num_sms, cudaStream_t s,
+                            int inject) {
   const bool glu = g.epi == kEpiGluF16;
   if (!g.w_scale || (g.epi != kEpiGluF16 && g.epi != kEpiScaleF16)) return cudaErrorInvalidValue;
   if (g.K % 512 || g.K > kMaxChunks * 32 || g.ldc <= 0) return cudaErrorInvalidValue;
@@ -453,6 +465,7 @@ cudaError_t launch_gemv_fp4(const TcSwap& g, uint32_t* status, uint64_t timeout_
   p.row_scale = g.row_scale;
   p.status = status;
   p.timeout_ns = timeout_ns;
+  p.inject = inject;
   const int64_t rows_total = g.w.depth * g.w.rows;
   CUtensorMap mw, ms;
   if (!make_map_weight_rows(&mw, g.w.ptr, rows_total, p.row_bytes, glu ? kItemRows / 2 : kItemRows) ||

@@ -54,13 +54,16 @@ struct RouterSrc {
 // fp32 CUDA-core GEMM): measured errors are below 1e-4 at d = 7168 (tested).
 constexpr float kRouterLogitMargin = 1e-3f;
 // s = sigmoid(logits), key = s + b, top-k by (key desc, index asc), p = s / sum(s over T_k);
-// membership at the k-th/(k+1)-th boundary is decided on exact fp64 keys when the
-// approximate keys are within the margin.
-// Two kernels: a selection pass that appends tokens with an uncertain boundary to
-// refine_list[T] (count in *refine_count, reset here), and a refinement pass over that list.
+// wherever two keys that decide the selected set or the rank order are within the key
+// uncertainty the margin implies, they are compared as exact fp64 keys.
+// Two kernels: a selection pass that appends tokens with an uncertain list to refine_list[T],
+// and a refinement pass over that list.  refine_count[0] is the list length and refine_count[1]
+// the number of near ties (exact k-th/(k+1)-th key gap below 1e-6); both are reset here.  A
+// recomputed logit further than margin/2 from the GEMM's sets kStatusDeviceCheck |
+// kStatusRouterMargin in *status (may be null).
 cudaError_t launch_topk(const float* logits, const float* bias, const RouterSrc& src, int T, int E, int k,
-                        int32_t* idx, float* p, int32_t* refine_list, int32_t* refine_count, int num_sms,
-                        cudaStream_t s);
+                        int32_t* idx, float* p, int32_t* refine_list, int32_t* refine_count, uint32_t* status,
+                        int num_sms, cudaStream_t s);
 // Deterministic expert batches: per-chunk counts, scan, stable (expert, token) rows, the
 // grouped-GEMM M-tile list, and per-row weights.  idx entries outside [0,E) are reported.
 struct DispatchBuffers {
@@ -74,6 +77,8 @@ struct DispatchBuffers {
   int4* tiles_p;          // [T*k/256 + E + 1]: 256-row tiles, same layout as `tiles` (or nullptr)
                           // (one load gives a work item everything: the tile count is ceil(rows / tile))
   int32_t* num_tiles_p;   // [1]
+  int4* tiles_m;          // [T*k/192 + E + 1]: 192-row tiles of the block-scaled kernel, same layout (or nullptr)
+  int32_t* num_tiles_m;   // [1]
   int32_t* tok_of_row;    // [T*k]
   int32_t* row_of;        // [T][k]
   float* p_row;           // [T*k]
@@ -155,8 +160,10 @@ cudaError_t launch_tc_gemm(const TcGemm& g, uint32_t* status, uint64_t timeout_n
 // The same GEMM on CTA pairs (gemm_pair.cu): 256 x 256 tiles, tcgen05.mma.cta_group::2.  Dense
 // (not grouped), bf16 operands, bf16, GLU or fp32 epilogue; tc_pair_supported says whether `g`
 // qualifies.
+// inject != 0 (test hook): the first pair skips its first ring stage, so that its MMA's bounded
+// wait runs out and reports a timeout.
 bool tc_pair_supported(const TcGemm& g);
-cudaError_t launch_tc_pair(const TcGemm& g, uint32_t* status, uint64_t timeout_ns, cudaStream_t s);
+cudaError_t launch_tc_pair(const TcGemm& g, uint32_t* status, uint64_t timeout_ns, cudaStream_t s, int inject = 0);
 
 // Swapped-operand grouped GEMM for experts with few rows (gemm_swap.cu): weights are the
 // 128-row M operand, the tile's token rows (up to 128) the N operand.
@@ -174,18 +181,48 @@ struct TcSwap {
   void* C; int64_t ldc;
   const float* row_scale;   // down: routing weight per row
 };
-cudaError_t launch_tc_swap(const TcSwap& g, uint32_t* status, uint64_t timeout_ns, int num_sms, cudaStream_t s);
+cudaError_t launch_tc_swap(const TcSwap& g, uint32_t* status, uint64_t timeout_ns, int num_sms, cudaStream_t s,
+                           int inject = 0);
 // MXFP4 routed experts for units of at most 4 rows on the CUDA cores (gemv_fp4.cu): the same
 // descriptor as launch_tc_swap (kEpiGluF16 or kEpiScaleF16, fp16 activations, K % 512 == 0,
 // K <= 4096); units with more rows are skipped (run launch_tc_swap with skip_rows_upto = 4).
 constexpr int kGemvMaxRows = 4;
-cudaError_t launch_gemv_fp4(const TcSwap& g, uint32_t* status, uint64_t timeout_ns, int num_sms, cudaStream_t s);
+cudaError_t launch_gemv_fp4(const TcSwap& g, uint32_t* status, uint64_t timeout_ns, int num_sms, cudaStream_t s,
+                            int inject = 0);
 
 // The same swapped-operand grouped GEMM on CTA pairs for experts with many rows
 // (gemm_pair_swap.cu): 256 weight rows x up to 256 token rows per tile, each expert's rows cut
 // into ceil(rows/256) equal token tiles (tiles_p: the dispatch's 256-row tile list).  bf16 only
 // (kEpiGluBF16 with glu_h % 128 == 0, or kEpiScaleBF16 with out_features % 256 == 0).
 cudaError_t launch_tc_pair_swap(const TcSwap& g, const int4* tiles_p, const int32_t* num_tiles_p, int max_tiles_p,
-                                uint32_t* status, uint64_t timeout_ns, cudaStream_t s);
+                                uint32_t* status, uint64_t timeout_ns, cudaStream_t s, int inject = 0);
+
+// ---------------------------------------------------------------- block-scaled MXFP4 experts
+// Three-term MXFP4 records of token rows (mx.cuh): rows of z in expert-contiguous order.  z
+// [T][K] fp16 or bf16 (K % 512 == 0); dst[row_of[t][j]] = record of z[t] for every (t, j) with
+// row_of[t][j] >= 0.  k <= 32.
+size_t scatter_mx3_smem_bytes(int K, int in_elem_bytes);
+cudaError_t launch_scatter_mx3(const void* src, int src_dtype, void* dst, const int32_t* row_of, int T, int k, int K,
+                               uint32_t* status, uint64_t timeout_ns, int num_sms, cudaStream_t s);
+// Grouped expert GEMM on tcgen05.mma.cta_group::2.kind::mxf4 (gemm_mx.cu): E2M1 weights with E8M0
+// scales per 32 along K against token records; 192-row token tiles (tiles_m from the dispatch).
+//   glu_h > 0: gate/up weights [E][2h][K] (out_features == glu_h, multiple of 512); C receives
+//              the records of SiLU(gate) * up ([rows][mx3_row_bytes(h)]).
+//   glu_h == 0: down weights [E][out_features][K]; C receives fp16 rows [rows][ldc], each scaled
+//              by row_scale[row].
+struct TcMx {
+  int K;                    // reduction width (multiple of 512)
+  int out_features;
+  int glu_h;
+  TcOperand w;              // [E][w_rows][K] in elements (packed E2M1 bytes)
+  const uint8_t* w_scale;   // E8M0 [E][w_rows][K/32]
+  const void* x;            // token records [rows][mx3_row_bytes(K)]
+  int64_t rows;             // rows of x
+  void* C;
+  int64_t ldc;              // down: fp16 elements per output row
+  const float* row_scale;
+};
+cudaError_t launch_tc_mx(const TcMx& g, const int4* tiles_m, const int32_t* num_tiles_m, int max_tiles_m,
+                         uint32_t* status, uint64_t timeout_ns, cudaStream_t s, int inject = 0);
 
 }  // namespace lmoe

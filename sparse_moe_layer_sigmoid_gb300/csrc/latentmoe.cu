@@ -27,16 +27,17 @@ struct lmoe_handle {
   uint32_t* status;
   float* logits;
   int32_t* refine_list;   // [T] tokens whose top-k boundary is settled exactly
-  int32_t* refine_count;
+  int32_t* refine_count;  // [2]: refined tokens, near ties of the last routing
   int32_t* idx;
   float* p;
   DispatchBuffers db;
   int max_tiles;
   int max_tiles_s;
   int max_tiles_p;
+  int max_tiles_m;
   void* z;
-  void* z_perm;  // gathered expert-contiguous rows; reused for the routed down output
-  void* a;       // routed GLU activations [T*k][h]
+  void* z_perm;  // gathered expert-contiguous rows (or their MXFP4 records); reused for the routed down output
+  void* a;       // routed GLU activations [T*k][h] (or their MXFP4 records)
   void* act_cat; // [T][N_s*h_s + l]: shared GLU activations | RMSNorm(u)
   void* x_stage; // forward_host staging
   void* y_stage;
@@ -103,7 +104,8 @@ lmoe_status validate_config(const lmoe_config& c) {
   if (c.router_w != LMOE_F32 && c.router_w != LMOE_BF16) return LMOE_ERR_INVALID_ARG;
   if (c.routed_w != LMOE_F32 && c.routed_w != LMOE_BF16 && c.routed_w != LMOE_MXFP4) return LMOE_ERR_INVALID_ARG;
   if (!(c.rms_eps >= 0.0f)) return LMOE_ERR_INVALID_ARG;
-  if (c.flags & ~(LMOE_FLAG_IDENTITY_EXPERTS | LMOE_FLAG_SINGLE_CTA_GEMM)) return LMOE_ERR_INVALID_ARG;
+  if (c.flags & ~(LMOE_FLAG_IDENTITY_EXPERTS | LMOE_FLAG_SINGLE_CTA_GEMM | LMOE_FLAG_MXFP4_DEQUANT))
+    return LMOE_ERR_INVALID_ARG;
   // router GEMM and the CUDA-core path step K by 16; combine moves 16-byte vectors
   if (c.d % 16 || c.latent % 16) return LMOE_ERR_UNSUPPORTED;
   if (c.act == LMOE_F32) {
@@ -143,7 +145,7 @@ size_t layout(lmoe_handle* h, uint8_t* base) {
   h->status = reinterpret_cast<uint32_t*>(take(sizeof(uint32_t)));
   h->logits = reinterpret_cast<float*>(take(T * E * 4));
   h->refine_list = reinterpret_cast<int32_t*>(take(T * 4));
-  h->refine_count = reinterpret_cast<int32_t*>(take(4));
+  h->refine_count = reinterpret_cast<int32_t*>(take(8));
   h->idx = reinterpret_cast<int32_t*>(take(rows * 4));
   h->p = reinterpret_cast<float*>(take(rows * 4));
   h->db.chunk_counts = reinterpret_cast<int32_t*>(take(nchunks * E * 4));
@@ -157,6 +159,9 @@ size_t layout(lmoe_handle* h, uint8_t* base) {
   h->max_tiles_p = (int)(rows / kTileP + E + 1);
   h->db.tiles_p = reinterpret_cast<int4*>(take((size_t)h->max_tiles_p * 16));
   h->db.num_tiles_p = reinterpret_cast<int32_t*>(take(4));
+  h->max_tiles_m = (int)(rows / kTileMx + E + 1);
+  h->db.tiles_m = reinterpret_cast<int4*>(take((size_t)h->max_tiles_m * 16));
+  h->db.num_tiles_m = reinterpret_cast<int32_t*>(take(4));
   h->db.tok_of_row = reinterpret_cast<int32_t*>(take(rows * 4));
   h->db.row_of = reinterpret_cast<int32_t*>(take(rows * 4));
   h->db.p_row = reinterpret_cast<float*>(take(rows * 4));
@@ -221,7 +226,7 @@ lmoe_status run_routing(lmoe_handle* h, const void* x, int T, const lmoe_weights
     stage_end(h, kStRouter, s);
     const RouterSrc rs{x, c.act, w->w_router, c.router_w, c.d, kRouterLogitMargin};
     LMOE_TRY(launch_topk(h->logits, w->router_bias, rs, T, c.num_experts, c.top_k, h->idx, h->p, h->refine_list,
-                         h->refine_count, h->num_sms, s));
+                         h->refine_count, h->status, h->num_sms, s));
     stage_end(h, kStTopk, s);
     h->last_launches += 2;
     idx = h->idx;
@@ -239,10 +244,10 @@ lmoe_status run_routing(lmoe_handle* h, const void* x, int T, const lmoe_weights
 // tiles), everything else on single CTAs (128-row tiles; dense ones with at most half as many
 // output tiles as SMs split K).  Adds its launches to *launches.
 cudaError_t run_tc_gemm(lmoe_handle* h, TcGemm g, int inject, int* launches, cudaStream_t s) {
-  const bool pair = !(h->cfg.flags & LMOE_FLAG_SINGLE_CTA_GEMM) && !inject && g.M >= kTileP && tc_pair_supported(g);
+  const bool pair = !(h->cfg.flags & LMOE_FLAG_SINGLE_CTA_GEMM) && g.M >= kTileP && tc_pair_supported(g);
   if (pair) {
     *launches += 1;
-    return launch_tc_pair(g, h->status, h->timeout_ns, s);
+    return launch_tc_pair(g, h->status, h->timeout_ns, s, inject);
   }
   // dense GEMMs of at most 128 rows may split K over the SMs (decode batches)
   if (!g.tiles) {
@@ -267,6 +272,10 @@ lmoe_status run_forward(lmoe_handle* h, const void* x, int T, const lmoe_weights
   h->last_T = T;
   stages_start(h, s);
 
+  // test hook (latentmoe_set_wait_limit): drop one pipeline signal in the first routed GEMM (1)
+  // or in the W_down GEMM (2) of this call
+  const int inject_routed = h->inject == 1 ? 1 : 0, inject_wdown = h->inject == 2 ? 1 : 0;
+  h->inject = 0;
   const int32_t* idx;
   const float* p;
   lmoe_status st = run_routing(h, x, T, w, ext_idx, ext_p, &idx, &p, s);
@@ -283,7 +292,7 @@ lmoe_status run_forward(lmoe_handle* h, const void* x, int T, const lmoe_weights
     g.B0 = op2d(w->w_down_proj, l, d);
     g.k0_len = d; g.k0_per_group = d;
     g.C = h->z; g.ldc = l;
-    LMOE_TRY(run_tc_gemm(h, g, 0, &h->last_launches, s));
+    LMOE_TRY(run_tc_gemm(h, g, inject_wdown, &h->last_launches, s));
   } else {
     SimtGemm g = {};
     g.A = x; g.lda = d; g.a_dtype = c.act; g.b_dtype = c.act;
@@ -294,9 +303,16 @@ lmoe_status run_forward(lmoe_handle* h, const void* x, int T, const lmoe_weights
     h->last_launches += 1;
   }
   stage_end(h, kStWDown, s);
-  // rows of z into expert-contiguous order
-  LMOE_TRY(launch_scatter_rows(h->z, h->z_perm, h->db.row_of, T, k, l, (int)ab, h->status, h->timeout_ns,
-                               h->num_sms, s));
+  // MXFP4 experts on the block-scaled MMA (CTA pairs): gathered rows and GLU activations as
+  // three-term MXFP4 records (each no larger than the 16-bit row it replaces), expert outputs fp16
+  const bool mx = tc && !identity && c.routed_w == LMOE_MXFP4 &&
+                  !(c.flags & (LMOE_FLAG_MXFP4_DEQUANT | LMOE_FLAG_SINGLE_CTA_GEMM));
+  // rows of z into expert-contiguous order (as MXFP4 records for the block-scaled expert GEMMs)
+  if (mx)
+    LMOE_TRY(launch_scatter_mx3(h->z, rt, h->z_perm, h->db.row_of, T, k, l, h->status, h->timeout_ns, h->num_sms, s));
+  else
+    LMOE_TRY(launch_scatter_rows(h->z, h->z_perm, h->db.row_of, T, k, l, (int)ab, h->status, h->timeout_ns,
+                                 h->num_sms, s));
   stage_end(h, kStScatter, s);
   h->last_launches += 1;
 
@@ -315,8 +331,28 @@ lmoe_status run_forward(lmoe_handle* h, const void* x, int T, const lmoe_weights
   const bool swap = tc && (int64_t)T * k <= 32LL * c.num_experts;
   // many rows per expert, bf16 experts: swapped operands on CTA pairs (token tiles cut to fit)
   const bool pair_swap = tc && !swap && c.routed_w == LMOE_BF16 && !(c.flags & LMOE_FLAG_SINGLE_CTA_GEMM) &&
-                         !h->inject && hdim % 128 == 0 && l % 256 == 0;
-  if (pair_swap) {
+                         hdim % 128 == 0 && l % 256 == 0;
+  if (mx) {
+    TcMx g = {};
+    g.K = l; g.out_features = hdim; g.glu_h = hdim;
+    g.w = op3d(w->routed_gate_up, c.num_experts, 2 * hdim, l);
+    g.w_scale = w->routed_gate_up_scale;
+    g.x = h->z_perm; g.rows = rows;
+    g.C = h->a;
+    LMOE_TRY(launch_tc_mx(g, h->db.tiles_m, h->db.num_tiles_m, h->max_tiles_m, h->status, h->timeout_ns, s,
+                          inject_routed));
+    stage_end(h, kStGlu, s);
+
+    TcMx dn = {};
+    dn.K = hdim; dn.out_features = l; dn.glu_h = 0;
+    dn.w = op3d(w->routed_down, c.num_experts, l, hdim);
+    dn.w_scale = w->routed_down_scale;
+    dn.x = h->a; dn.rows = rows;
+    dn.C = o; dn.ldc = l; dn.row_scale = h->db.p_row;
+    LMOE_TRY(launch_tc_mx(dn, h->db.tiles_m, h->db.num_tiles_m, h->max_tiles_m, h->status, h->timeout_ns, s));
+    stage_end(h, kStDown, s);
+    h->last_launches += 2;
+  } else if (pair_swap) {
     TcSwap g = {};
     g.epi = kEpiGluBF16;
     g.K = l; g.out_features = hdim; g.glu_h = hdim;
@@ -324,7 +360,7 @@ lmoe_status run_forward(lmoe_handle* h, const void* x, int T, const lmoe_weights
     g.w = op3d(w->routed_gate_up, c.num_experts, 2 * hdim, l);
     g.C = h->a; g.ldc = hdim;
     LMOE_TRY(launch_tc_pair_swap(g, h->db.tiles_p, h->db.num_tiles_p, h->max_tiles_p, h->status,
-                                 h->timeout_ns, s));
+                                 h->timeout_ns, s, inject_routed));
     stage_end(h, kStGlu, s);
 
     TcSwap dn = {};
@@ -351,8 +387,8 @@ lmoe_status run_forward(lmoe_handle* h, const void* x, int T, const lmoe_weights
     // MXFP4: units of at most kGemvMaxRows rows stream their weights through the CUDA cores,
     // larger ones go to the tensor cores
     g.skip_rows_upto = fp4 ? kGemvMaxRows : 0;
-    if (fp4) LMOE_TRY(launch_gemv_fp4(g, h->status, h->timeout_ns, h->num_sms, s));
-    LMOE_TRY(launch_tc_swap(g, h->status, h->timeout_ns, h->num_sms, s));
+    if (fp4) LMOE_TRY(launch_gemv_fp4(g, h->status, h->timeout_ns, h->num_sms, s, inject_routed));
+    LMOE_TRY(launch_tc_swap(g, h->status, h->timeout_ns, h->num_sms, s, inject_routed));
     stage_end(h, kStGlu, s);
 
     TcSwap dn = {};
@@ -381,8 +417,7 @@ lmoe_status run_forward(lmoe_handle* h, const void* x, int T, const lmoe_weights
     g.k0_len = l; g.k0_per_group = l; g.glu_h = hdim;
     g.tiles = h->db.tiles; g.num_tiles = h->db.num_tiles; g.offsets = h->db.offsets; g.max_tiles = h->max_tiles;
     g.C = h->a; g.ldc = hdim;
-    LMOE_TRY(run_tc_gemm(h, g, h->inject, &h->last_launches, s));
-    h->inject = 0;
+    LMOE_TRY(run_tc_gemm(h, g, inject_routed, &h->last_launches, s));
     stage_end(h, kStGlu, s);
 
     TcGemm dn = {};
@@ -646,8 +681,9 @@ size_t latentmoe_workspace_bytes(const lmoe_handle* h) { return h ? h->ws_bytes 
 
 lmoe_status latentmoe_set_wait_limit(lmoe_handle* h, uint64_t timeout_ns, int32_t inject) {
   if (!h || timeout_ns == 0) return LMOE_ERR_INVALID_ARG;
+  if (inject < 0 || inject > 2) return LMOE_ERR_INVALID_ARG;
   h->timeout_ns = timeout_ns;
-  h->inject = inject ? 1 : 0;
+  h->inject = inject;
   return LMOE_OK;
 }
 
@@ -679,6 +715,7 @@ lmoe_status latentmoe_debug_buffer(const lmoe_handle* h, const char* name, void*
   else if (!strcmp(name, "act")) { p = h->a; n = T * k * (size_t)c.hidden * ab; }
   else if (!strcmp(name, "act_cat")) { p = h->act_cat; n = T * kcat * ab; }
   else if (!strcmp(name, "p_row")) { p = h->db.p_row; n = T * k * 4; }
+  else if (!strcmp(name, "refine_count")) { p = h->refine_count; n = 2 * sizeof(int32_t); }
   if (!p) return LMOE_ERR_INVALID_ARG;
   *ptr = p;
   *bytes = n;

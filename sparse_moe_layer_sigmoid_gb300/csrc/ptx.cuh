@@ -63,6 +63,32 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   }
 }
 
+// ---------------------------------------------------------------- teardown after an abort
+// A CTA whose bounded wait gave up must not exit (or free TMEM) while its own asynchronous work
+// still runs: TMA loads writing its shared memory, or MMAs reading shared memory and writing
+// TMEM.  The producer records every ring stage it armed (arrive.expect_tx, then loads) with the
+// phase parity of that use; drain_armed waits, bounded, until the last load of each armed stage
+// has landed.  Each phase of a stage's `full` barrier is completed by exactly one armed use and
+// the producer arms a stage again only after its previous use was consumed, so the barrier is
+// either in the recorded phase or just past it: waiting on the recorded parity always ends.
+struct ArmedStages {
+  uint32_t mask = 0, parity = 0;
+  __device__ __forceinline__ void arm(int s, uint32_t ph) {
+    mask |= 1u << s;
+    parity = (parity & ~(1u << s)) | ((ph & 1u) << s);
+  }
+};
+__device__ __forceinline__ void drain_armed(uint64_t* full, const ArmedStages& a, uint64_t timeout_ns) {
+  const uint64_t t0 = globaltimer_ns();
+#pragma unroll 1
+  for (int s = 0; s < 32; ++s)
+    if ((a.mask >> s) & 1u) {
+      const uint32_t bar = smem_addr(&full[s]);
+      while (!mbar_try_wait(bar, (a.parity >> s) & 1u) && globaltimer_ns() - t0 < timeout_ns) {
+      }
+    }
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
@@ -124,6 +150,14 @@ __device__ __forceinline__ void tma_load_3d_pair(void* dst, const CUtensorMap* m
       "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_addr(dst)),
       "l"(reinterpret_cast<uint64_t>(m)), "r"(bar_cluster), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* m, uint32_t bar_cluster, int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar_cluster), "r"(c0), "r"(c1)
       : "memory");
 }
 
@@ -200,6 +234,16 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
                : "memory");
 }
 
+// The MMA issuer's teardown after an abort: a commit on `bar` (a barrier of count 1 used for
+// nothing else) arrives once every MMA this thread issued has completed; wait for it, bounded.
+__device__ __forceinline__ void drain_mma(uint64_t* bar, uint64_t timeout_ns) {
+  mma_commit(bar);
+  const uint32_t a = smem_addr(bar);
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(a, 0) && globaltimer_ns() - t0 < timeout_ns) {
+  }
+}
+
 // ---------------------------------------------------------------- tcgen05, CTA pair
 // The cta_group::2 forms: both CTAs of the pair allocate (one warp each, same columns), the
 // even CTA issues MMAs of M = 256 whose A rows and B columns are split between the two CTAs'
@@ -228,6 +272,59 @@ __device__ __forceinline__ void mma_commit_pair(uint64_t* bar) {
                    smem_addr(bar))
                : "memory");
 }
+// drain_mma for the pair MMAs of the even CTA.
+__device__ __forceinline__ void drain_mma_pair(uint64_t* bar, uint64_t timeout_ns) {
+  mma_commit_pair(bar);
+  const uint32_t a = smem_addr(bar);
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(a, 0) && globaltimer_ns() - t0 < timeout_ns) {
+  }
+}
+
+// ---------------------------------------------------------------- block-scaled MMA (kind::mxf4)
+// D[tmem] (+)= (A * 2^sfa) * (B * 2^sfb)^T with A, B packed E2M1 (K = 64 per instruction: 32
+// bytes of each K-major row) and one E8M0 scale per 32 elements along K, read from TMEM: for A
+// row m, lane m and column sfa_tmem + m/32; for B row n, lane n % 32 of the reading lane quadrant
+// and column sfb_tmem + n/32 (so B scales are replicated in all four quadrants); within the
+// 32-bit cell, byte sf_id holds the scale of K elements 0..31 and byte sf_id + 1 that of 32..63
+// (sf_id 0 or 2, set in the instruction descriptor).  CTA pair: the even CTA issues; each CTA's
+// TMEM holds the scales of its own A rows and of every B row.
+__device__ __forceinline__ void mma_mxf4_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                              uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+// Instruction descriptor for kind::mxf4: E2M1 A and B (format code 1), E8M0 scales, both
+// K-major, M x N, scale bytes selected by a_sf / b_sf.
+__host__ __device__ constexpr uint32_t idesc_mxf4(int M, int N, uint32_t a_sf, uint32_t b_sf) {
+  return (b_sf << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | (1u << 23) |
+         ((uint32_t)(M >> 4) << 24) | (a_sf << 29);
+}
+// Arrive once on the barrier at `bar`'s offset in both CTAs of the pair when all previously
+// issued pair MMAs of this thread complete.
+__device__ __forceinline__ void mma_commit_pair_both(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_addr(bar)),
+      "h"((uint16_t)3)
+      : "memory");
+}
+// Registers -> TMEM: thread i of the warp writes lane (taddr.lane + i), 1 or 8 consecutive
+// 32-bit columns from taddr's column.  A warp may write only its own lane quadrant.
+__device__ __forceinline__ void tmem_st_32x32b_x1(uint32_t taddr, uint32_t v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
+}
+__device__ __forceinline__ void tmem_st_32x32b_x8(uint32_t taddr, const uint32_t (&v)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+               "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // 32 lanes x 32 consecutive 32-bit columns: thread i receives lane (taddr.lane + i).
 __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {

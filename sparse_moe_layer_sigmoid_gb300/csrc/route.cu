@@ -132,12 +132,14 @@ __device__ void exact_logit_parts(const RouterSrc& r, int t, const int (&ce)[kCa
 // 32-entry scratch arrays private to the warp.
 //
 // The logits come from a GEMM whose error is bounded by `src.margin`, so a key is known to
-// within eta = margin/4 (+ fp32 rounding).  When the k-th and (k+1)-th keys are closer than
-// 2*eta the selected set is not certain: every expert whose key lies in the band around the
-// boundary has its logit recomputed to ~44 bits and its key evaluated in fp64, and the open
-// slots are filled from those keys (ties to the lower index).  Experts above the band are in
-// for certain, experts below it out.  The output lists the certain experts in descending key
-// order, then the refined winners in descending exact-key order.
+// within eta = margin/4 (+ fp32 rounding), and two keys further apart than 2*eta are ordered
+// correctly.  A token is settled exactly (second pass) when the order of its list is not certain:
+// when the k-th and (k+1)-th keys are closer than 2*eta (the selected set itself), or when two
+// neighbouring ranks are (the rank order).  There every expert whose key lies in the band around
+// an uncertain boundary, and every selected expert with a neighbour closer than 2*eta, has its
+// logit recomputed to ~44 bits and its key evaluated in fp64; the k winners are then the
+// contenders (the selected experts and the band) in descending order of their keys, exact where
+// recomputed, else the fp32 key (which is at least 2*eta away from every other contender's).
 template <int NPL>
 struct TopkState {
   float kf[NPL], sv[NPL];  // keys and scores of this lane's experts
@@ -286,7 +288,10 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ log
   if (t >= T) return;
   TopkState<NPL> st;
   topk_pass<NPL>(logits, bias, t, E, k, lane, st, s_sk[warp], s_ss[warp]);
-  if (k < E && st.a_k - st.a_k1 < 2.0f * key_eta(src)) {
+  const float eta2 = 2.0f * key_eta(src);
+  const float next = __shfl_down_sync(0xffffffffu, st.my_kf, 1);
+  const bool close = lane + 1 < k && st.my_kf - next < eta2;  // rank order of lanes j, j+1 uncertain
+  if ((k < E && st.a_k - st.a_k1 < eta2) || __any_sync(0xffffffffu, close)) {
     // the ranked list stays in idx for the refinement, which rewrites idx and p
     if (lane < k) idx[(size_t)t * k + lane] = st.my_e;
     if (lane == 0) refine_list[atomicAdd(refine_count, 1)] = t;  // list order is irrelevant: tokens are independent
@@ -315,26 +320,39 @@ __device__ __forceinline__ void group_sync() {
     __syncthreads();
 }
 
-// Exact fp64 key -> unsigned integer of the same order (0 stays below every key).
+// fp64 key -> unsigned integer of the same order (0 stays below every key), and back.
 __device__ __forceinline__ uint64_t orderable64(double d) {
   const uint64_t u = (uint64_t)__double_as_longlong(d);
   return (u >> 63) ? ~u : (u | 0x8000000000000000ull);
 }
 
-// Settle the selection of token t exactly: G warps (gw = 0..G-1) cooperate.  Warp 0 of the group
-// takes pass 1's ranked list from idx (recomputing its keys and the (k+1)-th key) and lists the
-// experts in the band around the boundary (rounds of at most kMaxCand); the G warps recompute
-// their logits to ~44 bits, warp gw over the 256-element blocks gw, gw + G, ... of d, and warp 0
-// sums the G partials in a fixed order, takes fp64 keys and fills the open ranks.
+__device__ __forceinline__ double from_orderable64(uint64_t u) {
+  return __longlong_as_double((long long)((u >> 63) ? (u & 0x7FFFFFFFFFFFFFFFull) : ~u));
+}
+
+// Gap between the k-th and (k+1)-th keys below which a token is a near tie (its selected set may
+// differ from the fp64 evaluation's; such tokens are counted).
+constexpr double kNearTieGap = 1e-6;
+
+// Settle the list of token t exactly: G warps (gw = 0..G-1) cooperate.  Warp 0 of the group takes
+// pass 1's ranked list from idx (recomputing its keys and the (k+1)-th key), marks the experts
+// whose order is uncertain (the band around an uncertain boundary; selected experts with a
+// neighbouring rank closer than the key uncertainty) and lists them in rounds of at most
+// kMaxCand; the G warps recompute their logits to ~44 bits, warp gw over the 256-element blocks
+// gw, gw + G, ... of d, and warp 0 sums the G partials in a fixed order, takes fp64 keys, checks
+// each recomputed logit against the GEMM's (an error above half the margin is reported) and
+// ranks the contenders.  A token whose exact k-th and (k+1)-th keys differ by less than
+// kNearTieGap is counted in *near_ties.
 template <int NPL, int G>
 __device__ __forceinline__ void refine_token(const float* __restrict__ logits, const float* __restrict__ bias,
                                              const RouterSrc& src, int t, int E, int k, int32_t* __restrict__ idx,
-                                             float* __restrict__ p, int gw, int lane, const RefineSmem& sm) {
+                                             float* __restrict__ p, int gw, int lane, const RefineSmem& sm,
+                                             uint32_t* status, int32_t* near_ties) {
   const uint32_t lt_mask = (1u << lane) - 1u;
   TopkState<NPL> st;
-  uint64_t ex[NPL];   // orderable exact keys of this lane's refined experts (0: not refined or taken)
-  uint32_t pend = 0;  // bit i: this lane's expert lane + 32 i is in the band and not yet refined
-  int n_cert = 0;
+  uint64_t ex[NPL];    // sort keys of this lane's contenders (orderable; 0: not a contender)
+  uint32_t pend = 0;   // bit i: expert lane + 32 i awaits recomputation
+  uint32_t exact = 0;  // bit i: ex[i] is the exact key
   if (gw == 0) {
     topk_keys<NPL>(logits, bias, t, E, lane, st);
     st.my_e = lane < k ? idx[(size_t)t * k + lane] : 0;
@@ -355,15 +373,33 @@ __device__ __forceinline__ void refine_token(const float* __restrict__ logits, c
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) below = fmaxf(below, __shfl_xor_sync(0xffffffffu, below, off));
     st.a_k1 = n_ge > k ? st.a_k : below;
-    const float eta = key_eta(src);
-    const float hi = st.a_k + 2.0f * eta, lo = st.a_k1 - 2.0f * eta;
-    n_cert = __popc(__ballot_sync(0xffffffffu, lane < k && st.my_kf > hi));  // ranks 0..n_cert-1
-#pragma unroll
-    for (int i = 0; i < NPL; ++i) {
-      ex[i] = 0;
-      const int e = lane + 32 * i;
-      if (e < E && st.kf[i] >= lo && st.kf[i] <= hi) pend |= 1u << i;
+    const float eta2 = 2.0f * key_eta(src);
+    const bool uncertain = k < E && st.a_k - st.a_k1 < eta2;
+    // ranks whose order against a neighbouring rank (or, for the last, against the experts below
+    // an uncertain boundary) is not certain
+    const float prev = __shfl_up_sync(0xffffffffu, st.my_kf, 1);
+    const float next = __shfl_down_sync(0xffffffffu, st.my_kf, 1);
+    const int close = lane < k && ((lane > 0 && prev - st.my_kf < eta2) || (lane + 1 < k && st.my_kf - next < eta2) ||
+                                   (lane == k - 1 && uncertain));
+    uint32_t sel = 0;
+    for (int j = 0; j < k; ++j) {
+      const int e = __shfl_sync(0xffffffffu, st.my_e, j);
+      const int c = __shfl_sync(0xffffffffu, close, j);
+      if ((e & 31) == lane) {
+        sel |= 1u << (e >> 5);
+        if (c) pend |= 1u << (e >> 5);
+      }
     }
+    if (uncertain) {  // the band: every expert that may cross the boundary
+      const float hi = st.a_k + eta2, lo = st.a_k1 - eta2;
+#pragma unroll
+      for (int i = 0; i < NPL; ++i) {
+        const int e = lane + 32 * i;
+        if (e < E && st.kf[i] >= lo && st.kf[i] <= hi) pend |= 1u << i;
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < NPL; ++i) ex[i] = ((sel | pend) >> i) & 1u ? orderable64((double)st.kf[i]) : 0ull;
   }
   while (true) {
     int pos[NPL];
@@ -406,8 +442,13 @@ __device__ __forceinline__ void refine_token(const float* __restrict__ logits, c
         DF a{sm.part[c].x, sm.part[c].y};
 #pragma unroll
         for (int q = 1; q < G; ++q) a = df_add(a, DF{sm.part[q * kMaxCand + c].x, sm.part[q * kMaxCand + c].y});
-        const double s64 = 1.0 / (1.0 + exp(-((double)a.hi + (double)a.lo)));
-        sm.key[c] = s64 + (bias ? (double)bias[sm.cand[c]] : 0.0);
+        const int e = sm.cand[c];
+        const double l64 = (double)a.hi + (double)a.lo;
+        // the margin the selection relies on, checked on every logit recomputed here
+        if (fabs((double)logits[(size_t)t * E + e] - l64) > 0.5 * (double)src.margin)
+          report(status, kStatusDeviceCheck | kStatusRouterMargin);
+        const double s64 = 1.0 / (1.0 + exp(-l64));
+        sm.key[c] = s64 + (bias ? (double)bias[e] : 0.0);
         sm.s[c] = (float)s64;
       }
       __syncwarp();
@@ -416,12 +457,17 @@ __device__ __forceinline__ void refine_token(const float* __restrict__ logits, c
         if (pos[i] >= 0) {
           ex[i] = orderable64(sm.key[pos[i]]);
           st.sv[i] = sm.s[pos[i]];
+          exact |= 1u << i;
         }
     }
     group_sync<G>();  // cand, part and key are rewritten by the next round
   }
   if (gw == 0) {
-    for (int q = n_cert; q < k; ++q) {
+    // ranks 0..k-1 by (key descending, index ascending); round k finds the (k+1)-th contender,
+    // for the near-tie count only
+    uint64_t key_k = 0;
+    int exact_k = 0;
+    for (int q = 0; q <= k; ++q) {
       uint64_t bv = 0;
       int be = 0x7FFFFFFF;
 #pragma unroll
@@ -441,20 +487,30 @@ __device__ __forceinline__ void refine_token(const float* __restrict__ logits, c
           be = oe;
         }
       }
+      if (bv == 0) break;  // no contender left (round k only: the k selected experts contend)
       const int owner = be & 31, slot = be >> 5;
       float s_here = 0.f;
+      int x_here = 0;
       if (lane == owner) {
 #pragma unroll
         for (int i = 0; i < NPL; ++i)
           if (i == slot) {
             s_here = st.sv[i];
+            x_here = (exact >> i) & 1u;
             ex[i] = 0;
           }
       }
       const float s_win = __shfl_sync(0xffffffffu, s_here, owner);
-      if (lane == q) {
-        st.my_e = be;
-        st.my_s = s_win;
+      const int x_win = __shfl_sync(0xffffffffu, x_here, owner);
+      if (q < k) {
+        if (lane == q) {
+          st.my_e = be;
+          st.my_s = s_win;
+        }
+        key_k = bv;
+        exact_k = x_win;
+      } else if (exact_k && x_win && lane == 0 && from_orderable64(key_k) - from_orderable64(bv) < kNearTieGap) {
+        atomicAdd(near_ties, 1);
       }
     }
     topk_write(t, k, st.my_e, st.my_s, idx, p, lane);
@@ -464,27 +520,30 @@ __device__ __forceinline__ void refine_token(const float* __restrict__ logits, c
 
 // Pass 2: the listed tokens.  With enough of them to keep every warp busy for several tokens,
 // each warp settles its own tokens; otherwise the 4 warps of a CTA split d for one token at a
-// time (short lists: decode and most prefill batches).
+// time (short lists: decode and most prefill batches).  refine_count[0] is the list length,
+// refine_count[1] the near-tie counter.
 template <int NPL>
 __global__ void __launch_bounds__(32 * kRefineWarps) topk_refine_kernel(
     const float* __restrict__ logits, const float* __restrict__ bias, RouterSrc src, int E, int k,
     int32_t* __restrict__ idx, float* __restrict__ p, const int32_t* __restrict__ refine_list,
-    const int32_t* __restrict__ refine_count) {
+    int32_t* __restrict__ refine_count, uint32_t* status) {
   __shared__ int s_cand[kRefineWarps][kMaxCand];
   __shared__ float2 s_part[kRefineWarps][kMaxCand];
   __shared__ double s_key[kRefineWarps][kMaxCand];
   __shared__ float s_s[kRefineWarps][kMaxCand];
   __shared__ int s_n[kRefineWarps];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n = *refine_count;
+  const int n = refine_count[0];
+  int32_t* near_ties = refine_count + 1;
   if (n >= 4 * (int)gridDim.x * kRefineWarps) {  // at least 4 tokens per warp
     const RefineSmem sm{s_cand[warp], s_part[warp], s_key[warp], s_s[warp], &s_n[warp]};
     for (int w = blockIdx.x * kRefineWarps + warp; w < n; w += gridDim.x * kRefineWarps)
-      refine_token<NPL, 1>(logits, bias, src, refine_list[w], E, k, idx, p, 0, lane, sm);
+      refine_token<NPL, 1>(logits, bias, src, refine_list[w], E, k, idx, p, 0, lane, sm, status, near_ties);
   } else {
     const RefineSmem sm{s_cand[0], &s_part[0][0], s_key[0], s_s[0], &s_n[0]};
     for (int w = blockIdx.x; w < n; w += gridDim.x)
-      refine_token<NPL, kRefineWarps>(logits, bias, src, refine_list[w], E, k, idx, p, warp, lane, sm);
+      refine_token<NPL, kRefineWarps>(logits, bias, src, refine_list[w], E, k, idx, p, warp, lane, sm, status,
+                                      near_ties);
   }
 }
 
@@ -546,11 +605,14 @@ __global__ void __launch_bounds__(1024) dispatch_scan_kernel(const int32_t* __re
                                                              int4* __restrict__ tiles_s,
                                                              int32_t* __restrict__ num_tiles_s,
                                                              int4* __restrict__ tiles_p,
-                                                             int32_t* __restrict__ num_tiles_p) {
+                                                             int32_t* __restrict__ num_tiles_p,
+                                                             int4* __restrict__ tiles_m,
+                                                             int32_t* __restrict__ num_tiles_m) {
   __shared__ int s_cnt[1024];
   __shared__ int s_tiles[1024];
   __shared__ int s_tiles_s[1024];
   __shared__ int s_tiles_p[1024];
+  __shared__ int s_tiles_m[1024];
   const int e = threadIdx.x;
   int total = 0;
   if (e < E)
@@ -558,10 +620,12 @@ __global__ void __launch_bounds__(1024) dispatch_scan_kernel(const int32_t* __re
   const int nt = (total + kTileM - 1) / kTileM;
   const int nts = (total + kTileS - 1) / kTileS;
   const int ntp = (total + kTileP - 1) / kTileP;
+  const int ntm = (total + kTileMx - 1) / kTileMx;
   s_cnt[e] = total;
   s_tiles[e] = nt;
   s_tiles_s[e] = nts;
   s_tiles_p[e] = ntp;
+  s_tiles_m[e] = ntm;
   __syncthreads();
   // Hillis-Steele inclusive scans over 1024 entries (fixed order, integer: exact).
   for (int off = 1; off < 1024; off <<= 1) {
@@ -569,17 +633,20 @@ __global__ void __launch_bounds__(1024) dispatch_scan_kernel(const int32_t* __re
     const int b = e >= off ? s_tiles[e - off] : 0;
     const int c = e >= off ? s_tiles_s[e - off] : 0;
     const int f = e >= off ? s_tiles_p[e - off] : 0;
+    const int m = e >= off ? s_tiles_m[e - off] : 0;
     __syncthreads();
     s_cnt[e] += a;
     s_tiles[e] += b;
     s_tiles_s[e] += c;
     s_tiles_p[e] += f;
+    s_tiles_m[e] += m;
     __syncthreads();
   }
   const int row0 = s_cnt[e] - total;
   const int tile0 = s_tiles[e] - nt;
   const int tile0s = s_tiles_s[e] - nts;
   const int tile0p = s_tiles_p[e] - ntp;
+  const int tile0m = s_tiles_m[e] - ntm;
   if (e < E) {
     offsets[e] = row0;
     int run = row0;
@@ -592,12 +659,15 @@ __global__ void __launch_bounds__(1024) dispatch_scan_kernel(const int32_t* __re
       for (int j = 0; j < nts; ++j) tiles_s[tile0s + j] = make_int4(e, row0 + kTileS * j, min(kTileS, total - kTileS * j), 0);
     if (tiles_p)
       for (int j = 0; j < ntp; ++j) tiles_p[tile0p + j] = make_int4(e, tile0p, total, row0);
+    if (tiles_m)
+      for (int j = 0; j < ntm; ++j) tiles_m[tile0m + j] = make_int4(e, tile0m, total, row0);
   }
   if (e == E - 1) {
     offsets[E] = s_cnt[e];
     *num_tiles = s_tiles[e];
     if (num_tiles_s) *num_tiles_s = s_tiles_s[e];
     if (num_tiles_p) *num_tiles_p = s_tiles_p[e];
+    if (num_tiles_m) *num_tiles_m = s_tiles_m[e];
   }
 }
 
@@ -754,9 +824,9 @@ cudaError_t launch_split_bf16x3(const float* w, int64_t n, void* out, cudaStream
 }
 
 cudaError_t launch_topk(const float* logits, const float* bias, const RouterSrc& src, int T, int E, int k,
-                        int32_t* idx, float* p, int32_t* refine_list, int32_t* refine_count, int num_sms,
-                        cudaStream_t s) {
-  cudaError_t e = cudaMemsetAsync(refine_count, 0, sizeof(int32_t), s);
+                        int32_t* idx, float* p, int32_t* refine_list, int32_t* refine_count, uint32_t* status,
+                        int num_sms, cudaStream_t s) {
+  cudaError_t e = cudaMemsetAsync(refine_count, 0, 2 * sizeof(int32_t), s);
   if (e != cudaSuccess) return e;
   const int warps_per_block = 8;
   dim3 grid((T + warps_per_block - 1) / warps_per_block), block(32 * warps_per_block);
@@ -765,7 +835,8 @@ cudaError_t launch_topk(const float* logits, const float* bias, const RouterSrc&
 #define LMOE_TOPK(N)                                                                                     \
   do {                                                                                                   \
     topk_kernel<N><<<grid, block, 0, s>>>(logits, bias, src, T, E, k, idx, p, refine_list, refine_count); \
-    topk_refine_kernel<N><<<rgrid, 128, 0, s>>>(logits, bias, src, E, k, idx, p, refine_list, refine_count); \
+    topk_refine_kernel<N><<<rgrid, 128, 0, s>>>(logits, bias, src, E, k, idx, p, refine_list, refine_count, \
+                                                 status);                                                         \
   } while (0)
   if (npl <= 1) LMOE_TOPK(1);
   else if (npl <= 2) LMOE_TOPK(2);
@@ -784,7 +855,8 @@ cudaError_t launch_dispatch(const int32_t* idx, const float* p, int T, int E, in
   const size_t smem = (size_t)E * kMaskWords * sizeof(uint32_t);
   dispatch_count_kernel<<<nchunks, kDispatchChunk, smem, s>>>(idx, T, E, k, b.chunk_counts, status);
   dispatch_scan_kernel<<<1, 1024, 0, s>>>(b.chunk_counts, nchunks, E, b.chunk_base, b.offsets, b.tiles,
-                                          b.num_tiles, b.tiles_s, b.num_tiles_s, b.tiles_p, b.num_tiles_p);
+                                          b.num_tiles, b.tiles_s, b.num_tiles_s, b.tiles_p, b.num_tiles_p,
+                                          b.tiles_m, b.num_tiles_m);
   dispatch_scatter_kernel<<<nchunks, kDispatchChunk, smem, s>>>(idx, p, T, E, k, b.chunk_base, b.tok_of_row,
                                                                 b.row_of, b.p_row);
   if (launches) *launches += 3;

@@ -11,8 +11,12 @@
 // Scratch: kScratchBytes in `g_route_scratch`, present on every GPU that loads the library
 // until the process exits.  All calls share it, so calls that overlap on the GPU (different
 // streams, or different host threads without ordering) race and must be serialised by the
-// caller.  The refinement-list counter is reset (cudaMemsetAsync, no allocation) at the start
-// of every call; every other scratch word a kernel reads is written earlier in the same call.
+// caller.  Its first 256 bytes hold a status word: errors the kernels detect (a bounded wait
+// that ran out, an out-of-range index, a router logit outside the error margin) are ORed into
+// it and stay there until latentmoe_route_noalloc_status() reads and clears it (the array
+// starts zeroed).  The refinement-list counters are reset (cudaMemsetAsync, no allocation) at
+// the start of every call; every other scratch word a kernel reads is written earlier in the
+// same call.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -35,14 +39,15 @@ void* g_scratch_addr[kMaxDevices] = {};
 size_t round256(size_t v) { return (v + 255) / 256 * 256; }
 
 struct ScratchLayout {
-  size_t logits, chunk_counts, chunk_base, tiles, num_tiles, refine_list, refine_count, wr_split, total;
+  size_t status, logits, chunk_counts, chunk_base, tiles, num_tiles, refine_list, refine_count, wr_split, total;
 };
 
 ScratchLayout scratch_layout(int T, int E, int k, size_t wr_split_bytes) {
   const size_t nchunks = ((size_t)T + lmoe::kDispatchChunk - 1) / lmoe::kDispatchChunk;
   const size_t max_tiles = (size_t)T * k / lmoe::kTileM + E + 1;
   ScratchLayout s;
-  s.logits = 0;
+  s.status = 0;  // sticky status word (uint32)
+  s.logits = 256;
   s.chunk_counts = s.logits + round256((size_t)T * E * sizeof(float));
   s.chunk_base = s.chunk_counts + round256(nchunks * E * sizeof(int32_t));
   s.tiles = s.chunk_base + round256(nchunks * E * sizeof(int32_t));
@@ -93,12 +98,14 @@ extern "C" lmoe_status latentmoe_route_noalloc(const lmoe_config* cfg, const voi
   const size_t wr_split_bytes = (cfg->act == LMOE_BF16 && cfg->router_w == LMOE_F32) ? (size_t)3 * E * d * 2 : 0;
   const ScratchLayout L = scratch_layout(T, E, k, wr_split_bytes);
   if (L.total > kScratchBytes) return LMOE_ERR_INVALID_ARG;  // beyond the fixed scratch
-  if (T == 0) return LMOE_OK;
 
+  // the set-up of this device (the array's address) happens here even for T == 0, so that a
+  // T == 0 call made at start-up does it ahead of any stream capture
   uint8_t* base = nullptr;
   lmoe_status st = scratch_for_current_device(&base);
-  if (st != LMOE_OK) return st;
+  if (st != LMOE_OK || T == 0) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint32_t* status = reinterpret_cast<uint32_t*>(base + L.status);
   float* logits = reinterpret_cast<float*>(base + L.logits);
   lmoe::DispatchBuffers db;
   db.chunk_counts = reinterpret_cast<int32_t*>(base + L.chunk_counts);
@@ -110,6 +117,8 @@ extern "C" lmoe_status latentmoe_route_noalloc(const lmoe_config* cfg, const voi
   db.num_tiles_s = nullptr;
   db.tiles_p = nullptr;
   db.num_tiles_p = nullptr;
+  db.tiles_m = nullptr;
+  db.num_tiles_m = nullptr;
   db.tok_of_row = tok_of_row;
   db.row_of = row_of;
   db.p_row = nullptr;
@@ -118,15 +127,31 @@ extern "C" lmoe_status latentmoe_route_noalloc(const lmoe_config* cfg, const voi
       cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return LMOE_ERR_CUDA;
   if (lmoe::launch_router(x, cfg->act, w->w_router, cfg->router_w, logits,
-                          wr_split_bytes ? base + L.wr_split : nullptr, T, E, d, nullptr, 4000000000ull, num_sms,
+                          wr_split_bytes ? base + L.wr_split : nullptr, T, E, d, status, 4000000000ull, num_sms,
                           nullptr, s) != cudaSuccess)
     return LMOE_ERR_CUDA;
   const lmoe::RouterSrc rs{x, cfg->act, w->w_router, cfg->router_w, d, lmoe::kRouterLogitMargin};
   if (lmoe::launch_topk(logits, w->router_bias, rs, T, E, k, topk_idx, topk_p,
                         reinterpret_cast<int32_t*>(base + L.refine_list),
-                        reinterpret_cast<int32_t*>(base + L.refine_count), num_sms, s) != cudaSuccess)
+                        reinterpret_cast<int32_t*>(base + L.refine_count), status, num_sms, s) != cudaSuccess)
     return LMOE_ERR_CUDA;
-  if (lmoe::launch_dispatch(topk_idx, topk_p, T, E, k, db, nullptr, nullptr, s) != cudaSuccess)
+  if (lmoe::launch_dispatch(topk_idx, topk_p, T, E, k, db, status, nullptr, s) != cudaSuccess)
     return LMOE_ERR_CUDA;
+  return LMOE_OK;
+}
+
+// Reads and clears the status word the no-allocation route's kernels report into, after
+// `stream` has finished; allocates nothing either.
+extern "C" lmoe_status latentmoe_route_noalloc_status(void* stream) {
+  uint8_t* base = nullptr;
+  lmoe_status st = scratch_for_current_device(&base);
+  if (st != LMOE_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint32_t word = 0;
+  if (cudaMemcpyAsync(&word, base, sizeof(word), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaMemsetAsync(base, 0, sizeof(word), s) != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess)
+    return LMOE_ERR_CUDA;
+  if (word & lmoe::kStatusTimeout) return LMOE_ERR_TIMEOUT;
+  if (word & lmoe::kStatusDeviceCheck) return LMOE_ERR_DEVICE_CHECK;
   return LMOE_OK;
 }
