@@ -45,44 +45,66 @@ namespace {
 
 using namespace tc;
 constexpr int kWRows = 128;                              // weight rows per CTA (M = 256 per pair)
-constexpr int kMaxN = 192;                               // token columns per tile (MMA N)
-constexpr int kXRows = kMaxN / 2;                        // token rows per CTA
 constexpr int KB = 256;                                  // K elements per stage (128 packed bytes)
 constexpr uint32_t kWBytes = kWRows * 128;               // 16 KB
-constexpr uint32_t kXTermBytes = kXRows * 128;           // 12 KB
-constexpr uint32_t kXBytes = kMxTerms * kXTermBytes;     // 36 KB
-constexpr uint32_t kStageBytes = kWBytes + kXBytes;      // 52 KB
-constexpr int kStages = 3;
-// scale ring: per stage the scale bytes of two k-blocks (16 bytes of each row)
-constexpr uint32_t kWsBytes = kWRows * 16;               // 2 KB: this CTA's weight rows
-constexpr uint32_t kXsTermBytes = kMaxN * 16;            // 3 KB: all 192 token rows of one term
-constexpr uint32_t kSfStageBytes = kWsBytes + kMxTerms * kXsTermBytes;  // 11 KB
-// Token boxes sized to the tile: a CTA loads 8, 32 or 96 rows of each term (tiles of N <= 16,
-// <= 64, <= 192 tokens) and 16, 64 or 192 rows of their scales; decode tiles hold 1-4 rows.
-constexpr int kNumBoxes = 3;
-__host__ __device__ constexpr int x_box_rows(int b) { return b == 0 ? 8 : b == 1 ? 32 : kXRows; }
-__host__ __device__ constexpr int box_for(int n) { return n <= 16 ? 0 : n <= 64 ? 1 : 2; }
-constexpr int kSfStages = 3;
-constexpr int kSfSlots = 2;
-constexpr uint32_t kSfCols = 64;                         // weight scales 8 + token scales 3 x 2 x 8
-constexpr uint32_t kSfBase = 2 * kMaxN;                  // TMEM column of slot 0
-constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kWsBytes = kWRows * 16;               // 2 KB: this CTA's weight rows' scale bytes of 2 k-blocks
 constexpr int kThreads = 320;                            // producer, MMA, 4 epilogue, 4 scale warps
-constexpr int kEpiTokens = 64;                           // tokens per GLU epilogue chunk
 constexpr int kEpiStride = 72;                           // floats per staged token: blocks at 0 and 36
-constexpr uint32_t kEpiBytes = kEpiTokens * kEpiStride * 4;  // 18 KB (the down epilogue uses 8 KB)
-constexpr size_t kSmem =
-    (size_t)kStages * kStageBytes + (size_t)kSfStages * kSfStageBytes + kEpiBytes + 1024 + 512;
-static_assert(kSfBase + kSfSlots * kSfCols <= kTmemCols, "TMEM budget");
-static_assert(kMaxN == kTileMx, "the dispatch cuts expert rows into tiles of this kernel's width");
-static_assert(kSmem <= 227 * 1024, "shared memory budget");
+
+// Layout of the kernel for token tiles of NT columns: 192 (prefill; the dispatch's 192-row tile
+// list) or 16 (decode; its 16-row unit list).  Decode tiles carry a few token rows against whole
+// weight tiles, so their stages are small and the ring is deep (eight k-blocks of weights in
+// flight per CTA instead of three): the kernel then streams weights as fast as HBM delivers them.
+template <int NT>
+struct MxCfg {
+  static constexpr int kN = NT;                                      // token columns per tile (MMA N)
+  static constexpr int kXRows = NT / 2;                              // token rows per CTA
+  static constexpr uint32_t kXTermBytes = kXRows * 128;              // one term's rows of a k-block
+  static constexpr uint32_t kStageBytes = kWBytes + kMxTerms * kXTermBytes;
+  static constexpr int kStages = NT >= 64 ? 3 : 8;
+  // scale ring: per stage the scale bytes of two k-blocks (16 bytes of each row): this CTA's weight
+  // rows, and all NT token rows of each term (both CTAs' MMA halves read every token row)
+  static constexpr uint32_t kXsTermBytes = NT * 16;
+  static constexpr uint32_t kSfStageBytes = kWsBytes + kMxTerms * kXsTermBytes;
+  static constexpr int kSfStages = NT >= 64 ? 3 : 4;
+  // token boxes sized to the tile: 8, 32 or 96 rows of each term per CTA (tiles of N <= 16, <= 64,
+  // <= 192 tokens) and 16, 64 or 192 rows of their scales
+  static constexpr int kNumBoxes = NT >= 64 ? 3 : 1;
+  // TMEM: two accumulators (at least 32 columns apart: the epilogue reads 32 at a time), then the
+  // scale slots: weight scales in 8 columns (4 per 4-block chunk, one per lane quadrant), token
+  // scales of term t and chunk h at 8 + t * 16 + h * 8 (row n at + n / 32).  Every scale-factor
+  // address the MMA is given is a multiple of 4 columns (weights) or 8 (tokens) from a 64-column
+  // slot start: the MMA reads its scale operands at such aligned addresses only.
+  static constexpr uint32_t kAccCols = NT >= 32 ? NT : 32;
+  static constexpr uint32_t kChunkCols = 8;
+  static constexpr uint32_t kSfCols = 64;
+  static constexpr int kSfSlots = NT >= 32 ? 2 : 4;
+  static constexpr uint32_t kSfBase = 2 * kAccCols;
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr int kEpiTokens = NT >= 64 ? 64 : 32;              // tokens per GLU epilogue chunk
+  static constexpr uint32_t kEpiBytes = kEpiTokens * kEpiStride * 4; // >= the down epilogue's 8 KB
+  static constexpr size_t kSmem =
+      (size_t)kStages * kStageBytes + (size_t)kSfStages * kSfStageBytes + kEpiBytes + 1024 + 512;
+  static_assert(kSfBase + kSfSlots * kSfCols <= kTmemCols, "TMEM budget");
+  static_assert(kSfBase % 64 == 0 && kSfCols % 64 == 0, "scale slots start on 64-column boundaries");
+  static_assert(8 + kMxTerms * 2 * kChunkCols <= kSfCols, "scale slot");
+  static_assert(kSmem <= 227 * 1024, "shared memory budget");
+  static_assert(kEpiBytes >= 4 * 32 * 32 * 2, "down epilogue staging");
+};
+static_assert(MxCfg<192>::kN == kTileMx, "the dispatch cuts expert rows into tiles of this kernel's width");
+static_assert(MxCfg<16>::kN == kTileS, "decode units are the dispatch's 16-row units");
+__host__ __device__ constexpr int x_box_rows(int NT, int b) {
+  return NT < 64 ? NT / 2 : (b == 0 ? 8 : b == 1 ? 32 : NT / 2);
+}
+__host__ __device__ constexpr int box_for(int n) { return n <= 16 ? 0 : n <= 64 ? 1 : 2; }
 
 struct MxParams {
   int num_kb;             // 256-element k-blocks (even: K % 512 == 0)
   int K;                  // reduction width
   int num_wt;             // weight tiles per expert
   int glu_h;              // > 0: gate/up weights [2h][K], 128 features per tile; 0: 256 rows per tile
-  const int4* tiles;      // token tiles of 192 rows: {expert, first tile of expert, rows of expert, first row}
+  const int4* tiles;      // NT = 192: tiles {expert, first tile of expert, rows of expert, first row};
+                          // NT = 16: units {expert, first row, rows (<= 16), 0}
   const int32_t* num_tiles;
   void* C;                // GLU: records of the activations [rows][ldc bytes]; down: fp16 [rows][ldc]
   int64_t ldc;
@@ -100,15 +122,23 @@ struct MxTile {
 
 __device__ __forceinline__ int4 mx_entry(const MxParams& p, int t) { return p.tiles[t / p.num_wt]; }
 
+template <int NT>
 __device__ __forceinline__ MxTile decode_mx(const MxParams& p, int t, int4 tl) {
-  const int rows = tl.z;
-  const int ntiles = (rows + kMaxN - 1) / kMaxN;
-  const int local = t - tl.y * p.num_wt;
   MxTile ti;
   ti.expert = tl.x;
+  if (NT == 16) {  // a unit of at most 16 rows, against weight tile t % num_wt
+    ti.wt = t - (t / p.num_wt) * p.num_wt;
+    ti.row0 = tl.y;
+    ti.nrows = tl.z;
+    ti.n = 16;
+    return ti;
+  }
+  const int rows = tl.z;
+  const int ntiles = (rows + NT - 1) / NT;
+  const int local = t - tl.y * p.num_wt;
   ti.wt = local / ntiles;
   const int j = local - ti.wt * ntiles;
-  // equal widths (multiples of 16, at most 192): width * (ntiles - 1) < rows, so no tile is empty
+  // equal widths (multiples of 16, at most NT): width * (ntiles - 1) < rows, so no tile is empty
   const int width = ((rows + ntiles - 1) / ntiles + 15) & ~15;
   ti.row0 = tl.w + j * width;
   ti.nrows = min(width, rows - j * width);
@@ -119,13 +149,20 @@ __device__ __forceinline__ MxTile decode_mx(const MxParams& p, int t, int4 tl) {
 // Epilogue-warp barrier (the 4 epilogue warps only).
 __device__ __forceinline__ void epi_barrier() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
-template <bool GLU>
+template <bool GLU, int NT>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tc_mx_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmWs,
                  const __grid_constant__ CUtensorMap tmX0, const __grid_constant__ CUtensorMap tmX1,
                  const __grid_constant__ CUtensorMap tmX2, const __grid_constant__ CUtensorMap tmXs0,
                  const __grid_constant__ CUtensorMap tmXs1, const __grid_constant__ CUtensorMap tmXs2,
                  const MxParams p) {
+  using C = MxCfg<NT>;
+  constexpr int kStages = C::kStages, kSfStages = C::kSfStages, kSfSlots = C::kSfSlots;
+  constexpr uint32_t kStageBytes = C::kStageBytes, kXTermBytes = C::kXTermBytes, kSfStageBytes = C::kSfStageBytes;
+  constexpr uint32_t kXsTermBytes = C::kXsTermBytes, kEpiBytes = C::kEpiBytes, kSfBase = C::kSfBase;
+  constexpr uint32_t kSfCols = C::kSfCols, kAccCols = C::kAccCols, kChunkCols = C::kChunkCols;
+  constexpr uint32_t kTmemCols = C::kTmemCols;
+  constexpr int kEpiTokens = C::kEpiTokens;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = ptx::smem_addr(smem_raw);
   uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);  // same offset in both CTAs
@@ -194,16 +231,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     bool first = true;
     int4 entry = pair < total ? mx_entry(p, pair) : make_int4(0, 0, 0, 0);
     for (int t = pair; t < total; t += npairs) {
-      const MxTile ti = decode_mx(p, t, entry);
+      const MxTile ti = decode_mx<NT>(p, t, entry);
       if (t + npairs < total) entry = mx_entry(p, t + npairs);
       const int xrow0 = ti.row0 + (int)rank * (ti.n >> 1);  // this CTA's N/2 token rows
       const int wrow_glu = (ti.wt * 128 + (int)rank * 64) / 16;                // GLU: first 16-row group
       const int wrow = ti.wt * 2 * kWRows + (int)rank * kWRows;                // down: first weight row
-      const int bsel = box_for(ti.n);
+      const int bsel = C::kNumBoxes == 1 ? 0 : box_for(ti.n);
       const CUtensorMap* tmX = bsel == 0 ? &tmX0 : bsel == 1 ? &tmX1 : &tmX2;
       const CUtensorMap* tmXs = bsel == 0 ? &tmXs0 : bsel == 1 ? &tmXs1 : &tmXs2;
-      const uint32_t stage_tx = kWBytes + kMxTerms * (uint32_t)x_box_rows(bsel) * 128u;
-      const uint32_t sf_tx = kWsBytes + kMxTerms * (uint32_t)(2 * x_box_rows(bsel)) * 16u;
+      const uint32_t stage_tx = kWBytes + kMxTerms * (uint32_t)x_box_rows(NT, bsel) * 128u;
+      const uint32_t sf_tx = kWsBytes + kMxTerms * (uint32_t)(2 * x_box_rows(NT, bsel)) * 16u;
       for (int kb = 0; kb < p.num_kb; ++kb, ++iter) {
         if ((kb & 1) == 0) {
           // scale bytes of k-blocks kb, kb+1 (16 bytes of every row) into this CTA's scale ring
@@ -262,7 +299,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     int it = 0;
     int4 entry = pair < total ? mx_entry(p, pair) : make_int4(0, 0, 0, 0);
     for (int t = pair; t < total; t += npairs, ++it) {
-      const MxTile ti = decode_mx(p, t, entry);
+      const MxTile ti = decode_mx<NT>(p, t, entry);
       if (t + npairs < total) entry = mx_entry(p, t + npairs);
       const int acc = it & 1;
       const uint32_t use = (uint32_t)(it >> 1);
@@ -270,12 +307,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                   kWaitAccFree))
         goto done;
       ptx::tc_fence_after();
-      const uint32_t d_tmem = tmem_base + (uint32_t)(acc * kMaxN);
+      const uint32_t d_tmem = tmem_base + (uint32_t)acc * kAccCols;
       for (int kb = 0; kb < p.num_kb; ++kb, ++g) {
-        const int slot = g & 1;
+        const int slot = g % kSfSlots;
         if (!ptx::mbar_wait_bounded(&full[s], ph, abort_flag, p.status, p.timeout_ns, kWaitFull)) goto done;
-        if (!ptx::mbar_wait_bounded(&sf_full[slot], (uint32_t)(g >> 1) & 1u, abort_flag, p.status, p.timeout_ns,
-                                    kWaitConverted))
+        if (!ptx::mbar_wait_bounded(&sf_full[slot], (uint32_t)(g / kSfSlots) & 1u, abort_flag, p.status,
+                                    p.timeout_ns, kWaitConverted))
           goto done;
         ptx::tc_fence_after();
         const uint32_t w_addr = ptx::smem_addr(smem + s * kStageBytes);
@@ -289,7 +326,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int q = 0; q < kMxTerms; ++q)
             ptx::mma_mxf4_pair(d_tmem, a_desc, ptx::sw128_kmajor_desc(x_addr + q * kXTermBytes + kk * 32), idesc,
-                               sf + 4u * (uint32_t)(kk >> 1), sf + 8u + 16u * (uint32_t)q + 8u * (uint32_t)(kk >> 1),
+                               sf + 4u * (uint32_t)(kk >> 1),
+                               sf + 8u + 2u * kChunkCols * (uint32_t)q + kChunkCols * (uint32_t)(kk >> 1),
                                (kb | kk | q) != 0 ? 1u : 0u);
         }
         ptx::mma_commit_pair(&empty[s]);
@@ -309,37 +347,48 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     uint32_t sph = 0;
     for (int t = pair; t < total; t += npairs) {
       for (int kb = 0; kb < p.num_kb; ++kb, ++g) {
-        const int slot = g & 1;
+        const int slot = g % kSfSlots;
         int ok = 1;
         if (lane == 0) {
           if ((kb & 1) == 0)
             ok = ptx::mbar_wait_bounded(&sfr_full[ss], sph, abort_flag, p.status, p.timeout_ns, kWaitFull);
-          ok = ok && ptx::mbar_wait_bounded(&sf_empty[slot], ((uint32_t)(g >> 1) & 1u) ^ 1u, abort_flag, p.status,
-                                            p.timeout_ns, kWaitAccFree);
+          ok = ok && ptx::mbar_wait_bounded(&sf_empty[slot], ((uint32_t)(g / kSfSlots) & 1u) ^ 1u, abort_flag,
+                                            p.status, p.timeout_ns, kWaitAccFree);
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) goto sf_done;
         {
           const uint8_t* st = sf_ring + ss * kSfStageBytes + 8 * (kb & 1);  // this k-block's 8 bytes of a row
           const uint2 wv = *reinterpret_cast<const uint2*>(st + (32 * q + lane) * 16);
-          uint32_t lo[kMxTerms][8], hi[kMxTerms][8];
-#pragma unroll
-          for (int tt = 0; tt < kMxTerms; ++tt)
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-              uint2 v = make_uint2(0u, 0u);
-              if (c < kMaxN / 32) v = *reinterpret_cast<const uint2*>(st + kWsBytes + tt * kXsTermBytes + (32 * c + lane) * 16);
-              lo[tt][c] = v.x;
-              hi[tt][c] = v.y;
-            }
           ptx::tc_fence_after();
           const uint32_t col = lane_base + (uint32_t)slot * kSfCols;
           ptx::tmem_st_32x32b_x1(col + (uint32_t)q, wv.x);       // weight scale blocks 0..3 of the k-block
           ptx::tmem_st_32x32b_x1(col + 4u + (uint32_t)q, wv.y);  // blocks 4..7
+          if (NT >= 32) {
+            uint32_t lo[kMxTerms][8], hi[kMxTerms][8];
 #pragma unroll
-          for (int tt = 0; tt < kMxTerms; ++tt) {
-            ptx::tmem_st_32x32b_x8(col + 8u + 16u * (uint32_t)tt, lo[tt]);
-            ptx::tmem_st_32x32b_x8(col + 16u + 16u * (uint32_t)tt, hi[tt]);
+            for (int tt = 0; tt < kMxTerms; ++tt)
+#pragma unroll
+              for (int c = 0; c < 8; ++c) {
+                uint2 v = make_uint2(0u, 0u);
+                if (c < NT / 32)
+                  v = *reinterpret_cast<const uint2*>(st + kWsBytes + tt * kXsTermBytes + (32 * c + lane) * 16);
+                lo[tt][c] = v.x;
+                hi[tt][c] = v.y;
+              }
+#pragma unroll
+            for (int tt = 0; tt < kMxTerms; ++tt) {
+              ptx::tmem_st_32x32b_x8(col + 8u + 2u * kChunkCols * tt, lo[tt]);
+              ptx::tmem_st_32x32b_x8(col + 8u + 2u * kChunkCols * tt + kChunkCols, hi[tt]);
+            }
+          } else {  // one column per term and chunk: token rows 0 .. NT-1 in lanes 0 .. NT-1
+#pragma unroll
+            for (int tt = 0; tt < kMxTerms; ++tt) {
+              uint2 v = make_uint2(0u, 0u);
+              if (lane < NT) v = *reinterpret_cast<const uint2*>(st + kWsBytes + tt * kXsTermBytes + lane * 16);
+              ptx::tmem_st_32x32b_x1(col + 8u + 2u * kChunkCols * tt, v.x);
+              ptx::tmem_st_32x32b_x1(col + 8u + 2u * kChunkCols * tt + kChunkCols, v.y);
+            }
           }
           ptx::tmem_st_wait();
           ptx::tc_fence_before();
@@ -368,14 +417,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     int it = 0;
     int4 entry = pair < total ? mx_entry(p, pair) : make_int4(0, 0, 0, 0);
     for (int t = pair; t < total; t += npairs, ++it) {
-      const MxTile ti = decode_mx(p, t, entry);
+      const MxTile ti = decode_mx<NT>(p, t, entry);
       if (t + npairs < total) entry = mx_entry(p, t + npairs);
       const int acc = it & 1;
       const uint32_t use = (uint32_t)(it >> 1);
       // down x p: the item's row scales, lane l holding token 32 c + l
-      float sc_reg[kMaxN / 32];
+      constexpr int kChunks = (NT + 31) / 32;
+      float sc_reg[kChunks];
 #pragma unroll
-      for (int c = 0; c < kMaxN / 32; ++c) {
+      for (int c = 0; c < kChunks; ++c) {
         const int jl = c * 32 + lane;
         sc_reg[c] = !GLU && jl < ti.nrows ? p.row_scale[ti.row0 + jl] : 0.0f;
       }
@@ -391,7 +441,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       epi_barrier();  // every warp has read the flag before the next item rewrites it
       if (!ok) break;
       ptx::tc_fence_after();
-      const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * kMaxN);
+      const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)acc * kAccCols;
       if (GLU) {
         // this CTA's 64 features fb .. fb+63: warp q holds 16 of them.  64 tokens at a time are
         // staged as fp32 [token][2 blocks of 32 features] (block b at float 36 b of a 72-float
@@ -458,7 +508,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const int c = c0 >> 5;
           float scv = 0.f;
 #pragma unroll
-          for (int cc = 0; cc < kMaxN / 32; ++cc)
+          for (int cc = 0; cc < kChunks; ++cc)
             if (cc == c) scv = sc_reg[cc];
 #pragma unroll
           for (int i2 = 0; i2 < 32; ++i2) {
@@ -504,9 +554,10 @@ done:
   }
 }
 
-template <bool GLU>
+template <bool GLU, int NT>
 cudaError_t launch_mx_inst(const CUtensorMap (&maps)[8], const MxParams& p, long long items, cudaStream_t s) {
-  auto kern = tc_mx_kernel<GLU>;
+  auto kern = tc_mx_kernel<GLU, NT>;
+  constexpr size_t kSmem = MxCfg<NT>::kSmem;
   static PerDeviceValue max_pairs_of;
   std::atomic<int>* slot = max_pairs_of.current();
   if (!slot) return cudaErrorInvalidDevice;
@@ -542,10 +593,12 @@ bool encode_u8(CUtensorMap* m, const void* ptr, int rank, const cuuint64_t* dims
 
 }  // namespace
 
-cudaError_t launch_tc_mx(const TcMx& g, const int4* tiles_m, const int32_t* num_tiles_m, int max_tiles_m,
+cudaError_t launch_tc_mx(const TcMx& g, const int4* tiles, const int32_t* num_tiles, int max_tiles, int unit_rows,
                          uint32_t* status, uint64_t timeout_ns, cudaStream_t s, int inject) {
   const bool glu = g.glu_h > 0;
-  if (!g.w.ptr || !g.w_scale || !g.x || !g.C || !tiles_m || !num_tiles_m) return cudaErrorInvalidValue;
+  if (!g.w.ptr || !g.w_scale || !g.x || !g.C || !tiles || !num_tiles) return cudaErrorInvalidValue;
+  if (unit_rows != MxCfg<192>::kN && unit_rows != MxCfg<16>::kN) return cudaErrorInvalidValue;
+  const bool decode = unit_rows == MxCfg<16>::kN;
   if (g.K % 512 || g.rows < 1) return cudaErrorInvalidValue;
   if (glu ? (g.glu_h % 128 || g.out_features != g.glu_h || g.out_features % 512 || g.w.rows != 2 * g.glu_h)
           : (g.out_features % (2 * kWRows) || g.w.rows != g.out_features || !g.row_scale || g.ldc % 8))
@@ -554,15 +607,16 @@ cudaError_t launch_tc_mx(const TcMx& g, const int4* tiles_m, const int32_t* num_
   CUtensorMap maps[8];  // weights, weight scales, token terms (3 box heights), token scales (3)
   bool ok = glu ? make_map_glu_interleaved(&maps[0], g.w, g.glu_h, kWRows / 32, true)
                 : make_map_fp4(&maps[0], g.w, kWRows, 128, true);
-  for (int b = 0; b < kNumBoxes; ++b) {
+  for (int b = 0; b < 3; ++b) {  // the decode layout uses its one box size in all three slots
     // the packed terms of the records as a 2-D byte array {3 K/2, rows}: boxes of 128 bytes
     const cuuint64_t dims[2] = {(cuuint64_t)(kMxTerms * g.K / 2), (cuuint64_t)g.rows};
     const cuuint64_t strides[1] = {(cuuint64_t)x_rec};
-    const cuuint32_t box[2] = {128, (cuuint32_t)x_box_rows(b)};
+    const int rows_b = x_box_rows(unit_rows, b);
+    const cuuint32_t box[2] = {128, (cuuint32_t)rows_b};
     ok = ok && encode_u8(&maps[2 + b], g.x, 2, dims, strides, box, true);
     // the records' scale bytes {3 K/32, rows}: boxes of 16 bytes x (2 x the term box) rows
     const cuuint64_t sdims[2] = {(cuuint64_t)(kMxTerms * kscale), (cuuint64_t)g.rows};
-    const cuuint32_t sbox[2] = {16, (cuuint32_t)(2 * x_box_rows(b))};
+    const cuuint32_t sbox[2] = {16, (cuuint32_t)(2 * rows_b)};
     ok = ok && encode_u8(&maps[5 + b], static_cast<const uint8_t*>(g.x) + mx3_scale_offset(g.K), 2, sdims, strides,
                          sbox, false);
   }
@@ -585,8 +639,8 @@ cudaError_t launch_tc_mx(const TcMx& g, const int4* tiles_m, const int32_t* num_
   p.K = g.K;
   p.num_wt = glu ? g.glu_h / 128 : g.out_features / (2 * kWRows);
   p.glu_h = glu ? g.glu_h : 0;
-  p.tiles = tiles_m;
-  p.num_tiles = num_tiles_m;
+  p.tiles = tiles;
+  p.num_tiles = num_tiles;
   p.C = g.C;
   p.ldc = glu ? mx3_row_bytes(g.out_features) : g.ldc;
   p.out_k = g.out_features;
@@ -594,9 +648,11 @@ cudaError_t launch_tc_mx(const TcMx& g, const int4* tiles_m, const int32_t* num_
   p.status = status;
   p.timeout_ns = timeout_ns;
   p.inject = inject;
-  const long long items = (long long)max_tiles_m * p.num_wt;
+  const long long items = (long long)max_tiles * p.num_wt;
   if (items == 0) return cudaSuccess;
-  return glu ? launch_mx_inst<true>(maps, p, items, s) : launch_mx_inst<false>(maps, p, items, s);
+  if (decode)
+    return glu ? launch_mx_inst<true, 16>(maps, p, items, s) : launch_mx_inst<false, 16>(maps, p, items, s);
+  return glu ? launch_mx_inst<true, 192>(maps, p, items, s) : launch_mx_inst<false, 192>(maps, p, items, s);
 }
 
 }  // namespace lmoe

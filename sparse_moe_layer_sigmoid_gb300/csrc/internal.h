@@ -205,7 +205,8 @@ size_t scatter_mx3_smem_bytes(int K, int in_elem_bytes);
 cudaError_t launch_scatter_mx3(const void* src, int src_dtype, void* dst, const int32_t* row_of, int T, int k, int K,
                                uint32_t* status, uint64_t timeout_ns, int num_sms, cudaStream_t s);
 // Grouped expert GEMM on tcgen05.mma.cta_group::2.kind::mxf4 (gemm_mx.cu): E2M1 weights with E8M0
-// scales per 32 along K against token records; 192-row token tiles (tiles_m from the dispatch).
+// scales per 32 along K against token records.  unit_rows 192: the dispatch's 192-row tile list
+// (tiles_m; prefill); unit_rows 16: its 16-row unit list (tiles_s; decode, a deep weight ring).
 //   glu_h > 0: gate/up weights [E][2h][K] (out_features == glu_h, multiple of 512); C receives
 //              the records of SiLU(gate) * up ([rows][mx3_row_bytes(h)]).
 //   glu_h == 0: down weights [E][out_features][K]; C receives fp16 rows [rows][ldc], each scaled
@@ -222,7 +223,7 @@ struct TcMx {
   int64_t ldc;              // down: fp16 elements per output row
   const float* row_scale;
 };
-cudaError_t launch_tc_mx(const TcMx& g, const int4* tiles_m, const int32_t* num_tiles_m, int max_tiles_m,
+cudaError_t launch_tc_mx(const TcMx& g, const int4* tiles, const int32_t* num_tiles, int max_tiles, int unit_rows,
                          uint32_t* status, uint64_t timeout_ns, cudaStream_t s, int inject = 0);
 
 }  // namespace lmoe

@@ -333,14 +333,18 @@ lmoe_status run_forward(lmoe_handle* h, const void* x, int T, const lmoe_weights
   const bool pair_swap = tc && !swap && c.routed_w == LMOE_BF16 && !(c.flags & LMOE_FLAG_SINGLE_CTA_GEMM) &&
                          hdim % 128 == 0 && l % 256 == 0;
   if (mx) {
+    // few rows per expert (decode): 16-row units and a deep weight ring; else 192-row tiles
+    const int4* tl = swap ? h->db.tiles_s : h->db.tiles_m;
+    const int32_t* ntl = swap ? h->db.num_tiles_s : h->db.num_tiles_m;
+    const int max_tl = swap ? h->max_tiles_s : h->max_tiles_m;
+    const int unit = swap ? kTileS : kTileMx;
     TcMx g = {};
     g.K = l; g.out_features = hdim; g.glu_h = hdim;
     g.w = op3d(w->routed_gate_up, c.num_experts, 2 * hdim, l);
     g.w_scale = w->routed_gate_up_scale;
     g.x = h->z_perm; g.rows = rows;
     g.C = h->a;
-    LMOE_TRY(launch_tc_mx(g, h->db.tiles_m, h->db.num_tiles_m, h->max_tiles_m, h->status, h->timeout_ns, s,
-                          inject_routed));
+    LMOE_TRY(launch_tc_mx(g, tl, ntl, max_tl, unit, h->status, h->timeout_ns, s, inject_routed));
     stage_end(h, kStGlu, s);
 
     TcMx dn = {};
@@ -349,7 +353,7 @@ lmoe_status run_forward(lmoe_handle* h, const void* x, int T, const lmoe_weights
     dn.w_scale = w->routed_down_scale;
     dn.x = h->a; dn.rows = rows;
     dn.C = o; dn.ldc = l; dn.row_scale = h->db.p_row;
-    LMOE_TRY(launch_tc_mx(dn, h->db.tiles_m, h->db.num_tiles_m, h->max_tiles_m, h->status, h->timeout_ns, s));
+    LMOE_TRY(launch_tc_mx(dn, tl, ntl, max_tl, unit, h->status, h->timeout_ns, s));
     stage_end(h, kStDown, s);
     h->last_launches += 2;
   } else if (pair_swap) {

@@ -132,8 +132,8 @@ __device__ void exact_logit_parts(const RouterSrc& r, int t, const int (&ce)[kCa
 // 32-entry scratch arrays private to the warp.
 //
 // The logits come from a GEMM whose error is bounded by `src.margin`, so a key is known to
-// within eta = margin/4 (+ fp32 rounding), and two keys further apart than 2*eta are ordered
-// correctly.  A token is settled exactly (second pass) when the order of its list is not certain:
+// within eta (token_eta: margin times the largest sigmoid' among the token's contenders, + fp32
+// rounding), and two keys further apart than 2*eta are ordered correctly.  A token is settled exactly (second pass) when the order of its list is not certain:
 // when the k-th and (k+1)-th keys are closer than 2*eta (the selected set itself), or when two
 // neighbouring ranks are (the rank order).  There every expert whose key lies in the band around
 // an uncertain boundary, and every selected expert with a neighbour closer than 2*eta, has its
@@ -148,7 +148,28 @@ struct TopkState {
   float a_k, a_k1;         // k-th and (k+1)-th keys
 };
 
+// Bound on |key - exact key| for any expert: a logit error of at most `margin` moves s = sigmoid(l)
+// by at most margin * max sigmoid' = margin / 4 (+ fp32 rounding of s and s + b).
 __device__ __forceinline__ float key_eta(const RouterSrc& src) { return 0.25f * src.margin + 1e-6f; }
+
+// The key uncertainty of one token's contenders.  Expert e's key moves by at most margin *
+// max sigmoid'(l) over [l_e - margin, l_e + margin] <= margin * (s_e (1 - s_e) + 1e-4) (sigmoid''
+// is at most 0.1 in size), + 1e-6 for rounding.  Every expert whose key could reach the boundary
+// lies within the widest band (2 key_eta around the k-th and (k+1)-th keys), so the largest bound
+// over that band and the selected experts bounds every comparison the selection and the rank
+// order make; near the top of 896 experts sigmoid' is ~0.08, a third of the worst case.
+template <int NPL>
+__device__ __forceinline__ float token_eta(const float (&kf)[NPL], const float (&sv)[NPL], float a_k1,
+                                           const RouterSrc& src) {
+  const float lo = a_k1 - 2.0f * key_eta(src);
+  float d = 0.0f;
+#pragma unroll
+  for (int i = 0; i < NPL; ++i)
+    if (kf[i] >= lo) d = fmaxf(d, sv[i] * (1.0f - sv[i]));
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) d = fmaxf(d, __shfl_xor_sync(0xffffffffu, d, off));
+  return src.margin * (d + 1e-4f) + 1e-6f;
+}
 
 template <int NPL>
 __device__ __forceinline__ int count_at_least(const uint32_t (&ko)[NPL], uint32_t v) {
@@ -288,7 +309,7 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ log
   if (t >= T) return;
   TopkState<NPL> st;
   topk_pass<NPL>(logits, bias, t, E, k, lane, st, s_sk[warp], s_ss[warp]);
-  const float eta2 = 2.0f * key_eta(src);
+  const float eta2 = 2.0f * token_eta<NPL>(st.kf, st.sv, st.a_k1, src);
   const float next = __shfl_down_sync(0xffffffffu, st.my_kf, 1);
   const bool close = lane + 1 < k && st.my_kf - next < eta2;  // rank order of lanes j, j+1 uncertain
   if ((k < E && st.a_k - st.a_k1 < eta2) || __any_sync(0xffffffffu, close)) {
@@ -301,15 +322,17 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ log
 }
 
 constexpr int kRefineWarps = 4;  // warps of a refinement CTA
-constexpr int kMaxCand = 64;     // boundary candidates per round
+constexpr int kMaxCont = 64;     // contenders of one token: its selected experts and the band
 
-// Shared memory of one refinement group (a warp, or the whole CTA).
+// Shared memory of one refinement group (a warp, or the whole CTA): the token's contenders.
 struct RefineSmem {
-  int* cand;       // [kMaxCand] candidate experts of this round
-  float2* part;    // [G][kMaxCand] partial logits (double-float) of the G warps
-  double* key;     // [kMaxCand] exact keys
-  float* s;        // [kMaxCand] exact scores rounded to fp32
-  int* n;          // candidates in this round
+  int* ce;          // [kMaxCont] contender experts
+  uint64_t* key;    // [kMaxCont] sort keys (order-preserving images of the fp64 keys)
+  float* s;         // [kMaxCont] scores
+  int* exa;         // [kMaxCont] 1: key and score recomputed exactly
+  int* cand;        // [kMaxCont] positions (in ce) of the contenders to recompute
+  float2* part;     // [G][kMaxCont] partial logits (double-float) of the G warps
+  int* n;           // [2]: contenders, contenders to recompute
 };
 
 template <int G>
@@ -325,7 +348,6 @@ __device__ __forceinline__ uint64_t orderable64(double d) {
   const uint64_t u = (uint64_t)__double_as_longlong(d);
   return (u >> 63) ? ~u : (u | 0x8000000000000000ull);
 }
-
 __device__ __forceinline__ double from_orderable64(uint64_t u) {
   return __longlong_as_double((long long)((u >> 63) ? (u & 0x7FFFFFFFFFFFFFFFull) : ~u));
 }
@@ -335,25 +357,24 @@ __device__ __forceinline__ double from_orderable64(uint64_t u) {
 constexpr double kNearTieGap = 1e-6;
 
 // Settle the list of token t exactly: G warps (gw = 0..G-1) cooperate.  Warp 0 of the group takes
-// pass 1's ranked list from idx (recomputing its keys and the (k+1)-th key), marks the experts
-// whose order is uncertain (the band around an uncertain boundary; selected experts with a
-// neighbouring rank closer than the key uncertainty) and lists them in rounds of at most
-// kMaxCand; the G warps recompute their logits to ~44 bits, warp gw over the 256-element blocks
-// gw, gw + G, ... of d, and warp 0 sums the G partials in a fixed order, takes fp64 keys, checks
-// each recomputed logit against the GEMM's (an error above half the margin is reported) and
-// ranks the contenders.  A token whose exact k-th and (k+1)-th keys differ by less than
-// kNearTieGap is counted in *near_ties.
+// pass 1's ranked list from idx (recomputing its keys and the (k+1)-th key), and lists the token's
+// contenders in shared memory: the selected experts and, when the boundary is uncertain, the band
+// of experts that may cross it; those whose order is uncertain (the band; selected experts with a
+// neighbouring rank closer than the key uncertainty) are recomputed.  The G warps compute their
+// logits to ~44 bits, warp gw over the 256-element blocks gw, gw + G, ... of d; warp 0 sums the G
+// partials in a fixed order, takes fp64 keys, checks each recomputed logit against the GEMM's (an
+// error above half the margin is reported) and ranks the contenders (two per lane) by key, exact
+// where recomputed.  A token whose exact k-th and (k+1)-th keys differ by less than kNearTieGap
+// is counted in *near_ties.  More than kMaxCont contenders (dozens of experts within the key
+// uncertainty of the boundary) is reported as a device check and ranks the first kMaxCont.
 template <int NPL, int G>
 __device__ __forceinline__ void refine_token(const float* __restrict__ logits, const float* __restrict__ bias,
                                              const RouterSrc& src, int t, int E, int k, int32_t* __restrict__ idx,
                                              float* __restrict__ p, int gw, int lane, const RefineSmem& sm,
                                              uint32_t* status, int32_t* near_ties) {
   const uint32_t lt_mask = (1u << lane) - 1u;
-  TopkState<NPL> st;
-  uint64_t ex[NPL];    // sort keys of this lane's contenders (orderable; 0: not a contender)
-  uint32_t pend = 0;   // bit i: expert lane + 32 i awaits recomputation
-  uint32_t exact = 0;  // bit i: ex[i] is the exact key
   if (gw == 0) {
+    TopkState<NPL> st;
     topk_keys<NPL>(logits, bias, t, E, lane, st);
     st.my_e = lane < k ? idx[(size_t)t * k + lane] : 0;
     st.my_s = 0.f;
@@ -373,7 +394,7 @@ __device__ __forceinline__ void refine_token(const float* __restrict__ logits, c
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) below = fmaxf(below, __shfl_xor_sync(0xffffffffu, below, off));
     st.a_k1 = n_ge > k ? st.a_k : below;
-    const float eta2 = 2.0f * key_eta(src);
+    const float eta2 = 2.0f * token_eta<NPL>(st.kf, st.sv, st.a_k1, src);
     const bool uncertain = k < E && st.a_k - st.a_k1 < eta2;
     // ranks whose order against a neighbouring rank (or, for the last, against the experts below
     // an uncertain boundary) is not certain
@@ -381,7 +402,7 @@ __device__ __forceinline__ void refine_token(const float* __restrict__ logits, c
     const float next = __shfl_down_sync(0xffffffffu, st.my_kf, 1);
     const int close = lane < k && ((lane > 0 && prev - st.my_kf < eta2) || (lane + 1 < k && st.my_kf - next < eta2) ||
                                    (lane == k - 1 && uncertain));
-    uint32_t sel = 0;
+    uint32_t sel = 0, pend = 0;  // bit i: expert lane + 32 i is selected / awaits recomputation
     for (int j = 0; j < k; ++j) {
       const int e = __shfl_sync(0xffffffffu, st.my_e, j);
       const int c = __shfl_sync(0xffffffffu, close, j);
@@ -398,114 +419,102 @@ __device__ __forceinline__ void refine_token(const float* __restrict__ logits, c
         if (e < E && st.kf[i] >= lo && st.kf[i] <= hi) pend |= 1u << i;
       }
     }
+    // contenders into shared memory (slot-major, then lane: a fixed order)
+    int cnt = 0, nrc = 0;
 #pragma unroll
-    for (int i = 0; i < NPL; ++i) ex[i] = ((sel | pend) >> i) & 1u ? orderable64((double)st.kf[i]) : 0ull;
+    for (int i = 0; i < NPL; ++i) {
+      const bool c = ((sel | pend) >> i) & 1u;
+      const uint32_t m = __ballot_sync(0xffffffffu, c);
+      const int at = cnt + __popc(m & lt_mask);
+      const bool in = c && at < kMaxCont;
+      const bool r = in && ((pend >> i) & 1u);
+      const uint32_t mr = __ballot_sync(0xffffffffu, r);
+      if (in) {
+        sm.ce[at] = lane + 32 * i;
+        sm.key[at] = orderable64((double)st.kf[i]);
+        sm.s[at] = st.sv[i];
+        sm.exa[at] = 0;
+        if (r) sm.cand[nrc + __popc(mr & lt_mask)] = at;
+      }
+      cnt += __popc(m);
+      nrc += __popc(mr);
+    }
+    if (cnt > kMaxCont) {  // the first kMaxCont are ranked; the result is not exact
+      if (lane == 0) report(status, kStatusDeviceCheck);
+      cnt = kMaxCont;
+    }
+    if (lane == 0) {
+      sm.n[0] = cnt;
+      sm.n[1] = nrc;
+    }
   }
-  while (true) {
-    int pos[NPL];
-    if (gw == 0) {
-      int cnt = 0;
+  group_sync<G>();
+  const int n_cont = sm.n[0], n_rc = sm.n[1];
+  for (int b0 = 0; b0 < n_rc; b0 += kCandBatch) {
+    int ce[kCandBatch];
+    const int nc = n_rc - b0 < kCandBatch ? n_rc - b0 : kCandBatch;
 #pragma unroll
-      for (int i = 0; i < NPL; ++i) {
-        pos[i] = -1;
-        const bool mine = (pend >> i) & 1u;
-        const uint32_t m = __ballot_sync(0xffffffffu, mine);
-        const int at = cnt + __popc(m & lt_mask);
-        if (mine && at < kMaxCand) {
-          sm.cand[at] = lane + 32 * i;
-          pos[i] = at;
-          pend &= ~(1u << i);
-        }
-        cnt += __popc(m);
-      }
-      if (lane == 0) *sm.n = cnt < kMaxCand ? cnt : kMaxCand;
+    for (int m = 0; m < kCandBatch; ++m) ce[m] = m < nc ? sm.ce[sm.cand[b0 + m]] : 0;
+    DF part[kCandBatch];
+    exact_logit_parts(src, t, ce, nc, gw, G, lane, part);
+    if (lane == 0) {
+#pragma unroll
+      for (int m = 0; m < kCandBatch; ++m)
+        if (m < nc) sm.part[gw * kMaxCont + b0 + m] = make_float2(part[m].hi, part[m].lo);
     }
-    group_sync<G>();
-    const int nc_total = *sm.n;
-    if (nc_total == 0) break;  // uniform over the group
-    for (int b0 = 0; b0 < nc_total; b0 += kCandBatch) {
-      int ce[kCandBatch];
-      const int nc = nc_total - b0 < kCandBatch ? nc_total - b0 : kCandBatch;
-#pragma unroll
-      for (int m = 0; m < kCandBatch; ++m) ce[m] = m < nc ? sm.cand[b0 + m] : 0;
-      DF part[kCandBatch];
-      exact_logit_parts(src, t, ce, nc, gw, G, lane, part);
-      if (lane == 0) {
-#pragma unroll
-        for (int m = 0; m < kCandBatch; ++m)
-          if (m < nc) sm.part[gw * kMaxCand + b0 + m] = make_float2(part[m].hi, part[m].lo);
-      }
-    }
-    group_sync<G>();
-    if (gw == 0) {
-      for (int c = lane; c < nc_total; c += 32) {
-        DF a{sm.part[c].x, sm.part[c].y};
-#pragma unroll
-        for (int q = 1; q < G; ++q) a = df_add(a, DF{sm.part[q * kMaxCand + c].x, sm.part[q * kMaxCand + c].y});
-        const int e = sm.cand[c];
-        const double l64 = (double)a.hi + (double)a.lo;
-        // the margin the selection relies on, checked on every logit recomputed here
-        if (fabs((double)logits[(size_t)t * E + e] - l64) > 0.5 * (double)src.margin)
-          report(status, kStatusDeviceCheck | kStatusRouterMargin);
-        const double s64 = 1.0 / (1.0 + exp(-l64));
-        sm.key[c] = s64 + (bias ? (double)bias[e] : 0.0);
-        sm.s[c] = (float)s64;
-      }
-      __syncwarp();
-#pragma unroll
-      for (int i = 0; i < NPL; ++i)
-        if (pos[i] >= 0) {
-          ex[i] = orderable64(sm.key[pos[i]]);
-          st.sv[i] = sm.s[pos[i]];
-          exact |= 1u << i;
-        }
-    }
-    group_sync<G>();  // cand, part and key are rewritten by the next round
   }
+  group_sync<G>();
   if (gw == 0) {
-    // ranks 0..k-1 by (key descending, index ascending); round k finds the (k+1)-th contender,
-    // for the near-tie count only
+    for (int c = lane; c < n_rc; c += 32) {
+      DF a{sm.part[c].x, sm.part[c].y};
+#pragma unroll
+      for (int q = 1; q < G; ++q) a = df_add(a, DF{sm.part[q * kMaxCont + c].x, sm.part[q * kMaxCont + c].y});
+      const int at = sm.cand[c];
+      const int e = sm.ce[at];
+      const double l64 = (double)a.hi + (double)a.lo;
+      // the margin the selection relies on, checked on every logit recomputed here
+      if (fabs((double)logits[(size_t)t * E + e] - l64) > 0.5 * (double)src.margin)
+        report(status, kStatusDeviceCheck | kStatusRouterMargin);
+      const double s64 = 1.0 / (1.0 + exp(-l64));
+      sm.key[at] = orderable64(s64 + (bias ? (double)bias[e] : 0.0));
+      sm.s[at] = (float)s64;
+      sm.exa[at] = 1;
+    }
+    __syncwarp();
+    // ranks 0..k-1 by (key descending, index ascending) over the contenders, lane l holding
+    // contenders l and l + 32; round k finds the (k+1)-th contender, for the near-tie count only
+    const bool h0 = lane < n_cont, h1 = lane + 32 < n_cont;
+    const uint64_t k0 = h0 ? sm.key[lane] : 0ull, k1 = h1 ? sm.key[lane + 32] : 0ull;
+    const int e0 = h0 ? sm.ce[lane] : 0x7FFFFFFF, e1 = h1 ? sm.ce[lane + 32] : 0x7FFFFFFF;
+    bool taken0 = !h0, taken1 = !h1;
+    int my_e = 0;
+    float my_s = 0.f;
     uint64_t key_k = 0;
     int exact_k = 0;
     for (int q = 0; q <= k; ++q) {
       uint64_t bv = 0;
-      int be = 0x7FFFFFFF;
-#pragma unroll
-      for (int i = 0; i < NPL; ++i) {
-        const int e = lane + 32 * i;
-        if (ex[i] > bv || (ex[i] == bv && ex[i] != 0 && e < be)) {
-          bv = ex[i];
-          be = e;
-        }
-      }
+      int be = 0x7FFFFFFF, bp = -1;
+      if (!taken0) { bv = k0; be = e0; bp = lane; }
+      if (!taken1 && (k1 > bv || (k1 == bv && e1 < be))) { bv = k1; be = e1; bp = lane + 32; }
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) {
         const uint64_t ov = __shfl_xor_sync(0xffffffffu, bv, off);
         const int oe = __shfl_xor_sync(0xffffffffu, be, off);
+        const int op = __shfl_xor_sync(0xffffffffu, bp, off);
         if (ov > bv || (ov == bv && oe < be)) {
           bv = ov;
           be = oe;
+          bp = op;
         }
       }
-      if (bv == 0) break;  // no contender left (round k only: the k selected experts contend)
-      const int owner = be & 31, slot = be >> 5;
-      float s_here = 0.f;
-      int x_here = 0;
-      if (lane == owner) {
-#pragma unroll
-        for (int i = 0; i < NPL; ++i)
-          if (i == slot) {
-            s_here = st.sv[i];
-            x_here = (exact >> i) & 1u;
-            ex[i] = 0;
-          }
-      }
-      const float s_win = __shfl_sync(0xffffffffu, s_here, owner);
-      const int x_win = __shfl_sync(0xffffffffu, x_here, owner);
+      if (bp < 0) break;  // no contender left (round k only: the k selected experts contend)
+      if (bp == lane) taken0 = true;
+      if (bp == lane + 32) taken1 = true;
+      const int x_win = sm.exa[bp];
       if (q < k) {
         if (lane == q) {
-          st.my_e = be;
-          st.my_s = s_win;
+          my_e = be;
+          my_s = sm.s[bp];
         }
         key_k = bv;
         exact_k = x_win;
@@ -513,34 +522,35 @@ __device__ __forceinline__ void refine_token(const float* __restrict__ logits, c
         atomicAdd(near_ties, 1);
       }
     }
-    topk_write(t, k, st.my_e, st.my_s, idx, p, lane);
+    topk_write(t, k, my_e, my_s, idx, p, lane);
   }
-  group_sync<G>();  // *n of this token is read by every warp before the next token's round
+  group_sync<G>();  // the contender list of this token is read by every warp before the next token's
 }
 
-// Pass 2: the listed tokens.  With enough of them to keep every warp busy for several tokens,
-// each warp settles its own tokens; otherwise the 4 warps of a CTA split d for one token at a
-// time (short lists: decode and most prefill batches).  refine_count[0] is the list length,
-// refine_count[1] the near-tie counter.
+// Pass 2: the listed tokens.  With at least one token per warp each warp settles its own tokens;
+// otherwise the 4 warps of a CTA split d for one token at a time (short lists: decode batches).
+// refine_count[0] is the list length, refine_count[1] the near-tie counter.
 template <int NPL>
-__global__ void __launch_bounds__(32 * kRefineWarps) topk_refine_kernel(
+__global__ void __launch_bounds__(32 * kRefineWarps, 4) topk_refine_kernel(
     const float* __restrict__ logits, const float* __restrict__ bias, RouterSrc src, int E, int k,
     int32_t* __restrict__ idx, float* __restrict__ p, const int32_t* __restrict__ refine_list,
     int32_t* __restrict__ refine_count, uint32_t* status) {
-  __shared__ int s_cand[kRefineWarps][kMaxCand];
-  __shared__ float2 s_part[kRefineWarps][kMaxCand];
-  __shared__ double s_key[kRefineWarps][kMaxCand];
-  __shared__ float s_s[kRefineWarps][kMaxCand];
-  __shared__ int s_n[kRefineWarps];
+  __shared__ int s_ce[kRefineWarps][kMaxCont];
+  __shared__ uint64_t s_key[kRefineWarps][kMaxCont];
+  __shared__ float s_s[kRefineWarps][kMaxCont];
+  __shared__ int s_exa[kRefineWarps][kMaxCont];
+  __shared__ int s_cand[kRefineWarps][kMaxCont];
+  __shared__ float2 s_part[kRefineWarps][kMaxCont];
+  __shared__ int s_n[kRefineWarps][2];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n = refine_count[0];
   int32_t* near_ties = refine_count + 1;
-  if (n >= 4 * (int)gridDim.x * kRefineWarps) {  // at least 4 tokens per warp
-    const RefineSmem sm{s_cand[warp], s_part[warp], s_key[warp], s_s[warp], &s_n[warp]};
+  if (n >= (int)gridDim.x * kRefineWarps) {  // at least one token per warp
+    const RefineSmem sm{s_ce[warp], s_key[warp], s_s[warp], s_exa[warp], s_cand[warp], s_part[warp], s_n[warp]};
     for (int w = blockIdx.x * kRefineWarps + warp; w < n; w += gridDim.x * kRefineWarps)
       refine_token<NPL, 1>(logits, bias, src, refine_list[w], E, k, idx, p, 0, lane, sm, status, near_ties);
   } else {
-    const RefineSmem sm{s_cand[0], &s_part[0][0], s_key[0], s_s[0], &s_n[0]};
+    const RefineSmem sm{s_ce[0], s_key[0], s_s[0], s_exa[0], s_cand[0], &s_part[0][0], s_n[0]};
     for (int w = blockIdx.x; w < n; w += gridDim.x)
       refine_token<NPL, kRefineWarps>(logits, bias, src, refine_list[w], E, k, idx, p, warp, lane, sm, status,
                                       near_ties);
@@ -830,7 +840,7 @@ cudaError_t launch_topk(const float* logits, const float* bias, const RouterSrc&
   if (e != cudaSuccess) return e;
   const int warps_per_block = 8;
   dim3 grid((T + warps_per_block - 1) / warps_per_block), block(32 * warps_per_block);
-  const int rgrid = 4 * num_sms;
+  const int rgrid = 4 * num_sms;  // the residency the launch bounds give
   const int npl = (E + 31) / 32;
 #define LMOE_TOPK(N)                                                                                     \
   do {                                                                                                   \
