@@ -14,7 +14,10 @@
 // rows in each CTA of the pair), its token rows the N side (at most 192 per tile, each expert's
 // rows cut into ceil(rows / 192) tiles of equal width rounded up to 16).  Per 256-element k-block
 // each CTA stages 16 KB of weights and 3 x 12 KB of token terms; the even CTA issues 3 terms x 4
-// MMAs of K = 64.
+// MMAs of K = 64.  Decode tiles (16 token rows) put the three terms side by side in N instead:
+// one MMA of N = 48 per K = 64 (a CTA-pair MMA of N <= 64 costs the same issue time whatever N
+// is, about 49 cycles, so three N = 16 MMAs per 4 KB of weights would bound the weight stream
+// near half of HBM bandwidth); the epilogue adds the three terms' accumulator columns.
 //
 // Scale factors live in TMEM (two slots of 64 columns beside the two 192-column accumulators).
 // The producer brings each pair of k-blocks' scale bytes into a ring of their own by TMA (the
@@ -72,10 +75,15 @@ struct MxCfg {
   static constexpr int kNumBoxes = NT >= 64 ? 3 : 1;
   // TMEM: two accumulators (at least 32 columns apart: the epilogue reads 32 at a time), then the
   // scale slots: weight scales in 8 columns (4 per 4-block chunk, one per lane quadrant), token
-  // scales of term t and chunk h at 8 + t * 16 + h * 8 (row n at + n / 32).  Every scale-factor
+  // scales of term t and chunk h at 8 + t * 16 + h * 8 (row n at + n / 32; decode: the 48 MMA
+  // rows of chunk h at 8 + 16 h, row n at + n / 32).  Every scale-factor
   // address the MMA is given is a multiple of 4 columns (weights) or 8 (tokens) from a 64-column
   // slot start: the MMA reads its scale operands at such aligned addresses only.
-  static constexpr uint32_t kAccCols = NT >= 32 ? NT : 32;
+  // decode: N = 3 * 16 token-term columns, CTA c providing rows 24 c + 8 q + j' (term q of token
+  // 8 c + j'), the three terms of a k-block being contiguous 8-row swizzle atoms in its stage
+  static constexpr bool kTermsInN = NT < 32;
+  static constexpr int kMmaN = kTermsInN ? kMxTerms * NT : NT;
+  static constexpr uint32_t kAccCols = kTermsInN ? 64 : (NT >= 32 ? NT : 32);
   static constexpr uint32_t kChunkCols = 8;
   static constexpr uint32_t kSfCols = 64;
   static constexpr int kSfSlots = NT >= 32 ? 2 : 4;
@@ -90,6 +98,7 @@ struct MxCfg {
   static_assert(8 + kMxTerms * 2 * kChunkCols <= kSfCols, "scale slot");
   static_assert(kSmem <= 227 * 1024, "shared memory budget");
   static_assert(kEpiBytes >= 4 * 32 * 32 * 2, "down epilogue staging");
+  static_assert(!kTermsInN || (NT == 16 && kXTermBytes == 1024 && kMmaN <= 64), "decode: terms as 8-row atoms");
 };
 static_assert(MxCfg<192>::kN == kTileMx, "the dispatch cuts expert rows into tiles of this kernel's width");
 static_assert(MxCfg<16>::kN == kTileS, "decode units are the dispatch's 16-row units");
@@ -144,6 +153,29 @@ __device__ __forceinline__ MxTile decode_mx(const MxParams& p, int t, int4 tl) {
   ti.nrows = min(width, rows - j * width);
   ti.n = (ti.nrows + 15) & ~15;
   return ti;
+}
+
+// 32 token columns of an accumulator row, r[i] = token c0 + i.  With the terms in N (16-token
+// tiles) token j's three terms sit in columns 24 (j / 8) + 8 q + j % 8 and are added here (fp32,
+// term order); tokens 16..31 read as 0.
+template <bool kTermsInN>
+__device__ __forceinline__ void load_acc(uint32_t taddr, uint32_t (&r)[32]) {
+  if (!kTermsInN) {
+    ptx::tmem_ld_32x32b_x32(taddr, r);
+    ptx::tmem_ld_wait();
+    return;
+  }
+  uint32_t a[32], b[32];
+  ptx::tmem_ld_32x32b_x32(taddr, a);
+  ptx::tmem_ld_32x32b_x32(taddr + 32, b);
+  ptx::tmem_ld_wait();
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    r[j] = __float_as_uint(__uint_as_float(a[j]) + __uint_as_float(a[8 + j]) + __uint_as_float(a[16 + j]));
+    r[8 + j] = __float_as_uint(__uint_as_float(a[24 + j]) + __uint_as_float(b[j]) + __uint_as_float(b[8 + j]));
+  }
+#pragma unroll
+  for (int j = 16; j < 32; ++j) r[j] = 0u;
 }
 
 // Epilogue-warp barrier (the 4 epilogue warps only).
@@ -321,14 +353,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < KB / 64; ++kk) {
           const uint32_t sf_id = 2u * (uint32_t)(kk & 1);
-          const uint32_t idesc = ptx::idesc_mxf4(2 * kWRows, ti.n, sf_id, sf_id);
           const uint64_t a_desc = ptx::sw128_kmajor_desc(w_addr + kk * 32);
+          if (C::kTermsInN) {  // the three terms' 24 rows of each CTA as one operand: N = 48
+            ptx::mma_mxf4_pair(d_tmem, a_desc, ptx::sw128_kmajor_desc(x_addr + kk * 32),
+                               ptx::idesc_mxf4(2 * kWRows, C::kMmaN, sf_id, sf_id), sf + 4u * (uint32_t)(kk >> 1),
+                               sf + 8u + 2u * kChunkCols * (uint32_t)(kk >> 1), (kb | kk) != 0 ? 1u : 0u);
+          } else {
+            const uint32_t idesc = ptx::idesc_mxf4(2 * kWRows, ti.n, sf_id, sf_id);
 #pragma unroll
-          for (int q = 0; q < kMxTerms; ++q)
-            ptx::mma_mxf4_pair(d_tmem, a_desc, ptx::sw128_kmajor_desc(x_addr + q * kXTermBytes + kk * 32), idesc,
-                               sf + 4u * (uint32_t)(kk >> 1),
-                               sf + 8u + 2u * kChunkCols * (uint32_t)q + kChunkCols * (uint32_t)(kk >> 1),
-                               (kb | kk | q) != 0 ? 1u : 0u);
+            for (int q = 0; q < kMxTerms; ++q)
+              ptx::mma_mxf4_pair(d_tmem, a_desc, ptx::sw128_kmajor_desc(x_addr + q * kXTermBytes + kk * 32), idesc,
+                                 sf + 4u * (uint32_t)(kk >> 1),
+                                 sf + 8u + 2u * kChunkCols * (uint32_t)q + kChunkCols * (uint32_t)(kk >> 1),
+                                 (kb | kk | q) != 0 ? 1u : 0u);
+          }
         }
         ptx::mma_commit_pair(&empty[s]);
         ptx::mma_commit_pair_both(&sf_empty[slot]);
@@ -381,13 +419,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               ptx::tmem_st_32x32b_x8(col + 8u + 2u * kChunkCols * tt, lo[tt]);
               ptx::tmem_st_32x32b_x8(col + 8u + 2u * kChunkCols * tt + kChunkCols, hi[tt]);
             }
-          } else {  // one column per term and chunk: token rows 0 .. NT-1 in lanes 0 .. NT-1
+          } else {  // MMA rows n = 24 c + 8 q + j' (term q, token 8 c + j'): row n at lane n % 32,
+                    // column + n / 32 of chunk h's pair of columns at 8 + 2 h kChunkCols
 #pragma unroll
-            for (int tt = 0; tt < kMxTerms; ++tt) {
+            for (int half = 0; half < 2; ++half) {
+              const int n = 32 * half + lane;
               uint2 v = make_uint2(0u, 0u);
-              if (lane < NT) v = *reinterpret_cast<const uint2*>(st + kWsBytes + tt * kXsTermBytes + lane * 16);
-              ptx::tmem_st_32x32b_x1(col + 8u + 2u * kChunkCols * tt, v.x);
-              ptx::tmem_st_32x32b_x1(col + 8u + 2u * kChunkCols * tt + kChunkCols, v.y);
+              if (n < C::kMmaN) {
+                const int c = n / 24, tt = (n % 24) >> 3, j = 8 * c + (n & 7);
+                v = *reinterpret_cast<const uint2*>(st + kWsBytes + tt * kXsTermBytes + j * 16);
+              }
+              ptx::tmem_st_32x32b_x1(col + 8u + (uint32_t)half, v.x);
+              ptx::tmem_st_32x32b_x1(col + 8u + 2u * kChunkCols + (uint32_t)half, v.y);
             }
           }
           ptx::tmem_st_wait();
@@ -455,8 +498,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           for (int h2 = 0; h2 < kEpiTokens / 32; ++h2) {
             if (c0 + 32 * h2 >= ti.n) break;  // uniform
             uint32_t r[32];
-            ptx::tmem_ld_32x32b_x32(t_row + c0 + 32 * h2, r);
-            ptx::tmem_ld_wait();
+            load_acc<C::kTermsInN>(t_row + c0 + 32 * h2, r);
             // token pair (2i, 2i+1): lanes < 16 finish token 2i, lanes >= 16 token 2i+1
 #pragma unroll
             for (int i2 = 0; i2 < 16; ++i2) {
@@ -503,8 +545,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         uint16_t* st = reinterpret_cast<uint16_t*>(epi) + q * (32 * 32);
         for (int c0 = 0; c0 < ti.n; c0 += 32) {
           uint32_t r[32];
-          ptx::tmem_ld_32x32b_x32(t_row + c0, r);
-          ptx::tmem_ld_wait();
+          load_acc<C::kTermsInN>(t_row + c0, r);
           const int c = c0 >> 5;
           float scv = 0.f;
 #pragma unroll
