@@ -59,11 +59,15 @@ K3W_E32_BF16_PROFILE = replace(K3W_E128_BF16_PREFILL, name="k3w_e32_bf16_t1024",
 K3_MXFP4_DECODE_PROFILE = replace(K3_MXFP4_DECODE, name="k3_mxfp4_decode_e128_t8", tokens=8, experts=128)
 K3_MXFP4_PREFILL_PROFILE = replace(K3_MXFP4_PREFILL_SKEW, name="k3_mxfp4_prefill_e32_t1024", tokens=1024,
                                    experts=32, bias="none")
+# The routing stress workload at 8192 tokens (about 0.5 GB on the device) for captures of the
+# routing kernels.
+ROUTING_DISPATCH_PROFILE = replace(ROUTING_DISPATCH_STRESS, name="routing_dispatch_t8192", tokens=8192)
 
 CONFIGS = {c.name: c for c in (TINY_F32, K3W_E128_BF16_PREFILL, K3_MXFP4_DECODE,
                                K3_MXFP4_PREFILL_SKEW, K3_MXFP4_PREFILL_MILD,
                                ROUTING_DISPATCH_STRESS, K3W_E32_BF16_PROFILE,
-                               K3_MXFP4_DECODE_PROFILE, K3_MXFP4_PREFILL_PROFILE)}
+                               K3_MXFP4_DECODE_PROFILE, K3_MXFP4_PREFILL_PROFILE,
+                               ROUTING_DISPATCH_PROFILE)}
 
 
 def scaled(cfg: LayerConfig, **kw) -> LayerConfig:
