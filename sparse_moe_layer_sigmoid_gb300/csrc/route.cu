@@ -187,16 +187,26 @@ __device__ __forceinline__ void expert_key(const float* __restrict__ logits, con
   key = bias ? s + bias[e] : s;
 }
 
-// Keys and scores of this lane's experts (-inf / 0 past E).
+// Keys and scores of this lane's experts (-inf / 0 past E).  All of the lane's logits and biases
+// are loaded before any is used, so the loads are in flight together (one memory latency per
+// token instead of one per expert slot).
 template <int NPL>
 __device__ __forceinline__ void topk_keys(const float* __restrict__ logits, const float* __restrict__ bias, int t,
                                           int E, int lane, TopkState<NPL>& st) {
+  const float* row = logits + (size_t)t * E;
+  float lg[NPL], bs[NPL];
 #pragma unroll
   for (int i = 0; i < NPL; ++i) {
     const int e = lane + 32 * i;
-    st.kf[i] = -INFINITY;
-    st.sv[i] = 0.f;
-    if (e < E) expert_key(logits, bias, t, E, e, st.sv[i], st.kf[i]);
+    lg[i] = e < E ? __ldg(row + e) : 0.f;
+    bs[i] = bias && e < E ? __ldg(bias + e) : 0.f;
+  }
+#pragma unroll
+  for (int i = 0; i < NPL; ++i) {
+    const bool in = lane + 32 * i < E;
+    const float s = 1.0f / (1.0f + expf(-lg[i]));  // the arithmetic of expert_key
+    st.sv[i] = in ? s : 0.f;
+    st.kf[i] = in ? (bias ? s + bs[i] : s) : -INFINITY;
   }
 }
 
