@@ -135,7 +135,14 @@ lmoe_status latentmoe_route(lmoe_handle *h, const void *x, int32_t T, const lmoe
                             int32_t *tok_of_row, int32_t *row_of, void *stream);
 
 /* The whole layer: y [T][d] act dtype (with LMOE_FLAG_IDENTITY_EXPERTS: u [T][l]).
- * 0 <= T <= max_tokens; T == 0 returns LMOE_OK without launching anything. */
+ * 0 <= T <= max_tokens; T == 0 returns LMOE_OK without launching anything.
+ * With bf16 activations, W_down and the shared experts' GLU (they read x only) run on a second
+ * stream that the handle owns: it waits for an event recorded on `stream` at the start of the
+ * call, and `stream` waits for its events before the expert-row scatter and before the final
+ * GEMM, so the call stays ordered on `stream` like a single-stream launch sequence (and can be
+ * captured into a CUDA graph from `stream`).  While stage events are set
+ * (latentmoe_set_stage_events) every stage runs on `stream`, one after another.  Concurrent calls
+ * on one handle are not supported (they share the workspace). */
 lmoe_status latentmoe_forward(lmoe_handle *h, const void *x, int32_t T, const lmoe_weights *w,
                               void *y, void *stream);
 

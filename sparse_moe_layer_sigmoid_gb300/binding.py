@@ -273,6 +273,10 @@ class LatentMoE:
         arr = (C.c_void_p * len(self._events))(*[e.cuda_event for e in self._events])
         _check(_lib().latentmoe_set_stage_events(self._h, arr, len(self._events)), "set_stage_events")
 
+    def disable_stage_timing(self):
+        """Stop recording stage events (calls overlap W_down and the shared GLU again)."""
+        _check(_lib().latentmoe_set_stage_events(self._h, None, 0), "set_stage_events")
+
     def stage_times_ms(self) -> dict:
         """Device time of each stage of the last call (synchronises on its last event)."""
         self._events[-1].synchronize()

@@ -6,6 +6,10 @@
 //   fixed-order combine + RMSNorm -> shared-expert gate/up GLU -> final GEMM
 //   y = [shared activations | RMSNorm(u)] . [shared down | W_up]^T
 // (page "Lesson 6 - LatentMoE", kimi-k3-course.pages.dev, eq. 11 and eq. 13).
+// W_down and the shared experts' gate/up GLU depend on x alone: on the tensor-core path they run
+// on the handle's second stream, forked from the caller's stream by an event at the start of the
+// call and joined back (an event wait) before the row scatter and before the final GEMM, so they
+// overlap the routing chain (router, top-k, dispatch) and the routed experts.
 #include <cuda_runtime.h>
 #include <stdint.h>
 #include <string.h>
@@ -51,6 +55,9 @@ struct lmoe_handle {
   cudaEvent_t stage_ev[LMOE_NUM_STAGES + 1];  // caller-owned; recording on when stage_on
   bool stage_on;
   int marked;                                 // index of the last stage event recorded
+  cudaStream_t aux;                           // second stream: W_down and the shared GLU
+  cudaEvent_t ev_fork, ev_wdown, ev_shared;   // fork from / joins into the caller's stream
+  float* splitk_aux;                          // split-K partials of GEMMs on the second stream
 };
 
 namespace {
@@ -174,6 +181,7 @@ size_t layout(lmoe_handle* h, uint8_t* base) {
   h->wr_split = (c.act == LMOE_BF16 && c.router_w == LMOE_F32) ? take(3 * E * (size_t)c.d * 2) : nullptr;
   h->splitk_bytes = c.act == LMOE_BF16 ? tc_splitk_partial_bytes(h->num_sms) : 0;
   h->splitk = h->splitk_bytes ? reinterpret_cast<float*>(take(h->splitk_bytes)) : nullptr;
+  h->splitk_aux = h->splitk_bytes ? reinterpret_cast<float*>(take(h->splitk_bytes)) : nullptr;
   return off;
 }
 
@@ -244,6 +252,7 @@ lmoe_status run_routing(lmoe_handle* h, const void* x, int T, const lmoe_weights
 // tiles), everything else on single CTAs (128-row tiles; dense ones with at most half as many
 // output tiles as SMs split K).  Adds its launches to *launches.
 cudaError_t run_tc_gemm(lmoe_handle* h, TcGemm g, int inject, int* launches, cudaStream_t s) {
+  const bool on_aux = s == h->aux && h->aux != nullptr;
   const bool pair = !(h->cfg.flags & LMOE_FLAG_SINGLE_CTA_GEMM) && g.M >= kTileP && tc_pair_supported(g);
   if (pair) {
     *launches += 1;
@@ -251,12 +260,23 @@ cudaError_t run_tc_gemm(lmoe_handle* h, TcGemm g, int inject, int* launches, cud
   }
   // dense GEMMs of at most 128 rows may split K over the SMs (decode batches)
   if (!g.tiles) {
-    g.partial = h->splitk;
+    g.partial = on_aux ? h->splitk_aux : h->splitk;  // each stream has its own partials
     g.partial_bytes = h->splitk_bytes;
   }
   g.launch_count = launches;
   return launch_tc_gemm(g, h->status, h->timeout_ns, inject, h->num_sms, s);
 }
+
+// While armed, makes the caller's stream wait for everything enqueued on the handle's second
+// stream so far (used when a forward pass returns early after forking).
+struct AuxJoin {
+  lmoe_handle* h;
+  cudaStream_t s;
+  bool armed;
+  ~AuxJoin() {
+    if (armed && cudaEventRecord(h->ev_shared, h->aux) == cudaSuccess) cudaStreamWaitEvent(s, h->ev_shared, 0);
+  }
+};
 
 lmoe_status run_forward(lmoe_handle* h, const void* x, int T, const lmoe_weights* w, const int32_t* ext_idx,
                         const float* ext_p, void* y, cudaStream_t s) {
@@ -276,15 +296,9 @@ lmoe_status run_forward(lmoe_handle* h, const void* x, int T, const lmoe_weights
   // or in the W_down GEMM (2) of this call
   const int inject_routed = h->inject == 1 ? 1 : 0, inject_wdown = h->inject == 2 ? 1 : 0;
   h->inject = 0;
-  const int32_t* idx;
-  const float* p;
-  lmoe_status st = run_routing(h, x, T, w, ext_idx, ext_p, &idx, &p, s);
-  if (st != LMOE_OK) return st;
-  stage_begin(h, kStWDown, s);
-
-  // z = W_down x
   const int rt = routed_act_dtype(c);
-  if (tc) {
+  // z = W_down x (tensor cores)
+  auto launch_wdown = [&](cudaStream_t st) {
     TcGemm g = {};
     g.epi = rt == kF16 ? kEpiF16 : kEpiBF16;
     g.M = T; g.N = l; g.K = d;
@@ -292,7 +306,42 @@ lmoe_status run_forward(lmoe_handle* h, const void* x, int T, const lmoe_weights
     g.B0 = op2d(w->w_down_proj, l, d);
     g.k0_len = d; g.k0_per_group = d;
     g.C = h->z; g.ldc = l;
-    LMOE_TRY(run_tc_gemm(h, g, inject_wdown, &h->last_launches, s));
+    return run_tc_gemm(h, g, inject_wdown, &h->last_launches, st);
+  };
+  // shared experts' SiLU(gate) * up into the head columns of act_cat (tensor cores)
+  auto launch_shared = [&](cudaStream_t st) {
+    TcGemm g = {};
+    g.epi = kEpiGluBF16;
+    g.M = T; g.N = ns * hs; g.K = d;
+    g.A = op2d(x, T, d);
+    g.B0 = op3d(w->shared_gate_up, ns, 2 * hs, d);
+    g.k0_len = d; g.k0_per_group = d; g.glu_h = hs;
+    g.C = h->act_cat; g.ldc = kcat;
+    return run_tc_gemm(h, g, 0, &h->last_launches, st);
+  };
+  // Both depend on x alone: unless stages are being timed one by one, they go to the second
+  // stream at once and the caller's stream waits for them where their results are read.
+  const bool fork = tc && !h->stage_on && h->aux != nullptr;
+  AuxJoin join{h, s, false};  // on an early return the caller's stream still waits for the second
+  if (fork) {
+    LMOE_TRY(cudaEventRecord(h->ev_fork, s));
+    LMOE_TRY(cudaStreamWaitEvent(h->aux, h->ev_fork, 0));
+    join.armed = true;
+    LMOE_TRY(launch_wdown(h->aux));
+    LMOE_TRY(cudaEventRecord(h->ev_wdown, h->aux));
+    if (!identity && ns > 0) LMOE_TRY(launch_shared(h->aux));
+    LMOE_TRY(cudaEventRecord(h->ev_shared, h->aux));
+  }
+  const int32_t* idx;
+  const float* p;
+  lmoe_status st = run_routing(h, x, T, w, ext_idx, ext_p, &idx, &p, s);
+  if (st != LMOE_OK) return st;
+  stage_begin(h, kStWDown, s);
+
+  if (fork) {
+    LMOE_TRY(cudaStreamWaitEvent(s, h->ev_wdown, 0));
+  } else if (tc) {
+    LMOE_TRY(launch_wdown(s));
   } else {
     SimtGemm g = {};
     g.A = x; g.lda = d; g.a_dtype = c.act; g.b_dtype = c.act;
@@ -316,7 +365,8 @@ lmoe_status run_forward(lmoe_handle* h, const void* x, int T, const lmoe_weights
   stage_end(h, kStScatter, s);
   h->last_launches += 1;
 
-  if (identity) {
+  if (identity) {  // the second stream (W_down only) was joined before the row scatter
+    join.armed = false;
     stage_begin(h, kStCombine, s);
     LMOE_TRY(launch_combine(h->z_perm, c.act, c.act, h->db.row_of, p, nullptr, 0.f, T, k, l, y, l, s));
     stage_end(h, kStCombine, s);
@@ -462,15 +512,11 @@ lmoe_status run_forward(lmoe_handle* h, const void* x, int T, const lmoe_weights
   h->last_launches += 1;
 
   if (tc) {
-    if (ns > 0) {
-      TcGemm g = {};
-      g.epi = kEpiGluBF16;
-      g.M = T; g.N = ns * hs; g.K = d;
-      g.A = op2d(x, T, d);
-      g.B0 = op3d(w->shared_gate_up, ns, 2 * hs, d);
-      g.k0_len = d; g.k0_per_group = d; g.glu_h = hs;
-      g.C = h->act_cat; g.ldc = kcat;
-      LMOE_TRY(run_tc_gemm(h, g, 0, &h->last_launches, s));
+    if (fork) {
+      LMOE_TRY(cudaStreamWaitEvent(s, h->ev_shared, 0));
+      join.armed = false;  // every launch of the second stream is now ordered before the rest
+    } else if (ns > 0) {
+      LMOE_TRY(launch_shared(s));
       stage_end(h, kStSharedGlu, s);
     }
     stage_begin(h, kStFinal, s);
@@ -514,6 +560,15 @@ lmoe_status run_forward(lmoe_handle* h, const void* x, int T, const lmoe_weights
   }
   stages_finish(h, s);
   return LMOE_OK;
+}
+
+void release_streams(lmoe_handle* h) {
+  if (h->ev_fork) cudaEventDestroy(h->ev_fork);
+  if (h->ev_wdown) cudaEventDestroy(h->ev_wdown);
+  if (h->ev_shared) cudaEventDestroy(h->ev_shared);
+  if (h->aux) cudaStreamDestroy(h->aux);
+  h->ev_fork = h->ev_wdown = h->ev_shared = nullptr;
+  h->aux = nullptr;
 }
 
 lmoe_status check_call(lmoe_handle* h, const void* x, int32_t T) {
@@ -566,7 +621,12 @@ lmoe_status latentmoe_create(const lmoe_config* cfg, lmoe_handle** out) {
     return LMOE_ERR_OOM;
   }
   layout(h, h->ws);
-  if (cudaMemset(h->status, 0, sizeof(uint32_t)) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
+  if (cudaMemset(h->status, 0, sizeof(uint32_t)) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess ||
+      cudaStreamCreateWithFlags(&h->aux, cudaStreamNonBlocking) != cudaSuccess ||
+      cudaEventCreateWithFlags(&h->ev_fork, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&h->ev_wdown, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&h->ev_shared, cudaEventDisableTiming) != cudaSuccess) {
+    release_streams(h);
     cudaFree(h->ws);
     delete h;
     return LMOE_ERR_CUDA;
@@ -579,6 +639,7 @@ lmoe_status latentmoe_destroy(lmoe_handle* h) {
   if (!h) return LMOE_OK;
   DeviceGuard dg(h->device);
   cudaError_t e = dg.ok ? cudaDeviceSynchronize() : cudaErrorInvalidDevice;
+  release_streams(h);
   cudaFree(h->ws);
   delete h;
   return cuda_status(e);

@@ -295,6 +295,138 @@ __device__ __forceinline__ void topk_pass(const float* __restrict__ logits, cons
   __syncwarp();  // the scratch is rewritten by the warp's next token
 }
 
+// Bitonic sort of 64 (key, aux) entries held two per lane (entry j = 2 lane + h in key[h],
+// aux[h]) into descending key order, equal keys by ascending aux; afterwards entry j is rank j.
+__device__ __forceinline__ bool sorts_before(uint64_t ka, uint32_t aa, uint64_t kb, uint32_t ab) {
+  return ka > kb || (ka == kb && aa < ab);
+}
+__device__ __forceinline__ void sort64_desc(uint64_t (&key)[2], uint32_t (&aux)[2], int lane) {
+#pragma unroll
+  for (int size = 2; size <= 64; size <<= 1) {
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      if (stride == 1) {  // entries 2 lane and 2 lane + 1: in the lane
+        const bool desc = ((2 * lane) & size) == 0;
+        const bool swap = desc ? sorts_before(key[1], aux[1], key[0], aux[0])
+                               : sorts_before(key[0], aux[0], key[1], aux[1]);
+        if (swap) {
+          const uint64_t tk = key[0];
+          key[0] = key[1];
+          key[1] = tk;
+          const uint32_t ta = aux[0];
+          aux[0] = aux[1];
+          aux[1] = ta;
+        }
+      } else {  // partner entry j ^ stride sits in lane ^ (stride / 2), same h
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int j = 2 * lane + h;
+          const uint64_t ok = __shfl_xor_sync(0xffffffffu, key[h], stride >> 1);
+          const uint32_t oa = __shfl_xor_sync(0xffffffffu, aux[h], stride >> 1);
+          const bool keep_first = ((j & stride) == 0) == ((j & size) == 0);
+          const bool other_first = sorts_before(ok, oa, key[h], aux[h]);
+          if (keep_first ? other_first : !other_first) {
+            key[h] = ok;
+            aux[h] = oa;
+          }
+        }
+      }
+    }
+  }
+}
+
+// Entry r (0 <= r < 64) of a sort64_desc result, in every lane.
+__device__ __forceinline__ uint64_t entry_key(const uint64_t (&key)[2], int r) {
+  const uint64_t a = __shfl_sync(0xffffffffu, key[0], r >> 1), b = __shfl_sync(0xffffffffu, key[1], r >> 1);
+  return (r & 1) ? b : a;
+}
+__device__ __forceinline__ uint32_t entry_aux(const uint32_t (&aux)[2], int r) {
+  const uint32_t a = __shfl_sync(0xffffffffu, aux[0], r >> 1), b = __shfl_sync(0xffffffffu, aux[1], r >> 1);
+  return (r & 1) ? b : a;
+}
+
+// Pass 1 by candidates: the k-th largest of the 32 lane maxima bounds the k-th largest key from
+// below (those k lanes hold k keys at least that large), so only keys at or above it can be
+// selected.  When at most 64 keys qualify (k <= 32) they are compacted into the warp's scratch
+// and sorted by (key, lower index first) in one 64-entry bitonic network, which gives the
+// selection, its rank order and the (k+1)-th key at once: about 1.5 K warp instructions and a
+// few dozen dependent steps instead of a 32-step bisection.  Returns false (state untouched
+// but for the keys) when more than 64 keys qualify: topk_pass then selects by bisection.
+// `sk` / `ss`: 64-entry scratch private to the warp.
+template <int NPL>
+__device__ __forceinline__ bool topk_pass_sorted(const float* __restrict__ logits, const float* __restrict__ bias,
+                                                 int t, int E, int k, int lane, TopkState<NPL>& st, uint64_t* sk,
+                                                 float* ss) {
+  topk_keys<NPL>(logits, bias, t, E, lane, st);
+  if (k > 32) return false;
+  uint32_t ko[NPL];
+  uint32_t lm = 0;
+#pragma unroll
+  for (int i = 0; i < NPL; ++i) {
+    ko[i] = lane + 32 * i < E ? orderable(st.kf[i]) : 0u;
+    lm = ko[i] > lm ? ko[i] : lm;
+  }
+  // k-th largest lane maximum: bitonic sort of the 32 maxima, descending
+  uint32_t v = lm;
+#pragma unroll
+  for (int size = 2; size <= 32; size <<= 1)
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      const uint32_t o = __shfl_xor_sync(0xffffffffu, v, stride);
+      const bool keep_max = ((lane & stride) == 0) == ((lane & size) == 0);
+      v = keep_max ? (o > v ? o : v) : (o < v ? o : v);
+    }
+  const uint32_t lb = __shfl_sync(0xffffffffu, v, k - 1);
+  int cnt = 0;
+#pragma unroll
+  for (int i = 0; i < NPL; ++i) cnt += __popc(__ballot_sync(0xffffffffu, ko[i] >= lb && ko[i] != 0u));
+  if (cnt > 64) return false;
+  // candidates into the scratch: key, then 0xFFFF - expert (lower index first), then the position
+  const uint32_t lt = (1u << lane) - 1u;
+  int base = 0;
+#pragma unroll
+  for (int i = 0; i < NPL; ++i) {
+    const bool c = ko[i] >= lb && ko[i] != 0u;
+    const uint32_t m = __ballot_sync(0xffffffffu, c);
+    if (c) {
+      const int pos = base + __popc(m & lt);
+      sk[pos] = ((uint64_t)ko[i] << 32) | ((uint64_t)(0xFFFFu - (uint32_t)(lane + 32 * i)) << 16) | (uint64_t)pos;
+      ss[pos] = st.sv[i];
+    }
+    base += __popc(m);
+  }
+  __syncwarp();
+  uint64_t key[2];
+  uint32_t aux[2] = {0u, 0u};
+  key[0] = 2 * lane < cnt ? sk[2 * lane] : 0ull;
+  key[1] = 2 * lane + 1 < cnt ? sk[2 * lane + 1] : 0ull;
+  sort64_desc(key, aux, lane);
+  const uint64_t mine = entry_key(key, lane < k ? lane : 0);
+  st.my_e = 0;
+  st.my_s = 0.f;
+  st.my_kf = 0.f;
+  if (lane < k) {
+    st.my_e = (int)(0xFFFFu - (uint32_t)((mine >> 16) & 0xFFFFu));
+    st.my_kf = from_orderable((uint32_t)(mine >> 32));
+    st.my_s = ss[mine & 0xFFFFu];
+  }
+  st.a_k = from_orderable((uint32_t)(entry_key(key, k - 1) >> 32));
+  st.a_k1 = -INFINITY;
+  if (k < E) {
+    if (cnt > k) {
+      st.a_k1 = from_orderable((uint32_t)(entry_key(key, k) >> 32));
+    } else {  // exactly k candidates: the (k+1)-th key is the largest below the bound
+      uint32_t below = 0;
+#pragma unroll
+      for (int i = 0; i < NPL; ++i)
+        if (ko[i] < lb && ko[i] > below) below = ko[i];
+      st.a_k1 = from_orderable(__reduce_max_sync(0xffffffffu, below));
+    }
+  }
+  __syncwarp();  // the scratch is rewritten by the warp's next token
+  return true;
+}
+
 // p = s / sum(s over the selected set), summed in rank order; lanes j < k store rank j.
 __device__ __forceinline__ void topk_write(int t, int k, int my_e, float my_s, int32_t* __restrict__ idx,
                                            float* __restrict__ p, int lane) {
@@ -312,13 +444,14 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ log
                                                    RouterSrc src, int T, int E, int k, int32_t* __restrict__ idx,
                                                    float* __restrict__ p, int32_t* __restrict__ refine_list,
                                                    int32_t* __restrict__ refine_count) {
-  __shared__ uint64_t s_sk[8][32];
-  __shared__ float s_ss[8][32];
+  __shared__ uint64_t s_sk[8][64];
+  __shared__ float s_ss[8][64];
   const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (t >= T) return;
   TopkState<NPL> st;
-  topk_pass<NPL>(logits, bias, t, E, k, lane, st, s_sk[warp], s_ss[warp]);
+  if (!topk_pass_sorted<NPL>(logits, bias, t, E, k, lane, st, s_sk[warp], s_ss[warp]))
+    topk_pass<NPL>(logits, bias, t, E, k, lane, st, s_sk[warp], s_ss[warp]);
   const float eta2 = 2.0f * token_eta<NPL>(st.kf, st.sv, st.a_k1, src);
   const float next = __shfl_down_sync(0xffffffffu, st.my_kf, 1);
   const bool close = lane + 1 < k && st.my_kf - next < eta2;  // rank order of lanes j, j+1 uncertain
@@ -491,46 +624,26 @@ __device__ __forceinline__ void refine_token(const float* __restrict__ logits, c
       sm.exa[at] = 1;
     }
     __syncwarp();
-    // ranks 0..k-1 by (key descending, index ascending) over the contenders, lane l holding
-    // contenders l and l + 32; round k finds the (k+1)-th contender, for the near-tie count only
-    const bool h0 = lane < n_cont, h1 = lane + 32 < n_cont;
-    const uint64_t k0 = h0 ? sm.key[lane] : 0ull, k1 = h1 ? sm.key[lane + 32] : 0ull;
-    const int e0 = h0 ? sm.ce[lane] : 0x7FFFFFFF, e1 = h1 ? sm.ce[lane + 32] : 0x7FFFFFFF;
-    bool taken0 = !h0, taken1 = !h1;
-    int my_e = 0;
-    float my_s = 0.f;
-    uint64_t key_k = 0;
-    int exact_k = 0;
-    for (int q = 0; q <= k; ++q) {
-      uint64_t bv = 0;
-      int be = 0x7FFFFFFF, bp = -1;
-      if (!taken0) { bv = k0; be = e0; bp = lane; }
-      if (!taken1 && (k1 > bv || (k1 == bv && e1 < be))) { bv = k1; be = e1; bp = lane + 32; }
+    // ranks 0..k-1 by (key descending, index ascending) over the contenders: one 64-entry sort
+    // (aux = expert << 8 | position); entry k is the (k+1)-th contender, for the near-tie count
+    uint64_t key[2];
+    uint32_t aux[2];
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        const uint64_t ov = __shfl_xor_sync(0xffffffffu, bv, off);
-        const int oe = __shfl_xor_sync(0xffffffffu, be, off);
-        const int op = __shfl_xor_sync(0xffffffffu, bp, off);
-        if (ov > bv || (ov == bv && oe < be)) {
-          bv = ov;
-          be = oe;
-          bp = op;
-        }
-      }
-      if (bp < 0) break;  // no contender left (round k only: the k selected experts contend)
-      if (bp == lane) taken0 = true;
-      if (bp == lane + 32) taken1 = true;
-      const int x_win = sm.exa[bp];
-      if (q < k) {
-        if (lane == q) {
-          my_e = be;
-          my_s = sm.s[bp];
-        }
-        key_k = bv;
-        exact_k = x_win;
-      } else if (exact_k && x_win && lane == 0 && from_orderable64(key_k) - from_orderable64(bv) < kNearTieGap) {
+    for (int h = 0; h < 2; ++h) {
+      const int c = 2 * lane + h;
+      key[h] = c < n_cont ? sm.key[c] : 0ull;  // 0: below every key
+      aux[h] = c < n_cont ? ((uint32_t)sm.ce[c] << 8) | (uint32_t)c : 0xFFFFFFFFu;
+    }
+    sort64_desc(key, aux, lane);
+    const uint32_t mine = entry_aux(aux, lane < k ? lane : 0);
+    const int my_e = lane < k ? (int)(mine >> 8) : 0;
+    const float my_s = lane < k ? sm.s[mine & 0xFFu] : 0.f;
+    if (k < n_cont) {
+      const uint64_t key_k = entry_key(key, k - 1), key_k1 = entry_key(key, k);
+      const uint32_t pos_k = entry_aux(aux, k - 1) & 0xFFu, pos_k1 = entry_aux(aux, k) & 0xFFu;
+      if (lane == 0 && sm.exa[pos_k] && sm.exa[pos_k1] &&
+          from_orderable64(key_k) - from_orderable64(key_k1) < kNearTieGap)
         atomicAdd(near_ties, 1);
-      }
     }
     topk_write(t, k, my_e, my_s, idx, p, lane);
   }

@@ -191,6 +191,34 @@ def test_token_permutation_is_bitwise_invariant(binding):
     layer.close()
 
 
+@pytest.mark.parametrize("cfg", [replace(SMALL_BF16, name="fork_prefill", tokens=520, seed=42),
+                                 replace(SMALL_BF16, name="fork_decode_mx", routed_w="mxfp4", latent=512,
+                                         hidden=512, experts=24, tokens=40, seed=43),
+                                 replace(configs.ROUTING_DISPATCH_STRESS, name="fork_identity", tokens=700, d=512,
+                                         latent=256, experts=64, top_k=8, seed=44)],
+                         ids=lambda c: c.name)
+def test_second_stream_matches_one_stream(binding, cfg):
+    """W_down and the shared GLU run on the handle's second stream unless stages are timed (then
+    every stage runs on the caller's stream in order): the same kernels on the same inputs, so
+    the outputs are bitwise equal; a call on a side stream is ordered after earlier work there."""
+    dev = torch.device("cuda")
+    inp = device_inputs(cfg, dev, False)
+    layer = binding.LatentMoE(cfg)
+    y_fork = layer.forward(inp["x"], inp).clone()
+    layer.enable_stage_timing()
+    y_serial = layer.forward(inp["x"], inp).clone()
+    layer.disable_stage_timing()
+    side = torch.cuda.Stream()
+    with torch.cuda.stream(side):
+        x2 = inp["x"] * 1  # produced on the side stream just before the call
+        y_side = layer.forward(x2, inp, stream=side)
+    side.synchronize()
+    assert layer.status() == 0
+    assert torch.equal(y_fork, y_serial)
+    assert torch.equal(y_side, y_fork)
+    layer.close()
+
+
 @pytest.mark.parametrize("cfg", [SMALL_BF16, replace(SMALL_BF16, name="pair_grouped", tokens=700, experts=8,
                                                       bias="normal1.5", seed=41)], ids=lambda c: c.name)
 def test_cta_pair_gemms_match_single_cta(binding, cfg):
