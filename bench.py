@@ -526,6 +526,63 @@ def measure_workload(cfg, args, peaks, world, rank, dist, dev, flags, with_cpu):
     return rec
 
 
+EP_WORKLOAD = "k3_mxfp4_prefill_mild"  # routing of the mildly skewed K3 prefill (T=8192, E=896, k=16)
+EP_RANKS = 8
+
+
+def measure_ep(args, dev):
+    """Expert-parallel dispatch and combine emulated on one GPU (latentmoe_ep_emulate) at the
+    latent width and at the full width: per token the all-to-all carries k rows of l (latent) or
+    d (full) values each way.  Reports the rows crossing ranks, payload per token, and the
+    device time and HBM rate of pack / exchange / return / combine."""
+    import torch
+
+    from sparse_moe_layer_sigmoid_gb300 import binding, configs, inputs
+
+    cfg = configs.CONFIGS[EP_WORKLOAD]
+    inp = inputs.make_inputs(cfg, dev)
+    layer = binding.LatentMoE(cfg)
+    x = inp["x"]
+    rows = cfg.tokens * cfg.top_k
+    out = {"workload": f"ep_dispatch_combine_{cfg.name}_r{EP_RANKS}", "ranks": EP_RANKS, "tokens": cfg.tokens,
+           "experts": cfg.experts, "top_k": cfg.top_k, "rows": rows,
+           "rule": ("rank r owns tokens [r T/R, (r+1) T/R) and experts [r E/R, (r+1) E/R); identity experts; "
+                    "exchange = one HBM copy of every row per direction on this one GPU")}
+    for name, full in (("latent", False), ("full_width", True)):
+        width = cfg.d if full else cfg.latent
+        dt = x.dtype if full else torch.float16
+        send = torch.empty((rows, width), dtype=dt, device=dev)
+        recv = torch.empty((rows, width), dtype=dt, device=dev)
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+        for e in evs:
+            e.record()
+        times = []
+        for it in range(args.warmup + args.steps):
+            u, cells = layer.ep_emulate(x, inp, EP_RANKS, full, send=send, recv=recv, events=evs)
+            evs[-1].synchronize()
+            if it >= args.warmup:
+                times.append([evs[i].elapsed_time(evs[i + 1]) for i in range(5)])
+        if layer.status() != 0:
+            raise RuntimeError("ep emulation reported an error status")
+        t = [sum(c) / len(c) for c in zip(*times)]
+        cells = cells.cpu()
+        cross = int(cells.sum() - cells.diag().sum())
+        row_bytes = width * send.element_size()
+        out[name] = {"width": width, "row_bytes": row_bytes,
+                     "payload_values_per_token": cfg.top_k * width,
+                     "payload_bytes_per_token_all_rows": cfg.top_k * row_bytes,
+                     "cross_rank_rows": cross, "cross_rank_frac": cross / rows,
+                     "payload_bytes_per_token_cross_rank": cross * row_bytes / cfg.tokens,
+                     "ms": {"route_and_rows": t[0], "pack": t[1], "exchange": t[2], "return": t[3],
+                            "combine": t[4]},
+                     "exchange_gbs": 2 * rows * row_bytes / (t[2] * 1e-3) / 1e9}
+        del send, recv, u
+    out["payload_ratio_full_over_latent"] = (out["full_width"]["payload_bytes_per_token_all_rows"]
+                                             / out["latent"]["payload_bytes_per_token_all_rows"])
+    layer.close()
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -587,6 +644,7 @@ def main():
         line["cpu_baseline"] = head["cpu_baseline"]
     if subs:
         line["workloads"] = subs
+        line["ep_emulation"] = measure_ep(args, dev)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist:

@@ -193,6 +193,30 @@ lmoe_status latentmoe_set_stage_events(lmoe_handle *h, void *const *events, int3
  * final_gemm; NULL otherwise. */
 const char *latentmoe_stage_name(int32_t i);
 
+/* Expert-parallel dispatch and combine emulated on one GPU, to measure the all-to-all payload
+ * at the latent width against the full width (page "What K3 actually is", srikanthmalla.com,
+ * opening section: a routed token crosses the expert-parallel all-to-all at the experts' input
+ * width; page "Lesson 6 - LatentMoE", kimi-k3-course.pages.dev, table "What scales with what").
+ * `ranks` virtual ranks: rank r owns tokens [r T/ranks, (r+1) T/ranks) and experts
+ * [r E/ranks, (r+1) E/ranks) (T % ranks == 0, E % ranks == 0, 1 <= ranks <= 64).  The call
+ * routes x (router, top-k, dispatch), forms one row per selected (token, expert) pair -- the
+ * latent row z = W_down x (full_width 0: l values of the routed-expert activation dtype, fp16
+ * with MXFP4 experts) or x itself (full_width 1: d values, act dtype) -- packs each source
+ * rank's rows into send_buf ordered (destination rank, expert, token), exchanges them
+ * (send_buf -> recv_buf, the all-to-all), returns them unchanged as the outputs of identity
+ * experts (recv_buf -> send_buf) and combines each token's k rows in rank order weighted by p:
+ *   u [T][width] act dtype = sum_j p_(t,j) row(t, j)   (= z, resp. x, up to rounding: sum p = 1).
+ *   send_buf, recv_buf  device buffers of at least T*k*width*elem bytes each (buf_bytes)
+ *   cells     [ranks][ranks] int32 device, out (or NULL): rows sent from rank src to rank dst
+ *             (row-major by src); the payload of the all-to-all is sum over src != dst
+ *   events    6 cudaEvent_t (or NULL), recorded on `stream`: start, routed (and W_down done),
+ *             packed, exchanged, returned, combined.
+ * Errors: INVALID_ARG (sizes, alignment, ranks), CUDA. */
+lmoe_status latentmoe_ep_emulate(lmoe_handle *h, const void *x, int32_t T, const lmoe_weights *w,
+                                 int32_t ranks, int32_t full_width, void *send_buf, void *recv_buf,
+                                 size_t buf_bytes, void *u, int32_t *cells, void *const *events,
+                                 void *stream);
+
 /* Test hook: device address and byte size of an intermediate of the last call inside the
  * handle's workspace, by name: "logits" [T][E] fp32, "z" [T][l], "gathered" [T*k][l] (the
  * expert-contiguous rows; after a full forward it holds the p-scaled expert outputs), "act"

@@ -61,6 +61,8 @@ def _lib():
         lib.latentmoe_forward.argtypes = [vp, vp, i32, C.POINTER(LmoeWeights), vp, vp]
         lib.latentmoe_forward_routed.argtypes = [vp, vp, i32, C.POINTER(LmoeWeights), vp, vp, vp, vp]
         lib.latentmoe_forward_host.argtypes = [vp, vp, i32, C.POINTER(LmoeWeights), vp, vp]
+        lib.latentmoe_ep_emulate.argtypes = [vp, vp, i32, C.POINTER(LmoeWeights), i32, i32, vp, vp, C.c_size_t, vp,
+                                             vp, C.POINTER(vp), vp]
         lib.latentmoe_status.argtypes = [vp, vp]
         lib.latentmoe_last_launch_count.argtypes = [vp]
         lib.latentmoe_last_launch_count.restype = i32
@@ -215,6 +217,30 @@ class LatentMoE:
         _check(_lib().latentmoe_forward_routed(self._h, _ptr(x), x.shape[0], C.byref(w), _ptr(topk_idx),
                                                _ptr(topk_p), _ptr(y), _stream(stream)), "latentmoe_forward_routed")
         return y
+
+    def ep_emulate(self, x, weights: dict, ranks: int, full_width: bool, send=None, recv=None, stream=None,
+                   events=None):
+        """Expert-parallel dispatch + combine emulated on one GPU (latentmoe_ep_emulate): returns
+        (u, cells) with u [T][width] and cells [ranks][ranks] int32 rows sent src -> dst."""
+        T = x.shape[0]
+        width = self.cfg.d if full_width else self.cfg.latent
+        row_dtype = x.dtype if full_width else (torch.float16 if self.cfg.routed_w == "mxfp4" else x.dtype)
+        rows = T * self.cfg.top_k
+        if send is None:
+            send = torch.empty((rows, width), dtype=row_dtype, device=x.device)
+        if recv is None:
+            recv = torch.empty((rows, width), dtype=row_dtype, device=x.device)
+        nbytes = min(send.numel() * send.element_size(), recv.numel() * recv.element_size())
+        u = torch.empty((T, width), dtype=x.dtype, device=x.device)
+        cells = torch.zeros((ranks, ranks), dtype=torch.int32, device=x.device)
+        w = make_weights(weights)
+        ev = None
+        if events is not None:
+            ev = (C.c_void_p * 6)(*[e.cuda_event for e in events])
+        _check(_lib().latentmoe_ep_emulate(self._h, _ptr(x), T, C.byref(w), int(ranks), int(bool(full_width)),
+                                           _ptr(send), _ptr(recv), nbytes, _ptr(u), _ptr(cells), ev,
+                                           _stream(stream)), "latentmoe_ep_emulate")
+        return u, cells
 
     def forward_host(self, x_host, weights: dict, y_host=None, stream=None):
         if y_host is None:

@@ -98,6 +98,22 @@ cudaError_t launch_combine(const void* o, int in_dtype, int out_dtype, const int
                            const float* gain, float eps, int T, int k, int width, void* out, int64_t ld_out,
                            cudaStream_t s);
 
+// ---------------------------------------------------------------- expert-parallel emulation (ep_emulate.cu)
+// R virtual ranks over T/R tokens and E/R experts each (T % R == 0, E % R == 0, R <= kMaxEpRanks).
+constexpr int kMaxEpRanks = 64;
+size_t ep_plan_ints(int E, int R);
+// Plan from the dispatch's expert offsets and expert-sorted tokens (one CTA).
+cudaError_t launch_ep_plan(const int32_t* offsets, const int32_t* tok_of_row, int T, int E, int R, int32_t* plan,
+                           cudaStream_t s);
+// Token rows (src + t * src_ld_bytes, row_bytes each, a multiple of 16) into the send buffer
+// ordered (source rank, destination rank, expert, token); ep_row_of[t][j] = send position.
+cudaError_t launch_ep_pack(const void* src, int64_t src_ld_bytes, int row_bytes, const int32_t* idx,
+                           const int32_t* row_of, const int32_t* offsets, const int32_t* plan, int T, int E, int R,
+                           int k, void* send, int32_t* ep_row_of, int num_sms, cudaStream_t s);
+// forward: send -> recv (destination rank, source rank) order; backward: recv -> send order.
+cudaError_t launch_ep_exchange(const void* from, void* to, int row_bytes, int64_t rows, const int32_t* plan, int E,
+                               int R, int forward, int num_sms, cudaStream_t s);
+
 // ---------------------------------------------------------------- fp32 CUDA-core GEMM (simt.cu)
 struct SimtSegment {
   const void* ptr;        // B segment: element (group g, row n, col c) at ptr + g*group_stride + n*ld + c

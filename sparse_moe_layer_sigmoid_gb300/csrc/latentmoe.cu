@@ -58,6 +58,8 @@ struct lmoe_handle {
   cudaStream_t aux;                           // second stream: W_down and the shared GLU
   cudaEvent_t ev_fork, ev_wdown, ev_shared;   // fork from / joins into the caller's stream
   float* splitk_aux;                          // split-K partials of GEMMs on the second stream
+  int32_t* ep_plan;                           // expert-parallel emulation: plan (<= kMaxEpRanks ranks)
+  int32_t* ep_row_of;                         // [T*k]: send position of row (t, j)
 };
 
 namespace {
@@ -182,6 +184,8 @@ size_t layout(lmoe_handle* h, uint8_t* base) {
   h->splitk_bytes = c.act == LMOE_BF16 ? tc_splitk_partial_bytes(h->num_sms) : 0;
   h->splitk = h->splitk_bytes ? reinterpret_cast<float*>(take(h->splitk_bytes)) : nullptr;
   h->splitk_aux = h->splitk_bytes ? reinterpret_cast<float*>(take(h->splitk_bytes)) : nullptr;
+  h->ep_plan = reinterpret_cast<int32_t*>(take(ep_plan_ints(E, kMaxEpRanks) * 4));
+  h->ep_row_of = reinterpret_cast<int32_t*>(take(rows * 4));
   return off;
 }
 
@@ -675,6 +679,81 @@ lmoe_status latentmoe_route(lmoe_handle* h, const void* x, int32_t T, const lmoe
   }
   if (tok_of_row && rows) LMOE_TRY(cudaMemcpyAsync(tok_of_row, h->db.tok_of_row, rows * 4, cudaMemcpyDeviceToDevice, s));
   if (row_of && rows) LMOE_TRY(cudaMemcpyAsync(row_of, h->db.row_of, rows * 4, cudaMemcpyDeviceToDevice, s));
+  return LMOE_OK;
+}
+
+lmoe_status latentmoe_ep_emulate(lmoe_handle* h, const void* x, int32_t T, const lmoe_weights* w, int32_t ranks,
+                                 int32_t full_width, void* send_buf, void* recv_buf, size_t buf_bytes, void* u,
+                                 int32_t* cells, void* const* events, void* stream) {
+  lmoe_status st = check_call(h, x, T);
+  if (st != LMOE_OK) return st;
+  DeviceGuard dg(h->device);
+  if (!dg.ok) return LMOE_ERR_CUDA;
+  const lmoe_config& c = h->cfg;
+  const int E = c.num_experts, k = c.top_k, d = c.d, l = c.latent;
+  if (!w || !w->w_router || !aligned16(w->w_router) || !w->w_down_proj || !aligned16(w->w_down_proj) ||
+      (w->router_bias && !aligned16(w->router_bias)))
+    return LMOE_ERR_INVALID_ARG;
+  if (ranks < 1 || ranks > kMaxEpRanks || E % ranks || T % ranks || (full_width != 0 && full_width != 1))
+    return LMOE_ERR_INVALID_ARG;
+  const bool tc = c.act == LMOE_BF16;
+  const int row_dtype = full_width ? c.act : routed_act_dtype(c);
+  const int width = full_width ? d : l;
+  const int row_bytes = width * (int)dtype_bytes(row_dtype);
+  const int64_t rows = (int64_t)T * k;
+  if (row_bytes % 16 || (T > 0 && (!send_buf || !recv_buf || !u || !aligned16(send_buf) || !aligned16(recv_buf) ||
+                                   !aligned16(u) || buf_bytes < (size_t)rows * row_bytes)))
+    return LMOE_ERR_INVALID_ARG;
+  if (events)
+    for (int i = 0; i < 6; ++i)
+      if (!events[i]) return LMOE_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  auto mark = [&](int i) { return events ? cudaEventRecord(static_cast<cudaEvent_t>(events[i]), s) : cudaSuccess; };
+  h->last_launches = 0;
+  h->last_T = T;
+  if (T == 0) return LMOE_OK;
+  LMOE_TRY(mark(0));
+  const int32_t* idx;
+  const float* p;
+  st = run_routing(h, x, T, w, nullptr, nullptr, &idx, &p, s);
+  if (st != LMOE_OK) return st;
+  if (!full_width) {  // the latent rows z = W_down x
+    if (tc) {
+      TcGemm g = {};
+      g.epi = row_dtype == kF16 ? kEpiF16 : kEpiBF16;
+      g.M = T; g.N = l; g.K = d;
+      g.A = op2d(x, T, d);
+      g.B0 = op2d(w->w_down_proj, l, d);
+      g.k0_len = d; g.k0_per_group = d;
+      g.C = h->z; g.ldc = l;
+      LMOE_TRY(run_tc_gemm(h, g, 0, &h->last_launches, s));
+    } else {
+      SimtGemm g = {};
+      g.A = x; g.lda = d; g.a_dtype = c.act; g.b_dtype = c.act;
+      g.nseg = 1; g.seg[0] = SimtSegment{w->w_down_proj, d, 0, d, d};
+      g.M = T; g.N = l; g.K = d;
+      g.C = h->z; g.ldc = l; g.c_dtype = c.act;
+      LMOE_TRY(launch_simt_gemm(g, s));
+      h->last_launches += 1;
+    }
+  }
+  LMOE_TRY(mark(1));
+  const void* src = full_width ? x : h->z;
+  LMOE_TRY(launch_ep_plan(h->db.offsets, h->db.tok_of_row, T, E, ranks, h->ep_plan, s));
+  LMOE_TRY(launch_ep_pack(src, row_bytes, row_bytes, h->idx, h->db.row_of, h->db.offsets, h->ep_plan, T, E, ranks, k,
+                          send_buf, h->ep_row_of, h->num_sms, s));
+  LMOE_TRY(mark(2));
+  LMOE_TRY(launch_ep_exchange(send_buf, recv_buf, row_bytes, rows, h->ep_plan, E, ranks, 1, h->num_sms, s));
+  LMOE_TRY(mark(3));
+  // identity experts: the received rows return as the experts' outputs, into send order
+  LMOE_TRY(launch_ep_exchange(recv_buf, send_buf, row_bytes, rows, h->ep_plan, E, ranks, 0, h->num_sms, s));
+  LMOE_TRY(mark(4));
+  LMOE_TRY(launch_combine(send_buf, row_dtype, c.act, h->ep_row_of, p, nullptr, 0.f, T, k, width, u, width, s));
+  LMOE_TRY(mark(5));
+  h->last_launches += 5;
+  if (cells)
+    LMOE_TRY(cudaMemcpyAsync(cells, h->ep_plan + (size_t)2 * E * ranks, (size_t)ranks * ranks * 4,
+                             cudaMemcpyDeviceToDevice, s));
   return LMOE_OK;
 }
 
