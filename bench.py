@@ -417,6 +417,7 @@ def measure_workload(cfg, args, peaks, world, rank, dist, dev, flags, with_cpu):
             stages.setdefault(k_, []).append(v)
     layer.disable_stage_timing()
     serial_ms = sum(sum(v) / len(v) for v in stages.values())
+    graph_rec = graph_steps(layer, x, inp, y, flush, stream, args) if cfg.tokens <= GRAPH_MAX_TOKENS else None
     clk = clocks.stop() if clocks else None
     ms = max_over_ranks(sum(step_ms) / len(step_ms), dist, dev)
     if layer.status() != 0:
@@ -510,6 +511,9 @@ def measure_workload(cfg, args, peaks, world, rank, dist, dev, flags, with_cpu):
                    "h2d_bytes_per_step": cfg.tokens * cfg.d * elem,
                    "d2h_bytes_per_step": cfg.tokens * layer.out_width * elem},
            "gpu_launches": launches, "routing": route_stats, "clocks": clk}
+    if graph_rec:
+        graph_rec["value"] = job_tokens_per_s(world, cfg.tokens, graph_rec["ms_per_step"])
+        rec["graph"] = graph_rec
     layer.close()
     y = flush = None
     if with_cpu and rank == 0 and world == 1:
@@ -524,6 +528,50 @@ def measure_workload(cfg, args, peaks, world, rank, dist, dev, flags, with_cpu):
     torch.cuda.synchronize()
     torch.cuda.empty_cache()
     return rec
+
+
+GRAPH_MAX_TOKENS = 256  # decode-sized batches: also time the forward replayed as one CUDA graph
+
+
+def graph_steps(layer, x, inp, y, flush, stream, args):
+    """The whole forward captured once into a CUDA graph (the library's launches, its second
+    stream's fork and joins) and replayed: device time per step against the stream-launched
+    steps, i.e. what launch gaps cost; plus host time per launch of the two forms."""
+    import time
+
+    import torch
+
+    layer.forward(x, inp, y)  # the library's one-time setup (function attributes, occupancy) outside capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=torch.cuda.Stream()):
+        layer.forward(x, inp, y, stream=torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    dev_ms, host_graph, host_stream = [], [], []
+    for it in range(args.warmup + args.steps):
+        flush.zero_()
+        ev0.record(stream)
+        h0 = time.perf_counter()
+        g.replay()
+        h1 = time.perf_counter()
+        ev1.record(stream)
+        ev1.synchronize()
+        if it >= args.warmup:
+            dev_ms.append(ev0.elapsed_time(ev1))
+            host_graph.append((h1 - h0) * 1e3)
+    for it in range(args.steps):
+        torch.cuda.synchronize()
+        h0 = time.perf_counter()
+        layer.forward(x, inp, y)
+        host_stream.append((time.perf_counter() - h0) * 1e3)
+    torch.cuda.synchronize()
+    if layer.status() != 0:
+        raise RuntimeError("graph replay reported an error status")
+    del g
+    return {"ms_per_step": sum(dev_ms) / len(dev_ms), "host_ms_per_launch": sum(host_graph) / len(host_graph),
+            "host_ms_per_stream_forward": sum(host_stream) / len(host_stream),
+            "rule": "device time of a replay of the captured forward (events on the launching stream)"}
 
 
 EP_WORKLOAD = "k3_mxfp4_prefill_mild"  # routing of the mildly skewed K3 prefill (T=8192, E=896, k=16)
@@ -642,6 +690,8 @@ def main():
             "clocks": head["clocks"], "peaks": peaks}
     if "cpu_baseline" in head:
         line["cpu_baseline"] = head["cpu_baseline"]
+    if "graph" in head:
+        line["graph"] = head["graph"]
     if subs:
         line["workloads"] = subs
         line["ep_emulation"] = measure_ep(args, dev)

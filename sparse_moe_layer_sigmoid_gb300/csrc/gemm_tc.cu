@@ -455,9 +455,19 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float* __restr
     const int64_t col = GLU ? (int64_t)(f / 128) * 256 + f % 128 : f;
     const float* src = part + (int64_t)row * ldp + col;
     float g = 0.f, u = 0.f;
-    for (int sp = 0; sp < splits; ++sp) {
-      g += src[sp * split_stride];
-      if (GLU) u += src[sp * split_stride + 128];
+    for (int sp0 = 0; sp0 < splits; sp0 += 8) {  // eight splits' loads in flight, added in split order
+      float a[8], b[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        a[q] = sp0 + q < splits ? src[(sp0 + q) * split_stride] : 0.f;
+        b[q] = GLU && sp0 + q < splits ? src[(sp0 + q) * split_stride + 128] : 0.f;
+      }
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        if (sp0 + q < splits) {
+          g += a[q];
+          if (GLU) u += b[q];
+        }
     }
     v[e] = GLU ? silu(g) * u : g;
   }

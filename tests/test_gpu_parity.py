@@ -219,6 +219,35 @@ def test_second_stream_matches_one_stream(binding, cfg):
     layer.close()
 
 
+@pytest.mark.parametrize("cfg", [replace(SMALL_BF16, name="graph_decode_mx", routed_w="mxfp4", latent=512,
+                                         hidden=512, experts=24, tokens=40, seed=45),
+                                 replace(SMALL_BF16, name="graph_prefill", tokens=300, seed=46)],
+                         ids=lambda c: c.name)
+def test_forward_captured_in_a_cuda_graph(binding, cfg):
+    """The forward (every launch, the second stream's fork and joins) captures into one CUDA
+    graph; replays compute what stream launches compute, bit for bit, for new contents of x."""
+    dev = torch.device("cuda")
+    inp = device_inputs(cfg, dev, False)
+    layer = binding.LatentMoE(cfg)
+    x = inp["x"].clone()
+    y = torch.empty((cfg.tokens, layer.out_width), dtype=x.dtype, device=dev)
+    layer.forward(x, inp, y)  # one-time setup outside the capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=torch.cuda.Stream()):
+        layer.forward(x, inp, y, stream=torch.cuda.current_stream())
+    for seed in (1, 2):
+        x.copy_(torch.randn(x.shape, generator=torch.Generator().manual_seed(seed)).to(x.dtype).to(dev))
+        g.replay()
+        torch.cuda.synchronize()
+        y_graph = y.clone()
+        y_stream = layer.forward(x, inp)
+        assert layer.status() == 0
+        assert torch.equal(y_graph, y_stream)
+    del g
+    layer.close()
+
+
 @pytest.mark.parametrize("cfg", [SMALL_BF16, replace(SMALL_BF16, name="pair_grouped", tokens=700, experts=8,
                                                       bias="normal1.5", seed=41)], ids=lambda c: c.name)
 def test_cta_pair_gemms_match_single_cta(binding, cfg):
