@@ -465,6 +465,7 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ log
 }
 
 constexpr int kRefineWarps = 4;  // warps of a refinement CTA
+constexpr int kTopkFusedMaxT = 512;  // batches up to this many tokens run topk_fused_kernel
 constexpr int kMaxCont = 64;     // contenders of one token: its selected experts and the band
 
 // Shared memory of one refinement group (a warp, or the whole CTA): the token's contenders.
@@ -499,98 +500,84 @@ __device__ __forceinline__ double from_orderable64(uint64_t u) {
 // differ from the fp64 evaluation's; such tokens are counted).
 constexpr double kNearTieGap = 1e-6;
 
-// Settle the list of token t exactly: G warps (gw = 0..G-1) cooperate.  Warp 0 of the group takes
-// pass 1's ranked list from idx (recomputing its keys and the (k+1)-th key), and lists the token's
-// contenders in shared memory: the selected experts and, when the boundary is uncertain, the band
-// of experts that may cross it; those whose order is uncertain (the band; selected experts with a
-// neighbouring rank closer than the key uncertainty) are recomputed.  The G warps compute their
-// logits to ~44 bits, warp gw over the 256-element blocks gw, gw + G, ... of d; warp 0 sums the G
-// partials in a fixed order, takes fp64 keys, checks each recomputed logit against the GEMM's (an
-// error above half the margin is reported) and ranks the contenders (two per lane) by key, exact
-// where recomputed.  A token whose exact k-th and (k+1)-th keys differ by less than kNearTieGap
-// is counted in *near_ties.  More than kMaxCont contenders (dozens of experts within the key
-// uncertainty of the boundary) is reported as a device check and ranks the first kMaxCont.
-template <int NPL, int G>
-__device__ __forceinline__ void refine_token(const float* __restrict__ logits, const float* __restrict__ bias,
-                                             const RouterSrc& src, int t, int E, int k, int32_t* __restrict__ idx,
-                                             float* __restrict__ p, int gw, int lane, const RefineSmem& sm,
-                                             uint32_t* status, int32_t* near_ties) {
+// Settle the list of token t exactly: G warps (gw = 0..G-1) cooperate.  Warp 0 lists the
+// token's contenders in shared memory (build_contenders): the selected experts and, when the
+// boundary is uncertain, the band of experts that may cross it; those whose order is uncertain
+// (the band; selected experts with a neighbouring rank closer than the key uncertainty) are
+// recomputed.  The G warps compute their logits to ~44 bits, warp gw over the 256-element blocks
+// gw, gw + G, ... of d; warp 0 sums the G partials in a fixed order, takes fp64 keys, checks each
+// recomputed logit against the GEMM's (an error above half the margin is reported) and ranks the
+// contenders by key, exact where recomputed (refine_finish).  A token whose exact k-th and
+// (k+1)-th keys differ by less than kNearTieGap is counted in *near_ties.  More than kMaxCont
+// contenders (dozens of experts within the key uncertainty of the boundary) is reported as a
+// device check and ranks the first kMaxCont.
+
+// Warp 0: the contender list of a token from its keys (st.kf, st.sv), its ranked list (st.my_e /
+// my_kf on lanes < k), the k-th / (k+1)-th keys and 2 eta.
+template <int NPL>
+__device__ __forceinline__ void build_contenders(const TopkState<NPL>& st, float eta2, int E, int k, int lane,
+                                                 const RefineSmem& sm, uint32_t* status) {
   const uint32_t lt_mask = (1u << lane) - 1u;
-  if (gw == 0) {
-    TopkState<NPL> st;
-    topk_keys<NPL>(logits, bias, t, E, lane, st);
-    st.my_e = lane < k ? idx[(size_t)t * k + lane] : 0;
-    st.my_s = 0.f;
-    st.my_kf = 0.f;
-    if (lane < k) expert_key(logits, bias, t, E, st.my_e, st.my_s, st.my_kf);
-    // k-th key: the last rank's; (k+1)-th: equal to it if more than k keys reach it, else the
-    // largest key below it
-    st.a_k = __shfl_sync(0xffffffffu, st.my_kf, k - 1);
-    int n_ge = 0;
-    float below = -INFINITY;
-#pragma unroll
-    for (int i = 0; i < NPL; ++i) {
-      n_ge += st.kf[i] >= st.a_k ? 1 : 0;
-      if (st.kf[i] < st.a_k && st.kf[i] > below) below = st.kf[i];
-    }
-    n_ge = (int)__reduce_add_sync(0xffffffffu, (unsigned)n_ge);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) below = fmaxf(below, __shfl_xor_sync(0xffffffffu, below, off));
-    st.a_k1 = n_ge > k ? st.a_k : below;
-    const float eta2 = 2.0f * token_eta<NPL>(st.kf, st.sv, st.a_k1, src);
-    const bool uncertain = k < E && st.a_k - st.a_k1 < eta2;
-    // ranks whose order against a neighbouring rank (or, for the last, against the experts below
-    // an uncertain boundary) is not certain
-    const float prev = __shfl_up_sync(0xffffffffu, st.my_kf, 1);
-    const float next = __shfl_down_sync(0xffffffffu, st.my_kf, 1);
-    const int close = lane < k && ((lane > 0 && prev - st.my_kf < eta2) || (lane + 1 < k && st.my_kf - next < eta2) ||
-                                   (lane == k - 1 && uncertain));
-    uint32_t sel = 0, pend = 0;  // bit i: expert lane + 32 i is selected / awaits recomputation
-    for (int j = 0; j < k; ++j) {
-      const int e = __shfl_sync(0xffffffffu, st.my_e, j);
-      const int c = __shfl_sync(0xffffffffu, close, j);
-      if ((e & 31) == lane) {
-        sel |= 1u << (e >> 5);
-        if (c) pend |= 1u << (e >> 5);
-      }
-    }
-    if (uncertain) {  // the band: every expert that may cross the boundary
-      const float hi = st.a_k + eta2, lo = st.a_k1 - eta2;
-#pragma unroll
-      for (int i = 0; i < NPL; ++i) {
-        const int e = lane + 32 * i;
-        if (e < E && st.kf[i] >= lo && st.kf[i] <= hi) pend |= 1u << i;
-      }
-    }
-    // contenders into shared memory (slot-major, then lane: a fixed order)
-    int cnt = 0, nrc = 0;
-#pragma unroll
-    for (int i = 0; i < NPL; ++i) {
-      const bool c = ((sel | pend) >> i) & 1u;
-      const uint32_t m = __ballot_sync(0xffffffffu, c);
-      const int at = cnt + __popc(m & lt_mask);
-      const bool in = c && at < kMaxCont;
-      const bool r = in && ((pend >> i) & 1u);
-      const uint32_t mr = __ballot_sync(0xffffffffu, r);
-      if (in) {
-        sm.ce[at] = lane + 32 * i;
-        sm.key[at] = orderable64((double)st.kf[i]);
-        sm.s[at] = st.sv[i];
-        sm.exa[at] = 0;
-        if (r) sm.cand[nrc + __popc(mr & lt_mask)] = at;
-      }
-      cnt += __popc(m);
-      nrc += __popc(mr);
-    }
-    if (cnt > kMaxCont) {  // the first kMaxCont are ranked; the result is not exact
-      if (lane == 0) report(status, kStatusDeviceCheck);
-      cnt = kMaxCont;
-    }
-    if (lane == 0) {
-      sm.n[0] = cnt;
-      sm.n[1] = nrc;
+  const bool uncertain = k < E && st.a_k - st.a_k1 < eta2;
+  // ranks whose order against a neighbouring rank (or, for the last, against the experts below
+  // an uncertain boundary) is not certain
+  const float prev = __shfl_up_sync(0xffffffffu, st.my_kf, 1);
+  const float next = __shfl_down_sync(0xffffffffu, st.my_kf, 1);
+  const int close = lane < k && ((lane > 0 && prev - st.my_kf < eta2) || (lane + 1 < k && st.my_kf - next < eta2) ||
+                                 (lane == k - 1 && uncertain));
+  uint32_t sel = 0, pend = 0;  // bit i: expert lane + 32 i is selected / awaits recomputation
+  for (int j = 0; j < k; ++j) {
+    const int e = __shfl_sync(0xffffffffu, st.my_e, j);
+    const int c = __shfl_sync(0xffffffffu, close, j);
+    if ((e & 31) == lane) {
+      sel |= 1u << (e >> 5);
+      if (c) pend |= 1u << (e >> 5);
     }
   }
+  if (uncertain) {  // the band: every expert that may cross the boundary
+    const float hi = st.a_k + eta2, lo = st.a_k1 - eta2;
+#pragma unroll
+    for (int i = 0; i < NPL; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E && st.kf[i] >= lo && st.kf[i] <= hi) pend |= 1u << i;
+    }
+  }
+  // contenders into shared memory (slot-major, then lane: a fixed order)
+  int cnt = 0, nrc = 0;
+#pragma unroll
+  for (int i = 0; i < NPL; ++i) {
+    const bool c = ((sel | pend) >> i) & 1u;
+    const uint32_t m = __ballot_sync(0xffffffffu, c);
+    const int at = cnt + __popc(m & lt_mask);
+    const bool in = c && at < kMaxCont;
+    const bool r = in && ((pend >> i) & 1u);
+    const uint32_t mr = __ballot_sync(0xffffffffu, r);
+    if (in) {
+      sm.ce[at] = lane + 32 * i;
+      sm.key[at] = orderable64((double)st.kf[i]);
+      sm.s[at] = st.sv[i];
+      sm.exa[at] = 0;
+      if (r) sm.cand[nrc + __popc(mr & lt_mask)] = at;
+    }
+    cnt += __popc(m);
+    nrc += __popc(mr);
+  }
+  if (cnt > kMaxCont) {  // the first kMaxCont are ranked; the result is not exact
+    if (lane == 0) report(status, kStatusDeviceCheck);
+    cnt = kMaxCont;
+  }
+  if (lane == 0) {
+    sm.n[0] = cnt;
+    sm.n[1] = nrc;
+  }
+}
+
+// All G warps: recompute the listed logits, then warp 0 ranks the contenders and writes the list.
+template <int NPL, int G>
+__device__ __forceinline__ void refine_finish(const float* __restrict__ logits, const float* __restrict__ bias,
+                                              const RouterSrc& src, int t, int E, int k, int32_t* __restrict__ idx,
+                                              float* __restrict__ p, int gw, int lane, const RefineSmem& sm,
+                                              uint32_t* status, int32_t* near_ties) {
   group_sync<G>();
   const int n_cont = sm.n[0], n_rc = sm.n[1];
   for (int b0 = 0; b0 < n_rc; b0 += kCandBatch) {
@@ -650,6 +637,38 @@ __device__ __forceinline__ void refine_token(const float* __restrict__ logits, c
   group_sync<G>();  // the contender list of this token is read by every warp before the next token's
 }
 
+// Pass 2 for one listed token: warp 0 reloads its keys and pass 1's ranked list from idx.
+template <int NPL, int G>
+__device__ __forceinline__ void refine_token(const float* __restrict__ logits, const float* __restrict__ bias,
+                                             const RouterSrc& src, int t, int E, int k, int32_t* __restrict__ idx,
+                                             float* __restrict__ p, int gw, int lane, const RefineSmem& sm,
+                                             uint32_t* status, int32_t* near_ties) {
+  if (gw == 0) {
+    TopkState<NPL> st;
+    topk_keys<NPL>(logits, bias, t, E, lane, st);
+    st.my_e = lane < k ? idx[(size_t)t * k + lane] : 0;
+    st.my_s = 0.f;
+    st.my_kf = 0.f;
+    if (lane < k) expert_key(logits, bias, t, E, st.my_e, st.my_s, st.my_kf);
+    // k-th key: the last rank's; (k+1)-th: equal to it if more than k keys reach it, else the
+    // largest key below it
+    st.a_k = __shfl_sync(0xffffffffu, st.my_kf, k - 1);
+    int n_ge = 0;
+    float below = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < NPL; ++i) {
+      n_ge += st.kf[i] >= st.a_k ? 1 : 0;
+      if (st.kf[i] < st.a_k && st.kf[i] > below) below = st.kf[i];
+    }
+    n_ge = (int)__reduce_add_sync(0xffffffffu, (unsigned)n_ge);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) below = fmaxf(below, __shfl_xor_sync(0xffffffffu, below, off));
+    st.a_k1 = n_ge > k ? st.a_k : below;
+    build_contenders<NPL>(st, 2.0f * token_eta<NPL>(st.kf, st.sv, st.a_k1, src), E, k, lane, sm, status);
+  }
+  refine_finish<NPL, G>(logits, bias, src, t, E, k, idx, p, gw, lane, sm, status, near_ties);
+}
+
 // Pass 2: the listed tokens.  With at least one token per warp each warp settles its own tokens;
 // otherwise the 4 warps of a CTA split d for one token at a time (short lists: decode batches).
 // refine_count[0] is the list length, refine_count[1] the near-tie counter.
@@ -677,6 +696,51 @@ __global__ void __launch_bounds__(32 * kRefineWarps, 4) topk_refine_kernel(
     for (int w = blockIdx.x; w < n; w += gridDim.x)
       refine_token<NPL, kRefineWarps>(logits, bias, src, refine_list[w], E, k, idx, p, warp, lane, sm, status,
                                       near_ties);
+  }
+}
+
+// Both passes in one kernel for short batches (decode): one CTA per token.  Warp 0 runs pass 1;
+// when the token's list is uncertain it lists the contenders straight from pass 1's registers and
+// the CTA's warps settle it at once (no second launch, no reload of the keys).  refine_count[0]
+// counts the settled tokens (no list is written), refine_count[1] the near ties.
+template <int NPL>
+__global__ void __launch_bounds__(32 * kRefineWarps) topk_fused_kernel(
+    const float* __restrict__ logits, const float* __restrict__ bias, RouterSrc src, int T, int E, int k,
+    int32_t* __restrict__ idx, float* __restrict__ p, int32_t* __restrict__ refine_count, uint32_t* status) {
+  __shared__ uint64_t s_sk[64];
+  __shared__ float s_ss[64];
+  __shared__ int s_ce[kMaxCont];
+  __shared__ uint64_t s_key[kMaxCont];
+  __shared__ float s_s[kMaxCont];
+  __shared__ int s_exa[kMaxCont];
+  __shared__ int s_cand[kMaxCont];
+  __shared__ float2 s_part[kRefineWarps][kMaxCont];
+  __shared__ int s_n[2];
+  __shared__ int s_need;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const RefineSmem sm{s_ce, s_key, s_s, s_exa, s_cand, &s_part[0][0], s_n};
+  for (int t = blockIdx.x; t < T; t += gridDim.x) {
+    if (warp == 0) {
+      TopkState<NPL> st;
+      if (!topk_pass_sorted<NPL>(logits, bias, t, E, k, lane, st, s_sk, s_ss))
+        topk_pass<NPL>(logits, bias, t, E, k, lane, st, s_sk, s_ss);
+      const float eta2 = 2.0f * token_eta<NPL>(st.kf, st.sv, st.a_k1, src);
+      const float next = __shfl_down_sync(0xffffffffu, st.my_kf, 1);
+      const bool close = lane + 1 < k && st.my_kf - next < eta2;
+      const bool need = (k < E && st.a_k - st.a_k1 < eta2) || __any_sync(0xffffffffu, close);
+      if (need) {
+        if (lane == 0) atomicAdd(refine_count, 1);
+        build_contenders<NPL>(st, eta2, E, k, lane, sm, status);
+      } else {
+        topk_write(t, k, st.my_e, st.my_s, idx, p, lane);
+      }
+      if (lane == 0) s_need = need ? 1 : 0;
+    }
+    __syncthreads();
+    if (s_need)  // uniform over the CTA
+      refine_finish<NPL, kRefineWarps>(logits, bias, src, t, E, k, idx, p, warp, lane, sm, status,
+                                       refine_count + 1);
+    __syncthreads();  // shared memory is reused by the next token
   }
 }
 
@@ -731,6 +795,66 @@ __global__ void __launch_bounds__(kDispatchChunk) dispatch_count_kernel(const in
   }
 }
 
+// Per-expert row offsets, chunk bases and the four tile lists from thread e's expert total
+// (1024 threads, E <= 1024): Hillis-Steele inclusive scans over 1024 entries (fixed order,
+// integer: exact).  Returns the expert's first row.
+struct ScanSmem {
+  int *cnt, *tiles, *tiles_s, *tiles_p, *tiles_m;  // [1024] each
+};
+__device__ __forceinline__ int scan_experts(int e, int total, int E, const ScanSmem& sh, int32_t* __restrict__ offsets,
+                                            int4* __restrict__ tiles, int32_t* __restrict__ num_tiles,
+                                            int4* __restrict__ tiles_s, int32_t* __restrict__ num_tiles_s,
+                                            int4* __restrict__ tiles_p, int32_t* __restrict__ num_tiles_p,
+                                            int4* __restrict__ tiles_m, int32_t* __restrict__ num_tiles_m) {
+  const int nt = (total + kTileM - 1) / kTileM;
+  const int nts = (total + kTileS - 1) / kTileS;
+  const int ntp = (total + kTileP - 1) / kTileP;
+  const int ntm = (total + kTileMx - 1) / kTileMx;
+  sh.cnt[e] = total;
+  sh.tiles[e] = nt;
+  sh.tiles_s[e] = nts;
+  sh.tiles_p[e] = ntp;
+  sh.tiles_m[e] = ntm;
+  __syncthreads();
+  for (int off = 1; off < 1024; off <<= 1) {
+    const int a = e >= off ? sh.cnt[e - off] : 0;
+    const int b = e >= off ? sh.tiles[e - off] : 0;
+    const int c = e >= off ? sh.tiles_s[e - off] : 0;
+    const int f = e >= off ? sh.tiles_p[e - off] : 0;
+    const int m = e >= off ? sh.tiles_m[e - off] : 0;
+    __syncthreads();
+    sh.cnt[e] += a;
+    sh.tiles[e] += b;
+    sh.tiles_s[e] += c;
+    sh.tiles_p[e] += f;
+    sh.tiles_m[e] += m;
+    __syncthreads();
+  }
+  const int row0 = sh.cnt[e] - total;
+  const int tile0 = sh.tiles[e] - nt;
+  const int tile0s = sh.tiles_s[e] - nts;
+  const int tile0p = sh.tiles_p[e] - ntp;
+  const int tile0m = sh.tiles_m[e] - ntm;
+  if (e < E) {
+    offsets[e] = row0;
+    for (int j = 0; j < nt; ++j) tiles[tile0 + j] = make_int4(e, tile0, total, row0);
+    if (tiles_s)
+      for (int j = 0; j < nts; ++j) tiles_s[tile0s + j] = make_int4(e, row0 + kTileS * j, min(kTileS, total - kTileS * j), 0);
+    if (tiles_p)
+      for (int j = 0; j < ntp; ++j) tiles_p[tile0p + j] = make_int4(e, tile0p, total, row0);
+    if (tiles_m)
+      for (int j = 0; j < ntm; ++j) tiles_m[tile0m + j] = make_int4(e, tile0m, total, row0);
+  }
+  if (e == E - 1) {
+    offsets[E] = sh.cnt[e];
+    *num_tiles = sh.tiles[e];
+    if (num_tiles_s) *num_tiles_s = sh.tiles_s[e];
+    if (num_tiles_p) *num_tiles_p = sh.tiles_p[e];
+    if (num_tiles_m) *num_tiles_m = sh.tiles_m[e];
+  }
+  return row0;
+}
+
 __global__ void __launch_bounds__(1024) dispatch_scan_kernel(const int32_t* __restrict__ chunk_counts,
                                                              int nchunks, int E, int32_t* __restrict__ chunk_base,
                                                              int32_t* __restrict__ offsets, int4* __restrict__ tiles,
@@ -741,66 +865,60 @@ __global__ void __launch_bounds__(1024) dispatch_scan_kernel(const int32_t* __re
                                                              int32_t* __restrict__ num_tiles_p,
                                                              int4* __restrict__ tiles_m,
                                                              int32_t* __restrict__ num_tiles_m) {
-  __shared__ int s_cnt[1024];
-  __shared__ int s_tiles[1024];
-  __shared__ int s_tiles_s[1024];
-  __shared__ int s_tiles_p[1024];
-  __shared__ int s_tiles_m[1024];
+  __shared__ int s_cnt[1024], s_tiles[1024], s_tiles_s[1024], s_tiles_p[1024], s_tiles_m[1024];
+  const ScanSmem sh{s_cnt, s_tiles, s_tiles_s, s_tiles_p, s_tiles_m};
   const int e = threadIdx.x;
   int total = 0;
   if (e < E)
     for (int c = 0; c < nchunks; ++c) total += chunk_counts[(size_t)c * E + e];
-  const int nt = (total + kTileM - 1) / kTileM;
-  const int nts = (total + kTileS - 1) / kTileS;
-  const int ntp = (total + kTileP - 1) / kTileP;
-  const int ntm = (total + kTileMx - 1) / kTileMx;
-  s_cnt[e] = total;
-  s_tiles[e] = nt;
-  s_tiles_s[e] = nts;
-  s_tiles_p[e] = ntp;
-  s_tiles_m[e] = ntm;
-  __syncthreads();
-  // Hillis-Steele inclusive scans over 1024 entries (fixed order, integer: exact).
-  for (int off = 1; off < 1024; off <<= 1) {
-    const int a = e >= off ? s_cnt[e - off] : 0;
-    const int b = e >= off ? s_tiles[e - off] : 0;
-    const int c = e >= off ? s_tiles_s[e - off] : 0;
-    const int f = e >= off ? s_tiles_p[e - off] : 0;
-    const int m = e >= off ? s_tiles_m[e - off] : 0;
-    __syncthreads();
-    s_cnt[e] += a;
-    s_tiles[e] += b;
-    s_tiles_s[e] += c;
-    s_tiles_p[e] += f;
-    s_tiles_m[e] += m;
-    __syncthreads();
-  }
-  const int row0 = s_cnt[e] - total;
-  const int tile0 = s_tiles[e] - nt;
-  const int tile0s = s_tiles_s[e] - nts;
-  const int tile0p = s_tiles_p[e] - ntp;
-  const int tile0m = s_tiles_m[e] - ntm;
+  const int row0 = scan_experts(e, total, E, sh, offsets, tiles, num_tiles, tiles_s, num_tiles_s, tiles_p,
+                                num_tiles_p, tiles_m, num_tiles_m);
   if (e < E) {
-    offsets[e] = row0;
     int run = row0;
     for (int c = 0; c < nchunks; ++c) {
       chunk_base[(size_t)c * E + e] = run;
       run += chunk_counts[(size_t)c * E + e];
     }
-    for (int j = 0; j < nt; ++j) tiles[tile0 + j] = make_int4(e, tile0, total, row0);
-    if (tiles_s)
-      for (int j = 0; j < nts; ++j) tiles_s[tile0s + j] = make_int4(e, row0 + kTileS * j, min(kTileS, total - kTileS * j), 0);
-    if (tiles_p)
-      for (int j = 0; j < ntp; ++j) tiles_p[tile0p + j] = make_int4(e, tile0p, total, row0);
-    if (tiles_m)
-      for (int j = 0; j < ntm; ++j) tiles_m[tile0m + j] = make_int4(e, tile0m, total, row0);
   }
-  if (e == E - 1) {
-    offsets[E] = s_cnt[e];
-    *num_tiles = s_tiles[e];
-    if (num_tiles_s) *num_tiles_s = s_tiles_s[e];
-    if (num_tiles_p) *num_tiles_p = s_tiles_p[e];
-    if (num_tiles_m) *num_tiles_m = s_tiles_m[e];
+}
+
+// Batches of one dispatch chunk (T <= 256, E <= 1024): count, scan and scatter in one CTA, the
+// same arithmetic as the three-kernel path (masks of the chunk's tokens per expert, stable ranks).
+__global__ void __launch_bounds__(1024) dispatch_small_kernel(
+    const int32_t* __restrict__ idx, const float* __restrict__ p, int T, int E, int k, int32_t* __restrict__ offsets,
+    int4* __restrict__ tiles, int32_t* __restrict__ num_tiles, int4* __restrict__ tiles_s,
+    int32_t* __restrict__ num_tiles_s, int4* __restrict__ tiles_p, int32_t* __restrict__ num_tiles_p,
+    int4* __restrict__ tiles_m, int32_t* __restrict__ num_tiles_m, int32_t* __restrict__ tok_of_row,
+    int32_t* __restrict__ row_of, float* __restrict__ p_row, uint32_t* status) {
+  extern __shared__ uint32_t mask[];  // [E][kMaskWords]
+  __shared__ int s_cnt[1024], s_tiles[1024], s_tiles_s[1024], s_tiles_p[1024], s_tiles_m[1024], s_row0[1024];
+  const ScanSmem sh{s_cnt, s_tiles, s_tiles_s, s_tiles_p, s_tiles_m};
+  build_masks(idx, T, E, k, mask, status);  // thread t < T is token t
+  const int e = threadIdx.x;
+  int total = 0;
+  if (e < E)
+#pragma unroll
+    for (int w = 0; w < kMaskWords; ++w) total += __popc(mask[e * kMaskWords + w]);
+  s_row0[e] = scan_experts(e, total, E, sh, offsets, tiles, num_tiles, tiles_s, num_tiles_s, tiles_p, num_tiles_p,
+                           tiles_m, num_tiles_m);
+  __syncthreads();
+  const int t = threadIdx.x;
+  if (t >= T) return;
+  const int w = t >> 5;
+  const uint32_t below = (1u << (t & 31)) - 1u;
+  for (int j = 0; j < k; ++j) {
+    const int ex = idx[(size_t)t * k + j];
+    if (ex < 0 || ex >= E) {
+      if (row_of) row_of[(size_t)t * k + j] = -1;
+      continue;
+    }
+    const uint32_t* m = mask + ex * kMaskWords;
+    int rank = __popc(m[w] & below);
+    for (int q = 0; q < w; ++q) rank += __popc(m[q]);
+    const int row = s_row0[ex] + rank;
+    if (row_of) row_of[(size_t)t * k + j] = row;
+    if (tok_of_row) tok_of_row[row] = t;
+    if (p_row) p_row[row] = p ? p[(size_t)t * k + j] : 1.0f;
   }
 }
 
@@ -960,16 +1078,24 @@ cudaError_t launch_topk(const float* logits, const float* bias, const RouterSrc&
                         int32_t* idx, float* p, int32_t* refine_list, int32_t* refine_count, uint32_t* status,
                         int num_sms, cudaStream_t s) {
   cudaError_t e = cudaMemsetAsync(refine_count, 0, 2 * sizeof(int32_t), s);
-  if (e != cudaSuccess) return e;
+  if (e != cudaSuccess || T <= 0) return e;
   const int warps_per_block = 8;
   dim3 grid((T + warps_per_block - 1) / warps_per_block), block(32 * warps_per_block);
   const int rgrid = 4 * num_sms;  // the residency the launch bounds give
+  // short batches: both passes in one kernel, a CTA per token (the latency of one token's
+  // selection and refinement, not the throughput of many, sets the time)
+  const bool fused = T <= kTopkFusedMaxT;
   const int npl = (E + 31) / 32;
 #define LMOE_TOPK(N)                                                                                     \
   do {                                                                                                   \
-    topk_kernel<N><<<grid, block, 0, s>>>(logits, bias, src, T, E, k, idx, p, refine_list, refine_count); \
-    topk_refine_kernel<N><<<rgrid, 128, 0, s>>>(logits, bias, src, E, k, idx, p, refine_list, refine_count, \
-                                                 status);                                                         \
+    if (fused) {                                                                                         \
+      topk_fused_kernel<N><<<T, 32 * kRefineWarps, 0, s>>>(logits, bias, src, T, E, k, idx, p, refine_count, \
+                                                           status);                                       \
+    } else {                                                                                             \
+      topk_kernel<N><<<grid, block, 0, s>>>(logits, bias, src, T, E, k, idx, p, refine_list, refine_count); \
+      topk_refine_kernel<N><<<rgrid, 128, 0, s>>>(logits, bias, src, E, k, idx, p, refine_list, refine_count, \
+                                                   status);                                                       \
+    }                                                                                                    \
   } while (0)
   if (npl <= 1) LMOE_TOPK(1);
   else if (npl <= 2) LMOE_TOPK(2);
@@ -986,6 +1112,19 @@ cudaError_t launch_dispatch(const int32_t* idx, const float* p, int T, int E, in
                             uint32_t* status, int* launches, cudaStream_t s) {
   const int nchunks = (T + kDispatchChunk - 1) / kDispatchChunk;
   const size_t smem = (size_t)E * kMaskWords * sizeof(uint32_t);
+  if (nchunks == 1 && E <= 1024) {  // one chunk: one CTA does the three steps
+    // 24 KB of static scan arrays next to the masks: above 48 KB in all the opt-in is needed
+    if (smem > 16 * 1024) {
+      const cudaError_t ea =
+          cudaFuncSetAttribute(dispatch_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (ea != cudaSuccess) return ea;
+    }
+    dispatch_small_kernel<<<1, 1024, smem, s>>>(idx, p, T, E, k, b.offsets, b.tiles, b.num_tiles, b.tiles_s,
+                                                b.num_tiles_s, b.tiles_p, b.num_tiles_p, b.tiles_m, b.num_tiles_m,
+                                                b.tok_of_row, b.row_of, b.p_row, status);
+    if (launches) *launches += 1;
+    return cudaGetLastError();
+  }
   dispatch_count_kernel<<<nchunks, kDispatchChunk, smem, s>>>(idx, T, E, k, b.chunk_counts, status);
   dispatch_scan_kernel<<<1, 1024, 0, s>>>(b.chunk_counts, nchunks, E, b.chunk_base, b.offsets, b.tiles,
                                           b.num_tiles, b.tiles_s, b.num_tiles_s, b.tiles_p, b.num_tiles_p,
