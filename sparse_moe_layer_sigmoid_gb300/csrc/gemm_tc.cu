@@ -448,29 +448,32 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float* __restr
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= (int64_t)M * n4) return;
   const int row = (int)(i / n4), f0 = (int)(i - (int64_t)row * n4) * 4;
+  // the four outputs f0..f0+3 are adjacent partial columns (f0 % 4 == 0; GLU blocks of 128): one
+  // 16-byte load per split (and one for the up half), eight splits in flight, added in split order
+  const int64_t col = GLU ? (int64_t)(f0 / 128) * 256 + f0 % 128 : f0;
+  const float* src = part + (int64_t)row * ldp + col;
+  float g[4] = {0.f, 0.f, 0.f, 0.f}, u[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int sp0 = 0; sp0 < splits; sp0 += 8) {
+    float4 a[8], b[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      a[q] = sp0 + q < splits ? *reinterpret_cast<const float4*>(src + (sp0 + q) * split_stride)
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+      b[q] = GLU && sp0 + q < splits ? *reinterpret_cast<const float4*>(src + (sp0 + q) * split_stride + 128)
+                                     : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      if (sp0 + q < splits) {
+        g[0] += a[q].x; g[1] += a[q].y; g[2] += a[q].z; g[3] += a[q].w;
+        if (GLU) {
+          u[0] += b[q].x; u[1] += b[q].y; u[2] += b[q].z; u[3] += b[q].w;
+        }
+      }
+  }
   float v[4];
 #pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const int f = f0 + e;
-    const int64_t col = GLU ? (int64_t)(f / 128) * 256 + f % 128 : f;
-    const float* src = part + (int64_t)row * ldp + col;
-    float g = 0.f, u = 0.f;
-    for (int sp0 = 0; sp0 < splits; sp0 += 8) {  // eight splits' loads in flight, added in split order
-      float a[8], b[8];
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        a[q] = sp0 + q < splits ? src[(sp0 + q) * split_stride] : 0.f;
-        b[q] = GLU && sp0 + q < splits ? src[(sp0 + q) * split_stride + 128] : 0.f;
-      }
-#pragma unroll
-      for (int q = 0; q < 8; ++q)
-        if (sp0 + q < splits) {
-          g += a[q];
-          if (GLU) u += b[q];
-        }
-    }
-    v[e] = GLU ? silu(g) * u : g;
-  }
+  for (int e = 0; e < 4; ++e) v[e] = GLU ? silu(g[e]) * u[e] : g[e];
   if (EPI == kEpiF32) {
     *reinterpret_cast<float4*>(static_cast<float*>(C) + (int64_t)row * ldc + f0) = make_float4(v[0], v[1], v[2], v[3]);
   } else {
