@@ -72,6 +72,14 @@ typedef enum {
  * (kind::f16), or a CUDA-core GEMV for decode units of at most 4 rows, instead of the default
  * block-scaled kind::mxf4 MMAs on three-term MXFP4 activations.  For comparison and testing. */
 #define LMOE_FLAG_MXFP4_DEQUANT 0x4u
+/* MXFP4 experts with MXFP8 activations (bf16 layers only): the expert inputs and the GLU
+ * activations become MXFP8 records (E4M3 elements, one E8M0 scale per 32, round to nearest
+ * even, the smallest power-of-two scale that keeps every element within 448) and the expert
+ * GEMMs run tcgen05.mma kind::mxf8f6f4 (E2M1 x E4M3) -- K3's quantisation-aware-training
+ * numerics (page "What K3 actually is", srikanthmalla.com: MXFP4 weights with MXFP8
+ * activations).  A different numerics mode: it is compared with the oracle's MXFP8 mode, not
+ * with the bf16 evaluation. */
+#define LMOE_FLAG_MXFP8_ACT 0x8u
 
 typedef struct {
   int32_t d;             /* model width                                                 */
@@ -266,6 +274,11 @@ lmoe_status latentmoe_route_noalloc(const lmoe_config *cfg, const void *x, int32
  * power-of-two scale that leaves no element above 6.  Asynchronous on `stream`; allocates nothing.
  * Errors: INVALID_ARG, CUDA. */
 lmoe_status latentmoe_mx3_quantize(const void *src, int32_t src_dtype, int64_t rows, int32_t K, void *dst,
+                                   void *stream);
+
+/* Test hook: the MXFP8 records (LMOE_FLAG_MXFP8_ACT) of rows x K values, K % 512 == 0:
+ * dst [rows][K + K/32] bytes = K E4M3 codes (element i in byte i), then K/32 scale bytes. */
+lmoe_status latentmoe_mx8_quantize(const void *src, int32_t src_dtype, int64_t rows, int32_t K, void *dst,
                                    void *stream);
 
 /* Measurement hook: the dense tensor-core rate of this GPU, in TFLOP/s, for the instruction shape

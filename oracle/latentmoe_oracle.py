@@ -33,7 +33,10 @@ Pins (all in the CPU test suite): MXFP4 decode against the OCP E2M1 table for al
 x 255 scales; router/selection closed forms and a brute-force full sort; the pages'
 parameter and dispatch arithmetic; a dense all-experts-under-a-0/1-mask evaluation; scalar
 closed forms of the GLU and RMSNorm; identity-expert, zero-routed-weight and N_s=0
-reductions; token-permutation invariance.
+reductions; token-permutation invariance.  MXFP8 activation mode (K3's quantisation-aware
+numerics, page "What K3 actually is", srikanthmalla.com: MXFP4 weights with MXFP8 activations):
+the E4M3 codec against a library float8 conversion for all 256 codes, its rounding at every
+midpoint, the power-of-two block scale rule at its boundaries.
 """
 from __future__ import annotations
 
@@ -87,6 +90,47 @@ def mxfp4_decode(packed, scales) -> np.ndarray:
     values = e2m1_value(np.arange(16))[nib]
     values *= np.repeat(e8m0_value(scales), 32, axis=-1)
     return values
+
+
+def e4m3_value(code) -> np.ndarray:
+    """Value of 8-bit E4M3 codes (OCP 8-bit floating point, E4M3): bit 7 sign, bits 6..3
+    exponent (bias 7), bits 2..0 mantissa; exponent 0 is subnormal (mantissa * 2^-9); exponent
+    15 with mantissa 7 is NaN (no infinities; largest finite 448)."""
+    code = np.asarray(code, dtype=np.int64)
+    sign = np.where((code >> 7) & 1, -1.0, 1.0)
+    ex = (code >> 3) & 15
+    man = code & 7
+    mag = np.where(ex == 0, np.ldexp(man.astype(np.float64), -9), np.ldexp(1.0 + man / 8.0, ex - 7))
+    mag = np.where((ex == 15) & (man == 7), np.nan, mag)
+    return sign * mag
+
+
+def e4m3_round(v) -> np.ndarray:
+    """v rounded to the nearest E4M3 value, ties to the even code, |result| <= 448."""
+    v = np.asarray(v, dtype=np.float64)
+    a = np.minimum(np.abs(v), 448.0)
+    with np.errstate(divide="ignore"):
+        e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    # grid spacing: 2^-9 in the subnormal range (below 2^-6), else 2^(e-3) (3 mantissa bits)
+    step = np.where(a < 2.0 ** -6, 2.0 ** -9, np.ldexp(1.0, (np.maximum(e, -6) - 3).astype(np.int64)))
+    q = np.round(a / step) * step  # numpy rounds halves to even: the even multiple is the even code
+    return np.sign(v) * np.minimum(q, 448.0)
+
+
+def mxfp8_quantize(v) -> np.ndarray:
+    """Values of the MXFP8 encoding of rows v [..., K] (K % 32 == 0): per 32-element block the
+    scale is the smallest power of two s with max|v| <= 448 s (E8M0 exponent clamped to
+    [-126, 126]; an all-zero block gives zeros), each element E4M3(v / s) * s."""
+    v = np.asarray(v, dtype=np.float64)
+    blk = v.reshape(v.shape[:-1] + (v.shape[-1] // 32, 32))
+    amax = np.max(np.abs(blk), axis=-1, keepdims=True)
+    with np.errstate(divide="ignore"):
+        ex = np.ceil(np.log2(np.where(amax > 0, amax / 448.0, 1.0)))
+    ex = np.clip(ex, -126, 126)
+    s = np.ldexp(1.0, ex.astype(np.int64))
+    q = e4m3_round(blk / s) * s
+    q = np.where(amax > 0, q, 0.0)
+    return q.reshape(v.shape)
 
 
 def weight_values(w, scale=None) -> np.ndarray:
@@ -191,6 +235,15 @@ def glu_expert(v, gate_up, down, hidden):
     return a @ down.T
 
 
+def glu_expert_mxfp8(v, gate_up, down, hidden):
+    """The GLU expert with MXFP8 activations: its input rows and its GLU activations are
+    quantised (mxfp8_quantize) before the products that read them."""
+    gate, up = gate_up[:hidden], gate_up[hidden:]
+    vq = mxfp8_quantize(v)
+    a = silu(vq @ gate.T) * (vq @ up.T)
+    return mxfp8_quantize(a) @ down.T
+
+
 def rmsnorm(u, gain, eps):
     """n = u * g / sqrt(mean(u^2) + eps), per row."""
     ms = np.mean(u * u, axis=1, keepdims=True)
@@ -201,13 +254,14 @@ def rmsnorm(u, gain, eps):
 # The layer: eq. 11 with eq. 13 routing
 # ----------------------------------------------------------------------------------------
 
-def layer_forward(inp, cfg, tokens=None, routing=None):
+def layer_forward(inp, cfg, tokens=None, routing=None, act_quant=None):
     """Evaluate the layer for the token rows ``tokens`` (all rows when None).
 
     ``inp`` holds stored arrays as produced by the input generator's host copy (routed
     weights may be any object indexable by expert).  ``cfg`` supplies top_k, hidden,
     shared_hidden, n_shared, rms_eps and identity_experts.  ``routing`` optionally forces
-    (idx, p) for the evaluated rows instead of the router's choice.
+    (idx, p) for the evaluated rows instead of the router's choice.  ``act_quant="mxfp8"``:
+    the routed experts take MXFP8 activations (glu_expert_mxfp8).
 
     Returns a dict with s, idx, p, gap, z, u, and (unless identity experts) n and y.
     Rows are independent given routing, so a row subset is an exact sub-problem.
@@ -235,7 +289,8 @@ def layer_forward(inp, cfg, tokens=None, routing=None):
             t_sel, j_sel = np.nonzero(idx == e)
             gate_up = weight_values(gu_w[e], None if gu_s is None else gu_s[e])
             down = weight_values(dn_w[e], None if dn_s is None else dn_s[e])
-            out_rows[t_sel, j_sel] = glu_expert(z[t_sel], gate_up, down, cfg.hidden)
+            expert = glu_expert_mxfp8 if act_quant == "mxfp8" else glu_expert
+            out_rows[t_sel, j_sel] = expert(z[t_sel], gate_up, down, cfg.hidden)
     u = np.zeros_like(z)
     for j in range(k):                                       # sum in rank order
         u += p[:, j:j + 1] * out_rows[:, j, :]

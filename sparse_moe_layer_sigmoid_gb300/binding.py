@@ -23,6 +23,7 @@ DTYPES = {"f32": 0, "bf16": 1, "mxfp4": 2}
 LMOE_FLAG_IDENTITY_EXPERTS = 0x1
 LMOE_FLAG_SINGLE_CTA_GEMM = 0x2
 LMOE_FLAG_MXFP4_DEQUANT = 0x4
+LMOE_FLAG_MXFP8_ACT = 0x8
 LMOE_NUM_STAGES = 10
 
 
@@ -78,6 +79,8 @@ def _lib():
         lib.latentmoe_route_noalloc.restype = st
         lib.latentmoe_mx3_quantize.argtypes = [vp, i32, C.c_int64, i32, vp, vp]
         lib.latentmoe_mx3_quantize.restype = st
+        lib.latentmoe_mx8_quantize.argtypes = [vp, i32, C.c_int64, i32, vp, vp]
+        lib.latentmoe_mx8_quantize.restype = st
         lib.latentmoe_mma_peak.argtypes = [i32, C.POINTER(C.c_double), vp]
         lib.latentmoe_mma_peak.restype = st
         lib.latentmoe_route_noalloc_status.argtypes = [vp]
@@ -158,6 +161,15 @@ def mx3_quantize(x: torch.Tensor, stream=None) -> torch.Tensor:
     out = torch.empty((rows, 3 * K // 2 + 3 * K // 32), dtype=torch.uint8, device=x.device)
     dt = {torch.bfloat16: 1, torch.float16: 3}[x.dtype]
     _check(_lib().latentmoe_mx3_quantize(_ptr(x), dt, rows, K, _ptr(out), _stream(stream)), "mx3_quantize")
+    return out
+
+
+def mx8_quantize(x: torch.Tensor, stream=None) -> torch.Tensor:
+    """MXFP8 records of the rows of x (bf16 or fp16 [rows][K]) as uint8 [rows][K + K/32]."""
+    rows, K = x.shape
+    out = torch.empty((rows, K + K // 32), dtype=torch.uint8, device=x.device)
+    dt = {torch.bfloat16: 1, torch.float16: 3}[x.dtype]
+    _check(_lib().latentmoe_mx8_quantize(_ptr(x), dt, rows, K, _ptr(out), _stream(stream)), "mx8_quantize")
     return out
 
 

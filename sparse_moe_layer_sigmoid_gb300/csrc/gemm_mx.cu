@@ -58,17 +58,26 @@ constexpr int kEpiStride = 72;                           // floats per staged to
 // list) or 16 (decode; its 16-row unit list).  Decode tiles carry a few token rows against whole
 // weight tiles, so their stages are small and the ring is deep (eight k-blocks of weights in
 // flight per CTA instead of three): the kernel then streams weights as fast as HBM delivers them.
-template <int NT>
+//
+// F8: the token rows are MXFP8 records (one E4M3 term) and the MMA is kind::mxf8f6f4 (E2M1 x
+// E4M3, K = 32 per instruction, 8 per k-block).  That kind reads 4-bit elements from shared
+// memory one per byte: the weights land by TMA as CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B (16
+// packed elements of global memory padded to 16 bytes), two 128-element boxes per k-block, and
+// the transaction count of such a load is its packed (global) size.  Each token row's k-block is
+// two 128-byte chunks.
+template <int NT, bool F8 = false>
 struct MxCfg {
   static constexpr int kN = NT;                                      // token columns per tile (MMA N)
+  static constexpr int kTerms = F8 ? 1 : kMxTerms;                   // activation terms per record
   static constexpr int kXRows = NT / 2;                              // token rows per CTA
-  static constexpr uint32_t kXTermBytes = kXRows * 128;              // one term's rows of a k-block
-  static constexpr uint32_t kStageBytes = kWBytes + kMxTerms * kXTermBytes;
-  static constexpr int kStages = NT >= 64 ? 3 : 8;
+  static constexpr uint32_t kXTermBytes = kXRows * 128;              // one term's (F8: one chunk's) rows of a k-block
+  static constexpr uint32_t kWSmem = F8 ? 2 * kWBytes : kWBytes;     // weight bytes of a k-block in shared memory
+  static constexpr uint32_t kStageBytes = kWSmem + (F8 ? 2 : kMxTerms) * kXTermBytes;
+  static constexpr int kStages = NT >= 64 ? 3 : (F8 ? 5 : 8);
   // scale ring: per stage the scale bytes of two k-blocks (16 bytes of each row): this CTA's weight
   // rows, and all NT token rows of each term (both CTAs' MMA halves read every token row)
   static constexpr uint32_t kXsTermBytes = NT * 16;
-  static constexpr uint32_t kSfStageBytes = kWsBytes + kMxTerms * kXsTermBytes;
+  static constexpr uint32_t kSfStageBytes = kWsBytes + kTerms * kXsTermBytes;
   static constexpr int kSfStages = NT >= 64 ? 3 : 4;
   // token boxes sized to the tile: 8, 32 or 96 rows of each term per CTA (tiles of N <= 16, <= 64,
   // <= 192 tokens) and 16, 64 or 192 rows of their scales
@@ -81,7 +90,7 @@ struct MxCfg {
   // slot start: the MMA reads its scale operands at such aligned addresses only.
   // decode: N = 3 * 16 token-term columns, CTA c providing rows 24 c + 8 q + j' (term q of token
   // 8 c + j'), the three terms of a k-block being contiguous 8-row swizzle atoms in its stage
-  static constexpr bool kTermsInN = NT < 32;
+  static constexpr bool kTermsInN = !F8 && NT < 32;
   static constexpr int kMmaN = kTermsInN ? kMxTerms * NT : NT;
   static constexpr uint32_t kAccCols = kTermsInN ? 64 : (NT >= 32 ? NT : 32);
   static constexpr uint32_t kChunkCols = 8;
@@ -99,9 +108,11 @@ struct MxCfg {
   static_assert(kSmem <= 227 * 1024, "shared memory budget");
   static_assert(kEpiBytes >= 4 * 32 * 32 * 2, "down epilogue staging");
   static_assert(!kTermsInN || (NT == 16 && kXTermBytes == 1024 && kMmaN <= 64), "decode: terms as 8-row atoms");
+  static_assert(kStageBytes % 1024 == 0 && kXTermBytes % 1024 == 0, "swizzle atoms stay 1024-byte aligned");
 };
 static_assert(MxCfg<192>::kN == kTileMx, "the dispatch cuts expert rows into tiles of this kernel's width");
 static_assert(MxCfg<16>::kN == kTileS, "decode units are the dispatch's 16-row units");
+static_assert(MxCfg<192, true>::kN == kTileMx && MxCfg<16, true>::kN == kTileS, "MXFP8 tiles: the same lists");
 __host__ __device__ constexpr int x_box_rows(int NT, int b) {
   return NT < 64 ? NT / 2 : (b == 0 ? 8 : b == 1 ? 32 : NT / 2);
 }
@@ -181,14 +192,14 @@ __device__ __forceinline__ void load_acc(uint32_t taddr, uint32_t (&r)[32]) {
 // Epilogue-warp barrier (the 4 epilogue warps only).
 __device__ __forceinline__ void epi_barrier() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
-template <bool GLU, int NT>
+template <bool GLU, int NT, bool F8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tc_mx_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmWs,
                  const __grid_constant__ CUtensorMap tmX0, const __grid_constant__ CUtensorMap tmX1,
                  const __grid_constant__ CUtensorMap tmX2, const __grid_constant__ CUtensorMap tmXs0,
                  const __grid_constant__ CUtensorMap tmXs1, const __grid_constant__ CUtensorMap tmXs2,
                  const MxParams p) {
-  using C = MxCfg<NT>;
+  using C = MxCfg<NT, F8>;
   constexpr int kStages = C::kStages, kSfStages = C::kSfStages, kSfSlots = C::kSfSlots;
   constexpr uint32_t kStageBytes = C::kStageBytes, kXTermBytes = C::kXTermBytes, kSfStageBytes = C::kSfStageBytes;
   constexpr uint32_t kXsTermBytes = C::kXsTermBytes, kEpiBytes = C::kEpiBytes, kSfBase = C::kSfBase;
@@ -271,8 +282,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const int bsel = C::kNumBoxes == 1 ? 0 : box_for(ti.n);
       const CUtensorMap* tmX = bsel == 0 ? &tmX0 : bsel == 1 ? &tmX1 : &tmX2;
       const CUtensorMap* tmXs = bsel == 0 ? &tmXs0 : bsel == 1 ? &tmXs1 : &tmXs2;
-      const uint32_t stage_tx = kWBytes + kMxTerms * (uint32_t)x_box_rows(NT, bsel) * 128u;
-      const uint32_t sf_tx = kWsBytes + kMxTerms * (uint32_t)(2 * x_box_rows(NT, bsel)) * 16u;
+      // bytes a stage's loads deliver: weights (F8: counted packed), token rows of each term or chunk
+      const uint32_t stage_tx = kWBytes + (F8 ? 2u : (uint32_t)kMxTerms) * (uint32_t)x_box_rows(NT, bsel) * 128u;
+      const uint32_t sf_tx = kWsBytes + (uint32_t)C::kTerms * (uint32_t)(2 * x_box_rows(NT, bsel)) * 16u;
       for (int kb = 0; kb < p.num_kb; ++kb, ++iter) {
         if ((kb & 1) == 0) {
           // scale bytes of k-blocks kb, kb+1 (16 bytes of every row) into this CTA's scale ring
@@ -288,7 +300,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           else
             ptx::tma_load_3d(ss, &tmWs, &sfr_full[sstage], xb, wrow, ti.expert);
 #pragma unroll
-          for (int q = 0; q < kMxTerms; ++q)
+          for (int q = 0; q < C::kTerms; ++q)
             ptx::tma_load_2d(ss + kWsBytes + q * kXsTermBytes, tmXs, &sfr_full[sstage], q * (p.K / 32) + xb,
                              ti.row0);
           if (++sstage == kSfStages) {
@@ -301,7 +313,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // the MMA read both CTAs' copy of this stage: pass the release on to the partner
         if (rank == 0 && iter >= kStages) ptx::mbar_arrive_remote(&empty[stage], 1);
         uint8_t* sW = smem + stage * kStageBytes;
-        uint8_t* sX = sW + kWBytes;
+        uint8_t* sX = sW + C::kWSmem;  // F8: the weight chunks take 2 x kWBytes
         const uint32_t bar = ptx::mapa_shared(&full[stage], 0);  // the even CTA's full[stage]
         const bool skip = p.inject && first && pair == 0;  // test hook, the same in both CTAs
         first = false;
@@ -310,13 +322,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             ptx::mbar_arrive_expect_tx(&full[stage], 2 * stage_tx);
             armed.arm(stage, phase);
           }
-          if (GLU)  // 4 x (16 gate rows, 16 up rows) of features wt*128 + rank*64 ..
-            ptx::tma_load_5d_pair(sW, &tmW, bar, kb * 128, 0, 0, wrow_glu, ti.expert);
-          else
-            ptx::tma_load_3d_pair(sW, &tmW, bar, kb * 128, wrow, ti.expert);
+          if (F8) {  // two 128-element weight chunks (padded to a byte each), two 128-byte token chunks
 #pragma unroll
-          for (int q = 0; q < kMxTerms; ++q)  // term q: 96 rows x 128 bytes at byte q * K/2 + kb * 128 of each record
-            ptx::tma_load_2d_pair(sX + q * kXTermBytes, tmX, bar, q * (p.K / 2) + kb * 128, xrow0);
+            for (int c = 0; c < 2; ++c) {
+              if (GLU)
+                ptx::tma_load_5d_pair(sW + c * kWBytes, &tmW, bar, kb * 256 + c * 128, 0, 0, wrow_glu, ti.expert);
+              else
+                ptx::tma_load_3d_pair(sW + c * kWBytes, &tmW, bar, kb * 256 + c * 128, wrow, ti.expert);
+              ptx::tma_load_2d_pair(sX + c * kXTermBytes, tmX, bar, kb * 256 + c * 128, xrow0);
+            }
+          } else {
+            if (GLU)  // 4 x (16 gate rows, 16 up rows) of features wt*128 + rank*64 ..
+              ptx::tma_load_5d_pair(sW, &tmW, bar, kb * 128, 0, 0, wrow_glu, ti.expert);
+            else
+              ptx::tma_load_3d_pair(sW, &tmW, bar, kb * 128, wrow, ti.expert);
+#pragma unroll
+            for (int q = 0; q < kMxTerms; ++q)  // term q: 96 rows x 128 bytes at byte q * K/2 + kb * 128 of each record
+              ptx::tma_load_2d_pair(sX + q * kXTermBytes, tmX, bar, q * (p.K / 2) + kb * 128, xrow0);
+          }
         }
         if (++stage == kStages) {
           stage = 0;
@@ -348,8 +371,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           goto done;
         ptx::tc_fence_after();
         const uint32_t w_addr = ptx::smem_addr(smem + s * kStageBytes);
-        const uint32_t x_addr = w_addr + kWBytes;
+        const uint32_t x_addr = w_addr + C::kWSmem;
         const uint32_t sf = tmem_base + kSfBase + (uint32_t)slot * kSfCols;
+        if (F8) {  // 8 MMAs of K = 32: chunk c = kk / 4, scale byte kk % 4 of the chunk's columns
+#pragma unroll
+          for (int kk = 0; kk < KB / 32; ++kk) {
+            const uint32_t c = (uint32_t)(kk >> 2), sub = (uint32_t)(kk & 3);
+            ptx::mma_mxf8f6f4_pair(d_tmem, ptx::sw128_kmajor_desc(w_addr + c * kWBytes + sub * 32),
+                                   ptx::sw128_kmajor_desc(x_addr + c * kXTermBytes + sub * 32),
+                                   ptx::idesc_mxf8f6f4_e2m1_e4m3(2 * kWRows, ti.n, sub, sub), sf + 4u * c,
+                                   sf + 8u + kChunkCols * c, (kb | kk) != 0 ? 1u : 0u);
+          }
+        } else {
 #pragma unroll
         for (int kk = 0; kk < KB / 64; ++kk) {
           const uint32_t sf_id = 2u * (uint32_t)(kk & 1);
@@ -367,6 +400,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                  sf + 8u + 2u * kChunkCols * (uint32_t)q + kChunkCols * (uint32_t)(kk >> 1),
                                  (kb | kk | q) != 0 ? 1u : 0u);
           }
+        }
         }
         ptx::mma_commit_pair(&empty[s]);
         ptx::mma_commit_pair_both(&sf_empty[slot]);
@@ -403,9 +437,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           ptx::tmem_st_32x32b_x1(col + (uint32_t)q, wv.x);       // weight scale blocks 0..3 of the k-block
           ptx::tmem_st_32x32b_x1(col + 4u + (uint32_t)q, wv.y);  // blocks 4..7
           if (NT >= 32) {
-            uint32_t lo[kMxTerms][8], hi[kMxTerms][8];
+            uint32_t lo[C::kTerms][8], hi[C::kTerms][8];
 #pragma unroll
-            for (int tt = 0; tt < kMxTerms; ++tt)
+            for (int tt = 0; tt < C::kTerms; ++tt)
 #pragma unroll
               for (int c = 0; c < 8; ++c) {
                 uint2 v = make_uint2(0u, 0u);
@@ -415,10 +449,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 hi[tt][c] = v.y;
               }
 #pragma unroll
-            for (int tt = 0; tt < kMxTerms; ++tt) {
+            for (int tt = 0; tt < C::kTerms; ++tt) {
               ptx::tmem_st_32x32b_x8(col + 8u + 2u * kChunkCols * tt, lo[tt]);
               ptx::tmem_st_32x32b_x8(col + 8u + 2u * kChunkCols * tt + kChunkCols, hi[tt]);
             }
+          } else if (F8) {  // one term: token rows 0 .. NT-1 in lanes 0 .. NT-1, chunk h at 8 + 8 h
+            uint2 v = make_uint2(0u, 0u);
+            if (lane < NT) v = *reinterpret_cast<const uint2*>(st + kWsBytes + lane * 16);
+            ptx::tmem_st_32x32b_x1(col + 8u, v.x);
+            ptx::tmem_st_32x32b_x1(col + 8u + kChunkCols, v.y);
           } else {  // MMA rows n = 24 c + 8 q + j' (term q, token 8 c + j'): row n at lane n % 32,
                     // column + n / 32 of chunk h's pair of columns at 8 + 2 h kChunkCols
 #pragma unroll
@@ -523,15 +562,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 v[4 * e4 + 2] = f.z;
                 v[4 * e4 + 3] = f.w;
               }
-              uint32_t packed[kMxTerms][4], scb[kMxTerms];
-              mx::quantize_block(v, packed, scb);
               uint8_t* rec = out + (int64_t)(ti.row0 + c0 + j) * p.ldc;
               const int f = fb + 32 * b;
+              if (F8) {  // MXFP8 record: E4M3 codes at byte f, the scale after the K codes
+                uint32_t codes[8], scb8;
+                mx::quantize_block8(v, codes, scb8);
+                *reinterpret_cast<uint4*>(rec + f) = make_uint4(codes[0], codes[1], codes[2], codes[3]);
+                *reinterpret_cast<uint4*>(rec + f + 16) = make_uint4(codes[4], codes[5], codes[6], codes[7]);
+                rec[mx8_scale_offset(p.out_k) + f / 32] = (uint8_t)scb8;
+              } else {
+                uint32_t packed[kMxTerms][4], scb[kMxTerms];
+                mx::quantize_block(v, packed, scb);
 #pragma unroll
-              for (int tt = 0; tt < kMxTerms; ++tt) {
-                *reinterpret_cast<uint4*>(rec + tt * half_k + f / 2) =
-                    make_uint4(packed[tt][0], packed[tt][1], packed[tt][2], packed[tt][3]);
-                rec[sc0 + tt * kscale + f / 32] = (uint8_t)scb[tt];
+                for (int tt = 0; tt < kMxTerms; ++tt) {
+                  *reinterpret_cast<uint4*>(rec + tt * half_k + f / 2) =
+                      make_uint4(packed[tt][0], packed[tt][1], packed[tt][2], packed[tt][3]);
+                  rec[sc0 + tt * kscale + f / 32] = (uint8_t)scb[tt];
+                }
               }
             }
           }
@@ -595,10 +642,10 @@ done:
   }
 }
 
-template <bool GLU, int NT>
+template <bool GLU, int NT, bool F8>
 cudaError_t launch_mx_inst(const CUtensorMap (&maps)[8], const MxParams& p, long long items, cudaStream_t s) {
-  auto kern = tc_mx_kernel<GLU, NT>;
-  constexpr size_t kSmem = MxCfg<NT>::kSmem;
+  auto kern = tc_mx_kernel<GLU, NT, F8>;
+  constexpr size_t kSmem = MxCfg<NT, F8>::kSmem;
   static PerDeviceValue max_pairs_of;
   std::atomic<int>* slot = max_pairs_of.current();
   if (!slot) return cudaErrorInvalidDevice;
@@ -644,22 +691,25 @@ cudaError_t launch_tc_mx(const TcMx& g, const int4* tiles, const int32_t* num_ti
   if (glu ? (g.glu_h % 128 || g.out_features != g.glu_h || g.out_features % 512 || g.w.rows != 2 * g.glu_h)
           : (g.out_features % (2 * kWRows) || g.w.rows != g.out_features || !g.row_scale || g.ldc % 8))
     return cudaErrorInvalidValue;
-  const int64_t x_rec = mx3_row_bytes(g.K), kscale = g.K / 32, E = g.w.depth;
+  const bool f8 = g.f8;
+  const int64_t x_rec = f8 ? mx8_row_bytes(g.K) : mx3_row_bytes(g.K), kscale = g.K / 32, E = g.w.depth;
+  const int terms = f8 ? 1 : kMxTerms;
   CUtensorMap maps[8];  // weights, weight scales, token terms (3 box heights), token scales (3)
-  bool ok = glu ? make_map_glu_interleaved(&maps[0], g.w, g.glu_h, kWRows / 32, true)
-                : make_map_fp4(&maps[0], g.w, kWRows, 128, true);
+  bool ok = glu ? make_map_glu_interleaved(&maps[0], g.w, g.glu_h, kWRows / 32, true, f8)
+                : make_map_fp4(&maps[0], g.w, kWRows, 128, true, f8);
   for (int b = 0; b < 3; ++b) {  // the decode layout uses its one box size in all three slots
-    // the packed terms of the records as a 2-D byte array {3 K/2, rows}: boxes of 128 bytes
-    const cuuint64_t dims[2] = {(cuuint64_t)(kMxTerms * g.K / 2), (cuuint64_t)g.rows};
+    // the token bytes of the records as a 2-D byte array {3 K/2 (MXFP8: K), rows}: boxes of 128 bytes
+    const cuuint64_t dims[2] = {(cuuint64_t)(f8 ? g.K : kMxTerms * g.K / 2), (cuuint64_t)g.rows};
     const cuuint64_t strides[1] = {(cuuint64_t)x_rec};
     const int rows_b = x_box_rows(unit_rows, b);
     const cuuint32_t box[2] = {128, (cuuint32_t)rows_b};
     ok = ok && encode_u8(&maps[2 + b], g.x, 2, dims, strides, box, true);
     // the records' scale bytes {3 K/32, rows}: boxes of 16 bytes x (2 x the term box) rows
-    const cuuint64_t sdims[2] = {(cuuint64_t)(kMxTerms * kscale), (cuuint64_t)g.rows};
+    const cuuint64_t sdims[2] = {(cuuint64_t)(terms * kscale), (cuuint64_t)g.rows};
     const cuuint32_t sbox[2] = {16, (cuuint32_t)(2 * rows_b)};
-    ok = ok && encode_u8(&maps[5 + b], static_cast<const uint8_t*>(g.x) + mx3_scale_offset(g.K), 2, sdims, strides,
-                         sbox, false);
+    ok = ok && encode_u8(&maps[5 + b],
+                         static_cast<const uint8_t*>(g.x) + (f8 ? mx8_scale_offset(g.K) : mx3_scale_offset(g.K)), 2,
+                         sdims, strides, sbox, false);
   }
   if (glu) {  // weight scales [E][2h][K/32] as {K/32, 16, 2, h/16, E}: the rows in the weights' order
     const int64_t h = g.glu_h;
@@ -683,7 +733,7 @@ cudaError_t launch_tc_mx(const TcMx& g, const int4* tiles, const int32_t* num_ti
   p.tiles = tiles;
   p.num_tiles = num_tiles;
   p.C = g.C;
-  p.ldc = glu ? mx3_row_bytes(g.out_features) : g.ldc;
+  p.ldc = glu ? (f8 ? mx8_row_bytes(g.out_features) : mx3_row_bytes(g.out_features)) : g.ldc;
   p.out_k = g.out_features;
   p.row_scale = g.row_scale;
   p.status = status;
@@ -691,9 +741,14 @@ cudaError_t launch_tc_mx(const TcMx& g, const int4* tiles, const int32_t* num_ti
   p.inject = inject;
   const long long items = (long long)max_tiles * p.num_wt;
   if (items == 0) return cudaSuccess;
+  if (f8) {
+    if (decode)
+      return glu ? launch_mx_inst<true, 16, true>(maps, p, items, s) : launch_mx_inst<false, 16, true>(maps, p, items, s);
+    return glu ? launch_mx_inst<true, 192, true>(maps, p, items, s) : launch_mx_inst<false, 192, true>(maps, p, items, s);
+  }
   if (decode)
-    return glu ? launch_mx_inst<true, 16>(maps, p, items, s) : launch_mx_inst<false, 16>(maps, p, items, s);
-  return glu ? launch_mx_inst<true, 192>(maps, p, items, s) : launch_mx_inst<false, 192>(maps, p, items, s);
+    return glu ? launch_mx_inst<true, 16, false>(maps, p, items, s) : launch_mx_inst<false, 16, false>(maps, p, items, s);
+  return glu ? launch_mx_inst<true, 192, false>(maps, p, items, s) : launch_mx_inst<false, 192, false>(maps, p, items, s);
 }
 
 }  // namespace lmoe

@@ -216,10 +216,10 @@ cudaError_t launch_tc_pair_swap(const TcSwap& g, const int4* tiles_p, const int3
 // ---------------------------------------------------------------- block-scaled MXFP4 experts
 // Three-term MXFP4 records of token rows (mx.cuh): rows of z in expert-contiguous order.  z
 // [T][K] fp16 or bf16 (K % 512 == 0); dst[row_of[t][j]] = record of z[t] for every (t, j) with
-// row_of[t][j] >= 0.  k <= 32.
-size_t scatter_mx3_smem_bytes(int K, int in_elem_bytes);
+// row_of[t][j] >= 0.  k <= 32.  f8: MXFP8 records (mx8_row_bytes) instead.
+size_t scatter_mx3_smem_bytes(int K, int in_elem_bytes, bool f8 = false);
 cudaError_t launch_scatter_mx3(const void* src, int src_dtype, void* dst, const int32_t* row_of, int T, int k, int K,
-                               uint32_t* status, uint64_t timeout_ns, int num_sms, cudaStream_t s);
+                               uint32_t* status, uint64_t timeout_ns, int num_sms, cudaStream_t s, bool f8 = false);
 // Grouped expert GEMM on tcgen05.mma.cta_group::2.kind::mxf4 (gemm_mx.cu): E2M1 weights with E8M0
 // scales per 32 along K against token records.  unit_rows 192: the dispatch's 192-row tile list
 // (tiles_m; prefill); unit_rows 16: its 16-row unit list (tiles_s; decode, a deep weight ring).
@@ -238,6 +238,7 @@ struct TcMx {
   void* C;
   int64_t ldc;              // down: fp16 elements per output row
   const float* row_scale;
+  bool f8;                  // token records are MXFP8 (kind::mxf8f6f4) instead of three-term MXFP4
 };
 cudaError_t launch_tc_mx(const TcMx& g, const int4* tiles, const int32_t* num_tiles, int max_tiles, int unit_rows,
                          uint32_t* status, uint64_t timeout_ns, cudaStream_t s, int inject = 0);

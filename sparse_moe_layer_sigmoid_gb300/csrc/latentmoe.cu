@@ -113,7 +113,11 @@ lmoe_status validate_config(const lmoe_config& c) {
   if (c.router_w != LMOE_F32 && c.router_w != LMOE_BF16) return LMOE_ERR_INVALID_ARG;
   if (c.routed_w != LMOE_F32 && c.routed_w != LMOE_BF16 && c.routed_w != LMOE_MXFP4) return LMOE_ERR_INVALID_ARG;
   if (!(c.rms_eps >= 0.0f)) return LMOE_ERR_INVALID_ARG;
-  if (c.flags & ~(LMOE_FLAG_IDENTITY_EXPERTS | LMOE_FLAG_SINGLE_CTA_GEMM | LMOE_FLAG_MXFP4_DEQUANT))
+  if (c.flags & ~(LMOE_FLAG_IDENTITY_EXPERTS | LMOE_FLAG_SINGLE_CTA_GEMM | LMOE_FLAG_MXFP4_DEQUANT |
+                  LMOE_FLAG_MXFP8_ACT))
+    return LMOE_ERR_INVALID_ARG;
+  if ((c.flags & LMOE_FLAG_MXFP8_ACT) &&
+      (c.routed_w != LMOE_MXFP4 || c.act != LMOE_BF16 || (c.flags & (LMOE_FLAG_MXFP4_DEQUANT | LMOE_FLAG_SINGLE_CTA_GEMM))))
     return LMOE_ERR_INVALID_ARG;
   // router GEMM and the CUDA-core path step K by 16; combine moves 16-byte vectors
   if (c.d % 16 || c.latent % 16) return LMOE_ERR_UNSUPPORTED;
@@ -361,8 +365,10 @@ lmoe_status run_forward(lmoe_handle* h, const void* x, int T, const lmoe_weights
   const bool mx = tc && !identity && c.routed_w == LMOE_MXFP4 &&
                   !(c.flags & (LMOE_FLAG_MXFP4_DEQUANT | LMOE_FLAG_SINGLE_CTA_GEMM));
   // rows of z into expert-contiguous order (as MXFP4 records for the block-scaled expert GEMMs)
+  const bool f8 = (c.flags & LMOE_FLAG_MXFP8_ACT) != 0;
   if (mx)
-    LMOE_TRY(launch_scatter_mx3(h->z, rt, h->z_perm, h->db.row_of, T, k, l, h->status, h->timeout_ns, h->num_sms, s));
+    LMOE_TRY(launch_scatter_mx3(h->z, rt, h->z_perm, h->db.row_of, T, k, l, h->status, h->timeout_ns, h->num_sms, s,
+                                f8));
   else
     LMOE_TRY(launch_scatter_rows(h->z, h->z_perm, h->db.row_of, T, k, l, (int)ab, h->status, h->timeout_ns,
                                  h->num_sms, s));
@@ -398,6 +404,7 @@ lmoe_status run_forward(lmoe_handle* h, const void* x, int T, const lmoe_weights
     g.w_scale = w->routed_gate_up_scale;
     g.x = h->z_perm; g.rows = rows;
     g.C = h->a;
+    g.f8 = f8;
     LMOE_TRY(launch_tc_mx(g, tl, ntl, max_tl, unit, h->status, h->timeout_ns, s, inject_routed));
     stage_end(h, kStGlu, s);
 
@@ -407,6 +414,7 @@ lmoe_status run_forward(lmoe_handle* h, const void* x, int T, const lmoe_weights
     dn.w_scale = w->routed_down_scale;
     dn.x = h->a; dn.rows = rows;
     dn.C = o; dn.ldc = l; dn.row_scale = h->db.p_row;
+    dn.f8 = f8;
     LMOE_TRY(launch_tc_mx(dn, tl, ntl, max_tl, unit, h->status, h->timeout_ns, s));
     stage_end(h, kStDown, s);
     h->last_launches += 2;

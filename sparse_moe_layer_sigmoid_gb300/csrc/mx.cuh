@@ -93,5 +93,50 @@ __device__ __forceinline__ void quantize_block(float (&r)[32], uint32_t (&packed
   }
 }
 
+// ---------------------------------------------------------------- MXFP8 activation records
+// One term: E4M3 elements with an E8M0 scale per 32 (OCP Microscaling v1.0), for the
+// kind::mxf8f6f4 expert GEMMs (E2M1 weights x E4M3 activations; page "What K3 actually is",
+// srikanthmalla.com: K3's quantization-aware training with MXFP8 activations).  Scale: the
+// smallest power of two s with amax <= 448 s (no element saturates); elements round to nearest,
+// ties to the even code; a value that rounds to zero is stored as +0.  Record of one row of K
+// values, mx8_row_bytes(K) bytes: [K E4M3 codes][K/32 scale bytes].
+
+// Biased E8M0 exponent of the smallest power of two s with amax <= 448 s, clamped to [1, 253]:
+// with amax = m 2^E, m in [1, 2), 448 * 2^(E-8) = 1.75 * 2^E covers m <= 1.75.
+__device__ __forceinline__ uint32_t scale_byte8(float amax) {
+  const uint32_t b = __float_as_uint(amax);
+  int e = (int)((b >> 23) & 0xFFu) - 8 + ((b & 0x7FFFFFu) > 0x600000u ? 1 : 0);
+  e = e < 1 ? 1 : (e > 253 ? 253 : e);
+  return (uint32_t)e;
+}
+
+// 32 values r[] -> 32 E4M3 codes (element i in byte i of codes[i / 4]) and the scale byte.
+__device__ __forceinline__ void quantize_block8(const float (&r)[32], uint32_t (&codes)[8], uint32_t& sc) {
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(r[i]));
+  const uint32_t e = scale_byte8(amax);
+  const float inv = __uint_as_float((254u - e) << 23);  // 2^(127 - e), exact
+  sc = e;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) {
+    uint32_t lo, hi;
+    // cvt.rn.satfinite.e4m3x2.f32 d, a, b: b lands in the low byte
+    asm("{\n\t.reg .b16 h;\n\tcvt.rn.satfinite.e4m3x2.f32 h, %2, %1;\n\tcvt.u32.u16 %0, h;\n\t}"
+        : "=r"(lo) : "f"(r[4 * w] * inv), "f"(r[4 * w + 1] * inv));
+    asm("{\n\t.reg .b16 h;\n\tcvt.rn.satfinite.e4m3x2.f32 h, %2, %1;\n\tcvt.u32.u16 %0, h;\n\t}"
+        : "=r"(hi) : "f"(r[4 * w + 2] * inv), "f"(r[4 * w + 3] * inv));
+    uint32_t v = lo | (hi << 16);
+    // -0 (sign bit over a zero magnitude) -> +0
+    const uint32_t mag = v & 0x7F7F7F7Fu;
+    const uint32_t nonzero = ((mag + 0x7F7F7F7Fu) & 0x80808080u);  // bit 7 of a byte: magnitude != 0
+    codes[w] = mag | (v & nonzero);
+  }
+}
+
 }  // namespace mx
+
+__host__ __device__ constexpr int64_t mx8_row_bytes(int64_t K) { return K + K / 32; }
+__host__ __device__ constexpr int64_t mx8_scale_offset(int64_t K) { return K; }
+
 }  // namespace lmoe

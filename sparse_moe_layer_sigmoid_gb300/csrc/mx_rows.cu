@@ -1,5 +1,5 @@
-// Rows of z = W_down x into expert-contiguous order as three-term MXFP4 records (mx.cuh), the
-// input format of the block-scaled routed-expert GEMMs (page "Lesson 6 - LatentMoE",
+// Rows of z = W_down x into expert-contiguous order as three-term MXFP4 records, or MXFP8
+// records (mx.cuh), the input formats of the block-scaled routed-expert GEMMs (page "Lesson 6 - LatentMoE",
 // kimi-k3-course.pages.dev, eq. 11: each selected expert reads W_down x; the rows are grouped by
 // expert the way "Kimi K3 architectural innovations", manishklach.github.io, section "A router
 // decision is also a scheduling decision", converts selections into expert batches).
@@ -47,7 +47,7 @@ __device__ __forceinline__ void load32(const __nv_bfloat16* p, float (&v)[32]) {
   }
 }
 
-template <typename TIn>
+template <typename TIn, bool F8>
 __global__ void __launch_bounds__(32) scatter_mx3_kernel(const TIn* __restrict__ src, uint8_t* __restrict__ dst,
                                                          const int32_t* __restrict__ row_of, int T, int k, int K,
                                                          uint32_t* status, uint64_t timeout_ns) {
@@ -56,7 +56,7 @@ __global__ void __launch_bounds__(32) scatter_mx3_kernel(const TIn* __restrict__
   __shared__ int abort_flag;
   const int lane = threadIdx.x;
   const uint32_t in_bytes = (uint32_t)K * sizeof(TIn);
-  const uint32_t rec_bytes = (uint32_t)mx3_row_bytes(K);
+  const uint32_t rec_bytes = (uint32_t)(F8 ? mx8_row_bytes(K) : mx3_row_bytes(K));
   const uint32_t in_stride = (in_bytes + 127u) & ~127u, rec_stride = (rec_bytes + 127u) & ~127u;
   unsigned char* in_buf = smem;                   // [2][in_stride]
   unsigned char* rec_buf = smem + 2 * in_stride;  // [2][rec_stride]
@@ -101,12 +101,21 @@ __global__ void __launch_bounds__(32) scatter_mx3_kernel(const TIn* __restrict__
     for (int b = lane; b < nblocks; b += 32) {
       float v[32];
       load32(row + 32 * b, v);
-      uint32_t packed[kMxTerms][4], sc[kMxTerms];
-      mx::quantize_block(v, packed, sc);
+      if (F8) {
+        uint32_t codes[8], sc;
+        mx::quantize_block8(v, codes, sc);
+        *reinterpret_cast<uint4*>(rec + 32 * b) = make_uint4(codes[0], codes[1], codes[2], codes[3]);
+        *reinterpret_cast<uint4*>(rec + 32 * b + 16) = make_uint4(codes[4], codes[5], codes[6], codes[7]);
+        rec[K + b] = (unsigned char)sc;
+      } else {
+        uint32_t packed[kMxTerms][4], sc[kMxTerms];
+        mx::quantize_block(v, packed, sc);
 #pragma unroll
-      for (int q = 0; q < kMxTerms; ++q) {
-        *reinterpret_cast<uint4*>(rec + q * half_k + 16 * b) = make_uint4(packed[q][0], packed[q][1], packed[q][2], packed[q][3]);
-        rec[sc_off + q * (K / 32) + b] = (unsigned char)sc[q];
+        for (int q = 0; q < kMxTerms; ++q) {
+          *reinterpret_cast<uint4*>(rec + q * half_k + 16 * b) =
+              make_uint4(packed[q][0], packed[q][1], packed[q][2], packed[q][3]);
+          rec[sc_off + q * (K / 32) + b] = (unsigned char)sc[q];
+        }
       }
     }
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic writes -> bulk-copy reads
@@ -126,43 +135,45 @@ __global__ void __launch_bounds__(32) scatter_mx3_kernel(const TIn* __restrict__
 
 }  // namespace
 
-size_t scatter_mx3_smem_bytes(int K, int in_elem_bytes) {
+size_t scatter_mx3_smem_bytes(int K, int in_elem_bytes, bool f8) {
   const size_t in_stride = ((size_t)K * in_elem_bytes + 127) & ~(size_t)127;
-  const size_t rec_stride = ((size_t)mx3_row_bytes(K) + 127) & ~(size_t)127;
+  const size_t rec_stride = ((size_t)(f8 ? mx8_row_bytes(K) : mx3_row_bytes(K)) + 127) & ~(size_t)127;
   return 2 * in_stride + 2 * rec_stride;
 }
 
+template <typename TIn, bool F8>
+cudaError_t launch_scatter_typed(const void* src, void* dst, const int32_t* row_of, int T, int k, int K, uint32_t* status,
+                                 uint64_t timeout_ns, size_t smem, int grid, cudaStream_t s) {
+  auto kern = scatter_mx3_kernel<TIn, F8>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, 32, smem, s>>>(static_cast<const TIn*>(src), static_cast<uint8_t*>(dst), row_of, T, k, K, status,
+                              timeout_ns);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_scatter_mx3(const void* src, int src_dtype, void* dst, const int32_t* row_of, int T, int k, int K,
-                               uint32_t* status, uint64_t timeout_ns, int num_sms, cudaStream_t s) {
+                               uint32_t* status, uint64_t timeout_ns, int num_sms, cudaStream_t s, bool f8) {
   if (T <= 0) return cudaSuccess;
   if (k < 1 || k > 32 || K % 512 || (src_dtype != kF16 && src_dtype != kBF16) ||
       (reinterpret_cast<uintptr_t>(src) & 15u) || (reinterpret_cast<uintptr_t>(dst) & 15u))
     return cudaErrorInvalidValue;
-  const size_t smem = scatter_mx3_smem_bytes(K, 2);
+  const size_t smem = scatter_mx3_smem_bytes(K, 2, f8);
   if (smem > 200 * 1024) return cudaErrorInvalidValue;
   const int per_sm = (int)((200 * 1024) / (smem + 1024)) < 8 ? (int)((200 * 1024) / (smem + 1024)) : 8;
   const int grid = T < per_sm * num_sms ? T : per_sm * num_sms;
-  if (src_dtype == kF16) {
-    auto kern = scatter_mx3_kernel<__half>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    kern<<<grid, 32, smem, s>>>(static_cast<const __half*>(src), static_cast<uint8_t*>(dst), row_of, T, k, K, status,
-                                timeout_ns);
-  } else {
-    auto kern = scatter_mx3_kernel<__nv_bfloat16>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    kern<<<grid, 32, smem, s>>>(static_cast<const __nv_bfloat16*>(src), static_cast<uint8_t*>(dst), row_of, T, k,
-                                K, status, timeout_ns);
-  }
-  return cudaGetLastError();
+  if (src_dtype == kF16)
+    return f8 ? launch_scatter_typed<__half, true>(src, dst, row_of, T, k, K, status, timeout_ns, smem, grid, s)
+              : launch_scatter_typed<__half, false>(src, dst, row_of, T, k, K, status, timeout_ns, smem, grid, s);
+  return f8 ? launch_scatter_typed<__nv_bfloat16, true>(src, dst, row_of, T, k, K, status, timeout_ns, smem, grid, s)
+            : launch_scatter_typed<__nv_bfloat16, false>(src, dst, row_of, T, k, K, status, timeout_ns, smem, grid, s);
 }
 
 }  // namespace lmoe
 
-// Test hook (declared in latentmoe.h): the three-term MXFP4 records of rows x rows x K values.
-extern "C" lmoe_status latentmoe_mx3_quantize(const void* src, int32_t src_dtype, int64_t rows, int32_t K, void* dst,
-                                              void* stream) {
+namespace {
+lmoe_status quantize_rows(const void* src, int32_t src_dtype, int64_t rows, int32_t K, void* dst, void* stream,
+                          bool f8) {
   if (rows < 0 || rows > INT32_MAX || K <= 0 || K % 512 || (rows > 0 && (!src || !dst)))
     return LMOE_ERR_INVALID_ARG;
   if (src_dtype != LMOE_BF16 && src_dtype != LMOE_F16) return LMOE_ERR_INVALID_ARG;
@@ -174,6 +185,17 @@ extern "C" lmoe_status latentmoe_mx3_quantize(const void* src, int32_t src_dtype
     return LMOE_ERR_CUDA;
   const cudaError_t e =
       lmoe::launch_scatter_mx3(src, src_dtype == LMOE_BF16 ? lmoe::kBF16 : lmoe::kF16, dst, nullptr, (int)rows, 1, K,
-                               nullptr, 4000000000ull, num_sms, static_cast<cudaStream_t>(stream));
+                               nullptr, 4000000000ull, num_sms, static_cast<cudaStream_t>(stream), f8);
   return e == cudaSuccess ? LMOE_OK : LMOE_ERR_CUDA;
+}
+}  // namespace
+
+// Test hooks (declared in latentmoe.h): the three-term MXFP4 / the MXFP8 records of rows x K values.
+extern "C" lmoe_status latentmoe_mx3_quantize(const void* src, int32_t src_dtype, int64_t rows, int32_t K, void* dst,
+                                              void* stream) {
+  return quantize_rows(src, src_dtype, rows, K, dst, stream, false);
+}
+extern "C" lmoe_status latentmoe_mx8_quantize(const void* src, int32_t src_dtype, int64_t rows, int32_t K, void* dst,
+                                              void* stream) {
+  return quantize_rows(src, src_dtype, rows, K, dst, stream, true);
 }

@@ -301,6 +301,22 @@ __device__ __forceinline__ void mma_mxf4_pair(uint32_t d_tmem, uint64_t a_desc, 
 }
 // Instruction descriptor for kind::mxf4: E2M1 A and B (format code 1), E8M0 scales, both
 // K-major, M x N, scale bytes selected by a_sf / b_sf.
+// Instruction descriptor of kind::mxf8f6f4 with A = E2M1 (format 5), B = E4M3 (format 0), E8M0
+// scales (bit 23), scale_vec::1X: a_sf / b_sf pick the scale byte (0..3) of each 32-bit scale
+// column, one per 32 K.
+__host__ __device__ constexpr uint32_t idesc_mxf8f6f4_e2m1_e4m3(int M, int N, uint32_t a_sf, uint32_t b_sf) {
+  return (b_sf << 4) | (5u << 7) | (0u << 10) | ((uint32_t)(N >> 3) << 17) | (1u << 23) | ((uint32_t)(M >> 4) << 24) |
+         (a_sf << 29);
+}
+// D (+)= A . B^T on the CTA pair with block scales: kind::mxf8f6f4, K = 32.
+__device__ __forceinline__ void mma_mxf8f6f4_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                                  uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+      ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
 __host__ __device__ constexpr uint32_t idesc_mxf4(int M, int N, uint32_t a_sf, uint32_t b_sf) {
   return (b_sf << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | (1u << 23) |
          ((uint32_t)(M >> 4) << 24) | (a_sf << 29);

@@ -167,18 +167,24 @@ inline bool make_map(CUtensorMap* m, const TcOperand& op, int box_rows = 128) {
 // {cols, 16, 2, h/16, depth} with a box of {64 elements, 16, 2, groups, 1}: one load brings
 // `groups` x (16 gate rows, then the matching 16 up rows), 128-byte swizzled rows in that order.
 // `fp4`: the operand holds packed E2M1 bytes (cols/2 bytes per row, 128-byte box rows = 256
-// elements); otherwise bf16.
-inline bool make_map_glu_interleaved(CUtensorMap* m, const TcOperand& op, int glu_h, int groups, bool fp4 = false) {
+// elements); otherwise bf16.  `padded4` (with fp4): 4-bit elements that land one per byte
+// (CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B: 16 packed elements padded to 16 bytes), 128-element
+// boxes, for MMA kinds that read 4-bit operands from byte containers.
+inline bool make_map_glu_interleaved(CUtensorMap* m, const TcOperand& op, int glu_h, int groups, bool fp4 = false,
+                                     bool padded4 = false) {
   EncodeTiledFn enc = encode_fn();
   if (!enc || !op.ptr || glu_h % 16 || op.rows != 2 * (int64_t)glu_h) return false;
   const int64_t rs = fp4 ? op.row_stride / 2 : op.row_stride * 2;  // bytes per row
   const int64_t depth_stride = op.depth > 1 ? (fp4 ? op.depth_stride / 2 : op.depth_stride * 2) : op.rows * rs;
-  cuuint64_t dims[5] = {(cuuint64_t)(fp4 ? op.cols / 2 : op.cols), 16, 2, (cuuint64_t)(glu_h / 16),
+  const bool pad = fp4 && padded4;
+  cuuint64_t dims[5] = {(cuuint64_t)(fp4 && !pad ? op.cols / 2 : op.cols), 16, 2, (cuuint64_t)(glu_h / 16),
                         (cuuint64_t)op.depth};
   cuuint64_t strides[4] = {(cuuint64_t)rs, (cuuint64_t)(glu_h * rs), (cuuint64_t)(16 * rs), (cuuint64_t)depth_stride};
   cuuint32_t box[5] = {fp4 ? 128u : (cuuint32_t)BK, 16, 2, (cuuint32_t)groups, 1};
   cuuint32_t estr[5] = {1, 1, 1, 1, 1};
-  return enc(m, fp4 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(op.ptr),
+  return enc(m, pad ? CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B
+                    : (fp4 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16),
+             5, const_cast<void*>(op.ptr),
              dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -200,17 +206,20 @@ inline bool make_map_kslabs(CUtensorMap* m, const TcOperand& op, int box_rows, i
 // Packed E2M1 operand [depth][rows][cols/2 bytes] (element strides in `op`): boxes of
 // box_bytes bytes (2 elements per byte) x box_rows rows, no swizzle, or the 128-byte swizzle
 // (box_bytes == 128) when the reader takes column slices of the rows.
+// `padded4`: 4-bit elements landing one per byte (see make_map_glu_interleaved), boxes of
+// box_bytes elements.
 inline bool make_map_fp4(CUtensorMap* m, const TcOperand& op, int box_rows = 128, int box_bytes = BK / 2,
-                         bool swizzle128 = false) {
+                         bool swizzle128 = false, bool padded4 = false) {
   EncodeTiledFn enc = encode_fn();
   if (!enc || !op.ptr) return false;
   const int64_t rb = op.row_stride / 2;  // bytes per row
   const int64_t depth_stride = op.depth > 1 ? op.depth_stride / 2 : op.rows * rb;
-  cuuint64_t dims[3] = {(cuuint64_t)(op.cols / 2), (cuuint64_t)op.rows, (cuuint64_t)op.depth};
+  cuuint64_t dims[3] = {(cuuint64_t)(padded4 ? op.cols : op.cols / 2), (cuuint64_t)op.rows, (cuuint64_t)op.depth};
   cuuint64_t strides[2] = {(cuuint64_t)rb, (cuuint64_t)depth_stride};
   cuuint32_t box[3] = {(cuuint32_t)box_bytes, (cuuint32_t)box_rows, 1};
   cuuint32_t estr[3] = {1, 1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(op.ptr), dims, strides, box, estr,
+  return enc(m, padded4 ? CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B : CU_TENSOR_MAP_DATA_TYPE_UINT8, 3,
+             const_cast<void*>(op.ptr), dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }

@@ -351,3 +351,61 @@ def test_layer_mxfp4_and_bf16_storage_decoded_exactly():
     # bf16 bit patterns widen to the values torch holds
     x_t = inputs.make_inputs(cfg, "cpu")["x"].double().numpy()
     assert np.array_equal(oracle.widen(inp["x"]), x_t)
+
+
+# ---------------------------------------------------------------- MXFP8 activation mode
+
+def test_e4m3_codec_matches_library_float8():
+    """All 256 E4M3 codes decode to the values of torch's float8_e4m3fn; rounding to the E4M3
+    grid matches torch's conversion at every midpoint between neighbouring values (ties to the
+    even code) and on random values across the range."""
+    codes = np.arange(256)
+    lib = torch.tensor(codes, dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    mine = oracle.e4m3_value(codes)
+    assert np.array_equal(np.isnan(lib), np.isnan(mine))
+    assert np.array_equal(lib[~np.isnan(lib)], mine[~np.isnan(mine)])
+    assert oracle.e4m3_value(0x7E) == 448.0 and oracle.e4m3_value(0x01) == 2.0 ** -9
+    vals = np.unique(np.abs(mine[~np.isnan(mine)]))
+    mids = (vals[:-1] + vals[1:]) / 2
+    rng = np.random.default_rng(11)
+    x = np.concatenate([mids, -mids, vals, rng.uniform(-448, 448, 20000), rng.standard_normal(20000) * 1e-2])
+    lib_r = torch.tensor(x, dtype=torch.float64).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(oracle.e4m3_round(x), lib_r)
+    assert oracle.e4m3_round(np.array([1e6, -1e6])).tolist() == [448.0, -448.0]  # saturates
+
+
+def test_mxfp8_block_scale_rule():
+    """The scale is the smallest power of two s with max|v| <= 448 s: a block whose maximum is
+    448 * 2^k keeps it exactly (s = 2^k); one just above moves to s = 2^(k+1).  Encoding is
+    idempotent, an all-zero block stays zero, and each element is within half a grid step."""
+    v = np.zeros((1, 96))
+    v[0, :32] = np.linspace(-1, 1, 32) * 448.0 * 2.0 ** -3
+    v[0, 32:64] = np.linspace(-1, 1, 32) * 448.0 * 2.0 ** -3 * (1 + 2 ** -20)
+    q = oracle.mxfp8_quantize(v)
+    assert q[0, 31] == 448.0 * 2.0 ** -3           # exact at the top of its scale
+    assert q[0, 63] == 448.0 * 2.0 ** -3           # rounds back from the next scale up
+    assert np.all(q[0, 64:] == 0.0)
+    assert np.array_equal(oracle.mxfp8_quantize(q), q)
+    rng = np.random.default_rng(12)
+    w = rng.standard_normal((8, 256)) * np.logspace(-4, 4, 8)[:, None]
+    qw = oracle.mxfp8_quantize(w)
+    blk = np.abs(w).reshape(8, 8, 32).max(axis=2)
+    s = 2.0 ** np.ceil(np.log2(blk / 448.0))
+    step = np.repeat(s * 2.0 ** -3 * 2.0 ** np.floor(np.log2(blk / s)), 32, axis=1)  # a block's coarsest step
+    assert np.all(np.abs(qw - w) <= step / 2 + 1e-300)
+
+
+def test_mxfp8_expert_reduces_to_glu_without_quantisation(monkeypatch):
+    """With the activation quantiser replaced by the identity, the MXFP8 expert is the GLU expert
+    (same gate/up split and composition) and the MXFP8 layer is the plain layer."""
+    rng = np.random.default_rng(13)
+    v, gate_up, down = rng.standard_normal((5, 64)), rng.standard_normal((2 * 32, 64)), rng.standard_normal((64, 32))
+    monkeypatch.setattr(oracle, "mxfp8_quantize", lambda a: a)
+    import oracle.latentmoe_oracle as om
+    monkeypatch.setattr(om, "mxfp8_quantize", lambda a: a)
+    assert np.allclose(om.glu_expert_mxfp8(v, gate_up, down, 32), oracle.glu_expert(v, gate_up, down, 32), rtol=1e-13)
+    cfg = configs.TINY_F32
+    host = inputs.host_inputs(inputs.make_inputs(cfg, "cpu"))
+    a = oracle.layer_forward(host, cfg, tokens=np.arange(8))["y"]
+    b = oracle.layer_forward(host, cfg, tokens=np.arange(8), act_quant="mxfp8")["y"]
+    assert np.array_equal(a, b)
