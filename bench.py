@@ -40,6 +40,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 NOMINAL_FP4_RATIO = 6.0
 HEADLINE = "k3_mxfp4_prefill_skew"
 SUB_WORKLOADS = ("k3w_e128_bf16_prefill", "k3_mxfp4_decode", "k3_mxfp4_prefill_mild", "routing_dispatch_t65536")
+# the same MXFP4 layers in K3's quantisation-aware numerics (MXFP8 activations, kind::mxf8f6f4)
+MXFP8_SUB_WORKLOADS = ("k3_mxfp4_prefill_skew", "k3_mxfp4_decode")
+NOMINAL_FP8_RATIO = 2.0
 # token rows of the oracle's CPU baseline per workload (about 5-20 s of host work each: an MXFP4
 # row decodes up to 16 experts of 6144 x 3584 + 3584 x 3072 values)
 CPU_SAMPLE = {"k3_mxfp4_prefill_skew": 8, "k3w_e128_bf16_prefill": 8, "k3_mxfp4_decode": 4,
@@ -165,9 +168,10 @@ def stage_work(cfg, experts_touched, mx=None):
 
 def tensor_peak(stage, mx, peaks):
     """(peak TFLOP/s, name) a tensor stage is measured against: the routed stages of the
-    block-scaled path run E2M1 x E2M1 MMAs (the FP4 peak), everything else bf16 MMAs."""
+    block-scaled path run E2M1 x E2M1 MMAs (the FP4 peak; mx == "fp8": E2M1 x E4M3 on
+    kind::mxf8f6f4, the FP8 peak), everything else bf16 MMAs."""
     if mx and stage in ROUTED:
-        return peaks["fp4_tflops"], "fp4"
+        return (peaks["fp8_tflops"], "fp8") if mx == "fp8" else (peaks["fp4_tflops"], "fp4")
     return peaks["bf16_tflops"], "bf16"
 
 
@@ -347,6 +351,9 @@ def measured_peaks(binding, device, src):
     out["fp4_source"] = (f"{out['source']} bf16_tflops (burst) x nominal dense FP4/bf16 ratio "
                          f"{NOMINAL_FP4_RATIO:g} (13.5 / 2.25 PFLOP/s)")
     out["fp4_tflops"] = out["bf16_tflops"] * out["fp4_over_bf16"]
+    out["fp8_tflops"] = out["bf16_tflops"] * NOMINAL_FP8_RATIO
+    out["fp8_source"] = (f"{out['source']} bf16_tflops (burst) x nominal dense FP8/bf16 ratio "
+                         f"{NOMINAL_FP8_RATIO:g} (4.5 / 2.25 PFLOP/s)")
     return out
 
 
@@ -361,6 +368,8 @@ def measure_workload(cfg, args, peaks, world, rank, dist, dev, flags, with_cpu):
     inp = inputs.make_inputs(cfg, dev)
     layer = LatentMoE(cfg, flags=flags)
     mx = cfg.routed_w == "mxfp4" and not (flags & (binding.LMOE_FLAG_MXFP4_DEQUANT | binding.LMOE_FLAG_SINGLE_CTA_GEMM))
+    f8 = mx and bool(flags & binding.LMOE_FLAG_MXFP8_ACT)
+    mxk = ("fp8" if f8 else "fp4") if mx else None  # the MMA kind of the routed stages
     x = inp["x"]
     y = torch.empty((cfg.tokens, layer.out_width), dtype=x.dtype, device=dev)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
@@ -444,11 +453,12 @@ def measure_workload(cfg, args, peaks, world, rank, dist, dev, flags, with_cpu):
     kind, amount = work[dom]
     roof = {"bound": kind, "kernel": dom}
     if kind == "tensor":
-        peak, pname = tensor_peak(dom, mx, peaks)
+        peak, pname = tensor_peak(dom, mxk, peaks)
         achieved = amount / (st_ms[dom] * 1e-3) / 1e12
         roof.update({"achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                     "peak_source": f"{pname}: " + (peaks["fp4_source"] if pname == "fp4"
-                                                    else peaks["source"] + " bf16_tflops (burst)")})
+                     "peak_source": f"{pname}: " + (peaks["fp4_source"] if pname == "fp4" else
+                                                    peaks["fp8_source"] if pname == "fp8" else
+                                                    peaks["source"] + " bf16_tflops (burst)")})
         if pname == "fp4":  # three E2M1 activation terms: three MMAs per algorithmic product
             roof["mma_work_per_flop"] = 3
             roof["mma_pipe_frac_of_nominal"] = 3 * achieved / peak
@@ -467,7 +477,8 @@ def measure_workload(cfg, args, peaks, world, rank, dist, dev, flags, with_cpu):
     roof["traffic"] = None
     if tr and tr["bytes_per_launch"] and tr["sha256"] == file_sha(tr["src"]):
         roof["traffic"] = tr["bytes_per_launch"]
-    rt = TRAFFIC_RATIOS.get(("mxfp4_decode" if work[dom][0] == "hbm" else "mxfp4_prefill", dom)) if mx else None
+    rt = (TRAFFIC_RATIOS.get(("mxfp4_decode" if work[dom][0] == "hbm" else "mxfp4_prefill", dom))
+          if mx and not f8 else None)
     if rt and rt["sha256"] == file_sha(rt["src"]):
         rd, wr = traffic_alg_bytes(cfg, dom, route_stats["experts_touched"])
         roof["traffic"] = rt["read"] * rd + rt["write"] * wr
@@ -475,7 +486,7 @@ def measure_workload(cfg, args, peaks, world, rank, dist, dev, flags, with_cpu):
                                 "x this launch's algorithmic reads and writes")
     total_flops = sum(a for kd, a in work.values() if kd in ("tensor", "alu"))
     total_bytes = sum(a for kd, a in work.values() if kd == "hbm")
-    roof_ms = layer_roofline_ms(work, mx, peaks)
+    roof_ms = layer_roofline_ms(work, mxk, peaks)
     layer_rec = {"flops": total_flops, "hbm_bytes_counted": total_bytes,
                  "achieved_tflops": total_flops / (ms * 1e-3) / 1e12, "roofline_ms": roof_ms,
                  "roofline_frac": roof_ms / ms,
@@ -483,7 +494,13 @@ def measure_workload(cfg, args, peaks, world, rank, dist, dev, flags, with_cpu):
                  "stages_ms": st_ms, "stages_serial_sum_ms": serial_ms,
                  "stages_rule": ("stage times from separate steps run stage after stage on one stream; the "
                                  "timed steps overlap W_down and the shared GLU with the routing chain")}
-    if mx and work["routed_gate_up_glu"][0] == "tensor":
+    if f8 and work["routed_gate_up_glu"][0] == "tensor":
+        routed = work["routed_gate_up_glu"][1] + work["routed_down"][1]
+        dense = total_flops - routed
+        r8 = 1e3 * (routed / (peaks["fp8_tflops"] * 1e12) + dense / (peaks["bf16_tflops"] * 1e12))
+        layer_rec.update({"fp8_aware_roofline_ms": r8, "fp8_aware_frac": r8 / ms,
+                          "fp8_aware_rule": "routed FLOPs at the FP8 peak (kind::mxf8f6f4) + the rest at the bf16 peak"})
+    elif mx and work["routed_gate_up_glu"][0] == "tensor":
         routed = work["routed_gate_up_glu"][1] + work["routed_down"][1]
         dense = total_flops - routed
         fp4_roof = 1e3 * (routed / (peaks["fp4_tflops"] * 1e12) + dense / (peaks["bf16_tflops"] * 1e12))
@@ -503,7 +520,8 @@ def measure_workload(cfg, args, peaks, world, rank, dist, dev, flags, with_cpu):
         layer_rec["frac_of_bf16_peak"] = total_flops / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"]
     if cfg.identity_experts:
         layer_rec["achieved_gbs"] = total_bytes / (ms * 1e-3) / 1e9
-    dtype = ("e2m1 x e2m1 experts (three-term MXFP4 activations), bf16 dense" if mx else
+    dtype = ("e2m1 x e4m3 experts (MXFP8 activations), bf16 dense" if f8 else
+             "e2m1 x e2m1 experts (three-term MXFP4 activations), bf16 dense" if mx else
              "fp16 (MXFP4 experts decoded), bf16 dense" if cfg.routed_w == "mxfp4" else cfg.act)
     rec = {"value": job_tokens_per_s(world, cfg.tokens, ms), "unit": UNIT, "ms_per_step": ms, "dtype": dtype,
            "config": workload_config(cfg, args), "roofline": roof, "layer": layer_rec,
@@ -514,6 +532,8 @@ def measure_workload(cfg, args, peaks, world, rank, dist, dev, flags, with_cpu):
     if graph_rec:
         graph_rec["value"] = job_tokens_per_s(world, cfg.tokens, graph_rec["ms_per_step"])
         rec["graph"] = graph_rec
+    if f8:
+        rec["config"]["activations"] = "mxfp8 (LMOE_FLAG_MXFP8_ACT; compared with the oracle's MXFP8 mode)"
     layer.close()
     y = flush = None
     if with_cpu and rank == 0 and world == 1:
@@ -642,6 +662,8 @@ def main():
     ap.add_argument("--cpu-sample", type=int, default=None, help="token rows for the oracle CPU baseline")
     ap.add_argument("--single-cta", action="store_true",
                     help="run every tensor-core GEMM on single CTAs (no CTA-pair GEMMs)")
+    ap.add_argument("--mxfp8-act", action="store_true",
+                    help="MXFP4 experts with MXFP8 activations (kind::mxf8f6f4; K3's QAT numerics)")
     ap.add_argument("--mxfp4-dequant", action="store_true",
                     help="MXFP4 experts through the dequantizing kernels instead of the block-scaled MMA")
     args = ap.parse_args()
@@ -674,7 +696,8 @@ def main():
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     flags = ((binding.LMOE_FLAG_SINGLE_CTA_GEMM if args.single_cta else 0) |
-             (binding.LMOE_FLAG_MXFP4_DEQUANT if args.mxfp4_dequant else 0))
+             (binding.LMOE_FLAG_MXFP4_DEQUANT if args.mxfp4_dequant else 0) |
+             (binding.LMOE_FLAG_MXFP8_ACT if args.mxfp8_act else 0))
     peaks = measured_peaks(binding, dev, load_peaks())
     head = measure_workload(cfg, args, peaks, world, rank, dist, dev, flags, with_cpu=True)
     subs = {}
@@ -682,6 +705,9 @@ def main():
         for name in SUB_WORKLOADS:
             subs[name] = measure_workload(configs.CONFIGS[name], args, peaks, world, rank, dist, dev, flags,
                                           with_cpu=True)
+        for name in MXFP8_SUB_WORKLOADS:
+            subs[name + "_mxfp8act"] = measure_workload(configs.CONFIGS[name], args, peaks, world, rank, dist, dev,
+                                                        flags | binding.LMOE_FLAG_MXFP8_ACT, with_cpu=False)
     line = {"metric": METRIC, "value": head["value"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": head["dtype"], "data": "synthetic",
