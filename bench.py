@@ -66,16 +66,16 @@ TRAFFIC = {
 # capture of a smaller case of the same kernel; a full launch's traffic is those ratios times its
 # own algorithmic bytes (reads and writes each grow with experts touched and rows processed).
 TRAFFIC_RATIOS = {
-    # prefill tiles: k3_mxfp4_prefill_e32_t1024 (32 experts, 16384 rows): read 468074752 B of
-    # 467927040 B, write 69548800 B of 80216064 B
-    ("mxfp4_prefill", "routed_gate_up_glu"): {"read": 468074752 / 467927040, "write": 69548800 / 80216064,
+    # prefill tiles: k3_mxfp4_prefill_e32_t1024 (32 experts, 16384 rows): read 468240384 B of
+    # 467927040 B, write 69593600 B of 80216064 B
+    ("mxfp4_prefill", "routed_gate_up_glu"): {"read": 468240384 / 467927040, "write": 69593600 / 80216064,
                                               "src": "sparse_moe_layer_sigmoid_gb300/csrc/gemm_mx.cu",
-                                              "sha256": "154c4883a77c747ea5a6cee909870257fe1930730d40cb24237929a5f72faae8"},
-    # decode units: k3_mxfp4_decode_e128_t8 (85 experts, 128 rows): read 995247360 B of 995076096 B,
-    # write 4325376 B of 626688 B (dirty lines of the untimed L2 flush written back meanwhile)
-    ("mxfp4_decode", "routed_gate_up_glu"): {"read": 995247360 / 995076096, "write": 4325376 / 626688,
+                                              "sha256": "df7c7591113b3547382afef42370ef51d0ccc0bb86681d8f68f0056e80a51850"},
+    # decode units: k3_mxfp4_decode_e128_t8 (85 experts, 128 rows): read 995216128 B of 995076096 B,
+    # write 3759872 B of 626688 B (dirty lines of the untimed L2 flush written back meanwhile)
+    ("mxfp4_decode", "routed_gate_up_glu"): {"read": 995216128 / 995076096, "write": 3759872 / 626688,
                                              "src": "sparse_moe_layer_sigmoid_gb300/csrc/gemm_mx.cu",
-                                             "sha256": "154c4883a77c747ea5a6cee909870257fe1930730d40cb24237929a5f72faae8"},
+                                             "sha256": "df7c7591113b3547382afef42370ef51d0ccc0bb86681d8f68f0056e80a51850"},
 }
 
 
