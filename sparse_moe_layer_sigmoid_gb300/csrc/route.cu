@@ -465,7 +465,7 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ log
 }
 
 constexpr int kRefineWarps = 4;  // warps of a refinement CTA
-constexpr int kTopkFusedMaxT = 512;  // batches up to this many tokens run topk_fused_kernel
+constexpr int kTopkFusedMaxT = 512;  // batches up to this many tokens run topk_small_kernel
 constexpr int kMaxCont = 64;     // contenders of one token: its selected experts and the band
 
 // Shared memory of one refinement group (a warp, or the whole CTA): the token's contenders.
@@ -699,47 +699,228 @@ __global__ void __launch_bounds__(32 * kRefineWarps, 4) topk_refine_kernel(
   }
 }
 
-// Both passes in one kernel for short batches (decode): one CTA per token.  Warp 0 runs pass 1;
-// when the token's list is uncertain it lists the contenders straight from pass 1's registers and
-// the CTA's warps settle it at once (no second launch, no reload of the keys).  refine_count[0]
-// counts the settled tokens (no list is written), refine_count[1] the near ties.
+// Both passes in one kernel for short batches (decode): one CTA of kSmallWarps warps per token.
+// A token's selection runs once per CTA, so the instructions it executes are fetched once, mostly
+// from memory; the kernel therefore keeps its code short: the keys live in shared memory (and four
+// per thread in registers), each step is a short loop shared by the CTA's threads, and only the
+// rare fallback (more than 64 keys at or above the bound) runs the one-warp selection of
+// topk_pass.  Steps:
+//   bound     lb = the k-th largest of the threads' largest keys (bisection, a CTA count per
+//             probe): k threads hold keys at least that large, so every selected key is >= lb;
+//   rank      the keys >= lb (at most 64) sorted by (key descending, index ascending) in warp 0:
+//             ranks 0..k-1 and the (k+1)-th key (or the largest key below lb);
+//   settle    as topk_refine_kernel: when the list's order is not certain within the key
+//             uncertainty, the contenders (the selected experts and, at an uncertain boundary,
+//             the band) are listed in ascending expert order and the CTA's warps settle them
+//             with refine_finish.
+// refine_count[0] counts the settled tokens, refine_count[1] the near ties.
+constexpr int kSmallWarps = 8;
+constexpr int kSmallThreads = 32 * kSmallWarps;
+constexpr int kSmallSlots = 4;  // keys per thread: E <= kSmallSlots * kSmallThreads
+
+size_t topk_small_smem(int E) { return (size_t)E * (sizeof(float) + 1); }
+
 template <int NPL>
-__global__ void __launch_bounds__(32 * kRefineWarps) topk_fused_kernel(
+__global__ void __launch_bounds__(kSmallThreads, 2) topk_small_kernel(
     const float* __restrict__ logits, const float* __restrict__ bias, RouterSrc src, int T, int E, int k,
     int32_t* __restrict__ idx, float* __restrict__ p, int32_t* __restrict__ refine_count, uint32_t* status) {
-  __shared__ uint64_t s_sk[64];
-  __shared__ float s_ss[64];
+  extern __shared__ float s_dyn[];
+  float* s_sv = s_dyn;                                       // [E] scores
+  uint8_t* s_flag = reinterpret_cast<uint8_t*>(s_dyn + E);  // [E] 1: selected, 2: recompute
+  __shared__ uint64_t s_ck[64];  // candidates: orderable key << 32 | (0xFFFF - expert) << 16
+  __shared__ float s_ss[64];     // topk_pass scratch
   __shared__ int s_ce[kMaxCont];
   __shared__ uint64_t s_key[kMaxCont];
   __shared__ float s_s[kMaxCont];
   __shared__ int s_exa[kMaxCont];
   __shared__ int s_cand[kMaxCont];
-  __shared__ float2 s_part[kRefineWarps][kMaxCont];
+  __shared__ float2 s_part[kSmallWarps][kMaxCont];
   __shared__ int s_n[2];
-  __shared__ int s_need;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __shared__ uint32_t s_cnt, s_below, s_dmax;
+  __shared__ float s_ak, s_ak1;
+  __shared__ int s_need, s_unc;
+  __shared__ int s_wc[kSmallWarps], s_wr[kSmallWarps];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t lt_mask = (1u << lane) - 1u;
   const RefineSmem sm{s_ce, s_key, s_s, s_exa, s_cand, &s_part[0][0], s_n};
   for (int t = blockIdx.x; t < T; t += gridDim.x) {
-    if (warp == 0) {
-      TopkState<NPL> st;
-      if (!topk_pass_sorted<NPL>(logits, bias, t, E, k, lane, st, s_sk, s_ss))
-        topk_pass<NPL>(logits, bias, t, E, k, lane, st, s_sk, s_ss);
-      const float eta2 = 2.0f * token_eta<NPL>(st.kf, st.sv, st.a_k1, src);
-      const float next = __shfl_down_sync(0xffffffffu, st.my_kf, 1);
-      const bool close = lane + 1 < k && st.my_kf - next < eta2;
-      const bool need = (k < E && st.a_k - st.a_k1 < eta2) || __any_sync(0xffffffffu, close);
-      if (need) {
-        if (lane == 0) atomicAdd(refine_count, 1);
-        build_contenders<NPL>(st, eta2, E, k, lane, sm, status);
-      } else {
-        topk_write(t, k, st.my_e, st.my_s, idx, p, lane);
+    if (tid == 0) {
+      s_cnt = 0;
+      s_below = 0;
+      s_dmax = 0;
+    }
+    // keys and scores (every load in flight at once), this thread's largest key
+    float kf[kSmallSlots], sv[kSmallSlots];
+    uint32_t ko[kSmallSlots];
+    {
+      float lg[kSmallSlots], bs[kSmallSlots];
+#pragma unroll
+      for (int i = 0; i < kSmallSlots; ++i) {
+        const int e = tid + kSmallThreads * i;
+        lg[i] = e < E ? __ldg(logits + (size_t)t * E + e) : 0.f;
+        bs[i] = bias && e < E ? __ldg(bias + e) : 0.f;
       }
-      if (lane == 0) s_need = need ? 1 : 0;
+#pragma unroll
+      for (int i = 0; i < kSmallSlots; ++i) {
+        const int e = tid + kSmallThreads * i;
+        const float s = 1.0f / (1.0f + expf(-lg[i]));  // the arithmetic of expert_key
+        sv[i] = e < E ? s : 0.f;
+        kf[i] = e < E ? (bias ? s + bs[i] : s) : -INFINITY;
+        ko[i] = e < E ? orderable(kf[i]) : 0u;
+        if (e < E) {
+          s_sv[e] = s;
+          s_flag[e] = 0;
+        }
+      }
+    }
+    uint32_t tmax = 0;
+#pragma unroll
+    for (int i = 0; i < kSmallSlots; ++i) tmax = ko[i] > tmax ? ko[i] : tmax;
+    // bound: the largest v with at least k threads' largest keys >= v (uniform over the CTA)
+    uint32_t lo = 1, hi = 0xFFFFFFFFu;
+    while (lo < hi) {
+      const uint32_t mid = lo + ((hi - lo + 1u) >> 1);
+      if (__syncthreads_count(tmax >= mid) >= k)
+        lo = mid;
+      else
+        hi = mid - 1u;
+    }
+    const uint32_t lb = lo;
+    uint32_t below = 0;
+#pragma unroll
+    for (int i = 0; i < kSmallSlots; ++i) {
+      const int e = tid + kSmallThreads * i;
+      if (ko[i] >= lb && ko[i] != 0u) {
+        const uint32_t pos = atomicAdd(&s_cnt, 1u);
+        if (pos < 64) s_ck[pos] = ((uint64_t)ko[i] << 32) | ((uint64_t)(0xFFFFu - (uint32_t)e) << 16);
+      } else if (ko[i] > below) {
+        below = ko[i];
+      }
+    }
+    if (below) atomicMax(&s_below, below);
+    __syncthreads();
+    const int cnt = (int)s_cnt;
+    // rank (warp 0): ranks 0..k-1 on lanes 0..k-1, the k-th and (k+1)-th keys
+    int my_e = 0;
+    float my_s = 0.f, my_kf = 0.f;
+    if (warp == 0) {
+      float a_k, a_k1 = -INFINITY;
+      if (cnt <= 64) {
+        uint64_t key[2];
+        uint32_t aux[2] = {0u, 0u};
+        key[0] = 2 * lane < cnt ? s_ck[2 * lane] : 0ull;
+        key[1] = 2 * lane + 1 < cnt ? s_ck[2 * lane + 1] : 0ull;
+        sort64_desc(key, aux, lane);
+        const uint64_t mine = entry_key(key, lane < k ? lane : 0);
+        if (lane < k) {
+          my_e = (int)(0xFFFFu - (uint32_t)((mine >> 16) & 0xFFFFu));
+          my_kf = from_orderable((uint32_t)(mine >> 32));
+          my_s = s_sv[my_e];
+        }
+        a_k = from_orderable((uint32_t)(entry_key(key, k - 1) >> 32));
+        if (k < E) a_k1 = from_orderable(cnt > k ? (uint32_t)(entry_key(key, k) >> 32) : s_below);
+      } else {  // many keys tie at or near the bound: the one-warp selection by bisection
+        TopkState<NPL> st;
+        topk_pass<NPL>(logits, bias, t, E, k, lane, st, s_ck, s_ss);
+        my_e = st.my_e;
+        my_s = st.my_s;
+        my_kf = st.my_kf;
+        a_k = st.a_k;
+        a_k1 = st.a_k1;
+      }
+      if (lane == 0) {
+        s_ak = a_k;
+        s_ak1 = a_k1;
+      }
     }
     __syncthreads();
-    if (s_need)  // uniform over the CTA
-      refine_finish<NPL, kRefineWarps>(logits, bias, src, t, E, k, idx, p, warp, lane, sm, status,
-                                       refine_count + 1);
+    const float a_k = s_ak, a_k1 = s_ak1;
+    // the key uncertainty of the token's contenders (token_eta over the CTA)
+    {
+      const float lo_eta = a_k1 - 2.0f * key_eta(src);
+      float dm = 0.0f;
+#pragma unroll
+      for (int i = 0; i < kSmallSlots; ++i)
+        if (kf[i] >= lo_eta) dm = fmaxf(dm, sv[i] * (1.0f - sv[i]));
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) dm = fmaxf(dm, __shfl_xor_sync(0xffffffffu, dm, off));
+      if (lane == 0) atomicMax(&s_dmax, __float_as_uint(dm));  // dm >= 0: bit order is value order
+    }
+    __syncthreads();
+    const float eta2 = 2.0f * (src.margin * (__uint_as_float(s_dmax) + 1e-4f) + 1e-6f);
+    if (warp == 0) {
+      const bool unc = k < E && a_k - a_k1 < eta2;
+      const float prev = __shfl_up_sync(0xffffffffu, my_kf, 1);
+      const float next = __shfl_down_sync(0xffffffffu, my_kf, 1);
+      const bool close_next = lane + 1 < k && my_kf - next < eta2;
+      const bool need = unc || __any_sync(0xffffffffu, close_next);
+      if (need) {
+        // ranks whose order against a neighbouring rank (or an uncertain boundary) is not certain
+        const bool close = lane < k && ((lane > 0 && prev - my_kf < eta2) || close_next || (lane == k - 1 && unc));
+        if (lane < k) s_flag[my_e] = close ? 3 : 1;
+        if (lane == 0) atomicAdd(refine_count, 1);
+      } else {
+        topk_write(t, k, my_e, my_s, idx, p, lane);
+      }
+      if (lane == 0) {
+        s_need = need ? 1 : 0;
+        s_unc = unc ? 1 : 0;
+      }
+    }
+    __syncthreads();
+    if (s_need) {  // uniform over the CTA
+      // contenders in ascending expert order: the selected experts and the band
+      const bool unc = s_unc != 0;
+      const float band_hi = a_k + eta2, band_lo = a_k1 - eta2;
+      int n_cont = 0, n_rc = 0;
+#pragma unroll
+      for (int i = 0; i < kSmallSlots; ++i) {
+        const int e = tid + kSmallThreads * i;
+        int f = 0;
+        if (e < E) {
+          f = s_flag[e];
+          if (unc && kf[i] >= band_lo && kf[i] <= band_hi) f |= 2;
+        }
+        const uint32_t mc = __ballot_sync(0xffffffffu, f != 0);
+        if (lane == 0) s_wc[warp] = __popc(mc);
+        __syncthreads();
+        int before = 0, total = 0;
+        for (int w = 0; w < kSmallWarps; ++w) {
+          const int c = s_wc[w];
+          before += w < warp ? c : 0;
+          total += c;
+        }
+        const int at = n_cont + before + __popc(mc & lt_mask);
+        const bool in = f != 0 && at < kMaxCont;
+        const bool r = in && (f & 2);
+        const uint32_t mr = __ballot_sync(0xffffffffu, r);
+        if (lane == 0) s_wr[warp] = __popc(mr);
+        __syncthreads();
+        int before_r = 0, total_r = 0;
+        for (int w = 0; w < kSmallWarps; ++w) {
+          const int c = s_wr[w];
+          before_r += w < warp ? c : 0;
+          total_r += c;
+        }
+        if (in) {
+          s_ce[at] = e;
+          s_key[at] = orderable64((double)kf[i]);
+          s_s[at] = sv[i];
+          s_exa[at] = 0;
+          if (r) s_cand[n_rc + before_r + __popc(mr & lt_mask)] = at;
+        }
+        n_cont += total;
+        n_rc += total_r;
+        __syncthreads();  // s_wc / s_wr are rewritten by the next slot
+      }
+      if (tid == 0) {
+        if (n_cont > kMaxCont) report(status, kStatusDeviceCheck);  // the first kMaxCont are ranked
+        s_n[0] = n_cont < kMaxCont ? n_cont : kMaxCont;
+        s_n[1] = n_rc;
+      }
+      refine_finish<NPL, kSmallWarps>(logits, bias, src, t, E, k, idx, p, warp, lane, sm, status,
+                                      refine_count + 1);
+    }
     __syncthreads();  // shared memory is reused by the next token
   }
 }
@@ -1089,8 +1270,8 @@ cudaError_t launch_topk(const float* logits, const float* bias, const RouterSrc&
 #define LMOE_TOPK(N)                                                                                     \
   do {                                                                                                   \
     if (fused) {                                                                                         \
-      topk_fused_kernel<N><<<T, 32 * kRefineWarps, 0, s>>>(logits, bias, src, T, E, k, idx, p, refine_count, \
-                                                           status);                                       \
+      topk_small_kernel<N><<<T, kSmallThreads, topk_small_smem(E), s>>>(logits, bias, src, T, E, k, idx, p, \
+                                                                        refine_count, status);            \
     } else {                                                                                             \
       topk_kernel<N><<<grid, block, 0, s>>>(logits, bias, src, T, E, k, idx, p, refine_list, refine_count); \
       topk_refine_kernel<N><<<rgrid, 128, 0, s>>>(logits, bias, src, E, k, idx, p, refine_list, refine_count, \

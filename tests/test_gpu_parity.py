@@ -399,6 +399,42 @@ def test_exact_ties_go_to_the_lower_index(binding, cfg):
     assert np.allclose(p_gpu[clear], p_want[clear], rtol=1e-4, atol=1e-7)
 
 
+@pytest.mark.parametrize("tokens", [40, 600], ids=lambda t: f"T{t}")
+def test_clustered_keys_take_the_bisection_fallback(binding, tokens):
+    """The 128 largest keys sit four to a thread of the short-batch selection's 256-thread layout
+    (expert tid + 256 i holds rank 4 tid + i), so the 32nd-largest thread maximum, its bound, lets
+    125 keys through: more than its 64-entry sort, which hands the token to the bisection
+    selection.  Logits are exact (one non-zero column of x and W_r, bf16-representable values):
+    the selection must be the oracle's, ranks 0..31 in order.  T=600 runs the two-kernel path."""
+    cfg = replace(configs.ROUTING_DISPATCH_STRESS, name="clustered_keys", tokens=tokens, d=512, latent=256,
+                  experts=896, top_k=32, bias="none", router_w="bf16", seed=45)
+    E, k = cfg.experts, cfg.top_k
+    w = torch.zeros((E, cfg.d), dtype=torch.float32)
+    w[:, 0] = -2.0
+    for rank in range(128):
+        w[(rank // 4) + 256 * (rank % 4), 0] = 4.0 - rank / 32.0
+    x = torch.zeros((tokens, cfg.d), dtype=torch.float32)
+    x[:, 0] = 0.5 + (torch.arange(tokens) % 64).float() / 64.0
+    host_inp = {"x": x.to(torch.bfloat16), "w_router": w.to(torch.bfloat16), "router_bias": None,
+                "w_down_proj": torch.zeros((cfg.latent, cfg.d), dtype=torch.bfloat16),
+                "rms_gain": torch.ones(cfg.latent)}
+    dev = torch.device("cuda")
+    inp = {k_: (None if v is None else v.to(dev)) for k_, v in host_inp.items()}
+    layer = binding.LatentMoE(cfg)
+    r = layer.route(inp["x"], inp)
+    assert layer.status() == 0
+    idx_gpu = r["idx"].cpu().numpy().astype(np.int64)
+    p_gpu = r["p"].cpu().numpy()
+    layer.close()
+    s = oracle.router_scores(oracle.widen(host_inp["x"].float().numpy()),
+                             oracle.widen(host_inp["w_router"].float().numpy()))
+    want, _ = oracle.select_topk(s, None, k)
+    ranked = np.array([(rank // 4) + 256 * (rank % 4) for rank in range(k)])
+    assert np.all(want == ranked[None, :])
+    assert np.array_equal(idx_gpu, want)
+    assert np.allclose(p_gpu, oracle.route_weights(s, want), rtol=1e-5, atol=1e-7)
+
+
 def test_forward_routed_with_oracle_routing(binding):
     cfg = replace(SMALL_BF16, name="routed", seed=34)
     dev = torch.device("cuda")
