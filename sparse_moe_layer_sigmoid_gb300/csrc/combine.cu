@@ -71,9 +71,17 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const T* __restrict__
 #pragma unroll
     for (int e = 0; e < 8; ++e) acc[i][e] = 0.f;
 
-  // U expert rows at a time: their loads are all issued before any is summed, and the sums still
-  // run in rank order j = 0..k-1.
-  constexpr int U = VPT <= 4 ? 4 : 2;
+  // the token's k row indices and weights first (one round of loads), then U expert rows at a
+  // time: their loads are all issued before any is summed, and the sums still run in rank order
+  // j = 0..k-1.
+  __shared__ int s_r[32];
+  __shared__ float s_w[32];
+  if (threadIdx.x < k) {
+    s_r[threadIdx.x] = row_of[(size_t)t * k + threadIdx.x];
+    s_w[threadIdx.x] = p ? p[(size_t)t * k + threadIdx.x] : 1.0f;
+  }
+  __syncthreads();
+  constexpr int U = VPT <= 4 ? 8 : 4;
   for (int j0 = 0; j0 < k; j0 += U) {
     int r[U];
     float w[U];
@@ -81,8 +89,8 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const T* __restrict__
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int j = j0 + u;
-      r[u] = j < k ? row_of[(size_t)t * k + j] : -1;
-      w[u] = p && j < k ? p[(size_t)t * k + j] : 1.0f;
+      r[u] = j < k ? s_r[j] : -1;
+      w[u] = j < k ? s_w[j] : 1.0f;
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {

@@ -4,9 +4,10 @@
 // expert the way "Kimi K3 architectural innovations", manishklach.github.io, section "A router
 // decision is also a scheduling decision", converts selections into expert batches).
 //
-// Each token's row is quantised once and copied to its k destination rows.  One warp per CTA:
-// lane 0 loads the next token's row (cp.async.bulk) while the warp quantises the current one
-// (lane l takes the 32-element blocks l, l + 32, ...), and lane j writes the record to the
+// Each token's row is quantised once and copied to its k destination rows.  W warps per CTA (one
+// for long batches, where the CTA's tokens pipeline; four when every token has a CTA of its own):
+// thread 0 loads the next token's row (cp.async.bulk) while the CTA quantises the current one
+// (thread i takes the 32-element blocks i, i + 32 W, ...), and thread j writes the record to the
 // token's j-th destination row with a bulk store (row_of == nullptr: row t to row t).  Two row
 // buffers and two record buffers.
 #include <cuda_fp16.h>
@@ -47,14 +48,22 @@ __device__ __forceinline__ void load32(const __nv_bfloat16* p, float (&v)[32]) {
   }
 }
 
-template <typename TIn, bool F8>
-__global__ void __launch_bounds__(32) scatter_mx3_kernel(const TIn* __restrict__ src, uint8_t* __restrict__ dst,
-                                                         const int32_t* __restrict__ row_of, int T, int k, int K,
-                                                         uint32_t* status, uint64_t timeout_ns) {
+template <int W>
+__device__ __forceinline__ void cta_sync() {
+  if (W == 1)
+    __syncwarp();
+  else
+    __syncthreads();
+}
+
+template <typename TIn, bool F8, int W>
+__global__ void __launch_bounds__(32 * W) scatter_mx3_kernel(const TIn* __restrict__ src, uint8_t* __restrict__ dst,
+                                                             const int32_t* __restrict__ row_of, int T, int k, int K,
+                                                             uint32_t* status, uint64_t timeout_ns) {
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ __align__(8) uint64_t full[2];
   __shared__ int abort_flag;
-  const int lane = threadIdx.x;
+  const int lane = threadIdx.x;  // the thread's index in the CTA
   const uint32_t in_bytes = (uint32_t)K * sizeof(TIn);
   const uint32_t rec_bytes = (uint32_t)(F8 ? mx8_row_bytes(K) : mx3_row_bytes(K));
   const uint32_t in_stride = (in_bytes + 127u) & ~127u, rec_stride = (rec_bytes + 127u) & ~127u;
@@ -68,7 +77,7 @@ __global__ void __launch_bounds__(32) scatter_mx3_kernel(const TIn* __restrict__
     abort_flag = 0;
     ptx::fence_mbar_init();
   }
-  __syncwarp();
+  cta_sync<W>();
   auto load = [&](int i) {
     uint64_t* bar = &full[i & 1];
     ptx::mbar_arrive_expect_tx(bar, in_bytes);
@@ -91,14 +100,14 @@ __global__ void __launch_bounds__(32) scatter_mx3_kernel(const TIn* __restrict__
     const int t = first + i * stride;
     const int r = row_of ? (lane < k ? row_of[(size_t)t * k + lane] : -1) : (lane == 0 ? t : -1);
     const bool ok = ptx::mbar_wait_bounded(&full[i & 1], (uint32_t)(i >> 1) & 1u, &abort_flag, status, timeout_ns);
-    if (!__all_sync(0xffffffffu, ok)) break;
+    if (W == 1 ? !__all_sync(0xffffffffu, ok) : !__syncthreads_and(ok)) break;
     // record buffer i&1 was last stored from by token i-2: at most one group (token i-1) may
     // still be reading shared memory
     ptx::bulk_wait_read<1>();
-    __syncwarp();
+    cta_sync<W>();
     const TIn* row = reinterpret_cast<const TIn*>(in_buf + (size_t)(i & 1) * in_stride);
     unsigned char* rec = rec_buf + (size_t)(i & 1) * rec_stride;
-    for (int b = lane; b < nblocks; b += 32) {
+    for (int b = lane; b < nblocks; b += 32 * W) {
       float v[32];
       load32(row + 32 * b, v);
       if (F8) {
@@ -119,7 +128,7 @@ __global__ void __launch_bounds__(32) scatter_mx3_kernel(const TIn* __restrict__
       }
     }
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic writes -> bulk-copy reads
-    __syncwarp();
+    cta_sync<W>();
     if (r >= 0) ptx::bulk_store(dst + (size_t)r * rec_bytes, rec, rec_bytes);
     ptx::bulk_commit();
   }
@@ -144,11 +153,13 @@ size_t scatter_mx3_smem_bytes(int K, int in_elem_bytes, bool f8) {
 template <typename TIn, bool F8>
 cudaError_t launch_scatter_typed(const void* src, void* dst, const int32_t* row_of, int T, int k, int K, uint32_t* status,
                                  uint64_t timeout_ns, size_t smem, int grid, cudaStream_t s) {
-  auto kern = scatter_mx3_kernel<TIn, F8>;
+  // a CTA per token: four warps share each token's blocks; otherwise one warp pipelines its tokens
+  const bool wide = grid >= T;
+  auto kern = wide ? scatter_mx3_kernel<TIn, F8, 4> : scatter_mx3_kernel<TIn, F8, 1>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  kern<<<grid, 32, smem, s>>>(static_cast<const TIn*>(src), static_cast<uint8_t*>(dst), row_of, T, k, K, status,
-                              timeout_ns);
+  kern<<<grid, wide ? 128 : 32, smem, s>>>(static_cast<const TIn*>(src), static_cast<uint8_t*>(dst), row_of, T, k, K,
+                                           status, timeout_ns);
   return cudaGetLastError();
 }
 

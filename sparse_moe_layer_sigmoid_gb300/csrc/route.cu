@@ -572,15 +572,97 @@ __device__ __forceinline__ void build_contenders(const TopkState<NPL>& st, float
   }
 }
 
+// 16-byte asynchronous copies of `bytes` (a multiple of 16) from global to shared memory by the
+// `n` threads of the group, thread `i` taking chunks i, i + n, ...
+__device__ __forceinline__ void cp_async_bytes(uint8_t* dst, const uint8_t* src, int64_t bytes, int i, int n) {
+#pragma unroll 4
+  for (int64_t o = (int64_t)i * 16; o < bytes; o += (int64_t)n * 16)
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(ptx::smem_addr(dst + o)),
+                 "l"(__cvta_generic_to_global(src + o))
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
+// This thread's part of x . w over staged rows: elements i*8 .. i*8+7, + 8n, + 16n, ... in
+// double-float (the arithmetic of dots_df_part).
+template <typename TX, typename TW>
+__device__ __forceinline__ DF dot_staged(const uint8_t* sx, const uint8_t* sw, int d, int i, int n) {
+  const TX* x = reinterpret_cast<const TX*>(sx);
+  const TW* w = reinterpret_cast<const TW*>(sw);
+  DF a{0.f, 0.f};
+#pragma unroll 1
+  for (int c = i * 8; c < d; c += n * 8) {
+    float xf[8], wf[8];
+    load8(x + c, xf);
+    load8(w + c, wf);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) df_add_prod(a, xf[j], wf[j]);
+  }
+  return a;
+}
+
+// Shared-memory staging of the exact logits (short-batch selection): x's row and up to
+// `rows` router rows per batch, `bytes_x` / `bytes_w` each.
+struct RefineStage {
+  uint8_t* mem;  // nullptr: the logits are recomputed from global memory (dots_df_part)
+  int rows;
+};
+
 // All G warps: recompute the listed logits, then warp 0 ranks the contenders and writes the list.
+// With a stage (G warps = the whole CTA) the CTA copies x's row and a batch of router rows into
+// shared memory in one round of asynchronous copies and every thread sums its elements of each
+// row; warp gw's partial covers its lanes' elements.  Without, warp gw sums the 256-element blocks
+// gw, gw + G, ... of d straight from global memory.
 template <int NPL, int G>
 __device__ __forceinline__ void refine_finish(const float* __restrict__ logits, const float* __restrict__ bias,
                                               const RouterSrc& src, int t, int E, int k, int32_t* __restrict__ idx,
                                               float* __restrict__ p, int gw, int lane, const RefineSmem& sm,
-                                              uint32_t* status, int32_t* near_ties) {
+                                              uint32_t* status, int32_t* near_ties, RefineStage stage = {nullptr, 0}) {
   group_sync<G>();
   const int n_cont = sm.n[0], n_rc = sm.n[1];
-  for (int b0 = 0; b0 < n_rc; b0 += kCandBatch) {
+  if (stage.mem) {
+    const int tid = gw * 32 + lane, nthr = 32 * G;
+    const int64_t bx = (int64_t)src.d * (src.x_dtype == kBF16 ? 2 : 4);
+    const int64_t bw = (int64_t)src.d * (src.w_dtype == kBF16 ? 2 : 4);
+    uint8_t* sx = stage.mem;
+    uint8_t* sw = stage.mem + bx;
+#pragma unroll 1
+    for (int b0 = 0; b0 < n_rc; b0 += stage.rows) {
+      const int nc = n_rc - b0 < stage.rows ? n_rc - b0 : stage.rows;
+      if (b0 == 0) cp_async_bytes(sx, static_cast<const uint8_t*>(src.x) + (int64_t)t * bx, bx, tid, nthr);
+#pragma unroll 1
+      for (int m = 0; m < nc; ++m)
+        cp_async_bytes(sw + m * bw, static_cast<const uint8_t*>(src.w) + (int64_t)sm.ce[sm.cand[b0 + m]] * bw, bw,
+                       tid, nthr);
+      cp_async_wait_all();
+      group_sync<G>();
+#pragma unroll 1
+      for (int m = 0; m < nc; ++m) {
+        const uint8_t* wr = sw + m * bw;
+        DF a;
+        if (src.x_dtype == kBF16 && src.w_dtype == kBF16)
+          a = dot_staged<__nv_bfloat16, __nv_bfloat16>(sx, wr, src.d, tid, nthr);
+        else if (src.x_dtype == kBF16)
+          a = dot_staged<__nv_bfloat16, float>(sx, wr, src.d, tid, nthr);
+        else if (src.w_dtype == kBF16)
+          a = dot_staged<float, __nv_bfloat16>(sx, wr, src.d, tid, nthr);
+        else
+          a = dot_staged<float, float>(sx, wr, src.d, tid, nthr);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+          DF o;
+          o.hi = __shfl_xor_sync(0xffffffffu, a.hi, off);
+          o.lo = __shfl_xor_sync(0xffffffffu, a.lo, off);
+          a = df_add(a, o);
+        }
+        if (lane == 0) sm.part[gw * kMaxCont + b0 + m] = make_float2(a.hi, a.lo);
+      }
+      group_sync<G>();  // the stage is rewritten by the next batch
+    }
+  }
+  for (int b0 = 0; !stage.mem && b0 < n_rc; b0 += kCandBatch) {
     int ce[kCandBatch];
     const int nc = n_rc - b0 < kCandBatch ? n_rc - b0 : kCandBatch;
 #pragma unroll
@@ -705,28 +787,53 @@ __global__ void __launch_bounds__(32 * kRefineWarps, 4) topk_refine_kernel(
 // per thread in registers), each step is a short loop shared by the CTA's threads, and only the
 // rare fallback (more than 64 keys at or above the bound) runs the one-warp selection of
 // topk_pass.  Steps:
-//   bound     lb = the k-th largest of the threads' largest keys (bisection, a CTA count per
-//             probe): k threads hold keys at least that large, so every selected key is >= lb;
+//   bound     lb = the k-th largest of 32 group maxima (group g: the keys of threads g, g + 32,
+//             ..., 28 of E = 896), a 32-entry sort in warp 0: k groups hold keys at least that
+//             large, so every selected key is >= lb;
 //   rank      the keys >= lb (at most 64) sorted by (key descending, index ascending) in warp 0:
 //             ranks 0..k-1 and the (k+1)-th key (or the largest key below lb);
 //   settle    as topk_refine_kernel: when the list's order is not certain within the key
 //             uncertainty, the contenders (the selected experts and, at an uncertain boundary,
 //             the band) are listed in ascending expert order and the CTA's warps settle them
-//             with refine_finish.
+//             with refine_finish, from x's row and the router rows staged in shared memory
+//             (`stage_rows` rows per batch; 0: straight from global memory).
 // refine_count[0] counts the settled tokens, refine_count[1] the near ties.
 constexpr int kSmallWarps = 8;
 constexpr int kSmallThreads = 32 * kSmallWarps;
 constexpr int kSmallSlots = 4;  // keys per thread: E <= kSmallSlots * kSmallThreads
+constexpr int kSmallStageRows = 4;                   // router rows staged per batch
+constexpr size_t kSmallStageMax = 100 * 1024;        // staging budget (two CTAs per SM fit)
 
-size_t topk_small_smem(int E) { return (size_t)E * (sizeof(float) + 1); }
+// Dynamic shared memory: keys, scores and flags of the E experts, then the staging area.
+__device__ __forceinline__ size_t topk_small_keys_bytes_dev(int E) {
+  return ((size_t)E * (2 * sizeof(float) + 1) + 15) / 16 * 16;
+}
+size_t topk_small_keys_bytes(int E) { return ((size_t)E * (2 * sizeof(float) + 1) + 15) / 16 * 16; }
+int topk_small_stage_rows(const RouterSrc& src) {
+  const size_t bx = (size_t)src.d * (src.x_dtype == kBF16 ? 2 : 4);
+  const size_t bw = (size_t)src.d * (src.w_dtype == kBF16 ? 2 : 4);
+  for (int r = kSmallStageRows; r > 0; --r)
+    if (bx + r * bw <= kSmallStageMax) return r;
+  return 0;
+}
+size_t topk_small_smem(int E, const RouterSrc& src) {
+  const int r = topk_small_stage_rows(src);
+  const size_t bx = (size_t)src.d * (src.x_dtype == kBF16 ? 2 : 4);
+  const size_t bw = (size_t)src.d * (src.w_dtype == kBF16 ? 2 : 4);
+  return topk_small_keys_bytes(E) + (r > 0 ? bx + r * bw : 0);
+}
 
 template <int NPL>
 __global__ void __launch_bounds__(kSmallThreads, 2) topk_small_kernel(
     const float* __restrict__ logits, const float* __restrict__ bias, RouterSrc src, int T, int E, int k,
-    int32_t* __restrict__ idx, float* __restrict__ p, int32_t* __restrict__ refine_count, uint32_t* status) {
-  extern __shared__ float s_dyn[];
-  float* s_sv = s_dyn;                                       // [E] scores
-  uint8_t* s_flag = reinterpret_cast<uint8_t*>(s_dyn + E);  // [E] 1: selected, 2: recompute
+    int32_t* __restrict__ idx, float* __restrict__ p, int32_t* __restrict__ refine_count, uint32_t* status,
+    int stage_rows) {
+  extern __shared__ __align__(16) float s_dyn[];
+  float* s_sv = s_dyn;                                           // [E] scores
+  float* s_kf = s_dyn + E;                                       // [E] keys
+  uint8_t* s_flag = reinterpret_cast<uint8_t*>(s_dyn + 2 * E);  // [E] 1: selected, 2: recompute
+  const RefineStage stage{stage_rows > 0 ? reinterpret_cast<uint8_t*>(s_dyn) + topk_small_keys_bytes_dev(E) : nullptr,
+                          stage_rows};
   __shared__ uint64_t s_ck[64];  // candidates: orderable key << 32 | (0xFFFF - expert) << 16
   __shared__ float s_ss[64];     // topk_pass scratch
   __shared__ int s_ce[kMaxCont];
@@ -740,6 +847,8 @@ __global__ void __launch_bounds__(kSmallThreads, 2) topk_small_kernel(
   __shared__ float s_ak, s_ak1;
   __shared__ int s_need, s_unc;
   __shared__ int s_wc[kSmallWarps], s_wr[kSmallWarps];
+  __shared__ uint32_t s_tmax[kSmallThreads];
+  __shared__ uint32_t s_lb;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t lt_mask = (1u << lane) - 1u;
   const RefineSmem sm{s_ce, s_key, s_s, s_exa, s_cand, &s_part[0][0], s_n};
@@ -769,6 +878,7 @@ __global__ void __launch_bounds__(kSmallThreads, 2) topk_small_kernel(
         ko[i] = e < E ? orderable(kf[i]) : 0u;
         if (e < E) {
           s_sv[e] = s;
+          s_kf[e] = kf[i];
           s_flag[e] = 0;
         }
       }
@@ -776,16 +886,26 @@ __global__ void __launch_bounds__(kSmallThreads, 2) topk_small_kernel(
     uint32_t tmax = 0;
 #pragma unroll
     for (int i = 0; i < kSmallSlots; ++i) tmax = ko[i] > tmax ? ko[i] : tmax;
-    // bound: the largest v with at least k threads' largest keys >= v (uniform over the CTA)
-    uint32_t lo = 1, hi = 0xFFFFFFFFu;
-    while (lo < hi) {
-      const uint32_t mid = lo + ((hi - lo + 1u) >> 1);
-      if (__syncthreads_count(tmax >= mid) >= k)
-        lo = mid;
-      else
-        hi = mid - 1u;
+    s_tmax[tid] = tmax;
+    __syncthreads();
+    // bound (warp 0): the k-th largest group maximum, by a 32-entry bitonic sort (descending)
+    if (warp == 0) {
+      uint32_t v = 0;
+#pragma unroll
+      for (int j = 0; j < kSmallThreads / 32; ++j) v = s_tmax[lane + 32 * j] > v ? s_tmax[lane + 32 * j] : v;
+#pragma unroll
+      for (int size = 2; size <= 32; size <<= 1)
+#pragma unroll
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+          const uint32_t o = __shfl_xor_sync(0xffffffffu, v, stride);
+          const bool keep_max = ((lane & stride) == 0) == ((lane & size) == 0);
+          v = keep_max ? (o > v ? o : v) : (o < v ? o : v);
+        }
+      const uint32_t lb_w = __shfl_sync(0xffffffffu, v, k - 1);
+      if (lane == 0) s_lb = lb_w;
     }
-    const uint32_t lb = lo;
+    __syncthreads();
+    const uint32_t lb = s_lb;
     uint32_t below = 0;
 #pragma unroll
     for (int i = 0; i < kSmallSlots; ++i) {
@@ -873,13 +993,15 @@ __global__ void __launch_bounds__(kSmallThreads, 2) topk_small_kernel(
       const bool unc = s_unc != 0;
       const float band_hi = a_k + eta2, band_lo = a_k1 - eta2;
       int n_cont = 0, n_rc = 0;
-#pragma unroll
+#pragma unroll 1
       for (int i = 0; i < kSmallSlots; ++i) {
         const int e = tid + kSmallThreads * i;
         int f = 0;
+        float kfe = 0.f;
         if (e < E) {
           f = s_flag[e];
-          if (unc && kf[i] >= band_lo && kf[i] <= band_hi) f |= 2;
+          kfe = s_kf[e];
+          if (unc && kfe >= band_lo && kfe <= band_hi) f |= 2;
         }
         const uint32_t mc = __ballot_sync(0xffffffffu, f != 0);
         if (lane == 0) s_wc[warp] = __popc(mc);
@@ -904,8 +1026,8 @@ __global__ void __launch_bounds__(kSmallThreads, 2) topk_small_kernel(
         }
         if (in) {
           s_ce[at] = e;
-          s_key[at] = orderable64((double)kf[i]);
-          s_s[at] = sv[i];
+          s_key[at] = orderable64((double)kfe);
+          s_s[at] = s_sv[e];
           s_exa[at] = 0;
           if (r) s_cand[n_rc + before_r + __popc(mr & lt_mask)] = at;
         }
@@ -919,7 +1041,7 @@ __global__ void __launch_bounds__(kSmallThreads, 2) topk_small_kernel(
         s_n[1] = n_rc;
       }
       refine_finish<NPL, kSmallWarps>(logits, bias, src, t, E, k, idx, p, warp, lane, sm, status,
-                                      refine_count + 1);
+                                      refine_count + 1, stage);
     }
     __syncthreads();  // shared memory is reused by the next token
   }
@@ -948,15 +1070,23 @@ __device__ __forceinline__ void build_masks(const int32_t* __restrict__ idx, int
   __syncthreads();
   const int t = blockIdx.x * kDispatchChunk + threadIdx.x;
   if (t < T) {
-    for (int j = 0; j < k; ++j) {
-      const int e = idx[(size_t)t * k + j];
-      if (e < 0 || e >= E) {
-        report(status, kStatusDeviceCheck);
-        continue;
+    // the token's expert ids eight at a time, each batch's loads in flight together
+    for (int j0 = 0; j0 < k; j0 += 8) {
+      int ex[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) ex[u] = j0 + u < k ? __ldg(idx + (size_t)t * k + j0 + u) : 0;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (j0 + u >= k) break;
+        const int e = ex[u];
+        if (e < 0 || e >= E) {
+          report(status, kStatusDeviceCheck);
+          continue;
+        }
+        const uint32_t bit = 1u << (threadIdx.x & 31);
+        const uint32_t old = atomicOr(&mask[e * kMaskWords + (threadIdx.x >> 5)], bit);
+        if (old & bit) report(status, kStatusDeviceCheck);
       }
-      const uint32_t bit = 1u << (threadIdx.x & 31);
-      const uint32_t old = atomicOr(&mask[e * kMaskWords + (threadIdx.x >> 5)], bit);
-      if (old & bit) report(status, kStatusDeviceCheck);
     }
   }
   __syncthreads();
@@ -977,8 +1107,8 @@ __global__ void __launch_bounds__(kDispatchChunk) dispatch_count_kernel(const in
 }
 
 // Per-expert row offsets, chunk bases and the four tile lists from thread e's expert total
-// (1024 threads, E <= 1024): Hillis-Steele inclusive scans over 1024 entries (fixed order,
-// integer: exact).  Returns the expert's first row.
+// (1024 threads, E <= 1024): inclusive scans over the 1024 entries, within each warp by shuffles
+// and then over the 32 warp totals (integer: exact).  Returns the expert's first row.
 struct ScanSmem {
   int *cnt, *tiles, *tiles_s, *tiles_p, *tiles_m;  // [1024] each
 };
@@ -991,31 +1121,41 @@ __device__ __forceinline__ int scan_experts(int e, int total, int E, const ScanS
   const int nts = (total + kTileS - 1) / kTileS;
   const int ntp = (total + kTileP - 1) / kTileP;
   const int ntm = (total + kTileMx - 1) / kTileMx;
-  sh.cnt[e] = total;
-  sh.tiles[e] = nt;
-  sh.tiles_s[e] = nts;
-  sh.tiles_p[e] = ntp;
-  sh.tiles_m[e] = ntm;
+  int* const arr[5] = {sh.cnt, sh.tiles, sh.tiles_s, sh.tiles_p, sh.tiles_m};  // [32] warp totals each
+  int v[5] = {total, nt, nts, ntp, ntm};
+  const int lane = e & 31, w = e >> 5;
+#pragma unroll
+  for (int q = 0; q < 5; ++q)
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, v[q], off);
+      if (lane >= off) v[q] += o;
+    }
+  if (lane == 31)
+#pragma unroll
+    for (int q = 0; q < 5; ++q) arr[q][w] = v[q];
   __syncthreads();
-  for (int off = 1; off < 1024; off <<= 1) {
-    const int a = e >= off ? sh.cnt[e - off] : 0;
-    const int b = e >= off ? sh.tiles[e - off] : 0;
-    const int c = e >= off ? sh.tiles_s[e - off] : 0;
-    const int f = e >= off ? sh.tiles_p[e - off] : 0;
-    const int m = e >= off ? sh.tiles_m[e - off] : 0;
-    __syncthreads();
-    sh.cnt[e] += a;
-    sh.tiles[e] += b;
-    sh.tiles_s[e] += c;
-    sh.tiles_p[e] += f;
-    sh.tiles_m[e] += m;
-    __syncthreads();
+  if (w == 0) {
+#pragma unroll
+    for (int q = 0; q < 5; ++q) {
+      int x = arr[q][lane];
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, x, off);
+        if (lane >= off) x += o;
+      }
+      arr[q][lane] = x;  // inclusive over warps 0..lane
+    }
   }
-  const int row0 = sh.cnt[e] - total;
-  const int tile0 = sh.tiles[e] - nt;
-  const int tile0s = sh.tiles_s[e] - nts;
-  const int tile0p = sh.tiles_p[e] - ntp;
-  const int tile0m = sh.tiles_m[e] - ntm;
+  __syncthreads();
+#pragma unroll
+  for (int q = 0; q < 5; ++q) v[q] += w > 0 ? arr[q][w - 1] : 0;  // inclusive over entries 0..e
+  __syncthreads();  // the warp totals may be rewritten by the caller
+  const int row0 = v[0] - total;
+  const int tile0 = v[1] - nt;
+  const int tile0s = v[2] - nts;
+  const int tile0p = v[3] - ntp;
+  const int tile0m = v[4] - ntm;
   if (e < E) {
     offsets[e] = row0;
     for (int j = 0; j < nt; ++j) tiles[tile0 + j] = make_int4(e, tile0, total, row0);
@@ -1027,11 +1167,11 @@ __device__ __forceinline__ int scan_experts(int e, int total, int E, const ScanS
       for (int j = 0; j < ntm; ++j) tiles_m[tile0m + j] = make_int4(e, tile0m, total, row0);
   }
   if (e == E - 1) {
-    offsets[E] = sh.cnt[e];
-    *num_tiles = sh.tiles[e];
-    if (num_tiles_s) *num_tiles_s = sh.tiles_s[e];
-    if (num_tiles_p) *num_tiles_p = sh.tiles_p[e];
-    if (num_tiles_m) *num_tiles_m = sh.tiles_m[e];
+    offsets[E] = v[0];
+    *num_tiles = v[1];
+    if (num_tiles_s) *num_tiles_s = v[2];
+    if (num_tiles_p) *num_tiles_p = v[3];
+    if (num_tiles_m) *num_tiles_m = v[4];
   }
   return row0;
 }
@@ -1087,19 +1227,31 @@ __global__ void __launch_bounds__(1024) dispatch_small_kernel(
   if (t >= T) return;
   const int w = t >> 5;
   const uint32_t below = (1u << (t & 31)) - 1u;
-  for (int j = 0; j < k; ++j) {
-    const int ex = idx[(size_t)t * k + j];
-    if (ex < 0 || ex >= E) {
-      if (row_of) row_of[(size_t)t * k + j] = -1;
-      continue;
+  for (int j0 = 0; j0 < k; j0 += 8) {  // eight selections at a time, their loads in flight together
+    int exs[8];
+    float ps[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      exs[u] = j0 + u < k ? __ldg(idx + (size_t)t * k + j0 + u) : 0;
+      ps[u] = p && j0 + u < k ? __ldg(p + (size_t)t * k + j0 + u) : 1.0f;
     }
-    const uint32_t* m = mask + ex * kMaskWords;
-    int rank = __popc(m[w] & below);
-    for (int q = 0; q < w; ++q) rank += __popc(m[q]);
-    const int row = s_row0[ex] + rank;
-    if (row_of) row_of[(size_t)t * k + j] = row;
-    if (tok_of_row) tok_of_row[row] = t;
-    if (p_row) p_row[row] = p ? p[(size_t)t * k + j] : 1.0f;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int j = j0 + u;
+      if (j >= k) break;
+      const int ex = exs[u];
+      if (ex < 0 || ex >= E) {
+        if (row_of) row_of[(size_t)t * k + j] = -1;
+        continue;
+      }
+      const uint32_t* m = mask + ex * kMaskWords;
+      int rank = __popc(m[w] & below);
+      for (int q = 0; q < w; ++q) rank += __popc(m[q]);
+      const int row = s_row0[ex] + rank;
+      if (row_of) row_of[(size_t)t * k + j] = row;
+      if (tok_of_row) tok_of_row[row] = t;
+      if (p_row) p_row[row] = ps[u];
+    }
   }
 }
 
@@ -1270,8 +1422,14 @@ cudaError_t launch_topk(const float* logits, const float* bias, const RouterSrc&
 #define LMOE_TOPK(N)                                                                                     \
   do {                                                                                                   \
     if (fused) {                                                                                         \
-      topk_small_kernel<N><<<T, kSmallThreads, topk_small_smem(E), s>>>(logits, bias, src, T, E, k, idx, p, \
-                                                                        refine_count, status);            \
+      const size_t smem = topk_small_smem(E, src);                                                       \
+      if (smem > 48 * 1024) {                                                                            \
+        const cudaError_t ea = cudaFuncSetAttribute(topk_small_kernel<N>,                                \
+                                                    cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem); \
+        if (ea != cudaSuccess) return ea;                                                                \
+      }                                                                                                  \
+      topk_small_kernel<N><<<T, kSmallThreads, smem, s>>>(logits, bias, src, T, E, k, idx, p, refine_count, \
+                                                          status, topk_small_stage_rows(src));            \
     } else {                                                                                             \
       topk_kernel<N><<<grid, block, 0, s>>>(logits, bias, src, T, E, k, idx, p, refine_list, refine_count); \
       topk_refine_kernel<N><<<rgrid, 128, 0, s>>>(logits, bias, src, E, k, idx, p, refine_list, refine_count, \

@@ -401,11 +401,12 @@ def test_exact_ties_go_to_the_lower_index(binding, cfg):
 
 @pytest.mark.parametrize("tokens", [40, 600], ids=lambda t: f"T{t}")
 def test_clustered_keys_take_the_bisection_fallback(binding, tokens):
-    """The 128 largest keys sit four to a thread of the short-batch selection's 256-thread layout
-    (expert tid + 256 i holds rank 4 tid + i), so the 32nd-largest thread maximum, its bound, lets
-    125 keys through: more than its 64-entry sort, which hands the token to the bisection
-    selection.  Logits are exact (one non-zero column of x and W_r, bf16-representable values):
-    the selection must be the oracle's, ranks 0..31 in order.  T=600 runs the two-kernel path."""
+    """The 128 largest keys sit four to a group of the short-batch selection's bound (expert
+    e = r // 4 + 256 (r % 4) holds rank r: group e % 32 = r // 4, one CTA thread r // 4), so the
+    32nd-largest group maximum, the bound, lets 125 keys through: more than its 64-entry sort,
+    which hands the token to the bisection selection.  Logits are exact (one non-zero column of x
+    and W_r, bf16-representable values): the selection must be the oracle's, ranks 0..31 in
+    order.  T=600 runs the two-kernel path."""
     cfg = replace(configs.ROUTING_DISPATCH_STRESS, name="clustered_keys", tokens=tokens, d=512, latent=256,
                   experts=896, top_k=32, bias="none", router_w="bf16", seed=45)
     E, k = cfg.experts, cfg.top_k
