@@ -81,7 +81,7 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const T* __restrict__
     s_w[threadIdx.x] = p ? p[(size_t)t * k + threadIdx.x] : 1.0f;
   }
   __syncthreads();
-  constexpr int U = VPT <= 4 ? 8 : 4;
+  constexpr int U = VPT <= 4 ? 4 : 2;
   for (int j0 = 0; j0 < k; j0 += U) {
     int r[U];
     float w[U];

@@ -556,7 +556,9 @@ cudaError_t launch_tc_gemm(const TcGemm& g, uint32_t* status, uint64_t timeout_n
     if (splits > p.num_kb / 4) splits = p.num_kb / 4;  // at least 4 k-blocks per split
     if (splits < 1) splits = 1;
   }
-  if (g.launch_count) *g.launch_count += splits > 1 ? 2 : 1;
+  const bool defer = g.defer && g.epi == kEpiF32;
+  if (defer) g.defer->splits = 0;
+  if (g.launch_count) *g.launch_count += splits > 1 && !defer ? 2 : 1;
   if (fp4) {
     if (!grouped) return cudaErrorInvalidValue;
     switch (g.epi) {
@@ -575,6 +577,10 @@ cudaError_t launch_tc_gemm(const TcGemm& g, uint32_t* status, uint64_t timeout_n
     if ((size_t)p.k_splits * p.split_stride * sizeof(float) > g.partial_bytes) return cudaErrorInvalidValue;
     const long long work = tiles * p.k_splits;
     const int grid_s = (int)(work < num_sms ? work : num_sms);
+    if (defer) {  // the consumer adds the partial sums
+      *g.defer = SplitPartials{p.partial, p.k_splits, p.split_stride, p.ldp};
+      return launch_inst<256, kEpiF32, false, false, false, true>(ma, mb0, mb1, p, grid_s, s);
+    }
     switch (g.epi) {
       case kEpiBF16: return launch_split<kEpiBF16>(ma, mb0, mb1, p, grid_s, s);
       case kEpiF16: return launch_split<kEpiF16>(ma, mb0, mb1, p, grid_s, s);

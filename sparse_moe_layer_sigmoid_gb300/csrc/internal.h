@@ -28,6 +28,14 @@ struct PerDeviceValue {
 };
 
 // ---------------------------------------------------------------- routing (route.cu)
+// Split-K partial sums of a GEMM left for the consumer to add: output [row][col] = sum over
+// s = 0..splits-1, in that order, of part[s * split_stride + row * ldp + col].  splits == 0: the
+// output was written whole (no split).
+struct SplitPartials {
+  const float* part;
+  int splits;
+  int64_t split_stride, ldp;
+};
 // logits[T][E] = x[T][d] . W_r[E][d]^T in fp32 (CUDA cores, fixed K order per output).
 cudaError_t launch_router_logits(const void* x, int x_dtype, const void* w_router, int w_dtype, float* logits,
                                  int T, int E, int d, cudaStream_t s);
@@ -36,10 +44,12 @@ cudaError_t launch_router_logits(const void* x, int x_dtype, const void* w_route
 // K = 3d), fp32 activations the CUDA-core GEMM.  Adds its kernel count to *launches.
 // With `pair_ok`, a router GEMM of at least 256 rows whose 128-row tiles would more than half
 // fill the SMs runs on CTA pairs; fewer tiles split K on single CTAs (`splitk` workspace).
+// With `defer` (non-null) a split-K router GEMM leaves its partial sums unreduced and describes
+// them there (the short-batch top-k adds them); defer->splits == 0 when logits were written.
 cudaError_t launch_router(const void* x, int act, const void* w_router, int router_w, float* logits,
                           void* wr_split, int T, int E, int d, uint32_t* status, uint64_t timeout_ns, int num_sms,
                           int* launches, cudaStream_t s, float* splitk = nullptr, size_t splitk_bytes = 0,
-                          bool pair_ok = false);
+                          bool pair_ok = false, SplitPartials* defer = nullptr);
 // Exact split of fp32 W_r into three bf16 terms, out[t][e][c], t = hi, mid, lo:
 // w = hi + mid + lo with each term the bf16 rounding of what the previous terms left.
 cudaError_t launch_split_bf16x3(const float* w, int64_t n, void* out, cudaStream_t s);
@@ -61,9 +71,13 @@ constexpr float kRouterLogitMargin = 1e-3f;
 // the number of near ties (exact k-th/(k+1)-th key gap below 1e-6); both are reset here.  A
 // recomputed logit further than margin/2 from the GEMM's sets kStatusDeviceCheck |
 // kStatusRouterMargin in *status (may be null).
-cudaError_t launch_topk(const float* logits, const float* bias, const RouterSrc& src, int T, int E, int k,
-                        int32_t* idx, float* p, int32_t* refine_list, int32_t* refine_count, uint32_t* status,
-                        int num_sms, cudaStream_t s);
+// Batches of at most kTopkFusedMaxT tokens run both passes in one kernel; there `part` (when its
+// splits > 0) holds the router GEMM's unreduced split-K sums, which the kernel adds in split order
+// (the arithmetic of the split-K reduction) and writes to `logits`.
+constexpr int kTopkFusedMaxT = 512;
+cudaError_t launch_topk(float* logits, const float* bias, const RouterSrc& src, int T, int E, int k, int32_t* idx,
+                        float* p, int32_t* refine_list, int32_t* refine_count, uint32_t* status, int num_sms,
+                        cudaStream_t s, const SplitPartials* part = nullptr);
 // Deterministic expert batches: per-chunk counts, scan, stable (expert, token) rows, the
 // grouped-GEMM M-tile list, and per-row weights.  idx entries outside [0,E) are reported.
 struct DispatchBuffers {
@@ -166,6 +180,7 @@ struct TcGemm {
   const uint8_t* b_scale;    // non-null: B0 holds packed E2M1 bytes, b_scale E8M0 [depth][rows][K/32]
   float* partial;            // split-K workspace (dense GEMMs of few tiles) or nullptr: no split
   size_t partial_bytes;      // its size (tc_splitk_partial_bytes)
+  SplitPartials* defer;      // non-null (fp32 epilogue): leave split-K sums unreduced, described here
   int* launch_count;         // incremented by the number of kernels launched (or nullptr)
 };
 // Workspace the split-K path needs at most (splits x tiles <= SMs, 128 rows x 256 fp32 columns each).

@@ -236,13 +236,15 @@ lmoe_status run_routing(lmoe_handle* h, const void* x, int T, const lmoe_weights
   const float* p = ext_p;
   if (!ext_idx) {
     stage_begin(h, kStRouter, s);
+    // short batches: the top-k kernel adds the router GEMM's split-K sums itself
+    SplitPartials part{nullptr, 0, 0, 0};
     LMOE_TRY(launch_router(x, c.act, w->w_router, c.router_w, h->logits, h->wr_split, T, c.num_experts, c.d,
                            h->status, h->timeout_ns, h->num_sms, &h->last_launches, s, h->splitk, h->splitk_bytes,
-                           !(c.flags & LMOE_FLAG_SINGLE_CTA_GEMM)));
+                           !(c.flags & LMOE_FLAG_SINGLE_CTA_GEMM), T <= kTopkFusedMaxT ? &part : nullptr));
     stage_end(h, kStRouter, s);
     const RouterSrc rs{x, c.act, w->w_router, c.router_w, c.d, kRouterLogitMargin};
     LMOE_TRY(launch_topk(h->logits, w->router_bias, rs, T, c.num_experts, c.top_k, h->idx, h->p, h->refine_list,
-                         h->refine_count, h->status, h->num_sms, s));
+                         h->refine_count, h->status, h->num_sms, s, &part));
     stage_end(h, kStTopk, s);
     h->last_launches += 2;
     idx = h->idx;

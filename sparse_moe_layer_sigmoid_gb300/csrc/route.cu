@@ -212,8 +212,9 @@ __device__ __forceinline__ void topk_keys(const float* __restrict__ logits, cons
 
 template <int NPL>
 __device__ __forceinline__ void topk_pass(const float* __restrict__ logits, const float* __restrict__ bias, int t,
-                                          int E, int k, int lane, TopkState<NPL>& st, uint64_t* sk, float* ss) {
-  topk_keys<NPL>(logits, bias, t, E, lane, st);
+                                          int E, int k, int lane, TopkState<NPL>& st, uint64_t* sk, float* ss,
+                                          bool keys_ready = false) {
+  if (!keys_ready) topk_keys<NPL>(logits, bias, t, E, lane, st);  // else st.kf / st.sv are filled
   uint32_t ko[NPL];  // orderable keys; 0 (below every key) for slots past E
   uint32_t kmax = 0;
 #pragma unroll
@@ -465,7 +466,6 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ log
 }
 
 constexpr int kRefineWarps = 4;  // warps of a refinement CTA
-constexpr int kTopkFusedMaxT = 512;  // batches up to this many tokens run topk_small_kernel
 constexpr int kMaxCont = 64;     // contenders of one token: its selected experts and the band
 
 // Shared memory of one refinement group (a warp, or the whole CTA): the token's contenders.
@@ -611,12 +611,12 @@ struct RefineStage {
 };
 
 // All G warps: recompute the listed logits, then warp 0 ranks the contenders and writes the list.
-// With a stage (G warps = the whole CTA) the CTA copies x's row and a batch of router rows into
+// `lrow`: the token's logits from the router GEMM (global or shared memory).  With a stage (G warps = the whole CTA) the CTA copies x's row and a batch of router rows into
 // shared memory in one round of asynchronous copies and every thread sums its elements of each
 // row; warp gw's partial covers its lanes' elements.  Without, warp gw sums the 256-element blocks
 // gw, gw + G, ... of d straight from global memory.
 template <int NPL, int G>
-__device__ __forceinline__ void refine_finish(const float* __restrict__ logits, const float* __restrict__ bias,
+__device__ __forceinline__ void refine_finish(const float* lrow, const float* __restrict__ bias,
                                               const RouterSrc& src, int t, int E, int k, int32_t* __restrict__ idx,
                                               float* __restrict__ p, int gw, int lane, const RefineSmem& sm,
                                               uint32_t* status, int32_t* near_ties, RefineStage stage = {nullptr, 0}) {
@@ -685,7 +685,7 @@ __device__ __forceinline__ void refine_finish(const float* __restrict__ logits, 
       const int e = sm.ce[at];
       const double l64 = (double)a.hi + (double)a.lo;
       // the margin the selection relies on, checked on every logit recomputed here
-      if (fabs((double)logits[(size_t)t * E + e] - l64) > 0.5 * (double)src.margin)
+      if (fabs((double)lrow[e] - l64) > 0.5 * (double)src.margin)
         report(status, kStatusDeviceCheck | kStatusRouterMargin);
       const double s64 = 1.0 / (1.0 + exp(-l64));
       sm.key[at] = orderable64(s64 + (bias ? (double)bias[e] : 0.0));
@@ -748,7 +748,7 @@ __device__ __forceinline__ void refine_token(const float* __restrict__ logits, c
     st.a_k1 = n_ge > k ? st.a_k : below;
     build_contenders<NPL>(st, 2.0f * token_eta<NPL>(st.kf, st.sv, st.a_k1, src), E, k, lane, sm, status);
   }
-  refine_finish<NPL, G>(logits, bias, src, t, E, k, idx, p, gw, lane, sm, status, near_ties);
+  refine_finish<NPL, G>(logits + (size_t)t * E, bias, src, t, E, k, idx, p, gw, lane, sm, status, near_ties);
 }
 
 // Pass 2: the listed tokens.  With at least one token per warp each warp settles its own tokens;
@@ -806,9 +806,9 @@ constexpr size_t kSmallStageMax = 100 * 1024;        // staging budget (two CTAs
 
 // Dynamic shared memory: keys, scores and flags of the E experts, then the staging area.
 __device__ __forceinline__ size_t topk_small_keys_bytes_dev(int E) {
-  return ((size_t)E * (2 * sizeof(float) + 1) + 15) / 16 * 16;
+  return ((size_t)E * (3 * sizeof(float) + 1) + 15) / 16 * 16;
 }
-size_t topk_small_keys_bytes(int E) { return ((size_t)E * (2 * sizeof(float) + 1) + 15) / 16 * 16; }
+size_t topk_small_keys_bytes(int E) { return ((size_t)E * (3 * sizeof(float) + 1) + 15) / 16 * 16; }
 int topk_small_stage_rows(const RouterSrc& src) {
   const size_t bx = (size_t)src.d * (src.x_dtype == kBF16 ? 2 : 4);
   const size_t bw = (size_t)src.d * (src.w_dtype == kBF16 ? 2 : 4);
@@ -825,13 +825,14 @@ size_t topk_small_smem(int E, const RouterSrc& src) {
 
 template <int NPL>
 __global__ void __launch_bounds__(kSmallThreads, 2) topk_small_kernel(
-    const float* __restrict__ logits, const float* __restrict__ bias, RouterSrc src, int T, int E, int k,
-    int32_t* __restrict__ idx, float* __restrict__ p, int32_t* __restrict__ refine_count, uint32_t* status,
-    int stage_rows) {
+    float* logits, const float* __restrict__ bias, RouterSrc src, int T, int E, int k, int32_t* __restrict__ idx,
+    float* __restrict__ p, int32_t* __restrict__ refine_count, uint32_t* status, int stage_rows,
+    SplitPartials part) {
   extern __shared__ __align__(16) float s_dyn[];
   float* s_sv = s_dyn;                                           // [E] scores
   float* s_kf = s_dyn + E;                                       // [E] keys
-  uint8_t* s_flag = reinterpret_cast<uint8_t*>(s_dyn + 2 * E);  // [E] 1: selected, 2: recompute
+  float* s_lg = s_dyn + 2 * E;                                   // [E] logits
+  uint8_t* s_flag = reinterpret_cast<uint8_t*>(s_dyn + 3 * E);  // [E] 1: selected, 2: recompute
   const RefineStage stage{stage_rows > 0 ? reinterpret_cast<uint8_t*>(s_dyn) + topk_small_keys_bytes_dev(E) : nullptr,
                           stage_rows};
   __shared__ uint64_t s_ck[64];  // candidates: orderable key << 32 | (0xFFFF - expert) << 16
@@ -863,10 +864,43 @@ __global__ void __launch_bounds__(kSmallThreads, 2) topk_small_kernel(
     uint32_t ko[kSmallSlots];
     {
       float lg[kSmallSlots], bs[kSmallSlots];
+      if (part.splits > 0) {
+        // the router GEMM's split-K sums, added in split order from zero (the arithmetic of the
+        // split-K reduction), eight splits of every slot in flight at a time; then written out
+#pragma unroll
+        for (int i = 0; i < kSmallSlots; ++i) lg[i] = 0.f;
+        const float* pr = part.part + (int64_t)t * part.ldp;
+#pragma unroll 1
+        for (int s0 = 0; s0 < part.splits; s0 += 8) {
+          float a[kSmallSlots][8];
+#pragma unroll
+          for (int i = 0; i < kSmallSlots; ++i)
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              const int e = tid + kSmallThreads * i;
+              a[i][q] = e < E && s0 + q < part.splits ? pr[(int64_t)(s0 + q) * part.split_stride + e] : 0.f;
+            }
+#pragma unroll
+          for (int i = 0; i < kSmallSlots; ++i)
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              if (s0 + q < part.splits) lg[i] += a[i][q];
+        }
+#pragma unroll
+        for (int i = 0; i < kSmallSlots; ++i) {
+          const int e = tid + kSmallThreads * i;
+          if (e < E) logits[(size_t)t * E + e] = lg[i];
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < kSmallSlots; ++i) {
+          const int e = tid + kSmallThreads * i;
+          lg[i] = e < E ? logits[(size_t)t * E + e] : 0.f;
+        }
+      }
 #pragma unroll
       for (int i = 0; i < kSmallSlots; ++i) {
         const int e = tid + kSmallThreads * i;
-        lg[i] = e < E ? __ldg(logits + (size_t)t * E + e) : 0.f;
         bs[i] = bias && e < E ? __ldg(bias + e) : 0.f;
       }
 #pragma unroll
@@ -879,6 +913,7 @@ __global__ void __launch_bounds__(kSmallThreads, 2) topk_small_kernel(
         if (e < E) {
           s_sv[e] = s;
           s_kf[e] = kf[i];
+          s_lg[e] = lg[i];
           s_flag[e] = 0;
         }
       }
@@ -941,7 +976,13 @@ __global__ void __launch_bounds__(kSmallThreads, 2) topk_small_kernel(
         if (k < E) a_k1 = from_orderable(cnt > k ? (uint32_t)(entry_key(key, k) >> 32) : s_below);
       } else {  // many keys tie at or near the bound: the one-warp selection by bisection
         TopkState<NPL> st;
-        topk_pass<NPL>(logits, bias, t, E, k, lane, st, s_ck, s_ss);
+#pragma unroll
+        for (int i = 0; i < NPL; ++i) {
+          const int e = lane + 32 * i;
+          st.kf[i] = e < E ? s_kf[e] : -INFINITY;
+          st.sv[i] = e < E ? s_sv[e] : 0.f;
+        }
+        topk_pass<NPL>(logits, bias, t, E, k, lane, st, s_ck, s_ss, true);
         my_e = st.my_e;
         my_s = st.my_s;
         my_kf = st.my_kf;
@@ -1040,7 +1081,7 @@ __global__ void __launch_bounds__(kSmallThreads, 2) topk_small_kernel(
         s_n[0] = n_cont < kMaxCont ? n_cont : kMaxCont;
         s_n[1] = n_rc;
       }
-      refine_finish<NPL, kSmallWarps>(logits, bias, src, t, E, k, idx, p, warp, lane, sm, status,
+      refine_finish<NPL, kSmallWarps>(s_lg, bias, src, t, E, k, idx, p, warp, lane, sm, status,
                                       refine_count + 1, stage);
     }
     __syncthreads();  // shared memory is reused by the next token
@@ -1361,7 +1402,9 @@ cudaError_t launch_router_logits(const void* x, int x_dtype, const void* w_route
 
 cudaError_t launch_router(const void* x, int act, const void* w_router, int router_w, float* logits,
                           void* wr_split, int T, int E, int d, uint32_t* status, uint64_t timeout_ns, int num_sms,
-                          int* launches, cudaStream_t s, float* splitk, size_t splitk_bytes, bool pair_ok) {
+                          int* launches, cudaStream_t s, float* splitk, size_t splitk_bytes, bool pair_ok,
+                          SplitPartials* defer) {
+  if (defer) defer->splits = 0;
   if (act != kBF16) {
     if (launches) *launches += 1;
     return launch_router_logits(x, act, w_router, router_w, logits, T, E, d, s);
@@ -1390,6 +1433,7 @@ cudaError_t launch_router(const void* x, int act, const void* w_router, int rout
   g.ldc = E;
   g.partial = splitk;
   g.partial_bytes = splitk_bytes;
+  g.defer = defer;
   g.launch_count = launches;
   const long long single_tiles = (long long)((T + 127) / 128) * ((E + 255) / 256);
   if (pair_ok && T >= 256 && single_tiles * 2 > num_sms && tc_pair_supported(g)) {
@@ -1407,9 +1451,9 @@ cudaError_t launch_split_bf16x3(const float* w, int64_t n, void* out, cudaStream
   return cudaGetLastError();
 }
 
-cudaError_t launch_topk(const float* logits, const float* bias, const RouterSrc& src, int T, int E, int k,
-                        int32_t* idx, float* p, int32_t* refine_list, int32_t* refine_count, uint32_t* status,
-                        int num_sms, cudaStream_t s) {
+cudaError_t launch_topk(float* logits, const float* bias, const RouterSrc& src, int T, int E, int k, int32_t* idx,
+                        float* p, int32_t* refine_list, int32_t* refine_count, uint32_t* status, int num_sms,
+                        cudaStream_t s, const SplitPartials* part) {
   cudaError_t e = cudaMemsetAsync(refine_count, 0, 2 * sizeof(int32_t), s);
   if (e != cudaSuccess || T <= 0) return e;
   const int warps_per_block = 8;
@@ -1418,6 +1462,8 @@ cudaError_t launch_topk(const float* logits, const float* bias, const RouterSrc&
   // short batches: both passes in one kernel, a CTA per token (the latency of one token's
   // selection and refinement, not the throughput of many, sets the time)
   const bool fused = T <= kTopkFusedMaxT;
+  const SplitPartials sp = part ? *part : SplitPartials{nullptr, 0, 0, 0};
+  if (sp.splits > 0 && !fused) return cudaErrorInvalidValue;  // only the short-batch kernel adds partials
   const int npl = (E + 31) / 32;
 #define LMOE_TOPK(N)                                                                                     \
   do {                                                                                                   \
@@ -1429,7 +1475,7 @@ cudaError_t launch_topk(const float* logits, const float* bias, const RouterSrc&
         if (ea != cudaSuccess) return ea;                                                                \
       }                                                                                                  \
       topk_small_kernel<N><<<T, kSmallThreads, smem, s>>>(logits, bias, src, T, E, k, idx, p, refine_count, \
-                                                          status, topk_small_stage_rows(src));            \
+                                                          status, topk_small_stage_rows(src), sp);        \
     } else {                                                                                             \
       topk_kernel<N><<<grid, block, 0, s>>>(logits, bias, src, T, E, k, idx, p, refine_list, refine_count); \
       topk_refine_kernel<N><<<rgrid, 128, 0, s>>>(logits, bias, src, E, k, idx, p, refine_list, refine_count, \
