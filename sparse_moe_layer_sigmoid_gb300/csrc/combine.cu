@@ -2,8 +2,11 @@
 // eq. 11 "u = sum over the selected experts of p_i E_i(W_down x)", and section "What extreme
 // sparsity breaks": RMSNorm between aggregation and W_up).
 //
-// One CTA per token.  The k expert rows of the token are summed in rank order j = 0..k-1 in
-// fp32 registers (the same order on every run), then sum(u^2) is reduced in a fixed tree and
+// One CTA of 512 threads per token, whatever the batch size (the reduction tree below depends on
+// the CTA's width only, so a token's output does not depend on the batch).  The k expert rows of
+// the token are summed in rank order j = 0..k-1 in fp32 registers (the same order on every run),
+// U rows' loads in flight at a time (all 16 of a short batch's token at once, where latency rules;
+// fewer for long batches, where occupancy does), then sum(u^2) is reduced in a fixed tree and
 // n = u * g / sqrt(mean(u^2) + eps) is written.  HBM-bound: it reads k rows per token once.
 #include <cuda_fp16.h>
 
@@ -13,7 +16,8 @@
 namespace lmoe {
 namespace {
 
-constexpr int kThreads = 128;
+constexpr int kThreads = 512;
+constexpr int kShortBatch = 256;  // batches up to this many tokens load all of a token's rows at once
 
 template <typename T>
 struct Vec {  // 16-byte vector of T
@@ -56,7 +60,7 @@ __device__ __forceinline__ uint4 pack(const float (&f)[8], float) {
   return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]), __float_as_uint(f[3]));
 }
 
-template <typename T, typename TO, int VPT>
+template <typename T, typename TO, int VPT, int U>
 __global__ void __launch_bounds__(kThreads) combine_kernel(const T* __restrict__ o, const int32_t* __restrict__ row_of,
                                                            const float* __restrict__ p,
                                                            const float* __restrict__ gain, float eps, int k,
@@ -73,7 +77,7 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const T* __restrict__
 
   // the token's k row indices and weights first (one round of loads), then U expert rows at a
   // time: their loads are all issued before any is summed, and the sums still run in rank order
-  // j = 0..k-1.
+  // j = 0..k-1 (U does not change the arithmetic).
   __shared__ int s_r[32];
   __shared__ float s_w[32];
   if (threadIdx.x < k) {
@@ -81,7 +85,6 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const T* __restrict__
     s_w[threadIdx.x] = p ? p[(size_t)t * k + threadIdx.x] : 1.0f;
   }
   __syncthreads();
-  constexpr int U = VPT <= 4 ? 4 : 2;
   for (int j0 = 0; j0 < k; j0 += U) {
     int r[U];
     float w[U];
@@ -149,6 +152,16 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const T* __restrict__
   }
 }
 
+template <typename T, typename TO, int VPT>
+void launch_vpt(const T* op, const int32_t* row_of, const float* p, const float* gain, float eps, int T_, int k,
+                int width, TO* dp, int64_t ld_out, cudaStream_t s) {
+  constexpr int U_LONG = VPT == 1 ? 8 : 2;
+  if (T_ <= kShortBatch)
+    combine_kernel<T, TO, VPT, 16 / VPT><<<T_, kThreads, 0, s>>>(op, row_of, p, gain, eps, k, width, dp, ld_out);
+  else
+    combine_kernel<T, TO, VPT, U_LONG><<<T_, kThreads, 0, s>>>(op, row_of, p, gain, eps, k, width, dp, ld_out);
+}
+
 template <typename T, typename TO>
 cudaError_t launch_typed(const void* o, const int32_t* row_of, const float* p, const float* gain, float eps, int T_,
                          int k, int width, void* out, int64_t ld_out, cudaStream_t s) {
@@ -156,13 +169,11 @@ cudaError_t launch_typed(const void* o, const int32_t* row_of, const float* p, c
   const T* op = static_cast<const T*>(o);
   TO* dp = static_cast<TO*>(out);
   if (nvec <= kThreads)
-    combine_kernel<T, TO, 1><<<T_, kThreads, 0, s>>>(op, row_of, p, gain, eps, k, width, dp, ld_out);
+    launch_vpt<T, TO, 1>(op, row_of, p, gain, eps, T_, k, width, dp, ld_out, s);
   else if (nvec <= 2 * kThreads)
-    combine_kernel<T, TO, 2><<<T_, kThreads, 0, s>>>(op, row_of, p, gain, eps, k, width, dp, ld_out);
+    launch_vpt<T, TO, 2>(op, row_of, p, gain, eps, T_, k, width, dp, ld_out, s);
   else if (nvec <= 4 * kThreads)
-    combine_kernel<T, TO, 4><<<T_, kThreads, 0, s>>>(op, row_of, p, gain, eps, k, width, dp, ld_out);
-  else if (nvec <= 8 * kThreads)
-    combine_kernel<T, TO, 8><<<T_, kThreads, 0, s>>>(op, row_of, p, gain, eps, k, width, dp, ld_out);
+    launch_vpt<T, TO, 4>(op, row_of, p, gain, eps, T_, k, width, dp, ld_out, s);
   else
     return cudaErrorInvalidValue;
   return cudaGetLastError();
