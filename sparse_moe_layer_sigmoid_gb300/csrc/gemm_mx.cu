@@ -299,10 +299,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             ptx::tma_load_5d(ss, &tmWs, &sfr_full[sstage], xb, 0, 0, wrow_glu, ti.expert);
           else
             ptx::tma_load_3d(ss, &tmWs, &sfr_full[sstage], xb, wrow, ti.expert);
+          if (C::kTermsInN)  // decode: the three terms' scale bytes in one box {16 B, NT rows, 3 terms}
+            ptx::tma_load_3d(ss + kWsBytes, tmXs, &sfr_full[sstage], xb, ti.row0, 0);
+          else
 #pragma unroll
-          for (int q = 0; q < C::kTerms; ++q)
-            ptx::tma_load_2d(ss + kWsBytes + q * kXsTermBytes, tmXs, &sfr_full[sstage], q * (p.K / 32) + xb,
-                             ti.row0);
+            for (int q = 0; q < C::kTerms; ++q)
+              ptx::tma_load_2d(ss + kWsBytes + q * kXsTermBytes, tmXs, &sfr_full[sstage], q * (p.K / 32) + xb,
+                               ti.row0);
           if (++sstage == kSfStages) {
             sstage = 0;
             sphase ^= 1u;
@@ -336,9 +339,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               ptx::tma_load_5d_pair(sW, &tmW, bar, kb * 128, 0, 0, wrow_glu, ti.expert);
             else
               ptx::tma_load_3d_pair(sW, &tmW, bar, kb * 128, wrow, ti.expert);
+            if (C::kTermsInN)  // decode: the three terms' 8 rows in one box {128 B, 8 rows, 3 terms}, term-major
+              ptx::tma_load_3d_pair(sX, tmX, bar, kb * 128, xrow0, 0);
+            else
 #pragma unroll
-            for (int q = 0; q < kMxTerms; ++q)  // term q: 96 rows x 128 bytes at byte q * K/2 + kb * 128 of each record
-              ptx::tma_load_2d_pair(sX + q * kXTermBytes, tmX, bar, q * (p.K / 2) + kb * 128, xrow0);
+              for (int q = 0; q < kMxTerms; ++q)  // term q: 96 rows x 128 bytes at byte q * K/2 + kb * 128 of each record
+                ptx::tma_load_2d_pair(sX + q * kXTermBytes, tmX, bar, q * (p.K / 2) + kb * 128, xrow0);
           }
         }
         if (++stage == kStages) {
@@ -697,11 +703,29 @@ cudaError_t launch_tc_mx(const TcMx& g, const int4* tiles, const int32_t* num_ti
   CUtensorMap maps[8];  // weights, weight scales, token terms (3 box heights), token scales (3)
   bool ok = glu ? make_map_glu_interleaved(&maps[0], g.w, g.glu_h, kWRows / 32, true, f8)
                 : make_map_fp4(&maps[0], g.w, kWRows, 128, true, f8);
+  // decode (MXFP4 records): the three terms are a dimension of the maps, so that one load brings
+  // a k-block of all three (their 8-row atoms term-major, as separate loads would place them);
+  // the producer's issue rate, not HBM, had bounded the decode units at six loads per k-block
+  const bool terms_dim = decode && !f8;
   for (int b = 0; b < 3; ++b) {  // the decode layout uses its one box size in all three slots
+    const int rows_b = x_box_rows(unit_rows, b);
+    if (terms_dim) {
+      // token bytes {K/2, rows, 3 terms} (row stride: a record, term stride K/2): boxes {128, 8, 3}
+      const cuuint64_t dims3[3] = {(cuuint64_t)(g.K / 2), (cuuint64_t)g.rows, (cuuint64_t)kMxTerms};
+      const cuuint64_t strides3[2] = {(cuuint64_t)x_rec, (cuuint64_t)(g.K / 2)};
+      const cuuint32_t box3[3] = {128, (cuuint32_t)rows_b, (cuuint32_t)kMxTerms};
+      ok = ok && encode_u8(&maps[2 + b], g.x, 3, dims3, strides3, box3, true);
+      // scale bytes {K/32, rows, 3 terms}: boxes {16, 16, 3}
+      const cuuint64_t sdims3[3] = {(cuuint64_t)kscale, (cuuint64_t)g.rows, (cuuint64_t)kMxTerms};
+      const cuuint64_t sstrides3[2] = {(cuuint64_t)x_rec, (cuuint64_t)kscale};
+      const cuuint32_t sbox3[3] = {16, (cuuint32_t)(2 * rows_b), (cuuint32_t)kMxTerms};
+      ok = ok && encode_u8(&maps[5 + b], static_cast<const uint8_t*>(g.x) + mx3_scale_offset(g.K), 3, sdims3,
+                           sstrides3, sbox3, false);
+      continue;
+    }
     // the token bytes of the records as a 2-D byte array {3 K/2 (MXFP8: K), rows}: boxes of 128 bytes
     const cuuint64_t dims[2] = {(cuuint64_t)(f8 ? g.K : kMxTerms * g.K / 2), (cuuint64_t)g.rows};
     const cuuint64_t strides[1] = {(cuuint64_t)x_rec};
-    const int rows_b = x_box_rows(unit_rows, b);
     const cuuint32_t box[2] = {128, (cuuint32_t)rows_b};
     ok = ok && encode_u8(&maps[2 + b], g.x, 2, dims, strides, box, true);
     // the records' scale bytes {3 K/32, rows}: boxes of 16 bytes x (2 x the term box) rows
