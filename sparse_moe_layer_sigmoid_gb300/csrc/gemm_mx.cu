@@ -269,7 +269,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------------ TMA producer (both CTAs)
-    int stage = 0, iter = 0, sstage = 0;
+    int stage = 0, sstage = 0;
     uint32_t phase = 0, sphase = 0;
     bool first = true;
     int4 entry = pair < total ? mx_entry(p, pair) : make_int4(0, 0, 0, 0);
@@ -285,7 +285,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // bytes a stage's loads deliver: weights (F8: counted packed), token rows of each term or chunk
       const uint32_t stage_tx = kWBytes + (F8 ? 2u : (uint32_t)kMxTerms) * (uint32_t)x_box_rows(NT, bsel) * 128u;
       const uint32_t sf_tx = kWsBytes + (uint32_t)C::kTerms * (uint32_t)(2 * x_box_rows(NT, bsel)) * 16u;
-      for (int kb = 0; kb < p.num_kb; ++kb, ++iter) {
+      for (int kb = 0; kb < p.num_kb; ++kb) {
         if ((kb & 1) == 0) {
           // scale bytes of k-blocks kb, kb+1 (16 bytes of every row) into this CTA's scale ring
           if (!ptx::mbar_wait_bounded(&sfr_empty[sstage], sphase ^ 1u, abort_flag, p.status, p.timeout_ns,
@@ -311,10 +311,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             sphase ^= 1u;
           }
         }
+        // the stage's last reader has finished: the MMA's commit arrives in both CTAs of the pair
         if (!ptx::mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, p.status, p.timeout_ns, kWaitProducer))
           goto done;
-        // the MMA read both CTAs' copy of this stage: pass the release on to the partner
-        if (rank == 0 && iter >= kStages) ptx::mbar_arrive_remote(&empty[stage], 1);
         uint8_t* sW = smem + stage * kStageBytes;
         uint8_t* sX = sW + C::kWSmem;  // F8: the weight chunks take 2 x kWBytes
         const uint32_t bar = ptx::mapa_shared(&full[stage], 0);  // the even CTA's full[stage]
@@ -408,7 +407,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
         }
         }
-        ptx::mma_commit_pair(&empty[s]);
+        ptx::mma_commit_pair_both(&empty[s]);  // both CTAs' copies of the stage are free
         ptx::mma_commit_pair_both(&sf_empty[slot]);
         if (++s == kStages) {
           s = 0;
