@@ -50,7 +50,6 @@ using namespace tc;
 constexpr int kWRows = 128;                              // weight rows per CTA (M = 256 per pair)
 constexpr int KB = 256;                                  // K elements per stage (128 packed bytes)
 constexpr uint32_t kWBytes = kWRows * 128;               // 16 KB
-constexpr uint32_t kWsBytes = kWRows * 16;               // 2 KB: this CTA's weight rows' scale bytes of 2 k-blocks
 constexpr int kThreads = 320;                            // producer, MMA, 4 epilogue, 4 scale warps
 constexpr int kEpiStride = 72;                           // floats per staged token: blocks at 0 and 36
 
@@ -74,9 +73,14 @@ struct MxCfg {
   static constexpr uint32_t kWSmem = F8 ? 2 * kWBytes : kWBytes;     // weight bytes of a k-block in shared memory
   static constexpr uint32_t kStageBytes = kWSmem + (F8 ? 2 : kMxTerms) * kXTermBytes;
   static constexpr int kStages = NT >= 64 ? 3 : (F8 ? 5 : 8);
-  // scale ring: per stage the scale bytes of two k-blocks (16 bytes of each row): this CTA's weight
-  // rows, and all NT token rows of each term (both CTAs' MMA halves read every token row)
-  static constexpr uint32_t kXsTermBytes = NT * 16;
+  // scale ring: per stage the scale bytes of kSfKb k-blocks of this CTA's weight rows, and of all
+  // NT token rows of each term (both CTAs' MMA halves read every token row)
+  // scale ring: kSfKb k-blocks per stage (8 scale bytes of every row each): four for decode's
+  // MXFP4 units, whose producer issue rate bounds them, two where shared memory is scarce
+  static constexpr int kSfKb = (NT < 32 && !F8) ? 4 : 2;
+  static constexpr uint32_t kSfRowBytes = 8 * kSfKb;                  // bytes of a row per stage
+  static constexpr uint32_t kWsBytes = kWRows * kSfRowBytes;          // this CTA's weight rows
+  static constexpr uint32_t kXsTermBytes = NT * kSfRowBytes;
   static constexpr uint32_t kSfStageBytes = kWsBytes + kTerms * kXsTermBytes;
   static constexpr int kSfStages = NT >= 64 ? 3 : 4;
   // token boxes sized to the tile: 8, 32 or 96 rows of each term per CTA (tiles of N <= 16, <= 64,
@@ -203,6 +207,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   constexpr int kStages = C::kStages, kSfStages = C::kSfStages, kSfSlots = C::kSfSlots;
   constexpr uint32_t kStageBytes = C::kStageBytes, kXTermBytes = C::kXTermBytes, kSfStageBytes = C::kSfStageBytes;
   constexpr uint32_t kXsTermBytes = C::kXsTermBytes, kEpiBytes = C::kEpiBytes, kSfBase = C::kSfBase;
+  constexpr uint32_t kWsBytes = C::kWsBytes, kSfRowBytes = C::kSfRowBytes;
+  constexpr int kSfKb = C::kSfKb;
   constexpr uint32_t kSfCols = C::kSfCols, kAccCols = C::kAccCols, kChunkCols = C::kChunkCols;
   constexpr uint32_t kTmemCols = C::kTmemCols;
   constexpr int kEpiTokens = C::kEpiTokens;
@@ -284,10 +290,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const CUtensorMap* tmXs = bsel == 0 ? &tmXs0 : bsel == 1 ? &tmXs1 : &tmXs2;
       // bytes a stage's loads deliver: weights (F8: counted packed), token rows of each term or chunk
       const uint32_t stage_tx = kWBytes + (F8 ? 2u : (uint32_t)kMxTerms) * (uint32_t)x_box_rows(NT, bsel) * 128u;
-      const uint32_t sf_tx = kWsBytes + (uint32_t)C::kTerms * (uint32_t)(2 * x_box_rows(NT, bsel)) * 16u;
+      const uint32_t sf_tx = kWsBytes + (uint32_t)C::kTerms * (uint32_t)(2 * x_box_rows(NT, bsel)) * kSfRowBytes;
       for (int kb = 0; kb < p.num_kb; ++kb) {
-        if ((kb & 1) == 0) {
-          // scale bytes of k-blocks kb, kb+1 (16 bytes of every row) into this CTA's scale ring
+        if (kb % kSfKb == 0) {
+          // scale bytes of k-blocks kb .. kb+kSfKb-1 (8 bytes each of every row) into this CTA's
+          // scale ring (past the last k-block: the boxes' fill)
           if (!ptx::mbar_wait_bounded(&sfr_empty[sstage], sphase ^ 1u, abort_flag, p.status, p.timeout_ns,
                                       kWaitProducer))
             goto done;
@@ -427,7 +434,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int slot = g % kSfSlots;
         int ok = 1;
         if (lane == 0) {
-          if ((kb & 1) == 0)
+          if (kb % kSfKb == 0)
             ok = ptx::mbar_wait_bounded(&sfr_full[ss], sph, abort_flag, p.status, p.timeout_ns, kWaitFull);
           ok = ok && ptx::mbar_wait_bounded(&sf_empty[slot], ((uint32_t)(g / kSfSlots) & 1u) ^ 1u, abort_flag,
                                             p.status, p.timeout_ns, kWaitAccFree);
@@ -435,8 +442,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) goto sf_done;
         {
-          const uint8_t* st = sf_ring + ss * kSfStageBytes + 8 * (kb & 1);  // this k-block's 8 bytes of a row
-          const uint2 wv = *reinterpret_cast<const uint2*>(st + (32 * q + lane) * 16);
+          const uint8_t* st = sf_ring + ss * kSfStageBytes + 8 * (kb % kSfKb);  // this k-block's 8 bytes of a row
+          const uint2 wv = *reinterpret_cast<const uint2*>(st + (32 * q + lane) * kSfRowBytes);
           ptx::tc_fence_after();
           const uint32_t col = lane_base + (uint32_t)slot * kSfCols;
           ptx::tmem_st_32x32b_x1(col + (uint32_t)q, wv.x);       // weight scale blocks 0..3 of the k-block
@@ -449,7 +456,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               for (int c = 0; c < 8; ++c) {
                 uint2 v = make_uint2(0u, 0u);
                 if (c < NT / 32)
-                  v = *reinterpret_cast<const uint2*>(st + kWsBytes + tt * kXsTermBytes + (32 * c + lane) * 16);
+                  v = *reinterpret_cast<const uint2*>(st + kWsBytes + tt * kXsTermBytes + (32 * c + lane) * kSfRowBytes);
                 lo[tt][c] = v.x;
                 hi[tt][c] = v.y;
               }
@@ -460,7 +467,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
           } else if (F8) {  // one term: token rows 0 .. NT-1 in lanes 0 .. NT-1, chunk h at 8 + 8 h
             uint2 v = make_uint2(0u, 0u);
-            if (lane < NT) v = *reinterpret_cast<const uint2*>(st + kWsBytes + lane * 16);
+            if (lane < NT) v = *reinterpret_cast<const uint2*>(st + kWsBytes + lane * kSfRowBytes);
             ptx::tmem_st_32x32b_x1(col + 8u, v.x);
             ptx::tmem_st_32x32b_x1(col + 8u + kChunkCols, v.y);
           } else {  // MMA rows n = 24 c + 8 q + j' (term q, token 8 c + j'): row n at lane n % 32,
@@ -471,7 +478,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               uint2 v = make_uint2(0u, 0u);
               if (n < C::kMmaN) {
                 const int c = n / 24, tt = (n % 24) >> 3, j = 8 * c + (n & 7);
-                v = *reinterpret_cast<const uint2*>(st + kWsBytes + tt * kXsTermBytes + j * 16);
+                v = *reinterpret_cast<const uint2*>(st + kWsBytes + tt * kXsTermBytes + j * kSfRowBytes);
               }
               ptx::tmem_st_32x32b_x1(col + 8u + (uint32_t)half, v.x);
               ptx::tmem_st_32x32b_x1(col + 8u + 2u * kChunkCols + (uint32_t)half, v.y);
@@ -485,10 +492,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               ptx::mbar_arrive(&sf_full[slot]);
             else
               ptx::mbar_arrive_remote(&sf_full[slot], 0);
-            if (kb & 1) ptx::mbar_arrive(&sfr_empty[ss]);  // both k-blocks of the stage copied
+            if (kb % kSfKb == kSfKb - 1 || kb == p.num_kb - 1)
+              ptx::mbar_arrive(&sfr_empty[ss]);  // every k-block of the stage copied
           }
         }
-        if (kb & 1) {
+        if (kb % kSfKb == kSfKb - 1 || kb == p.num_kb - 1) {
           if (++ss == kSfStages) {
             ss = 0;
             sph ^= 1u;
@@ -706,6 +714,7 @@ cudaError_t launch_tc_mx(const TcMx& g, const int4* tiles, const int32_t* num_ti
   // a k-block of all three (their 8-row atoms term-major, as separate loads would place them);
   // the producer's issue rate, not HBM, had bounded the decode units at six loads per k-block
   const bool terms_dim = decode && !f8;
+  const cuuint32_t sf_row = terms_dim ? MxCfg<16, false>::kSfRowBytes : 16;  // scale bytes of a row per stage
   for (int b = 0; b < 3; ++b) {  // the decode layout uses its one box size in all three slots
     const int rows_b = x_box_rows(unit_rows, b);
     if (terms_dim) {
@@ -717,7 +726,7 @@ cudaError_t launch_tc_mx(const TcMx& g, const int4* tiles, const int32_t* num_ti
       // scale bytes {K/32, rows, 3 terms}: boxes {16, 16, 3}
       const cuuint64_t sdims3[3] = {(cuuint64_t)kscale, (cuuint64_t)g.rows, (cuuint64_t)kMxTerms};
       const cuuint64_t sstrides3[2] = {(cuuint64_t)x_rec, (cuuint64_t)kscale};
-      const cuuint32_t sbox3[3] = {16, (cuuint32_t)(2 * rows_b), (cuuint32_t)kMxTerms};
+      const cuuint32_t sbox3[3] = {sf_row, (cuuint32_t)(2 * rows_b), (cuuint32_t)kMxTerms};
       ok = ok && encode_u8(&maps[5 + b], static_cast<const uint8_t*>(g.x) + mx3_scale_offset(g.K), 3, sdims3,
                            sstrides3, sbox3, false);
       continue;
@@ -739,12 +748,12 @@ cudaError_t launch_tc_mx(const TcMx& g, const int4* tiles, const int32_t* num_ti
     const cuuint64_t dims[5] = {(cuuint64_t)kscale, 16, 2, (cuuint64_t)(h / 16), (cuuint64_t)E};
     const cuuint64_t strides[4] = {(cuuint64_t)kscale, (cuuint64_t)(h * kscale), (cuuint64_t)(16 * kscale),
                                    (cuuint64_t)(2 * h * kscale)};
-    const cuuint32_t box[5] = {16, 16, 2, (cuuint32_t)(kWRows / 32), 1};
+    const cuuint32_t box[5] = {sf_row, 16, 2, (cuuint32_t)(kWRows / 32), 1};
     ok = ok && encode_u8(&maps[1], g.w_scale, 5, dims, strides, box, false);
   } else {    // weight scales [E][rows][K/32]
     const cuuint64_t dims[3] = {(cuuint64_t)kscale, (cuuint64_t)g.w.rows, (cuuint64_t)E};
     const cuuint64_t strides[2] = {(cuuint64_t)kscale, (cuuint64_t)(g.w.rows * kscale)};
-    const cuuint32_t box[3] = {16, (cuuint32_t)kWRows, 1};
+    const cuuint32_t box[3] = {sf_row, (cuuint32_t)kWRows, 1};
     ok = ok && encode_u8(&maps[1], g.w_scale, 3, dims, strides, box, false);
   }
   if (!ok) return cudaErrorInvalidValue;
