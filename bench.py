@@ -66,16 +66,16 @@ TRAFFIC = {
 # capture of a smaller case of the same kernel; a full launch's traffic is those ratios times its
 # own algorithmic bytes (reads and writes each grow with experts touched and rows processed).
 TRAFFIC_RATIOS = {
-    # prefill tiles: k3_mxfp4_prefill_e32_t1024 (32 experts, 16384 rows): read 468073472 B of
-    # 467927040 B, write 69919744 B of 80216064 B
-    ("mxfp4_prefill", "routed_gate_up_glu"): {"read": 468073472 / 467927040, "write": 69919744 / 80216064,
+    # prefill tiles: k3_mxfp4_prefill_e32_t1024 (32 experts, 16384 rows): read 468150528 B of
+    # 467927040 B, write 69632768 B of 80216064 B
+    ("mxfp4_prefill", "routed_gate_up_glu"): {"read": 468150528 / 467927040, "write": 69632768 / 80216064,
                                               "src": "sparse_moe_layer_sigmoid_gb300/csrc/gemm_mx.cu",
-                                              "sha256": "f3c4bdb495017e079fd1b18758a7d435914cd25bac637d3ff3204637e2a8d833"},
-    # decode units: k3_mxfp4_decode_e128_t8 (85 experts, 128 rows): read 995188480 B of 995076096 B,
-    # write 3741184 B of 626688 B (dirty lines of the untimed L2 flush written back meanwhile)
-    ("mxfp4_decode", "routed_gate_up_glu"): {"read": 995188480 / 995076096, "write": 3741184 / 626688,
+                                              "sha256": "deb4f5de054232618e992038625d1a4be0f2f67fe858af5c8be67f51e92ae7c5"},
+    # decode units: k3_mxfp4_decode_e128_t8 (85 experts, 128 rows): read 995229184 B of 995076096 B,
+    # write 3851008 B of 626688 B (dirty lines of the untimed L2 flush written back meanwhile)
+    ("mxfp4_decode", "routed_gate_up_glu"): {"read": 995229184 / 995076096, "write": 3851008 / 626688,
                                              "src": "sparse_moe_layer_sigmoid_gb300/csrc/gemm_mx.cu",
-                                             "sha256": "f3c4bdb495017e079fd1b18758a7d435914cd25bac637d3ff3204637e2a8d833"},
+                                             "sha256": "deb4f5de054232618e992038625d1a4be0f2f67fe858af5c8be67f51e92ae7c5"},
 }
 
 
