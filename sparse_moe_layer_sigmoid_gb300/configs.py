@@ -62,12 +62,16 @@ K3_MXFP4_PREFILL_PROFILE = replace(K3_MXFP4_PREFILL_SKEW, name="k3_mxfp4_prefill
 # The routing stress workload at 8192 tokens (about 0.5 GB on the device) for captures of the
 # routing kernels.
 ROUTING_DISPATCH_PROFILE = replace(ROUTING_DISPATCH_STRESS, name="routing_dispatch_t8192", tokens=8192)
+# The decode layer's routing (T=32, E=896, the same seed and router) with identity experts: the
+# short-batch routing kernels on about 0.1 GB of weights, for captures of those kernels.
+ROUTING_DECODE_PROFILE = replace(K3_MXFP4_DECODE, name="routing_decode_t32", hidden=0, n_shared=0,
+                                 routed_w="bf16", identity_experts=True)
 
 CONFIGS = {c.name: c for c in (TINY_F32, K3W_E128_BF16_PREFILL, K3_MXFP4_DECODE,
                                K3_MXFP4_PREFILL_SKEW, K3_MXFP4_PREFILL_MILD,
                                ROUTING_DISPATCH_STRESS, K3W_E32_BF16_PROFILE,
                                K3_MXFP4_DECODE_PROFILE, K3_MXFP4_PREFILL_PROFILE,
-                               ROUTING_DISPATCH_PROFILE)}
+                               ROUTING_DISPATCH_PROFILE, ROUTING_DECODE_PROFILE)}
 
 
 def scaled(cfg: LayerConfig, **kw) -> LayerConfig:
