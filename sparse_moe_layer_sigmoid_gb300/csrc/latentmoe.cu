@@ -246,7 +246,7 @@ lmoe_status run_routing(lmoe_handle* h, const void* x, int T, const lmoe_weights
     LMOE_TRY(launch_topk(h->logits, w->router_bias, rs, T, c.num_experts, c.top_k, h->idx, h->p, h->refine_list,
                          h->refine_count, h->status, h->num_sms, s, &part));
     stage_end(h, kStTopk, s);
-    h->last_launches += 2;
+    h->last_launches += T <= kTopkFusedMaxT ? 1 : 2;  // one kernel for short batches, else select + refine
     idx = h->idx;
     p = h->p;
   }
